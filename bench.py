@@ -1,0 +1,399 @@
+#!/usr/bin/env python3
+"""Paged decode step benchmark on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME]
+                    [--partition P] [--impl ours|reference]
+
+A step is one pass of the whole hot path over one batch: slot mapping of
+the step's new tokens, reshape_and_cache of their K/V, copy-on-write block
+copies (when the workload has them) and paged decode attention (split-context
+partitions merged in the same launch).  Default workload: the GQA 70B-like
+decode layer (128 sequences, lognormal contexts, 64 query heads over 8 KV
+heads, d 128, block 16, bf16).
+
+Prints ONE JSON line.  `value` is the effective KV bandwidth of the whole
+step (attended K and V bytes / step time, summed over ranks); the roofline
+object reports the attention kernel alone against the measured HBM copy
+bandwidth.  `--impl reference` times the CPU oracle (plain C, fp64) on a
+bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = ("paged decode attention effective KV GB/s and % of GB300 HBM peak; "
+          "seqs/s per step")
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+DECODE_SRC = os.path.join(ROOT, "paged_kv_cache_96_gb300", "csrc", "pa_decode.cu")
+TRAFFIC_SUMMARY = os.path.join(ROOT, "profiles", "decode_gqa70b_ncu.md")
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__,
+                                 formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--config", default="gqa70b",
+                    choices=["tiny", "mha7b", "gqa70b", "longctx", "prefix"])
+    ap.add_argument("--partition", type=int, default=None,
+                    help="split-context partition tokens (0 = single pass)")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="target CPU time of the oracle baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args(argv)
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (one process per GPU, replicas: no data-path collective)
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def aggregate(elapsed_s: float, units: float, world: int, device=None):
+    """Max elapsed and summed units over ranks (identity when world == 1)."""
+    if world == 1:
+        return elapsed_s, units
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([elapsed_s], dtype=torch.float64, device=device)
+    u = torch.tensor([units], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.samples = []
+        self.proc = None
+        self.thread = None
+        self.error = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100", "-i", gpu_id],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError) as e:
+            self.error = str(e)
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float):
+        if self.error or not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [],
+                    "note": self.error or "no nvidia-smi samples"}
+        window = [p for (t, p) in self.samples if t0 <= t <= t1 + 0.15]
+        note = "sampled during the timed region (100 ms period)"
+        if not window:
+            window = [p for (_, p) in self.samples]
+            note = "timed region shorter than the sampling period: samples span warm-up + timing"
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(p[1]) for p in window if num(p[1]) is not None]
+        mx = [num(p[2]) for p in window if num(p[2]) is not None]
+        pw = [num(p[3]) for p in window if num(p[3]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for p in window for i in range(4)
+                          if p[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "power_w_max": max(pw) if pw else None,
+                "reasons": reasons, "samples": len(window), "note": note}
+
+
+# ---------------------------------------------------------------------------
+
+def measured_hbm_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def recorded_traffic():
+    """DRAM bytes per launch of the decode kernel from the committed ncu
+    summary -- only if the kernel source is unchanged since the capture."""
+    try:
+        text = open(TRAFFIC_SUMMARY).read()
+    except OSError:
+        return None
+    m_sha = re.search(r"kernel_source_sha256:\s*([0-9a-f]{64})", text)
+    m_b = re.search(r"dram_bytes_per_launch_full_workload:\s*([0-9.eE+]+)", text)
+    if not (m_sha and m_b):
+        return None
+    sha = hashlib.sha256(open(DECODE_SRC, "rb").read()).hexdigest()
+    return float(m_b.group(1)) if sha == m_sha.group(1) else None
+
+
+def cpu_baseline_sample(w, target_s: float):
+    """Time the oracle's step (new-token writes + attention) on the first
+    sequences of the workload until about target_s seconds of CPU work."""
+    import oracle
+    kc, vc = w.empty_pools()
+    dt = oracle.F16 if w.dtype == "f16" else oracle.BF16
+    slots = oracle.slot_mapping(w.block_tables, w.hist_seq, w.hist_pos, w.bs)
+    oracle.reshape_and_cache(w.hist_key, w.hist_value, kc, vc, slots)
+    done, tokens, elapsed = [], 0, 0.0
+    order = list(range(w.S))
+    for s in order:
+        t0 = time.perf_counter()
+        sl = oracle.slot_mapping(w.block_tables, w.new_seq[s:s + 1], w.new_pos[s:s + 1],
+                                 w.bs)
+        oracle.reshape_and_cache(w.new_key[s:s + 1], w.new_value[s:s + 1], kc, vc, sl)
+        oracle.paged_attention(w.query, kc, vc, w.step_block_tables, w.context_lens,
+                               w.scale, dt, seqs=[s])
+        elapsed += time.perf_counter() - t0
+        done.append(s)
+        tokens += int(w.context_lens[s])
+        if elapsed >= target_s:
+            break
+    kv = tokens * w.Hkv * w.D * 2 * 2
+    return {"value": kv / elapsed / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{len(done)} of {w.S} sequences ({tokens} attended tokens): "
+                      f"new-token write + fp64 attention, single-threaded C, "
+                      f"{elapsed:.1f} s"}
+
+
+# ---------------------------------------------------------------------------
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    from paged_kv_cache_96_gb300 import workloads as W
+    import oracle
+    w = W.build(W.CONFIGS[args.config])
+    kc, vc = w.empty_pools()
+    dt = oracle.F16 if w.dtype == "f16" else oracle.BF16
+    slots = oracle.slot_mapping(w.block_tables, w.hist_seq, w.hist_pos, w.bs)
+    oracle.reshape_and_cache(w.hist_key, w.hist_value, kc, vc, slots)
+    # per step: a bounded sample of sequences sized for ~2 s of CPU work
+    per_seq = []
+    t0 = time.perf_counter()
+    oracle.paged_attention(w.query, kc, vc, w.step_block_tables, w.context_lens, w.scale,
+                           dt, seqs=[0])
+    per_tok = (time.perf_counter() - t0) / max(1, int(w.context_lens[0]))
+    budget = 2.0
+    sample, toks = [], 0
+    for s in range(w.S):
+        if sample and (toks + int(w.context_lens[s])) * per_tok > budget:
+            break
+        sample.append(s)
+        toks += int(w.context_lens[s])
+    sub_seq = np.asarray(sample, dtype=np.int32)
+
+    def step():
+        sl = oracle.slot_mapping(w.block_tables, w.new_seq[sub_seq], w.new_pos[sub_seq], w.bs)
+        oracle.reshape_and_cache(w.new_key[sub_seq], w.new_value[sub_seq], kc, vc, sl)
+        if w.cow_pairs.shape[0]:
+            oracle.copy_blocks(kc, vc, w.cow_pairs)
+        oracle.paged_attention(w.query, kc, vc, w.step_block_tables, w.context_lens,
+                               w.scale, dt, seqs=sample)
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    el = time.perf_counter() - t0
+    kv = toks * w.Hkv * w.D * 2 * 2
+    val = kv * args.steps / el / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": val, "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": el / args.steps * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{w.spec.name}: {w.spec.description}",
+                   "sample": f"{len(sample)} of {w.S} sequences per step"},
+        "cpu_baseline": {"value": val, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{len(sample)} of {w.S} sequences ({toks} tokens) "
+                                   "per step, fp64 single-threaded C"},
+        "e2e": {"value": val, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args):
+    import torch
+    rank, world, local_rank = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local_rank if world > 1 else 0)
+    torch.cuda.set_device(dev)
+
+    from paged_kv_cache_96_gb300 import step as S
+    from paged_kv_cache_96_gb300 import workloads as W
+    w = W.build(W.CONFIGS[args.config])
+    st = S.DecodeStep(w, device=str(dev), partition_size=args.partition)
+    stream = torch.cuda.current_stream(dev)
+    torch.cuda.synchronize(dev)
+
+    sampler = None
+    if rank == 0:
+        gpu_id = str(getattr(torch.cuda.get_device_properties(dev), "uuid", local_rank))
+        if not gpu_id.startswith("GPU-") and re.fullmatch(r"[0-9a-f-]{36}", gpu_id):
+            gpu_id = "GPU-" + gpu_id
+        sampler = ClockSampler(gpu_id)
+
+    for _ in range(max(args.warmup, 3)):
+        st.run()
+    torch.cuda.synchronize(dev)
+    if st.error_word.item() != 0:
+        raise RuntimeError(f"device error word {int(st.error_word.item()):#x}")
+
+    K = args.steps
+    ev_a = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ev_b = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    t_host0 = time.time()
+    start.record(stream)
+    for i in range(K):
+        st.slot_mapping()
+        st.reshape_and_cache()
+        st.copy_blocks()
+        ev_a[i].record(stream)
+        st.attention()
+        ev_b[i].record(stream)
+    end.record(stream)
+    torch.cuda.synchronize(dev)
+    t_host1 = time.time()
+    if world > 1:
+        torch.distributed.barrier()
+    step_s = start.elapsed_time(end) / 1e3
+    attn_s = sum(a.elapsed_time(b) for a, b in zip(ev_a, ev_b)) / 1e3 / K
+    if sampler is not None:
+        sampler.stop()
+    clocks = sampler.summary(t_host0, t_host1) if sampler else None
+
+    kv = w.kv_bytes()
+    units = kv * K
+    max_elapsed, total_units = aggregate(step_s, units, world, device=dev)
+    value = total_units / max_elapsed / 1e9
+
+    # end to end through the public API: pinned host inputs -> step -> host output
+    e2e = None
+    if rank == 0 and args.e2e_steps > 0:
+        host = S.HostStepIO(st)
+        for _ in range(3):
+            host.step()
+        torch.cuda.synchronize(dev)
+        Ke = args.e2e_steps
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(Ke):
+            host.step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_s = e0.elapsed_time(e1) / 1e3 / Ke
+        e2e = {"value": kv / e2e_s / 1e9 * world, "unit": "GB/s",
+               "h2d_bytes_per_step": host.h2d_bytes, "d2h_bytes_per_step": host.d2h_bytes,
+               "us_per_step": e2e_s * 1e6}
+
+    if rank != 0:
+        return
+    peak, peak_kind = measured_hbm_peak()
+    attn_bytes = kv + w.qo_bytes()
+    achieved = attn_bytes / attn_s / 1e9
+    cpu = None
+    if not args.no_cpu_baseline:
+        cpu = cpu_baseline_sample(w, args.cpu_seconds)
+    per_step = step_s / K
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": per_step * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+        "config": {
+            "workload": f"{w.spec.name}: {w.spec.description}",
+            "num_seqs": w.S, "num_heads": w.H, "num_kv_heads": w.Hkv, "head_dim": w.D,
+            "block_size": w.bs, "num_blocks": w.num_blocks,
+            "partition_size": st.partition_size,
+            "context_tokens": int(w.context_lens.sum()),
+            "kv_bytes_per_step": kv,
+            "l2": f"inputs larger than L2: {kv / 1e9:.2f} GB of K/V read per step; no flush",
+            "parallelism": "replicas" if world > 1 else "single GPU",
+        },
+        "pct_of_hbm_peak_8tbps": 100.0 * value / world / NOMINAL_HBM_GBS,
+        "pct_of_hbm_measured": 100.0 * value / world / peak,
+        "seqs_per_s": w.S * world / per_step,
+        "us_per_step": per_step * 1e6,
+        "attention_us": attn_s * 1e6,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": recorded_traffic(),
+                     "kernel": "paged_decode_kernel", "peak_kind": f"{peak_kind} copy",
+                     "algorithmic_bytes_per_launch": attn_bytes},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": st.launches_per_step() * K,
+        "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+    rank, world, _ = dist_env()
+    if world > 1 and args.impl == "ours":
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

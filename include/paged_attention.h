@@ -1,0 +1,188 @@
+/*
+ * paged_attention.h -- C ABI of the GB300 (sm_103a) paged KV-cache decode
+ * library (libpaged_attention.so).
+ *
+ * The operations are those of a vLLM-style serving engine's decode step as
+ * the following web pages describe them (cited by title and section):
+ *   [GAO]  "PagedAttention & Continuous Batching" (gaoleia.github.io,
+ *          2026-01-25): §1.3 physical block, §1.4 block table, §1.5 slot
+ *          mapping, §1.6 paged attention, §2.4 decode is memory-bound.
+ *   [FEI]  "vLLM 架构详解: PagedAttention、Continuous Batching 与生产级推理优化"
+ *          (feifeigd.github.io): "Block Table 实现", "共享前缀的 Block 复用".
+ *   [LAKE] "vLLM源码解析(二): 调度系统与PagedAttention实现"
+ *          (lakecityint.com): §3.2 copy-on-write.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Tensors are caller-owned DEVICE memory, dense, row-major (last index
+ *    fastest), unless a parameter says "host".  The library allocates
+ *    nothing and keeps no pointer after a call returns.
+ *  - 16-bit elements (pa_dtype) are fp16 or bf16.  Tensor base addresses
+ *    must be 16-byte aligned.
+ *  - KV pool layout (token-major, separate K and V pools):
+ *        key_cache, value_cache : [num_blocks][block_size][num_kv_heads][head_dim]
+ *    Block b, row r holds the K (or V) vectors of all KV heads for the token
+ *    stored in slot b * block_size + r ([GAO] §1.3, §1.5).
+ *  - Block tables: int32 [num_seqs][max_blocks_per_seq]; entry i of row s is
+ *    the physical block holding tokens i*block_size .. i*block_size +
+ *    block_size - 1 of sequence s ([GAO] §1.4).  Entries past a sequence's
+ *    last block are never read.
+ *  - Calls are asynchronous and ordered on `stream` (a cudaStream_t; NULL is
+ *    the legacy default stream).  They never synchronise the device.
+ *  - Host-visible argument errors return a status before anything is
+ *    launched.  Device-resident indices (slots, table entries, block pairs,
+ *    context lengths) are checked on the device: an out-of-range index is
+ *    skipped (never dereferenced) and, when `error_word` is non-NULL, a
+ *    PA_DEVERR_* bit is OR-ed into that device int32.  No kernel traps.
+ *  - A launch failure returns PA_ERR_CUDA; pa_last_cuda_error() names it.
+ */
+#ifndef PAGED_ATTENTION_H
+#define PAGED_ATTENTION_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define PA_API __attribute__((visibility("default")))
+#else
+#define PA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    PA_OK = 0,
+    PA_ERR_INVALID_ARG = 1,  /* null pointer, negative size, misalignment, ... */
+    PA_ERR_UNSUPPORTED = 2,  /* valid but not implemented (head_dim, block_size, group) */
+    PA_ERR_WORKSPACE = 3,    /* workspace missing or smaller than required */
+    PA_ERR_CUDA = 4          /* a CUDA runtime/driver call failed */
+} pa_status;
+
+typedef enum { PA_F16 = 0, PA_BF16 = 1 } pa_dtype;
+
+/* Bits OR-ed into the optional device error word. */
+#define PA_DEVERR_SLOT_RANGE    0x01 /* slot >= num_blocks * block_size */
+#define PA_DEVERR_BLOCK_RANGE   0x02 /* block-table entry outside [0, num_blocks) */
+#define PA_DEVERR_PAIR_RANGE    0x04 /* copy pair block outside [0, num_blocks) */
+#define PA_DEVERR_CONTEXT_RANGE 0x08 /* context_len < 0, > max_context_len or past the table */
+#define PA_DEVERR_TOKEN_RANGE   0x10 /* token's sequence or position outside its table */
+#define PA_DEVERR_TIMEOUT       0x20 /* a bounded wait on staged data gave up */
+
+/*
+ * pa_slot_mapping -- [GAO] §1.5.  For every token t, writes
+ *     slot_mapping[t] = block_tables[s][p / block_size] * block_size
+ *                       + p % block_size,   s = token_seq[t], p = token_pos[t].
+ * token_seq, token_pos: int32 [num_tokens].  slot_mapping: int32 [num_tokens]
+ * (output).  A token whose sequence is outside [0, num_seqs), whose position
+ * is negative or past max_blocks_per_seq * block_size, or whose table entry
+ * is outside [0, num_blocks) gets slot -1 and sets PA_DEVERR_TOKEN_RANGE or
+ * PA_DEVERR_BLOCK_RANGE.  num_tokens == 0 is a no-op.
+ */
+PA_API pa_status pa_slot_mapping(int32_t *slot_mapping, const int32_t *block_tables,
+                          int max_blocks_per_seq, const int32_t *token_seq,
+                          const int32_t *token_pos, int num_tokens,
+                          int num_seqs, int block_size, int num_blocks,
+                          int32_t *error_word, void *stream);
+
+/*
+ * pa_reshape_and_cache -- [GAO] §1.5, [FEI] "Block Table 实现".  Copies the
+ * K and V vectors of num_tokens new tokens into the pools at their slots:
+ *     key_cache[slot / block_size][slot % block_size][h][:] = key[t][h][:]
+ * (same for value).  key, value: [num_tokens][num_kv_heads][head_dim].
+ * slot_mapping: int32 [num_tokens]; slot < 0 means "skip this token";
+ * slot >= num_blocks * block_size is skipped and sets PA_DEVERR_SLOT_RANGE.
+ * Bytes are copied verbatim.  Two tokens with the same slot race.
+ */
+PA_API pa_status pa_reshape_and_cache(const void *key, const void *value,
+                               void *key_cache, void *value_cache,
+                               const int32_t *slot_mapping, int num_tokens,
+                               int num_blocks, int block_size, int num_kv_heads,
+                               int head_dim, pa_dtype dtype,
+                               int32_t *error_word, void *stream);
+
+/*
+ * pa_copy_blocks -- the "copy the contents" step of copy-on-write
+ * ([LAKE] §3.2).  block_mapping: int32 [num_pairs][2] = (src, dst); for every
+ * pair, K block dst := K block src and V block dst := V block src (whole
+ * blocks of block_size * num_kv_heads * head_dim elements).  No block may be
+ * both a source and a destination, and destinations must be distinct;
+ * otherwise the result is unspecified.  A pair with a block outside
+ * [0, num_blocks) is skipped and sets PA_DEVERR_PAIR_RANGE.
+ */
+PA_API pa_status pa_copy_blocks(void *key_cache, void *value_cache,
+                         const int32_t *block_mapping, int num_pairs,
+                         int num_blocks, int block_size, int num_kv_heads,
+                         int head_dim, pa_dtype dtype, int32_t *error_word,
+                         void *stream);
+
+/*
+ * pa_decode_workspace_bytes -- bytes of device workspace pa_decode_attention
+ * needs for these sizes (0 when partition_size == 0 or every context fits in
+ * one partition).  Layout, with P = ceil(max_context_len / partition_size)
+ * and every region starting on a 256-byte boundary, in this order:
+ *     float    part_m  [num_seqs][num_heads][P]   partition stabiliser m_j
+ *     float    part_l  [num_seqs][num_heads][P]   sum_p exp(score_p - m_j)
+ *     float    part_o  [num_seqs][num_heads][P][head_dim]  partition output / l_j
+ *     uint32_t arrivals[num_seqs][num_kv_heads]   zero between calls
+ * score_p = scale * q . k_p (natural-log units).  m_j is a stabiliser: the
+ * partition's log-sum-exp is m_j + log(l_j).  Partials are written only for
+ * sequences that span more than one partition.  Returns 0 for invalid sizes.
+ */
+PA_API size_t pa_decode_workspace_bytes(int num_seqs, int num_heads, int num_kv_heads,
+                                 int head_dim, int max_context_len,
+                                 int partition_size);
+
+/*
+ * pa_decode_attention -- paged decode attention, [GAO] §1.6 and §2.4.
+ * For every sequence s and query head h (KV head kh = h / (num_heads /
+ * num_kv_heads), contiguous groups):
+ *     score_p = scale * q[s][h] . K[p][kh],    p in [0, context_lens[s])
+ *     out[s][h][:] = sum_p softmax(score)_p * V[p][kh][:]
+ * where K[p], V[p] are read from physical block block_tables[s][p /
+ * block_size], row p % block_size.  Accumulation is fp32 (online softmax
+ * with a running max and sum); the output is rounded to nearest even.
+ *   out, query   : [num_seqs][num_heads][head_dim], dtype.
+ *   context_lens : int32 [num_seqs] (device); max_context_len (host) must be
+ *                  >= every context_lens[s] (larger values are clipped and
+ *                  flagged PA_DEVERR_CONTEXT_RANGE).  context 0 gives a zero row.
+ *   partition_size: 0 = single pass (one work unit per sequence and KV
+ *                  head); otherwise a multiple of 16 tokens >= 32: contexts
+ *                  are split into partitions of that many tokens, each
+ *                  producing a partial (m, l, o) in the workspace, and the
+ *                  partials of a (sequence, KV head) are merged by
+ *                  log-sum-exp weights l_j * exp(m_j - max m) inside the same
+ *                  launch by the last partition to finish.
+ *   workspace    : device, >= pa_decode_workspace_bytes(...) bytes, its
+ *                  `arrivals` region zero before the first call (the call
+ *                  leaves it zero).  May be NULL when that size is 0.
+ *                  Calls sharing one workspace must not overlap in time.
+ * Supported: head_dim 64 or 128; block_size a multiple of 16 up to 256;
+ * num_heads / num_kv_heads in 1..16; num_blocks * block_size < 2^31.
+ */
+PA_API pa_status pa_decode_attention(void *out, const void *query,
+                              const void *key_cache, const void *value_cache,
+                              const int32_t *block_tables,
+                              int max_blocks_per_seq,
+                              const int32_t *context_lens, int max_context_len,
+                              int num_seqs, int num_heads, int num_kv_heads,
+                              int head_dim, int block_size, int num_blocks,
+                              float scale, int partition_size, void *workspace,
+                              size_t workspace_bytes, pa_dtype dtype,
+                              int32_t *error_word, void *stream);
+
+/* Human-readable name of a status code (static storage). */
+PA_API const char *pa_status_string(pa_status status);
+
+/* Name of the last CUDA error a call of this thread saw (static storage). */
+PA_API const char *pa_last_cuda_error(void);
+
+/* ABI version: major * 10000 + minor * 100 + patch. */
+PA_API int pa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGED_ATTENTION_H */

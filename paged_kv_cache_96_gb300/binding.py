@@ -1,0 +1,203 @@
+"""ctypes binding of ``libpaged_attention.so`` (the C ABI declared in
+``include/paged_attention.h``).
+
+Argument marshalling only: every function takes torch CUDA tensors, checks
+their dtype, device and contiguity, and passes raw pointers, sizes and the
+current CUDA stream to the library of the same name.  All computation runs
+in the library's kernels.  There is no fallback: if the library has not been
+built, importing this module raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.environ.get("PA_LIBRARY",
+                           os.path.join(_HERE, "lib", "libpaged_attention.so"))
+
+PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_WORKSPACE, PA_ERR_CUDA = range(5)
+PA_F16, PA_BF16 = 0, 1
+
+DEVERR_SLOT_RANGE = 0x01
+DEVERR_BLOCK_RANGE = 0x02
+DEVERR_PAIR_RANGE = 0x04
+DEVERR_CONTEXT_RANGE = 0x08
+DEVERR_TOKEN_RANGE = 0x10
+DEVERR_TIMEOUT = 0x20
+
+
+class PAError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        name = _lib.pa_status_string(status).decode()
+        extra = ""
+        if status == PA_ERR_CUDA:
+            extra = ": " + _lib.pa_last_cuda_error().decode()
+        super().__init__(f"{fn} returned {name}{extra}")
+        self.status = status
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(_LIB_PATH):
+        raise ImportError(
+            f"CUDA library {_LIB_PATH} is missing; build it with "
+            "`python -m paged_kv_cache_96_gb300.build` (no CPU fallback exists)")
+    lib = ctypes.CDLL(_LIB_PATH)
+    P, i32, f32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    sigs = {
+        "pa_slot_mapping": (i32, [P, P, i32, P, P, i32, i32, i32, i32, P, P]),
+        "pa_reshape_and_cache": (i32, [P, P, P, P, P, i32, i32, i32, i32, i32, i32, P, P]),
+        "pa_copy_blocks": (i32, [P, P, P, i32, i32, i32, i32, i32, i32, P, P]),
+        "pa_decode_workspace_bytes": (sz, [i32, i32, i32, i32, i32, i32]),
+        "pa_decode_attention": (i32, [P, P, P, P, P, i32, P, i32, i32, i32, i32, i32,
+                                      i32, i32, f32, i32, P, sz, i32, P, P]),
+        "pa_status_string": (ctypes.c_char_p, [i32]),
+        "pa_last_cuda_error": (ctypes.c_char_p, []),
+        "pa_version": (i32, []),
+    }
+    for name, (res, args) in sigs.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
+
+
+_lib = _load()
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded C library (for callers that pass raw pointers)."""
+    return _lib
+
+
+# ---------------------------------------------------------------------------
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float16:
+        return PA_F16
+    if t.dtype == torch.bfloat16:
+        return PA_BF16
+    raise TypeError(f"16-bit float tensor expected, got {t.dtype}")
+
+
+def _dev(t: torch.Tensor, name: str, dtype: Optional[torch.dtype] = None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name}: torch.Tensor expected")
+    if not t.is_cuda:
+        raise ValueError(f"{name}: must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name}: {dtype} expected, got {t.dtype}")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _opt(t: Optional[torch.Tensor], name: str):
+    return None if t is None else _dev(t, name, torch.int32)
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(fn: str, status: int) -> None:
+    if status != PA_OK:
+        raise PAError(fn, status)
+
+
+def pa_slot_mapping(slot_mapping: torch.Tensor, block_tables: torch.Tensor,
+                    token_seq: torch.Tensor, token_pos: torch.Tensor,
+                    block_size: int, num_blocks: int,
+                    error_word: Optional[torch.Tensor] = None, stream=None) -> None:
+    """slot_mapping[t] = block_tables[s][p // bs] * bs + p % bs (int32)."""
+    S, MB = block_tables.shape
+    T = token_seq.shape[0]
+    _check("pa_slot_mapping", _lib.pa_slot_mapping(
+        _dev(slot_mapping, "slot_mapping", torch.int32),
+        _dev(block_tables, "block_tables", torch.int32), MB,
+        _dev(token_seq, "token_seq", torch.int32),
+        _dev(token_pos, "token_pos", torch.int32), T, S, block_size, num_blocks,
+        _opt(error_word, "error_word"), _stream(stream)))
+
+
+def pa_reshape_and_cache(key: torch.Tensor, value: torch.Tensor,
+                         key_cache: torch.Tensor, value_cache: torch.Tensor,
+                         slot_mapping: torch.Tensor,
+                         error_word: Optional[torch.Tensor] = None,
+                         stream=None) -> None:
+    """Write key/value [T, Hkv, d] into the pools [N, bs, Hkv, d] at their slots."""
+    T, Hkv, d = key.shape
+    N, bs, Hkv2, d2 = key_cache.shape
+    if (Hkv, d) != (Hkv2, d2) or value.shape != key.shape or value_cache.shape != key_cache.shape:
+        raise ValueError("shape mismatch between new tokens and pools")
+    dt = _dtype_code(key_cache)
+    _check("pa_reshape_and_cache", _lib.pa_reshape_and_cache(
+        _dev(key, "key", key_cache.dtype), _dev(value, "value", key_cache.dtype),
+        _dev(key_cache, "key_cache"), _dev(value_cache, "value_cache", key_cache.dtype),
+        _dev(slot_mapping, "slot_mapping", torch.int32), T, N, bs, Hkv, d, dt,
+        _opt(error_word, "error_word"), _stream(stream)))
+
+
+def pa_copy_blocks(key_cache: torch.Tensor, value_cache: torch.Tensor,
+                   block_mapping: torch.Tensor,
+                   error_word: Optional[torch.Tensor] = None, stream=None) -> None:
+    """For each (src, dst) row of block_mapping [P, 2]: block dst := block src."""
+    N, bs, Hkv, d = key_cache.shape
+    P = block_mapping.shape[0]
+    _check("pa_copy_blocks", _lib.pa_copy_blocks(
+        _dev(key_cache, "key_cache"), _dev(value_cache, "value_cache", key_cache.dtype),
+        _dev(block_mapping, "block_mapping", torch.int32), P, N, bs, Hkv, d,
+        _dtype_code(key_cache), _opt(error_word, "error_word"), _stream(stream)))
+
+
+def pa_decode_workspace_bytes(num_seqs: int, num_heads: int, num_kv_heads: int,
+                              head_dim: int, max_context_len: int,
+                              partition_size: int) -> int:
+    return int(_lib.pa_decode_workspace_bytes(num_seqs, num_heads, num_kv_heads,
+                                              head_dim, max_context_len, partition_size))
+
+
+def pa_decode_attention(out: torch.Tensor, query: torch.Tensor,
+                        key_cache: torch.Tensor, value_cache: torch.Tensor,
+                        block_tables: torch.Tensor, context_lens: torch.Tensor,
+                        max_context_len: int, scale: float, partition_size: int = 0,
+                        workspace: Optional[torch.Tensor] = None,
+                        error_word: Optional[torch.Tensor] = None,
+                        stream=None) -> None:
+    """Paged decode attention; out and query are [S, H, d]."""
+    S, H, d = query.shape
+    N, bs, Hkv, d2 = key_cache.shape
+    MB = block_tables.shape[1]
+    if d != d2 or out.shape != query.shape:
+        raise ValueError("shape mismatch")
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not None:
+        ws_ptr = _dev(workspace, "workspace")
+        ws_bytes = workspace.numel() * workspace.element_size()
+    _check("pa_decode_attention", _lib.pa_decode_attention(
+        _dev(out, "out", query.dtype), _dev(query, "query", key_cache.dtype),
+        _dev(key_cache, "key_cache"), _dev(value_cache, "value_cache", key_cache.dtype),
+        _dev(block_tables, "block_tables", torch.int32), MB,
+        _dev(context_lens, "context_lens", torch.int32), int(max_context_len), S, H, Hkv,
+        d, bs, N, float(scale), int(partition_size), ws_ptr, ws_bytes,
+        _dtype_code(key_cache), _opt(error_word, "error_word"), _stream(stream)))
+
+
+def alloc_workspace(num_seqs: int, num_heads: int, num_kv_heads: int, head_dim: int,
+                    max_context_len: int, partition_size: int,
+                    device="cuda") -> Optional[torch.Tensor]:
+    """Zero-initialised workspace for pa_decode_attention (None if not needed)."""
+    n = pa_decode_workspace_bytes(num_seqs, num_heads, num_kv_heads, head_dim,
+                                  max_context_len, partition_size)
+    if n == 0:
+        return None
+    return torch.zeros(n, dtype=torch.uint8, device=device)

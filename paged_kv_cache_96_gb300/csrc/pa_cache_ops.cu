@@ -1,0 +1,230 @@
+// pa_cache_ops.cu -- the byte-moving and index kernels of the paged KV
+// cache: slot mapping and reshape_and_cache ("PagedAttention & Continuous
+// Batching" §1.5; "vLLM 架构详解", "Block Table 实现") and the copy-on-write
+// block copy ("vLLM源码解析(二)" §3.2).  All three are bit-exact: they move
+// 16-byte words or compute integers.
+#include <cstdio>
+#include <cstring>
+
+#include "pa_common.cuh"
+
+namespace pa {
+
+namespace {
+thread_local char g_last_error[256] = "no error";
+}
+
+pa_status record_cuda(cudaError_t err)
+{
+    if (err == cudaSuccess)
+        return PA_OK;
+    std::snprintf(g_last_error, sizeof g_last_error, "%s: %s", cudaGetErrorName(err),
+                  cudaGetErrorString(err));
+    return PA_ERR_CUDA;
+}
+
+// ---- slot mapping ------------------------------------------------------------
+
+// One thread per token: slot = table[s][p / bs] * bs + p % bs.
+__global__ void slot_mapping_kernel(int32_t *__restrict__ slot_mapping,
+                                    const int32_t *__restrict__ block_tables,
+                                    int max_blocks_per_seq,
+                                    const int32_t *__restrict__ token_seq,
+                                    const int32_t *__restrict__ token_pos, int num_tokens,
+                                    int num_seqs, int block_size, int num_blocks,
+                                    int32_t *error_word)
+{
+    const int t = blockIdx.x * blockDim.x + threadIdx.x;
+    if (t >= num_tokens)
+        return;
+    const int s = token_seq[t];
+    const int p = token_pos[t];
+    int32_t slot = -1;
+    if (s < 0 || s >= num_seqs || p < 0 || p / block_size >= max_blocks_per_seq) {
+        flag_error(error_word, PA_DEVERR_TOKEN_RANGE);
+    } else {
+        const int32_t block =
+            block_tables[static_cast<int64_t>(s) * max_blocks_per_seq + p / block_size];
+        if (block < 0 || block >= num_blocks)
+            flag_error(error_word, PA_DEVERR_BLOCK_RANGE);
+        else
+            slot = block * block_size + p % block_size;
+    }
+    slot_mapping[t] = slot;
+}
+
+// ---- reshape_and_cache --------------------------------------------------------
+
+// One CTA per token; threads stride over the token's K and V rows
+// (num_kv_heads * head_dim 16-bit elements each) in 16-byte words.
+__global__ void reshape_and_cache_kernel(const uint4 *__restrict__ key,
+                                         const uint4 *__restrict__ value,
+                                         uint4 *__restrict__ key_cache,
+                                         uint4 *__restrict__ value_cache,
+                                         const int32_t *__restrict__ slot_mapping,
+                                         int64_t num_slots, int words_per_token,
+                                         int32_t *error_word)
+{
+    const int t = blockIdx.x;
+    const int64_t slot = slot_mapping[t];
+    if (slot < 0)
+        return;
+    if (slot >= num_slots) {
+        if (threadIdx.x == 0)
+            flag_error(error_word, PA_DEVERR_SLOT_RANGE);
+        return;
+    }
+    const uint4 *ks = key + static_cast<int64_t>(t) * words_per_token;
+    const uint4 *vs = value + static_cast<int64_t>(t) * words_per_token;
+    uint4 *kd = key_cache + slot * words_per_token;
+    uint4 *vd = value_cache + slot * words_per_token;
+    for (int i = threadIdx.x; i < words_per_token; i += blockDim.x) {
+        const uint4 k = __ldg(ks + i);
+        const uint4 v = __ldg(vs + i);
+        kd[i] = k;
+        vd[i] = v;
+    }
+}
+
+// ---- copy_blocks ----------------------------------------------------------------
+
+// grid.x = pair, grid.y = 0 (K) / 1 (V), grid.z = slab of 16-byte words.
+constexpr int kCopyThreads = 256;
+constexpr int kCopyWordsPerThread = 4;
+
+__global__ void copy_blocks_kernel(uint4 *__restrict__ key_cache,
+                                   uint4 *__restrict__ value_cache,
+                                   const int32_t *__restrict__ block_mapping,
+                                   int num_blocks, int64_t words_per_block,
+                                   int32_t *error_word)
+{
+    const int pair = blockIdx.x;
+    const int src = block_mapping[2 * pair];
+    const int dst = block_mapping[2 * pair + 1];
+    if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) {
+        if (threadIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0)
+            flag_error(error_word, PA_DEVERR_PAIR_RANGE);
+        return;
+    }
+    uint4 *pool = blockIdx.y == 0 ? key_cache : value_cache;
+    const uint4 *from = pool + static_cast<int64_t>(src) * words_per_block;
+    uint4 *to = pool + static_cast<int64_t>(dst) * words_per_block;
+    const int64_t base =
+        static_cast<int64_t>(blockIdx.z) * kCopyThreads * kCopyWordsPerThread + threadIdx.x;
+    uint4 w[kCopyWordsPerThread];
+#pragma unroll
+    for (int k = 0; k < kCopyWordsPerThread; ++k) {
+        const int64_t i = base + k * kCopyThreads;
+        if (i < words_per_block)
+            w[k] = from[i];
+    }
+#pragma unroll
+    for (int k = 0; k < kCopyWordsPerThread; ++k) {
+        const int64_t i = base + k * kCopyThreads;
+        if (i < words_per_block)
+            to[i] = w[k];
+    }
+}
+
+} // namespace pa
+
+using namespace pa;
+
+extern "C" pa_status pa_slot_mapping(int32_t *slot_mapping, const int32_t *block_tables,
+                                     int max_blocks_per_seq, const int32_t *token_seq,
+                                     const int32_t *token_pos, int num_tokens,
+                                     int num_seqs, int block_size, int num_blocks,
+                                     int32_t *error_word, void *stream)
+{
+    if (num_tokens < 0 || num_seqs < 0 || max_blocks_per_seq <= 0 || block_size <= 0 ||
+        num_blocks <= 0)
+        return PA_ERR_INVALID_ARG;
+    if (num_tokens == 0)
+        return PA_OK;
+    if (!slot_mapping || !block_tables || !token_seq || !token_pos)
+        return PA_ERR_INVALID_ARG;
+    if (static_cast<int64_t>(num_blocks) * block_size > INT32_MAX)
+        return PA_ERR_UNSUPPORTED;
+    const int threads = 256;
+    const int blocks = (num_tokens + threads - 1) / threads;
+    slot_mapping_kernel<<<blocks, threads, 0, as_stream(stream)>>>(
+        slot_mapping, block_tables, max_blocks_per_seq, token_seq, token_pos, num_tokens,
+        num_seqs, block_size, num_blocks, error_word);
+    return record_cuda(cudaGetLastError());
+}
+
+extern "C" pa_status pa_reshape_and_cache(const void *key, const void *value,
+                                          void *key_cache, void *value_cache,
+                                          const int32_t *slot_mapping, int num_tokens,
+                                          int num_blocks, int block_size,
+                                          int num_kv_heads, int head_dim, pa_dtype dtype,
+                                          int32_t *error_word, void *stream)
+{
+    if (num_tokens < 0 || num_blocks <= 0 || block_size <= 0 || num_kv_heads <= 0 ||
+        head_dim <= 0 || (dtype != PA_F16 && dtype != PA_BF16))
+        return PA_ERR_INVALID_ARG;
+    if (num_tokens == 0)
+        return PA_OK;
+    if (!key || !value || !key_cache || !value_cache || !slot_mapping)
+        return PA_ERR_INVALID_ARG;
+    if (!aligned16(key) || !aligned16(value) || !aligned16(key_cache) ||
+        !aligned16(value_cache))
+        return PA_ERR_INVALID_ARG;
+    const int64_t row_bytes = static_cast<int64_t>(num_kv_heads) * head_dim * 2;
+    if (row_bytes % 16 != 0)
+        return PA_ERR_UNSUPPORTED;
+    const int words = static_cast<int>(row_bytes / 16);
+    const int threads = words >= 256 ? 256 : ((words + 31) / 32) * 32;
+    reshape_and_cache_kernel<<<num_tokens, threads, 0, as_stream(stream)>>>(
+        static_cast<const uint4 *>(key), static_cast<const uint4 *>(value),
+        static_cast<uint4 *>(key_cache), static_cast<uint4 *>(value_cache), slot_mapping,
+        static_cast<int64_t>(num_blocks) * block_size, words, error_word);
+    return record_cuda(cudaGetLastError());
+}
+
+extern "C" pa_status pa_copy_blocks(void *key_cache, void *value_cache,
+                                    const int32_t *block_mapping, int num_pairs,
+                                    int num_blocks, int block_size, int num_kv_heads,
+                                    int head_dim, pa_dtype dtype, int32_t *error_word,
+                                    void *stream)
+{
+    if (num_pairs < 0 || num_blocks <= 0 || block_size <= 0 || num_kv_heads <= 0 ||
+        head_dim <= 0 || (dtype != PA_F16 && dtype != PA_BF16))
+        return PA_ERR_INVALID_ARG;
+    if (num_pairs == 0)
+        return PA_OK;
+    if (!key_cache || !value_cache || !block_mapping)
+        return PA_ERR_INVALID_ARG;
+    if (!aligned16(key_cache) || !aligned16(value_cache))
+        return PA_ERR_INVALID_ARG;
+    const int64_t block_bytes =
+        static_cast<int64_t>(block_size) * num_kv_heads * head_dim * 2;
+    if (block_bytes % 16 != 0)
+        return PA_ERR_UNSUPPORTED;
+    const int64_t words = block_bytes / 16;
+    const int64_t per_cta = static_cast<int64_t>(kCopyThreads) * kCopyWordsPerThread;
+    const int64_t slabs = (words + per_cta - 1) / per_cta;
+    if (slabs > 65535 || num_pairs > INT32_MAX / 2)
+        return PA_ERR_UNSUPPORTED;
+    dim3 grid(num_pairs, 2, static_cast<unsigned>(slabs));
+    copy_blocks_kernel<<<grid, kCopyThreads, 0, as_stream(stream)>>>(
+        static_cast<uint4 *>(key_cache), static_cast<uint4 *>(value_cache), block_mapping,
+        num_blocks, words, error_word);
+    return record_cuda(cudaGetLastError());
+}
+
+extern "C" const char *pa_status_string(pa_status status)
+{
+    switch (status) {
+    case PA_OK: return "PA_OK";
+    case PA_ERR_INVALID_ARG: return "PA_ERR_INVALID_ARG";
+    case PA_ERR_UNSUPPORTED: return "PA_ERR_UNSUPPORTED";
+    case PA_ERR_WORKSPACE: return "PA_ERR_WORKSPACE";
+    case PA_ERR_CUDA: return "PA_ERR_CUDA";
+    }
+    return "PA_UNKNOWN_STATUS";
+}
+
+extern "C" const char *pa_last_cuda_error(void) { return g_last_error; }
+
+extern "C" int pa_version(void) { return 100; }

@@ -1,0 +1,768 @@
+// pa_decode.cu -- paged decode attention for sm_103a.
+//
+// What it computes ("PagedAttention & Continuous Batching", §1.6 and §2.4):
+// for every running sequence s and query head h, the softmax-weighted sum of
+// the value vectors of the sequence's cached tokens, where token p's K and V
+// live in physical block block_tables[s][p / block_size], row
+// p % block_size of the token-major pools [num_blocks][block_size]
+// [num_kv_heads][head_dim].  Query heads are grouped over KV heads
+// (kh = h / G), so one KV head serves G query heads.
+//
+// How (GB300 design):
+//  * Work unit = (sequence, KV head, partition of `part_tokens` tokens).  A
+//    persistent grid (one CTA per SM) walks the units round-robin; units are
+//    numbered KV-head-fastest so the CTAs working on the Hkv heads of one
+//    partition run side by side and together stream whole 2 KB token rows.
+//  * Each warp owns a ring of NST shared-memory stages.  A stage holds one
+//    16-token tile of K and of V for one KV head, fetched from the pool by
+//    4-D tiled TMA loads (128-byte swizzle) that complete on the stage's
+//    mbarrier.  The warp consumes tile i and immediately refills the stage
+//    with its tile i + NST, crossing into the next unit when the current
+//    one runs out, so the loads in flight never drain at unit boundaries.
+//  * The G query heads of a KV head form the N dimension of tensor-core
+//    tiles: S^T-tile [16 tokens x 8 heads] = K[16 x d] . Q^T[d x 8] and
+//    O^T[d x 8] += V^T[d x 16] . P^T[16 x 8] with mma.sync m16n8k16 (fp32
+//    accumulate); P goes from the S accumulator layout to the B-operand
+//    layout with movmatrix.  Every K/V byte is read from HBM once per step.
+//  * Softmax is online in fp32 (running max, running sum, exp2 with the
+//    scale folded into log2 units).  Warps merge their (m, l, O) through
+//    shared memory at the end of a unit.
+//  * Split context: a unit that is one of several partitions of its
+//    sequence writes a partial (m, l, o) to the workspace; the last unit of
+//    a (sequence, KV head) to arrive (an atomic counter) merges all of them
+//    by log-sum-exp weights and writes the output, then zeroes its counter.
+//  * Bounds: table entries outside [0, num_blocks) are never fetched (the
+//    tile is skipped, an error bit is set); tokens past the context are
+//    masked in the scores and their value rows are zeroed before the
+//    contraction, so poisoned (NaN) slots never reach the output.  Every
+//    wait on a stage is bounded in time.
+#include <cuda.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdio>
+#include <mutex>
+
+#include "pa_common.cuh"
+#include "pa_ptx.cuh"
+
+namespace pa {
+
+constexpr int kTileTokens = 16;
+constexpr uint64_t kWaitLimitNs = 1000000000ull;  // one second per stage wait
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr unsigned kFull = 0xffffffffu;
+
+struct DecodeParams {
+    void *out;
+    const void *query;
+    const int32_t *block_tables;
+    const int32_t *context_lens;
+    float *part_m;
+    float *part_l;
+    float *part_o;
+    uint32_t *arrivals;
+    int32_t *error_word;
+    int num_seqs, num_heads, num_kv_heads, group;
+    int max_blocks_per_seq, num_blocks, block_size, max_context_len;
+    int part_tokens;  // tokens per work unit (a multiple of 16)
+    int max_parts;    // partitions per sequence the workspace holds
+    float scale_log2; // scale * log2(e)
+};
+
+// Shared-memory layout (offsets from a 1024-byte aligned base).
+template <int D, int NT, int NW, int NST> struct Layout {
+    static constexpr int kHalfBytes = kTileTokens * 128;      // 16 rows x 64 elements
+    static constexpr int kTileBytes = (D / 64) * kHalfBytes;  // one K (or V) tile
+    static constexpr int kStageBytes = 2 * kTileBytes;        // K tile + V tile
+    static constexpr int kHeads = 8 * NT;
+    static constexpr int kPitch = D + 4;  // floats per merge row (bank spread)
+    static constexpr int kStages = 0;
+    static constexpr int kMergeO = kStages + NW * NST * kStageBytes;
+    static constexpr int kMergeM = kMergeO + NW * kHeads * kPitch * 4;
+    static constexpr int kMergeL = kMergeM + NW * kHeads * 4;
+    static constexpr int kBars = kMergeL + NW * kHeads * 4;
+    static constexpr int kFlags = kBars + NW * NST * 8;
+    static constexpr int kCtrl = kFlags + NW * NST * 4;
+    static constexpr int kSeq = kCtrl + 64;  // int ctx[S], int prefix[S + 1]
+    static size_t bytes(int num_seqs) { return 1024 + kSeq + 8 * (size_t)(num_seqs + 1); }
+    static_assert(kBars % 8 == 0, "mbarriers need 8-byte alignment");
+    static_assert(kStageBytes % 1024 == 0, "stages must keep 1024-byte alignment");
+};
+
+template <typename T, int D, int NT, int NW, int NST>
+__global__ void __launch_bounds__(NW * 32, 1)
+    paged_decode_kernel(const __grid_constant__ DecodeParams p,
+                        const __grid_constant__ CUtensorMap tmap_k,
+                        const __grid_constant__ CUtensorMap tmap_v)
+{
+    using L = Layout<D, NT, NW, NST>;
+    using Op = MmaOp<T>;
+    constexpr int KT = D / 16;  // k-steps of the score product, m-tiles of the output
+    constexpr int kHeads = L::kHeads;
+
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_addr = smem_addr(smem_raw);
+    uint8_t *smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+    const uint32_t sbase = smem_addr(smem);
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+    const int g = lane >> 2;  // mma group (row of the accumulator fragment)
+    const int t4 = lane & 3;  // thread in group (column pair)
+
+    const int S = p.num_seqs;
+    const int Hkv = p.num_kv_heads;
+    const int G = p.group;
+    const int P = p.part_tokens;
+
+    int *ctx_s = reinterpret_cast<int *>(smem + L::kSeq);
+    int *pref = ctx_s + S;
+    int *ctrl = reinterpret_cast<int *>(smem + L::kCtrl);
+    int *flags = reinterpret_cast<int *>(smem + L::kFlags);
+    float *merge_o = reinterpret_cast<float *>(smem + L::kMergeO);
+    float *merge_m = reinterpret_cast<float *>(smem + L::kMergeM);
+    float *merge_l = reinterpret_cast<float *>(smem + L::kMergeL);
+
+    // ---- context lengths and partition prefix sums -----------------------
+    const int ctx_limit = min(p.max_context_len, p.max_blocks_per_seq * p.block_size);
+    for (int s = tid; s < S; s += NW * 32) {
+        int c = p.context_lens[s];
+        if (c < 0 || c > ctx_limit) {
+            if (blockIdx.x == 0)
+                flag_error(p.error_word, PA_DEVERR_CONTEXT_RANGE);
+            c = c < 0 ? 0 : ctx_limit;
+        }
+        ctx_s[s] = c;
+    }
+    if (lane == 0) {
+        for (int k = 0; k < NST; ++k)
+            mbar_init(sbase + L::kBars + (warp * NST + k) * 8, 1);
+        fence_barrier_init();
+    }
+    if (tid == 0) {
+        prefetch_tensormap(&tmap_k);
+        prefetch_tensormap(&tmap_v);
+    }
+    __syncthreads();
+    if (warp == 0) {
+        int carry = 0;
+        for (int base = 0; base < S; base += 32) {
+            const int s = base + lane;
+            const int n = s < S ? (ctx_s[s] + P - 1) / P : 0;
+            int x = n;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(kFull, x, o);
+                if (lane >= o)
+                    x += y;
+            }
+            if (s < S)
+                pref[s] = carry + x - n;
+            carry += __shfl_sync(kFull, x, 31);
+        }
+        if (lane == 0)
+            pref[S] = carry;
+    }
+    __syncthreads();
+    const int total_units = pref[S] * Hkv;
+
+    // ---- sequences with no context get zero rows ----------------------------
+    for (int s = blockIdx.x; s < S; s += gridDim.x) {
+        if (ctx_s[s] != 0)
+            continue;
+        uint4 *row = reinterpret_cast<uint4 *>(static_cast<T *>(p.out) +
+                                               (size_t)s * p.num_heads * D);
+        for (int i = tid; i < p.num_heads * D / 8; i += NW * 32)
+            row[i] = make_uint4(0, 0, 0, 0);
+    }
+
+    // ---- unit decoding --------------------------------------------------------
+    // unit u -> partition q = u / Hkv, kv head u % Hkv; sequence s is the one
+    // with pref[s] <= q < pref[s + 1].
+    auto decode_unit = [&](int u, int &s, int &kh, int &j, int &tok0, int &ntiles) {
+        const int q = u / Hkv;
+        kh = u - q * Hkv;
+        int lo = 0, hi = S - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (pref[mid] <= q)
+                lo = mid;
+            else
+                hi = mid - 1;
+        }
+        s = lo;
+        j = q - pref[s];
+        tok0 = j * P;
+        const int tok_end = min(ctx_s[s], tok0 + P);
+        ntiles = (tok_end - tok0 + kTileTokens - 1) / kTileTokens;
+    };
+
+    // ---- producer: this warp's next tile to fetch -----------------------------
+    int pu = blockIdx.x, ps = 0, pkh = 0, pj = 0, ptok0 = 0, pnt = 0, ptile = warp;
+    bool pdone = pu >= total_units;
+    if (!pdone)
+        decode_unit(pu, ps, pkh, pj, ptok0, pnt);
+    auto producer_skip_empty = [&]() {
+        while (!pdone && ptile >= pnt) {
+            pu += gridDim.x;
+            if (pu >= total_units) {
+                pdone = true;
+                break;
+            }
+            decode_unit(pu, ps, pkh, pj, ptok0, pnt);
+            ptile = warp;
+        }
+    };
+    producer_skip_empty();
+
+    uint32_t issued = 0, consumed = 0;
+    uint32_t inflight = 0;  // stages with a fetch not yet waited for
+    bool aborted = false;
+
+    auto produce = [&]() {
+        if (pdone || aborted)
+            return;
+        const int stage = issued % NST;
+        const uint32_t bar = sbase + L::kBars + (warp * NST + stage) * 8;
+        const uint32_t dst = sbase + L::kStages + (warp * NST + stage) * L::kStageBytes;
+        if (lane == 0) {
+            const int tok = ptok0 + ptile * kTileTokens;
+            const int blk = tok / p.block_size;
+            const int row = tok - blk * p.block_size;
+            const int32_t phys =
+                p.block_tables[(size_t)ps * p.max_blocks_per_seq + blk];
+            const bool ok = phys >= 0 && phys < p.num_blocks;
+            flags[warp * NST + stage] = ok;
+            if (ok) {
+                mbar_arrive_expect_tx(bar, L::kStageBytes);
+#pragma unroll
+                for (int hf = 0; hf < D / 64; ++hf) {
+                    tma_load_4d(dst + hf * L::kHalfBytes, &tmap_k, bar, hf * 64, pkh, row,
+                                phys);
+                    tma_load_4d(dst + L::kTileBytes + hf * L::kHalfBytes, &tmap_v, bar,
+                                hf * 64, pkh, row, phys);
+                }
+            } else {
+                flag_error(p.error_word, PA_DEVERR_BLOCK_RANGE);
+                mbar_arrive(bar);
+            }
+        }
+        inflight |= 1u << stage;
+        ++issued;
+        ptile += NW;
+        producer_skip_empty();
+    };
+    for (int k = 0; k < NST; ++k)
+        produce();
+
+    // Per-lane ldmatrix row/chunk selectors (128-byte swizzle: the 16-byte
+    // chunk c of row r sits at chunk c ^ (r & 7)).
+    const int li = lane & 7, lj = lane >> 3;
+    const int k_row = li + ((lj & 1) << 3), k_cj = lj >> 1;   // K: A operand
+    const int v_row = li + ((lj >> 1) << 3), v_cj = lj & 1;   // V^T: A operand (trans)
+
+    // ---- units --------------------------------------------------------------------
+    for (int u = blockIdx.x; u < total_units; u += gridDim.x) {
+        int s, kh, j, tok0, ntiles;
+        decode_unit(u, s, kh, j, tok0, ntiles);
+        const int tok_end = min(ctx_s[s], tok0 + P);
+        const int nparts = (ctx_s[s] + P - 1) / P;
+
+        // Query fragments (B operand of the score product): head 8nt+g of
+        // the group, elements d = 16kk + 2t4 (+1) and +8 (+9).
+        uint32_t qf[NT][KT][2];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            const int hg = nt * 8 + g;
+            const uint32_t *qrow = reinterpret_cast<const uint32_t *>(
+                static_cast<const T *>(p.query) +
+                ((size_t)s * p.num_heads + (size_t)kh * G + (hg < G ? hg : 0)) * D);
+#pragma unroll
+            for (int kk = 0; kk < KT; ++kk) {
+                qf[nt][kk][0] = hg < G ? __ldg(qrow + kk * 8 + t4) : 0u;
+                qf[nt][kk][1] = hg < G ? __ldg(qrow + kk * 8 + 4 + t4) : 0u;
+            }
+        }
+
+        float o[KT][NT][4];
+        float mrun[NT][2], lrun[NT][2];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            mrun[nt][0] = mrun[nt][1] = -INFINITY;
+            lrun[nt][0] = lrun[nt][1] = 0.f;
+#pragma unroll
+            for (int mt = 0; mt < KT; ++mt)
+                o[mt][nt][0] = o[mt][nt][1] = o[mt][nt][2] = o[mt][nt][3] = 0.f;
+        }
+
+        for (int tile = warp; tile < ntiles; tile += NW) {
+            const int stage = consumed % NST;
+            const uint32_t parity = (consumed / NST) & 1u;
+            const uint32_t bar = sbase + L::kBars + (warp * NST + stage) * 8;
+            bool ready = false;
+            if (!aborted) {
+                ready = __all_sync(kFull, mbar_wait_bounded(bar, parity, kWaitLimitNs));
+                if (ready) {
+                    inflight &= ~(1u << stage);
+                } else {
+                    aborted = true;
+                    if (lane == 0)
+                        flag_error(p.error_word, PA_DEVERR_TIMEOUT);
+                }
+            }
+            const bool valid = ready && flags[warp * NST + stage] != 0;
+            if (valid) {
+                const uint32_t kbase =
+                    sbase + L::kStages + (warp * NST + stage) * L::kStageBytes;
+                const uint32_t vbase = kbase + L::kTileBytes;
+                const int nv = tok_end - (tok0 + tile * kTileTokens);  // valid rows
+                const bool partial = nv < kTileTokens;
+
+                // scores S[token][head] = K . Q^T
+                float sc[NT][4];
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+                    sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+#pragma unroll
+                for (int kk = 0; kk < KT; ++kk) {
+                    uint32_t a[4];
+                    ldmatrix_x4(kbase + (kk >> 2) * L::kHalfBytes + k_row * 128 +
+                                    ((((kk & 3) * 2 + k_cj) ^ li) << 4),
+                                a);
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt)
+                        Op::run(sc[nt], a, qf[nt][kk][0], qf[nt][kk][1]);
+                }
+
+                // online softmax; P^T fragments for the value product
+                uint32_t pb[NT][2];
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    float s0 = sc[nt][0] * p.scale_log2, s1 = sc[nt][1] * p.scale_log2;
+                    float s2 = sc[nt][2] * p.scale_log2, s3 = sc[nt][3] * p.scale_log2;
+                    if (partial) {
+                        if (g >= nv)
+                            s0 = s1 = -INFINITY;
+                        if (g + 8 >= nv)
+                            s2 = s3 = -INFINITY;
+                    }
+                    float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
+#pragma unroll
+                    for (int off = 4; off < 32; off <<= 1) {
+                        mx0 = fmaxf(mx0, __shfl_xor_sync(kFull, mx0, off));
+                        mx1 = fmaxf(mx1, __shfl_xor_sync(kFull, mx1, off));
+                    }
+                    const float mn0 = fmaxf(mrun[nt][0], mx0);
+                    const float mn1 = fmaxf(mrun[nt][1], mx1);
+                    const float mu0 = mn0 == -INFINITY ? 0.f : mn0;
+                    const float mu1 = mn1 == -INFINITY ? 0.f : mn1;
+                    const float al0 = exp2f(mrun[nt][0] - mu0);
+                    const float al1 = exp2f(mrun[nt][1] - mu1);
+                    const float p0 = exp2f(s0 - mu0), p2 = exp2f(s2 - mu0);
+                    const float p1 = exp2f(s1 - mu1), p3 = exp2f(s3 - mu1);
+                    const bool grew = mn0 != mrun[nt][0] || mn1 != mrun[nt][1];
+                    lrun[nt][0] = lrun[nt][0] * al0 + (p0 + p2);
+                    lrun[nt][1] = lrun[nt][1] * al1 + (p1 + p3);
+                    mrun[nt][0] = mn0;
+                    mrun[nt][1] = mn1;
+                    if (__any_sync(kFull, grew)) {
+#pragma unroll
+                        for (int mt = 0; mt < KT; ++mt) {
+                            o[mt][nt][0] *= al0;
+                            o[mt][nt][1] *= al1;
+                            o[mt][nt][2] *= al0;
+                            o[mt][nt][3] *= al1;
+                        }
+                    }
+                    pb[nt][0] = movmatrix_trans(Op::pack(p0, p1));
+                    pb[nt][1] = movmatrix_trans(Op::pack(p2, p3));
+                }
+
+                // O^T[d][head] += V^T . P^T
+                uint32_t m01 = 0xffffffffu, m89 = 0xffffffffu;
+                if (partial) {
+                    m01 = (2 * t4 < nv ? 0x0000ffffu : 0u) | (2 * t4 + 1 < nv ? 0xffff0000u : 0u);
+                    m89 = (2 * t4 + 8 < nv ? 0x0000ffffu : 0u) |
+                          (2 * t4 + 9 < nv ? 0xffff0000u : 0u);
+                }
+#pragma unroll
+                for (int mt = 0; mt < KT; ++mt) {
+                    uint32_t a[4];
+                    ldmatrix_x4_trans(vbase + (mt >> 2) * L::kHalfBytes + v_row * 128 +
+                                          ((((mt & 3) * 2 + v_cj) ^ li) << 4),
+                                      a);
+                    a[0] &= m01;
+                    a[1] &= m01;
+                    a[2] &= m89;
+                    a[3] &= m89;
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt)
+                        Op::run(o[mt][nt], a, pb[nt][0], pb[nt][1]);
+                }
+            }
+            __syncwarp();
+            ++consumed;
+            produce();
+        }
+
+        // ---- end of unit: merge the warps' (m, l, O) -------------------------------
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int k = 0; k < 2; ++k)
+#pragma unroll
+                for (int off = 4; off < 32; off <<= 1)
+                    lrun[nt][k] += __shfl_xor_sync(kFull, lrun[nt][k], off);
+        {
+            float *mo = merge_o + warp * kHeads * L::kPitch;
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                const int h0 = nt * 8 + 2 * t4;
+#pragma unroll
+                for (int mt = 0; mt < KT; ++mt) {
+                    const int d0 = mt * 16 + g;
+                    mo[h0 * L::kPitch + d0] = o[mt][nt][0];
+                    mo[(h0 + 1) * L::kPitch + d0] = o[mt][nt][1];
+                    mo[h0 * L::kPitch + d0 + 8] = o[mt][nt][2];
+                    mo[(h0 + 1) * L::kPitch + d0 + 8] = o[mt][nt][3];
+                }
+                if (g == 0) {
+                    merge_m[warp * kHeads + h0] = mrun[nt][0];
+                    merge_m[warp * kHeads + h0 + 1] = mrun[nt][1];
+                    merge_l[warp * kHeads + h0] = lrun[nt][0];
+                    merge_l[warp * kHeads + h0 + 1] = lrun[nt][1];
+                }
+            }
+        }
+        __syncthreads();
+
+        const int items = G * (D / 8);
+        for (int it = tid; it < items; it += NW * 32) {
+            const int jh = it / (D / 8);
+            const int d0 = (it - jh * (D / 8)) * 8;
+            float mmax = -INFINITY;
+#pragma unroll
+            for (int w = 0; w < NW; ++w)
+                mmax = fmaxf(mmax, merge_m[w * kHeads + jh]);
+            const float mu = mmax == -INFINITY ? 0.f : mmax;
+            float lsum = 0.f;
+            float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int w = 0; w < NW; ++w) {
+                const float wgt = exp2f(merge_m[w * kHeads + jh] - mu);
+                lsum += wgt * merge_l[w * kHeads + jh];
+                const float4 *src = reinterpret_cast<const float4 *>(
+                    merge_o + (w * kHeads + jh) * L::kPitch + d0);
+                const float4 x0 = src[0], x1 = src[1];
+                acc[0] += wgt * x0.x; acc[1] += wgt * x0.y; acc[2] += wgt * x0.z; acc[3] += wgt * x0.w;
+                acc[4] += wgt * x1.x; acc[5] += wgt * x1.y; acc[6] += wgt * x1.z; acc[7] += wgt * x1.w;
+            }
+            const float inv = 1.f / lsum;
+            const size_t h = (size_t)kh * G + jh;
+            if (nparts == 1) {
+                T vals[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    vals[e] = Op::from_float(acc[e] * inv);
+                *reinterpret_cast<uint4 *>(static_cast<T *>(p.out) +
+                                           ((size_t)s * p.num_heads + h) * D + d0) =
+                    *reinterpret_cast<const uint4 *>(vals);
+            } else {
+                const size_t idx = ((size_t)s * p.num_heads + h) * p.max_parts + j;
+                float4 *dst = reinterpret_cast<float4 *>(p.part_o + idx * D + d0);
+                dst[0] = make_float4(acc[0] * inv, acc[1] * inv, acc[2] * inv, acc[3] * inv);
+                dst[1] = make_float4(acc[4] * inv, acc[5] * inv, acc[6] * inv, acc[7] * inv);
+                if (d0 == 0) {
+                    p.part_m[idx] = mmax * kLn2;
+                    p.part_l[idx] = lsum;
+                }
+            }
+        }
+
+        if (nparts > 1) {
+            // last partition of (s, kh) to finish merges all of them
+            __syncthreads();
+            if (tid == 0) {
+                __threadfence();
+                const uint32_t prev = atomicAdd(p.arrivals + (size_t)s * Hkv + kh, 1u);
+                ctrl[0] = prev == (uint32_t)(nparts - 1);
+            }
+            __syncthreads();
+            if (ctrl[0]) {
+                __threadfence();
+                for (int it = tid; it < items; it += NW * 32) {
+                    const int jh = it / (D / 8);
+                    const int d0 = (it - jh * (D / 8)) * 8;
+                    const size_t h = (size_t)kh * G + jh;
+                    const size_t base = ((size_t)s * p.num_heads + h) * p.max_parts;
+                    float mmax = -INFINITY;
+                    for (int q = 0; q < nparts; ++q)
+                        mmax = fmaxf(mmax, __ldcg(p.part_m + base + q));
+                    float lsum = 0.f;
+                    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+                    for (int q = 0; q < nparts; ++q) {
+                        const float wgt =
+                            __ldcg(p.part_l + base + q) *
+                            exp2f((__ldcg(p.part_m + base + q) - mmax) * kLog2e);
+                        lsum += wgt;
+                        const float4 *src =
+                            reinterpret_cast<const float4 *>(p.part_o + (base + q) * D + d0);
+                        const float4 x0 = __ldcg(src), x1 = __ldcg(src + 1);
+                        acc[0] += wgt * x0.x; acc[1] += wgt * x0.y; acc[2] += wgt * x0.z; acc[3] += wgt * x0.w;
+                        acc[4] += wgt * x1.x; acc[5] += wgt * x1.y; acc[6] += wgt * x1.z; acc[7] += wgt * x1.w;
+                    }
+                    const float inv = 1.f / lsum;
+                    T vals[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        vals[e] = Op::from_float(acc[e] * inv);
+                    *reinterpret_cast<uint4 *>(static_cast<T *>(p.out) +
+                                               ((size_t)s * p.num_heads + h) * D + d0) =
+                        *reinterpret_cast<const uint4 *>(vals);
+                }
+                if (tid == 0)
+                    p.arrivals[(size_t)s * Hkv + kh] = 0u;
+            }
+        }
+        __syncthreads();  // merge scratch and ctrl are reused by the next unit
+    }
+
+    // ---- drain: wait (bounded) for any fetch still landing in this warp's ring ----
+    if (inflight != 0) {
+        for (int k = 0; k < NST; ++k) {
+            if (!(inflight & (1u << k)))
+                continue;
+            // the most recent fetch into stage k was issue number
+            // issued - 1 - ((issued - 1 - k) % NST)
+            const uint32_t last = issued - 1 - ((issued - 1 - k) % NST);
+            const uint32_t bar = sbase + L::kBars + (warp * NST + k) * 8;
+            mbar_wait_bounded(bar, (last / NST) & 1u, kWaitLimitNs);
+        }
+    }
+}
+
+// ---- host side -------------------------------------------------------------------
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *,
+                                   const cuuint32_t *, const cuuint32_t *,
+                                   CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn get_encode_fn()
+{
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    });
+    return fn;
+}
+
+// Tensor map over a pool [num_blocks][block_size][num_kv_heads][head_dim]
+// with a box of 64 elements x 1 head x 16 tokens x 1 block, 128-byte swizzle.
+static bool encode_pool_map(CUtensorMap *map, const void *pool, pa_dtype dtype,
+                            int num_blocks, int block_size, int num_kv_heads,
+                            int head_dim)
+{
+    EncodeTiledFn fn = get_encode_fn();
+    if (!fn)
+        return false;
+    const cuuint64_t dims[4] = {(cuuint64_t)head_dim, (cuuint64_t)num_kv_heads,
+                                (cuuint64_t)block_size, (cuuint64_t)num_blocks};
+    const cuuint64_t strides[3] = {(cuuint64_t)head_dim * 2,
+                                   (cuuint64_t)num_kv_heads * head_dim * 2,
+                                   (cuuint64_t)block_size * num_kv_heads * head_dim * 2};
+    const cuuint32_t box[4] = {64, 1, (cuuint32_t)kTileTokens, 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    const CUresult r = fn(map,
+                          dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                           : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                          4, const_cast<void *>(pool), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+constexpr int kWarps = 4;
+constexpr int kStagesPerWarp = 4;
+
+template <typename T, int D, int NT>
+static pa_status launch_decode(const DecodeParams &prm, const CUtensorMap &mk,
+                               const CUtensorMap &mv, cudaStream_t stream,
+                               long long max_units)
+{
+    using L = Layout<D, NT, kWarps, kStagesPerWarp>;
+    auto kernel = paged_decode_kernel<T, D, NT, kWarps, kStagesPerWarp>;
+    const size_t smem = L::bytes(prm.num_seqs);
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return record_cuda(e);
+    int optin = 0, sms = 0;
+    cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (smem > (size_t)optin)
+        return PA_ERR_UNSUPPORTED;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem);
+    if (e != cudaSuccess)
+        return record_cuda(e);
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kWarps * 32, smem);
+    if (e != cudaSuccess)
+        return record_cuda(e);
+    if (per_sm < 1)
+        return PA_ERR_UNSUPPORTED;
+    long long grid = (long long)sms * per_sm;
+    if (grid > max_units)
+        grid = max_units;
+    if (grid < 1)
+        grid = 1;
+    kernel<<<(unsigned)grid, kWarps * 32, smem, stream>>>(prm, mk, mv);
+    return record_cuda(cudaGetLastError());
+}
+
+static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+struct WorkspaceLayout {
+    size_t m_off, l_off, o_off, arr_off, total;
+};
+
+static WorkspaceLayout workspace_layout(int S, int H, int Hkv, int D, int parts)
+{
+    WorkspaceLayout w{};
+    if (parts <= 1)
+        return w;
+    const size_t ml = align256((size_t)S * H * parts * 4);
+    w.m_off = 0;
+    w.l_off = ml;
+    w.o_off = 2 * ml;
+    w.arr_off = w.o_off + align256((size_t)S * H * parts * D * 4);
+    w.total = w.arr_off + align256((size_t)S * Hkv * 4);
+    return w;
+}
+
+static int num_parts(int max_context_len, int partition_size)
+{
+    if (partition_size <= 0 || max_context_len <= 0)
+        return 1;
+    return (int)(((long long)max_context_len + partition_size - 1) / partition_size);
+}
+
+} // namespace pa
+
+using namespace pa;
+
+extern "C" size_t pa_decode_workspace_bytes(int num_seqs, int num_heads, int num_kv_heads,
+                                            int head_dim, int max_context_len,
+                                            int partition_size)
+{
+    if (num_seqs < 0 || num_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
+        max_context_len < 0 || partition_size < 0)
+        return 0;
+    const int parts = num_parts(max_context_len, partition_size);
+    return workspace_layout(num_seqs, num_heads, num_kv_heads, head_dim, parts).total;
+}
+
+extern "C" pa_status pa_decode_attention(void *out, const void *query, const void *key_cache,
+                                         const void *value_cache, const int32_t *block_tables,
+                                         int max_blocks_per_seq, const int32_t *context_lens,
+                                         int max_context_len, int num_seqs, int num_heads,
+                                         int num_kv_heads, int head_dim, int block_size,
+                                         int num_blocks, float scale, int partition_size,
+                                         void *workspace, size_t workspace_bytes,
+                                         pa_dtype dtype, int32_t *error_word, void *stream)
+{
+    if (num_seqs < 0 || num_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
+        block_size <= 0 || num_blocks <= 0 || max_blocks_per_seq <= 0 ||
+        max_context_len < 0 || partition_size < 0 || !std::isfinite(scale) ||
+        (dtype != PA_F16 && dtype != PA_BF16))
+        return PA_ERR_INVALID_ARG;
+    if (num_heads % num_kv_heads != 0)
+        return PA_ERR_INVALID_ARG;
+    if (num_seqs == 0)
+        return PA_OK;
+    if (!out || !query || !key_cache || !value_cache || !block_tables || !context_lens)
+        return PA_ERR_INVALID_ARG;
+    if (!aligned16(out) || !aligned16(query) || !aligned16(key_cache) ||
+        !aligned16(value_cache))
+        return PA_ERR_INVALID_ARG;
+    const int group = num_heads / num_kv_heads;
+    if ((head_dim != 64 && head_dim != 128) || block_size % kTileTokens != 0 ||
+        block_size > 256 || group > 16 ||
+        (long long)num_blocks * block_size >= (1ll << 31) ||
+        (long long)max_blocks_per_seq * block_size >= (1ll << 31))
+        return PA_ERR_UNSUPPORTED;
+    if (partition_size != 0 && partition_size % kTileTokens != 0)
+        return PA_ERR_UNSUPPORTED;
+
+    const int parts = num_parts(max_context_len, partition_size);
+    const WorkspaceLayout wl =
+        workspace_layout(num_seqs, num_heads, num_kv_heads, head_dim, parts);
+    if (wl.total > 0 && (workspace == nullptr || workspace_bytes < wl.total ||
+                         (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0))
+        return PA_ERR_WORKSPACE;
+
+    DecodeParams prm{};
+    prm.out = out;
+    prm.query = query;
+    prm.block_tables = block_tables;
+    prm.context_lens = context_lens;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    prm.part_m = wl.total ? reinterpret_cast<float *>(ws + wl.m_off) : nullptr;
+    prm.part_l = wl.total ? reinterpret_cast<float *>(ws + wl.l_off) : nullptr;
+    prm.part_o = wl.total ? reinterpret_cast<float *>(ws + wl.o_off) : nullptr;
+    prm.arrivals = wl.total ? reinterpret_cast<uint32_t *>(ws + wl.arr_off) : nullptr;
+    prm.error_word = error_word;
+    prm.num_seqs = num_seqs;
+    prm.num_heads = num_heads;
+    prm.num_kv_heads = num_kv_heads;
+    prm.group = group;
+    prm.max_blocks_per_seq = max_blocks_per_seq;
+    prm.num_blocks = num_blocks;
+    prm.block_size = block_size;
+    prm.max_context_len = max_context_len;
+    // Single pass: one unit covers the longest possible context.
+    const long long ctx_cap = (long long)max_blocks_per_seq * block_size;
+    const long long whole = ((std::max<long long>(1, std::min<long long>(
+                                  max_context_len, ctx_cap)) + kTileTokens - 1) /
+                             kTileTokens) * kTileTokens;
+    prm.part_tokens = parts > 1 ? partition_size : (int)whole;
+    prm.max_parts = parts;
+    prm.scale_log2 = scale * kLog2e;
+
+    CUtensorMap mk, mv;
+    if (!encode_pool_map(&mk, key_cache, dtype, num_blocks, block_size, num_kv_heads,
+                         head_dim) ||
+        !encode_pool_map(&mv, value_cache, dtype, num_blocks, block_size, num_kv_heads,
+                         head_dim))
+        return PA_ERR_CUDA;
+
+    const long long max_units = (long long)num_seqs * num_kv_heads * parts;
+    cudaStream_t st = as_stream(stream);
+    const bool bf = dtype == PA_BF16;
+    const bool wide = group > 8;
+    if (head_dim == 128) {
+        if (bf)
+            return wide ? launch_decode<__nv_bfloat16, 128, 2>(prm, mk, mv, st, max_units)
+                        : launch_decode<__nv_bfloat16, 128, 1>(prm, mk, mv, st, max_units);
+        return wide ? launch_decode<__half, 128, 2>(prm, mk, mv, st, max_units)
+                    : launch_decode<__half, 128, 1>(prm, mk, mv, st, max_units);
+    }
+    if (bf)
+        return wide ? launch_decode<__nv_bfloat16, 64, 2>(prm, mk, mv, st, max_units)
+                    : launch_decode<__nv_bfloat16, 64, 1>(prm, mk, mv, st, max_units);
+    return wide ? launch_decode<__half, 64, 2>(prm, mk, mv, st, max_units)
+                : launch_decode<__half, 64, 1>(prm, mk, mv, st, max_units);
+}

@@ -1,0 +1,166 @@
+"""One paged decode step on the GPU, driven through the C ABI.
+
+A decode step, in the order the serving engine of the pages runs it
+("vLLM源码解析(二)" §4.1 engine step; "PagedAttention & Continuous
+Batching" §1.5, §1.6):
+
+  1. slot mapping of the step's new tokens (one per running sequence),
+  2. reshape_and_cache of their K/V into the paged pools,
+  3. copy-on-write block copies, when the step has any,
+  4. paged decode attention of every sequence over its whole context
+     (single pass, or split-context partitions merged in the same launch).
+
+Torch provides device memory and the stream; every step above is a kernel
+of ``libpaged_attention.so``.
+"""
+from __future__ import annotations
+
+from typing import Optional
+
+import numpy as np
+import torch
+
+from . import binding as B
+from .workloads import Workload
+
+
+def _t16(a: np.ndarray, dtype: str, device) -> torch.Tensor:
+    t = torch.from_numpy(np.ascontiguousarray(a).view(np.int16))
+    t = t.view(torch.float16 if dtype == "f16" else torch.bfloat16)
+    return t.to(device)
+
+
+def _ti(a: np.ndarray, device) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(device)
+
+
+class DecodeStep:
+    """Device state of one workload: pools holding the cached history,
+    the step's inputs, and the output / workspace buffers."""
+
+    def __init__(self, w: Workload, device: str = "cuda",
+                 partition_size: Optional[int] = None, build_pools: bool = True):
+        self.w = w
+        self.device = torch.device(device)
+        self.partition_size = (w.spec.partition_size if partition_size is None
+                               else partition_size)
+        dt = w.dtype
+        self.torch_dtype = torch.float16 if dt == "f16" else torch.bfloat16
+        self.max_context_len = int(w.context_lens.max())
+        fill = int(np.int16(np.uint16(w.fill).view(np.int16)))
+        shape = w.pool_shape()
+        self.key_cache = torch.full(shape, fill, dtype=torch.int16,
+                                    device=self.device).view(self.torch_dtype)
+        self.value_cache = torch.full(shape, fill, dtype=torch.int16,
+                                      device=self.device).view(self.torch_dtype)
+        self.block_tables = _ti(w.block_tables, self.device)
+        self.step_block_tables = _ti(w.step_block_tables, self.device)
+        self.context_lens = _ti(w.context_lens, self.device)
+        self.query = _t16(w.query, dt, self.device)
+        self.new_seq = _ti(w.new_seq, self.device)
+        self.new_pos = _ti(w.new_pos, self.device)
+        self.new_key = _t16(w.new_key, dt, self.device)
+        self.new_value = _t16(w.new_value, dt, self.device)
+        self.cow_pairs = _ti(w.cow_pairs, self.device) if w.cow_pairs.shape[0] else None
+        self.slots = torch.empty(w.S, dtype=torch.int32, device=self.device)
+        self.out = torch.empty((w.S, w.H, w.D), dtype=self.torch_dtype, device=self.device)
+        self.error_word = torch.zeros(1, dtype=torch.int32, device=self.device)
+        self.workspace = B.alloc_workspace(w.S, w.H, w.Hkv, w.D, self.max_context_len,
+                                           self.partition_size, device=self.device)
+        if build_pools:
+            self.write_history()
+
+    def write_history(self, chunk: int = 1 << 18) -> None:
+        """Cache the workload's history tokens through the library's own
+        slot mapping and reshape_and_cache (the prefill writes)."""
+        w = self.w
+        n = w.hist_seq.shape[0]
+        for lo in range(0, n, chunk):
+            hi = min(n, lo + chunk)
+            seq = _ti(w.hist_seq[lo:hi], self.device)
+            pos = _ti(w.hist_pos[lo:hi], self.device)
+            k = _t16(w.hist_key[lo:hi], w.dtype, self.device)
+            v = _t16(w.hist_value[lo:hi], w.dtype, self.device)
+            slots = torch.empty(hi - lo, dtype=torch.int32, device=self.device)
+            B.pa_slot_mapping(slots, self.block_tables, seq, pos, w.bs, w.num_blocks,
+                              error_word=self.error_word)
+            B.pa_reshape_and_cache(k, v, self.key_cache, self.value_cache, slots,
+                                   error_word=self.error_word)
+
+    # individual steps ---------------------------------------------------------
+    def slot_mapping(self, stream=None) -> None:
+        B.pa_slot_mapping(self.slots, self.block_tables, self.new_seq, self.new_pos,
+                          self.w.bs, self.w.num_blocks, error_word=self.error_word,
+                          stream=stream)
+
+    def reshape_and_cache(self, stream=None) -> None:
+        B.pa_reshape_and_cache(self.new_key, self.new_value, self.key_cache,
+                               self.value_cache, self.slots, error_word=self.error_word,
+                               stream=stream)
+
+    def copy_blocks(self, stream=None) -> None:
+        if self.cow_pairs is not None:
+            B.pa_copy_blocks(self.key_cache, self.value_cache, self.cow_pairs,
+                             error_word=self.error_word, stream=stream)
+
+    def attention(self, stream=None, partition_size: Optional[int] = None) -> None:
+        P = self.partition_size if partition_size is None else partition_size
+        ws = self.workspace
+        if P != self.partition_size:
+            ws = B.alloc_workspace(self.w.S, self.w.H, self.w.Hkv, self.w.D,
+                                   self.max_context_len, P, device=self.device)
+        B.pa_decode_attention(self.out, self.query, self.key_cache, self.value_cache,
+                              self.step_block_tables, self.context_lens,
+                              self.max_context_len, self.w.scale, P, ws,
+                              error_word=self.error_word, stream=stream)
+
+    def run(self, stream=None) -> torch.Tensor:
+        """One whole decode step; returns the attention output tensor."""
+        self.slot_mapping(stream)
+        self.reshape_and_cache(stream)
+        self.copy_blocks(stream)
+        self.attention(stream)
+        return self.out
+
+    def launches_per_step(self) -> int:
+        return 4 if self.cow_pairs is not None else 3
+
+
+def to_bits(t: torch.Tensor) -> np.ndarray:
+    """Device 16-bit tensor -> host uint16 bit patterns."""
+    return t.detach().contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def to_float(t: torch.Tensor) -> np.ndarray:
+    return t.detach().float().cpu().numpy().astype(np.float64)
+
+
+class HostStepIO:
+    """A decode step driven from host memory: every call copies the step's
+    inputs (query, new K/V, their sequence ids and positions, block tables,
+    context lengths, copy-on-write pairs) from pinned host buffers to the
+    device, runs the step, and copies the attention output back to a pinned
+    host buffer.  The K/V pools stay resident on the device."""
+
+    def __init__(self, st: DecodeStep):
+        self.st = st
+        names = ["query", "new_key", "new_value", "new_seq", "new_pos", "block_tables",
+                 "step_block_tables", "context_lens"]
+        if st.cow_pairs is not None:
+            names.append("cow_pairs")
+        self.pairs = []
+        for n in names:
+            dev = getattr(st, n)
+            host = torch.empty(dev.shape, dtype=dev.dtype, pin_memory=True)
+            host.copy_(dev)
+            self.pairs.append((host, dev))
+        self.host_out = torch.empty(st.out.shape, dtype=st.out.dtype, pin_memory=True)
+        self.h2d_bytes = sum(h.numel() * h.element_size() for h, _ in self.pairs)
+        self.d2h_bytes = self.host_out.numel() * self.host_out.element_size()
+
+    def step(self) -> torch.Tensor:
+        for host, dev in self.pairs:
+            dev.copy_(host, non_blocking=True)
+        out = self.st.run()
+        self.host_out.copy_(out, non_blocking=True)
+        return self.host_out

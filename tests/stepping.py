@@ -1,0 +1,62 @@
+"""Test helpers: the same decode step on the oracle (CPU) and on the GPU.
+
+The oracle side builds its pools with its own slot mapping and
+reshape_and_cache, applies the step's writes and copy-on-write copies, and
+attends; the GPU side does the same through the C ABI.  Both start from the
+same seeded workload arrays; nothing flows from the GPU into the oracle.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+import oracle
+from paged_kv_cache_96_gb300.workloads import Workload
+
+# Attention tolerance of the contract: |gpu - oracle| <= ATOL + RTOL * |oracle|.
+ATOL = 1e-2
+RTOL = 1e-2
+
+
+def odt(w: Workload) -> int:
+    return oracle.F16 if w.dtype == "f16" else oracle.BF16
+
+
+class OracleStep:
+    def __init__(self, w: Workload):
+        self.w = w
+        kc, vc = w.empty_pools()
+        self.hist_slots = oracle.slot_mapping(w.block_tables, w.hist_seq, w.hist_pos,
+                                              w.bs)
+        oracle.reshape_and_cache(w.hist_key, w.hist_value, kc, vc, self.hist_slots)
+        self.new_slots = oracle.slot_mapping(w.block_tables, w.new_seq, w.new_pos, w.bs)
+        oracle.reshape_and_cache(w.new_key, w.new_value, kc, vc, self.new_slots)
+        if w.cow_pairs.shape[0]:
+            oracle.copy_blocks(kc, vc, w.cow_pairs)
+        self.key_cache, self.value_cache = kc, vc
+
+    def attention(self, seqs=None):
+        w = self.w
+        return oracle.paged_attention(w.query, self.key_cache, self.value_cache,
+                                      w.step_block_tables, w.context_lens, w.scale,
+                                      odt(w), seqs=seqs)
+
+    def partitions(self, partition_size, max_parts, seqs=None):
+        w = self.w
+        return oracle.partition_pass(w.query, self.key_cache, self.value_cache,
+                                     w.step_block_tables, w.context_lens, w.scale,
+                                     odt(w), partition_size, max_parts, seqs=seqs)
+
+
+def assert_attention_close(got: np.ndarray, want: np.ndarray, what: str = ""):
+    """Element-wise contract tolerance; returns (max abs err, max rel err)."""
+    assert got.shape == want.shape, (got.shape, want.shape)
+    assert np.isfinite(got).all(), f"{what}: non-finite GPU output"
+    err = np.abs(got - want)
+    bound = ATOL + RTOL * np.abs(want)
+    bad = err > bound
+    if bad.any():
+        idx = tuple(np.argwhere(bad)[0])
+        raise AssertionError(f"{what}: {int(bad.sum())} elements out of tolerance, "
+                             f"first {idx}: gpu {got[idx]} oracle {want[idx]}")
+    rel = err / np.maximum(np.abs(want), 1e-6)
+    return float(err.max()), float(np.median(rel))

@@ -1,0 +1,116 @@
+"""The C ABI on the host (no GPU): the library builds, loads and exports
+every entry point the header declares; host-side argument checks return
+their status before anything is launched; workspace sizes follow the
+documented layout."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "paged_attention.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from paged_kv_cache_96_gb300 import build
+    path = build.build()
+    return ctypes.CDLL(path)
+
+
+@pytest.fixture(scope="module")
+def B(lib):
+    from paged_kv_cache_96_gb300 import binding
+    return binding
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pa_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ("pa_slot_mapping", "pa_reshape_and_cache", "pa_copy_blocks",
+              "pa_decode_attention", "pa_decode_workspace_bytes"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(B):
+    L = B.lib()
+    assert L.pa_status_string(0) == b"PA_OK"
+    assert L.pa_status_string(3) == b"PA_ERR_WORKSPACE"
+    assert L.pa_version() >= 100
+
+
+FAKE = ctypes.c_void_p(0x10000)      # never dereferenced: checks fail first
+FAKE_ODD = ctypes.c_void_p(0x10002)  # not 16-byte aligned
+
+
+def _decode(L, **kw):
+    a = dict(out=FAKE, query=FAKE, kc=FAKE, vc=FAKE, bt=FAKE, mb=4, ctx=FAKE, maxctx=64,
+             S=2, H=8, Hkv=2, D=128, bs=16, N=8, scale=0.1, P=0, ws=None, wsb=0, dt=1,
+             err=None, stream=None)
+    a.update(kw)
+    return L.pa_decode_attention(a["out"], a["query"], a["kc"], a["vc"], a["bt"], a["mb"],
+                                 a["ctx"], a["maxctx"], a["S"], a["H"], a["Hkv"], a["D"],
+                                 a["bs"], a["N"], a["scale"], a["P"], a["ws"], a["wsb"],
+                                 a["dt"], a["err"], a["stream"])
+
+
+def test_decode_argument_checks(B):
+    L = B.lib()
+    assert _decode(L, out=None) == B.PA_ERR_INVALID_ARG
+    assert _decode(L, query=FAKE_ODD) == B.PA_ERR_INVALID_ARG
+    assert _decode(L, H=6, Hkv=4) == B.PA_ERR_INVALID_ARG
+    assert _decode(L, dt=7) == B.PA_ERR_INVALID_ARG
+    assert _decode(L, scale=float("nan")) == B.PA_ERR_INVALID_ARG
+    assert _decode(L, D=96) == B.PA_ERR_UNSUPPORTED
+    assert _decode(L, bs=8) == B.PA_ERR_UNSUPPORTED
+    assert _decode(L, H=34, Hkv=2) == B.PA_ERR_UNSUPPORTED      # group 17
+    assert _decode(L, P=24) == B.PA_ERR_UNSUPPORTED
+    # split path needs a workspace
+    assert _decode(L, P=16, maxctx=64) == B.PA_ERR_WORKSPACE
+    need = L.pa_decode_workspace_bytes(2, 8, 2, 128, 64, 16)
+    assert _decode(L, P=16, ws=FAKE, wsb=need - 1) == B.PA_ERR_WORKSPACE
+    assert _decode(L, P=16, ws=ctypes.c_void_p(0x10010), wsb=need) == B.PA_ERR_WORKSPACE
+    # no sequences: nothing to do
+    assert _decode(L, S=0, out=None) == B.PA_OK
+
+
+def test_cache_op_argument_checks(B):
+    L = B.lib()
+    assert L.pa_slot_mapping(None, None, 4, None, None, 0, 1, 16, 8, None, None) == B.PA_OK
+    assert L.pa_slot_mapping(None, FAKE, 4, FAKE, FAKE, 3, 1, 16, 8, None, None) == \
+        B.PA_ERR_INVALID_ARG
+    assert L.pa_reshape_and_cache(FAKE, FAKE, FAKE, FAKE, FAKE, 0, 8, 16, 2, 128, 1,
+                                  None, None) == B.PA_OK
+    assert L.pa_reshape_and_cache(FAKE_ODD, FAKE, FAKE, FAKE, FAKE, 2, 8, 16, 2, 128, 1,
+                                  None, None) == B.PA_ERR_INVALID_ARG
+    assert L.pa_reshape_and_cache(FAKE, FAKE, FAKE, FAKE, FAKE, 2, 8, 16, 1, 4, 1,
+                                  None, None) == B.PA_ERR_UNSUPPORTED  # 8-byte rows
+    assert L.pa_copy_blocks(FAKE, FAKE, FAKE, 0, 8, 16, 2, 128, 1, None, None) == B.PA_OK
+    assert L.pa_copy_blocks(FAKE, FAKE, None, 3, 8, 16, 2, 128, 1, None, None) == \
+        B.PA_ERR_INVALID_ARG
+    assert L.pa_copy_blocks(FAKE, FAKE, FAKE, 3, 8, 16, 2, 128, 5, None, None) == \
+        B.PA_ERR_INVALID_ARG
+
+
+def test_workspace_layout_sizes(B):
+    L = B.lib()
+    a256 = lambda x: (x + 255) // 256 * 256  # noqa: E731
+    # long-context workload: 16 seqs, 32 heads over 8, d 128, 32768 tokens / 512
+    S, H, Hkv, D, P = 16, 32, 8, 128, 64
+    want = 2 * a256(S * H * P * 4) + a256(S * H * P * D * 4) + a256(S * Hkv * 4)
+    assert L.pa_decode_workspace_bytes(S, H, Hkv, D, 32768, 512) == want
+    # everything fits one partition, or single pass: no workspace
+    assert L.pa_decode_workspace_bytes(S, H, Hkv, D, 512, 512) == 0
+    assert L.pa_decode_workspace_bytes(S, H, Hkv, D, 32768, 0) == 0
+    assert L.pa_decode_workspace_bytes(-1, H, Hkv, D, 32768, 512) == 0
