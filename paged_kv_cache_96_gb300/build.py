@@ -32,9 +32,9 @@ def nvcc() -> str:
     raise RuntimeError("nvcc not found: the CUDA toolkit is required to build")
 
 
-def _compile(src: str, verbose_ptxas: bool) -> str:
-    obj = os.path.join(OBJDIR, os.path.basename(src).replace(".cu", ".o"))
-    cmd = [nvcc(), *ARCH, *NVCC_FLAGS, "-c", src, "-o", obj]
+def _compile(src: str, verbose_ptxas: bool, objdir: str = OBJDIR, extra=()) -> str:
+    obj = os.path.join(objdir, os.path.basename(src).replace(".cu", ".o"))
+    cmd = [nvcc(), *ARCH, *NVCC_FLAGS, *extra, "-c", src, "-o", obj]
     if verbose_ptxas:
         cmd += ["-Xptxas", "-v"]
     r = subprocess.run(cmd, capture_output=True, text=True)
@@ -58,21 +58,26 @@ def up_to_date() -> bool:
     return all(os.path.getmtime(d) <= t for d in deps)
 
 
-def build(force: bool = False, verbose_ptxas: bool = False) -> str:
-    if not force and up_to_date():
+def build(force: bool = False, verbose_ptxas: bool = False, extra=(),
+          out: str = None) -> str:
+    """Compile and link; `extra` nvcc flags and `out` library path are for
+    building tuning variants next to the default library."""
+    lib = out or LIB
+    if not force and out is None and not extra and up_to_date():
         return LIB
-    os.makedirs(OBJDIR, exist_ok=True)
-    os.makedirs(LIBDIR, exist_ok=True)
+    objdir = OBJDIR if out is None else os.path.join(os.path.dirname(out), "_obj")
+    os.makedirs(objdir, exist_ok=True)
+    os.makedirs(os.path.dirname(lib), exist_ok=True)
     srcs = sources()
     with cf.ThreadPoolExecutor(max_workers=len(srcs)) as ex:
-        objs = list(ex.map(lambda s: _compile(s, verbose_ptxas), srcs))
-    tmp = LIB + f".tmp{os.getpid()}"
+        objs = list(ex.map(lambda s: _compile(s, verbose_ptxas, objdir, extra), srcs))
+    tmp = lib + f".tmp{os.getpid()}"
     cmd = [nvcc(), *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

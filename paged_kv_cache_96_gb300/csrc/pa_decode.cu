@@ -594,8 +594,14 @@ static bool encode_pool_map(CUtensorMap *map, const void *pool, pa_dtype dtype,
     return r == CUDA_SUCCESS;
 }
 
-constexpr int kWarps = 4;
-constexpr int kStagesPerWarp = 4;
+#ifndef PA_DECODE_WARPS
+#define PA_DECODE_WARPS 4
+#endif
+#ifndef PA_DECODE_STAGES
+#define PA_DECODE_STAGES 4
+#endif
+constexpr int kWarps = PA_DECODE_WARPS;
+constexpr int kStagesPerWarp = PA_DECODE_STAGES;
 
 template <typename T, int D, int NT>
 static pa_status launch_decode(const DecodeParams &prm, const CUtensorMap &mk,
