@@ -122,13 +122,13 @@ PA_API pa_status pa_copy_blocks(void *key_cache, void *value_cache,
  * needs for these sizes (0 when partition_size == 0 or every context fits in
  * one partition).  Layout, with P = ceil(max_context_len / partition_size)
  * and every region starting on a 256-byte boundary, in this order:
- *     float    part_m  [num_seqs][num_heads][P]   partition stabiliser m_j
- *     float    part_l  [num_seqs][num_heads][P]   sum_p exp(score_p - m_j)
- *     float    part_o  [num_seqs][num_heads][P][head_dim]  partition output / l_j
- *     uint32_t arrivals[num_seqs][num_kv_heads]   zero between calls
+ *     float part_m[num_seqs][num_heads][P]            partition stabiliser m_j
+ *     float part_l[num_seqs][num_heads][P]            sum_p exp(score_p - m_j)
+ *     float part_o[num_seqs][num_heads][P][head_dim]  partition output / l_j
  * score_p = scale * q . k_p (natural-log units).  m_j is a stabiliser: the
  * partition's log-sum-exp is m_j + log(l_j).  Partials are written only for
- * sequences that span more than one partition.  Returns 0 for invalid sizes.
+ * sequences that span more than one partition.  num_kv_heads is accepted for
+ * symmetry with pa_decode_attention.  Returns 0 for invalid sizes.
  */
 PA_API size_t pa_decode_workspace_bytes(int num_seqs, int num_heads, int num_kv_heads,
                                  int head_dim, int max_context_len,
@@ -148,17 +148,17 @@ PA_API size_t pa_decode_workspace_bytes(int num_seqs, int num_heads, int num_kv_
  *                  >= every context_lens[s] (larger values are clipped and
  *                  flagged PA_DEVERR_CONTEXT_RANGE).  context 0 gives a zero row.
  *   partition_size: 0 = single pass (one work unit per sequence and KV
- *                  head); otherwise a multiple of 16 tokens >= 32: contexts
- *                  are split into partitions of that many tokens, each
- *                  producing a partial (m, l, o) in the workspace, and the
- *                  partials of a (sequence, KV head) are merged by
- *                  log-sum-exp weights l_j * exp(m_j - max m) inside the same
- *                  launch by the last partition to finish.
- *   workspace    : device, >= pa_decode_workspace_bytes(...) bytes, its
- *                  `arrivals` region zero before the first call (the call
- *                  leaves it zero).  May be NULL when that size is 0.
- *                  Calls sharing one workspace must not overlap in time.
- * Supported: head_dim 64 or 128; block_size a multiple of 16 up to 256;
+ *                  head); otherwise a multiple of 16 tokens: contexts are
+ *                  split into partitions of that many tokens.  The partition
+ *                  pass writes a partial (m, l, o) per partition to the
+ *                  workspace, and a reduce kernel, queued behind it on the
+ *                  same stream by this call, merges them by log-sum-exp
+ *                  weights l_j * exp(m_j - max m).  A sequence that fits one
+ *                  partition is written by the pass directly.
+ *   workspace    : device, 256-byte aligned, >= pa_decode_workspace_bytes(...)
+ *                  bytes; no initial contents needed.  May be NULL when that
+ *                  size is 0.  Calls sharing one workspace must not overlap.
+ * Supported: head_dim 64 or 128; block_size a power of two from 16 to 256;
  * num_heads / num_kv_heads in 1..16; num_blocks * block_size < 2^31.
  */
 PA_API pa_status pa_decode_attention(void *out, const void *query,

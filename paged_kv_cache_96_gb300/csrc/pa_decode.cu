@@ -62,16 +62,17 @@ struct DecodeParams {
     float *part_m;
     float *part_l;
     float *part_o;
-    uint32_t *arrivals;
     int32_t *error_word;
     int num_seqs, num_heads, num_kv_heads, group;
     int max_blocks_per_seq, num_blocks, block_size, max_context_len;
+    int block_shift;  // log2(block_size)
     int part_tokens;  // tokens per work unit (a multiple of 16)
     int max_parts;    // partitions per sequence the workspace holds
     float scale_log2; // scale * log2(e)
 };
 
-// Shared-memory layout (offsets from a 1024-byte aligned base).
+// Shared-memory layout (offsets from a 1024-byte aligned base): NW warps,
+// each with a private ring of NST stages.
 template <int D, int NT, int NW, int NST> struct Layout {
     static constexpr int kHalfBytes = kTileTokens * 128;      // 16 rows x 64 elements
     static constexpr int kTileBytes = (D / 64) * kHalfBytes;  // one K (or V) tile
@@ -84,12 +85,35 @@ template <int D, int NT, int NW, int NST> struct Layout {
     static constexpr int kMergeL = kMergeM + NW * kHeads * 4;
     static constexpr int kBars = kMergeL + NW * kHeads * 4;
     static constexpr int kFlags = kBars + NW * NST * 8;
-    static constexpr int kCtrl = kFlags + NW * NST * 4;
-    static constexpr int kSeq = kCtrl + 64;  // int ctx[S], int prefix[S + 1]
+    static constexpr int kSeq = kFlags + NW * NST * 4;  // int ctx[S], int prefix[S + 1]
     static size_t bytes(int num_seqs) { return 1024 + kSeq + 8 * (size_t)(num_seqs + 1); }
     static_assert(kBars % 8 == 0, "mbarriers need 8-byte alignment");
     static_assert(kStageBytes % 1024 == 0, "stages must keep 1024-byte alignment");
 };
+
+// Program-dependent launch: let the grid queued behind this one start
+// launching, and (in that grid) wait for this one's memory to be visible.
+__device__ __forceinline__ void pdl_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait_primary()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Clamped context length (same rule in both kernels).
+__device__ __forceinline__ int clamp_context(const DecodeParams &p, int s, bool flag)
+{
+    const int limit = min(p.max_context_len, p.max_blocks_per_seq * p.block_size);
+    int c = p.context_lens[s];
+    if (c < 0 || c > limit) {
+        if (flag)
+            flag_error(p.error_word, PA_DEVERR_CONTEXT_RANGE);
+        c = c < 0 ? 0 : limit;
+    }
+    return c;
+}
 
 template <typename T, int D, int NT, int NW, int NST>
 __global__ void __launch_bounds__(NW * 32, 1)
@@ -101,6 +125,7 @@ __global__ void __launch_bounds__(NW * 32, 1)
     using Op = MmaOp<T>;
     constexpr int KT = D / 16;  // k-steps of the score product, m-tiles of the output
     constexpr int kHeads = L::kHeads;
+    constexpr int kThreads = NW * 32;
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_addr(smem_raw);
@@ -120,26 +145,21 @@ __global__ void __launch_bounds__(NW * 32, 1)
 
     int *ctx_s = reinterpret_cast<int *>(smem + L::kSeq);
     int *pref = ctx_s + S;
-    int *ctrl = reinterpret_cast<int *>(smem + L::kCtrl);
-    int *flags = reinterpret_cast<int *>(smem + L::kFlags);
+    volatile int *flags = reinterpret_cast<volatile int *>(smem + L::kFlags);
     float *merge_o = reinterpret_cast<float *>(smem + L::kMergeO);
     float *merge_m = reinterpret_cast<float *>(smem + L::kMergeM);
     float *merge_l = reinterpret_cast<float *>(smem + L::kMergeL);
+    auto bar_of = [&](int stage) { return sbase + L::kBars + (warp * NST + stage) * 8; };
+    auto stage_of = [&](int stage) {
+        return sbase + L::kStages + (warp * NST + stage) * L::kStageBytes;
+    };
 
     // ---- context lengths and partition prefix sums -----------------------
-    const int ctx_limit = min(p.max_context_len, p.max_blocks_per_seq * p.block_size);
-    for (int s = tid; s < S; s += NW * 32) {
-        int c = p.context_lens[s];
-        if (c < 0 || c > ctx_limit) {
-            if (blockIdx.x == 0)
-                flag_error(p.error_word, PA_DEVERR_CONTEXT_RANGE);
-            c = c < 0 ? 0 : ctx_limit;
-        }
-        ctx_s[s] = c;
-    }
+    for (int s = tid; s < S; s += kThreads)
+        ctx_s[s] = clamp_context(p, s, blockIdx.x == 0);
     if (lane == 0) {
         for (int k = 0; k < NST; ++k)
-            mbar_init(sbase + L::kBars + (warp * NST + k) * 8, 1);
+            mbar_init(bar_of(k), 1);
         fence_barrier_init();
     }
     if (tid == 0) {
@@ -175,11 +195,10 @@ __global__ void __launch_bounds__(NW * 32, 1)
             continue;
         uint4 *row = reinterpret_cast<uint4 *>(static_cast<T *>(p.out) +
                                                (size_t)s * p.num_heads * D);
-        for (int i = tid; i < p.num_heads * D / 8; i += NW * 32)
+        for (int i = tid; i < p.num_heads * D / 8; i += kThreads)
             row[i] = make_uint4(0, 0, 0, 0);
     }
 
-    // ---- unit decoding --------------------------------------------------------
     // unit u -> partition q = u / Hkv, kv head u % Hkv; sequence s is the one
     // with pref[s] <= q < pref[s + 1].
     auto decode_unit = [&](int u, int &s, int &kh, int &j, int &tok0, int &ntiles) {
@@ -200,12 +219,12 @@ __global__ void __launch_bounds__(NW * 32, 1)
         ntiles = (tok_end - tok0 + kTileTokens - 1) / kTileTokens;
     };
 
-    // ---- producer: this warp's next tile to fetch -----------------------------
+    // ---- this warp's fetch cursor: its next tile, possibly in a later unit ----
     int pu = blockIdx.x, ps = 0, pkh = 0, pj = 0, ptok0 = 0, pnt = 0, ptile = warp;
     bool pdone = pu >= total_units;
     if (!pdone)
         decode_unit(pu, ps, pkh, pj, ptok0, pnt);
-    auto producer_skip_empty = [&]() {
+    auto skip_empty = [&]() {
         while (!pdone && ptile >= pnt) {
             pu += gridDim.x;
             if (pu >= total_units) {
@@ -216,64 +235,79 @@ __global__ void __launch_bounds__(NW * 32, 1)
             ptile = warp;
         }
     };
-    producer_skip_empty();
+    skip_empty();
+    // Lane 0 loads the table entry of the tile at the cursor one tile ahead
+    // of issuing its fetch, so the load's latency overlaps a tile of compute.
+    int pphys = 0, prow = 0;
+    auto prefetch_entry = [&]() {
+        if (!pdone && lane == 0) {
+            const int tok = ptok0 + ptile * kTileTokens;
+            prow = tok & (p.block_size - 1);
+            pphys = __ldg(p.block_tables + (size_t)ps * p.max_blocks_per_seq +
+                          (tok >> p.block_shift));
+        }
+    };
+    prefetch_entry();
 
     uint32_t issued = 0, consumed = 0;
     uint32_t inflight = 0;  // stages with a fetch not yet waited for
     bool aborted = false;
-
     auto produce = [&]() {
         if (pdone || aborted)
             return;
         const int stage = issued % NST;
-        const uint32_t bar = sbase + L::kBars + (warp * NST + stage) * 8;
-        const uint32_t dst = sbase + L::kStages + (warp * NST + stage) * L::kStageBytes;
         if (lane == 0) {
-            const int tok = ptok0 + ptile * kTileTokens;
-            const int blk = tok / p.block_size;
-            const int row = tok - blk * p.block_size;
-            const int32_t phys =
-                p.block_tables[(size_t)ps * p.max_blocks_per_seq + blk];
-            const bool ok = phys >= 0 && phys < p.num_blocks;
+            const bool ok = pphys >= 0 && pphys < p.num_blocks;
             flags[warp * NST + stage] = ok;
             if (ok) {
-                mbar_arrive_expect_tx(bar, L::kStageBytes);
+                const uint32_t dst = stage_of(stage);
+                mbar_arrive_expect_tx(bar_of(stage), L::kStageBytes);
+#if PA_DECODE_PACKED5D
+                tma_load_5d(dst, &tmap_k, bar_of(stage), 0, 0, pkh, prow, pphys);
+                tma_load_5d(dst + L::kTileBytes, &tmap_v, bar_of(stage), 0, 0, pkh, prow, pphys);
+#else
 #pragma unroll
                 for (int hf = 0; hf < D / 64; ++hf) {
-                    tma_load_4d(dst + hf * L::kHalfBytes, &tmap_k, bar, hf * 64, pkh, row,
-                                phys);
-                    tma_load_4d(dst + L::kTileBytes + hf * L::kHalfBytes, &tmap_v, bar,
-                                hf * 64, pkh, row, phys);
+                    tma_load_4d(dst + hf * L::kHalfBytes, &tmap_k, bar_of(stage), hf * 64, pkh,
+                                prow, pphys);
+                    tma_load_4d(dst + L::kTileBytes + hf * L::kHalfBytes, &tmap_v,
+                                bar_of(stage), hf * 64, pkh, prow, pphys);
                 }
+#endif
             } else {
                 flag_error(p.error_word, PA_DEVERR_BLOCK_RANGE);
-                mbar_arrive(bar);
+                mbar_arrive(bar_of(stage));
             }
         }
         inflight |= 1u << stage;
         ++issued;
         ptile += NW;
-        producer_skip_empty();
+        skip_empty();
+        prefetch_entry();
     };
     for (int k = 0; k < NST; ++k)
         produce();
 
-    // Per-lane ldmatrix row/chunk selectors (128-byte swizzle: the 16-byte
-    // chunk c of row r sits at chunk c ^ (r & 7)).
+    // Per-lane ldmatrix row/chunk selectors.
     const int li = lane & 7, lj = lane >> 3;
-    const int k_row = li + ((lj & 1) << 3), k_cj = lj >> 1;   // K: A operand
-    const int v_row = li + ((lj >> 1) << 3), v_cj = lj & 1;   // V^T: A operand (trans)
+    const int k_row = li + ((lj & 1) << 3), k_cj = lj >> 1;  // K: A operand
+    const int v_row = li + ((lj >> 1) << 3), v_cj = lj & 1;  // V^T: A operand (trans)
+    // Shared-memory address of 16-byte chunk `chunk` of (token, d-half) in a
+    // tile at `base`: rows of 128 bytes; chunk c of row r sits at chunk
+    // c ^ (r & 7) (the TMA's 128-byte swizzle).
+    auto tile_addr = [&](uint32_t base, int token, int half, int chunk) -> uint32_t {
+#if PA_DECODE_PACKED5D
+        const int r = token * (D / 64) + half;
+#else
+        const int r = half * kTileTokens + token;
+#endif
+        return base + r * 128 + ((chunk ^ (r & 7)) << 4);
+    };
 
-    // ---- units --------------------------------------------------------------------
-    for (int u = blockIdx.x; u < total_units; u += gridDim.x) {
-        int s, kh, j, tok0, ntiles;
-        decode_unit(u, s, kh, j, tok0, ntiles);
-        const int tok_end = min(ctx_s[s], tok0 + P);
-        const int nparts = (ctx_s[s] + P - 1) / P;
-
-        // Query fragments (B operand of the score product): head 8nt+g of
-        // the group, elements d = 16kk + 2t4 (+1) and +8 (+9).
-        uint32_t qf[NT][KT][2];
+    // Query fragments (B operand of the score product): head 8nt+g of the
+    // group, elements d = 16kk + 2t4 (+1) and +8 (+9).
+    uint32_t qf[NT][KT][2];
+    auto load_query = [&](int s, int kh) {
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
             const int hg = nt * 8 + g;
@@ -286,6 +320,19 @@ __global__ void __launch_bounds__(NW * 32, 1)
                 qf[nt][kk][1] = hg < G ? __ldg(qrow + kk * 8 + 4 + t4) : 0u;
             }
         }
+    };
+    if (blockIdx.x < total_units) {
+        int s, kh, j, tok0, ntiles;
+        decode_unit(blockIdx.x, s, kh, j, tok0, ntiles);
+        load_query(s, kh);
+    }
+
+    // ---- units --------------------------------------------------------------------
+    for (int u = blockIdx.x; u < total_units; u += gridDim.x) {
+        int s, kh, j, tok0, ntiles;
+        decode_unit(u, s, kh, j, tok0, ntiles);
+        const int tok_end = min(ctx_s[s], tok0 + P);
+        const int nparts = (ctx_s[s] + P - 1) / P;
 
         float o[KT][NT][4];
         float mrun[NT][2], lrun[NT][2];
@@ -301,10 +348,9 @@ __global__ void __launch_bounds__(NW * 32, 1)
         for (int tile = warp; tile < ntiles; tile += NW) {
             const int stage = consumed % NST;
             const uint32_t parity = (consumed / NST) & 1u;
-            const uint32_t bar = sbase + L::kBars + (warp * NST + stage) * 8;
             bool ready = false;
             if (!aborted) {
-                ready = __all_sync(kFull, mbar_wait_bounded(bar, parity, kWaitLimitNs));
+                ready = __all_sync(kFull, mbar_wait_bounded(bar_of(stage), parity, kWaitLimitNs));
                 if (ready) {
                     inflight &= ~(1u << stage);
                 } else {
@@ -313,28 +359,56 @@ __global__ void __launch_bounds__(NW * 32, 1)
                         flag_error(p.error_word, PA_DEVERR_TIMEOUT);
                 }
             }
-            const bool valid = ready && flags[warp * NST + stage] != 0;
-            if (valid) {
-                const uint32_t kbase =
-                    sbase + L::kStages + (warp * NST + stage) * L::kStageBytes;
+            if (ready && flags[warp * NST + stage] != 0) {
+                const uint32_t kbase = stage_of(stage);
                 const uint32_t vbase = kbase + L::kTileBytes;
                 const int nv = tok_end - (tok0 + tile * kTileTokens);  // valid rows
                 const bool partial = nv < kTileTokens;
 
-                // scores S[token][head] = K . Q^T
-                float sc[NT][4];
+                // scores S[token][head] = K . Q^T, two accumulator chains
+                float sc[NT][4], sc2[NT][4];
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt)
+                for (int nt = 0; nt < NT; ++nt) {
                     sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+                    sc2[nt][0] = sc2[nt][1] = sc2[nt][2] = sc2[nt][3] = 0.f;
+                }
 #pragma unroll
                 for (int kk = 0; kk < KT; ++kk) {
                     uint32_t a[4];
-                    ldmatrix_x4(kbase + (kk >> 2) * L::kHalfBytes + k_row * 128 +
-                                    ((((kk & 3) * 2 + k_cj) ^ li) << 4),
-                                a);
+                    ldmatrix_x4(tile_addr(kbase, k_row, kk >> 2, (kk & 3) * 2 + k_cj), a);
 #pragma unroll
-                    for (int nt = 0; nt < NT; ++nt)
-                        Op::run(sc[nt], a, qf[nt][kk][0], qf[nt][kk][1]);
+                    for (int nt = 0; nt < NT; ++nt) {
+                        if (kk & 1)
+                            Op::run(sc2[nt], a, qf[nt][kk][0], qf[nt][kk][1]);
+                        else
+                            Op::run(sc[nt], a, qf[nt][kk][0], qf[nt][kk][1]);
+                    }
+                }
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        sc[nt][e] += sc2[nt][e];
+
+                // V^T fragments (their latency overlaps the softmax); rows past
+                // the context are zeroed so NaN padding never meets a zero weight
+                uint32_t va[KT][4];
+#pragma unroll
+                for (int mt = 0; mt < KT; ++mt)
+                    ldmatrix_x4_trans(tile_addr(vbase, v_row, mt >> 2, (mt & 3) * 2 + v_cj),
+                                      va[mt]);
+                if (partial) {
+                    const uint32_t m01 = (2 * t4 < nv ? 0x0000ffffu : 0u) |
+                                         (2 * t4 + 1 < nv ? 0xffff0000u : 0u);
+                    const uint32_t m89 = (2 * t4 + 8 < nv ? 0x0000ffffu : 0u) |
+                                         (2 * t4 + 9 < nv ? 0xffff0000u : 0u);
+#pragma unroll
+                    for (int mt = 0; mt < KT; ++mt) {
+                        va[mt][0] &= m01;
+                        va[mt][1] &= m01;
+                        va[mt][2] &= m89;
+                        va[mt][3] &= m89;
+                    }
                 }
 
                 // online softmax; P^T fragments for the value product
@@ -382,33 +456,25 @@ __global__ void __launch_bounds__(NW * 32, 1)
                 }
 
                 // O^T[d][head] += V^T . P^T
-                uint32_t m01 = 0xffffffffu, m89 = 0xffffffffu;
-                if (partial) {
-                    m01 = (2 * t4 < nv ? 0x0000ffffu : 0u) | (2 * t4 + 1 < nv ? 0xffff0000u : 0u);
-                    m89 = (2 * t4 + 8 < nv ? 0x0000ffffu : 0u) |
-                          (2 * t4 + 9 < nv ? 0xffff0000u : 0u);
-                }
 #pragma unroll
-                for (int mt = 0; mt < KT; ++mt) {
-                    uint32_t a[4];
-                    ldmatrix_x4_trans(vbase + (mt >> 2) * L::kHalfBytes + v_row * 128 +
-                                          ((((mt & 3) * 2 + v_cj) ^ li) << 4),
-                                      a);
-                    a[0] &= m01;
-                    a[1] &= m01;
-                    a[2] &= m89;
-                    a[3] &= m89;
+                for (int mt = 0; mt < KT; ++mt)
 #pragma unroll
                     for (int nt = 0; nt < NT; ++nt)
-                        Op::run(o[mt][nt], a, pb[nt][0], pb[nt][1]);
-                }
+                        Op::run(o[mt][nt], va[mt], pb[nt][0], pb[nt][1]);
             }
             __syncwarp();
             ++consumed;
-            produce();
+            produce();  // refill the stage just consumed
         }
 
-        // ---- end of unit: merge the warps' (m, l, O) -------------------------------
+        // Next unit's query: its loads land while this unit's merge runs.
+        if (u + (int)gridDim.x < total_units) {
+            int sn, khn, jn, tn, ntn;
+            decode_unit(u + gridDim.x, sn, khn, jn, tn, ntn);
+            load_query(sn, khn);
+        }
+
+        // ---- end of unit: merge the warps' (m, l, O) ------------------------------
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
@@ -440,7 +506,7 @@ __global__ void __launch_bounds__(NW * 32, 1)
         __syncthreads();
 
         const int items = G * (D / 8);
-        for (int it = tid; it < items; it += NW * 32) {
+        for (int it = tid; it < items; it += kThreads) {
             const int jh = it / (D / 8);
             const int d0 = (it - jh * (D / 8)) * 8;
             float mmax = -INFINITY;
@@ -471,6 +537,7 @@ __global__ void __launch_bounds__(NW * 32, 1)
                                            ((size_t)s * p.num_heads + h) * D + d0) =
                     *reinterpret_cast<const uint4 *>(vals);
             } else {
+                // partial of partition j, merged by the reduce kernel
                 const size_t idx = ((size_t)s * p.num_heads + h) * p.max_parts + j;
                 float4 *dst = reinterpret_cast<float4 *>(p.part_o + idx * D + d0);
                 dst[0] = make_float4(acc[0] * inv, acc[1] * inv, acc[2] * inv, acc[3] * inv);
@@ -481,55 +548,9 @@ __global__ void __launch_bounds__(NW * 32, 1)
                 }
             }
         }
-
-        if (nparts > 1) {
-            // last partition of (s, kh) to finish merges all of them
-            __syncthreads();
-            if (tid == 0) {
-                __threadfence();
-                const uint32_t prev = atomicAdd(p.arrivals + (size_t)s * Hkv + kh, 1u);
-                ctrl[0] = prev == (uint32_t)(nparts - 1);
-            }
-            __syncthreads();
-            if (ctrl[0]) {
-                __threadfence();
-                for (int it = tid; it < items; it += NW * 32) {
-                    const int jh = it / (D / 8);
-                    const int d0 = (it - jh * (D / 8)) * 8;
-                    const size_t h = (size_t)kh * G + jh;
-                    const size_t base = ((size_t)s * p.num_heads + h) * p.max_parts;
-                    float mmax = -INFINITY;
-                    for (int q = 0; q < nparts; ++q)
-                        mmax = fmaxf(mmax, __ldcg(p.part_m + base + q));
-                    float lsum = 0.f;
-                    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll 4
-                    for (int q = 0; q < nparts; ++q) {
-                        const float wgt =
-                            __ldcg(p.part_l + base + q) *
-                            exp2f((__ldcg(p.part_m + base + q) - mmax) * kLog2e);
-                        lsum += wgt;
-                        const float4 *src =
-                            reinterpret_cast<const float4 *>(p.part_o + (base + q) * D + d0);
-                        const float4 x0 = __ldcg(src), x1 = __ldcg(src + 1);
-                        acc[0] += wgt * x0.x; acc[1] += wgt * x0.y; acc[2] += wgt * x0.z; acc[3] += wgt * x0.w;
-                        acc[4] += wgt * x1.x; acc[5] += wgt * x1.y; acc[6] += wgt * x1.z; acc[7] += wgt * x1.w;
-                    }
-                    const float inv = 1.f / lsum;
-                    T vals[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e)
-                        vals[e] = Op::from_float(acc[e] * inv);
-                    *reinterpret_cast<uint4 *>(static_cast<T *>(p.out) +
-                                               ((size_t)s * p.num_heads + h) * D + d0) =
-                        *reinterpret_cast<const uint4 *>(vals);
-                }
-                if (tid == 0)
-                    p.arrivals[(size_t)s * Hkv + kh] = 0u;
-            }
-        }
-        __syncthreads();  // merge scratch and ctrl are reused by the next unit
+        __syncthreads();  // merge scratch is reused by the next unit
     }
+    pdl_launch_dependents();
 
     // ---- drain: wait (bounded) for any fetch still landing in this warp's ring ----
     if (inflight != 0) {
@@ -539,9 +560,118 @@ __global__ void __launch_bounds__(NW * 32, 1)
             // the most recent fetch into stage k was issue number
             // issued - 1 - ((issued - 1 - k) % NST)
             const uint32_t last = issued - 1 - ((issued - 1 - k) % NST);
-            const uint32_t bar = sbase + L::kBars + (warp * NST + k) * 8;
-            mbar_wait_bounded(bar, (last / NST) & 1u, kWaitLimitNs);
+            mbar_wait_bounded(bar_of(k), (last / NST) & 1u, kWaitLimitNs);
         }
+    }
+}
+
+// ---- split-context reduce ----------------------------------------------------------
+//
+// One CTA per (sequence, KV head).  For the G query heads of the group it
+// merges the nparts partials (m_q, l_q, o_q) of a sequence that spans more
+// than one partition: M = max_q m_q, w_q = l_q exp(m_q - M),
+// out = sum_q w_q o_q / sum_q w_q.  Sequences with one partition were written
+// by the partition pass itself.  (1) warp w finds M and sum_q w_q for heads
+// jh = w, w + 4, ...; (2) thread (item, qg) sums w_q o_q over q = qg, qg + QG,
+// ...; (3) the QG group sums are added in shared memory.
+constexpr int kReduceThreads = 128;
+
+template <typename T, int D>
+__global__ void __launch_bounds__(kReduceThreads)
+    paged_reduce_kernel(const __grid_constant__ DecodeParams p)
+{
+    using Op = MmaOp<T>;
+    __shared__ float head_m[16], head_l[16];
+    __shared__ __align__(16) float red[kReduceThreads * 8];
+    pdl_wait_primary();  // the partition pass's partials are visible past here
+
+    const int Hkv = p.num_kv_heads;
+    const int G = p.group;
+    const int s = blockIdx.x / Hkv;
+    const int kh = blockIdx.x - s * Hkv;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int ctx = clamp_context(p, s, false);
+    const int nparts = (ctx + p.part_tokens - 1) / p.part_tokens;
+    if (nparts <= 1)
+        return;
+
+    const size_t hbase = ((size_t)s * p.num_heads + (size_t)kh * G) * p.max_parts;
+    for (int jh = warp; jh < G; jh += kReduceThreads / 32) {
+        const float *pm = p.part_m + hbase + (size_t)jh * p.max_parts;
+        const float *pl = p.part_l + hbase + (size_t)jh * p.max_parts;
+        float mx = -INFINITY;
+        for (int q = lane; q < nparts; q += 32)
+            mx = fmaxf(mx, pm[q]);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1)
+            mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, off));
+        float ls = 0.f;
+        for (int q = lane; q < nparts; q += 32)
+            ls += pl[q] * exp2f((pm[q] - mx) * kLog2e);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1)
+            ls += __shfl_xor_sync(kFull, ls, off);
+        if (lane == 0) {
+            head_m[jh] = mx;
+            head_l[jh] = ls;
+        }
+    }
+    __syncthreads();
+
+    const int items = G * (D / 8);
+    const int qgroups = max(1, kReduceThreads / items);
+    for (int w_it = tid; w_it < items * qgroups; w_it += kReduceThreads) {
+        const int item = w_it % items;
+        const int qg = w_it / items;
+        const int jh = item / (D / 8);
+        const int d0 = (item - jh * (D / 8)) * 8;
+        const size_t base = hbase + (size_t)jh * p.max_parts;
+        const float mx = head_m[jh];
+        const float inv_l = 1.f / head_l[jh];
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+        for (int q = qg; q < nparts; q += qgroups) {
+            const float wgt = p.part_l[base + q] * exp2f((p.part_m[base + q] - mx) * kLog2e) *
+                              inv_l;
+            const float4 *src = reinterpret_cast<const float4 *>(p.part_o + (base + q) * D + d0);
+            const float4 x0 = src[0], x1 = src[1];
+            acc[0] += wgt * x0.x; acc[1] += wgt * x0.y; acc[2] += wgt * x0.z; acc[3] += wgt * x0.w;
+            acc[4] += wgt * x1.x; acc[5] += wgt * x1.y; acc[6] += wgt * x1.z; acc[7] += wgt * x1.w;
+        }
+        if (qgroups == 1) {
+            T vals[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                vals[e] = Op::from_float(acc[e]);
+            *reinterpret_cast<uint4 *>(static_cast<T *>(p.out) +
+                                       ((size_t)s * p.num_heads + (size_t)kh * G + jh) * D +
+                                       d0) = *reinterpret_cast<const uint4 *>(vals);
+        } else {
+            float4 *dst = reinterpret_cast<float4 *>(red + (size_t)(qg * items + item) * 8);
+            dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+            dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+        }
+    }
+    if (qgroups == 1)
+        return;
+    __syncthreads();
+    for (int it = tid; it < items; it += kReduceThreads) {
+        const int jh = it / (D / 8);
+        const int d0 = (it - jh * (D / 8)) * 8;
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        for (int g2 = 0; g2 < qgroups; ++g2) {
+            const float4 *src = reinterpret_cast<const float4 *>(red + (size_t)(g2 * items + it) * 8);
+            const float4 x0 = src[0], x1 = src[1];
+            acc[0] += x0.x; acc[1] += x0.y; acc[2] += x0.z; acc[3] += x0.w;
+            acc[4] += x1.x; acc[5] += x1.y; acc[6] += x1.z; acc[7] += x1.w;
+        }
+        T vals[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+            vals[e] = Op::from_float(acc[e]);
+        *reinterpret_cast<uint4 *>(static_cast<T *>(p.out) +
+                                   ((size_t)s * p.num_heads + (size_t)kh * G + jh) * D + d0) =
+            *reinterpret_cast<const uint4 *>(vals);
     }
 }
 
@@ -568,8 +698,16 @@ static EncodeTiledFn get_encode_fn()
     return fn;
 }
 
-// Tensor map over a pool [num_blocks][block_size][num_kv_heads][head_dim]
-// with a box of 64 elements x 1 head x 16 tokens x 1 block, 128-byte swizzle.
+// Tensor map over a pool [num_blocks][block_size][num_kv_heads][head_dim].
+// Default (4-D, dims d, head, token, block): a box of 64 elements x 1 head x
+// 16 tokens x 1 block lands as 16 rows of 128 bytes, 128-byte swizzle; a
+// 16-token K (or V) tile of one KV head takes D / 64 boxes.
+// PA_DECODE_PACKED5D (5-D, the same packed layout with d split into
+// [D/64][64]): one box {64, D/64, 1, 16, 1} brings the whole tile, rows
+// ordered (token, half).
+#ifndef PA_DECODE_PACKED5D
+#define PA_DECODE_PACKED5D 0
+#endif
 static bool encode_pool_map(CUtensorMap *map, const void *pool, pa_dtype dtype,
                             int num_blocks, int block_size, int num_kv_heads,
                             int head_dim)
@@ -577,17 +715,29 @@ static bool encode_pool_map(CUtensorMap *map, const void *pool, pa_dtype dtype,
     EncodeTiledFn fn = get_encode_fn();
     if (!fn)
         return false;
+    const cuuint64_t e = 2;
+    const CUtensorMapDataType ty = dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                    : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+#if PA_DECODE_PACKED5D
+    const cuuint64_t dims[5] = {64, (cuuint64_t)head_dim / 64, (cuuint64_t)num_kv_heads,
+                                (cuuint64_t)block_size, (cuuint64_t)num_blocks};
+    const cuuint64_t strides[4] = {64 * e, (cuuint64_t)head_dim * e,
+                                   (cuuint64_t)num_kv_heads * head_dim * e,
+                                   (cuuint64_t)block_size * num_kv_heads * head_dim * e};
+    const cuuint32_t box[5] = {64, (cuuint32_t)head_dim / 64, 1, (cuuint32_t)kTileTokens, 1};
+    const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    const cuuint32_t rank = 5;
+#else
     const cuuint64_t dims[4] = {(cuuint64_t)head_dim, (cuuint64_t)num_kv_heads,
                                 (cuuint64_t)block_size, (cuuint64_t)num_blocks};
-    const cuuint64_t strides[3] = {(cuuint64_t)head_dim * 2,
-                                   (cuuint64_t)num_kv_heads * head_dim * 2,
-                                   (cuuint64_t)block_size * num_kv_heads * head_dim * 2};
+    const cuuint64_t strides[3] = {(cuuint64_t)head_dim * e,
+                                   (cuuint64_t)num_kv_heads * head_dim * e,
+                                   (cuuint64_t)block_size * num_kv_heads * head_dim * e};
     const cuuint32_t box[4] = {64, 1, (cuuint32_t)kTileTokens, 1};
     const cuuint32_t estr[4] = {1, 1, 1, 1};
-    const CUresult r = fn(map,
-                          dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
-                                           : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
-                          4, const_cast<void *>(pool), dims, strides, box, estr,
+    const cuuint32_t rank = 4;
+#endif
+    const CUresult r = fn(map, ty, rank, const_cast<void *>(pool), dims, strides, box, estr,
                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -595,21 +745,24 @@ static bool encode_pool_map(CUtensorMap *map, const void *pool, pa_dtype dtype,
 }
 
 #ifndef PA_DECODE_WARPS
-#define PA_DECODE_WARPS 4
+#define PA_DECODE_WARPS 8
 #endif
 #ifndef PA_DECODE_STAGES
-#define PA_DECODE_STAGES 4
+#define PA_DECODE_STAGES 2
 #endif
-constexpr int kWarps = PA_DECODE_WARPS;
-constexpr int kStagesPerWarp = PA_DECODE_STAGES;
+constexpr int kWarps = PA_DECODE_WARPS;          // warps per CTA
+constexpr int kStagesPerWarp = PA_DECODE_STAGES; // ring stages per warp
+// Fewer stages for batches whose per-sequence shared arrays (8 B each) do
+// not fit next to the default rings.
+constexpr int kStagesManySeqs = 1;
 
-template <typename T, int D, int NT>
-static pa_status launch_decode(const DecodeParams &prm, const CUtensorMap &mk,
-                               const CUtensorMap &mv, cudaStream_t stream,
-                               long long max_units)
+template <typename T, int D, int NT, int NST>
+static pa_status launch_pass(const DecodeParams &prm, const CUtensorMap &mk,
+                             const CUtensorMap &mv, cudaStream_t stream, long long max_units)
 {
-    using L = Layout<D, NT, kWarps, kStagesPerWarp>;
-    auto kernel = paged_decode_kernel<T, D, NT, kWarps, kStagesPerWarp>;
+    using L = Layout<D, NT, kWarps, NST>;
+    auto kernel = paged_decode_kernel<T, D, NT, kWarps, NST>;
+    constexpr int kThreads = kWarps * 32;
     const size_t smem = L::bytes(prm.num_seqs);
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -625,7 +778,7 @@ static pa_status launch_decode(const DecodeParams &prm, const CUtensorMap &mk,
     if (e != cudaSuccess)
         return record_cuda(e);
     int per_sm = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kWarps * 32, smem);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, smem);
     if (e != cudaSuccess)
         return record_cuda(e);
     if (per_sm < 1)
@@ -635,17 +788,49 @@ static pa_status launch_decode(const DecodeParams &prm, const CUtensorMap &mk,
         grid = max_units;
     if (grid < 1)
         grid = 1;
-    kernel<<<(unsigned)grid, kWarps * 32, smem, stream>>>(prm, mk, mv);
+    kernel<<<(unsigned)grid, kThreads, smem, stream>>>(prm, mk, mv);
     return record_cuda(cudaGetLastError());
+}
+
+// The reduce is queued behind the partition pass with programmatic
+// dependent launch: its CTAs may start while the pass drains and wait in
+// griddepcontrol.wait until the pass's writes are visible.
+template <typename T, int D>
+static pa_status launch_reduce(const DecodeParams &prm, cudaStream_t stream)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(prm.num_seqs * prm.num_kv_heads));
+    cfg.blockDim = dim3(kReduceThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return record_cuda(cudaLaunchKernelEx(&cfg, paged_reduce_kernel<T, D>, prm));
+}
+
+template <typename T, int D, int NT>
+static pa_status launch_decode(const DecodeParams &prm, const CUtensorMap &mk,
+                               const CUtensorMap &mv, cudaStream_t stream,
+                               long long max_units)
+{
+    pa_status st = launch_pass<T, D, NT, kStagesPerWarp>(prm, mk, mv, stream, max_units);
+    if (st == PA_ERR_UNSUPPORTED)
+        st = launch_pass<T, D, NT, kStagesManySeqs>(prm, mk, mv, stream, max_units);
+    if (st != PA_OK || prm.max_parts <= 1)
+        return st;
+    return launch_reduce<T, D>(prm, stream);
 }
 
 static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 struct WorkspaceLayout {
-    size_t m_off, l_off, o_off, arr_off, total;
+    size_t m_off, l_off, o_off, total;
 };
 
-static WorkspaceLayout workspace_layout(int S, int H, int Hkv, int D, int parts)
+static WorkspaceLayout workspace_layout(int S, int H, int D, int parts)
 {
     WorkspaceLayout w{};
     if (parts <= 1)
@@ -654,8 +839,7 @@ static WorkspaceLayout workspace_layout(int S, int H, int Hkv, int D, int parts)
     w.m_off = 0;
     w.l_off = ml;
     w.o_off = 2 * ml;
-    w.arr_off = w.o_off + align256((size_t)S * H * parts * D * 4);
-    w.total = w.arr_off + align256((size_t)S * Hkv * 4);
+    w.total = w.o_off + align256((size_t)S * H * parts * D * 4);
     return w;
 }
 
@@ -678,7 +862,7 @@ extern "C" size_t pa_decode_workspace_bytes(int num_seqs, int num_heads, int num
         max_context_len < 0 || partition_size < 0)
         return 0;
     const int parts = num_parts(max_context_len, partition_size);
-    return workspace_layout(num_seqs, num_heads, num_kv_heads, head_dim, parts).total;
+    return workspace_layout(num_seqs, num_heads, head_dim, parts).total;
 }
 
 extern "C" pa_status pa_decode_attention(void *out, const void *query, const void *key_cache,
@@ -705,8 +889,8 @@ extern "C" pa_status pa_decode_attention(void *out, const void *query, const voi
         !aligned16(value_cache))
         return PA_ERR_INVALID_ARG;
     const int group = num_heads / num_kv_heads;
-    if ((head_dim != 64 && head_dim != 128) || block_size % kTileTokens != 0 ||
-        block_size > 256 || group > 16 ||
+    if ((head_dim != 64 && head_dim != 128) || block_size < kTileTokens ||
+        block_size > 256 || (block_size & (block_size - 1)) != 0 || group > 16 ||
         (long long)num_blocks * block_size >= (1ll << 31) ||
         (long long)max_blocks_per_seq * block_size >= (1ll << 31))
         return PA_ERR_UNSUPPORTED;
@@ -714,8 +898,7 @@ extern "C" pa_status pa_decode_attention(void *out, const void *query, const voi
         return PA_ERR_UNSUPPORTED;
 
     const int parts = num_parts(max_context_len, partition_size);
-    const WorkspaceLayout wl =
-        workspace_layout(num_seqs, num_heads, num_kv_heads, head_dim, parts);
+    const WorkspaceLayout wl = workspace_layout(num_seqs, num_heads, head_dim, parts);
     if (wl.total > 0 && (workspace == nullptr || workspace_bytes < wl.total ||
                          (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0))
         return PA_ERR_WORKSPACE;
@@ -729,7 +912,6 @@ extern "C" pa_status pa_decode_attention(void *out, const void *query, const voi
     prm.part_m = wl.total ? reinterpret_cast<float *>(ws + wl.m_off) : nullptr;
     prm.part_l = wl.total ? reinterpret_cast<float *>(ws + wl.l_off) : nullptr;
     prm.part_o = wl.total ? reinterpret_cast<float *>(ws + wl.o_off) : nullptr;
-    prm.arrivals = wl.total ? reinterpret_cast<uint32_t *>(ws + wl.arr_off) : nullptr;
     prm.error_word = error_word;
     prm.num_seqs = num_seqs;
     prm.num_heads = num_heads;
@@ -739,6 +921,7 @@ extern "C" pa_status pa_decode_attention(void *out, const void *query, const voi
     prm.num_blocks = num_blocks;
     prm.block_size = block_size;
     prm.max_context_len = max_context_len;
+    prm.block_shift = __builtin_ctz((unsigned)block_size);
     // Single pass: one unit covers the longest possible context.
     const long long ctx_cap = (long long)max_blocks_per_seq * block_size;
     const long long whole = ((std::max<long long>(1, std::min<long long>(

@@ -74,6 +74,7 @@ def test_decode_argument_checks(B):
     assert _decode(L, scale=float("nan")) == B.PA_ERR_INVALID_ARG
     assert _decode(L, D=96) == B.PA_ERR_UNSUPPORTED
     assert _decode(L, bs=8) == B.PA_ERR_UNSUPPORTED
+    assert _decode(L, bs=48) == B.PA_ERR_UNSUPPORTED
     assert _decode(L, H=34, Hkv=2) == B.PA_ERR_UNSUPPORTED      # group 17
     assert _decode(L, P=24) == B.PA_ERR_UNSUPPORTED
     # split path needs a workspace
@@ -108,7 +109,7 @@ def test_workspace_layout_sizes(B):
     a256 = lambda x: (x + 255) // 256 * 256  # noqa: E731
     # long-context workload: 16 seqs, 32 heads over 8, d 128, 32768 tokens / 512
     S, H, Hkv, D, P = 16, 32, 8, 128, 64
-    want = 2 * a256(S * H * P * 4) + a256(S * H * P * D * 4) + a256(S * Hkv * 4)
+    want = 2 * a256(S * H * P * 4) + a256(S * H * P * D * 4)
     assert L.pa_decode_workspace_bytes(S, H, Hkv, D, 32768, 512) == want
     # everything fits one partition, or single pass: no workspace
     assert L.pa_decode_workspace_bytes(S, H, Hkv, D, 512, 512) == 0

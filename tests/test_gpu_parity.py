@@ -200,20 +200,19 @@ def test_split_agrees_with_single_pass(B, S, small):
         assert np.abs(o - outs[0]).max() < 2e-2
 
 
-def test_repeated_calls_are_identical_and_leave_counters_zero(B, S, small):
+def test_repeated_calls_are_identical(B, S, small):
+    """Re-running the step (same writes, same copies, same attention) gives
+    bit-identical output, single pass and split."""
     w, _ = small("longctx")
     st = S.DecodeStep(w)
-    a = st.run().clone()
-    for _ in range(3):
-        b = st.run()
-        assert torch.equal(a, b)
-    ws = st.workspace
-    S_, H, Hkv, D = w.S, w.H, w.Hkv, w.D
-    Pm = math.ceil(int(w.context_lens.max()) / w.spec.partition_size)
-    a256 = lambda x: (x + 255) // 256 * 256  # noqa: E731
-    off = 2 * a256(4 * S_ * H * Pm) + a256(4 * S_ * H * Pm * D)
-    arrivals = ws[off:off + 4 * S_ * Hkv].view(torch.int32)
-    assert int(arrivals.abs().sum()) == 0
+    st.run()
+    for P in (0, w.spec.partition_size):
+        st.attention(partition_size=P)
+        a = st.out.clone()
+        for _ in range(3):
+            st.run()
+            st.attention(partition_size=P)
+            assert torch.equal(a, st.out), P
 
 
 def test_empty_context_gives_zero_row(B, S, small):
