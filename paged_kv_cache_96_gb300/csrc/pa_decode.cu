@@ -53,6 +53,7 @@ constexpr uint64_t kWaitLimitNs = 1000000000ull;  // one second per stage wait
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr unsigned kFull = 0xffffffffu;
+constexpr float kSlack = 8.f;  // log2 units: softmax weights stay <= 256 before rescaling
 
 struct DecodeParams {
     void *out;
@@ -365,30 +366,34 @@ __global__ void __launch_bounds__(NW * 32, 1)
                 const int nv = tok_end - (tok0 + tile * kTileTokens);  // valid rows
                 const bool partial = nv < kTileTokens;
 
-                // scores S[token][head] = K . Q^T, two accumulator chains
-                float sc[NT][4], sc2[NT][4];
+                // scores S[token][head] = K . Q^T in independent accumulator
+                // chains (k-step kk feeds chain kk % kChains), summed at the end
+                constexpr int kChains = KT >= 4 ? 4 : KT;
+                float part[kChains][NT][4];
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt) {
-                    sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
-                    sc2[nt][0] = sc2[nt][1] = sc2[nt][2] = sc2[nt][3] = 0.f;
-                }
+                for (int c = 0; c < kChains; ++c)
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt)
+                        part[c][nt][0] = part[c][nt][1] = part[c][nt][2] = part[c][nt][3] = 0.f;
 #pragma unroll
                 for (int kk = 0; kk < KT; ++kk) {
                     uint32_t a[4];
                     ldmatrix_x4(tile_addr(kbase, k_row, kk >> 2, (kk & 3) * 2 + k_cj), a);
 #pragma unroll
-                    for (int nt = 0; nt < NT; ++nt) {
-                        if (kk & 1)
-                            Op::run(sc2[nt], a, qf[nt][kk][0], qf[nt][kk][1]);
-                        else
-                            Op::run(sc[nt], a, qf[nt][kk][0], qf[nt][kk][1]);
-                    }
+                    for (int nt = 0; nt < NT; ++nt)
+                        Op::run(part[kk % kChains][nt], a, qf[nt][kk][0], qf[nt][kk][1]);
                 }
+                float sc[NT][4];
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        sc[nt][e] += sc2[nt][e];
+                    for (int e = 0; e < 4; ++e) {
+                        float x = part[0][nt][e];
+#pragma unroll
+                        for (int c = 1; c < kChains; ++c)
+                            x += part[c][nt][e];
+                        sc[nt][e] = x;
+                    }
 
                 // V^T fragments (their latency overlaps the softmax); rows past
                 // the context are zeroed so NaN padding never meets a zero weight
@@ -423,26 +428,26 @@ __global__ void __launch_bounds__(NW * 32, 1)
                         if (g + 8 >= nv)
                             s2 = s3 = -INFINITY;
                     }
-                    float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
+                    // mrun is a reference point, not necessarily the running max:
+                    // while every score of the tile stays within kSlack of it
+                    // (weights <= 2^kSlack) it is kept, which skips the
+                    // cross-lane max and the rescale; otherwise it moves up to
+                    // the running max and l and O are rescaled.
+                    const bool fits = s0 <= mrun[nt][0] + kSlack && s2 <= mrun[nt][0] + kSlack &&
+                                      s1 <= mrun[nt][1] + kSlack && s3 <= mrun[nt][1] + kSlack;
+                    if (!__all_sync(kFull, fits)) {
+                        float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
 #pragma unroll
-                    for (int off = 4; off < 32; off <<= 1) {
-                        mx0 = fmaxf(mx0, __shfl_xor_sync(kFull, mx0, off));
-                        mx1 = fmaxf(mx1, __shfl_xor_sync(kFull, mx1, off));
-                    }
-                    const float mn0 = fmaxf(mrun[nt][0], mx0);
-                    const float mn1 = fmaxf(mrun[nt][1], mx1);
-                    const float mu0 = mn0 == -INFINITY ? 0.f : mn0;
-                    const float mu1 = mn1 == -INFINITY ? 0.f : mn1;
-                    const float al0 = exp2f(mrun[nt][0] - mu0);
-                    const float al1 = exp2f(mrun[nt][1] - mu1);
-                    const float p0 = exp2f(s0 - mu0), p2 = exp2f(s2 - mu0);
-                    const float p1 = exp2f(s1 - mu1), p3 = exp2f(s3 - mu1);
-                    const bool grew = mn0 != mrun[nt][0] || mn1 != mrun[nt][1];
-                    lrun[nt][0] = lrun[nt][0] * al0 + (p0 + p2);
-                    lrun[nt][1] = lrun[nt][1] * al1 + (p1 + p3);
-                    mrun[nt][0] = mn0;
-                    mrun[nt][1] = mn1;
-                    if (__any_sync(kFull, grew)) {
+                        for (int off = 4; off < 32; off <<= 1) {
+                            mx0 = fmaxf(mx0, __shfl_xor_sync(kFull, mx0, off));
+                            mx1 = fmaxf(mx1, __shfl_xor_sync(kFull, mx1, off));
+                        }
+                        const float mn0 = fmaxf(mrun[nt][0], mx0);
+                        const float mn1 = fmaxf(mrun[nt][1], mx1);
+                        const float al0 = mn0 == -INFINITY ? 1.f : exp2f(mrun[nt][0] - mn0);
+                        const float al1 = mn1 == -INFINITY ? 1.f : exp2f(mrun[nt][1] - mn1);
+                        lrun[nt][0] *= al0;
+                        lrun[nt][1] *= al1;
 #pragma unroll
                         for (int mt = 0; mt < KT; ++mt) {
                             o[mt][nt][0] *= al0;
@@ -450,7 +455,15 @@ __global__ void __launch_bounds__(NW * 32, 1)
                             o[mt][nt][2] *= al0;
                             o[mt][nt][3] *= al1;
                         }
+                        mrun[nt][0] = mn0;
+                        mrun[nt][1] = mn1;
                     }
+                    const float mu0 = mrun[nt][0] == -INFINITY ? 0.f : mrun[nt][0];
+                    const float mu1 = mrun[nt][1] == -INFINITY ? 0.f : mrun[nt][1];
+                    const float p0 = exp2f(s0 - mu0), p2 = exp2f(s2 - mu0);
+                    const float p1 = exp2f(s1 - mu1), p3 = exp2f(s3 - mu1);
+                    lrun[nt][0] += p0 + p2;
+                    lrun[nt][1] += p1 + p3;
                     pb[nt][0] = movmatrix_trans(Op::pack(p0, p1));
                     pb[nt][1] = movmatrix_trans(Op::pack(p2, p3));
                 }
@@ -574,14 +587,16 @@ __global__ void __launch_bounds__(NW * 32, 1)
 // by the partition pass itself.  (1) warp w finds M and sum_q w_q for heads
 // jh = w, w + 4, ...; (2) thread (item, qg) sums w_q o_q over q = qg, qg + QG,
 // ...; (3) the QG group sums are added in shared memory.
-constexpr int kReduceThreads = 128;
+constexpr int kReduceThreads = 256;
+constexpr int kReduceChunk = 128;  // partitions whose weights are staged at once
 
 template <typename T, int D>
 __global__ void __launch_bounds__(kReduceThreads)
     paged_reduce_kernel(const __grid_constant__ DecodeParams p)
 {
     using Op = MmaOp<T>;
-    __shared__ float head_m[16], head_l[16];
+    __shared__ float head_m[16], head_inv_l[16];
+    __shared__ float wts[16 * kReduceChunk];
     __shared__ __align__(16) float red[kReduceThreads * 8];
     pdl_wait_primary();  // the partition pass's partials are visible past here
 
@@ -595,6 +610,7 @@ __global__ void __launch_bounds__(kReduceThreads)
     if (nparts <= 1)
         return;
 
+    // (1) per head: M = max_q m_q and L = sum_q l_q exp(m_q - M) (warp per head)
     const size_t hbase = ((size_t)s * p.num_heads + (size_t)kh * G) * p.max_parts;
     for (int jh = warp; jh < G; jh += kReduceThreads / 32) {
         const float *pm = p.part_m + hbase + (size_t)jh * p.max_parts;
@@ -613,31 +629,47 @@ __global__ void __launch_bounds__(kReduceThreads)
             ls += __shfl_xor_sync(kFull, ls, off);
         if (lane == 0) {
             head_m[jh] = mx;
-            head_l[jh] = ls;
+            head_inv_l[jh] = 1.f / ls;
         }
     }
     __syncthreads();
 
+    // (2) thread (item, qg) sums w_q o_q over q = qg, qg + QG, ... with the
+    // weights w_q = l_q exp(m_q - M) / L of a chunk of partitions staged in
+    // shared memory; (3) the QG group sums are added in shared memory.
+    // G * D / 8 <= 16 * 128 / 8 = kReduceThreads: one (item, qg) per thread.
+    static_assert(16 * D / 8 <= kReduceThreads, "one work item per thread");
     const int items = G * (D / 8);
     const int qgroups = max(1, kReduceThreads / items);
-    for (int w_it = tid; w_it < items * qgroups; w_it += kReduceThreads) {
-        const int item = w_it % items;
-        const int qg = w_it / items;
-        const int jh = item / (D / 8);
-        const int d0 = (item - jh * (D / 8)) * 8;
-        const size_t base = hbase + (size_t)jh * p.max_parts;
-        const float mx = head_m[jh];
-        const float inv_l = 1.f / head_l[jh];
-        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll 4
-        for (int q = qg; q < nparts; q += qgroups) {
-            const float wgt = p.part_l[base + q] * exp2f((p.part_m[base + q] - mx) * kLog2e) *
-                              inv_l;
-            const float4 *src = reinterpret_cast<const float4 *>(p.part_o + (base + q) * D + d0);
-            const float4 x0 = src[0], x1 = src[1];
-            acc[0] += wgt * x0.x; acc[1] += wgt * x0.y; acc[2] += wgt * x0.z; acc[3] += wgt * x0.w;
-            acc[4] += wgt * x1.x; acc[5] += wgt * x1.y; acc[6] += wgt * x1.z; acc[7] += wgt * x1.w;
+    const bool active = tid < items * qgroups;
+    const int item = tid % items;
+    const int qg = tid / items;
+    const int jh = item / (D / 8);
+    const int d0 = (item - jh * (D / 8)) * 8;
+    const float *po = p.part_o + (hbase + (size_t)jh * p.max_parts) * D + d0;
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int c0 = 0; c0 < nparts; c0 += kReduceChunk) {
+        const int cn = min(kReduceChunk, nparts - c0);
+        for (int i = tid; i < G * cn; i += kReduceThreads) {
+            const int h = i / cn, q = c0 + (i - h * cn);
+            const size_t idx = hbase + (size_t)h * p.max_parts + q;
+            wts[h * kReduceChunk + (q - c0)] =
+                p.part_l[idx] * exp2f((p.part_m[idx] - head_m[h]) * kLog2e) * head_inv_l[h];
         }
+        __syncthreads();
+        if (active) {
+#pragma unroll 8
+            for (int q = c0 + qg; q < c0 + cn; q += qgroups) {
+                const float wgt = wts[jh * kReduceChunk + (q - c0)];
+                const float4 x0 = reinterpret_cast<const float4 *>(po + (size_t)q * D)[0];
+                const float4 x1 = reinterpret_cast<const float4 *>(po + (size_t)q * D)[1];
+                acc[0] += wgt * x0.x; acc[1] += wgt * x0.y; acc[2] += wgt * x0.z; acc[3] += wgt * x0.w;
+                acc[4] += wgt * x1.x; acc[5] += wgt * x1.y; acc[6] += wgt * x1.z; acc[7] += wgt * x1.w;
+            }
+        }
+        __syncthreads();
+    }
+    if (active) {
         if (qgroups == 1) {
             T vals[8];
 #pragma unroll
@@ -647,7 +679,7 @@ __global__ void __launch_bounds__(kReduceThreads)
                                        ((size_t)s * p.num_heads + (size_t)kh * G + jh) * D +
                                        d0) = *reinterpret_cast<const uint4 *>(vals);
         } else {
-            float4 *dst = reinterpret_cast<float4 *>(red + (size_t)(qg * items + item) * 8);
+            float4 *dst = reinterpret_cast<float4 *>(red + (size_t)tid * 8);
             dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
             dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
         }
@@ -658,17 +690,17 @@ __global__ void __launch_bounds__(kReduceThreads)
     for (int it = tid; it < items; it += kReduceThreads) {
         const int jh = it / (D / 8);
         const int d0 = (it - jh * (D / 8)) * 8;
-        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        float sum[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
         for (int g2 = 0; g2 < qgroups; ++g2) {
             const float4 *src = reinterpret_cast<const float4 *>(red + (size_t)(g2 * items + it) * 8);
             const float4 x0 = src[0], x1 = src[1];
-            acc[0] += x0.x; acc[1] += x0.y; acc[2] += x0.z; acc[3] += x0.w;
-            acc[4] += x1.x; acc[5] += x1.y; acc[6] += x1.z; acc[7] += x1.w;
+            sum[0] += x0.x; sum[1] += x0.y; sum[2] += x0.z; sum[3] += x0.w;
+            sum[4] += x1.x; sum[5] += x1.y; sum[6] += x1.z; sum[7] += x1.w;
         }
         T vals[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e)
-            vals[e] = Op::from_float(acc[e]);
+            vals[e] = Op::from_float(sum[e]);
         *reinterpret_cast<uint4 *>(static_cast<T *>(p.out) +
                                    ((size_t)s * p.num_heads + (size_t)kh * G + jh) * D + d0) =
             *reinterpret_cast<const uint4 *>(vals);
@@ -745,7 +777,7 @@ static bool encode_pool_map(CUtensorMap *map, const void *pool, pa_dtype dtype,
 }
 
 #ifndef PA_DECODE_WARPS
-#define PA_DECODE_WARPS 8
+#define PA_DECODE_WARPS 10
 #endif
 #ifndef PA_DECODE_STAGES
 #define PA_DECODE_STAGES 2

@@ -292,14 +292,15 @@ CONFIGS: Dict[str, WorkloadSpec] = {
         description="MHA 7B-like decode layer: 64 seqs, context U[128,2048], "
                     "32 heads, d 128, block 16, bf16, pool 1.25x",
         num_seqs=64, num_heads=32, num_kv_heads=32, head_dim=128, block_size=16,
-        dtype="bf16", context_lens=_uniform(64, 128, 2048)),
+        dtype="bf16", context_lens=_uniform(64, 128, 2048), partition_size=2048),
     "gqa70b": WorkloadSpec(
         name="gqa70b", seed=9603,
         description="GQA 70B-like decode layer: 128 seqs, context lognormal "
                     "(median 1500, sigma 0.8) clipped [16,8192], 64 query heads "
                     "over 8 KV heads, d 128, block 16, bf16, pool 1.25x",
         num_seqs=128, num_heads=64, num_kv_heads=8, head_dim=128, block_size=16,
-        dtype="bf16", context_lens=_lognormal(128, 1500.0, 0.8, 16, 8192)),
+        dtype="bf16", context_lens=_lognormal(128, 1500.0, 0.8, 16, 8192),
+        partition_size=1024),
     "longctx": WorkloadSpec(
         name="longctx", seed=9604,
         description="long-context skew: 16 seqs (4 x 32768, 12 x U[64,512]), "
@@ -314,7 +315,7 @@ CONFIGS: Dict[str, WorkloadSpec] = {
                     "8 KV heads, d 128, block 16, bf16; 32 copy-on-write pairs",
         num_seqs=256, num_heads=32, num_kv_heads=8, head_dim=128, block_size=16,
         dtype="bf16", context_lens=_prefix_plus(256, 1024, 1, 1024),
-        shared_prefix_tokens=1024, cow_pairs=32),
+        shared_prefix_tokens=1024, cow_pairs=32, partition_size=2048),
 }
 
 
