@@ -172,6 +172,39 @@ PA_API pa_status pa_decode_attention(void *out, const void *query,
                               size_t workspace_bytes, pa_dtype dtype,
                               int32_t *error_word, void *stream);
 
+/*
+ * pa_decode_attention_noalloc -- no counterpart on the pages: an addition
+ * for callers that may not allocate device memory on their decode path (a
+ * plugin whose host engine owns all device memory through its own pool, a
+ * latency-critical loop that cannot take an allocation's implicit
+ * synchronisation, a C interface that only passes inputs and outputs).
+ * Same arguments, meaning and result as pa_decode_attention, minus the
+ * workspace: the split-context partials go to a statically sized device
+ * array of PA_NOALLOC_WORKSPACE_BYTES inside the library, created when the
+ * library's device code is loaded on a GPU and kept by every such GPU until
+ * the process exits.  The call itself allocates nothing.
+ *   - Sizes whose workspace (pa_decode_workspace_bytes) exceeds
+ *     PA_NOALLOC_WORKSPACE_BYTES are rejected with PA_ERR_WORKSPACE before
+ *     anything is launched.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress, once per device, with that device current);
+ *     make that first call before any stream capture.
+ *   - Every call on a device shares the one array and leaves its last
+ *     contents there; no part of it needs to start at zero (each call
+ *     writes every partial it later reads).  Calls whose GPU work overlaps
+ *     in time (for instance on two streams) race on the array.
+ */
+#define PA_NOALLOC_WORKSPACE_BYTES (32u * 1024u * 1024u)
+PA_API pa_status pa_decode_attention_noalloc(void *out, const void *query,
+                                             const void *key_cache, const void *value_cache,
+                                             const int32_t *block_tables,
+                                             int max_blocks_per_seq,
+                                             const int32_t *context_lens, int max_context_len,
+                                             int num_seqs, int num_heads, int num_kv_heads,
+                                             int head_dim, int block_size, int num_blocks,
+                                             float scale, int partition_size, pa_dtype dtype,
+                                             int32_t *error_word, void *stream);
+
 /* Human-readable name of a status code (static storage). */
 PA_API const char *pa_status_string(pa_status status);
 

@@ -58,6 +58,8 @@ def _load() -> ctypes.CDLL:
         "pa_decode_workspace_bytes": (sz, [i32, i32, i32, i32, i32, i32]),
         "pa_decode_attention": (i32, [P, P, P, P, P, i32, P, i32, i32, i32, i32, i32,
                                       i32, i32, f32, i32, P, sz, i32, P, P]),
+        "pa_decode_attention_noalloc": (i32, [P, P, P, P, P, i32, P, i32, i32, i32, i32,
+                                              i32, i32, i32, f32, i32, i32, P, P]),
         "pa_status_string": (ctypes.c_char_p, [i32]),
         "pa_last_cuda_error": (ctypes.c_char_p, []),
         "pa_version": (i32, []),
@@ -190,6 +192,31 @@ def pa_decode_attention(out: torch.Tensor, query: torch.Tensor,
         _dev(context_lens, "context_lens", torch.int32), int(max_context_len), S, H, Hkv,
         d, bs, N, float(scale), int(partition_size), ws_ptr, ws_bytes,
         _dtype_code(key_cache), _opt(error_word, "error_word"), _stream(stream)))
+
+
+def pa_decode_attention_noalloc(out: torch.Tensor, query: torch.Tensor,
+                                key_cache: torch.Tensor, value_cache: torch.Tensor,
+                                block_tables: torch.Tensor, context_lens: torch.Tensor,
+                                max_context_len: int, scale: float, partition_size: int = 0,
+                                error_word: Optional[torch.Tensor] = None,
+                                stream=None) -> None:
+    """As pa_decode_attention, with the library's static device workspace
+    (for callers that cannot allocate one)."""
+    S, H, d = query.shape
+    N, bs, Hkv, d2 = key_cache.shape
+    MB = block_tables.shape[1]
+    if d != d2 or out.shape != query.shape:
+        raise ValueError("shape mismatch")
+    _check("pa_decode_attention_noalloc", _lib.pa_decode_attention_noalloc(
+        _dev(out, "out", query.dtype), _dev(query, "query", key_cache.dtype),
+        _dev(key_cache, "key_cache"), _dev(value_cache, "value_cache", key_cache.dtype),
+        _dev(block_tables, "block_tables", torch.int32), MB,
+        _dev(context_lens, "context_lens", torch.int32), int(max_context_len), S, H, Hkv,
+        d, bs, N, float(scale), int(partition_size), _dtype_code(key_cache),
+        _opt(error_word, "error_word"), _stream(stream)))
+
+
+NOALLOC_WORKSPACE_BYTES = 32 * 1024 * 1024
 
 
 def alloc_workspace(num_seqs: int, num_heads: int, num_kv_heads: int, head_dim: int,
