@@ -34,6 +34,8 @@ __global__ void slot_mapping_kernel(int32_t *__restrict__ slot_mapping,
                                     int num_seqs, int block_size, int num_blocks,
                                     int32_t *error_word)
 {
+    pdl_wait_primary();
+    pdl_launch_dependents();
     const int t = blockIdx.x * blockDim.x + threadIdx.x;
     if (t >= num_tokens)
         return;
@@ -65,6 +67,8 @@ __global__ void reshape_and_cache_kernel(const uint4 *__restrict__ key,
                                          int64_t num_slots, int words_per_token,
                                          int32_t *error_word)
 {
+    pdl_wait_primary();
+    pdl_launch_dependents();
     const int t = blockIdx.x;
     const int64_t slot = slot_mapping[t];
     if (slot < 0)
@@ -98,6 +102,8 @@ __global__ void copy_blocks_kernel(uint4 *__restrict__ key_cache,
                                    int num_blocks, int64_t words_per_block,
                                    int32_t *error_word)
 {
+    pdl_wait_primary();
+    pdl_launch_dependents();
     const int pair = blockIdx.x;
     const int src = block_mapping[2 * pair];
     const int dst = block_mapping[2 * pair + 1];
@@ -147,10 +153,9 @@ extern "C" pa_status pa_slot_mapping(int32_t *slot_mapping, const int32_t *block
         return PA_ERR_UNSUPPORTED;
     const int threads = 256;
     const int blocks = (num_tokens + threads - 1) / threads;
-    slot_mapping_kernel<<<blocks, threads, 0, as_stream(stream)>>>(
-        slot_mapping, block_tables, max_blocks_per_seq, token_seq, token_pos, num_tokens,
-        num_seqs, block_size, num_blocks, error_word);
-    return record_cuda(cudaGetLastError());
+    return launch_pdl(slot_mapping_kernel, dim3(blocks), dim3(threads), 0, as_stream(stream),
+                      slot_mapping, block_tables, max_blocks_per_seq, token_seq, token_pos,
+                      num_tokens, num_seqs, block_size, num_blocks, error_word);
 }
 
 extern "C" pa_status pa_reshape_and_cache(const void *key, const void *value,
@@ -175,11 +180,11 @@ extern "C" pa_status pa_reshape_and_cache(const void *key, const void *value,
         return PA_ERR_UNSUPPORTED;
     const int words = static_cast<int>(row_bytes / 16);
     const int threads = words >= 256 ? 256 : ((words + 31) / 32) * 32;
-    reshape_and_cache_kernel<<<num_tokens, threads, 0, as_stream(stream)>>>(
-        static_cast<const uint4 *>(key), static_cast<const uint4 *>(value),
-        static_cast<uint4 *>(key_cache), static_cast<uint4 *>(value_cache), slot_mapping,
-        static_cast<int64_t>(num_blocks) * block_size, words, error_word);
-    return record_cuda(cudaGetLastError());
+    return launch_pdl(reshape_and_cache_kernel, dim3(num_tokens), dim3(threads), 0,
+                      as_stream(stream), static_cast<const uint4 *>(key),
+                      static_cast<const uint4 *>(value), static_cast<uint4 *>(key_cache),
+                      static_cast<uint4 *>(value_cache), slot_mapping,
+                      static_cast<int64_t>(num_blocks) * block_size, words, error_word);
 }
 
 extern "C" pa_status pa_copy_blocks(void *key_cache, void *value_cache,
@@ -207,10 +212,9 @@ extern "C" pa_status pa_copy_blocks(void *key_cache, void *value_cache,
     if (slabs > 65535 || num_pairs > INT32_MAX / 2)
         return PA_ERR_UNSUPPORTED;
     dim3 grid(num_pairs, 2, static_cast<unsigned>(slabs));
-    copy_blocks_kernel<<<grid, kCopyThreads, 0, as_stream(stream)>>>(
-        static_cast<uint4 *>(key_cache), static_cast<uint4 *>(value_cache), block_mapping,
-        num_blocks, words, error_word);
-    return record_cuda(cudaGetLastError());
+    return launch_pdl(copy_blocks_kernel, grid, dim3(kCopyThreads), 0, as_stream(stream),
+                      static_cast<uint4 *>(key_cache), static_cast<uint4 *>(value_cache),
+                      block_mapping, num_blocks, words, error_word);
 }
 
 extern "C" const char *pa_status_string(pa_status status)

@@ -4,6 +4,7 @@
 #pragma once
 
 #include <cstdint>
+#include <utility>
 #include <cuda_runtime.h>
 
 #include "../../include/paged_attention.h"
@@ -20,6 +21,37 @@ inline bool aligned16(const void *p)
 }
 
 inline cudaStream_t as_stream(void *s) { return reinterpret_cast<cudaStream_t>(s); }
+
+// Programmatic dependent launch.  Every kernel of the library is launched
+// with programmatic stream serialisation: it may begin while the kernel
+// before it on the stream finishes, and waits in pdl_wait_primary() --
+// before its first global read -- until that kernel's writes are visible.
+// pdl_launch_dependents() lets the next kernel on the stream begin early.
+__device__ __forceinline__ void pdl_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait_primary()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+inline pa_status launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                            cudaStream_t stream, Args &&...args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return record_cuda(cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...));
+}
 
 // OR `bits` into the optional device error word.
 __device__ __forceinline__ void flag_error(int32_t *error_word, int32_t bits)

@@ -92,17 +92,6 @@ template <int D, int NT, int NW, int NST> struct Layout {
     static_assert(kStageBytes % 1024 == 0, "stages must keep 1024-byte alignment");
 };
 
-// Program-dependent launch: let the grid queued behind this one start
-// launching, and (in that grid) wait for this one's memory to be visible.
-__device__ __forceinline__ void pdl_launch_dependents()
-{
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-__device__ __forceinline__ void pdl_wait_primary()
-{
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-}
-
 // Clamped context length (same rule in both kernels).
 __device__ __forceinline__ int clamp_context(const DecodeParams &p, int s, bool flag)
 {
@@ -155,9 +144,6 @@ __global__ void __launch_bounds__(NW * 32, 1)
         return sbase + L::kStages + (warp * NST + stage) * L::kStageBytes;
     };
 
-    // ---- context lengths and partition prefix sums -----------------------
-    for (int s = tid; s < S; s += kThreads)
-        ctx_s[s] = clamp_context(p, s, blockIdx.x == 0);
     if (lane == 0) {
         for (int k = 0; k < NST; ++k)
             mbar_init(bar_of(k), 1);
@@ -167,6 +153,14 @@ __global__ void __launch_bounds__(NW * 32, 1)
         prefetch_tensormap(&tmap_k);
         prefetch_tensormap(&tmap_v);
     }
+    // Launched as a programmatic dependent of the kernel before it on the
+    // stream: every global read below comes after the predecessor's writes
+    // are visible.
+    pdl_wait_primary();
+
+    // ---- context lengths and partition prefix sums -----------------------
+    for (int s = tid; s < S; s += kThreads)
+        ctx_s[s] = clamp_context(p, s, blockIdx.x == 0);
     __syncthreads();
     if (warp == 0) {
         int carry = 0;
@@ -777,7 +771,7 @@ static bool encode_pool_map(CUtensorMap *map, const void *pool, pa_dtype dtype,
 }
 
 #ifndef PA_DECODE_WARPS
-#define PA_DECODE_WARPS 10
+#define PA_DECODE_WARPS 5
 #endif
 #ifndef PA_DECODE_STAGES
 #define PA_DECODE_STAGES 2
@@ -820,8 +814,7 @@ static pa_status launch_pass(const DecodeParams &prm, const CUtensorMap &mk,
         grid = max_units;
     if (grid < 1)
         grid = 1;
-    kernel<<<(unsigned)grid, kThreads, smem, stream>>>(prm, mk, mv);
-    return record_cuda(cudaGetLastError());
+    return launch_pdl(kernel, dim3((unsigned)grid), dim3(kThreads), smem, stream, prm, mk, mv);
 }
 
 // The reduce is queued behind the partition pass with programmatic
@@ -830,17 +823,8 @@ static pa_status launch_pass(const DecodeParams &prm, const CUtensorMap &mk,
 template <typename T, int D>
 static pa_status launch_reduce(const DecodeParams &prm, cudaStream_t stream)
 {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(prm.num_seqs * prm.num_kv_heads));
-    cfg.blockDim = dim3(kReduceThreads);
-    cfg.dynamicSmemBytes = 0;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return record_cuda(cudaLaunchKernelEx(&cfg, paged_reduce_kernel<T, D>, prm));
+    return launch_pdl(paged_reduce_kernel<T, D>, dim3((unsigned)(prm.num_seqs * prm.num_kv_heads)),
+                      dim3(kReduceThreads), 0, stream, prm);
 }
 
 template <typename T, int D, int NT>

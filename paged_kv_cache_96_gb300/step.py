@@ -123,7 +123,13 @@ class DecodeStep:
         return self.out
 
     def launches_per_step(self) -> int:
-        return 4 if self.cow_pairs is not None else 3
+        """Kernels one run() launches: slot mapping, cache write, block copy
+        (when the step has copy-on-write pairs), the attention pass, and the
+        reduce (when some context spans more than one partition)."""
+        n = 3 + (1 if self.cow_pairs is not None else 0)
+        if self.workspace is not None:
+            n += 1
+        return n
 
 
 def to_bits(t: torch.Tensor) -> np.ndarray:

@@ -1,0 +1,60 @@
+"""The five decode-layer workloads at full size, in the launch configuration
+the benchmark times (each workload's own partition size): slots and both
+pools -- after the history writes, the step's writes and its copy-on-write
+copies -- bit-exact against the oracle; attention of sampled sequences (the
+longest, the shortest and seeded random ones, every head and element)
+within the contract tolerance."""
+import numpy as np
+import pytest
+import torch
+
+pytestmark = [pytest.mark.gpu, pytest.mark.slow]
+
+import oracle  # noqa: E402
+from paged_kv_cache_96_gb300 import workloads as W  # noqa: E402
+from stepping import assert_attention_close, odt  # noqa: E402
+
+NAMES = ["tiny", "mha7b", "gqa70b", "longctx", "prefix"]
+
+
+def _oracle_pools(w):
+    kc, vc = w.empty_pools()
+    slots = oracle.slot_mapping(w.block_tables, w.hist_seq, w.hist_pos, w.bs)
+    oracle.reshape_and_cache(w.hist_key, w.hist_value, kc, vc, slots)
+    new_slots = oracle.slot_mapping(w.block_tables, w.new_seq, w.new_pos, w.bs)
+    oracle.reshape_and_cache(w.new_key, w.new_value, kc, vc, new_slots)
+    if w.cow_pairs.shape[0]:
+        oracle.copy_blocks(kc, vc, w.cow_pairs)
+    return kc, vc, new_slots
+
+
+def _sample(w, k=6, seed=7):
+    ctx = w.context_lens
+    order = np.argsort(ctx)
+    picks = {int(order[0]), int(order[-1]), int(order[len(order) // 2])}
+    rng = np.random.default_rng(seed)
+    picks.update(int(x) for x in rng.choice(w.S, size=min(k, w.S), replace=False))
+    return sorted(picks)
+
+
+@pytest.mark.parametrize("name", NAMES)
+def test_full_size_step(name):
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from paged_kv_cache_96_gb300 import step as S
+    w = W.build(W.CONFIGS[name])
+    st = S.DecodeStep(w)  # the workload's own partition size, as the benchmark runs it
+    out = st.run()
+    torch.cuda.synchronize()
+    assert int(st.error_word.item()) == 0
+
+    kc, vc, new_slots = _oracle_pools(w)
+    assert np.array_equal(st.slots.cpu().numpy().astype(np.int64), new_slots)
+    assert np.array_equal(S.to_bits(st.key_cache), kc)
+    assert np.array_equal(S.to_bits(st.value_cache), vc)
+
+    seqs = _sample(w)
+    want = oracle.paged_attention(w.query, kc, vc, w.step_block_tables, w.context_lens,
+                                  w.scale, odt(w), seqs=seqs)
+    got = S.to_float(out)
+    assert_attention_close(got[seqs], want[seqs], f"{name} seqs {seqs}")
