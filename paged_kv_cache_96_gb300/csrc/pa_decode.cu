@@ -782,6 +782,41 @@ constexpr int kStagesPerWarp = PA_DECODE_STAGES; // ring stages per warp
 // not fit next to the default rings.
 constexpr int kStagesManySeqs = 1;
 
+// Per-device facts and per-kernel launch settings, looked up once: the SM
+// count and shared-memory limit of each device, and for each kernel the
+// largest dynamic shared memory it has been enabled for and the residency
+// found for the last shared-memory size.
+constexpr int kMaxDevices = 64;
+struct DeviceInfo {
+    int sms = 0, optin = 0;
+};
+static pa_status device_info(int dev, DeviceInfo *out)
+{
+    static DeviceInfo cache[kMaxDevices];
+    static std::mutex mu;
+    if (dev < 0 || dev >= kMaxDevices)
+        return PA_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(mu);
+    if (cache[dev].sms == 0) {
+        cudaError_t e = cudaDeviceGetAttribute(&cache[dev].optin,
+                                               cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+        if (e == cudaSuccess)
+            e = cudaDeviceGetAttribute(&cache[dev].sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) {
+            cache[dev].sms = 0;
+            return record_cuda(e);
+        }
+    }
+    *out = cache[dev];
+    return PA_OK;
+}
+
+struct KernelSetting {
+    size_t smem_enabled = 0;  // dynamic shared memory the kernel may use
+    size_t smem_queried = 0;  // shared-memory size of the cached residency
+    int per_sm = 0;           // resident CTAs per SM at smem_queried
+};
+
 template <typename T, int D, int NT, int NST>
 static pa_status launch_pass(const DecodeParams &prm, const CUtensorMap &mk,
                              const CUtensorMap &mv, cudaStream_t stream, long long max_units)
@@ -789,24 +824,39 @@ static pa_status launch_pass(const DecodeParams &prm, const CUtensorMap &mk,
     using L = Layout<D, NT, kWarps, NST>;
     auto kernel = paged_decode_kernel<T, D, NT, kWarps, NST>;
     constexpr int kThreads = kWarps * 32;
+    static KernelSetting setting[kMaxDevices];
+    static std::mutex mu;
     const size_t smem = L::bytes(prm.num_seqs);
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess)
         return record_cuda(e);
-    int optin = 0, sms = 0;
-    cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (smem > (size_t)optin)
+    DeviceInfo info;
+    const pa_status st = device_info(dev, &info);
+    if (st != PA_OK)
+        return st;
+    if (smem > (size_t)info.optin)
         return PA_ERR_UNSUPPORTED;
-    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem);
-    if (e != cudaSuccess)
-        return record_cuda(e);
+    const int sms = info.sms;
     int per_sm = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, smem);
-    if (e != cudaSuccess)
-        return record_cuda(e);
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        KernelSetting &ks = setting[dev];
+        if (smem > ks.smem_enabled) {
+            e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)smem);
+            if (e != cudaSuccess)
+                return record_cuda(e);
+            ks.smem_enabled = smem;
+        }
+        if (smem != ks.smem_queried) {
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&ks.per_sm, kernel, kThreads, smem);
+            if (e != cudaSuccess)
+                return record_cuda(e);
+            ks.smem_queried = smem;
+        }
+        per_sm = ks.per_sm;
+    }
     if (per_sm < 1)
         return PA_ERR_UNSUPPORTED;
     long long grid = (long long)sms * per_sm;
