@@ -84,6 +84,13 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
                                          i32, i32, i32, dbl, i32, i32, i32, P,
                                          i32]),
         "oracle_partition_merge": (None, [P, P, P, P, P, i32, i32, i32, i32]),
+        "oracle_decode_e4m3": (None, [P, P, i64]),
+        "oracle_quantize_e4m3": (None, [P, P, i64, i32, ctypes.c_float]),
+        "oracle_reshape_and_cache_fp8": (None, [P, P, P, P, P, i32, i32, i32, i32, i32,
+                                                ctypes.c_float, ctypes.c_float]),
+        "oracle_paged_attention_fp8": (None, [P, P, P, P, P, i32, P, i32, i32, i32, i32,
+                                              i32, dbl, i32, dbl, dbl, P, i32]),
+        "oracle_copy_blocks_u8": (None, [P, P, P, i32, i32, i32, i32]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -268,3 +275,81 @@ def partition_merge(m: np.ndarray, l: np.ndarray, o: np.ndarray,
     lib.oracle_partition_merge(_ptr(out), _ptr(m), _ptr(l), _ptr(o), _ptr(npart),
                                S, H, d, P)
     return out
+
+
+# ---------------------------------------------------------------------------
+# FP8 (e4m3) KV cache -- the "--kv-cache-dtype fp8" option of "vLLM 架构详解"
+# (deployment flags); format and rounding readings are in pa_oracle.c.
+
+def decode_e4m3(codes: np.ndarray, lib=None) -> np.ndarray:
+    """e4m3 codes (uint8) -> exact float64 values."""
+    lib = lib or load()
+    c = np.ascontiguousarray(codes, dtype=np.uint8)
+    out = np.empty(c.shape, dtype=np.float64)
+    lib.oracle_decode_e4m3(_ptr(out), _ptr(c), c.size)
+    return out
+
+
+def quantize_e4m3(x_bits: np.ndarray, dtype: int, inv_scale: float, lib=None) -> np.ndarray:
+    """16-bit values -> e4m3 codes of float(x) * inv_scale (fp32 product)."""
+    lib = lib or load()
+    x = _u16(x_bits)
+    out = np.empty(x.shape, dtype=np.uint8)
+    lib.oracle_quantize_e4m3(_ptr(out), _ptr(x), x.size, dtype, float(inv_scale))
+    return out
+
+
+def _inplace_u8(a: np.ndarray) -> np.ndarray:
+    if not (isinstance(a, np.ndarray) and a.flags["C_CONTIGUOUS"] and a.dtype == np.uint8):
+        raise TypeError("FP8 pools written in place must be C-contiguous uint8 arrays")
+    return a
+
+
+def reshape_and_cache_fp8(key: np.ndarray, value: np.ndarray, key_cache: np.ndarray,
+                          value_cache: np.ndarray, slots: np.ndarray, dtype: int,
+                          k_scale: float, v_scale: float, lib=None) -> None:
+    """In place: quantise key/value [T, Hkv, d] into FP8 pools [N, bs, Hkv, d]."""
+    lib = lib or load()
+    k, v = _u16(key), _u16(value)
+    kc, vc = _inplace_u8(key_cache), _inplace_u8(value_cache)
+    sl = np.ascontiguousarray(slots, dtype=np.int64)
+    T, Hkv, d = k.shape
+    lib.oracle_reshape_and_cache_fp8(_ptr(k), _ptr(v), _ptr(kc), _ptr(vc), _ptr(sl), T, Hkv,
+                                     d, kc.shape[1], dtype, _f32_inv(k_scale),
+                                     _f32_inv(v_scale))
+
+
+def _f32_inv(scale: float) -> float:
+    """1 / scale rounded to fp32 (the inverse both sides multiply by)."""
+    return float(np.float32(1.0) / np.float32(scale))
+
+
+def paged_attention_fp8(query: np.ndarray, key_cache: np.ndarray, value_cache: np.ndarray,
+                        block_tables: np.ndarray, context_lens: np.ndarray, scale: float,
+                        dtype: int, k_scale: float, v_scale: float,
+                        seqs: Optional[Sequence[int]] = None, lib=None) -> np.ndarray:
+    """fp64 attention over FP8 pools (dequantised codes)."""
+    lib = lib or load()
+    q = _u16(query)
+    kc = np.ascontiguousarray(key_cache, dtype=np.uint8)
+    vc = np.ascontiguousarray(value_cache, dtype=np.uint8)
+    bt, cl = _i32(block_tables), _i32(context_lens)
+    S, H, d = q.shape
+    N, bs, Hkv, _ = kc.shape
+    out = np.full((S, H, d), np.nan, dtype=np.float64)
+    sub = None if seqs is None else _i32(list(seqs))
+    lib.oracle_paged_attention_fp8(_ptr(out), _ptr(q), _ptr(kc), _ptr(vc), _ptr(bt),
+                                   bt.shape[1], _ptr(cl), S, H, Hkv, d, bs, float(scale),
+                                   dtype, float(np.float32(k_scale)),
+                                   float(np.float32(v_scale)), _ptr(sub),
+                                   0 if sub is None else sub.shape[0])
+    return out
+
+
+def copy_blocks_u8(key_cache: np.ndarray, value_cache: np.ndarray,
+                   block_mapping: np.ndarray, lib=None) -> None:
+    lib = lib or load()
+    kc, vc = _inplace_u8(key_cache), _inplace_u8(value_cache)
+    bm = _i32(block_mapping).reshape(-1, 2)
+    N, bs, Hkv, d = kc.shape
+    lib.oracle_copy_blocks_u8(_ptr(kc), _ptr(vc), _ptr(bm), bm.shape[0], bs, Hkv, d)

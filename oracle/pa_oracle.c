@@ -93,6 +93,82 @@ void oracle_decode(double *out, const uint16_t *bits, int64_t n, int dtype)
         out[i] = decode(bits[i], dtype);
 }
 
+/* ---- FP8 (e4m3) KV codes ----------------------------------------------- */
+/*
+ * Reading (the pages name an FP8 KV cache, "--kv-cache-dtype fp8", without a
+ * format): OCP e4m3 -- 1 sign bit, 4 exponent bits (bias 7), 3 fraction
+ * bits, no infinities, S.1111.111 is NaN, largest finite 448, subnormals
+ * fraction * 2^-9.  A cached value is stored as code = e4m3(x * inv_scale)
+ * with one per-tensor scale; x * inv_scale is one fp32 product, rounded to
+ * the nearest e4m3 value (ties to even), out-of-range finite values
+ * saturate to +-448, NaN stays NaN.  Dequantised value = e4m3 value * scale.
+ */
+static double decode_e4m3(uint8_t c)
+{
+    int sign = (c >> 7) & 1;
+    int expo = (c >> 3) & 0xf;
+    int frac = c & 0x7;
+    double mag;
+    if (expo == 15 && frac == 7)
+        return NAN;
+    if (expo == 0)
+        mag = ldexp((double)frac, -9);
+    else
+        mag = ldexp((double)(8 + frac), expo - 10);
+    return sign ? -mag : mag;
+}
+
+void oracle_decode_e4m3(double *out, const uint8_t *codes, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = decode_e4m3(codes[i]);
+}
+
+/* Nearest e4m3 code to a float (ties to even), saturating finite values:
+ * the value's binade fixes the spacing of representable values (2^-9 below
+ * 2^-6, else 2^(E-3) in [2^E, 2^(E+1))); the value is rounded to a multiple
+ * of that spacing, an even multiple on a tie (the code's last bit), and the
+ * multiple is written back as exponent and fraction. */
+static uint8_t encode_e4m3(float v)
+{
+    if (isnan(v))
+        return 0x7f;
+    uint8_t sign = signbit(v) ? 0x80 : 0x00;
+    double a = fabs((double)v);
+    if (a >= 448.0)
+        return sign | 0x7e; /* 448 = 1.75 * 2^8, the largest finite value */
+    double spacing;
+    if (a < ldexp(1.0, -6)) {
+        spacing = ldexp(1.0, -9);
+    } else {
+        int e;
+        frexp(a, &e); /* a in [2^(e-1), 2^e) */
+        spacing = ldexp(1.0, (e - 1) - 3);
+    }
+    double q = nearbyint(a / spacing); /* ties to even in the default mode */
+    double val = q * spacing;
+    if (val == 0.0)
+        return sign;
+    if (val < ldexp(1.0, -6))
+        return sign | (uint8_t)(val / ldexp(1.0, -9));
+    int e;
+    frexp(val, &e);
+    int E = e - 1; /* val in [2^E, 2^(E+1)) */
+    int mant = (int)(val / ldexp(1.0, E - 3)) - 8;
+    return sign | (uint8_t)(((E + 7) << 3) | mant);
+}
+
+/* codes[i] = e4m3(float(x[i]) * inv_scale), x 16-bit (dtype). */
+void oracle_quantize_e4m3(uint8_t *codes, const uint16_t *x, int64_t n, int dtype,
+                          float inv_scale)
+{
+    for (int64_t i = 0; i < n; ++i) {
+        float v = (float)decode(x[i], dtype);
+        float scaled = v * inv_scale;
+        codes[i] = encode_e4m3(scaled);
+    }
+}
+
 /* ---- slot mapping ([GAO] §1.5) ---------------------------------------- */
 
 /* Slot of one token: logical block = position / block_size, offset =
@@ -147,6 +223,29 @@ void oracle_reshape_and_cache(const uint16_t *key, const uint16_t *value,
                 value_cache[dst_i] = value[src_i];
             }
         }
+    }
+}
+
+/* FP8 pools: token t's K/V rows quantised with the per-tensor inverse
+ * scales and stored at its slot; negative slots are skipped. */
+void oracle_reshape_and_cache_fp8(const uint16_t *key, const uint16_t *value,
+                                  uint8_t *key_cache, uint8_t *value_cache,
+                                  const int64_t *slot_mapping, int num_tokens,
+                                  int num_kv_heads, int head_dim, int block_size,
+                                  int dtype, float k_inv_scale, float v_inv_scale)
+{
+    int64_t row_elems = (int64_t)num_kv_heads * head_dim;
+    for (int t = 0; t < num_tokens; ++t) {
+        int64_t slot = slot_mapping[t];
+        if (slot < 0)
+            continue;
+        int64_t block = slot / block_size;
+        int64_t offset = slot % block_size;
+        int64_t dst = (block * block_size + offset) * row_elems;
+        oracle_quantize_e4m3(key_cache + dst, key + (int64_t)t * row_elems, row_elems,
+                             dtype, k_inv_scale);
+        oracle_quantize_e4m3(value_cache + dst, value + (int64_t)t * row_elems, row_elems,
+                             dtype, v_inv_scale);
     }
 }
 
@@ -265,6 +364,74 @@ void oracle_paged_attention(double *out, const uint16_t *query,
                          h / group, num_kv_heads, head_dim, block_size, scale,
                          dtype);
         }
+    }
+}
+
+/* Paged attention over FP8 pools: K and V are the dequantised codes
+ * (code value * k_scale, * v_scale); everything else as above. */
+void oracle_paged_attention_fp8(double *out, const uint16_t *query,
+                                const uint8_t *key_cache, const uint8_t *value_cache,
+                                const int32_t *block_tables, int max_blocks_per_seq,
+                                const int32_t *context_lens, int num_seqs, int num_heads,
+                                int num_kv_heads, int head_dim, int block_size,
+                                double scale, int dtype, double k_scale, double v_scale,
+                                const int32_t *seq_subset, int n_subset)
+{
+    int group = num_heads / num_kv_heads;
+    int count = seq_subset ? n_subset : num_seqs;
+    for (int c = 0; c < count; ++c) {
+        int s = seq_subset ? seq_subset[c] : c;
+        const int32_t *row = block_tables + (int64_t)s * max_blocks_per_seq;
+        int64_t ctx = context_lens[s];
+        for (int h = 0; h < num_heads; ++h) {
+            double *o = out + ((int64_t)s * num_heads + h) * head_dim;
+            for (int i = 0; i < head_dim; ++i)
+                o[i] = 0.0;
+            if (ctx <= 0)
+                continue;
+            const uint16_t *q_row = query + ((int64_t)s * num_heads + h) * head_dim;
+            int kh = h / group;
+            double *scores = (double *)malloc(sizeof(double) * (size_t)ctx);
+            double m = -INFINITY;
+            for (int64_t p = 0; p < ctx; ++p) {
+                int64_t k = cache_row(row, p, kh, num_kv_heads, head_dim, block_size);
+                double dot = 0.0;
+                for (int i = 0; i < head_dim; ++i)
+                    dot += decode(q_row[i], dtype) * (decode_e4m3(key_cache[k + i]) * k_scale);
+                scores[p] = scale * dot;
+                if (scores[p] > m)
+                    m = scores[p];
+            }
+            double l = 0.0;
+            for (int64_t p = 0; p < ctx; ++p) {
+                scores[p] = exp(scores[p] - m);
+                l += scores[p];
+            }
+            for (int64_t p = 0; p < ctx; ++p) {
+                int64_t v = cache_row(row, p, kh, num_kv_heads, head_dim, block_size);
+                for (int i = 0; i < head_dim; ++i)
+                    o[i] += scores[p] * (decode_e4m3(value_cache[v + i]) * v_scale);
+            }
+            for (int i = 0; i < head_dim; ++i)
+                o[i] /= l;
+            free(scores);
+        }
+    }
+}
+
+/* Block copies of 1-byte (FP8) pools, pairs applied in order. */
+void oracle_copy_blocks_u8(uint8_t *key_cache, uint8_t *value_cache,
+                           const int32_t *block_mapping, int num_pairs, int block_size,
+                           int num_kv_heads, int head_dim)
+{
+    int64_t block_elems = (int64_t)block_size * num_kv_heads * head_dim;
+    for (int p = 0; p < num_pairs; ++p) {
+        int64_t src = block_mapping[2 * p];
+        int64_t dst = block_mapping[2 * p + 1];
+        memcpy(key_cache + dst * block_elems, key_cache + src * block_elems,
+               (size_t)block_elems);
+        memcpy(value_cache + dst * block_elems, value_cache + src * block_elems,
+               (size_t)block_elems);
     }
 }
 

@@ -449,4 +449,118 @@ def pin_empty_context(lib):
     assert oracle.num_partitions(0, 16, lib=lib) == 0
 
 
+# ---------------------------------------------------------------------------
+# FP8 (e4m3) KV cache
+
+def _torch_e4m3(x_f32: np.ndarray) -> np.ndarray:
+    """torch's float32 -> float8_e4m3fn codes (round to nearest even)."""
+    return torch.from_numpy(np.ascontiguousarray(x_f32, dtype=np.float32)).to(
+        torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
+def _e4m3_values() -> np.ndarray:
+    c = np.arange(256, dtype=np.uint8)
+    return torch.from_numpy(c).view(torch.float8_e4m3fn).double().numpy()
+
+
+def pin_e4m3_decode_exact(lib):
+    """Every e4m3 code decodes to torch's float8_e4m3fn value (NaN for
+    S.1111.111)."""
+    got = oracle.decode_e4m3(np.arange(256, dtype=np.uint8), lib=lib)
+    want = _e4m3_values()
+    nan = np.isnan(want)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], want[~nan])
+
+
+def pin_e4m3_encode_matches_torch(lib):
+    """Every finite fp16 value below 448 in magnitude (plenty of exact ties)
+    encodes to torch's round-to-nearest-even code; larger ones saturate to
+    +-448; NaN stays NaN."""
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    vals = bits.view(np.float16).astype(np.float32)
+    got = oracle.quantize_e4m3(bits, oracle.F16, 1.0, lib=lib)
+    fin = np.isfinite(vals)
+    small = fin & (np.abs(vals) < 448)
+    assert np.array_equal(got[small], _torch_e4m3(vals[small]))
+    big = fin & (np.abs(vals) >= 448)
+    assert np.array_equal(got[big], np.where(vals[big] > 0, 0x7E, 0xFE).astype(np.uint8))
+    assert (got[np.isnan(vals)] & 0x7F == 0x7F).all()
+
+
+def pin_e4m3_encode_nearest_brute_force(lib):
+    """Encoding picks the nearest representable value (ties to the even
+    code), checked against an exhaustive nearest search, including the
+    fp32 product with a non-trivial inverse scale."""
+    rng = np.random.default_rng(47)
+    x = f16_bits(np.concatenate([rng.standard_normal(3000) * 50,
+                                 rng.standard_normal(1000) * 0.01]))
+    inv = np.float32(1.0) / np.float32(0.37)
+    got = oracle.quantize_e4m3(x, oracle.F16, float(inv), lib=lib)
+    v = (f16_vals(x).astype(np.float32) * inv).astype(np.float64)
+    table = _e4m3_values()
+    codes = np.arange(127)                       # non-negative finite codes
+    mags = table[codes]
+    want = []
+    for a in v:
+        m = min(abs(a), 448.0)
+        err = np.abs(mags - m)
+        best = np.flatnonzero(err == err.min())
+        c = int(best[0]) if len(best) == 1 else int(best[best % 2 == 0][0])
+        want.append(c | (0x80 if (a < 0 or (a == 0 and np.signbit(a))) else 0))
+    assert np.array_equal(got, np.asarray(want, dtype=np.uint8))
+
+
+def pin_fp8_reshape_and_cache(lib):
+    """FP8 cache write: gathering whole blocks in table order gives back the
+    codes torch makes from float(x) * (1/scale) in fp32."""
+    rng = np.random.default_rng(53)
+    bs, Hkv, d, N = 4, 2, 8, 9
+    ctx = 11
+    table = np.array([[6, 1, 4]], dtype=np.int32)
+    key = bf16_bits(rng.standard_normal((ctx, Hkv, d)) * 3)
+    val = bf16_bits(rng.standard_normal((ctx, Hkv, d)) * 3)
+    ks, vs = 0.02, 0.015
+    kc = np.zeros((N, bs, Hkv, d), np.uint8)
+    vc = np.zeros((N, bs, Hkv, d), np.uint8)
+    slots = oracle.slot_mapping(table, np.zeros(ctx, np.int32), np.arange(ctx, dtype=np.int32),
+                                bs, lib=lib)
+    oracle.reshape_and_cache_fp8(key, val, kc, vc, slots, oracle.BF16, ks, vs, lib=lib)
+    dec = _dec("bf16")
+    for pool, src, sc in ((kc, key, ks), (vc, val, vs)):
+        gathered = np.concatenate([pool[b] for b in table[0]])[:ctx]
+        inv = np.float32(1.0) / np.float32(sc)
+        want = _torch_e4m3(np.clip(dec(src).astype(np.float32) * inv, -448, 448))
+        assert np.array_equal(gathered, want)
+
+
+def pin_fp8_attention_matches_sdpa(lib):
+    """Attention over FP8 pools equals torch's float64 attention on the
+    dequantised K and V (codes from torch's conversion)."""
+    rng = np.random.default_rng(59)
+    H, Hkv, d, bs = 4, 2, 16, 4
+    ctxs = [1, 6, 13]
+    ks, vs = 0.011, 0.013
+    perm = rng.permutation(12)
+    tables = np.array([perm[0:4], perm[4:8], perm[8:12]], dtype=np.int32)
+    kl = [_torch_e4m3(rng.standard_normal((c, Hkv, d)).astype(np.float32) * 60) for c in ctxs]
+    vl = [_torch_e4m3(rng.standard_normal((c, Hkv, d)).astype(np.float32) * 60) for c in ctxs]
+    q = bf16_bits(rng.standard_normal((3, H, d)))
+    kc = place_sequences(kl, tables, 12, bs, fill=np.uint8(0x7F)).astype(np.uint8)
+    vc = place_sequences(vl, tables, 12, bs, fill=np.uint8(0x7F)).astype(np.uint8)
+    got = oracle.paged_attention_fp8(q, kc, vc, tables, ctxs, 0.25, oracle.BF16, ks, vs,
+                                     lib=lib)
+    table = _e4m3_values()
+    want = np.zeros_like(got)
+    for i in range(3):
+        kd = torch.from_numpy(table[kl[i]] * float(np.float32(ks)))
+        vd = torch.from_numpy(table[vl[i]] * float(np.float32(vs)))
+        kd = kd.permute(1, 0, 2).repeat_interleave(H // Hkv, 0)
+        vd = vd.permute(1, 0, 2).repeat_interleave(H // Hkv, 0)
+        qd = torch.from_numpy(_dec("bf16")(q[i]))[:, None, :]
+        want[i] = torch.nn.functional.scaled_dot_product_attention(
+            qd[None], kd[None], vd[None], scale=0.25)[0, :, 0, :].numpy()
+    _close(got, want, 1e-11, 1e-12, "fp8 sdpa")
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -89,6 +89,24 @@ MUTANTS = [
     ("empty_context_not_zero",
      "            if (ctx <= 0) {\n                for (int i = 0; i < head_dim; ++i)\n                    o[i] = 0.0;",
      "            if (ctx <= 0) {\n                for (int i = 0; i < head_dim; ++i)\n                    o[i] = 1.0;", 0),
+    ("e4m3_decode_bias",
+     "mag = ldexp((double)(8 + frac), expo - 10);",
+     "mag = ldexp((double)(8 + frac), expo - 11);", 0),
+    ("e4m3_encode_truncates",
+     "double q = nearbyint(a / spacing);",
+     "double q = floor(a / spacing);", 0),
+    ("e4m3_saturates_low",
+     "        return sign | 0x7e; /* 448 = 1.75 * 2^8, the largest finite value */",
+     "        return sign | 0x7d; /* 448 = 1.75 * 2^8, the largest finite value */", 0),
+    ("fp8_attention_drops_k_scale",
+     "dot += decode(q_row[i], dtype) * (decode_e4m3(key_cache[k + i]) * k_scale);",
+     "dot += decode(q_row[i], dtype) * decode_e4m3(key_cache[k + i]);", 0),
+    ("fp8_attention_value_scale_is_k_scale",
+     "o[i] += scores[p] * (decode_e4m3(value_cache[v + i]) * v_scale);",
+     "o[i] += scores[p] * (decode_e4m3(value_cache[v + i]) * k_scale);", 0),
+    ("fp8_cache_swaps_scales",
+     "                             dtype, k_inv_scale);",
+     "                             dtype, v_inv_scale);", 0),
 ]
 
 RUNNER = r"""
