@@ -50,7 +50,8 @@ def parse_args(argv=None):
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--config", default="gqa70b",
-                    choices=["tiny", "mha7b", "gqa70b", "longctx", "prefix"])
+                    choices=["tiny", "mha7b", "gqa70b", "longctx", "prefix", "gqa70b-fp8",
+                             "longctx-fp8"])
     ap.add_argument("--partition", type=int, default=None,
                     help="split-context partition tokens (0 = single pass)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
@@ -181,32 +182,66 @@ def workload_config(w, partition_size, world=1):
         "context_tokens": int(w.context_lens.sum()), "kv_bytes_per_step": kv,
         "l2": f"inputs larger than L2: {kv / 1e9:.2f} GB of K/V read per step; no flush",
         "parallelism": "replicas" if world > 1 else "single GPU",
+        "kv_cache_dtype": "fp8-e4m3" if w.fp8 else w.dtype,
     }
+
+
+class OracleCache:
+    """The oracle's own pools for a workload (history written through its
+    slot mapping and cache write) and its step operations, 16-bit or FP8."""
+
+    def __init__(self, w):
+        import oracle
+        self.o, self.w = oracle, w
+        self.dt = oracle.F16 if w.dtype == "f16" else oracle.BF16
+        self.kc, self.vc = w.empty_pools()
+        slots = oracle.slot_mapping(w.block_tables, w.hist_seq, w.hist_pos, w.bs)
+        self.write(w.hist_key, w.hist_value, slots)
+
+    def write(self, k, v, slots):
+        o, w = self.o, self.w
+        if w.fp8:
+            o.reshape_and_cache_fp8(k, v, self.kc, self.vc, slots, self.dt, w.spec.kv_scale,
+                                    w.spec.kv_scale)
+        else:
+            o.reshape_and_cache(k, v, self.kc, self.vc, slots)
+
+    def new_tokens(self, seqs):
+        o, w = self.o, self.w
+        seqs = np.asarray(seqs, dtype=np.int32)
+        sl = o.slot_mapping(w.block_tables, w.new_seq[seqs], w.new_pos[seqs], w.bs)
+        self.write(w.new_key[seqs], w.new_value[seqs], sl)
+
+    def copy_blocks(self):
+        o, w = self.o, self.w
+        if w.cow_pairs.shape[0]:
+            (o.copy_blocks_u8 if w.fp8 else o.copy_blocks)(self.kc, self.vc, w.cow_pairs)
+
+    def attention(self, seqs):
+        o, w = self.o, self.w
+        if w.fp8:
+            return o.paged_attention_fp8(w.query, self.kc, self.vc, w.step_block_tables,
+                                         w.context_lens, w.scale, self.dt, w.spec.kv_scale,
+                                         w.spec.kv_scale, seqs=seqs)
+        return o.paged_attention(w.query, self.kc, self.vc, w.step_block_tables,
+                                 w.context_lens, w.scale, self.dt, seqs=seqs)
 
 
 def cpu_baseline_sample(w, target_s: float):
     """Time the oracle's step (new-token writes + attention) on the first
     sequences of the workload until about target_s seconds of CPU work."""
-    import oracle
-    kc, vc = w.empty_pools()
-    dt = oracle.F16 if w.dtype == "f16" else oracle.BF16
-    slots = oracle.slot_mapping(w.block_tables, w.hist_seq, w.hist_pos, w.bs)
-    oracle.reshape_and_cache(w.hist_key, w.hist_value, kc, vc, slots)
+    oc = OracleCache(w)
     done, tokens, elapsed = [], 0, 0.0
-    order = list(range(w.S))
-    for s in order:
+    for s in range(w.S):
         t0 = time.perf_counter()
-        sl = oracle.slot_mapping(w.block_tables, w.new_seq[s:s + 1], w.new_pos[s:s + 1],
-                                 w.bs)
-        oracle.reshape_and_cache(w.new_key[s:s + 1], w.new_value[s:s + 1], kc, vc, sl)
-        oracle.paged_attention(w.query, kc, vc, w.step_block_tables, w.context_lens,
-                               w.scale, dt, seqs=[s])
+        oc.new_tokens([s])
+        oc.attention([s])
         elapsed += time.perf_counter() - t0
         done.append(s)
         tokens += int(w.context_lens[s])
         if elapsed >= target_s:
             break
-    kv = tokens * w.Hkv * w.D * 2 * 2
+    kv = tokens * w.Hkv * w.D * 2 * w.kv_elem_bytes
     return {"value": kv / elapsed / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
             "sample": f"{len(done)} of {w.S} sequences ({tokens} attended tokens): "
                       f"new-token write + fp64 attention, single-threaded C, "
@@ -220,17 +255,11 @@ def run_reference(args):
     if rank != 0:
         return
     from paged_kv_cache_96_gb300 import workloads as W
-    import oracle
     w = W.build(W.CONFIGS[args.config])
-    kc, vc = w.empty_pools()
-    dt = oracle.F16 if w.dtype == "f16" else oracle.BF16
-    slots = oracle.slot_mapping(w.block_tables, w.hist_seq, w.hist_pos, w.bs)
-    oracle.reshape_and_cache(w.hist_key, w.hist_value, kc, vc, slots)
+    oc = OracleCache(w)
     # per step: a bounded sample of sequences sized for ~2 s of CPU work
-    per_seq = []
     t0 = time.perf_counter()
-    oracle.paged_attention(w.query, kc, vc, w.step_block_tables, w.context_lens, w.scale,
-                           dt, seqs=[0])
+    oc.attention([0])
     per_tok = (time.perf_counter() - t0) / max(1, int(w.context_lens[0]))
     budget = 2.0
     sample, toks = [], 0
@@ -239,22 +268,18 @@ def run_reference(args):
             break
         sample.append(s)
         toks += int(w.context_lens[s])
-    sub_seq = np.asarray(sample, dtype=np.int32)
 
     def step():
-        sl = oracle.slot_mapping(w.block_tables, w.new_seq[sub_seq], w.new_pos[sub_seq], w.bs)
-        oracle.reshape_and_cache(w.new_key[sub_seq], w.new_value[sub_seq], kc, vc, sl)
-        if w.cow_pairs.shape[0]:
-            oracle.copy_blocks(kc, vc, w.cow_pairs)
-        oracle.paged_attention(w.query, kc, vc, w.step_block_tables, w.context_lens,
-                               w.scale, dt, seqs=sample)
+        oc.new_tokens(sample)
+        oc.copy_blocks()
+        oc.attention(sample)
     for _ in range(args.warmup):
         step()
     t0 = time.perf_counter()
     for _ in range(args.steps):
         step()
     el = time.perf_counter() - t0
-    kv = toks * w.Hkv * w.D * 2 * 2
+    kv = toks * w.Hkv * w.D * 2 * w.kv_elem_bytes
     val = kv * args.steps / el / 1e9
     line = {
         "impl": "reference", "metric": METRIC, "value": val, "unit": "GB/s",
@@ -368,7 +393,9 @@ def run_ours(args):
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": per_step * 1e3, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "fp8-e4m3 KV, fp16 MMA, fp32 accumulate" if w.fp8 else w.dtype,
+        "data": "synthetic",
         "config": workload_config(w, st.partition_size, world),
         "pct_of_hbm_peak_8tbps": 100.0 * value / world / NOMINAL_HBM_GBS,
         "pct_of_hbm_measured": 100.0 * value / world / peak,

@@ -60,7 +60,11 @@ typedef enum {
     PA_ERR_CUDA = 4          /* a CUDA runtime/driver call failed */
 } pa_status;
 
-typedef enum { PA_F16 = 0, PA_BF16 = 1 } pa_dtype;
+typedef enum {
+    PA_F16 = 0,      /* IEEE binary16 */
+    PA_BF16 = 1,     /* bfloat16 */
+    PA_FP8_E4M3 = 2  /* 1-byte e4m3 KV codes (pools only; see the FP8 calls) */
+} pa_dtype;
 
 /* Bits OR-ed into the optional device error word. */
 #define PA_DEVERR_SLOT_RANGE    0x01 /* slot >= num_blocks * block_size */
@@ -103,13 +107,34 @@ PA_API pa_status pa_reshape_and_cache(const void *key, const void *value,
                                int32_t *error_word, void *stream);
 
 /*
+ * pa_reshape_and_cache_fp8 -- the FP8 KV cache of the deployment options in
+ * [FEI] ("--kv-cache-dtype fp8"): as pa_reshape_and_cache, but the pools
+ * hold 1-byte e4m3 codes (OCP e4m3: bias 7, no infinities, largest finite
+ * 448) with one scale per pool.  For every element
+ *     code = e4m3(float(x) * inv),   inv = 1.0f / scale (fp32),
+ * the product rounded once in fp32, then to the nearest e4m3 value (ties to
+ * even), finite values beyond +-448 saturating; the cached value stands for
+ * e4m3(code) * scale.  key, value: [num_tokens][num_kv_heads][head_dim] of
+ * src_dtype (PA_F16 or PA_BF16); key_cache, value_cache: uint8
+ * [num_blocks][block_size][num_kv_heads][head_dim].  Scales must be finite
+ * and > 0.  Slot rules as pa_reshape_and_cache.
+ */
+PA_API pa_status pa_reshape_and_cache_fp8(const void *key, const void *value,
+                                          void *key_cache, void *value_cache,
+                                          const int32_t *slot_mapping, int num_tokens,
+                                          int num_blocks, int block_size, int num_kv_heads,
+                                          int head_dim, pa_dtype src_dtype, float k_scale,
+                                          float v_scale, int32_t *error_word, void *stream);
+
+/*
  * pa_copy_blocks -- the "copy the contents" step of copy-on-write
  * ([LAKE] §3.2).  block_mapping: int32 [num_pairs][2] = (src, dst); for every
  * pair, K block dst := K block src and V block dst := V block src (whole
  * blocks of block_size * num_kv_heads * head_dim elements).  No block may be
  * both a source and a destination, and destinations must be distinct;
  * otherwise the result is unspecified.  A pair with a block outside
- * [0, num_blocks) is skipped and sets PA_DEVERR_PAIR_RANGE.
+ * [0, num_blocks) is skipped and sets PA_DEVERR_PAIR_RANGE.  dtype gives the
+ * element size: 2 bytes for PA_F16 / PA_BF16, 1 byte for PA_FP8_E4M3 pools.
  */
 PA_API pa_status pa_copy_blocks(void *key_cache, void *value_cache,
                          const int32_t *block_mapping, int num_pairs,
@@ -171,6 +196,26 @@ PA_API pa_status pa_decode_attention(void *out, const void *query,
                               float scale, int partition_size, void *workspace,
                               size_t workspace_bytes, pa_dtype dtype,
                               int32_t *error_word, void *stream);
+
+/*
+ * pa_decode_attention_fp8 -- pa_decode_attention over FP8 pools written by
+ * pa_reshape_and_cache_fp8: K and V elements are e4m3 codes standing for
+ * e4m3(code) * k_scale and * v_scale.  query and out are dtype (PA_F16 or
+ * PA_BF16).  Codes are widened to fp16 and the query is rounded to fp16 for
+ * the tensor-core products (|q| must stay below 65504); scores and weights
+ * accumulate in fp32 as in pa_decode_attention; the V scale is applied to
+ * the output.  Workspace, partitions and errors as pa_decode_attention
+ * (same workspace size).  Supported: head_dim 128.
+ */
+PA_API pa_status pa_decode_attention_fp8(void *out, const void *query, const void *key_cache,
+                                         const void *value_cache, const int32_t *block_tables,
+                                         int max_blocks_per_seq, const int32_t *context_lens,
+                                         int max_context_len, int num_seqs, int num_heads,
+                                         int num_kv_heads, int head_dim, int block_size,
+                                         int num_blocks, float scale, float k_scale,
+                                         float v_scale, int partition_size, void *workspace,
+                                         size_t workspace_bytes, pa_dtype dtype,
+                                         int32_t *error_word, void *stream);
 
 /*
  * pa_decode_attention_noalloc -- no counterpart on the pages: an addition

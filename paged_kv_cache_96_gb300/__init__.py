@@ -15,6 +15,7 @@ from __future__ import annotations
 __all__ = [
     "pa_slot_mapping", "pa_reshape_and_cache", "pa_copy_blocks",
     "pa_decode_attention", "pa_decode_workspace_bytes", "PAError",
+    "pa_reshape_and_cache_fp8", "pa_decode_attention_fp8", "pa_decode_attention_noalloc",
     "library_path",
 ]
 

@@ -20,7 +20,7 @@ _LIB_PATH = os.environ.get("PA_LIBRARY",
                            os.path.join(_HERE, "lib", "libpaged_attention.so"))
 
 PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_WORKSPACE, PA_ERR_CUDA = range(5)
-PA_F16, PA_BF16 = 0, 1
+PA_F16, PA_BF16, PA_FP8_E4M3 = 0, 1, 2
 
 DEVERR_SLOT_RANGE = 0x01
 DEVERR_BLOCK_RANGE = 0x02
@@ -60,6 +60,10 @@ def _load() -> ctypes.CDLL:
                                       i32, i32, f32, i32, P, sz, i32, P, P]),
         "pa_decode_attention_noalloc": (i32, [P, P, P, P, P, i32, P, i32, i32, i32, i32,
                                               i32, i32, i32, f32, i32, i32, P, P]),
+        "pa_reshape_and_cache_fp8": (i32, [P, P, P, P, P, i32, i32, i32, i32, i32, i32, f32,
+                                           f32, P, P]),
+        "pa_decode_attention_fp8": (i32, [P, P, P, P, P, i32, P, i32, i32, i32, i32, i32,
+                                          i32, i32, f32, f32, f32, i32, P, sz, i32, P, P]),
         "pa_status_string": (ctypes.c_char_p, [i32]),
         "pa_last_cuda_error": (ctypes.c_char_p, []),
         "pa_version": (i32, []),
@@ -86,7 +90,9 @@ def _dtype_code(t: torch.Tensor) -> int:
         return PA_F16
     if t.dtype == torch.bfloat16:
         return PA_BF16
-    raise TypeError(f"16-bit float tensor expected, got {t.dtype}")
+    if t.dtype == torch.uint8:
+        return PA_FP8_E4M3
+    raise TypeError(f"fp16 / bf16 tensor (or uint8 FP8 pool) expected, got {t.dtype}")
 
 
 def _dev(t: torch.Tensor, name: str, dtype: Optional[torch.dtype] = None):
@@ -185,6 +191,8 @@ def pa_decode_attention(out: torch.Tensor, query: torch.Tensor,
     if workspace is not None:
         ws_ptr = _dev(workspace, "workspace")
         ws_bytes = workspace.numel() * workspace.element_size()
+    if key_cache.dtype == torch.uint8:
+        raise TypeError("FP8 pools: use pa_decode_attention_fp8")
     _check("pa_decode_attention", _lib.pa_decode_attention(
         _dev(out, "out", query.dtype), _dev(query, "query", key_cache.dtype),
         _dev(key_cache, "key_cache"), _dev(value_cache, "value_cache", key_cache.dtype),
@@ -217,6 +225,51 @@ def pa_decode_attention_noalloc(out: torch.Tensor, query: torch.Tensor,
 
 
 NOALLOC_WORKSPACE_BYTES = 32 * 1024 * 1024
+
+
+def pa_reshape_and_cache_fp8(key: torch.Tensor, value: torch.Tensor,
+                             key_cache: torch.Tensor, value_cache: torch.Tensor,
+                             slot_mapping: torch.Tensor, k_scale: float, v_scale: float,
+                             error_word: Optional[torch.Tensor] = None,
+                             stream=None) -> None:
+    """Quantise key/value [T, Hkv, d] (fp16/bf16) into uint8 e4m3 pools."""
+    T, Hkv, d = key.shape
+    N, bs, Hkv2, d2 = key_cache.shape
+    if (Hkv, d) != (Hkv2, d2) or value.shape != key.shape or value_cache.shape != key_cache.shape:
+        raise ValueError("shape mismatch between new tokens and pools")
+    _check("pa_reshape_and_cache_fp8", _lib.pa_reshape_and_cache_fp8(
+        _dev(key, "key"), _dev(value, "value", key.dtype),
+        _dev(key_cache, "key_cache", torch.uint8), _dev(value_cache, "value_cache", torch.uint8),
+        _dev(slot_mapping, "slot_mapping", torch.int32), T, N, bs, Hkv, d, _dtype_code(key),
+        float(k_scale), float(v_scale), _opt(error_word, "error_word"), _stream(stream)))
+
+
+def pa_decode_attention_fp8(out: torch.Tensor, query: torch.Tensor,
+                            key_cache: torch.Tensor, value_cache: torch.Tensor,
+                            block_tables: torch.Tensor, context_lens: torch.Tensor,
+                            max_context_len: int, scale: float, k_scale: float,
+                            v_scale: float, partition_size: int = 0,
+                            workspace: Optional[torch.Tensor] = None,
+                            error_word: Optional[torch.Tensor] = None,
+                            stream=None) -> None:
+    """Paged decode attention over uint8 e4m3 pools."""
+    S, H, d = query.shape
+    N, bs, Hkv, d2 = key_cache.shape
+    MB = block_tables.shape[1]
+    if d != d2 or out.shape != query.shape:
+        raise ValueError("shape mismatch")
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not None:
+        ws_ptr = _dev(workspace, "workspace")
+        ws_bytes = workspace.numel() * workspace.element_size()
+    _check("pa_decode_attention_fp8", _lib.pa_decode_attention_fp8(
+        _dev(out, "out", query.dtype), _dev(query, "query"),
+        _dev(key_cache, "key_cache", torch.uint8), _dev(value_cache, "value_cache", torch.uint8),
+        _dev(block_tables, "block_tables", torch.int32), MB,
+        _dev(context_lens, "context_lens", torch.int32), int(max_context_len), S, H, Hkv,
+        d, bs, N, float(scale), float(k_scale), float(v_scale), int(partition_size),
+        ws_ptr, ws_bytes, _dtype_code(query), _opt(error_word, "error_word"),
+        _stream(stream)))
 
 
 def alloc_workspace(num_seqs: int, num_heads: int, num_kv_heads: int, head_dim: int,

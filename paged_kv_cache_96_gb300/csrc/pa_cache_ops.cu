@@ -6,7 +6,13 @@
 #include <cstdio>
 #include <cstring>
 
+#include <cmath>
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
 #include "pa_common.cuh"
+#include "pa_ptx.cuh"
 
 namespace pa {
 
@@ -87,6 +93,53 @@ __global__ void reshape_and_cache_kernel(const uint4 *__restrict__ key,
         const uint4 v = __ldg(vs + i);
         kd[i] = k;
         vd[i] = v;
+    }
+}
+
+// ---- reshape_and_cache into FP8 (e4m3) pools ----------------------------------
+
+__device__ __forceinline__ float to_float(__nv_bfloat16 x) { return __bfloat162float(x); }
+__device__ __forceinline__ float to_float(__half x) { return __half2float(x); }
+
+// One CTA per token; each thread converts 8 elements at a time: 16 bytes of
+// 16-bit input -> 8 bytes of e4m3 codes, code = e4m3(float(x) * inv_scale).
+template <typename T>
+__global__ void reshape_and_cache_fp8_kernel(const uint4 *__restrict__ key,
+                                             const uint4 *__restrict__ value,
+                                             uint2 *__restrict__ key_cache,
+                                             uint2 *__restrict__ value_cache,
+                                             const int32_t *__restrict__ slot_mapping,
+                                             int64_t num_slots, int words_per_token,
+                                             float k_inv_scale, float v_inv_scale,
+                                             int32_t *error_word)
+{
+    pdl_wait_primary();
+    pdl_launch_dependents();
+    const int t = blockIdx.x;
+    const int64_t slot = slot_mapping[t];
+    if (slot < 0)
+        return;
+    if (slot >= num_slots) {
+        if (threadIdx.x == 0)
+            flag_error(error_word, PA_DEVERR_SLOT_RANGE);
+        return;
+    }
+    auto quantise = [](uint4 w, float inv) {
+        const T *e = reinterpret_cast<const T *>(&w);
+        uint2 out;
+        out.x = (uint32_t)f32x2_to_e4m3x2(to_float(e[0]) * inv, to_float(e[1]) * inv) |
+                ((uint32_t)f32x2_to_e4m3x2(to_float(e[2]) * inv, to_float(e[3]) * inv) << 16);
+        out.y = (uint32_t)f32x2_to_e4m3x2(to_float(e[4]) * inv, to_float(e[5]) * inv) |
+                ((uint32_t)f32x2_to_e4m3x2(to_float(e[6]) * inv, to_float(e[7]) * inv) << 16);
+        return out;
+    };
+    const uint4 *ks = key + static_cast<int64_t>(t) * words_per_token;
+    const uint4 *vs = value + static_cast<int64_t>(t) * words_per_token;
+    uint2 *kd = key_cache + slot * words_per_token;
+    uint2 *vd = value_cache + slot * words_per_token;
+    for (int i = threadIdx.x; i < words_per_token; i += blockDim.x) {
+        kd[i] = quantise(__ldg(ks + i), k_inv_scale);
+        vd[i] = quantise(__ldg(vs + i), v_inv_scale);
     }
 }
 
@@ -187,6 +240,48 @@ extern "C" pa_status pa_reshape_and_cache(const void *key, const void *value,
                       static_cast<int64_t>(num_blocks) * block_size, words, error_word);
 }
 
+extern "C" pa_status pa_reshape_and_cache_fp8(const void *key, const void *value,
+                                              void *key_cache, void *value_cache,
+                                              const int32_t *slot_mapping, int num_tokens,
+                                              int num_blocks, int block_size,
+                                              int num_kv_heads, int head_dim,
+                                              pa_dtype src_dtype, float k_scale,
+                                              float v_scale, int32_t *error_word,
+                                              void *stream)
+{
+    if (num_tokens < 0 || num_blocks <= 0 || block_size <= 0 || num_kv_heads <= 0 ||
+        head_dim <= 0 || (src_dtype != PA_F16 && src_dtype != PA_BF16) ||
+        !std::isfinite(k_scale) || !std::isfinite(v_scale) || k_scale <= 0.f ||
+        v_scale <= 0.f)
+        return PA_ERR_INVALID_ARG;
+    if (num_tokens == 0)
+        return PA_OK;
+    if (!key || !value || !key_cache || !value_cache || !slot_mapping)
+        return PA_ERR_INVALID_ARG;
+    if (!aligned16(key) || !aligned16(value) || !aligned16(key_cache) ||
+        !aligned16(value_cache))
+        return PA_ERR_INVALID_ARG;
+    const int64_t row_elems = static_cast<int64_t>(num_kv_heads) * head_dim;
+    if (row_elems % 8 != 0)
+        return PA_ERR_UNSUPPORTED;
+    const int words = static_cast<int>(row_elems / 8);
+    const int threads = words >= 256 ? 256 : ((words + 31) / 32) * 32;
+    const float k_inv = 1.0f / k_scale;  // fp32, as the codes' contract states
+    const float v_inv = 1.0f / v_scale;
+    const int64_t slots = static_cast<int64_t>(num_blocks) * block_size;
+    if (src_dtype == PA_BF16)
+        return launch_pdl(reshape_and_cache_fp8_kernel<__nv_bfloat16>, dim3(num_tokens),
+                          dim3(threads), 0, as_stream(stream), static_cast<const uint4 *>(key),
+                          static_cast<const uint4 *>(value), static_cast<uint2 *>(key_cache),
+                          static_cast<uint2 *>(value_cache), slot_mapping, slots, words, k_inv,
+                          v_inv, error_word);
+    return launch_pdl(reshape_and_cache_fp8_kernel<__half>, dim3(num_tokens), dim3(threads), 0,
+                      as_stream(stream), static_cast<const uint4 *>(key),
+                      static_cast<const uint4 *>(value), static_cast<uint2 *>(key_cache),
+                      static_cast<uint2 *>(value_cache), slot_mapping, slots, words, k_inv,
+                      v_inv, error_word);
+}
+
 extern "C" pa_status pa_copy_blocks(void *key_cache, void *value_cache,
                                     const int32_t *block_mapping, int num_pairs,
                                     int num_blocks, int block_size, int num_kv_heads,
@@ -194,7 +289,7 @@ extern "C" pa_status pa_copy_blocks(void *key_cache, void *value_cache,
                                     void *stream)
 {
     if (num_pairs < 0 || num_blocks <= 0 || block_size <= 0 || num_kv_heads <= 0 ||
-        head_dim <= 0 || (dtype != PA_F16 && dtype != PA_BF16))
+        head_dim <= 0 || (dtype != PA_F16 && dtype != PA_BF16 && dtype != PA_FP8_E4M3))
         return PA_ERR_INVALID_ARG;
     if (num_pairs == 0)
         return PA_OK;
@@ -202,8 +297,9 @@ extern "C" pa_status pa_copy_blocks(void *key_cache, void *value_cache,
         return PA_ERR_INVALID_ARG;
     if (!aligned16(key_cache) || !aligned16(value_cache))
         return PA_ERR_INVALID_ARG;
+    const int64_t elem_bytes = dtype == PA_FP8_E4M3 ? 1 : 2;
     const int64_t block_bytes =
-        static_cast<int64_t>(block_size) * num_kv_heads * head_dim * 2;
+        static_cast<int64_t>(block_size) * num_kv_heads * head_dim * elem_bytes;
     if (block_bytes % 16 != 0)
         return PA_ERR_UNSUPPORTED;
     const int64_t words = block_bytes / 16;

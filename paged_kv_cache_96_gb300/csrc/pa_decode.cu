@@ -38,45 +38,23 @@
 //    wait on a stage is bounded in time.
 #include <cuda.h>
 
+#include <type_traits>
+
 #include <algorithm>
 #include <cmath>
 #include <cstdio>
 #include <mutex>
 
-#include "pa_common.cuh"
-#include "pa_ptx.cuh"
+#include "pa_decode_common.cuh"
 
 namespace pa {
 
-constexpr int kTileTokens = 16;
-constexpr uint64_t kWaitLimitNs = 1000000000ull;  // one second per stage wait
-constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kLn2 = 0.6931471805599453f;
-constexpr unsigned kFull = 0xffffffffu;
-constexpr float kSlack = 8.f;  // log2 units: softmax weights stay <= 256 before rescaling
-
-struct DecodeParams {
-    void *out;
-    const void *query;
-    const int32_t *block_tables;
-    const int32_t *context_lens;
-    float *part_m;
-    float *part_l;
-    float *part_o;
-    int32_t *error_word;
-    int num_seqs, num_heads, num_kv_heads, group;
-    int max_blocks_per_seq, num_blocks, block_size, max_context_len;
-    int block_shift;  // log2(block_size)
-    int part_tokens;  // tokens per work unit (a multiple of 16)
-    int max_parts;    // partitions per sequence the workspace holds
-    float scale_log2; // scale * log2(e)
-};
-
 // Shared-memory layout (offsets from a 1024-byte aligned base): NW warps,
-// each with a private ring of NST stages.
-template <int D, int NT, int NW, int NST> struct Layout {
-    static constexpr int kHalfBytes = kTileTokens * 128;      // 16 rows x 64 elements
-    static constexpr int kTileBytes = (D / 64) * kHalfBytes;  // one K (or V) tile
+// each with a private ring of NST stages.  EB = bytes per cached element
+// (2 for fp16/bf16 pools, 1 for FP8 pools).
+template <int D, int NT, int NW, int NST, int EB> struct Layout {
+    static constexpr int kHalfBytes = kTileTokens * 128;      // 16 rows x 64 elements (EB 2)
+    static constexpr int kTileBytes = kTileTokens * D * EB;   // one K (or V) tile
     static constexpr int kStageBytes = 2 * kTileBytes;        // K tile + V tile
     static constexpr int kHeads = 8 * NT;
     static constexpr int kPitch = D + 4;  // floats per merge row (bank spread)
@@ -92,27 +70,20 @@ template <int D, int NT, int NW, int NST> struct Layout {
     static_assert(kStageBytes % 1024 == 0, "stages must keep 1024-byte alignment");
 };
 
-// Clamped context length (same rule in both kernels).
-__device__ __forceinline__ int clamp_context(const DecodeParams &p, int s, bool flag)
-{
-    const int limit = min(p.max_context_len, p.max_blocks_per_seq * p.block_size);
-    int c = p.context_lens[s];
-    if (c < 0 || c > limit) {
-        if (flag)
-            flag_error(p.error_word, PA_DEVERR_CONTEXT_RANGE);
-        c = c < 0 ? 0 : limit;
-    }
-    return c;
-}
-
-template <typename T, int D, int NT, int NW, int NST>
+// T: query/output type.  KV: cached element type -- T itself, or uint8_t
+// for FP8 (e4m3) pools, whose tiles are widened to fp16 in registers (the
+// tensor-core products then run in fp16).
+template <typename T, typename KV, int D, int NT, int NW, int NST>
 __global__ void __launch_bounds__(NW * 32, 1)
     paged_decode_kernel(const __grid_constant__ DecodeParams p,
                         const __grid_constant__ CUtensorMap tmap_k,
                         const __grid_constant__ CUtensorMap tmap_v)
 {
-    using L = Layout<D, NT, NW, NST>;
-    using Op = MmaOp<T>;
+    constexpr bool kFp8 = sizeof(KV) == 1;
+    static_assert(!kFp8 || D == 128, "FP8 pools are supported with head_dim 128");
+    using L = Layout<D, NT, NW, NST, sizeof(KV)>;
+    using MT = typename std::conditional<kFp8, __half, T>::type;  // tensor-core input type
+    using Op = MmaOp<MT>;
     constexpr int KT = D / 16;  // k-steps of the score product, m-tiles of the output
     constexpr int kHeads = L::kHeads;
     constexpr int kThreads = NW * 32;
@@ -257,6 +228,12 @@ __global__ void __launch_bounds__(NW * 32, 1)
             if (ok) {
                 const uint32_t dst = stage_of(stage);
                 mbar_arrive_expect_tx(bar_of(stage), L::kStageBytes);
+                if constexpr (kFp8) {
+                    // one 128-byte row per token: a 2 KB box per tile and tensor
+                    tma_load_4d(dst, &tmap_k, bar_of(stage), 0, pkh, prow, pphys);
+                    tma_load_4d(dst + L::kTileBytes, &tmap_v, bar_of(stage), 0, pkh, prow,
+                                pphys);
+                } else {
 #if PA_DECODE_PACKED5D
                 tma_load_5d(dst, &tmap_k, bar_of(stage), 0, 0, pkh, prow, pphys);
                 tma_load_5d(dst + L::kTileBytes, &tmap_v, bar_of(stage), 0, 0, pkh, prow, pphys);
@@ -269,6 +246,7 @@ __global__ void __launch_bounds__(NW * 32, 1)
                                 bar_of(stage), hf * 64, pkh, prow, pphys);
                 }
 #endif
+                }
             } else {
                 flag_error(p.error_word, PA_DEVERR_BLOCK_RANGE);
                 mbar_arrive(bar_of(stage));
@@ -291,6 +269,10 @@ __global__ void __launch_bounds__(NW * 32, 1)
     // tile at `base`: rows of 128 bytes; chunk c of row r sits at chunk
     // c ^ (r & 7) (the TMA's 128-byte swizzle).
     auto tile_addr = [&](uint32_t base, int token, int half, int chunk) -> uint32_t {
+        if constexpr (kFp8) {
+            const int r = token;  // FP8: one 128-byte row per token, chunk 0..7
+            return base + r * 128 + (((chunk + 4 * half) ^ (r & 7)) << 4);
+        }
 #if PA_DECODE_PACKED5D
         const int r = token * (D / 64) + half;
 #else
@@ -300,19 +282,36 @@ __global__ void __launch_bounds__(NW * 32, 1)
     };
 
     // Query fragments (B operand of the score product): head 8nt+g of the
-    // group, elements d = 16kk + 2t4 (+1) and +8 (+9).
+    // group.  16-bit pools: elements d = 16kk + 2t4 (+1) and +8 (+9).  FP8
+    // pools: the score's sum over d is taken in a permuted order matching the
+    // FP8 tile fragments -- k-steps 2t4, 2t4+1 <- d = 16kk + 4t4 (+1) and
+    // k-steps 2t4+8, 2t4+9 <- d = 16kk + 4t4 + 2 (+3) -- in fp16.
     uint32_t qf[NT][KT][2];
     auto load_query = [&](int s, int kh) {
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
             const int hg = nt * 8 + g;
-            const uint32_t *qrow = reinterpret_cast<const uint32_t *>(
-                static_cast<const T *>(p.query) +
-                ((size_t)s * p.num_heads + (size_t)kh * G + (hg < G ? hg : 0)) * D);
+            const T *qrow = static_cast<const T *>(p.query) +
+                            ((size_t)s * p.num_heads + (size_t)kh * G + (hg < G ? hg : 0)) * D;
 #pragma unroll
             for (int kk = 0; kk < KT; ++kk) {
-                qf[nt][kk][0] = hg < G ? __ldg(qrow + kk * 8 + t4) : 0u;
-                qf[nt][kk][1] = hg < G ? __ldg(qrow + kk * 8 + 4 + t4) : 0u;
+                if constexpr (kFp8) {
+                    uint2 w = make_uint2(0u, 0u);
+                    if (hg < G)
+                        w = __ldg(reinterpret_cast<const uint2 *>(qrow + kk * 16 + 4 * t4));
+                    if constexpr (std::is_same<T, __half>::value) {
+                        qf[nt][kk][0] = w.x;
+                        qf[nt][kk][1] = w.y;
+                    } else {
+                        const T *e = reinterpret_cast<const T *>(&w);
+                        qf[nt][kk][0] = pack_f16x2(__bfloat162float(e[0]), __bfloat162float(e[1]));
+                        qf[nt][kk][1] = pack_f16x2(__bfloat162float(e[2]), __bfloat162float(e[3]));
+                    }
+                } else {
+                    const uint32_t *qw = reinterpret_cast<const uint32_t *>(qrow);
+                    qf[nt][kk][0] = hg < G ? __ldg(qw + kk * 8 + t4) : 0u;
+                    qf[nt][kk][1] = hg < G ? __ldg(qw + kk * 8 + 4 + t4) : 0u;
+                }
             }
         }
     };
@@ -369,13 +368,37 @@ __global__ void __launch_bounds__(NW * 32, 1)
 #pragma unroll
                     for (int nt = 0; nt < NT; ++nt)
                         part[c][nt][0] = part[c][nt][1] = part[c][nt][2] = part[c][nt][3] = 0.f;
+                if constexpr (kFp8) {
+                    // one ldmatrix brings two 16-d chunks of 16 tokens as byte
+                    // pairs: thread (g, t4) gets d = 16c + 4t4 .. +3 of tokens g
+                    // and g + 8; widening gives the (permuted-k) A fragment
 #pragma unroll
-                for (int kk = 0; kk < KT; ++kk) {
-                    uint32_t a[4];
-                    ldmatrix_x4(tile_addr(kbase, k_row, kk >> 2, (kk & 3) * 2 + k_cj), a);
+                    for (int kp = 0; kp < KT / 2; ++kp) {
+                        uint32_t r[4];
+                        ldmatrix_x4(tile_addr(kbase, k_row, 0, 2 * kp + k_cj), r);
 #pragma unroll
-                    for (int nt = 0; nt < NT; ++nt)
-                        Op::run(part[kk % kChains][nt], a, qf[nt][kk][0], qf[nt][kk][1]);
+                        for (int h = 0; h < 2; ++h) {
+                            const int kk = 2 * kp + h;
+                            const uint32_t w0 = r[2 * h], w1 = r[2 * h + 1];
+                            uint32_t a[4];
+                            a[0] = e4m3x2_to_f16x2((uint16_t)(w0 & 0xffffu));
+                            a[1] = e4m3x2_to_f16x2((uint16_t)(w1 & 0xffffu));
+                            a[2] = e4m3x2_to_f16x2((uint16_t)(w0 >> 16));
+                            a[3] = e4m3x2_to_f16x2((uint16_t)(w1 >> 16));
+#pragma unroll
+                            for (int nt = 0; nt < NT; ++nt)
+                                Op::run(part[kk % kChains][nt], a, qf[nt][kk][0], qf[nt][kk][1]);
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int kk = 0; kk < KT; ++kk) {
+                        uint32_t a[4];
+                        ldmatrix_x4(tile_addr(kbase, k_row, kk >> 2, (kk & 3) * 2 + k_cj), a);
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt)
+                            Op::run(part[kk % kChains][nt], a, qf[nt][kk][0], qf[nt][kk][1]);
+                    }
                 }
                 float sc[NT][4];
 #pragma unroll
@@ -392,10 +415,30 @@ __global__ void __launch_bounds__(NW * 32, 1)
                 // V^T fragments (their latency overlaps the softmax); rows past
                 // the context are zeroed so NaN padding never meets a zero weight
                 uint32_t va[KT][4];
+                if constexpr (kFp8) {
+                    // transposed byte-pair loads: thread (g, t4) gets tokens 2t4,
+                    // 2t4+1 (and +8, +9) at d = 16c + 2g, 2g+1; fragment row g is
+                    // d = 16c + 2g and row g + 8 is d = 16c + 2g + 1
 #pragma unroll
-                for (int mt = 0; mt < KT; ++mt)
-                    ldmatrix_x4_trans(tile_addr(vbase, v_row, mt >> 2, (mt & 3) * 2 + v_cj),
-                                      va[mt]);
+                    for (int mp = 0; mp < KT / 2; ++mp) {
+                        uint32_t r[4];
+                        ldmatrix_x4_trans(tile_addr(vbase, k_row, 0, 2 * mp + k_cj), r);
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            const uint32_t p0 = byte_perm(r[2 * h], 0u, 0x3120u);
+                            const uint32_t p1 = byte_perm(r[2 * h + 1], 0u, 0x3120u);
+                            va[2 * mp + h][0] = e4m3x2_to_f16x2((uint16_t)(p0 & 0xffffu));
+                            va[2 * mp + h][1] = e4m3x2_to_f16x2((uint16_t)(p0 >> 16));
+                            va[2 * mp + h][2] = e4m3x2_to_f16x2((uint16_t)(p1 & 0xffffu));
+                            va[2 * mp + h][3] = e4m3x2_to_f16x2((uint16_t)(p1 >> 16));
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int mt = 0; mt < KT; ++mt)
+                        ldmatrix_x4_trans(tile_addr(vbase, v_row, mt >> 2, (mt & 3) * 2 + v_cj),
+                                          va[mt]);
+                }
                 if (partial) {
                     const uint32_t m01 = (2 * t4 < nv ? 0x0000ffffu : 0u) |
                                          (2 * t4 + 1 < nv ? 0xffff0000u : 0u);
@@ -496,11 +539,14 @@ __global__ void __launch_bounds__(NW * 32, 1)
                 const int h0 = nt * 8 + 2 * t4;
 #pragma unroll
                 for (int mt = 0; mt < KT; ++mt) {
-                    const int d0 = mt * 16 + g;
+                    // fragment rows g, g + 8 are d = 16mt + g, + 8 (16-bit pools)
+                    // or d = 16mt + 2g, + 1 (FP8 pools)
+                    const int d0 = kFp8 ? mt * 16 + 2 * g : mt * 16 + g;
+                    const int d1 = kFp8 ? d0 + 1 : d0 + 8;
                     mo[h0 * L::kPitch + d0] = o[mt][nt][0];
                     mo[(h0 + 1) * L::kPitch + d0] = o[mt][nt][1];
-                    mo[h0 * L::kPitch + d0 + 8] = o[mt][nt][2];
-                    mo[(h0 + 1) * L::kPitch + d0 + 8] = o[mt][nt][3];
+                    mo[h0 * L::kPitch + d1] = o[mt][nt][2];
+                    mo[(h0 + 1) * L::kPitch + d1] = o[mt][nt][3];
                 }
                 if (g == 0) {
                     merge_m[warp * kHeads + h0] = mrun[nt][0];
@@ -533,13 +579,13 @@ __global__ void __launch_bounds__(NW * 32, 1)
                 acc[0] += wgt * x0.x; acc[1] += wgt * x0.y; acc[2] += wgt * x0.z; acc[3] += wgt * x0.w;
                 acc[4] += wgt * x1.x; acc[5] += wgt * x1.y; acc[6] += wgt * x1.z; acc[7] += wgt * x1.w;
             }
-            const float inv = 1.f / lsum;
+            const float inv = p.out_scale / lsum;
             const size_t h = (size_t)kh * G + jh;
             if (nparts == 1) {
                 T vals[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e)
-                    vals[e] = Op::from_float(acc[e] * inv);
+                    vals[e] = MmaOp<T>::from_float(acc[e] * inv);
                 *reinterpret_cast<uint4 *>(static_cast<T *>(p.out) +
                                            ((size_t)s * p.num_heads + h) * D + d0) =
                     *reinterpret_cast<const uint4 *>(vals);
@@ -572,157 +618,7 @@ __global__ void __launch_bounds__(NW * 32, 1)
     }
 }
 
-// ---- split-context reduce ----------------------------------------------------------
-//
-// One CTA per (sequence, KV head).  For the G query heads of the group it
-// merges the nparts partials (m_q, l_q, o_q) of a sequence that spans more
-// than one partition: M = max_q m_q, w_q = l_q exp(m_q - M),
-// out = sum_q w_q o_q / sum_q w_q.  Sequences with one partition were written
-// by the partition pass itself.  (1) warp w finds M and sum_q w_q for heads
-// jh = w, w + 4, ...; (2) thread (item, qg) sums w_q o_q over q = qg, qg + QG,
-// ...; (3) the QG group sums are added in shared memory.
-constexpr int kReduceThreads = 256;
-constexpr int kReduceChunk = 128;  // partitions whose weights are staged at once
-
-template <typename T, int D>
-__global__ void __launch_bounds__(kReduceThreads)
-    paged_reduce_kernel(const __grid_constant__ DecodeParams p)
-{
-    using Op = MmaOp<T>;
-    __shared__ float head_m[16], head_inv_l[16];
-    __shared__ float wts[16 * kReduceChunk];
-    __shared__ __align__(16) float red[kReduceThreads * 8];
-    pdl_wait_primary();  // the partition pass's partials are visible past here
-
-    const int Hkv = p.num_kv_heads;
-    const int G = p.group;
-    const int s = blockIdx.x / Hkv;
-    const int kh = blockIdx.x - s * Hkv;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int ctx = clamp_context(p, s, false);
-    const int nparts = (ctx + p.part_tokens - 1) / p.part_tokens;
-    if (nparts <= 1)
-        return;
-
-    // (1) per head: M = max_q m_q and L = sum_q l_q exp(m_q - M) (warp per head)
-    const size_t hbase = ((size_t)s * p.num_heads + (size_t)kh * G) * p.max_parts;
-    for (int jh = warp; jh < G; jh += kReduceThreads / 32) {
-        const float *pm = p.part_m + hbase + (size_t)jh * p.max_parts;
-        const float *pl = p.part_l + hbase + (size_t)jh * p.max_parts;
-        float mx = -INFINITY;
-        for (int q = lane; q < nparts; q += 32)
-            mx = fmaxf(mx, pm[q]);
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1)
-            mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, off));
-        float ls = 0.f;
-        for (int q = lane; q < nparts; q += 32)
-            ls += pl[q] * exp2f((pm[q] - mx) * kLog2e);
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1)
-            ls += __shfl_xor_sync(kFull, ls, off);
-        if (lane == 0) {
-            head_m[jh] = mx;
-            head_inv_l[jh] = 1.f / ls;
-        }
-    }
-    __syncthreads();
-
-    // (2) thread (item, qg) sums w_q o_q over q = qg, qg + QG, ... with the
-    // weights w_q = l_q exp(m_q - M) / L of a chunk of partitions staged in
-    // shared memory; (3) the QG group sums are added in shared memory.
-    // G * D / 8 <= 16 * 128 / 8 = kReduceThreads: one (item, qg) per thread.
-    static_assert(16 * D / 8 <= kReduceThreads, "one work item per thread");
-    const int items = G * (D / 8);
-    const int qgroups = max(1, kReduceThreads / items);
-    const bool active = tid < items * qgroups;
-    const int item = tid % items;
-    const int qg = tid / items;
-    const int jh = item / (D / 8);
-    const int d0 = (item - jh * (D / 8)) * 8;
-    const float *po = p.part_o + (hbase + (size_t)jh * p.max_parts) * D + d0;
-    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    for (int c0 = 0; c0 < nparts; c0 += kReduceChunk) {
-        const int cn = min(kReduceChunk, nparts - c0);
-        for (int i = tid; i < G * cn; i += kReduceThreads) {
-            const int h = i / cn, q = c0 + (i - h * cn);
-            const size_t idx = hbase + (size_t)h * p.max_parts + q;
-            wts[h * kReduceChunk + (q - c0)] =
-                p.part_l[idx] * exp2f((p.part_m[idx] - head_m[h]) * kLog2e) * head_inv_l[h];
-        }
-        __syncthreads();
-        if (active) {
-#pragma unroll 8
-            for (int q = c0 + qg; q < c0 + cn; q += qgroups) {
-                const float wgt = wts[jh * kReduceChunk + (q - c0)];
-                const float4 x0 = reinterpret_cast<const float4 *>(po + (size_t)q * D)[0];
-                const float4 x1 = reinterpret_cast<const float4 *>(po + (size_t)q * D)[1];
-                acc[0] += wgt * x0.x; acc[1] += wgt * x0.y; acc[2] += wgt * x0.z; acc[3] += wgt * x0.w;
-                acc[4] += wgt * x1.x; acc[5] += wgt * x1.y; acc[6] += wgt * x1.z; acc[7] += wgt * x1.w;
-            }
-        }
-        __syncthreads();
-    }
-    if (active) {
-        if (qgroups == 1) {
-            T vals[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e)
-                vals[e] = Op::from_float(acc[e]);
-            *reinterpret_cast<uint4 *>(static_cast<T *>(p.out) +
-                                       ((size_t)s * p.num_heads + (size_t)kh * G + jh) * D +
-                                       d0) = *reinterpret_cast<const uint4 *>(vals);
-        } else {
-            float4 *dst = reinterpret_cast<float4 *>(red + (size_t)tid * 8);
-            dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-            dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
-        }
-    }
-    if (qgroups == 1)
-        return;
-    __syncthreads();
-    for (int it = tid; it < items; it += kReduceThreads) {
-        const int jh = it / (D / 8);
-        const int d0 = (it - jh * (D / 8)) * 8;
-        float sum[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        for (int g2 = 0; g2 < qgroups; ++g2) {
-            const float4 *src = reinterpret_cast<const float4 *>(red + (size_t)(g2 * items + it) * 8);
-            const float4 x0 = src[0], x1 = src[1];
-            sum[0] += x0.x; sum[1] += x0.y; sum[2] += x0.z; sum[3] += x0.w;
-            sum[4] += x1.x; sum[5] += x1.y; sum[6] += x1.z; sum[7] += x1.w;
-        }
-        T vals[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e)
-            vals[e] = Op::from_float(sum[e]);
-        *reinterpret_cast<uint4 *>(static_cast<T *>(p.out) +
-                                   ((size_t)s * p.num_heads + (size_t)kh * G + jh) * D + d0) =
-            *reinterpret_cast<const uint4 *>(vals);
-    }
-}
-
 // ---- host side -------------------------------------------------------------------
-
-using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
-                                   const cuuint64_t *, const cuuint64_t *,
-                                   const cuuint32_t *, const cuuint32_t *,
-                                   CUtensorMapInterleave, CUtensorMapSwizzle,
-                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-static EncodeTiledFn get_encode_fn()
-{
-    static EncodeTiledFn fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void *ptr = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
-                                             cudaEnableDefault, &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(ptr);
-    });
-    return fn;
-}
 
 // Tensor map over a pool [num_blocks][block_size][num_kv_heads][head_dim].
 // Default (4-D, dims d, head, token, block): a box of 64 elements x 1 head x
@@ -741,6 +637,21 @@ static bool encode_pool_map(CUtensorMap *map, const void *pool, pa_dtype dtype,
     EncodeTiledFn fn = get_encode_fn();
     if (!fn)
         return false;
+    if (dtype == PA_FP8_E4M3) {
+        // FP8 pools: 1-byte elements, a box of 128 elements (a 128-byte row) x
+        // 1 head x 16 tokens x 1 block, 128-byte swizzle
+        const cuuint64_t dims[4] = {(cuuint64_t)head_dim, (cuuint64_t)num_kv_heads,
+                                    (cuuint64_t)block_size, (cuuint64_t)num_blocks};
+        const cuuint64_t strides[3] = {(cuuint64_t)head_dim,
+                                       (cuuint64_t)num_kv_heads * head_dim,
+                                       (cuuint64_t)block_size * num_kv_heads * head_dim};
+        const cuuint32_t box[4] = {128, 1, (cuuint32_t)kTileTokens, 1};
+        const cuuint32_t estr[4] = {1, 1, 1, 1};
+        return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void *>(pool), dims,
+                  strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    }
     const cuuint64_t e = 2;
     const CUtensorMapDataType ty = dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                                     : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
@@ -778,51 +689,20 @@ static bool encode_pool_map(CUtensorMap *map, const void *pool, pa_dtype dtype,
 #endif
 constexpr int kWarps = PA_DECODE_WARPS;          // warps per CTA
 constexpr int kStagesPerWarp = PA_DECODE_STAGES; // ring stages per warp
+#ifndef PA_DECODE_STAGES_FP8
+#define PA_DECODE_STAGES_FP8 4
+#endif
+constexpr int kStagesPerWarpFp8 = PA_DECODE_STAGES_FP8;  // FP8 stages are half the size
 // Fewer stages for batches whose per-sequence shared arrays (8 B each) do
 // not fit next to the default rings.
 constexpr int kStagesManySeqs = 1;
 
-// Per-device facts and per-kernel launch settings, looked up once: the SM
-// count and shared-memory limit of each device, and for each kernel the
-// largest dynamic shared memory it has been enabled for and the residency
-// found for the last shared-memory size.
-constexpr int kMaxDevices = 64;
-struct DeviceInfo {
-    int sms = 0, optin = 0;
-};
-static pa_status device_info(int dev, DeviceInfo *out)
-{
-    static DeviceInfo cache[kMaxDevices];
-    static std::mutex mu;
-    if (dev < 0 || dev >= kMaxDevices)
-        return PA_ERR_UNSUPPORTED;
-    std::lock_guard<std::mutex> lock(mu);
-    if (cache[dev].sms == 0) {
-        cudaError_t e = cudaDeviceGetAttribute(&cache[dev].optin,
-                                               cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-        if (e == cudaSuccess)
-            e = cudaDeviceGetAttribute(&cache[dev].sms, cudaDevAttrMultiProcessorCount, dev);
-        if (e != cudaSuccess) {
-            cache[dev].sms = 0;
-            return record_cuda(e);
-        }
-    }
-    *out = cache[dev];
-    return PA_OK;
-}
-
-struct KernelSetting {
-    size_t smem_enabled = 0;  // dynamic shared memory the kernel may use
-    size_t smem_queried = 0;  // shared-memory size of the cached residency
-    int per_sm = 0;           // resident CTAs per SM at smem_queried
-};
-
-template <typename T, int D, int NT, int NST>
+template <typename T, typename KV, int D, int NT, int NST>
 static pa_status launch_pass(const DecodeParams &prm, const CUtensorMap &mk,
                              const CUtensorMap &mv, cudaStream_t stream, long long max_units)
 {
-    using L = Layout<D, NT, kWarps, NST>;
-    auto kernel = paged_decode_kernel<T, D, NT, kWarps, NST>;
+    using L = Layout<D, NT, kWarps, NST, sizeof(KV)>;
+    auto kernel = paged_decode_kernel<T, KV, D, NT, kWarps, NST>;
     constexpr int kThreads = kWarps * 32;
     static KernelSetting setting[kMaxDevices];
     static std::mutex mu;
@@ -867,53 +747,18 @@ static pa_status launch_pass(const DecodeParams &prm, const CUtensorMap &mk,
     return launch_pdl(kernel, dim3((unsigned)grid), dim3(kThreads), smem, stream, prm, mk, mv);
 }
 
-// The reduce is queued behind the partition pass with programmatic
-// dependent launch: its CTAs may start while the pass drains and wait in
-// griddepcontrol.wait until the pass's writes are visible.
-template <typename T, int D>
-static pa_status launch_reduce(const DecodeParams &prm, cudaStream_t stream)
-{
-    return launch_pdl(paged_reduce_kernel<T, D>, dim3((unsigned)(prm.num_seqs * prm.num_kv_heads)),
-                      dim3(kReduceThreads), 0, stream, prm);
-}
-
-template <typename T, int D, int NT>
+template <typename T, typename KV, int D, int NT>
 static pa_status launch_decode(const DecodeParams &prm, const CUtensorMap &mk,
                                const CUtensorMap &mv, cudaStream_t stream,
                                long long max_units)
 {
-    pa_status st = launch_pass<T, D, NT, kStagesPerWarp>(prm, mk, mv, stream, max_units);
+    constexpr int kStages = sizeof(KV) == 1 ? kStagesPerWarpFp8 : kStagesPerWarp;
+    pa_status st = launch_pass<T, KV, D, NT, kStages>(prm, mk, mv, stream, max_units);
     if (st == PA_ERR_UNSUPPORTED)
-        st = launch_pass<T, D, NT, kStagesManySeqs>(prm, mk, mv, stream, max_units);
+        st = launch_pass<T, KV, D, NT, kStagesManySeqs>(prm, mk, mv, stream, max_units);
     if (st != PA_OK || prm.max_parts <= 1)
         return st;
     return launch_reduce<T, D>(prm, stream);
-}
-
-static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
-
-struct WorkspaceLayout {
-    size_t m_off, l_off, o_off, total;
-};
-
-static WorkspaceLayout workspace_layout(int S, int H, int D, int parts)
-{
-    WorkspaceLayout w{};
-    if (parts <= 1)
-        return w;
-    const size_t ml = align256((size_t)S * H * parts * 4);
-    w.m_off = 0;
-    w.l_off = ml;
-    w.o_off = 2 * ml;
-    w.total = w.o_off + align256((size_t)S * H * parts * D * 4);
-    return w;
-}
-
-static int num_parts(int max_context_len, int partition_size)
-{
-    if (partition_size <= 0 || max_context_len <= 0)
-        return 1;
-    return (int)(((long long)max_context_len + partition_size - 1) / partition_size);
 }
 
 } // namespace pa
@@ -940,62 +785,18 @@ extern "C" pa_status pa_decode_attention(void *out, const void *query, const voi
                                          void *workspace, size_t workspace_bytes,
                                          pa_dtype dtype, int32_t *error_word, void *stream)
 {
-    if (num_seqs < 0 || num_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
-        block_size <= 0 || num_blocks <= 0 || max_blocks_per_seq <= 0 ||
-        max_context_len < 0 || partition_size < 0 || !std::isfinite(scale) ||
-        (dtype != PA_F16 && dtype != PA_BF16))
+    if (dtype != PA_F16 && dtype != PA_BF16)
         return PA_ERR_INVALID_ARG;
-    if (num_heads % num_kv_heads != 0)
-        return PA_ERR_INVALID_ARG;
-    if (num_seqs == 0)
-        return PA_OK;
-    if (!out || !query || !key_cache || !value_cache || !block_tables || !context_lens)
-        return PA_ERR_INVALID_ARG;
-    if (!aligned16(out) || !aligned16(query) || !aligned16(key_cache) ||
-        !aligned16(value_cache))
-        return PA_ERR_INVALID_ARG;
-    const int group = num_heads / num_kv_heads;
-    if ((head_dim != 64 && head_dim != 128) || block_size < kTileTokens ||
-        block_size > 256 || (block_size & (block_size - 1)) != 0 || group > 16 ||
-        (long long)num_blocks * block_size >= (1ll << 31) ||
-        (long long)max_blocks_per_seq * block_size >= (1ll << 31))
-        return PA_ERR_UNSUPPORTED;
-    if (partition_size != 0 && partition_size % kTileTokens != 0)
-        return PA_ERR_UNSUPPORTED;
-
-    const int parts = num_parts(max_context_len, partition_size);
-    const WorkspaceLayout wl = workspace_layout(num_seqs, num_heads, head_dim, parts);
-    if (wl.total > 0 && (workspace == nullptr || workspace_bytes < wl.total ||
-                         (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0))
-        return PA_ERR_WORKSPACE;
-
     DecodeParams prm{};
-    prm.out = out;
-    prm.query = query;
-    prm.block_tables = block_tables;
-    prm.context_lens = context_lens;
-    uint8_t *ws = static_cast<uint8_t *>(workspace);
-    prm.part_m = wl.total ? reinterpret_cast<float *>(ws + wl.m_off) : nullptr;
-    prm.part_l = wl.total ? reinterpret_cast<float *>(ws + wl.l_off) : nullptr;
-    prm.part_o = wl.total ? reinterpret_cast<float *>(ws + wl.o_off) : nullptr;
-    prm.error_word = error_word;
-    prm.num_seqs = num_seqs;
-    prm.num_heads = num_heads;
-    prm.num_kv_heads = num_kv_heads;
-    prm.group = group;
-    prm.max_blocks_per_seq = max_blocks_per_seq;
-    prm.num_blocks = num_blocks;
-    prm.block_size = block_size;
-    prm.max_context_len = max_context_len;
-    prm.block_shift = __builtin_ctz((unsigned)block_size);
-    // Single pass: one unit covers the longest possible context.
-    const long long ctx_cap = (long long)max_blocks_per_seq * block_size;
-    const long long whole = ((std::max<long long>(1, std::min<long long>(
-                                  max_context_len, ctx_cap)) + kTileTokens - 1) /
-                             kTileTokens) * kTileTokens;
-    prm.part_tokens = parts > 1 ? partition_size : (int)whole;
-    prm.max_parts = parts;
-    prm.scale_log2 = scale * kLog2e;
+    const pa_status ok = prepare_decode(
+        &prm, out, query, key_cache, value_cache, block_tables, max_blocks_per_seq,
+        context_lens, max_context_len, num_seqs, num_heads, num_kv_heads, head_dim,
+        block_size, num_blocks, scale, partition_size, workspace, workspace_bytes,
+        error_word);
+    if (ok != PA_OK || num_seqs == 0)
+        return ok;
+    const int group = prm.group;
+    const int parts = prm.max_parts;
 
     CUtensorMap mk, mv;
     if (!encode_pool_map(&mk, key_cache, dtype, num_blocks, block_size, num_kv_heads,
@@ -1008,16 +809,61 @@ extern "C" pa_status pa_decode_attention(void *out, const void *query, const voi
     cudaStream_t st = as_stream(stream);
     const bool bf = dtype == PA_BF16;
     const bool wide = group > 8;
+    using B16 = __nv_bfloat16;
+    using F16 = __half;
     if (head_dim == 128) {
         if (bf)
-            return wide ? launch_decode<__nv_bfloat16, 128, 2>(prm, mk, mv, st, max_units)
-                        : launch_decode<__nv_bfloat16, 128, 1>(prm, mk, mv, st, max_units);
-        return wide ? launch_decode<__half, 128, 2>(prm, mk, mv, st, max_units)
-                    : launch_decode<__half, 128, 1>(prm, mk, mv, st, max_units);
+            return wide ? launch_decode<B16, B16, 128, 2>(prm, mk, mv, st, max_units)
+                        : launch_decode<B16, B16, 128, 1>(prm, mk, mv, st, max_units);
+        return wide ? launch_decode<F16, F16, 128, 2>(prm, mk, mv, st, max_units)
+                    : launch_decode<F16, F16, 128, 1>(prm, mk, mv, st, max_units);
     }
     if (bf)
-        return wide ? launch_decode<__nv_bfloat16, 64, 2>(prm, mk, mv, st, max_units)
-                    : launch_decode<__nv_bfloat16, 64, 1>(prm, mk, mv, st, max_units);
-    return wide ? launch_decode<__half, 64, 2>(prm, mk, mv, st, max_units)
-                : launch_decode<__half, 64, 1>(prm, mk, mv, st, max_units);
+        return wide ? launch_decode<B16, B16, 64, 2>(prm, mk, mv, st, max_units)
+                    : launch_decode<B16, B16, 64, 1>(prm, mk, mv, st, max_units);
+    return wide ? launch_decode<F16, F16, 64, 2>(prm, mk, mv, st, max_units)
+                : launch_decode<F16, F16, 64, 1>(prm, mk, mv, st, max_units);
+}
+
+extern "C" pa_status pa_decode_attention_fp8(
+    void *out, const void *query, const void *key_cache, const void *value_cache,
+    const int32_t *block_tables, int max_blocks_per_seq, const int32_t *context_lens,
+    int max_context_len, int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+    int block_size, int num_blocks, float scale, float k_scale, float v_scale,
+    int partition_size, void *workspace, size_t workspace_bytes, pa_dtype dtype,
+    int32_t *error_word, void *stream)
+{
+    if ((dtype != PA_F16 && dtype != PA_BF16) || !std::isfinite(k_scale) ||
+        !std::isfinite(v_scale) || k_scale <= 0.f || v_scale <= 0.f)
+        return PA_ERR_INVALID_ARG;
+    DecodeParams prm{};
+    const pa_status ok = prepare_decode(
+        &prm, out, query, key_cache, value_cache, block_tables, max_blocks_per_seq,
+        context_lens, max_context_len, num_seqs, num_heads, num_kv_heads, head_dim,
+        block_size, num_blocks, scale, partition_size, workspace, workspace_bytes,
+        error_word);
+    if (ok != PA_OK || num_seqs == 0)
+        return ok;
+    if (head_dim != 128)
+        return PA_ERR_UNSUPPORTED;
+    // scores use the K codes: fold the K scale into the exponent's scale;
+    // outputs (and partials) get the V scale
+    prm.scale_log2 = scale * k_scale * kLog2e;
+    prm.out_scale = v_scale;
+
+    CUtensorMap mk, mv;
+    if (!encode_pool_map(&mk, key_cache, PA_FP8_E4M3, num_blocks, block_size, num_kv_heads,
+                         head_dim) ||
+        !encode_pool_map(&mv, value_cache, PA_FP8_E4M3, num_blocks, block_size, num_kv_heads,
+                         head_dim))
+        return PA_ERR_CUDA;
+    const long long max_units = (long long)num_seqs * num_kv_heads * prm.max_parts;
+    cudaStream_t st = as_stream(stream);
+    const bool wide = prm.group > 8;
+    using U8 = uint8_t;
+    if (dtype == PA_BF16)
+        return wide ? launch_decode<__nv_bfloat16, U8, 128, 2>(prm, mk, mv, st, max_units)
+                    : launch_decode<__nv_bfloat16, U8, 128, 1>(prm, mk, mv, st, max_units);
+    return wide ? launch_decode<__half, U8, 128, 2>(prm, mk, mv, st, max_units)
+                : launch_decode<__half, U8, 128, 1>(prm, mk, mv, st, max_units);
 }

@@ -155,6 +155,41 @@ __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x)
     return y;
 }
 
+// ---- FP8 (e4m3) -------------------------------------------------------------
+
+// Two e4m3 values (low byte first) -> two fp16 values (exact).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t x)
+{
+    uint32_t r;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(x));
+    return r;
+}
+
+// Two floats -> two e4m3 values (`lo` in the low byte), nearest even,
+// saturating finite values to +-448.
+__device__ __forceinline__ uint16_t f32x2_to_e4m3x2(float lo, float hi)
+{
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// Byte permute: result byte i = byte sel_i of the 8-byte pair {b:a}.
+__device__ __forceinline__ uint32_t byte_perm(uint32_t a, uint32_t b, uint32_t sel)
+{
+    uint32_t r;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+    return r;
+}
+
+// fp16 pair from two floats (`lo` in the low half), nearest even.
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi)
+{
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
 // ---- mma.sync m16n8k16, fp32 accumulate ------------------------------------
 
 template <typename T> struct MmaOp;

@@ -47,12 +47,19 @@ class DecodeStep:
         dt = w.dtype
         self.torch_dtype = torch.float16 if dt == "f16" else torch.bfloat16
         self.max_context_len = int(w.context_lens.max())
-        fill = int(np.int16(np.uint16(w.fill).view(np.int16)))
         shape = w.pool_shape()
-        self.key_cache = torch.full(shape, fill, dtype=torch.int16,
-                                    device=self.device).view(self.torch_dtype)
-        self.value_cache = torch.full(shape, fill, dtype=torch.int16,
-                                      device=self.device).view(self.torch_dtype)
+        self.fp8 = w.fp8
+        self.kv_scale = float(w.spec.kv_scale)
+        if self.fp8:
+            # e4m3 codes; 0x7F is NaN
+            self.key_cache = torch.full(shape, 0x7F, dtype=torch.uint8, device=self.device)
+            self.value_cache = torch.full(shape, 0x7F, dtype=torch.uint8, device=self.device)
+        else:
+            fill = int(np.int16(np.uint16(w.fill).view(np.int16)))
+            self.key_cache = torch.full(shape, fill, dtype=torch.int16,
+                                        device=self.device).view(self.torch_dtype)
+            self.value_cache = torch.full(shape, fill, dtype=torch.int16,
+                                          device=self.device).view(self.torch_dtype)
         self.block_tables = _ti(w.block_tables, self.device)
         self.step_block_tables = _ti(w.step_block_tables, self.device)
         self.context_lens = _ti(w.context_lens, self.device)
@@ -84,8 +91,16 @@ class DecodeStep:
             slots = torch.empty(hi - lo, dtype=torch.int32, device=self.device)
             B.pa_slot_mapping(slots, self.block_tables, seq, pos, w.bs, w.num_blocks,
                               error_word=self.error_word)
+            self._cache_write(k, v, slots)
+
+    def _cache_write(self, k, v, slots, stream=None) -> None:
+        if self.fp8:
+            B.pa_reshape_and_cache_fp8(k, v, self.key_cache, self.value_cache, slots,
+                                       self.kv_scale, self.kv_scale,
+                                       error_word=self.error_word, stream=stream)
+        else:
             B.pa_reshape_and_cache(k, v, self.key_cache, self.value_cache, slots,
-                                   error_word=self.error_word)
+                                   error_word=self.error_word, stream=stream)
 
     # individual steps ---------------------------------------------------------
     def slot_mapping(self, stream=None) -> None:
@@ -94,9 +109,7 @@ class DecodeStep:
                           stream=stream)
 
     def reshape_and_cache(self, stream=None) -> None:
-        B.pa_reshape_and_cache(self.new_key, self.new_value, self.key_cache,
-                               self.value_cache, self.slots, error_word=self.error_word,
-                               stream=stream)
+        self._cache_write(self.new_key, self.new_value, self.slots, stream)
 
     def copy_blocks(self, stream=None) -> None:
         if self.cow_pairs is not None:
@@ -109,10 +122,17 @@ class DecodeStep:
         if P != self.partition_size:
             ws = B.alloc_workspace(self.w.S, self.w.H, self.w.Hkv, self.w.D,
                                    self.max_context_len, P, device=self.device)
-        B.pa_decode_attention(self.out, self.query, self.key_cache, self.value_cache,
-                              self.step_block_tables, self.context_lens,
-                              self.max_context_len, self.w.scale, P, ws,
-                              error_word=self.error_word, stream=stream)
+        if self.fp8:
+            B.pa_decode_attention_fp8(self.out, self.query, self.key_cache, self.value_cache,
+                                      self.step_block_tables, self.context_lens,
+                                      self.max_context_len, self.w.scale, self.kv_scale,
+                                      self.kv_scale, P, ws, error_word=self.error_word,
+                                      stream=stream)
+        else:
+            B.pa_decode_attention(self.out, self.query, self.key_cache, self.value_cache,
+                                  self.step_block_tables, self.context_lens,
+                                  self.max_context_len, self.w.scale, P, ws,
+                                  error_word=self.error_word, stream=stream)
 
     def run(self, stream=None) -> torch.Tensor:
         """One whole decode step; returns the attention output tensor."""
@@ -133,7 +153,9 @@ class DecodeStep:
 
 
 def to_bits(t: torch.Tensor) -> np.ndarray:
-    """Device 16-bit tensor -> host uint16 bit patterns."""
+    """Device 16-bit tensor -> host uint16 bit patterns (uint8 stays uint8)."""
+    if t.dtype == torch.uint8:
+        return t.detach().contiguous().cpu().numpy()
     return t.detach().contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
 
 

@@ -32,6 +32,7 @@ import torch
 
 F16_NAN = np.uint16(0x7E00)
 BF16_NAN = np.uint16(0x7FC0)
+FP8_NAN = np.uint8(0x7F)
 
 
 @dataclasses.dataclass
@@ -51,6 +52,8 @@ class WorkloadSpec:
     cow_pairs: int = 0              # copy-on-write (src, dst) pairs per step
     partition_size: int = 512       # split-context partition (tokens); 0 = single pass
     seed: int = 0
+    kv_dtype: str = "same"          # "same" (pools in dtype) or "fp8" (e4m3 codes)
+    kv_scale: float = 0.0137        # per-pool scale of FP8 codes (K and V)
 
 
 @dataclasses.dataclass
@@ -107,8 +110,21 @@ class Workload:
     def pool_shape(self):
         return (self.num_blocks, self.bs, self.Hkv, self.D)
 
+    @property
+    def fp8(self) -> bool:
+        return self.spec.kv_dtype == "fp8"
+
+    @property
+    def kv_elem_bytes(self) -> int:
+        return 1 if self.fp8 else 2
+
     def empty_pools(self):
-        """Two pools filled with the NaN pattern (host, uint16)."""
+        """Two pools filled with the NaN pattern (host): uint16 bit patterns,
+        or uint8 e4m3 codes (0x7F is NaN) for FP8 pools."""
+        if self.fp8:
+            kc = np.full(self.pool_shape(), FP8_NAN, dtype=np.uint8)
+            vc = np.full(self.pool_shape(), FP8_NAN, dtype=np.uint8)
+            return kc, vc
         kc = np.full(self.pool_shape(), self.fill, dtype=np.uint16)
         vc = np.full(self.pool_shape(), self.fill, dtype=np.uint16)
         return kc, vc
@@ -116,12 +132,12 @@ class Workload:
     def kv_bytes(self) -> int:
         """Bytes of K and V the step's attention must read: one K row and
         one V row per (attended token, KV head)."""
-        elem = 2
+        elem = self.kv_elem_bytes
         return int(self.context_lens.astype(np.int64).sum()) * self.Hkv * self.D * 2 * elem
 
     def unique_kv_bytes(self) -> int:
         """As kv_bytes, but the shared prefix counted once."""
-        elem = 2
+        elem = self.kv_elem_bytes
         pre = self.spec.shared_prefix_tokens
         toks = int(self.context_lens.astype(np.int64).sum())
         if pre:
@@ -319,11 +335,20 @@ CONFIGS: Dict[str, WorkloadSpec] = {
 }
 
 
+def fp8_variant(spec: WorkloadSpec) -> WorkloadSpec:
+    """The same workload with e4m3 KV pools ("--kv-cache-dtype fp8")."""
+    return dataclasses.replace(spec, name=spec.name + "-fp8", kv_dtype="fp8",
+                               description=spec.description + "; KV cache FP8 e4m3 "
+                               f"(per-pool scale {spec.kv_scale})")
+
+
 def small_variant(name: str, seed: int = 0) -> WorkloadSpec:
     """A reduced copy of one of the five workloads -- same head layout,
     dtype and block size, fewer and shorter sequences -- that the oracle
     finishes in seconds while still spanning several tiles, partitions and a
     ragged tail."""
+    if name.endswith("-fp8"):
+        return fp8_variant(small_variant(name[:-4], seed))
     base = CONFIGS[name]
     if name == "tiny":
         return dataclasses.replace(base, seed=seed or base.seed)
@@ -349,3 +374,7 @@ def small_variant(name: str, seed: int = 0) -> WorkloadSpec:
                                    shared_prefix_tokens=128, cow_pairs=4,
                                    partition_size=128)
     raise KeyError(name)
+
+
+CONFIGS["gqa70b-fp8"] = fp8_variant(CONFIGS["gqa70b"])
+CONFIGS["longctx-fp8"] = fp8_variant(CONFIGS["longctx"])

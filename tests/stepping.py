@@ -27,15 +27,31 @@ class OracleStep:
         kc, vc = w.empty_pools()
         self.hist_slots = oracle.slot_mapping(w.block_tables, w.hist_seq, w.hist_pos,
                                               w.bs)
-        oracle.reshape_and_cache(w.hist_key, w.hist_value, kc, vc, self.hist_slots)
+        self._write(w.hist_key, w.hist_value, kc, vc, self.hist_slots)
         self.new_slots = oracle.slot_mapping(w.block_tables, w.new_seq, w.new_pos, w.bs)
-        oracle.reshape_and_cache(w.new_key, w.new_value, kc, vc, self.new_slots)
+        self._write(w.new_key, w.new_value, kc, vc, self.new_slots)
         if w.cow_pairs.shape[0]:
-            oracle.copy_blocks(kc, vc, w.cow_pairs)
+            if w.fp8:
+                oracle.copy_blocks_u8(kc, vc, w.cow_pairs)
+            else:
+                oracle.copy_blocks(kc, vc, w.cow_pairs)
         self.key_cache, self.value_cache = kc, vc
+
+    def _write(self, k, v, kc, vc, slots):
+        w = self.w
+        if w.fp8:
+            oracle.reshape_and_cache_fp8(k, v, kc, vc, slots, odt(w), w.spec.kv_scale,
+                                         w.spec.kv_scale)
+        else:
+            oracle.reshape_and_cache(k, v, kc, vc, slots)
 
     def attention(self, seqs=None):
         w = self.w
+        if w.fp8:
+            return oracle.paged_attention_fp8(w.query, self.key_cache, self.value_cache,
+                                              w.step_block_tables, w.context_lens, w.scale,
+                                              odt(w), w.spec.kv_scale, w.spec.kv_scale,
+                                              seqs=seqs)
         return oracle.paged_attention(w.query, self.key_cache, self.value_cache,
                                       w.step_block_tables, w.context_lens, w.scale,
                                       odt(w), seqs=seqs)

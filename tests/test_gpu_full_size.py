@@ -10,22 +10,10 @@ import torch
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
-import oracle  # noqa: E402
 from paged_kv_cache_96_gb300 import workloads as W  # noqa: E402
-from stepping import assert_attention_close, odt  # noqa: E402
+from stepping import OracleStep, assert_attention_close  # noqa: E402
 
-NAMES = ["tiny", "mha7b", "gqa70b", "longctx", "prefix"]
-
-
-def _oracle_pools(w):
-    kc, vc = w.empty_pools()
-    slots = oracle.slot_mapping(w.block_tables, w.hist_seq, w.hist_pos, w.bs)
-    oracle.reshape_and_cache(w.hist_key, w.hist_value, kc, vc, slots)
-    new_slots = oracle.slot_mapping(w.block_tables, w.new_seq, w.new_pos, w.bs)
-    oracle.reshape_and_cache(w.new_key, w.new_value, kc, vc, new_slots)
-    if w.cow_pairs.shape[0]:
-        oracle.copy_blocks(kc, vc, w.cow_pairs)
-    return kc, vc, new_slots
+NAMES = ["tiny", "mha7b", "gqa70b", "longctx", "prefix", "gqa70b-fp8", "longctx-fp8"]
 
 
 def _sample(w, k=6, seed=7):
@@ -48,13 +36,12 @@ def test_full_size_step(name):
     torch.cuda.synchronize()
     assert int(st.error_word.item()) == 0
 
-    kc, vc, new_slots = _oracle_pools(w)
-    assert np.array_equal(st.slots.cpu().numpy().astype(np.int64), new_slots)
-    assert np.array_equal(S.to_bits(st.key_cache), kc)
-    assert np.array_equal(S.to_bits(st.value_cache), vc)
+    ref = OracleStep(w)
+    assert np.array_equal(st.slots.cpu().numpy().astype(np.int64), ref.new_slots)
+    assert np.array_equal(S.to_bits(st.key_cache), ref.key_cache)
+    assert np.array_equal(S.to_bits(st.value_cache), ref.value_cache)
 
     seqs = _sample(w)
-    want = oracle.paged_attention(w.query, kc, vc, w.step_block_tables, w.context_lens,
-                                  w.scale, odt(w), seqs=seqs)
+    want = ref.attention(seqs=seqs)
     got = S.to_float(out)
     assert_attention_close(got[seqs], want[seqs], f"{name} seqs {seqs}")

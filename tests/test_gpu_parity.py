@@ -15,7 +15,8 @@ import oracle  # noqa: E402
 from paged_kv_cache_96_gb300 import workloads as W  # noqa: E402
 from stepping import OracleStep, assert_attention_close, odt  # noqa: E402
 
-NAMES = ["tiny", "mha7b", "gqa70b", "longctx", "prefix"]
+NAMES = ["tiny", "mha7b", "gqa70b", "longctx", "prefix",
+         "mha7b-fp8", "gqa70b-fp8", "longctx-fp8", "prefix-fp8"]
 
 
 @pytest.fixture(scope="module")
