@@ -10,9 +10,10 @@
 //
 // How (GB300 design):
 //  * Work unit = (sequence, KV head, partition of `part_tokens` tokens).  A
-//    persistent grid (one CTA per SM) walks the units round-robin; units are
-//    numbered KV-head-fastest so the CTAs working on the Hkv heads of one
-//    partition run side by side and together stream whole 2 KB token rows.
+//    persistent grid (as many CTAs as fit on every SM) walks the units
+//    round-robin; units are numbered KV-head-fastest so the CTAs working on
+//    the Hkv heads of one partition run side by side and together stream
+//    whole token rows of the pool.
 //  * Each warp owns a ring of NST shared-memory stages.  A stage holds one
 //    16-token tile of K and of V for one KV head, fetched from the pool by
 //    4-D tiled TMA loads (128-byte swizzle) that complete on the stage's
@@ -24,13 +25,12 @@
 //    O^T[d x 8] += V^T[d x 16] . P^T[16 x 8] with mma.sync m16n8k16 (fp32
 //    accumulate); P goes from the S accumulator layout to the B-operand
 //    layout with movmatrix.  Every K/V byte is read from HBM once per step.
-//  * Softmax is online in fp32 (running max, running sum, exp2 with the
+//  * Softmax is online in fp32 (a reference max, running sum, exp2 with the
 //    scale folded into log2 units).  Warps merge their (m, l, O) through
 //    shared memory at the end of a unit.
 //  * Split context: a unit that is one of several partitions of its
-//    sequence writes a partial (m, l, o) to the workspace; the last unit of
-//    a (sequence, KV head) to arrive (an atomic counter) merges all of them
-//    by log-sum-exp weights and writes the output, then zeroes its counter.
+//    sequence writes a partial (m, l, o) to the workspace; the reduce kernel
+//    queued behind this one merges them by log-sum-exp weights.
 //  * Bounds: table entries outside [0, num_blocks) are never fetched (the
 //    tile is skipped, an error bit is set); tokens past the context are
 //    masked in the scores and their value rows are zeroed before the
@@ -73,8 +73,8 @@ template <int D, int NT, int NW, int NST, int EB> struct Layout {
 // T: query/output type.  KV: cached element type -- T itself, or uint8_t
 // for FP8 (e4m3) pools, whose tiles are widened to fp16 in registers (the
 // tensor-core products then run in fp16).
-template <typename T, typename KV, int D, int NT, int NW, int NST>
-__global__ void __launch_bounds__(NW * 32, 1)
+template <typename T, typename KV, int D, int NT, int NW, int NST, int MINB>
+__global__ void __launch_bounds__(NW * 32, MINB)
     paged_decode_kernel(const __grid_constant__ DecodeParams p,
                         const __grid_constant__ CUtensorMap tmap_k,
                         const __grid_constant__ CUtensorMap tmap_v)
@@ -687,12 +687,28 @@ static bool encode_pool_map(CUtensorMap *map, const void *pool, pa_dtype dtype,
 #ifndef PA_DECODE_STAGES
 #define PA_DECODE_STAGES 2
 #endif
-constexpr int kWarps = PA_DECODE_WARPS;          // warps per CTA
-constexpr int kStagesPerWarp = PA_DECODE_STAGES; // ring stages per warp
-#ifndef PA_DECODE_STAGES_FP8
-#define PA_DECODE_STAGES_FP8 4
+#ifndef PA_DECODE_MINB
+#define PA_DECODE_MINB 1
 #endif
-constexpr int kStagesPerWarpFp8 = PA_DECODE_STAGES_FP8;  // FP8 stages are half the size
+#ifndef PA_DECODE_WARPS_FP8
+#define PA_DECODE_WARPS_FP8 4
+#endif
+#ifndef PA_DECODE_STAGES_FP8
+#define PA_DECODE_STAGES_FP8 2
+#endif
+#ifndef PA_DECODE_MINB_FP8
+#define PA_DECODE_MINB_FP8 4
+#endif
+// 16-bit pools: warps per CTA, ring stages per warp, CTAs per SM the
+// register budget is sized for.
+constexpr int kWarps = PA_DECODE_WARPS;
+constexpr int kStagesPerWarp = PA_DECODE_STAGES;
+constexpr int kMinBlocks = PA_DECODE_MINB;
+// FP8 pools: stages are half the size and the widening adds arithmetic per
+// byte, so the kernel wants more warps per SM than the 16-bit one.
+constexpr int kWarpsFp8 = PA_DECODE_WARPS_FP8;
+constexpr int kStagesPerWarpFp8 = PA_DECODE_STAGES_FP8;
+constexpr int kMinBlocksFp8 = PA_DECODE_MINB_FP8;
 // Fewer stages for batches whose per-sequence shared arrays (8 B each) do
 // not fit next to the default rings.
 constexpr int kStagesManySeqs = 1;
@@ -701,9 +717,13 @@ template <typename T, typename KV, int D, int NT, int NST>
 static pa_status launch_pass(const DecodeParams &prm, const CUtensorMap &mk,
                              const CUtensorMap &mv, cudaStream_t stream, long long max_units)
 {
-    using L = Layout<D, NT, kWarps, NST, sizeof(KV)>;
-    auto kernel = paged_decode_kernel<T, KV, D, NT, kWarps, NST>;
-    constexpr int kThreads = kWarps * 32;
+    constexpr bool kFp8 = sizeof(KV) == 1;
+    constexpr int NW = kFp8 ? kWarpsFp8 : kWarps;
+    // the 16-head variant keeps twice the accumulators: no register cap
+    constexpr int MINB = NT > 1 ? 1 : kFp8 ? kMinBlocksFp8 : kMinBlocks;
+    using L = Layout<D, NT, NW, NST, sizeof(KV)>;
+    auto kernel = paged_decode_kernel<T, KV, D, NT, NW, NST, MINB>;
+    constexpr int kThreads = NW * 32;
     static KernelSetting setting[kMaxDevices];
     static std::mutex mu;
     const size_t smem = L::bytes(prm.num_seqs);

@@ -59,59 +59,37 @@ __device__ __forceinline__ int clamp_context(const DecodeParams &p, int s, bool 
 // merges the nparts partials (m_q, l_q, o_q) of a sequence that spans more
 // than one partition: M = max_q m_q, w_q = l_q exp(m_q - M),
 // out = sum_q w_q o_q / sum_q w_q.  Sequences with one partition were written
-// by the partition pass itself.  (1) warp w finds M and sum_q w_q for heads
-// jh = w, w + 4, ...; (2) thread (item, qg) sums w_q o_q over q = qg, qg + QG,
-// ...; (3) the QG group sums are added in shared memory.
+// by the partition pass itself.
+//
+// Thread (item, qg) -- item = (head, 8 consecutive d) -- takes partitions
+// q = qg, qg + QG, ... in chunks of kReduceUnroll whose loads are all issued
+// before any is used, and keeps its own (M_t, L_t, A_t) with the same
+// log-sum-exp rescaling; the QG threads of an item then combine theirs in
+// shared memory.  After the context length, every global load of a chunk is
+// independent, so a sequence with up to QG * kReduceUnroll partitions costs
+// two dependent trips to memory.
 constexpr int kReduceThreads = 256;
-constexpr int kReduceChunk = 128;  // partitions whose weights are staged at once
+constexpr int kReduceUnroll = 8;
 
 template <typename T, int D>
 __global__ void __launch_bounds__(kReduceThreads)
     paged_reduce_kernel(const __grid_constant__ DecodeParams p)
 {
     using Op = MmaOp<T>;
-    __shared__ float head_m[16], head_inv_l[16];
-    __shared__ float wts[16 * kReduceChunk];
-    __shared__ __align__(16) float red[kReduceThreads * 8];
+    __shared__ __align__(16) float red_o[kReduceThreads * 8];
+    __shared__ float red_m[kReduceThreads], red_l[kReduceThreads];
     pdl_wait_primary();  // the partition pass's partials are visible past here
 
     const int Hkv = p.num_kv_heads;
     const int G = p.group;
     const int s = blockIdx.x / Hkv;
     const int kh = blockIdx.x - s * Hkv;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int tid = threadIdx.x;
     const int ctx = clamp_context(p, s, false);
     const int nparts = (ctx + p.part_tokens - 1) / p.part_tokens;
     if (nparts <= 1)
         return;
 
-    // (1) per head: M = max_q m_q and L = sum_q l_q exp(m_q - M) (warp per head)
-    const size_t hbase = ((size_t)s * p.num_heads + (size_t)kh * G) * p.max_parts;
-    for (int jh = warp; jh < G; jh += kReduceThreads / 32) {
-        const float *pm = p.part_m + hbase + (size_t)jh * p.max_parts;
-        const float *pl = p.part_l + hbase + (size_t)jh * p.max_parts;
-        float mx = -INFINITY;
-        for (int q = lane; q < nparts; q += 32)
-            mx = fmaxf(mx, pm[q]);
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1)
-            mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, off));
-        float ls = 0.f;
-        for (int q = lane; q < nparts; q += 32)
-            ls += pl[q] * exp2f((pm[q] - mx) * kLog2e);
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1)
-            ls += __shfl_xor_sync(kFull, ls, off);
-        if (lane == 0) {
-            head_m[jh] = mx;
-            head_inv_l[jh] = 1.f / ls;
-        }
-    }
-    __syncthreads();
-
-    // (2) thread (item, qg) sums w_q o_q over q = qg, qg + QG, ... with the
-    // weights w_q = l_q exp(m_q - M) / L of a chunk of partitions staged in
-    // shared memory; (3) the QG group sums are added in shared memory.
     // G * D / 8 <= 16 * 128 / 8 = kReduceThreads: one (item, qg) per thread.
     static_assert(16 * D / 8 <= kReduceThreads, "one work item per thread");
     const int items = G * (D / 8);
@@ -121,65 +99,98 @@ __global__ void __launch_bounds__(kReduceThreads)
     const int qg = tid / items;
     const int jh = item / (D / 8);
     const int d0 = (item - jh * (D / 8)) * 8;
-    const float *po = p.part_o + (hbase + (size_t)jh * p.max_parts) * D + d0;
+    const size_t hrow = ((size_t)s * p.num_heads + (size_t)kh * G + jh) * p.max_parts;
+
+    float mt = -INFINITY, lt = 0.f;  // natural-log units, like the stored m_q
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    for (int c0 = 0; c0 < nparts; c0 += kReduceChunk) {
-        const int cn = min(kReduceChunk, nparts - c0);
-        for (int i = tid; i < G * cn; i += kReduceThreads) {
-            const int h = i / cn, q = c0 + (i - h * cn);
-            const size_t idx = hbase + (size_t)h * p.max_parts + q;
-            wts[h * kReduceChunk + (q - c0)] =
-                p.part_l[idx] * exp2f((p.part_m[idx] - head_m[h]) * kLog2e) * head_inv_l[h];
-        }
-        __syncthreads();
-        if (active) {
-#pragma unroll 8
-            for (int q = c0 + qg; q < c0 + cn; q += qgroups) {
-                const float wgt = wts[jh * kReduceChunk + (q - c0)];
-                const float4 x0 = reinterpret_cast<const float4 *>(po + (size_t)q * D)[0];
-                const float4 x1 = reinterpret_cast<const float4 *>(po + (size_t)q * D)[1];
-                acc[0] += wgt * x0.x; acc[1] += wgt * x0.y; acc[2] += wgt * x0.z; acc[3] += wgt * x0.w;
-                acc[4] += wgt * x1.x; acc[5] += wgt * x1.y; acc[6] += wgt * x1.z; acc[7] += wgt * x1.w;
-            }
-        }
-        __syncthreads();
-    }
     if (active) {
-        if (qgroups == 1) {
+        for (int c0 = qg; c0 < nparts; c0 += qgroups * kReduceUnroll) {
+            float cm[kReduceUnroll], cl[kReduceUnroll];
+            float4 c_lo[kReduceUnroll], c_hi[kReduceUnroll];
+#pragma unroll
+            for (int u = 0; u < kReduceUnroll; ++u) {
+                const int q = c0 + u * qgroups;
+                if (q < nparts) {
+                    cm[u] = p.part_m[hrow + q];
+                    cl[u] = p.part_l[hrow + q];
+                    const float4 *src = reinterpret_cast<const float4 *>(
+                        p.part_o + (hrow + q) * D + d0);
+                    c_lo[u] = src[0];
+                    c_hi[u] = src[1];
+                } else {
+                    cm[u] = -INFINITY;
+                    cl[u] = 0.f;
+                    c_lo[u] = c_hi[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+            }
+            // q = c0 < nparts, so the chunk's maximum is finite
+            float mn = mt;
+#pragma unroll
+            for (int u = 0; u < kReduceUnroll; ++u)
+                mn = fmaxf(mn, cm[u]);
+            const float alpha = exp2f((mt - mn) * kLog2e);  // 0 while mt is -inf
+            lt *= alpha;
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                acc[e] *= alpha;
+#pragma unroll
+            for (int u = 0; u < kReduceUnroll; ++u) {
+                const float w = cl[u] * exp2f((cm[u] - mn) * kLog2e);
+                lt += w;
+                acc[0] += w * c_lo[u].x; acc[1] += w * c_lo[u].y;
+                acc[2] += w * c_lo[u].z; acc[3] += w * c_lo[u].w;
+                acc[4] += w * c_hi[u].x; acc[5] += w * c_hi[u].y;
+                acc[6] += w * c_hi[u].z; acc[7] += w * c_hi[u].w;
+            }
+            mt = mn;
+        }
+    }
+
+    const size_t out_off = ((size_t)s * p.num_heads + (size_t)kh * G + jh) * D + d0;
+    if (qgroups == 1) {
+        if (active) {
+            const float inv = 1.f / lt;
             T vals[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e)
-                vals[e] = Op::from_float(acc[e]);
-            *reinterpret_cast<uint4 *>(static_cast<T *>(p.out) +
-                                       ((size_t)s * p.num_heads + (size_t)kh * G + jh) * D +
-                                       d0) = *reinterpret_cast<const uint4 *>(vals);
-        } else {
-            float4 *dst = reinterpret_cast<float4 *>(red + (size_t)tid * 8);
-            dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-            dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+                vals[e] = Op::from_float(acc[e] * inv);
+            *reinterpret_cast<uint4 *>(static_cast<T *>(p.out) + out_off) =
+                *reinterpret_cast<const uint4 *>(vals);
         }
-    }
-    if (qgroups == 1)
         return;
-    __syncthreads();
-    for (int it = tid; it < items; it += kReduceThreads) {
-        const int jh = it / (D / 8);
-        const int d0 = (it - jh * (D / 8)) * 8;
-        float sum[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        for (int g2 = 0; g2 < qgroups; ++g2) {
-            const float4 *src = reinterpret_cast<const float4 *>(red + (size_t)(g2 * items + it) * 8);
-            const float4 x0 = src[0], x1 = src[1];
-            sum[0] += x0.x; sum[1] += x0.y; sum[2] += x0.z; sum[3] += x0.w;
-            sum[4] += x1.x; sum[5] += x1.y; sum[6] += x1.z; sum[7] += x1.w;
-        }
-        T vals[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e)
-            vals[e] = Op::from_float(sum[e]);
-        *reinterpret_cast<uint4 *>(static_cast<T *>(p.out) +
-                                   ((size_t)s * p.num_heads + (size_t)kh * G + jh) * D + d0) =
-            *reinterpret_cast<const uint4 *>(vals);
     }
+    if (active) {
+        red_m[tid] = mt;
+        red_l[tid] = lt;
+        float4 *dst = reinterpret_cast<float4 *>(red_o + (size_t)tid * 8);
+        dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+        dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+    }
+    __syncthreads();
+    if (tid >= items)
+        return;
+    // group 0 holds q = 0 < nparts: the maximum over groups is finite
+    float mx = -INFINITY;
+    for (int g2 = 0; g2 < qgroups; ++g2)
+        mx = fmaxf(mx, red_m[g2 * items + tid]);
+    float lsum = 0.f;
+    float sum[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int g2 = 0; g2 < qgroups; ++g2) {
+        const int r = g2 * items + tid;
+        const float w = exp2f((red_m[r] - mx) * kLog2e);  // 0 for a group with no partition
+        lsum += w * red_l[r];
+        const float4 *src = reinterpret_cast<const float4 *>(red_o + (size_t)r * 8);
+        const float4 x0 = src[0], x1 = src[1];
+        sum[0] += w * x0.x; sum[1] += w * x0.y; sum[2] += w * x0.z; sum[3] += w * x0.w;
+        sum[4] += w * x1.x; sum[5] += w * x1.y; sum[6] += w * x1.z; sum[7] += w * x1.w;
+    }
+    const float inv = 1.f / lsum;
+    T vals[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+        vals[e] = Op::from_float(sum[e] * inv);
+    *reinterpret_cast<uint4 *>(static_cast<T *>(p.out) + out_off) =
+        *reinterpret_cast<const uint4 *>(vals);
 }
 
 // ---- host side -------------------------------------------------------------------
