@@ -91,6 +91,8 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
         "oracle_paged_attention_fp8": (None, [P, P, P, P, P, i32, P, i32, i32, i32, i32,
                                               i32, dbl, i32, dbl, dbl, P, i32]),
         "oracle_copy_blocks_u8": (None, [P, P, P, i32, i32, i32, i32]),
+        "oracle_prefill_attention": (None, [P, P, P, P, P, i32, P, P, i32, i32, i32,
+                                            i32, i32, dbl, i32]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -212,6 +214,29 @@ def paged_attention(query: np.ndarray, key_cache: np.ndarray,
                                bt.shape[1], _ptr(cl), S, H, Hkv, d, bs,
                                float(scale), dtype, _ptr(sub),
                                0 if sub is None else sub.shape[0])
+    return out
+
+
+def prefill_attention(query: np.ndarray, key_cache: np.ndarray,
+                      value_cache: np.ndarray, block_tables: np.ndarray,
+                      query_start: np.ndarray, context_lens: np.ndarray,
+                      scale: float, dtype: int, lib=None) -> np.ndarray:
+    """Chunked prefill / mixed batch: fp64 output [T, H, d] for the query rows
+    [T, H, d]; sequence s owns rows [query_start[s], query_start[s+1]), the
+    newest tokens of its context, each attending its own position and the
+    earlier ones."""
+    lib = lib or load()
+    q = _u16(query)
+    kc, vc = _u16(key_cache), _u16(value_cache)
+    bt, qs, cl = _i32(block_tables), _i32(query_start), _i32(context_lens)
+    T, H, d = q.shape
+    N, bs, Hkv, d2 = kc.shape
+    S = cl.shape[0]
+    assert d == d2 and H % Hkv == 0 and qs.shape[0] == S + 1 and int(qs[-1]) == T
+    out = np.full((T, H, d), np.nan, dtype=np.float64)
+    lib.oracle_prefill_attention(_ptr(out), _ptr(q), _ptr(kc), _ptr(vc), _ptr(bt),
+                                 bt.shape[1], _ptr(qs), _ptr(cl), S, H, Hkv, d, bs,
+                                 float(scale), dtype)
     return out
 
 

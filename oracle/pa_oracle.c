@@ -19,7 +19,10 @@
  *          §1.5 slot mapping (worked example: position 35, block_size 16,
  *          block_table[2] = 9 -> slot 147), §1.6 paged attention
  *          (gather K over the block table, softmax(q K^T / sqrt(d)),
- *          gather V, weighted sum, truncated to seq_len).
+ *          gather V, weighted sum, truncated to seq_len), §2.4 prefill vs
+ *          decode (a prompt's tokens processed in parallel; a mixed batch of
+ *          decode and prefill requests), §2.5 chunked prefill (a long prompt
+ *          split into chunks of 512 tokens).
  *   [FEI]  "vLLM 架构详解: PagedAttention、Continuous Batching 与生产级推理优化"
  *          (feifeigd.github.io): "Block Table 实现" (append a token's K/V at
  *          its position in the last block), "共享前缀的 Block 复用"
@@ -363,6 +366,51 @@ void oracle_paged_attention(double *out, const uint16_t *query,
             attend_range(o, &m, &l, q_row, key_cache, value_cache, row, 0, ctx,
                          h / group, num_kv_heads, head_dim, block_size, scale,
                          dtype);
+        }
+    }
+}
+
+/* ---- chunked prefill over the paged pool ([GAO] §2.4, §2.5) ----------- */
+
+/* A batch row of sequence s is one of its q_len newest tokens (a prompt
+ * chunk, or q_len = 1 for a decode request in the same mixed batch), whose
+ * K/V are already in the cache.  Reading (the pages show prefill processing
+ * a prompt's tokens in parallel and decode seeing only earlier tokens, and
+ * give no mask): row i of the chunk is the token at position
+ * pos = context_len - q_len + i and attends positions [0, pos], i.e. it is
+ * exactly a decode query over the first pos + 1 tokens.
+ *
+ * out: [num_rows][num_heads][head_dim] doubles; query: [num_rows][num_heads]
+ * [head_dim] with num_rows = query_start[num_seqs]; sequence s owns rows
+ * [query_start[s], query_start[s+1]).  A row whose position is negative
+ * (a chunk longer than its context) attends nothing and gets zeros. */
+void oracle_prefill_attention(double *out, const uint16_t *query,
+                              const uint16_t *key_cache, const uint16_t *value_cache,
+                              const int32_t *block_tables, int max_blocks_per_seq,
+                              const int32_t *query_start, const int32_t *context_lens,
+                              int num_seqs, int num_heads, int num_kv_heads,
+                              int head_dim, int block_size, double scale, int dtype)
+{
+    int group = num_heads / num_kv_heads;
+    for (int s = 0; s < num_seqs; ++s) {
+        const int32_t *row = block_tables + (int64_t)s * max_blocks_per_seq;
+        int64_t q0 = query_start[s], q_len = query_start[s + 1] - query_start[s];
+        int64_t ctx = context_lens[s];
+        for (int64_t i = 0; i < q_len; ++i) {
+            int64_t pos = ctx - q_len + i;
+            for (int h = 0; h < num_heads; ++h) {
+                int64_t r = (q0 + i) * num_heads + h;
+                double *o = out + r * head_dim;
+                if (pos < 0) {
+                    for (int k = 0; k < head_dim; ++k)
+                        o[k] = 0.0;
+                    continue;
+                }
+                double m, l;
+                attend_range(o, &m, &l, query + r * head_dim, key_cache, value_cache, row,
+                             0, pos + 1, h / group, num_kv_heads, head_dim, block_size,
+                             scale, dtype);
+            }
         }
     }
 }

@@ -563,4 +563,79 @@ def pin_fp8_attention_matches_sdpa(lib):
     _close(got, want, 1e-11, 1e-12, "fp8 sdpa")
 
 
+def _prefill_case(rng, ctxs, q_lens, H, Hkv, d, bs, dtype="f16"):
+    """A mixed batch: sequence s has its newest q_lens[s] tokens as query
+    rows (stacked into [T, H, d]) and all ctxs[s] tokens in the pool."""
+    c = random_paged_case(rng, ctxs, H, Hkv, d, bs, dtype=dtype)
+    conv = f16_bits if dtype == "f16" else bf16_bits
+    qs = np.zeros(len(ctxs) + 1, dtype=np.int32)
+    qs[1:] = np.cumsum(q_lens)
+    c["qrows"] = conv(rng.standard_normal((int(qs[-1]), H, d)))
+    c["qs"] = qs
+    return c
+
+
+def _causal_sdpa(c, scale, dec):
+    """torch float64 SDPA per sequence with an explicit mask: chunk row i
+    (position ctx - q_len + i) may see key positions <= its own."""
+    T, H, d = c["qrows"].shape
+    out = np.zeros((T, H, d))
+    for s, ctx in enumerate(c["ctx"]):
+        q0, q1 = int(c["qs"][s]), int(c["qs"][s + 1])
+        n = q1 - q0
+        if n == 0:
+            continue
+        k = torch.from_numpy(dec(c["kl"][s]))
+        v = torch.from_numpy(dec(c["vl"][s]))
+        g = H // k.shape[1]
+        k = k.permute(1, 0, 2).repeat_interleave(g, dim=0)   # [H, ctx, d]
+        v = v.permute(1, 0, 2).repeat_interleave(g, dim=0)
+        q = torch.from_numpy(dec(c["qrows"][q0:q1])).permute(1, 0, 2)  # [H, n, d]
+        pos = int(ctx) - n + torch.arange(n)[:, None]
+        mask = torch.arange(int(ctx))[None, :] <= pos          # [n, ctx]
+        o = torch.nn.functional.scaled_dot_product_attention(
+            q[None], k[None], v[None], attn_mask=mask[None, None], scale=scale)[0]
+        out[q0:q1] = o.permute(1, 0, 2).numpy()
+    return out
+
+
+def pin_prefill_matches_causal_sdpa(lib):
+    """Chunked prefill (GAO §2.4, §2.5): each chunk row attends the cached
+    tokens up to its own position -- torch float64 SDPA with a boolean mask
+    on the gathered K/V; a mixed batch with decode rows (q_len 1), whole
+    prompts (q_len = ctx), chunks in mid-context and an empty chunk."""
+    rng = np.random.default_rng(31)
+    for dtype, (H, Hkv, d, bs) in (("f16", (4, 2, 16, 4)), ("bf16", (6, 3, 8, 8)),
+                                   ("f16", (2, 2, 32, 16))):
+        ctxs, q_lens = [7, 5, 20, 41, 9, 3], [1, 5, 3, 16, 0, 3]
+        c = _prefill_case(rng, ctxs, q_lens, H, Hkv, d, bs, dtype)
+        scale = 1.0 / math.sqrt(d)
+        dt = oracle.F16 if dtype == "f16" else oracle.BF16
+        got = oracle.prefill_attention(c["qrows"], c["kc"], c["vc"], c["tables"], c["qs"],
+                                       c["ctx"], scale, dt, lib=lib)
+        want = _causal_sdpa(c, scale, _dec(dtype))
+        _close(got, want, 1e-11, 1e-12, f"causal sdpa {dtype} {H}/{Hkv}")
+
+
+def pin_prefill_causal_closed_forms(lib):
+    """A whole prompt as one chunk: its first row sees only token 0, so its
+    output is v_0 exactly; poisoning (NaN) the K/V of the last token leaves
+    every earlier row finite and unchanged and makes only the last row NaN."""
+    rng = np.random.default_rng(37)
+    H, Hkv, d, bs, ctx = 4, 2, 16, 4, 11
+    c = _prefill_case(rng, [ctx], [ctx], H, Hkv, d, bs)
+    scale = 0.3
+    args = (c["tables"], c["qs"], c["ctx"], scale, oracle.F16)
+    o = oracle.prefill_attention(c["qrows"], c["kc"], c["vc"], *args, lib=lib)
+    for h in range(H):
+        assert np.array_equal(o[0, h], f16_vals(c["vl"][0][0, h // (H // Hkv)])), "row 0"
+    last_blk, last_off = c["tables"][0][(ctx - 1) // bs], (ctx - 1) % bs
+    kc, vc = c["kc"].copy(), c["vc"].copy()
+    kc[last_blk, last_off] = np.uint16(0x7E00)
+    vc[last_blk, last_off] = np.uint16(0x7E00)
+    o2 = oracle.prefill_attention(c["qrows"], kc, vc, *args, lib=lib)
+    assert np.array_equal(o2[:-1], o[:-1]), "earlier rows changed by a later token"
+    assert np.isnan(o2[-1]).all(), "the last row must see its own token"
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

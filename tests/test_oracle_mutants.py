@@ -104,6 +104,15 @@ MUTANTS = [
     ("fp8_attention_value_scale_is_k_scale",
      "o[i] += scores[p] * (decode_e4m3(value_cache[v + i]) * v_scale);",
      "o[i] += scores[p] * (decode_e4m3(value_cache[v + i]) * k_scale);", 0),
+    ("prefill_excludes_own_token",
+     "                             0, pos + 1, h / group, num_kv_heads, head_dim, block_size,",
+     "                             0, pos, h / group, num_kv_heads, head_dim, block_size,", 0),
+    ("prefill_positions_from_chunk_start",
+     "int64_t pos = ctx - q_len + i;",
+     "int64_t pos = i;", 0),
+    ("prefill_query_row_unshifted",
+     "int64_t r = (q0 + i) * num_heads + h;",
+     "int64_t r = i * num_heads + h;", 0),
     ("fp8_cache_swaps_scales",
      "                             dtype, k_inv_scale);",
      "                             dtype, v_inv_scale);", 0),
