@@ -16,6 +16,11 @@ step (attended K and V bytes / step time, summed over ranks); the roofline
 object reports the attention kernel alone against the measured HBM copy
 bandwidth.  `--impl reference` times the CPU oracle (plain C, fp64) on a
 bounded sample of the same workload.
+
+The chunked-prefill workloads (`--config chunked`, `mixed`) report the
+attention's tensor throughput instead (TFLOP/s of the step, roofline against
+the measured sustained bf16 tensor rate); `prefix-cascade` is the
+prefix-sharing step decoded with the shared prefix read once per group.
 """
 from __future__ import annotations
 
@@ -37,6 +42,7 @@ import numpy as np  # noqa: E402
 
 METRIC = ("paged decode attention effective KV GB/s and % of GB300 HBM peak; "
           "seqs/s per step")
+PREFILL_METRIC = "chunked-prefill paged attention TFLOP/s; tokens/s per step"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 DECODE_SRC = os.path.join(ROOT, "paged_kv_cache_96_gb300", "csrc", "pa_decode.cu")
@@ -51,7 +57,7 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--config", default="gqa70b",
                     choices=["tiny", "mha7b", "gqa70b", "longctx", "prefix", "gqa70b-fp8",
-                             "longctx-fp8"])
+                             "longctx-fp8", "prefix-cascade", "mixed", "chunked"])
     ap.add_argument("--partition", type=int, default=None,
                     help="split-context partition tokens (0 = single pass)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
@@ -150,6 +156,15 @@ class ClockSampler:
 
 # ---------------------------------------------------------------------------
 
+def measured_tensor_peak():
+    """Sustained bf16 tensor rate (a kernel timed inside a long loop)."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops_sustained"]), "measured sustained"
+    except (OSError, KeyError, ValueError):
+        return 1700.0, "fallback sustained"
+
+
 def measured_hbm_peak():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -175,6 +190,17 @@ def recorded_traffic():
 
 def workload_config(w, partition_size, world=1):
     kv = w.kv_bytes()
+    if w.prefill:
+        return {
+            "workload": f"{w.spec.name}: {w.spec.description}",
+            "num_seqs": w.S, "query_rows": w.T, "num_heads": w.H, "num_kv_heads": w.Hkv,
+            "head_dim": w.D, "block_size": w.bs, "num_blocks": w.num_blocks,
+            "context_tokens": int(w.context_lens.sum()),
+            "attention_flops_per_step": w.prefill_flops(),
+            "l2": "compute-bound step; K/V re-reads hit L2 by design, no flush",
+            "parallelism": "replicas" if world > 1 else "single GPU",
+            "kv_cache_dtype": w.dtype,
+        }
     return {
         "workload": f"{w.spec.name}: {w.spec.description}",
         "num_seqs": w.S, "num_heads": w.H, "num_kv_heads": w.Hkv, "head_dim": w.D,
@@ -207,10 +233,12 @@ class OracleCache:
             o.reshape_and_cache(k, v, self.kc, self.vc, slots)
 
     def new_tokens(self, seqs):
+        """The step's new tokens of the listed sequences (one each for
+        decode, the chunk for prefill)."""
         o, w = self.o, self.w
-        seqs = np.asarray(seqs, dtype=np.int32)
-        sl = o.slot_mapping(w.block_tables, w.new_seq[seqs], w.new_pos[seqs], w.bs)
-        self.write(w.new_key[seqs], w.new_value[seqs], sl)
+        idx = np.nonzero(np.isin(w.new_seq, np.asarray(seqs, dtype=np.int32)))[0]
+        sl = o.slot_mapping(w.block_tables, w.new_seq[idx], w.new_pos[idx], w.bs)
+        self.write(w.new_key[idx], w.new_value[idx], sl)
 
     def copy_blocks(self):
         o, w = self.o, self.w
@@ -219,6 +247,17 @@ class OracleCache:
 
     def attention(self, seqs):
         o, w = self.o, self.w
+        if w.prefill:
+            # the listed sequences' chunk rows
+            qs = w.query_start
+            rows = np.concatenate([np.arange(qs[s], qs[s + 1]) for s in seqs]).astype(np.int64)
+            sq = np.asarray(seqs, dtype=np.int64)
+            sub_qs = np.zeros(len(seqs) + 1, dtype=np.int32)
+            sub_qs[1:] = np.cumsum(qs[sq + 1] - qs[sq])
+            return o.prefill_attention(np.ascontiguousarray(w.query[rows]), self.kc, self.vc,
+                                       np.ascontiguousarray(w.step_block_tables[sq]), sub_qs,
+                                       np.ascontiguousarray(w.context_lens[sq]), w.scale,
+                                       self.dt)
         if w.fp8:
             return o.paged_attention_fp8(w.query, self.kc, self.vc, w.step_block_tables,
                                          w.context_lens, w.scale, self.dt, w.spec.kv_scale,
@@ -227,11 +266,18 @@ class OracleCache:
                                  w.context_lens, w.scale, self.dt, seqs=seqs)
 
 
+def _seq_flops(w, s):
+    """Attention multiply-adds x 2 of sequence s's rows (prefill)."""
+    n = int(w.query_start[s + 1] - w.query_start[s])
+    pos1 = int(w.context_lens[s]) - n + np.arange(1, n + 1)
+    return 4 * w.D * w.H * int(np.maximum(pos1, 0).sum())
+
+
 def cpu_baseline_sample(w, target_s: float):
     """Time the oracle's step (new-token writes + attention) on the first
     sequences of the workload until about target_s seconds of CPU work."""
     oc = OracleCache(w)
-    done, tokens, elapsed = [], 0, 0.0
+    done, tokens, elapsed, flops = [], 0, 0.0, 0
     for s in range(w.S):
         t0 = time.perf_counter()
         oc.new_tokens([s])
@@ -239,8 +285,16 @@ def cpu_baseline_sample(w, target_s: float):
         elapsed += time.perf_counter() - t0
         done.append(s)
         tokens += int(w.context_lens[s])
+        if w.prefill:
+            flops += _seq_flops(w, s)
         if elapsed >= target_s:
             break
+    if w.prefill:
+        return {"value": flops / elapsed / 1e12, "unit": "TFLOP/s", "cores": 1,
+                "kind": "oracle",
+                "sample": f"{len(done)} of {w.S} sequences ({flops / 1e9:.1f} GFLOP): "
+                          f"chunk writes + fp64 attention of every chunk row, "
+                          f"single-threaded C, {elapsed:.1f} s"}
     kv = tokens * w.Hkv * w.D * 2 * w.kv_elem_bytes
     return {"value": kv / elapsed / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
             "sample": f"{len(done)} of {w.S} sequences ({tokens} attended tokens): "
@@ -258,16 +312,18 @@ def run_reference(args):
     w = W.build(W.CONFIGS[args.config])
     oc = OracleCache(w)
     # per step: a bounded sample of sequences sized for ~2 s of CPU work
+    cost = (lambda s: _seq_flops(w, s)) if w.prefill else (lambda s: int(w.context_lens[s]))
     t0 = time.perf_counter()
     oc.attention([0])
-    per_tok = (time.perf_counter() - t0) / max(1, int(w.context_lens[0]))
+    per_unit = (time.perf_counter() - t0) / max(1, cost(0))
     budget = 2.0
-    sample, toks = [], 0
+    sample, toks, units = [], 0, 0
     for s in range(w.S):
-        if sample and (toks + int(w.context_lens[s])) * per_tok > budget:
+        if sample and (units + cost(s)) * per_unit > budget:
             break
         sample.append(s)
         toks += int(w.context_lens[s])
+        units += cost(s)
 
     def step():
         oc.new_tokens(sample)
@@ -279,19 +335,22 @@ def run_reference(args):
     for _ in range(args.steps):
         step()
     el = time.perf_counter() - t0
-    kv = toks * w.Hkv * w.D * 2 * w.kv_elem_bytes
-    val = kv * args.steps / el / 1e9
+    if w.prefill:
+        val, unit, metric = units * args.steps / el / 1e12, "TFLOP/s", PREFILL_METRIC
+    else:
+        kv = toks * w.Hkv * w.D * 2 * w.kv_elem_bytes
+        val, unit, metric = kv * args.steps / el / 1e9, "GB/s", METRIC
     line = {
-        "impl": "reference", "metric": METRIC, "value": val, "unit": "GB/s",
+        "impl": "reference", "metric": metric, "value": val, "unit": unit,
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": el / args.steps * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": workload_config(w, w.spec.partition_size if args.partition is None
                                   else args.partition),
-        "cpu_baseline": {"value": val, "unit": "GB/s", "cores": 1, "kind": "oracle",
+        "cpu_baseline": {"value": val, "unit": unit, "cores": 1, "kind": "oracle",
                          "sample": f"{len(sample)} of {w.S} sequences ({toks} tokens) "
                                    "per step, fp64 single-threaded C"},
-        "e2e": {"value": val, "unit": "GB/s", "h2d_bytes_per_step": 0,
+        "e2e": {"value": val, "unit": unit, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -356,9 +415,13 @@ def run_ours(args):
     clocks = sampler.summary(t_host0, t_host1) if sampler else None
 
     kv = w.kv_bytes()
-    units = kv * K
+    if w.prefill:
+        per_unit, scale_u = w.prefill_flops(), 1e12   # TFLOP/s
+    else:
+        per_unit, scale_u = kv, 1e9                    # GB/s of attended K/V
+    units = per_unit * K
     max_elapsed, total_units = aggregate(step_s, units, world, device=dev)
-    value = total_units / max_elapsed / 1e9
+    value = total_units / max_elapsed / scale_u
 
     # end to end through the public API: pinned host inputs -> step -> host output
     e2e = None
@@ -376,20 +439,50 @@ def run_ours(args):
         e1.record(stream)
         torch.cuda.synchronize(dev)
         e2e_s = e0.elapsed_time(e1) / 1e3 / Ke
-        e2e = {"value": kv / e2e_s / 1e9 * world, "unit": "GB/s",
+        e2e = {"value": per_unit / e2e_s / scale_u * world,
+               "unit": "TFLOP/s" if w.prefill else "GB/s",
                "h2d_bytes_per_step": host.h2d_bytes, "d2h_bytes_per_step": host.d2h_bytes,
                "us_per_step": e2e_s * 1e6}
 
     if rank != 0:
         return
-    peak, peak_kind = measured_hbm_peak()
-    # HBM minimum: each physical block once (a shared prefix counts once)
-    attn_bytes = w.unique_kv_bytes() + w.qo_bytes()
-    achieved = attn_bytes / attn_s / 1e9
     cpu = None
     if not args.no_cpu_baseline:
         cpu = cpu_baseline_sample(w, args.cpu_seconds)
     per_step = step_s / K
+    if w.prefill:
+        tpeak, tpeak_kind = measured_tensor_peak()
+        flops = w.prefill_flops()
+        achieved = flops / attn_s / 1e12
+        line = {
+            "metric": PREFILL_METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": K, "warmup": args.warmup, "ms_per_step": per_step * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": f"{w.dtype} mma.sync, fp32 accumulate", "data": "synthetic",
+            "config": workload_config(w, 0, world),
+            "tokens_per_s": w.T * world / per_step,
+            "us_per_step": per_step * 1e6,
+            "attention_us": attn_s * 1e6,
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": tpeak,
+                         "unit": "TFLOP/s", "frac": achieved / tpeak, "traffic": None,
+                         "kernel": "pa_prefill_attention (paged_mq_kernel)",
+                         "peak_kind": f"{tpeak_kind} bf16 (cuBLAS)",
+                         "algorithmic_flops_per_launch": flops},
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": st.launches_per_step() * K,
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+        return
+    peak, peak_kind = measured_hbm_peak()
+    # HBM minimum: each physical block once (a shared prefix counts once)
+    attn_bytes = w.unique_kv_bytes() + w.qo_bytes()
+    achieved = attn_bytes / attn_s / 1e9
+    kernel = "pa_decode_attention (paged_decode_kernel + paged_reduce_kernel)"
+    if st.cascade:
+        kernel = ("pa_decode_attention_cascade (paged_decode_kernel + paged_mq_kernel "
+                  "prefix pass + paged_reduce_kernel)")
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": per_step * 1e3, "higher_is_better": True,
@@ -404,8 +497,9 @@ def run_ours(args):
         "attention_us": attn_s * 1e6,
         "unique_kv_gbs": w.unique_kv_bytes() * world / per_step / 1e9,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": recorded_traffic(),
-                     "kernel": "pa_decode_attention (paged_decode_kernel + paged_reduce_kernel)",
+                     "frac": achieved / peak,
+                     "traffic": None if st.cascade else recorded_traffic(),
+                     "kernel": kernel,
                      "peak_kind": f"{peak_kind} copy",
                      "algorithmic_bytes_per_launch": attn_bytes},
         "cpu_baseline": cpu,

@@ -73,6 +73,7 @@ typedef enum {
 #define PA_DEVERR_CONTEXT_RANGE 0x08 /* context_len < 0, > max_context_len or past the table */
 #define PA_DEVERR_TOKEN_RANGE   0x10 /* token's sequence or position outside its table */
 #define PA_DEVERR_TIMEOUT       0x20 /* a bounded wait on staged data gave up */
+#define PA_DEVERR_PREFIX_PLAN   0x40 /* prefix plan inconsistent with the tables or contexts */
 
 /*
  * pa_slot_mapping -- [GAO] §1.5.  For every token t, writes
@@ -216,6 +217,120 @@ PA_API pa_status pa_decode_attention_fp8(void *out, const void *query, const voi
                                          float v_scale, int partition_size, void *workspace,
                                          size_t workspace_bytes, pa_dtype dtype,
                                          int32_t *error_word, void *stream);
+
+/*
+ * pa_prefill_attention -- chunked prefill and mixed batches over the paged
+ * pool, [GAO] §2.4 (prefill processes a prompt's tokens in parallel; a batch
+ * mixes decode requests of one token with prefill requests of many) and
+ * §2.5 (a long prompt is processed in chunks, 512 tokens each).
+ * Sequence s brings q_len = query_start[s+1] - query_start[s] query rows:
+ * its q_len newest tokens, whose K/V have already been written to the pool
+ * (pa_slot_mapping + pa_reshape_and_cache of the same tokens).  Chunk row i
+ * is the token at position pos = context_lens[s] - q_len + i and attends
+ * positions [0, pos] (reading, the pages give no mask: each token sees
+ * itself and the tokens before it, as in decode, which is the q_len = 1
+ * case):
+ *     out[r][h][:] = sum_{p <= pos} softmax_p(scale * q[r][h] . K[p][kh]) V[p][kh][:]
+ * with r = query_start[s] + i and K/V read through block_tables[s] as in
+ * pa_decode_attention.
+ *   out, query  : [num_tokens][num_heads][head_dim], dtype (PA_F16/PA_BF16).
+ *   query_start : int32 [num_seqs + 1] (device), non-decreasing, query_start[0]
+ *                 = 0 and query_start[num_seqs] = num_tokens (host).
+ *   context_lens: int32 [num_seqs] (device), tokens in the pool for s
+ *                 including its chunk; values outside [0, max_context_len] or
+ *                 past the table are clipped and flagged
+ *                 PA_DEVERR_CONTEXT_RANGE.  A row whose position is negative
+ *                 (chunk longer than the context) gets a zero row.
+ * Accumulation fp32 (online softmax), output rounded to nearest even.  No
+ * workspace.  Supported: as pa_decode_attention (FP8 pools: PA_ERR_UNSUPPORTED).
+ */
+PA_API pa_status pa_prefill_attention(void *out, const void *query, const void *key_cache,
+                                      const void *value_cache, const int32_t *block_tables,
+                                      int max_blocks_per_seq, const int32_t *query_start,
+                                      const int32_t *context_lens, int max_context_len,
+                                      int num_seqs, int num_tokens, int num_heads,
+                                      int num_kv_heads, int head_dim, int block_size,
+                                      int num_blocks, float scale, pa_dtype dtype,
+                                      int32_t *error_word, void *stream);
+
+/*
+ * Prefix plan -- which sequences of a decode batch share leading physical
+ * blocks ([FEI] "共享前缀的 Block 复用": block tables that name the same
+ * physical blocks for a common prefix, the blocks' reference counts > 1).
+ * One int32 array, laid out as
+ *     seq_prefix_len[num_seqs]      shared tokens of s's group, 0 if none
+ *     group_start[num_groups + 1]   members of group g: [group_start[g], group_start[g+1])
+ *     group_prefix_len[num_groups]  shared tokens L_g (a multiple of the block size)
+ *     group_members[num_members]    sequence ids, group by group
+ * (pa_prefix_plan_ints gives its length).  The first member of a group is
+ * its leader; every member's first L_g / block_size table entries equal the
+ * leader's, and L_g < every member's context length.
+ */
+PA_API size_t pa_prefix_plan_ints(int num_seqs, int num_groups, int num_members);
+
+/*
+ * pa_plan_prefix_groups -- host (CPU) planner of the prefix plan above, from
+ * host copies of the block tables [num_seqs][max_blocks_per_seq] and context
+ * lengths.  Sequences are ordered by their table rows; runs of sequences
+ * sharing leading blocks become groups, each with the longest prefix all its
+ * members share, split further where a smaller group with a longer prefix
+ * saves more block reads ((members - 1) * L).  A shared prefix stops before
+ * each member's last token and is at least min_shared_blocks blocks long.
+ *   plan: host int32, capacity plan_capacity ints (3 * num_seqs + 1 always
+ *         suffices); num_groups, num_members: out.
+ * Deterministic; allocates only host memory it frees.  Returns
+ * PA_ERR_INVALID_ARG on bad sizes or pointers, PA_ERR_WORKSPACE when the
+ * plan does not fit plan_capacity.
+ */
+PA_API pa_status pa_plan_prefix_groups(const int32_t *block_tables, int max_blocks_per_seq,
+                                       const int32_t *context_lens, int num_seqs,
+                                       int block_size, int min_shared_blocks, int32_t *plan,
+                                       size_t plan_capacity, int *num_groups,
+                                       int *num_members);
+
+/*
+ * pa_cascade_workspace_bytes -- workspace of pa_decode_attention_cascade:
+ * the layout of pa_decode_workspace_bytes with P = 1 + ceil(max_context_len
+ * / partition_size) (1 + 1 for partition_size 0) partials per (sequence,
+ * head); partial 0 is the shared prefix's.
+ */
+PA_API size_t pa_cascade_workspace_bytes(int num_seqs, int num_heads, int num_kv_heads,
+                                         int head_dim, int max_context_len,
+                                         int partition_size);
+
+/*
+ * pa_decode_attention_cascade -- prefix-aware decode: the result of
+ * pa_decode_attention, computed so that each group's shared prefix is read
+ * from HBM once for all of its members instead of once per member.
+ *   1. prefix pass: for every group g and KV head, the decode queries of all
+ *      members (times the G query heads) attend the prefix [0, L_g), read
+ *      through the leader's table, with tensor-core tiles of 64 query rows;
+ *      each (member, head) gets partial 0 = (m, l, o) in the workspace.
+ *   2. partition pass: every sequence attends its own tokens [L, ctx) (L = 0
+ *      outside any group) in partitions of partition_size tokens (0: one).
+ *   3. reduce: log-sum-exp merge of each grouped or split sequence's
+ *      partials; ungrouped single-partition sequences are written by step 2.
+ * All three are queued on `stream` by this call.  prefix_plan is the device
+ * copy of a prefix plan (num_groups, num_members as planned); an
+ * inconsistent plan (a table that differs from the leader's on the prefix,
+ * a prefix not below a member's context or off the 16-token grid, a
+ * member's seq_prefix_len that differs from its group's) sets
+ * PA_DEVERR_PREFIX_PLAN and leaves those rows undefined.  num_groups == 0
+ * is plain split decode.  Other arguments, limits and errors as
+ * pa_decode_attention (16-bit pools).
+ */
+PA_API pa_status pa_decode_attention_cascade(void *out, const void *query, const void *key_cache,
+                                             const void *value_cache,
+                                             const int32_t *block_tables,
+                                             int max_blocks_per_seq,
+                                             const int32_t *context_lens, int max_context_len,
+                                             int num_seqs, int num_heads, int num_kv_heads,
+                                             int head_dim, int block_size, int num_blocks,
+                                             float scale, const int32_t *prefix_plan,
+                                             int num_groups, int num_members,
+                                             int partition_size, void *workspace,
+                                             size_t workspace_bytes, pa_dtype dtype,
+                                             int32_t *error_word, void *stream);
 
 /*
  * pa_decode_attention_noalloc -- no counterpart on the pages: an addition

@@ -28,6 +28,7 @@ DEVERR_PAIR_RANGE = 0x04
 DEVERR_CONTEXT_RANGE = 0x08
 DEVERR_TOKEN_RANGE = 0x10
 DEVERR_TIMEOUT = 0x20
+DEVERR_PREFIX_PLAN = 0x40
 
 
 class PAError(RuntimeError):
@@ -64,6 +65,14 @@ def _load() -> ctypes.CDLL:
                                            f32, P, P]),
         "pa_decode_attention_fp8": (i32, [P, P, P, P, P, i32, P, i32, i32, i32, i32, i32,
                                           i32, i32, f32, f32, f32, i32, P, sz, i32, P, P]),
+        "pa_prefill_attention": (i32, [P, P, P, P, P, i32, P, P, i32, i32, i32, i32, i32,
+                                       i32, i32, i32, f32, i32, P, P]),
+        "pa_prefix_plan_ints": (sz, [i32, i32, i32]),
+        "pa_plan_prefix_groups": (i32, [P, i32, P, i32, i32, i32, P, sz, P, P]),
+        "pa_cascade_workspace_bytes": (sz, [i32, i32, i32, i32, i32, i32]),
+        "pa_decode_attention_cascade": (i32, [P, P, P, P, P, i32, P, i32, i32, i32, i32, i32,
+                                              i32, i32, f32, P, i32, i32, i32, P, sz, i32, P,
+                                              P]),
         "pa_status_string": (ctypes.c_char_p, [i32]),
         "pa_last_cuda_error": (ctypes.c_char_p, []),
         "pa_version": (i32, []),
@@ -281,3 +290,88 @@ def alloc_workspace(num_seqs: int, num_heads: int, num_kv_heads: int, head_dim: 
     if n == 0:
         return None
     return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+def pa_prefill_attention(out: torch.Tensor, query: torch.Tensor, key_cache: torch.Tensor,
+                         value_cache: torch.Tensor, block_tables: torch.Tensor,
+                         query_start: torch.Tensor, context_lens: torch.Tensor,
+                         max_context_len: int, scale: float,
+                         error_word: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Chunked prefill / mixed batch: out and query are [T, H, d]; sequence s
+    owns rows [query_start[s], query_start[s+1]), its newest tokens."""
+    T, H, d = query.shape
+    N, bs, Hkv, d2 = key_cache.shape
+    MB = block_tables.shape[1]
+    S = context_lens.shape[0]
+    if d != d2 or out.shape != query.shape or query_start.shape[0] != S + 1:
+        raise ValueError("shape mismatch")
+    if key_cache.dtype == torch.uint8:
+        raise TypeError("FP8 pools are not supported by pa_prefill_attention")
+    _check("pa_prefill_attention", _lib.pa_prefill_attention(
+        _dev(out, "out", query.dtype), _dev(query, "query", key_cache.dtype),
+        _dev(key_cache, "key_cache"), _dev(value_cache, "value_cache", key_cache.dtype),
+        _dev(block_tables, "block_tables", torch.int32), MB,
+        _dev(query_start, "query_start", torch.int32),
+        _dev(context_lens, "context_lens", torch.int32), int(max_context_len), S, T, H, Hkv,
+        d, bs, N, float(scale), _dtype_code(key_cache), _opt(error_word, "error_word"),
+        _stream(stream)))
+
+
+def pa_plan_prefix_groups(block_tables, context_lens, block_size: int,
+                          min_shared_blocks: int = 1):
+    """Host planner of prefix-aware decode on host (numpy-convertible) int32
+    block tables [S, MB] and context lengths [S].  Returns (plan, num_groups,
+    num_members); plan is an int32 CPU tensor in the layout the cascade
+    decode takes (copy it to the device)."""
+    import numpy as np
+    bt = np.ascontiguousarray(np.asarray(block_tables, dtype=np.int32))
+    cl = np.ascontiguousarray(np.asarray(context_lens, dtype=np.int32))
+    S, MB = bt.shape
+    cap = 3 * S + 1
+    plan = np.zeros(max(cap, 1), dtype=np.int32)
+    ng, nm = ctypes.c_int(0), ctypes.c_int(0)
+    _check("pa_plan_prefix_groups", _lib.pa_plan_prefix_groups(
+        bt.ctypes.data_as(ctypes.c_void_p), MB, cl.ctypes.data_as(ctypes.c_void_p), S,
+        int(block_size), int(min_shared_blocks), plan.ctypes.data_as(ctypes.c_void_p), cap,
+        ctypes.byref(ng), ctypes.byref(nm)))
+    n = int(_lib.pa_prefix_plan_ints(S, ng.value, nm.value))
+    return torch.from_numpy(plan[:n].copy()), ng.value, nm.value
+
+
+def pa_cascade_workspace_bytes(num_seqs: int, num_heads: int, num_kv_heads: int,
+                               head_dim: int, max_context_len: int,
+                               partition_size: int) -> int:
+    return int(_lib.pa_cascade_workspace_bytes(num_seqs, num_heads, num_kv_heads, head_dim,
+                                               max_context_len, partition_size))
+
+
+def pa_decode_attention_cascade(out: torch.Tensor, query: torch.Tensor,
+                                key_cache: torch.Tensor, value_cache: torch.Tensor,
+                                block_tables: torch.Tensor, context_lens: torch.Tensor,
+                                max_context_len: int, scale: float, prefix_plan: torch.Tensor,
+                                num_groups: int, num_members: int, partition_size: int,
+                                workspace: torch.Tensor,
+                                error_word: Optional[torch.Tensor] = None,
+                                stream=None) -> None:
+    """Prefix-aware decode: pa_decode_attention's result with each planned
+    group's shared prefix read once (prefix_plan on the device)."""
+    S, H, d = query.shape
+    N, bs, Hkv, d2 = key_cache.shape
+    MB = block_tables.shape[1]
+    if d != d2 or out.shape != query.shape:
+        raise ValueError("shape mismatch")
+    if key_cache.dtype == torch.uint8:
+        raise TypeError("FP8 pools are not supported by pa_decode_attention_cascade")
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not None:
+        ws_ptr = _dev(workspace, "workspace")
+        ws_bytes = workspace.numel() * workspace.element_size()
+    _check("pa_decode_attention_cascade", _lib.pa_decode_attention_cascade(
+        _dev(out, "out", query.dtype), _dev(query, "query", key_cache.dtype),
+        _dev(key_cache, "key_cache"), _dev(value_cache, "value_cache", key_cache.dtype),
+        _dev(block_tables, "block_tables", torch.int32), MB,
+        _dev(context_lens, "context_lens", torch.int32), int(max_context_len), S, H, Hkv,
+        d, bs, N, float(scale), _dev(prefix_plan, "prefix_plan", torch.int32),
+        int(num_groups), int(num_members), int(partition_size), ws_ptr, ws_bytes,
+        _dtype_code(key_cache), _opt(error_word, "error_word"), _stream(stream)))
+

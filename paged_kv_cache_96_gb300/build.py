@@ -2,8 +2,9 @@
 
     python -m paged_kv_cache_96_gb300.build
 
-compiles every ``csrc/*.cu`` in parallel (one ``-gencode`` each, CUDA
-runtime linked statically) and links ``lib/libpaged_attention.so``.
+compiles every ``csrc/*.cu`` (device code, one ``-gencode`` each) and
+``csrc/*.cpp`` (host-only runtime code) in parallel, CUDA runtime linked
+statically, and links ``lib/libpaged_attention.so``.
 """
 from __future__ import annotations
 
@@ -33,7 +34,7 @@ def nvcc() -> str:
 
 
 def _compile(src: str, verbose_ptxas: bool, objdir: str = OBJDIR, extra=()) -> str:
-    obj = os.path.join(objdir, os.path.basename(src).replace(".cu", ".o"))
+    obj = os.path.join(objdir, os.path.splitext(os.path.basename(src))[0] + ".o")
     cmd = [nvcc(), *ARCH, *NVCC_FLAGS, *extra, "-c", src, "-o", obj]
     if verbose_ptxas:
         cmd += ["-Xptxas", "-v"]
@@ -46,7 +47,7 @@ def _compile(src: str, verbose_ptxas: bool, objdir: str = OBJDIR, extra=()) -> s
 
 
 def sources():
-    return sorted(glob.glob(os.path.join(CSRC, "*.cu")))
+    return sorted(glob.glob(os.path.join(CSRC, "*.cu")) + glob.glob(os.path.join(CSRC, "*.cpp")))
 
 
 def up_to_date() -> bool:

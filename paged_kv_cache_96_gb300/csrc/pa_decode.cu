@@ -46,6 +46,7 @@
 #include <mutex>
 
 #include "pa_decode_common.cuh"
+#include "pa_prefill.cuh"
 
 namespace pa {
 
@@ -64,8 +65,8 @@ template <int D, int NT, int NW, int NST, int EB> struct Layout {
     static constexpr int kMergeL = kMergeM + NW * kHeads * 4;
     static constexpr int kBars = kMergeL + NW * kHeads * 4;
     static constexpr int kFlags = kBars + NW * NST * 8;
-    static constexpr int kSeq = kFlags + NW * NST * 4;  // int ctx[S], int prefix[S + 1]
-    static size_t bytes(int num_seqs) { return 1024 + kSeq + 8 * (size_t)(num_seqs + 1); }
+    static constexpr int kSeq = kFlags + NW * NST * 4;  // int ctx[S], prefix[S + 1], start[S]
+    static size_t bytes(int num_seqs) { return 1024 + kSeq + 4 * (3 * (size_t)num_seqs + 1); }
     static_assert(kBars % 8 == 0, "mbarriers need 8-byte alignment");
     static_assert(kStageBytes % 1024 == 0, "stages must keep 1024-byte alignment");
 };
@@ -106,6 +107,7 @@ __global__ void __launch_bounds__(NW * 32, MINB)
 
     int *ctx_s = reinterpret_cast<int *>(smem + L::kSeq);
     int *pref = ctx_s + S;
+    int *start_s = pref + S + 1;
     volatile int *flags = reinterpret_cast<volatile int *>(smem + L::kFlags);
     float *merge_o = reinterpret_cast<float *>(smem + L::kMergeO);
     float *merge_m = reinterpret_cast<float *>(smem + L::kMergeM);
@@ -130,14 +132,17 @@ __global__ void __launch_bounds__(NW * 32, MINB)
     pdl_wait_primary();
 
     // ---- context lengths and partition prefix sums -----------------------
-    for (int s = tid; s < S; s += kThreads)
-        ctx_s[s] = clamp_context(p, s, blockIdx.x == 0);
+    for (int s = tid; s < S; s += kThreads) {
+        const int c = clamp_context(p, s, blockIdx.x == 0);
+        ctx_s[s] = c;
+        start_s[s] = seq_start_of(p, s, c);
+    }
     __syncthreads();
     if (warp == 0) {
         int carry = 0;
         for (int base = 0; base < S; base += 32) {
             const int s = base + lane;
-            const int n = s < S ? (ctx_s[s] + P - 1) / P : 0;
+            const int n = s < S ? own_partitions(ctx_s[s], start_s[s], P) : 0;
             int x = n;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
@@ -180,7 +185,7 @@ __global__ void __launch_bounds__(NW * 32, MINB)
         }
         s = lo;
         j = q - pref[s];
-        tok0 = j * P;
+        tok0 = start_s[s] + j * P;
         const int tok_end = min(ctx_s[s], tok0 + P);
         ntiles = (tok_end - tok0 + kTileTokens - 1) / kTileTokens;
     };
@@ -234,18 +239,13 @@ __global__ void __launch_bounds__(NW * 32, MINB)
                     tma_load_4d(dst + L::kTileBytes, &tmap_v, bar_of(stage), 0, pkh, prow,
                                 pphys);
                 } else {
-#if PA_DECODE_PACKED5D
-                tma_load_5d(dst, &tmap_k, bar_of(stage), 0, 0, pkh, prow, pphys);
-                tma_load_5d(dst + L::kTileBytes, &tmap_v, bar_of(stage), 0, 0, pkh, prow, pphys);
-#else
 #pragma unroll
-                for (int hf = 0; hf < D / 64; ++hf) {
-                    tma_load_4d(dst + hf * L::kHalfBytes, &tmap_k, bar_of(stage), hf * 64, pkh,
-                                prow, pphys);
-                    tma_load_4d(dst + L::kTileBytes + hf * L::kHalfBytes, &tmap_v,
-                                bar_of(stage), hf * 64, pkh, prow, pphys);
-                }
-#endif
+                    for (int hf = 0; hf < D / 64; ++hf) {
+                        tma_load_4d(dst + hf * L::kHalfBytes, &tmap_k, bar_of(stage), hf * 64,
+                                    pkh, prow, pphys);
+                        tma_load_4d(dst + L::kTileBytes + hf * L::kHalfBytes, &tmap_v,
+                                    bar_of(stage), hf * 64, pkh, prow, pphys);
+                    }
                 }
             } else {
                 flag_error(p.error_word, PA_DEVERR_BLOCK_RANGE);
@@ -273,11 +273,7 @@ __global__ void __launch_bounds__(NW * 32, MINB)
             const int r = token;  // FP8: one 128-byte row per token, chunk 0..7
             return base + r * 128 + (((chunk + 4 * half) ^ (r & 7)) << 4);
         }
-#if PA_DECODE_PACKED5D
-        const int r = token * (D / 64) + half;
-#else
         const int r = half * kTileTokens + token;
-#endif
         return base + r * 128 + ((chunk ^ (r & 7)) << 4);
     };
 
@@ -326,7 +322,8 @@ __global__ void __launch_bounds__(NW * 32, MINB)
         int s, kh, j, tok0, ntiles;
         decode_unit(u, s, kh, j, tok0, ntiles);
         const int tok_end = min(ctx_s[s], tok0 + P);
-        const int nparts = (ctx_s[s] + P - 1) / P;
+        const int nparts = pref[s + 1] - pref[s];
+        const int pbase = start_s[s] > 0 ? 1 : 0;  // partial 0 belongs to the prefix pass
 
         float o[KT][NT][4];
         float mrun[NT][2], lrun[NT][2];
@@ -581,7 +578,7 @@ __global__ void __launch_bounds__(NW * 32, MINB)
             }
             const float inv = p.out_scale / lsum;
             const size_t h = (size_t)kh * G + jh;
-            if (nparts == 1) {
+            if (nparts == 1 && pbase == 0) {
                 T vals[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e)
@@ -591,7 +588,7 @@ __global__ void __launch_bounds__(NW * 32, MINB)
                     *reinterpret_cast<const uint4 *>(vals);
             } else {
                 // partial of partition j, merged by the reduce kernel
-                const size_t idx = ((size_t)s * p.num_heads + h) * p.max_parts + j;
+                const size_t idx = ((size_t)s * p.num_heads + h) * p.max_parts + pbase + j;
                 float4 *dst = reinterpret_cast<float4 *>(p.part_o + idx * D + d0);
                 dst[0] = make_float4(acc[0] * inv, acc[1] * inv, acc[2] * inv, acc[3] * inv);
                 dst[1] = make_float4(acc[4] * inv, acc[5] * inv, acc[6] * inv, acc[7] * inv);
@@ -619,67 +616,6 @@ __global__ void __launch_bounds__(NW * 32, MINB)
 }
 
 // ---- host side -------------------------------------------------------------------
-
-// Tensor map over a pool [num_blocks][block_size][num_kv_heads][head_dim].
-// Default (4-D, dims d, head, token, block): a box of 64 elements x 1 head x
-// 16 tokens x 1 block lands as 16 rows of 128 bytes, 128-byte swizzle; a
-// 16-token K (or V) tile of one KV head takes D / 64 boxes.
-// PA_DECODE_PACKED5D (5-D, the same packed layout with d split into
-// [D/64][64]): one box {64, D/64, 1, 16, 1} brings the whole tile, rows
-// ordered (token, half).
-#ifndef PA_DECODE_PACKED5D
-#define PA_DECODE_PACKED5D 0
-#endif
-static bool encode_pool_map(CUtensorMap *map, const void *pool, pa_dtype dtype,
-                            int num_blocks, int block_size, int num_kv_heads,
-                            int head_dim)
-{
-    EncodeTiledFn fn = get_encode_fn();
-    if (!fn)
-        return false;
-    if (dtype == PA_FP8_E4M3) {
-        // FP8 pools: 1-byte elements, a box of 128 elements (a 128-byte row) x
-        // 1 head x 16 tokens x 1 block, 128-byte swizzle
-        const cuuint64_t dims[4] = {(cuuint64_t)head_dim, (cuuint64_t)num_kv_heads,
-                                    (cuuint64_t)block_size, (cuuint64_t)num_blocks};
-        const cuuint64_t strides[3] = {(cuuint64_t)head_dim,
-                                       (cuuint64_t)num_kv_heads * head_dim,
-                                       (cuuint64_t)block_size * num_kv_heads * head_dim};
-        const cuuint32_t box[4] = {128, 1, (cuuint32_t)kTileTokens, 1};
-        const cuuint32_t estr[4] = {1, 1, 1, 1};
-        return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void *>(pool), dims,
-                  strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-    }
-    const cuuint64_t e = 2;
-    const CUtensorMapDataType ty = dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
-                                                    : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-#if PA_DECODE_PACKED5D
-    const cuuint64_t dims[5] = {64, (cuuint64_t)head_dim / 64, (cuuint64_t)num_kv_heads,
-                                (cuuint64_t)block_size, (cuuint64_t)num_blocks};
-    const cuuint64_t strides[4] = {64 * e, (cuuint64_t)head_dim * e,
-                                   (cuuint64_t)num_kv_heads * head_dim * e,
-                                   (cuuint64_t)block_size * num_kv_heads * head_dim * e};
-    const cuuint32_t box[5] = {64, (cuuint32_t)head_dim / 64, 1, (cuuint32_t)kTileTokens, 1};
-    const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
-    const cuuint32_t rank = 5;
-#else
-    const cuuint64_t dims[4] = {(cuuint64_t)head_dim, (cuuint64_t)num_kv_heads,
-                                (cuuint64_t)block_size, (cuuint64_t)num_blocks};
-    const cuuint64_t strides[3] = {(cuuint64_t)head_dim * e,
-                                   (cuuint64_t)num_kv_heads * head_dim * e,
-                                   (cuuint64_t)block_size * num_kv_heads * head_dim * e};
-    const cuuint32_t box[4] = {64, 1, (cuuint32_t)kTileTokens, 1};
-    const cuuint32_t estr[4] = {1, 1, 1, 1};
-    const cuuint32_t rank = 4;
-#endif
-    const CUresult r = fn(map, ty, rank, const_cast<void *>(pool), dims, strides, box, estr,
-                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
-}
 
 #ifndef PA_DECODE_WARPS
 #define PA_DECODE_WARPS 5
@@ -767,15 +703,28 @@ static pa_status launch_pass(const DecodeParams &prm, const CUtensorMap &mk,
     return launch_pdl(kernel, dim3((unsigned)grid), dim3(kThreads), smem, stream, prm, mk, mv);
 }
 
+// The partition pass, then (prefix-aware decode) the shared-prefix pass, then
+// the reduce when any partial exists; all on one stream, each a programmatic
+// dependent of the one before.
+struct PrefixPass {
+    const MqParams *prm;
+    pa_dtype dtype;
+    const void *key_cache, *value_cache;
+    long long max_units;
+};
+
 template <typename T, typename KV, int D, int NT>
 static pa_status launch_decode(const DecodeParams &prm, const CUtensorMap &mk,
                                const CUtensorMap &mv, cudaStream_t stream,
-                               long long max_units)
+                               long long max_units, const PrefixPass *prefix = nullptr)
 {
     constexpr int kStages = sizeof(KV) == 1 ? kStagesPerWarpFp8 : kStagesPerWarp;
     pa_status st = launch_pass<T, KV, D, NT, kStages>(prm, mk, mv, stream, max_units);
     if (st == PA_ERR_UNSUPPORTED)
         st = launch_pass<T, KV, D, NT, kStagesManySeqs>(prm, mk, mv, stream, max_units);
+    if (st == PA_OK && prefix != nullptr)
+        st = launch_prefix_pass(*prefix->prm, prefix->dtype, prefix->key_cache,
+                                prefix->value_cache, D, stream, prefix->max_units);
     if (st != PA_OK || prm.max_parts <= 1)
         return st;
     return launch_reduce<T, D>(prm, stream);
@@ -886,4 +835,117 @@ extern "C" pa_status pa_decode_attention_fp8(
                     : launch_decode<__nv_bfloat16, U8, 128, 1>(prm, mk, mv, st, max_units);
     return wide ? launch_decode<__half, U8, 128, 2>(prm, mk, mv, st, max_units)
                 : launch_decode<__half, U8, 128, 1>(prm, mk, mv, st, max_units);
+}
+
+extern "C" size_t pa_prefix_plan_ints(int num_seqs, int num_groups, int num_members)
+{
+    if (num_seqs < 0 || num_groups < 0 || num_members < 0)
+        return 0;
+    return (size_t)num_seqs + 2 * (size_t)num_groups + 1 + (size_t)num_members;
+}
+
+extern "C" size_t pa_cascade_workspace_bytes(int num_seqs, int num_heads, int num_kv_heads,
+                                             int head_dim, int max_context_len,
+                                             int partition_size)
+{
+    if (num_seqs < 0 || num_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
+        max_context_len < 0 || partition_size < 0)
+        return 0;
+    const int parts = num_parts(max_context_len, partition_size) + 1;
+    return workspace_layout(num_seqs, num_heads, head_dim, parts).total;
+}
+
+extern "C" pa_status pa_decode_attention_cascade(
+    void *out, const void *query, const void *key_cache, const void *value_cache,
+    const int32_t *block_tables, int max_blocks_per_seq, const int32_t *context_lens,
+    int max_context_len, int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+    int block_size, int num_blocks, float scale, const int32_t *prefix_plan, int num_groups,
+    int num_members, int partition_size, void *workspace, size_t workspace_bytes,
+    pa_dtype dtype, int32_t *error_word, void *stream)
+{
+    if (dtype != PA_F16 && dtype != PA_BF16)
+        return dtype == PA_FP8_E4M3 ? PA_ERR_UNSUPPORTED : PA_ERR_INVALID_ARG;
+    if (num_groups < 0 || num_members < 0 || (num_groups > 0 && num_members < 2 * num_groups))
+        return PA_ERR_INVALID_ARG;
+    if (num_groups == 0)
+        return pa_decode_attention(out, query, key_cache, value_cache, block_tables,
+                                   max_blocks_per_seq, context_lens, max_context_len, num_seqs,
+                                   num_heads, num_kv_heads, head_dim, block_size, num_blocks,
+                                   scale, partition_size, workspace, workspace_bytes, dtype,
+                                   error_word, stream);
+    DecodeParams prm{};
+    const pa_status ok = prepare_decode(
+        &prm, out, query, key_cache, value_cache, block_tables, max_blocks_per_seq,
+        context_lens, max_context_len, num_seqs, num_heads, num_kv_heads, head_dim,
+        block_size, num_blocks, scale, partition_size, workspace, workspace_bytes,
+        error_word);
+    if (ok != PA_OK || num_seqs == 0)
+        return ok;
+    if (prefix_plan == nullptr)
+        return PA_ERR_INVALID_ARG;
+    // partial 0 of every (sequence, head) is reserved for the prefix pass
+    const int parts = prm.max_parts + 1;
+    const WorkspaceLayout wl = workspace_layout(num_seqs, num_heads, head_dim, parts);
+    if (workspace == nullptr || workspace_bytes < wl.total ||
+        (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return PA_ERR_WORKSPACE;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    prm.part_m = reinterpret_cast<float *>(ws + wl.m_off);
+    prm.part_l = reinterpret_cast<float *>(ws + wl.l_off);
+    prm.part_o = reinterpret_cast<float *>(ws + wl.o_off);
+    prm.max_parts = parts;
+    prm.seq_start = prefix_plan;
+
+    MqParams mq{};
+    mq.query = query;
+    mq.block_tables = block_tables;
+    mq.context_lens = context_lens;
+    mq.seq_start = prefix_plan;
+    mq.group_start = prefix_plan + num_seqs;
+    mq.group_prefix = prefix_plan + num_seqs + num_groups + 1;
+    mq.group_members = prefix_plan + num_seqs + 2 * num_groups + 1;
+    mq.part_m = prm.part_m;
+    mq.part_l = prm.part_l;
+    mq.part_o = prm.part_o;
+    mq.error_word = error_word;
+    mq.prefix_mode = 1;
+    mq.num_segments = num_groups;
+    mq.num_seqs = num_seqs;
+    mq.num_heads = num_heads;
+    mq.num_kv_heads = num_kv_heads;
+    mq.group = prm.group;
+    mq.max_blocks_per_seq = max_blocks_per_seq;
+    mq.num_blocks = num_blocks;
+    mq.block_size = block_size;
+    mq.block_shift = prm.block_shift;
+    mq.max_context_len = max_context_len;
+    mq.max_parts = parts;
+    mq.scale_log2 = prm.scale_log2;
+    PrefixPass pp{&mq, dtype, key_cache, value_cache,
+                  ((long long)num_members * prm.group / 64 + num_groups) * num_kv_heads};
+
+    CUtensorMap mk, mv;
+    if (!encode_pool_map(&mk, key_cache, dtype, num_blocks, block_size, num_kv_heads,
+                         head_dim) ||
+        !encode_pool_map(&mv, value_cache, dtype, num_blocks, block_size, num_kv_heads,
+                         head_dim))
+        return PA_ERR_CUDA;
+    const long long max_units = (long long)num_seqs * num_kv_heads * parts;
+    cudaStream_t st = as_stream(stream);
+    const bool bf = dtype == PA_BF16;
+    const bool wide = prm.group > 8;
+    using B16 = __nv_bfloat16;
+    using F16 = __half;
+    if (head_dim == 128) {
+        if (bf)
+            return wide ? launch_decode<B16, B16, 128, 2>(prm, mk, mv, st, max_units, &pp)
+                        : launch_decode<B16, B16, 128, 1>(prm, mk, mv, st, max_units, &pp);
+        return wide ? launch_decode<F16, F16, 128, 2>(prm, mk, mv, st, max_units, &pp)
+                    : launch_decode<F16, F16, 128, 1>(prm, mk, mv, st, max_units, &pp);
+    }
+    if (bf)
+        return wide ? launch_decode<B16, B16, 64, 2>(prm, mk, mv, st, max_units, &pp)
+                    : launch_decode<B16, B16, 64, 1>(prm, mk, mv, st, max_units, &pp);
+    return wide ? launch_decode<F16, F16, 64, 2>(prm, mk, mv, st, max_units, &pp)
+                : launch_decode<F16, F16, 64, 1>(prm, mk, mv, st, max_units, &pp);
 }

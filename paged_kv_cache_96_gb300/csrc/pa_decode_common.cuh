@@ -27,6 +27,7 @@ struct DecodeParams {
     const void *query;
     const int32_t *block_tables;
     const int32_t *context_lens;
+    const int32_t *seq_start;  // prefix-aware decode: first private token per sequence (or null)
     float *part_m;
     float *part_l;
     float *part_o;
@@ -53,13 +54,34 @@ __device__ __forceinline__ int clamp_context(const DecodeParams &p, int s, bool 
     return c;
 }
 
+// First token a sequence's own units attend: 0, or (prefix-aware decode) the
+// length of the shared prefix that the prefix pass covers.  A start outside
+// [0, ctx] or off the 16-token tile grid is ignored here (the prefix pass
+// flags the plan); both the partition pass and the reduce use this rule, so
+// they agree on where a sequence's partials go.
+__device__ __forceinline__ int seq_start_of(const DecodeParams &p, int s, int ctx)
+{
+    if (p.seq_start == nullptr)
+        return 0;
+    const int st = p.seq_start[s];
+    return (st < 0 || st > ctx || (st & (kTileTokens - 1)) != 0) ? 0 : st;
+}
+
+// Partials a sequence leaves in the workspace: its own partitions of
+// [start, ctx), after the prefix pass's partial (index 0) when start > 0.
+__device__ __forceinline__ int own_partitions(int ctx, int start, int part_tokens)
+{
+    return ctx > start ? (ctx - start + part_tokens - 1) / part_tokens : 0;
+}
+
 // ---- split-context reduce ----------------------------------------------------------
 //
 // One CTA per (sequence, KV head).  For the G query heads of the group it
 // merges the nparts partials (m_q, l_q, o_q) of a sequence that spans more
 // than one partition: M = max_q m_q, w_q = l_q exp(m_q - M),
 // out = sum_q w_q o_q / sum_q w_q.  Sequences with one partition were written
-// by the partition pass itself.
+// by the partition pass itself.  With a shared prefix (start > 0) partial 0
+// is the prefix pass's and the sequence's own partitions follow it.
 //
 // Thread (item, qg) -- item = (head, 8 consecutive d) -- takes partitions
 // q = qg, qg + QG, ... in chunks of kReduceUnroll whose loads are all issued
@@ -86,9 +108,10 @@ __global__ void __launch_bounds__(kReduceThreads)
     const int kh = blockIdx.x - s * Hkv;
     const int tid = threadIdx.x;
     const int ctx = clamp_context(p, s, false);
-    const int nparts = (ctx + p.part_tokens - 1) / p.part_tokens;
-    if (nparts <= 1)
-        return;
+    const int start = seq_start_of(p, s, ctx);
+    const int nparts = own_partitions(ctx, start, p.part_tokens) + (start > 0 ? 1 : 0);
+    if (nparts == 0 || (nparts == 1 && start == 0))
+        return;  // nothing to merge: the partition pass wrote the row
 
     // G * D / 8 <= 16 * 128 / 8 = kReduceThreads: one (item, qg) per thread.
     static_assert(16 * D / 8 <= kReduceThreads, "one work item per thread");
@@ -214,6 +237,37 @@ static EncodeTiledFn get_encode_fn()
             fn = reinterpret_cast<EncodeTiledFn>(ptr);
     });
     return fn;
+}
+
+// Tensor map over a pool [num_blocks][block_size][num_kv_heads][head_dim]
+// (dims d, head, token, block).  16-bit pools: a box of 64 elements x 1 head
+// x 16 tokens x 1 block lands as 16 rows of 128 bytes with the 128-byte
+// swizzle; a 16-token tile of one KV head takes head_dim / 64 boxes.  FP8
+// pools: a box of 128 one-byte elements (one 128-byte row) x 1 head x 16
+// tokens x 1 block.
+static bool encode_pool_map(CUtensorMap *map, const void *pool, pa_dtype dtype,
+                            int num_blocks, int block_size, int num_kv_heads,
+                            int head_dim)
+{
+    EncodeTiledFn fn = get_encode_fn();
+    if (!fn)
+        return false;
+    const bool fp8 = dtype == PA_FP8_E4M3;
+    const cuuint64_t e = fp8 ? 1 : 2;
+    const CUtensorMapDataType ty = fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                   : dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                      : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    const cuuint64_t dims[4] = {(cuuint64_t)head_dim, (cuuint64_t)num_kv_heads,
+                                (cuuint64_t)block_size, (cuuint64_t)num_blocks};
+    const cuuint64_t strides[3] = {(cuuint64_t)head_dim * e,
+                                   (cuuint64_t)num_kv_heads * head_dim * e,
+                                   (cuuint64_t)block_size * num_kv_heads * head_dim * e};
+    const cuuint32_t box[4] = {fp8 ? 128u : 64u, 1, (cuuint32_t)kTileTokens, 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    return fn(map, ty, 4, const_cast<void *>(pool), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // Per-device facts and per-kernel launch settings, looked up once: the SM

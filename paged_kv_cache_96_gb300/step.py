@@ -1,14 +1,17 @@
-"""One paged decode step on the GPU, driven through the C ABI.
+"""One paged attention step on the GPU, driven through the C ABI.
 
-A decode step, in the order the serving engine of the pages runs it
+A step, in the order the serving engine of the pages runs it
 ("vLLM源码解析(二)" §4.1 engine step; "PagedAttention & Continuous
-Batching" §1.5, §1.6):
+Batching" §1.5, §1.6, §2.4, §2.5):
 
-  1. slot mapping of the step's new tokens (one per running sequence),
+  1. slot mapping of the step's new tokens (one per running sequence for
+     decode; a chunk of tokens per sequence for chunked prefill),
   2. reshape_and_cache of their K/V into the paged pools,
   3. copy-on-write block copies, when the step has any,
-  4. paged decode attention of every sequence over its whole context
-     (single pass, or split-context partitions merged in the same launch).
+  4. attention: paged decode of every sequence over its whole context
+     (single pass, or split-context partitions merged by a reduce; with a
+     prefix plan, each group's shared prefix read once), or, for a prefill
+     step, each chunk row over the context up to its own position.
 
 Torch provides device memory and the stream; every step above is a kernel
 of ``libpaged_attention.so``.
@@ -69,11 +72,25 @@ class DecodeStep:
         self.new_key = _t16(w.new_key, dt, self.device)
         self.new_value = _t16(w.new_value, dt, self.device)
         self.cow_pairs = _ti(w.cow_pairs, self.device) if w.cow_pairs.shape[0] else None
-        self.slots = torch.empty(w.S, dtype=torch.int32, device=self.device)
-        self.out = torch.empty((w.S, w.H, w.D), dtype=self.torch_dtype, device=self.device)
+        self.query_start = _ti(w.query_start, self.device)
+        self.slots = torch.empty(w.new_seq.shape[0], dtype=torch.int32, device=self.device)
+        self.out = torch.empty((w.T, w.H, w.D), dtype=self.torch_dtype, device=self.device)
         self.error_word = torch.zeros(1, dtype=torch.int32, device=self.device)
-        self.workspace = B.alloc_workspace(w.S, w.H, w.Hkv, w.D, self.max_context_len,
-                                           self.partition_size, device=self.device)
+        self.cascade = bool(w.spec.cascade)
+        self.plan = None
+        if w.prefill:
+            self.workspace = None
+        elif self.cascade:
+            # host planner over the step's tables (the tables attention reads)
+            plan, self.num_groups, self.num_members = B.pa_plan_prefix_groups(
+                w.step_block_tables, w.context_lens, w.bs)
+            self.plan = plan.to(self.device)
+            n = B.pa_cascade_workspace_bytes(w.S, w.H, w.Hkv, w.D, self.max_context_len,
+                                             self.partition_size)
+            self.workspace = torch.zeros(n, dtype=torch.uint8, device=self.device)
+        else:
+            self.workspace = B.alloc_workspace(w.S, w.H, w.Hkv, w.D, self.max_context_len,
+                                               self.partition_size, device=self.device)
         if build_pools:
             self.write_history()
 
@@ -117,7 +134,25 @@ class DecodeStep:
                              error_word=self.error_word, stream=stream)
 
     def attention(self, stream=None, partition_size: Optional[int] = None) -> None:
+        w = self.w
+        if w.prefill:
+            B.pa_prefill_attention(self.out, self.query, self.key_cache, self.value_cache,
+                                   self.step_block_tables, self.query_start,
+                                   self.context_lens, self.max_context_len, w.scale,
+                                   error_word=self.error_word, stream=stream)
+            return
         P = self.partition_size if partition_size is None else partition_size
+        if self.cascade:
+            ws = self.workspace
+            if P != self.partition_size:
+                n = B.pa_cascade_workspace_bytes(w.S, w.H, w.Hkv, w.D, self.max_context_len, P)
+                ws = torch.zeros(n, dtype=torch.uint8, device=self.device)
+            B.pa_decode_attention_cascade(self.out, self.query, self.key_cache,
+                                          self.value_cache, self.step_block_tables,
+                                          self.context_lens, self.max_context_len, w.scale,
+                                          self.plan, self.num_groups, self.num_members, P, ws,
+                                          error_word=self.error_word, stream=stream)
+            return
         ws = self.workspace
         if P != self.partition_size:
             ws = B.alloc_workspace(self.w.S, self.w.H, self.w.Hkv, self.w.D,
@@ -144,10 +179,18 @@ class DecodeStep:
 
     def launches_per_step(self) -> int:
         """Kernels one run() launches: slot mapping, cache write, block copy
-        (when the step has copy-on-write pairs), the attention pass, and the
-        reduce (when some context spans more than one partition)."""
+        (when the step has copy-on-write pairs), the attention pass, the
+        shared-prefix pass (prefix-aware decode with at least one group), and
+        the reduce (when some context spans more than one partition, or a
+        prefix group exists)."""
         n = 3 + (1 if self.cow_pairs is not None else 0)
-        if self.workspace is not None:
+        if self.cascade and self.num_groups > 0:
+            n += 2
+        elif self.workspace is not None and not self.cascade:
+            n += 1
+        elif self.cascade and B.pa_decode_workspace_bytes(
+                self.w.S, self.w.H, self.w.Hkv, self.w.D, self.max_context_len,
+                self.partition_size) > 0:
             n += 1
         return n
 
@@ -176,6 +219,10 @@ class HostStepIO:
                  "step_block_tables", "context_lens"]
         if st.cow_pairs is not None:
             names.append("cow_pairs")
+        if st.w.prefill:
+            names.append("query_start")
+        if st.plan is not None:
+            names.append("plan")
         self.pairs = []
         for n in names:
             dev = getattr(st, n)

@@ -54,6 +54,10 @@ class WorkloadSpec:
     seed: int = 0
     kv_dtype: str = "same"          # "same" (pools in dtype) or "fp8" (e4m3 codes)
     kv_scale: float = 0.0137        # per-pool scale of FP8 codes (K and V)
+    # Chunked prefill / mixed batch: query rows (newest tokens) per sequence,
+    # drawn from (rng, context_lens); None = decode, one row per sequence.
+    query_lens: Optional[Callable[[np.random.Generator, np.ndarray], np.ndarray]] = None
+    cascade: bool = False           # decode with the prefix-aware (cascade) path
 
 
 @dataclasses.dataclass
@@ -69,7 +73,7 @@ class Workload:
     context_lens: np.ndarray        # int32 [S]
     block_tables: np.ndarray        # int32 [S, MB]
     step_block_tables: np.ndarray   # int32 [S, MB]
-    query: np.ndarray               # uint16 [S, H, d]
+    query: np.ndarray               # uint16 [T, H, d] (T = S for decode)
     hist_seq: np.ndarray            # int32 [Th]  tokens cached before the step
     hist_pos: np.ndarray            # int32 [Th]
     hist_key: np.ndarray            # uint16 [Th, Hkv, d]
@@ -81,6 +85,7 @@ class Workload:
     cow_pairs: np.ndarray           # int32 [P, 2]  (src, dst)
     pad_block: int                  # block id that table padding points at
     fill: np.uint16                 # NaN pattern of unowned pool elements
+    query_start: np.ndarray = None  # int32 [S + 1]: query rows of each sequence
 
     # convenience -------------------------------------------------------
     @property
@@ -115,6 +120,30 @@ class Workload:
         return self.spec.kv_dtype == "fp8"
 
     @property
+    def prefill(self) -> bool:
+        """Query rows are chunks of prompts (many per sequence), not one
+        decode token per sequence."""
+        return self.spec.query_lens is not None
+
+    @property
+    def T(self) -> int:
+        """Query rows (= new tokens) of the step."""
+        return int(self.query.shape[0])
+
+    def prefill_flops(self) -> int:
+        """Multiply-adds x 2 of the step's attention: each query row at
+        position pos scores pos + 1 keys (q . k, d products) and sums as many
+        value rows (d products), for every query head."""
+        qs = self.query_start.astype(np.int64)
+        ctx = self.context_lens.astype(np.int64)
+        keys = 0
+        for s in range(self.S):
+            n = int(qs[s + 1] - qs[s])
+            pos1 = ctx[s] - n + np.arange(1, n + 1)
+            keys += int(np.maximum(pos1, 0).sum())
+        return 4 * self.D * self.H * keys
+
+    @property
     def kv_elem_bytes(self) -> int:
         return 1 if self.fp8 else 2
 
@@ -136,16 +165,19 @@ class Workload:
         return int(self.context_lens.astype(np.int64).sum()) * self.Hkv * self.D * 2 * elem
 
     def unique_kv_bytes(self) -> int:
-        """As kv_bytes, but the shared prefix counted once."""
+        """As kv_bytes, but each physical block counted once: the shared
+        prefix once, plus the private copies made by copy-on-write (each
+        remapped sequence reads its copy instead of the shared block)."""
         elem = self.kv_elem_bytes
         pre = self.spec.shared_prefix_tokens
         toks = int(self.context_lens.astype(np.int64).sum())
         if pre:
             toks -= pre * (self.S - 1)
+            toks += self.cow_pairs.shape[0] * self.bs
         return toks * self.Hkv * self.D * 2 * elem
 
     def qo_bytes(self) -> int:
-        return 2 * self.S * self.H * self.D * 2
+        return 2 * self.T * self.H * self.D * 2
 
 
 # ---------------------------------------------------------------------------
@@ -211,30 +243,41 @@ def build(spec: WorkloadSpec, seed: Optional[int] = None) -> Workload:
         cursor += k
     assert cursor == needed
 
+    # Query rows per sequence: its newest q_len tokens (one for decode).
+    if spec.query_lens is not None:
+        ql = np.asarray(spec.query_lens(rng, ctx), dtype=np.int64)
+        assert ql.shape == (S,) and (ql >= 0).all() and (ql <= ctx - pre).all()
+    else:
+        ql = np.ones(S, dtype=np.int64)
+    query_start = np.zeros(S + 1, dtype=np.int32)
+    query_start[1:] = np.cumsum(ql)
+    T = int(query_start[-1])
+
     # Tokens cached before the step: the shared prefix once (through
     # sequence 0, whose table names the shared blocks), then each
-    # sequence's private history; the last position of every sequence is
-    # the token the step appends.
+    # sequence's private history; the newest q_len positions of every
+    # sequence are the tokens the step appends.
     hist_seq, hist_pos = [], []
     if pre:
         hist_seq.append(np.zeros(pre, dtype=np.int32))
         hist_pos.append(np.arange(pre, dtype=np.int32))
     for s in range(S):
-        lo, hi = pre, int(ctx[s]) - 1
+        lo, hi = pre, int(ctx[s] - ql[s])
         if hi > lo:
             hist_seq.append(np.full(hi - lo, s, dtype=np.int32))
             hist_pos.append(np.arange(lo, hi, dtype=np.int32))
     hist_seq = np.concatenate(hist_seq) if hist_seq else np.zeros(0, np.int32)
     hist_pos = np.concatenate(hist_pos) if hist_pos else np.zeros(0, np.int32)
     Th = hist_seq.shape[0]
-    new_seq = np.arange(S, dtype=np.int32)
-    new_pos = (ctx - 1).astype(np.int32)
+    new_seq = np.repeat(np.arange(S, dtype=np.int32), ql)
+    new_pos = np.concatenate([np.arange(ctx[s] - ql[s], ctx[s]) for s in range(S)]
+                             ).astype(np.int32) if T else np.zeros(0, np.int32)
 
-    query = _normal16(rng, (S, H, D), spec.dtype)
+    query = _normal16(rng, (T, H, D), spec.dtype)
     hist_key = _normal16(rng, (Th, Hkv, D), spec.dtype)
     hist_value = _normal16(rng, (Th, Hkv, D), spec.dtype)
-    new_key = _normal16(rng, (S, Hkv, D), spec.dtype)
-    new_value = _normal16(rng, (S, Hkv, D), spec.dtype)
+    new_key = _normal16(rng, (T, Hkv, D), spec.dtype)
+    new_value = _normal16(rng, (T, Hkv, D), spec.dtype)
 
     # Copy-on-write: distinct shared blocks are copied into distinct free
     # blocks, and one sequence per pair has its table entry remapped to the
@@ -262,7 +305,7 @@ def build(spec: WorkloadSpec, seed: Optional[int] = None) -> Workload:
                     query=query, hist_seq=hist_seq, hist_pos=hist_pos,
                     hist_key=hist_key, hist_value=hist_value, new_seq=new_seq,
                     new_pos=new_pos, new_key=new_key, new_value=new_value,
-                    cow_pairs=cow, pad_block=pad_block, fill=fill)
+                    cow_pairs=cow, pad_block=pad_block, fill=fill, query_start=query_start)
 
 
 # ---------------------------------------------------------------------------
@@ -335,6 +378,34 @@ CONFIGS: Dict[str, WorkloadSpec] = {
 }
 
 
+def _fixed_q(values):
+    return lambda rng, ctx: np.asarray(values, dtype=np.int64)
+
+
+# Prefill-side workloads ("PagedAttention & Continuous Batching" §2.4, §2.5)
+# and the prefix-aware decode of the prefix-sharing step.
+CONFIGS["mixed"] = WorkloadSpec(
+    name="mixed", seed=9606,
+    description="mixed batch of the continuous-batching iteration: 2 decode requests "
+                "(1 token; contexts 37, 70) + 2 fresh prompts prefilled whole (50 and "
+                "30 tokens), 8 query heads over 2 KV heads, d 64, block 16, fp16",
+    num_seqs=4, num_heads=8, num_kv_heads=2, head_dim=64, block_size=16, dtype="f16",
+    context_lens=_fixed([37, 70, 50, 30]), query_lens=_fixed_q([1, 1, 50, 30]),
+    partition_size=0)
+CONFIGS["chunked"] = WorkloadSpec(
+    name="chunked", seed=9607,
+    description="chunked-prefill iteration: four 2048-token prompts, each at a "
+                "different 512-token chunk (contexts 512, 1024, 1536, 2048; 2048 "
+                "batched tokens), 64 query heads over 8 KV heads, d 128, block 16, bf16",
+    num_seqs=4, num_heads=64, num_kv_heads=8, head_dim=128, block_size=16, dtype="bf16",
+    context_lens=_fixed([512, 1024, 1536, 2048]), query_lens=_fixed_q([512] * 4),
+    partition_size=0)
+CONFIGS["prefix-cascade"] = dataclasses.replace(
+    CONFIGS["prefix"], name="prefix-cascade", cascade=True,
+    description=CONFIGS["prefix"].description + "; prefix-aware decode (shared "
+    "prefix read once per group)")
+
+
 def fp8_variant(spec: WorkloadSpec) -> WorkloadSpec:
     """The same workload with e4m3 KV pools ("--kv-cache-dtype fp8")."""
     return dataclasses.replace(spec, name=spec.name + "-fp8", kv_dtype="fp8",
@@ -367,8 +438,15 @@ def small_variant(name: str, seed: int = 0) -> WorkloadSpec:
                                    num_seqs=5, num_heads=8, num_kv_heads=2,
                                    context_lens=_long_skew(2, 1500, 3, 1, 120),
                                    partition_size=256)
-    if name == "prefix":
-        return dataclasses.replace(base, name="prefix-small", seed=seed or 19605,
+    if name == "mixed":
+        return dataclasses.replace(base, seed=seed or base.seed)
+    if name == "chunked":
+        return dataclasses.replace(base, name="chunked-small", seed=seed or 19607,
+                                   num_seqs=4, num_heads=16, num_kv_heads=2,
+                                   context_lens=_fixed([100, 300, 513, 7]),
+                                   query_lens=_fixed_q([100, 64, 129, 1]))
+    if name in ("prefix", "prefix-cascade"):
+        return dataclasses.replace(base, name=name + "-small", seed=seed or 19605,
                                    num_seqs=6, num_heads=8, num_kv_heads=2,
                                    context_lens=_prefix_plus(6, 128, 1, 200),
                                    shared_prefix_tokens=128, cow_pairs=4,

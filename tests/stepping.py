@@ -45,8 +45,26 @@ class OracleStep:
         else:
             oracle.reshape_and_cache(k, v, kc, vc, slots)
 
-    def attention(self, seqs=None):
+    def attention(self, seqs=None, rows=None):
+        """Decode: [S, H, d] (rows of `seqs` only, if given).  Prefill:
+        [T, H, d] for every chunk row, or [len(rows), H, d] for the listed
+        rows -- computed as a batch of one-row chunks, each with its own
+        sequence's table and the context ending at the row's position."""
         w = self.w
+        if w.prefill:
+            if rows is None:
+                return oracle.prefill_attention(w.query, self.key_cache, self.value_cache,
+                                                w.step_block_tables, w.query_start,
+                                                w.context_lens, w.scale, odt(w))
+            rows = np.asarray(rows, dtype=np.int64)
+            seq_of = np.searchsorted(w.query_start, rows, side="right") - 1
+            q_len = w.query_start[seq_of + 1] - w.query_start[seq_of]
+            pos = w.context_lens[seq_of] - q_len + (rows - w.query_start[seq_of])
+            qs = np.arange(rows.shape[0] + 1, dtype=np.int32)
+            return oracle.prefill_attention(
+                np.ascontiguousarray(w.query[rows]), self.key_cache, self.value_cache,
+                np.ascontiguousarray(w.step_block_tables[seq_of]), qs,
+                (pos + 1).astype(np.int32), w.scale, odt(w))
         if w.fp8:
             return oracle.paged_attention_fp8(w.query, self.key_cache, self.value_cache,
                                               w.step_block_tables, w.context_lens, w.scale,

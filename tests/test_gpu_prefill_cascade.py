@@ -1,0 +1,234 @@
+"""Chunked prefill / mixed batches and prefix-aware (cascade) decode on the
+GPU against the CPU oracle: slots and pools bit-exact; attention within the
+contract tolerance on every row; invariants; plan and index errors flagged
+on the device without a fault."""
+import numpy as np
+import pytest
+import torch
+
+pytestmark = pytest.mark.gpu
+
+import oracle  # noqa: E402
+from paged_kv_cache_96_gb300 import workloads as W  # noqa: E402
+from stepping import OracleStep, assert_attention_close  # noqa: E402
+
+
+@pytest.fixture(scope="module")
+def B():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from paged_kv_cache_96_gb300 import binding
+    return binding
+
+
+@pytest.fixture(scope="module")
+def S():
+    from paged_kv_cache_96_gb300 import step
+    return step
+
+
+@pytest.fixture(scope="module")
+def small():
+    cache = {}
+
+    def get(name):
+        if name not in cache:
+            w = W.build(W.small_variant(name))
+            cache[name] = (w, OracleStep(w))
+        return cache[name]
+    return get
+
+
+# ---- chunked prefill / mixed batch ------------------------------------------------
+
+@pytest.mark.parametrize("name", ["mixed", "chunked"])
+def test_prefill_step_matches_oracle(B, S, small, name):
+    w, ref = small(name)
+    st = S.DecodeStep(w)
+    out = st.run()
+    torch.cuda.synchronize()
+    assert int(st.error_word.item()) == 0
+    assert np.array_equal(st.slots.cpu().numpy().astype(np.int64), ref.new_slots)
+    assert np.array_equal(S.to_bits(st.key_cache), ref.key_cache)
+    assert np.array_equal(S.to_bits(st.value_cache), ref.value_cache)
+    assert_attention_close(S.to_float(out), ref.attention(), name)
+
+
+def test_prefill_rows_subset_matches_whole(B, S, small):
+    """The sampled-row oracle used at full size agrees with the whole-batch
+    oracle (and so with the GPU) on the reduced workload."""
+    w, ref = small("chunked")
+    rows = [0, 1, 99, 100, 163, 164, 200, 292, 293]
+    assert np.array_equal(ref.attention(rows=rows), ref.attention()[rows])
+
+
+def test_prompt_first_row_is_value_row(B, S, small):
+    """A prompt prefilled whole: its first row sees only token 0, so the
+    output is that token's value row, bit for bit."""
+    w, _ = small("mixed")
+    st = S.DecodeStep(w)
+    out = S.to_bits(st.run())
+    G = w.H // w.Hkv
+    whole = [s for s in range(w.S)
+             if w.query_start[s + 1] - w.query_start[s] == w.context_lens[s]]
+    assert whole
+    for s in whole:
+        r = int(w.query_start[s])
+        for h in range(w.H):
+            assert np.array_equal(out[r, h], w.new_value[r, h // G])
+
+
+def test_prefill_block_placement_invariance(B, S, small):
+    w, _ = small("chunked")
+    st = S.DecodeStep(w)
+    a = st.run().clone()
+    g = torch.Generator().manual_seed(5)
+    perm = torch.randperm(w.num_blocks, generator=g).to("cuda")
+    kc2 = torch.empty_like(st.key_cache)
+    vc2 = torch.empty_like(st.value_cache)
+    kc2[perm] = st.key_cache
+    vc2[perm] = st.value_cache
+    t2 = perm[st.step_block_tables.long()].to(torch.int32)
+    b = torch.full_like(a, float("nan"))
+    B.pa_prefill_attention(b, st.query, kc2, vc2, t2, st.query_start, st.context_lens,
+                           st.max_context_len, w.scale)
+    assert torch.equal(a, b)
+
+
+def test_prefill_index_errors_are_flagged(B, S, small):
+    w, _ = small("chunked")
+    st = S.DecodeStep(w)
+    st.run()
+    torch.cuda.synchronize()
+    tables = st.step_block_tables.clone()
+    tables[2, 1] = w.num_blocks + 7
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = torch.empty_like(st.out)
+    B.pa_prefill_attention(out, st.query, st.key_cache, st.value_cache, tables,
+                           st.query_start, st.context_lens, st.max_context_len, w.scale,
+                           error_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & B.DEVERR_BLOCK_RANGE
+    ctx = st.context_lens.clone()
+    ctx[0] = st.max_context_len + 50
+    err.zero_()
+    B.pa_prefill_attention(out, st.query, st.key_cache, st.value_cache,
+                           st.step_block_tables, st.query_start, ctx, st.max_context_len,
+                           w.scale, error_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & B.DEVERR_CONTEXT_RANGE
+
+
+def test_prefill_host_errors(B, S, small):
+    w, _ = small("chunked")
+    st = S.DecodeStep(w, build_pools=False)
+    with pytest.raises(ValueError):
+        B.pa_prefill_attention(st.out, st.query, st.key_cache, st.value_cache,
+                               st.step_block_tables, st.query_start[:-1], st.context_lens,
+                               st.max_context_len, w.scale)
+    lib = B.lib()
+    r = lib.pa_prefill_attention(None, None, None, None, None, 1, None, None, 16, 1, 1, 8, 2,
+                                 96, 16, 4, 1.0, 1, None, None)
+    assert r == B.PA_ERR_UNSUPPORTED or r == B.PA_ERR_INVALID_ARG
+    r = lib.pa_prefill_attention(None, None, None, None, None, 1, None, None, 16, 1, 1, 8, 3,
+                                 128, 16, 4, 1.0, 1, None, None)
+    assert r == B.PA_ERR_INVALID_ARG
+
+
+# ---- prefix-aware (cascade) decode -------------------------------------------------
+
+@pytest.mark.parametrize("P", [0, 48, 128])
+def test_cascade_step_matches_oracle(B, S, small, P):
+    w, ref = small("prefix-cascade")
+    st = S.DecodeStep(w, partition_size=P)
+    assert st.num_groups >= 1
+    out = st.run()
+    torch.cuda.synchronize()
+    assert int(st.error_word.item()) == 0
+    assert np.array_equal(S.to_bits(st.key_cache), ref.key_cache)
+    assert np.array_equal(S.to_bits(st.value_cache), ref.value_cache)
+    assert_attention_close(S.to_float(out), ref.attention(), f"cascade P={P}")
+
+
+def test_cascade_prefix_partial_matches_oracle(B, S, small):
+    """Partial 0 of every grouped (sequence, head) is the attention over the
+    group's shared prefix: the oracle's first partition of that length."""
+    w, ref = small("prefix-cascade")
+    st = S.DecodeStep(w, partition_size=0)
+    st.run()
+    torch.cuda.synchronize()
+    plan = st.plan.cpu().numpy()
+    Sn, H, D = w.S, w.H, w.D
+    ng = st.num_groups
+    gstart = plan[Sn:Sn + ng + 1]
+    gprefix = plan[Sn + ng + 1:Sn + 2 * ng + 1]
+    members = plan[Sn + 2 * ng + 1:]
+    parts = 2  # partition_size 0: the prefix's partial + one own partition
+    ws = st.workspace
+
+    def a256(x):
+        return (x + 255) // 256 * 256
+    n_ml = Sn * H * parts
+
+    def region(off, count):
+        return ws[off:off + 4 * count].view(torch.float32).cpu().numpy().astype(np.float64)
+    m_g = region(0, n_ml).reshape(Sn, H, parts)
+    l_g = region(a256(4 * n_ml), n_ml).reshape(Sn, H, parts)
+    o_g = region(2 * a256(4 * n_ml), n_ml * D).reshape(Sn, H, parts, D)
+    for g in range(ng):
+        L = int(gprefix[g])
+        mem = members[gstart[g]:gstart[g + 1]].tolist()
+        m_o, l_o, o_o = ref.partitions(L, 1, seqs=mem)
+        for s in mem:
+            lse_g = m_g[s, :, 0] + np.log(l_g[s, :, 0])
+            lse_o = m_o[s, :, 0] + np.log(l_o[s, :, 0])
+            assert np.allclose(lse_g, lse_o, atol=1e-3, rtol=1e-4), s
+            assert_attention_close(o_g[s, :, 0], o_o[s, :, 0], f"prefix partial s={s}")
+
+
+def test_cascade_without_groups_is_plain_decode(B, S, small):
+    w, _ = small("gqa70b")
+    st = S.DecodeStep(w)
+    st.run()
+    plan, ng, nm = B.pa_plan_prefix_groups(w.step_block_tables, w.context_lens, w.bs)
+    assert ng == 0
+    P = w.spec.partition_size
+    ws = torch.zeros(B.pa_cascade_workspace_bytes(w.S, w.H, w.Hkv, w.D, st.max_context_len, P),
+                     dtype=torch.uint8, device="cuda")
+    a = torch.empty_like(st.out)
+    B.pa_decode_attention_cascade(a, st.query, st.key_cache, st.value_cache,
+                                  st.step_block_tables, st.context_lens, st.max_context_len,
+                                  w.scale, plan.cuda(), ng, nm, P, ws)
+    st.attention()
+    assert torch.equal(a, st.out)
+
+
+def test_cascade_bad_plan_is_flagged(B, S, small):
+    """A plan whose member records another prefix length, or whose member's
+    table differs from the leader's on the prefix, sets the plan error bit;
+    nothing faults."""
+    w, _ = small("prefix-cascade")
+    st = S.DecodeStep(w)
+    st.run()
+    torch.cuda.synchronize()
+    Sn = w.S
+    ng = st.num_groups
+    plan = st.plan.clone()
+    member = int(plan[Sn + 2 * ng + 1 + 1])
+    plan[member] = plan[member] + w.bs  # seq_prefix_len disagrees with its group
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = torch.empty_like(st.out)
+    B.pa_decode_attention_cascade(out, st.query, st.key_cache, st.value_cache,
+                                  st.step_block_tables, st.context_lens, st.max_context_len,
+                                  w.scale, plan, ng, st.num_members, 0, st.workspace,
+                                  error_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & B.DEVERR_PREFIX_PLAN
+    tables = st.step_block_tables.clone()
+    tables[member, 0] = (int(tables[member, 0]) + 1) % w.num_blocks
+    err.zero_()
+    B.pa_decode_attention_cascade(out, st.query, st.key_cache, st.value_cache, tables,
+                                  st.context_lens, st.max_context_len, w.scale, st.plan, ng,
+                                  st.num_members, 0, st.workspace, error_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & B.DEVERR_PREFIX_PLAN
