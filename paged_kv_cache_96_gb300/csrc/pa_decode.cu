@@ -323,7 +323,8 @@ __global__ void __launch_bounds__(NW * 32, MINB)
         decode_unit(u, s, kh, j, tok0, ntiles);
         const int tok_end = min(ctx_s[s], tok0 + P);
         const int nparts = pref[s + 1] - pref[s];
-        const int pbase = start_s[s] > 0 ? 1 : 0;  // partial 0 belongs to the prefix pass
+        // the first partials belong to the prefix pass
+        const int pbase = prefix_partitions(start_s[s], P);
 
         float o[KT][NT][4];
         float mrun[NT][2], lrun[NT][2];
@@ -883,7 +884,9 @@ extern "C" pa_status pa_decode_attention_cascade(
         return ok;
     if (prefix_plan == nullptr)
         return PA_ERR_INVALID_ARG;
-    // partial 0 of every (sequence, head) is reserved for the prefix pass
+    // the shared prefix [0, L) and the own tokens [L, ctx) are each cut into
+    // partitions of part_tokens: ceil(L / P) + ceil((ctx - L) / P) <=
+    // ceil(ctx / P) + 1 partials per (sequence, head)
     const int parts = prm.max_parts + 1;
     const WorkspaceLayout wl = workspace_layout(num_seqs, num_heads, head_dim, parts);
     if (workspace == nullptr || workspace_bytes < wl.total ||
@@ -920,9 +923,12 @@ extern "C" pa_status pa_decode_attention_cascade(
     mq.block_shift = prm.block_shift;
     mq.max_context_len = max_context_len;
     mq.max_parts = parts;
+    mq.part_tokens = prm.part_tokens;
     mq.scale_log2 = prm.scale_log2;
+    const long long prefix_parts = (max_context_len + prm.part_tokens - 1) / prm.part_tokens;
     PrefixPass pp{&mq, dtype, key_cache, value_cache,
-                  ((long long)num_members * prm.group / 64 + num_groups) * num_kv_heads};
+                  ((long long)num_members * prm.group / 128 + num_groups) * prefix_parts *
+                      num_kv_heads};
 
     CUtensorMap mk, mv;
     if (!encode_pool_map(&mk, key_cache, dtype, num_blocks, block_size, num_kv_heads,

@@ -68,10 +68,17 @@ __device__ __forceinline__ int seq_start_of(const DecodeParams &p, int s, int ct
 }
 
 // Partials a sequence leaves in the workspace: its own partitions of
-// [start, ctx), after the prefix pass's partial (index 0) when start > 0.
+// [start, ctx), after the prefix pass's partitions of [0, start).
 __device__ __forceinline__ int own_partitions(int ctx, int start, int part_tokens)
 {
     return ctx > start ? (ctx - start + part_tokens - 1) / part_tokens : 0;
+}
+
+// Partials of the shared prefix [0, start): partitions of part_tokens tokens
+// (partial indices 0 .. n-1, ahead of the sequence's own partitions).
+__device__ __forceinline__ int prefix_partitions(int start, int part_tokens)
+{
+    return start > 0 ? (start + part_tokens - 1) / part_tokens : 0;
 }
 
 // ---- split-context reduce ----------------------------------------------------------
@@ -80,8 +87,8 @@ __device__ __forceinline__ int own_partitions(int ctx, int start, int part_token
 // merges the nparts partials (m_q, l_q, o_q) of a sequence that spans more
 // than one partition: M = max_q m_q, w_q = l_q exp(m_q - M),
 // out = sum_q w_q o_q / sum_q w_q.  Sequences with one partition were written
-// by the partition pass itself.  With a shared prefix (start > 0) partial 0
-// is the prefix pass's and the sequence's own partitions follow it.
+// by the partition pass itself.  With a shared prefix (start > 0) the first
+// partials are the prefix pass's and the sequence's own partitions follow.
 //
 // Thread (item, qg) -- item = (head, 8 consecutive d) -- takes partitions
 // q = qg, qg + QG, ... in chunks of kReduceUnroll whose loads are all issued
@@ -109,7 +116,8 @@ __global__ void __launch_bounds__(kReduceThreads)
     const int tid = threadIdx.x;
     const int ctx = clamp_context(p, s, false);
     const int start = seq_start_of(p, s, ctx);
-    const int nparts = own_partitions(ctx, start, p.part_tokens) + (start > 0 ? 1 : 0);
+    const int nparts = own_partitions(ctx, start, p.part_tokens) +
+                       prefix_partitions(start, p.part_tokens);
     if (nparts == 0 || (nparts == 1 && start == 0))
         return;  // nothing to merge: the partition pass wrote the row
 

@@ -1,4 +1,5 @@
-// pa_prefill.cu -- multi-query paged attention for sm_103a.
+// pa_prefill.cu -- multi-query paged attention for sm_103a on the
+// 5th-generation tensor cores (tcgen05, accumulators in tensor memory).
 //
 // Two uses of one kernel:
 //  * Chunked prefill and mixed batches ("PagedAttention & Continuous
@@ -9,22 +10,29 @@
 //    reshape_and_cache before the call).  A decode request is q_len = 1.
 //  * The shared-prefix pass of prefix-aware decode ("vLLM 架构详解",
 //    "共享前缀的 Block 复用": several block tables naming the same physical
-//    blocks): the decode queries of every member of a group attend the
-//    group's shared prefix [0, L) once, read through the first member's
-//    table, and leave a partial (m, l, o) per (sequence, head) for the
-//    split-context reduce to merge with the members' own partitions.
+//    blocks): the decode queries of every member of a group attend each
+//    partition of the group's shared prefix [0, L) once, read through the
+//    first member's table, and leave a partial (m, l, o) per (sequence,
+//    head, partition) for the split-context reduce to merge with the
+//    members' own partitions.
 //
-// Design (GB300): the rows of one KV head -- a chunk's tokens times the G
-// query heads of the group, or the members' decode queries times G -- are
-// the M dimension of mma.sync m16n8k16 tiles; 64 rows per CTA (4 warps x 16
-// rows), keys and values stream through a 2-stage shared-memory ring of
-// 64-token tiles fetched by 4-D TMA loads (the same 2 KB boxes and 128-byte
-// swizzle as the decode pass), the score tile S = Q K^T and O += P V stay
-// in registers (FA2 register reuse: the S accumulator fragment is the A
-// operand of P V), softmax is online in fp32 log2 units.  Causal rows only
-// fetch the tiles up to the tile's last position; tokens past a row's limit
-// are masked in the scores and value rows past the key range are zeroed
-// before the contraction (no poisoned slot reaches the output).
+// Design (GB300): a CTA takes 128 query rows of one KV head -- a chunk's
+// tokens times the G query heads of the group, or the members' decode
+// queries times G -- as the M = 128 dimension of tcgen05.mma tiles.  The
+// rows sit in shared memory as the K-major A operand (128-byte swizzle);
+// keys and values stream through a 2-stage ring of 64-token tiles fetched by
+// 4-D TMA loads (2 KB boxes, 128-byte swizzle) whose layout is directly the
+// K-major B operand of S = Q K^T and the MN-major B operand of O += P V.
+// S (128 x 64, fp32) and O (128 x d, fp32) live in tensor memory; one thread
+// per row reads its S row, applies the causal / range mask and the online
+// softmax (fp32, log2 units, a reference maximum that moves only when a
+// score exceeds it by 2^8, rescaling O in tensor memory then), and writes P
+// as bf16/fp16 pairs back over S, where it is the A operand of the value
+// product.  One elected thread issues the MMAs and commits them to
+// mbarriers; every wait is bounded in time, and tensor memory is released on
+// every exit path.  Value rows past the key range are zeroed in shared memory
+// before the value product, so a poisoned (NaN) slot never reaches the
+// output.
 #include <cuda.h>
 
 #include <algorithm>
@@ -33,29 +41,30 @@
 
 #include "pa_decode_common.cuh"
 #include "pa_prefill.cuh"
+#include "pa_tcgen05.cuh"
 
 namespace pa {
 
-constexpr int kMqWarps = 4;
-constexpr int kMqRows = 16 * kMqWarps;  // query rows per CTA
-constexpr int kMqTokens = 64;           // key/value tokens per stage
-constexpr int kMqSubs = kMqTokens / kTileTokens;
-constexpr int kMqStages = 2;
+constexpr int kTcRows = 128;     // query rows per CTA (M of the MMAs)
+constexpr int kTcThreads = 128;  // one thread per row
+constexpr int kTcTokens = 64;    // key/value tokens per stage (N of S = Q K^T)
+constexpr int kTcSubs = kTcTokens / kTileTokens;
+constexpr int kTcStages = 2;
+constexpr uint32_t kTmemCols = 256;  // S/P at column 0, O at column 128
+constexpr uint32_t kTmemO = 128;
 
-template <int D> struct MqLayout {
-    static constexpr int kSubBytes = kTileTokens * D * 2;  // one 16-token K (or V) tile
-    static constexpr int kKVBytes = kMqSubs * kSubBytes;   // 64 tokens of K (or V)
-    static constexpr int kStageBytes = 2 * kKVBytes;
-    static constexpr int kQPitch = D + 8;                  // elements per staged query row
-    static constexpr int kQ = kMqStages * kStageBytes;
-    static constexpr int kRowQ = kQ + kMqRows * kQPitch * 2;  // int64 query row offsets
-    static constexpr int kRowO = kRowQ + kMqRows * 8;          // int64 output offsets
-    static constexpr int kRowLim = kRowO + kMqRows * 8;        // int key limits
-    static constexpr int kBars = kRowLim + kMqRows * 4;
-    static constexpr int kSeg = kBars + kMqStages * 8;         // int tile prefix[n + 1]
+template <int D> struct TcLayout {
+    static constexpr int kHalves = D / 64;                    // 128-byte rows of 64 elements
+    static constexpr int kQHalf = kTcRows * 128;              // 16 KB: 128 rows of one d-half
+    static constexpr int kKVHalf = kTcTokens * 128;           // 8 KB: 64 tokens of one d-half
+    static constexpr int kKVBytes = kHalves * kKVHalf;        // K (or V) of one stage
+    static constexpr int kStageBytes = 2 * kKVBytes;          // K then V
+    static constexpr int kQ = kTcStages * kStageBytes;
+    static constexpr int kBars = kQ + kHalves * kQHalf;       // full[2], s, o
+    static constexpr int kTmemSlot = kBars + 4 * 8;
+    static constexpr int kSeg = kTmemSlot + 16;               // int unit prefix[n + 1]
     static size_t bytes(int segments) { return 1024 + kSeg + 4 * ((size_t)segments + 1); }
-    static_assert(kStageBytes % 1024 == 0, "stages keep 1024-byte alignment");
-    static_assert(kBars % 8 == 0, "mbarriers need 8-byte alignment");
+    static_assert(kStageBytes % 1024 == 0 && kQ % 1024 == 0, "1024-byte aligned operands");
 };
 
 // Context length of a chunked-prefill sequence, clamped like the decode pass.
@@ -78,50 +87,78 @@ __device__ __forceinline__ int mq_segment_count(const MqParams &p, int seg)
     return max(0, p.query_start[seg + 1] - p.query_start[seg]);
 }
 
+// Shared prefix length of a group, kept inside the table.
+__device__ __forceinline__ int mq_group_prefix(const MqParams &p, int seg)
+{
+    return min(max(p.group_prefix[seg], 0), p.max_blocks_per_seq * p.block_size);
+}
+
+// Work units of a segment per KV head: row tiles (x prefix partitions).
+__device__ __forceinline__ int mq_segment_units(const MqParams &p, int seg)
+{
+    const int tiles = (mq_segment_count(p, seg) * p.group + kTcRows - 1) / kTcRows;
+    if (!p.prefix_mode)
+        return tiles;
+    return tiles * ((mq_group_prefix(p, seg) + p.part_tokens - 1) / p.part_tokens);
+}
+
 template <typename T, int D>
-__global__ void __launch_bounds__(kMqWarps * 32)
+__global__ void __launch_bounds__(kTcThreads, 1)
     paged_mq_kernel(const __grid_constant__ MqParams p,
                     const __grid_constant__ CUtensorMap tmap_k,
                     const __grid_constant__ CUtensorMap tmap_v)
 {
-    using L = MqLayout<D>;
-    using Op = MmaOp<T>;
-    constexpr int KT = D / 16;  // k-steps of the score product
-    constexpr int NO = D / 8;   // n-tiles of the output
-    constexpr int kThreads = kMqWarps * 32;
+    using L = TcLayout<D>;
+    constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
+    constexpr uint32_t kIdescS = idesc_f16(kBf16, kTcRows, kTcTokens, false, false);
+    constexpr uint32_t kIdescO = idesc_f16(kBf16, kTcRows, D, false, true);
+    constexpr int KT = D / 16;  // MMAs of S = Q K^T (16 elements of d each)
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_addr(smem_raw);
     uint8_t *smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
     const uint32_t sbase = smem_addr(smem);
-    T *qs = reinterpret_cast<T *>(smem + L::kQ);
-    long long *row_q = reinterpret_cast<long long *>(smem + L::kRowQ);
-    long long *row_o = reinterpret_cast<long long *>(smem + L::kRowO);
-    int *row_lim = reinterpret_cast<int *>(smem + L::kRowLim);
+    const uint32_t qbase = sbase + L::kQ;
     int *pref = reinterpret_cast<int *>(smem + L::kSeg);
-    auto bar_of = [&](int st) { return sbase + L::kBars + st * 8; };
-    auto stage_of = [&](int st) { return sbase + st * L::kStageBytes; };
+    auto full_bar = [&](int st) { return sbase + L::kBars + st * 8; };
+    const uint32_t bar_s = sbase + L::kBars + 16, bar_o = sbase + L::kBars + 24;
+    auto kbase = [&](int st) { return sbase + st * L::kStageBytes; };
 
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int g = lane >> 2, t4 = lane & 3;
+    const int tid = threadIdx.x, warp = tid >> 5;
     const int G = p.group, Hkv = p.num_kv_heads, H = p.num_heads;
     const int nseg = p.num_segments;
 
     if (tid == 0) {
-        for (int k = 0; k < kMqStages; ++k)
-            mbar_init(bar_of(k), 1);
+        mbar_init(full_bar(0), 1);
+        mbar_init(full_bar(1), 1);
+        mbar_init(bar_s, 1);
+        mbar_init(bar_o, 1);
         fence_barrier_init();
         prefetch_tensormap(&tmap_k);
         prefetch_tensormap(&tmap_v);
     }
+    // Everything from here on comes after the kernel before this one on the
+    // stream has finished -- including an earlier launch of this kernel, so
+    // the tensor memory below is never contended by one.
     pdl_wait_primary();
-
-    // ---- row tiles per segment and their prefix sums ------------------------------
+    // tensor memory: one warp allocates, every thread reads the address
     if (warp == 0) {
+        tmem_alloc(sbase + L::kTmemSlot, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + L::kTmemSlot);
+    const uint32_t lane_base = (uint32_t)(32 * warp) << 16;  // this warp's TMEM lanes
+
+    // ---- work units per segment and their prefix sums -------------------------------
+    if (warp == 0) {
+        const int lane = tid & 31;
         int carry = 0;
         for (int base = 0; base < nseg; base += 32) {
             const int sg = base + lane;
-            const int n = sg < nseg ? (mq_segment_count(p, sg) * G + kMqRows - 1) / kMqRows : 0;
+            const int n = sg < nseg ? mq_segment_units(p, sg) : 0;
             int x = n;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
@@ -139,21 +176,12 @@ __global__ void __launch_bounds__(kMqWarps * 32)
     __syncthreads();
     const int total_units = pref[nseg] * Hkv;
 
-    uint32_t phase = 0;     // parity bit per stage
-    uint32_t pending = 0;   // stages with a fill not yet waited for
+    uint32_t ph_full = 0, ph_s = 0, ph_o = 0;  // mbarrier parities
+    uint32_t pending = 0;                       // stages with a fill not yet waited for
     bool aborted = false;
 
-    // ldmatrix lane selectors
-    const int li = lane & 7, mi = lane >> 3;
-    // address of 16-byte chunk `chunk` (0..7) of d-half `half` of token `tok`
-    // (0..15) in the 16-token tile at `base` (TMA 128-byte swizzle)
-    auto tile_addr = [](uint32_t base, int tok, int half, int chunk) -> uint32_t {
-        const int r = half * kTileTokens + tok;
-        return base + r * 128 + ((chunk ^ (r & 7)) << 4);
-    };
-
     for (int u = blockIdx.x; u < total_units && !aborted; u += gridDim.x) {
-        // ---- unit -> (segment, KV head, row tile) ---------------------------------
+        // ---- unit -> (segment, KV head, row tile, prefix partition) ---------------------
         const int q = u / Hkv;
         const int kh = u - q * Hkv;
         int lo = 0, hi = nseg - 1;
@@ -165,54 +193,62 @@ __global__ void __launch_bounds__(kMqWarps * 32)
                 hi = mid - 1;
         }
         const int seg = lo;
-        const int rt = q - pref[seg];
         const int count = mq_segment_count(p, seg);
-        const int nrows = min(kMqRows, count * G - rt * kMqRows);
+        const int tiles = (count * G + kTcRows - 1) / kTcRows;
+        const int idx = q - pref[seg];
+        const int rt = idx % tiles;     // row tile
+        const int part = idx / tiles;   // prefix partition (0 for prefill)
+        const int nrows = min(kTcRows, count * G - rt * kTcRows);
 
-        // the table the keys are read through, and the key range of the tile
-        int table_seq, kend;
+        int table_seq, kbeg, kend;
         if (p.prefix_mode) {
             // a bad leader id is flagged by the plan check below
             table_seq = min(max(p.group_members[p.group_start[seg]], 0), p.num_seqs - 1);
-            kend = min(max(p.group_prefix[seg], 0), p.max_blocks_per_seq * p.block_size);
+            kbeg = part * p.part_tokens;
+            kend = min(mq_group_prefix(p, seg), kbeg + p.part_tokens);
         } else {
             table_seq = seg;
             const int ctx = clamp_context_mq(p, seg);
-            const int last = (rt * kMqRows + nrows - 1) / G;  // chunk row of the tile's last row
+            const int last = (rt * kTcRows + nrows - 1) / G;  // chunk row of the last row
+            kbeg = 0;
             kend = max(0, ctx - count + last + 1);
         }
         const int32_t *table = p.block_tables + (size_t)table_seq * p.max_blocks_per_seq;
-        const int nstages = (kend + kMqTokens - 1) / kMqTokens;
+        const int nstages = kend > kbeg ? (kend - kbeg + kTcTokens - 1) / kTcTokens : 0;
 
-        __syncthreads();  // the previous unit is done with the stages, rows and Q tile
+        tc_fence_before();
+        __syncthreads();  // the previous unit is done with the stages, Q tile and TMEM
+        tc_fence_after();
 
-        // prefix pass, first KV head: check the plan for this tile's members --
-        // the group's length is on the tile grid and within every member's
-        // context, each member records it as its start, and each member's
-        // table names the leader's blocks for the whole prefix
-        if (p.prefix_mode && kh == 0 && tid < nrows && (rt * kMqRows + tid) % G == 0) {
-            const int s = p.group_members[p.group_start[seg] + (rt * kMqRows + tid) / G];
-            const int L = p.group_prefix[seg];
+        // prefix pass, first KV head and partition: check the plan for this
+        // tile's members -- the prefix is on the tile grid and within every
+        // member's context, each member records it as its start, and each
+        // member's table names the leader's blocks for the whole prefix
+        if (p.prefix_mode && kh == 0 && part == 0 && tid < nrows &&
+            (rt * kTcRows + tid) % G == 0) {
+            const int s = p.group_members[p.group_start[seg] + (rt * kTcRows + tid) / G];
+            const int Lg = p.group_prefix[seg];
             const int leader = p.group_members[p.group_start[seg]];
-            bool bad = s < 0 || s >= p.num_seqs || L <= 0 || (L & (kTileTokens - 1)) != 0 ||
-                       L > p.max_blocks_per_seq * p.block_size || leader < 0 ||
+            bool bad = s < 0 || s >= p.num_seqs || Lg <= 0 || (Lg & (kTileTokens - 1)) != 0 ||
+                       Lg > p.max_blocks_per_seq * p.block_size || leader < 0 ||
                        leader >= p.num_seqs;
             if (!bad) {
                 const int c = p.context_lens[s];
-                bad = c < L || c > p.max_context_len || p.seq_start[s] != L;
+                bad = c < Lg || c > p.max_context_len || p.seq_start[s] != Lg;
                 const int32_t *mine = p.block_tables + (size_t)s * p.max_blocks_per_seq;
-                for (int b = 0; !bad && b < (L >> p.block_shift); ++b)
+                for (int b = 0; !bad && b < (Lg >> p.block_shift); ++b)
                     bad = __ldg(mine + b) != __ldg(table + b);
             }
             if (bad)
                 flag_error(p.error_word, PA_DEVERR_PREFIX_PLAN);
         }
 
-        auto issue = [&](int j) {  // thread 0: fetch key/value tile j into stage j % 2
-            const int st = j % kMqStages;
-            const int t0 = j * kMqTokens;
-            const int nsub = min(kMqSubs, (kend - t0 + kTileTokens - 1) / kTileTokens);
-            mbar_arrive_expect_tx(bar_of(st), (uint32_t)(nsub * 2 * L::kSubBytes));
+        // thread 0: fetch key/value tile `si` into stage si % 2
+        auto issue = [&](int si) {
+            const int st = si % kTcStages;
+            const int t0 = kbeg + si * kTcTokens;
+            const int nsub = min(kTcSubs, (kend - t0 + kTileTokens - 1) / kTileTokens);
+            mbar_arrive_expect_tx(full_bar(st), (uint32_t)(nsub * L::kHalves * 2 * 2048));
             for (int sb = 0; sb < nsub; ++sb) {
                 const int tok = t0 + sb * kTileTokens;
                 int phys = __ldg(table + (tok >> p.block_shift));
@@ -221,223 +257,241 @@ __global__ void __launch_bounds__(kMqWarps * 32)
                     phys = 0;  // stays inside the pool; the row's output is undefined
                 }
                 const int row = tok & (p.block_size - 1);
-                const uint32_t dst = stage_of(st) + sb * L::kSubBytes;
 #pragma unroll
-                for (int hf = 0; hf < D / 64; ++hf) {
-                    tma_load_4d(dst + hf * (L::kSubBytes / (D / 64)), &tmap_k, bar_of(st),
-                                hf * 64, kh, row, phys);
-                    tma_load_4d(dst + L::kKVBytes + hf * (L::kSubBytes / (D / 64)), &tmap_v,
-                                bar_of(st), hf * 64, kh, row, phys);
+                for (int hf = 0; hf < L::kHalves; ++hf) {
+                    const uint32_t off = hf * L::kKVHalf + sb * 2048;
+                    tma_load_4d(kbase(st) + off, &tmap_k, full_bar(st), hf * 64, kh, row, phys);
+                    tma_load_4d(kbase(st) + L::kKVBytes + off, &tmap_v, full_bar(st), hf * 64,
+                                kh, row, phys);
                 }
             }
         };
         if (tid == 0) {
-            for (int j = 0; j < min(kMqStages, nstages); ++j)
-                issue(j);
+            for (int si = 0; si < min(kTcStages, nstages); ++si)
+                issue(si);
         }
-        pending = (1u << min(kMqStages, nstages)) - 1u;
+        pending = (1u << min(kTcStages, nstages)) - 1u;
 
-        // ---- row descriptors: query row, output location, key limit ----------------
-        if (tid < kMqRows) {
-            long long qoff = -1, ooff = -1;
-            int lim = 0;
-            if (tid < nrows) {
-                const int r = rt * kMqRows + tid;
-                const int i = r / G, hg = r - (r / G) * G;
-                const int h = kh * G + hg;
-                if (p.prefix_mode) {
-                    int s = p.group_members[p.group_start[seg] + i];
-                    s = min(max(s, 0), p.num_seqs - 1);  // a bad member id is flagged above
-                    qoff = ((long long)s * H + h) * D;
-                    ooff = ((long long)s * H + h) * p.max_parts;  // partial 0 of (s, h)
-                    lim = kend;
-                } else {
-                    const long long row = (long long)p.query_start[seg] + i;
-                    qoff = (row * H + h) * D;
-                    ooff = qoff;
-                    lim = max(0, kend - (((rt * kMqRows + nrows - 1) / G) - i));
-                }
+        // ---- this thread's row: query row, output location, key limit ------------------
+        long long qoff = -1, ooff = -1;
+        int lim = 0;
+        if (tid < nrows) {
+            const int r = rt * kTcRows + tid;
+            const int i = r / G, hg = r - (r / G) * G;
+            const int h = kh * G + hg;
+            if (p.prefix_mode) {
+                int s = p.group_members[p.group_start[seg] + i];
+                s = min(max(s, 0), p.num_seqs - 1);  // a bad member id is flagged above
+                qoff = ((long long)s * H + h) * D;
+                ooff = ((long long)s * H + h) * p.max_parts + part;
+                lim = kend;
+            } else {
+                const long long row = (long long)p.query_start[seg] + i;
+                qoff = (row * H + h) * D;
+                ooff = qoff;
+                const int last = (rt * kTcRows + nrows - 1) / G;
+                lim = max(0, kend - (last - i));
             }
-            row_q[tid] = qoff;
-            row_o[tid] = ooff;
-            row_lim[tid] = lim;
         }
-        __syncthreads();
-        // ---- query tile into shared memory (zero rows past the tile) --------------
-        for (int c = tid; c < kMqRows * (D / 8); c += kThreads) {
-            const int r = c / (D / 8), ch = c - r * (D / 8);
-            uint4 v = make_uint4(0, 0, 0, 0);
-            if (row_q[r] >= 0)
-                v = __ldg(reinterpret_cast<const uint4 *>(static_cast<const T *>(p.query) +
-                                                          row_q[r]) + ch);
-            *reinterpret_cast<uint4 *>(qs + r * L::kQPitch + ch * 8) = v;
-        }
-        __syncthreads();
-        uint32_t qa[KT][4];
+        // query row -> shared memory (K-major, 128-byte swizzle; zeros past the tile)
+        {
+            const uint4 *src = reinterpret_cast<const uint4 *>(static_cast<const T *>(p.query) +
+                                                               (qoff < 0 ? 0 : qoff));
 #pragma unroll
-        for (int kk = 0; kk < KT; ++kk) {
-            const int r = warp * 16 + li + (mi & 1) * 8;
-            const int col = kk * 16 + (mi >> 1) * 8;
-            ldmatrix_x4(smem_addr(qs + r * L::kQPitch + col), qa[kk]);
+            for (int c = 0; c < D / 8; ++c) {
+                const uint4 v = qoff >= 0 ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
+                const uint32_t a = qbase + (c >> 3) * L::kQHalf + tid * 128 +
+                                   (((c & 7) ^ (tid & 7)) << 4);
+                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(v.x),
+                             "r"(v.y), "r"(v.z), "r"(v.w)
+                             : "memory");
+            }
         }
-        const int lim0 = row_lim[warp * 16 + g], lim1 = row_lim[warp * 16 + g + 8];
+        fence_proxy_async_smem();
 
-        float o[NO][4];
-#pragma unroll
-        for (int n = 0; n < NO; ++n)
-            o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
-        float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-
-        for (int j = 0; j < nstages; ++j) {
-            const int st = j % kMqStages;
-            const bool ok = mbar_wait_bounded(bar_of(st), (phase >> st) & 1u, kWaitLimitNs);
-            phase ^= 1u << st;
+        float m_ref = -INFINITY, l_run = 0.f;
+        for (int si = 0; si < nstages; ++si) {
+            const int st = si % kTcStages;
+            const int t0 = kbeg + si * kTcTokens;
+            bool ok = mbar_wait_bounded(full_bar(st), (ph_full >> st) & 1u, kWaitLimitNs);
+            ph_full ^= 1u << st;
             pending &= ~(1u << st);
+            // value rows past the key range -> zero (never fetched, or past the context)
+            const int nvalid = kend - t0;
+            if (nvalid < kTcTokens) {
+                const int rows = kTcTokens - nvalid;
+                for (int c = tid; c < L::kHalves * rows * 8; c += kTcThreads) {
+                    const int hf = c / (rows * 8), rem = c - hf * rows * 8;
+                    const uint32_t a = kbase(st) + L::kKVBytes + hf * L::kKVHalf +
+                                       (nvalid + rem / 8) * 128 + (rem % 8) * 16;
+                    asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(a), "r"(0)
+                                 : "memory");
+                }
+                fence_proxy_async_smem();
+            }
             if (__syncthreads_or(!ok)) {
-                if (tid == 0)
-                    flag_error(p.error_word, PA_DEVERR_TIMEOUT);
                 aborted = true;
                 break;
             }
-            const uint32_t kb = stage_of(st), vb = kb + L::kKVBytes;
-            const int t0 = j * kMqTokens;
 
-            // S[16 rows x 64 tokens] = Q K^T
-            float sacc[8][4];
-#pragma unroll
-            for (int n = 0; n < 8; ++n)
-                sacc[n][0] = sacc[n][1] = sacc[n][2] = sacc[n][3] = 0.f;
-#pragma unroll
-            for (int sb = 0; sb < kMqSubs; ++sb) {
-                if (t0 + sb * kTileTokens >= kend)
-                    break;  // sub-tile not fetched (uniform across the CTA)
+            // S = Q K^T (fp32 in TMEM columns [0, 64))
+            if (tid == 0) {
+                tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < KT; ++kk) {
-                    uint32_t b[4];
-                    const int tok = (mi >> 1) * 8 + li;
-                    const int dc = (kk & 3) * 2 + (mi & 1);
-                    ldmatrix_x4(tile_addr(kb + sb * L::kSubBytes, tok, kk >> 2, dc), b);
-                    Op::run(sacc[2 * sb], qa[kk], b[0], b[1]);
-                    Op::run(sacc[2 * sb + 1], qa[kk], b[2], b[3]);
+                    const uint64_t a = smem_desc_sw128(qbase + (kk >> 2) * L::kQHalf + (kk & 3) * 32,
+                                                       16, 1024);
+                    const uint64_t b = smem_desc_sw128(kbase(st) + (kk >> 2) * L::kKVHalf +
+                                                           (kk & 3) * 32,
+                                                       16, 1024);
+                    tc_mma_ss(tmem, a, b, kIdescS, kk > 0 ? 1u : 0u);
+                }
+                tc_commit(bar_s);
+            }
+            ok = mbar_wait_bounded(bar_s, ph_s, kWaitLimitNs);
+            ph_s ^= 1u;
+            tc_fence_after();
+            if (__syncthreads_or(!ok)) {
+                aborted = true;
+                break;
+            }
+
+            // ---- softmax of this thread's row -------------------------------------------
+            float sv[kTcTokens];
+#pragma unroll
+            for (int c = 0; c < kTcTokens / 32; ++c) {
+                uint32_t r[32];
+                tmem_ld_32x32b_x32(tmem + lane_base + c * 32, r);
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    sv[c * 32 + i] = __uint_as_float(r[i]);
+            }
+            float mx = -INFINITY;
+#pragma unroll
+            for (int i = 0; i < kTcTokens; ++i) {
+                sv[i] = t0 + i < lim ? sv[i] * p.scale_log2 : -INFINITY;
+                mx = fmaxf(mx, sv[i]);
+            }
+            // the reference maximum moves only when a score passes it by 2^kSlack
+            const bool moved = mx > m_ref + kSlack;
+            float alpha = 1.f;
+            if (moved) {
+                alpha = exp2f(m_ref - mx);  // 0 while m_ref is -inf
+                m_ref = mx;
+                l_run *= alpha;
+            }
+            const float mu = m_ref == -INFINITY ? 0.f : m_ref;
+            uint32_t pw[kTcTokens / 2];
+#pragma unroll
+            for (int i = 0; i < kTcTokens / 2; ++i) {
+                const float p0 = exp2f(sv[2 * i] - mu), p1 = exp2f(sv[2 * i + 1] - mu);
+                l_run += p0 + p1;
+                pw[i] = MmaOp<T>::pack(p0, p1);
+            }
+            tmem_st_32x32b_x32(tmem + lane_base, pw);  // P over S: columns [0, 32)
+            // O was accumulated by earlier stages: rescale it in TMEM
+            if (si > 0 && __any_sync(kFull, moved)) {
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t r[32];
+                    tmem_ld_32x32b_x32(tmem + lane_base + kTmemO + c * 32, r);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+                    tmem_st_32x32b_x32(tmem + lane_base + kTmemO + c * 32, r);
                 }
             }
-
-            // online softmax (log2 units) with the causal / range mask
-            float mx0 = m0, mx1 = m1;
-#pragma unroll
-            for (int n = 0; n < 8; ++n) {
-                const int tk = t0 + n * 8 + 2 * t4;
-                sacc[n][0] = tk < lim0 ? sacc[n][0] * p.scale_log2 : -INFINITY;
-                sacc[n][1] = tk + 1 < lim0 ? sacc[n][1] * p.scale_log2 : -INFINITY;
-                sacc[n][2] = tk < lim1 ? sacc[n][2] * p.scale_log2 : -INFINITY;
-                sacc[n][3] = tk + 1 < lim1 ? sacc[n][3] * p.scale_log2 : -INFINITY;
-                mx0 = fmaxf(mx0, fmaxf(sacc[n][0], sacc[n][1]));
-                mx1 = fmaxf(mx1, fmaxf(sacc[n][2], sacc[n][3]));
-            }
-#pragma unroll
-            for (int off = 1; off < 4; off <<= 1) {
-                mx0 = fmaxf(mx0, __shfl_xor_sync(kFull, mx0, off));
-                mx1 = fmaxf(mx1, __shfl_xor_sync(kFull, mx1, off));
-            }
-            const float al0 = mx0 == -INFINITY ? 1.f : exp2f(m0 - mx0);
-            const float al1 = mx1 == -INFINITY ? 1.f : exp2f(m1 - mx1);
-            m0 = mx0;
-            m1 = mx1;
-            const float mu0 = mx0 == -INFINITY ? 0.f : mx0;
-            const float mu1 = mx1 == -INFINITY ? 0.f : mx1;
-            l0 *= al0;
-            l1 *= al1;
-#pragma unroll
-            for (int n = 0; n < NO; ++n) {
-                o[n][0] *= al0;
-                o[n][1] *= al0;
-                o[n][2] *= al1;
-                o[n][3] *= al1;
-            }
-            uint32_t pa[4][4];  // P as the A operand, one k-step per 16 tokens
-#pragma unroll
-            for (int n = 0; n < 8; ++n) {
-                const float p0 = exp2f(sacc[n][0] - mu0), p1 = exp2f(sacc[n][1] - mu0);
-                const float p2 = exp2f(sacc[n][2] - mu1), p3 = exp2f(sacc[n][3] - mu1);
-                l0 += p0 + p1;
-                l1 += p2 + p3;
-                pa[n >> 1][(n & 1) * 2 + 0] = Op::pack(p0, p1);
-                pa[n >> 1][(n & 1) * 2 + 1] = Op::pack(p2, p3);
-            }
-
-            // O[16 x D] += P V; value rows past the key range are zeroed
-#pragma unroll
-            for (int sb = 0; sb < kMqSubs; ++sb) {
-                const int nv = kend - (t0 + sb * kTileTokens);
-                if (nv <= 0)
-                    break;
-                const uint32_t m01 = (2 * t4 < nv ? 0x0000ffffu : 0u) |
-                                     (2 * t4 + 1 < nv ? 0xffff0000u : 0u);
-                const uint32_t m89 = (2 * t4 + 8 < nv ? 0x0000ffffu : 0u) |
-                                     (2 * t4 + 9 < nv ? 0xffff0000u : 0u);
-#pragma unroll
-                for (int np = 0; np < NO / 2; ++np) {
-                    uint32_t b[4];
-                    const int tok = (mi & 1) * 8 + li;
-                    const int d = np * 16 + (mi >> 1) * 8;
-                    ldmatrix_x4_trans(tile_addr(vb + sb * L::kSubBytes, tok, d >> 6, (d & 63) >> 3),
-                                      b);
-                    Op::run(o[2 * np], pa[sb], b[0] & m01, b[1] & m89);
-                    Op::run(o[2 * np + 1], pa[sb], b[2] & m01, b[3] & m89);
-                }
-            }
-
-            // everyone is done with stage st: refill it with tile j + 2
+            tc_fence_before();
             __syncthreads();
-            if (j + kMqStages < nstages) {
+
+            // O += P V (fp32 in TMEM columns [128, 128 + D))
+            if (tid == 0) {
+                tc_fence_after();
+#pragma unroll
+                for (int ks = 0; ks < kTcTokens / 16; ++ks) {
+                    const uint64_t b = smem_desc_sw128(kbase(st) + L::kKVBytes + ks * 2048,
+                                                       L::kKVHalf, 1024);
+                    tc_mma_ts(tmem + kTmemO, tmem + ks * 8, b, kIdescO,
+                              (si > 0 || ks > 0) ? 1u : 0u);
+                }
+                tc_commit(bar_o);
+            }
+            ok = mbar_wait_bounded(bar_o, ph_o, kWaitLimitNs);
+            ph_o ^= 1u;
+            tc_fence_after();
+            if (__syncthreads_or(!ok)) {
+                aborted = true;
+                break;
+            }
+            // stage st is free: refill it with tile si + 2
+            if (si + kTcStages < nstages) {
                 if (tid == 0)
-                    issue(j + kMqStages);
+                    issue(si + kTcStages);
                 pending |= 1u << st;
             }
         }
         if (aborted)
             break;
 
-        // ---- epilogue -------------------------------------------------------------------
-#pragma unroll
-        for (int off = 1; off < 4; off <<= 1) {
-            l0 += __shfl_xor_sync(kFull, l0, off);
-            l1 += __shfl_xor_sync(kFull, l1, off);
+        // ---- epilogue: this thread's row of O / l (TMEM loads are warp-wide) -----------
+        const float inv = (nstages > 0 && l_run > 0.f) ? 1.f / l_run : 0.f;
+        if (p.prefix_mode && ooff >= 0) {
+            p.part_m[ooff] = m_ref * kLn2;
+            p.part_l[ooff] = l_run;
         }
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-            const int r = warp * 16 + g + half * 8;
-            const long long ooff = row_o[r];
+        for (int c = 0; c < D / 32; ++c) {
+            uint32_t r[32];
+            if (nstages > 0) {
+                tmem_ld_32x32b_x32(tmem + lane_base + kTmemO + c * 32, r);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    r[i] = 0u;
+            }
             if (ooff < 0)
                 continue;
-            const float l = half ? l1 : l0;
-            const float inv = l > 0.f ? 1.f / l : 0.f;
             if (p.prefix_mode) {
-                float *po = p.part_o + ooff * D;
+                float4 *dst = reinterpret_cast<float4 *>(p.part_o + ooff * D) + c * 8;
 #pragma unroll
-                for (int n = 0; n < NO; ++n)
-                    *reinterpret_cast<float2 *>(po + n * 8 + 2 * t4) =
-                        make_float2(o[n][half * 2] * inv, o[n][half * 2 + 1] * inv);
-                if (t4 == 0) {
-                    p.part_m[ooff] = (half ? m1 : m0) * kLn2;
-                    p.part_l[ooff] = l;
-                }
+                for (int i = 0; i < 8; ++i)
+                    dst[i] = make_float4(__uint_as_float(r[4 * i]) * inv,
+                                         __uint_as_float(r[4 * i + 1]) * inv,
+                                         __uint_as_float(r[4 * i + 2]) * inv,
+                                         __uint_as_float(r[4 * i + 3]) * inv);
             } else {
-                T *po = static_cast<T *>(p.out) + ooff;
+                uint4 *dst = reinterpret_cast<uint4 *>(static_cast<T *>(p.out) + ooff) + c * 4;
 #pragma unroll
-                for (int n = 0; n < NO; ++n)
-                    *reinterpret_cast<uint32_t *>(po + n * 8 + 2 * t4) =
-                        Op::pack(o[n][half * 2] * inv, o[n][half * 2 + 1] * inv);
+                for (int i = 0; i < 4; ++i) {
+                    uint4 w;
+                    w.x = MmaOp<T>::pack(__uint_as_float(r[8 * i]) * inv,
+                                         __uint_as_float(r[8 * i + 1]) * inv);
+                    w.y = MmaOp<T>::pack(__uint_as_float(r[8 * i + 2]) * inv,
+                                         __uint_as_float(r[8 * i + 3]) * inv);
+                    w.z = MmaOp<T>::pack(__uint_as_float(r[8 * i + 4]) * inv,
+                                         __uint_as_float(r[8 * i + 5]) * inv);
+                    w.w = MmaOp<T>::pack(__uint_as_float(r[8 * i + 6]) * inv,
+                                         __uint_as_float(r[8 * i + 7]) * inv);
+                    dst[i] = w;
+                }
             }
         }
     }
     pdl_launch_dependents();
 
-    // ---- drain: a fill still landing (only after an abort) -------------------------------
+    // ---- drain (only after an abort): fills still landing -------------------------------
     if (tid == 0) {
-        for (int st = 0; st < kMqStages; ++st)
+        for (int st = 0; st < kTcStages; ++st)
             if (pending & (1u << st))
-                mbar_wait_bounded(bar_of(st), (phase >> st) & 1u, kWaitLimitNs);
+                mbar_wait_bounded(full_bar(st), (ph_full >> st) & 1u, kWaitLimitNs);
+    }
+    if (aborted && tid == 0)
+        flag_error(p.error_word, PA_DEVERR_TIMEOUT);
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
     }
 }
 
@@ -447,7 +501,7 @@ template <typename T, int D>
 static pa_status launch_mq(const MqParams &prm, const CUtensorMap &mk, const CUtensorMap &mv,
                            cudaStream_t stream, long long max_units)
 {
-    using L = MqLayout<D>;
+    using L = TcLayout<D>;
     auto kernel = paged_mq_kernel<T, D>;
     static KernelSetting setting[kMaxDevices];
     static std::mutex mu;
@@ -475,7 +529,7 @@ static pa_status launch_mq(const MqParams &prm, const CUtensorMap &mk, const CUt
         }
         if (smem != ks.smem_queried) {
             e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&ks.per_sm, kernel,
-                                                              kMqWarps * 32, smem);
+                                                              kTcThreads, smem);
             if (e != cudaSuccess)
                 return record_cuda(e);
             ks.smem_queried = smem;
@@ -484,10 +538,12 @@ static pa_status launch_mq(const MqParams &prm, const CUtensorMap &mk, const CUt
     }
     if (per_sm < 1)
         return PA_ERR_UNSUPPORTED;
+    // each CTA holds kTmemCols of the SM's 512 tensor-memory columns
+    per_sm = std::min(per_sm, (int)(512 / kTmemCols));
     long long grid = std::min<long long>((long long)info.sms * per_sm, max_units);
     if (grid < 1)
         grid = 1;
-    return launch_pdl(kernel, dim3((unsigned)grid), dim3(kMqWarps * 32), smem, stream, prm, mk,
+    return launch_pdl(kernel, dim3((unsigned)grid), dim3(kTcThreads), smem, stream, prm, mk,
                       mv);
 }
 
@@ -569,10 +625,11 @@ extern "C" pa_status pa_prefill_attention(void *out, const void *query, const vo
     prm.block_shift = __builtin_ctz((unsigned)block_size);
     prm.max_context_len = max_context_len;
     prm.max_parts = 0;
+    prm.part_tokens = 0;
     prm.scale_log2 = scale * kLog2e;
     // row tiles: at most one partial tile per sequence beyond the full ones
     const long long max_units =
-        ((long long)num_tokens * group / kMqRows + num_seqs) * num_kv_heads;
+        ((long long)num_tokens * group / kTcRows + num_seqs) * num_kv_heads;
     return dispatch_mq(prm, dtype, key_cache, value_cache, head_dim, as_stream(stream),
                        max_units);
 }

@@ -26,6 +26,7 @@ struct MqParams {
     int num_seqs, num_heads, num_kv_heads, group;
     int max_blocks_per_seq, num_blocks, block_size, block_shift, max_context_len;
     int max_parts;     // partials per (sequence, head) in the workspace
+    int part_tokens;   // prefix pass: tokens per prefix partition (partial j)
     float scale_log2;
 };
 
