@@ -241,8 +241,9 @@ PA_API pa_status pa_decode_attention_fp8(void *out, const void *query, const voi
  *                 past the table are clipped and flagged
  *                 PA_DEVERR_CONTEXT_RANGE.  A row whose position is negative
  *                 (chunk longer than the context) gets a zero row.
- * Accumulation fp32 (online softmax), output rounded to nearest even.  No
- * workspace.  Supported: as pa_decode_attention (FP8 pools: PA_ERR_UNSUPPORTED).
+ * scale must be positive (PA_ERR_INVALID_ARG otherwise).  Accumulation fp32
+ * (online softmax), output rounded to nearest even.  No workspace.
+ * Supported: as pa_decode_attention (FP8 pools: PA_ERR_UNSUPPORTED).
  */
 PA_API pa_status pa_prefill_attention(void *out, const void *query, const void *key_cache,
                                       const void *value_cache, const int32_t *block_tables,
@@ -316,8 +317,9 @@ PA_API size_t pa_cascade_workspace_bytes(int num_seqs, int num_heads, int num_kv
  * a prefix not below a member's context or off the 16-token grid, a
  * member's seq_prefix_len that differs from its group's) sets
  * PA_DEVERR_PREFIX_PLAN and leaves those rows undefined.  num_groups == 0
- * is plain split decode.  Other arguments, limits and errors as
- * pa_decode_attention (16-bit pools).
+ * is plain split decode.  scale must be positive (PA_ERR_INVALID_ARG
+ * otherwise).  Other arguments, limits and errors as pa_decode_attention
+ * (16-bit pools).
  */
 PA_API pa_status pa_decode_attention_cascade(void *out, const void *query, const void *key_cache,
                                              const void *value_cache,

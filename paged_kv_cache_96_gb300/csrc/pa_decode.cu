@@ -682,6 +682,11 @@ static pa_status launch_pass(const DecodeParams &prm, const CUtensorMap &mk,
         if (smem > ks.smem_enabled) {
             e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      (int)smem);
+            // the whole unified L1/shared array as shared memory, so that the
+            // residency below is the one shared memory allows
+            if (e == cudaSuccess)
+                e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                         (int)cudaSharedmemCarveoutMaxShared);
             if (e != cudaSuccess)
                 return record_cuda(e);
             ks.smem_enabled = smem;
@@ -866,7 +871,8 @@ extern "C" pa_status pa_decode_attention_cascade(
 {
     if (dtype != PA_F16 && dtype != PA_BF16)
         return dtype == PA_FP8_E4M3 ? PA_ERR_UNSUPPORTED : PA_ERR_INVALID_ARG;
-    if (num_groups < 0 || num_members < 0 || (num_groups > 0 && num_members < 2 * num_groups))
+    if (num_groups < 0 || num_members < 0 || (num_groups > 0 && num_members < 2 * num_groups) ||
+        !(scale > 0.f))
         return PA_ERR_INVALID_ARG;
     if (num_groups == 0)
         return pa_decode_attention(out, query, key_cache, value_cache, block_tables,

@@ -60,8 +60,8 @@ template <int D> struct TcLayout {
     static constexpr int kKVBytes = kHalves * kKVHalf;        // K (or V) of one stage
     static constexpr int kStageBytes = 2 * kKVBytes;          // K then V
     static constexpr int kQ = kTcStages * kStageBytes;
-    static constexpr int kBars = kQ + kHalves * kQHalf;       // full[2], s, o
-    static constexpr int kTmemSlot = kBars + 4 * 8;
+    static constexpr int kBars = kQ + kHalves * kQHalf;       // k[2], v[2], s, o
+    static constexpr int kTmemSlot = kBars + 6 * 8;
     static constexpr int kSeg = kTmemSlot + 16;               // int unit prefix[n + 1]
     static size_t bytes(int segments) { return 1024 + kSeg + 4 * ((size_t)segments + 1); }
     static_assert(kStageBytes % 1024 == 0 && kQ % 1024 == 0, "1024-byte aligned operands");
@@ -120,8 +120,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const uint32_t sbase = smem_addr(smem);
     const uint32_t qbase = sbase + L::kQ;
     int *pref = reinterpret_cast<int *>(smem + L::kSeg);
-    auto full_bar = [&](int st) { return sbase + L::kBars + st * 8; };
-    const uint32_t bar_s = sbase + L::kBars + 16, bar_o = sbase + L::kBars + 24;
+    auto kbar = [&](int st) { return sbase + L::kBars + st * 8; };       // K tile landed
+    auto vbar = [&](int st) { return sbase + L::kBars + 16 + st * 8; };  // V tile landed
+    const uint32_t bar_s = sbase + L::kBars + 32, bar_o = sbase + L::kBars + 40;
     auto kbase = [&](int st) { return sbase + st * L::kStageBytes; };
 
     const int tid = threadIdx.x, warp = tid >> 5;
@@ -129,8 +130,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int nseg = p.num_segments;
 
     if (tid == 0) {
-        mbar_init(full_bar(0), 1);
-        mbar_init(full_bar(1), 1);
+        for (int st = 0; st < kTcStages; ++st) {
+            mbar_init(kbar(st), 1);
+            mbar_init(vbar(st), 1);
+        }
         mbar_init(bar_s, 1);
         mbar_init(bar_o, 1);
         fence_barrier_init();
@@ -176,8 +179,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     __syncthreads();
     const int total_units = pref[nseg] * Hkv;
 
-    uint32_t ph_full = 0, ph_s = 0, ph_o = 0;  // mbarrier parities
-    uint32_t pending = 0;                       // stages with a fill not yet waited for
+    uint32_t ph_k = 0, ph_v = 0, ph_s = 0, ph_o = 0;  // mbarrier parities
+    uint32_t pend_k = 0, pend_v = 0;  // stages with a K / V fill not yet waited for
     bool aborted = false;
 
     for (int u = blockIdx.x; u < total_units && !aborted; u += gridDim.x) {
@@ -243,34 +246,49 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 flag_error(p.error_word, PA_DEVERR_PREFIX_PLAN);
         }
 
-        // thread 0: fetch key/value tile `si` into stage si % 2
-        auto issue = [&](int si) {
-            const int st = si % kTcStages;
+        // thread 0: the physical blocks of tile `si` (up to 4 independent table
+        // loads), then the K or the V half of its fetch into stage si % 2.  K
+        // is refilled as soon as S = Q K^T of the tile two back has finished,
+        // V once its value product has: the key fetch gets a longer lead.
+        int ent[kTcSubs];
+        auto lookup = [&](int si) {
             const int t0 = kbeg + si * kTcTokens;
-            const int nsub = min(kTcSubs, (kend - t0 + kTileTokens - 1) / kTileTokens);
-            mbar_arrive_expect_tx(full_bar(st), (uint32_t)(nsub * L::kHalves * 2 * 2048));
-            for (int sb = 0; sb < nsub; ++sb) {
-                const int tok = t0 + sb * kTileTokens;
-                int phys = __ldg(table + (tok >> p.block_shift));
-                if (phys < 0 || phys >= p.num_blocks) {
-                    flag_error(p.error_word, PA_DEVERR_BLOCK_RANGE);
-                    phys = 0;  // stays inside the pool; the row's output is undefined
-                }
-                const int row = tok & (p.block_size - 1);
 #pragma unroll
-                for (int hf = 0; hf < L::kHalves; ++hf) {
-                    const uint32_t off = hf * L::kKVHalf + sb * 2048;
-                    tma_load_4d(kbase(st) + off, &tmap_k, full_bar(st), hf * 64, kh, row, phys);
-                    tma_load_4d(kbase(st) + L::kKVBytes + off, &tmap_v, full_bar(st), hf * 64,
-                                kh, row, phys);
+            for (int sb = 0; sb < kTcSubs; ++sb) {
+                const int tok = t0 + sb * kTileTokens;
+                ent[sb] = tok < kend ? __ldg(table + (tok >> p.block_shift)) : 0;
+            }
+#pragma unroll
+            for (int sb = 0; sb < kTcSubs; ++sb) {
+                if (ent[sb] < 0 || ent[sb] >= p.num_blocks) {
+                    flag_error(p.error_word, PA_DEVERR_BLOCK_RANGE);
+                    ent[sb] = 0;  // stays inside the pool; the row's output is undefined
                 }
             }
         };
+        auto issue = [&](int si, bool values) {
+            const int st = si % kTcStages;
+            const int t0 = kbeg + si * kTcTokens;
+            const int nsub = min(kTcSubs, (kend - t0 + kTileTokens - 1) / kTileTokens);
+            const uint32_t bar = values ? vbar(st) : kbar(st);
+            const uint32_t dst = kbase(st) + (values ? L::kKVBytes : 0);
+            mbar_arrive_expect_tx(bar, (uint32_t)(nsub * L::kHalves * 2048));
+            for (int sb = 0; sb < nsub; ++sb) {
+                const int row = (t0 + sb * kTileTokens) & (p.block_size - 1);
+#pragma unroll
+                for (int hf = 0; hf < L::kHalves; ++hf)
+                    tma_load_4d(dst + hf * L::kKVHalf + sb * 2048, values ? &tmap_v : &tmap_k,
+                                bar, hf * 64, kh, row, ent[sb]);
+            }
+        };
         if (tid == 0) {
-            for (int si = 0; si < min(kTcStages, nstages); ++si)
-                issue(si);
+            for (int si = 0; si < min(kTcStages, nstages); ++si) {
+                lookup(si);
+                issue(si, false);
+                issue(si, true);
+            }
         }
-        pending = (1u << min(kTcStages, nstages)) - 1u;
+        pend_k = pend_v = (1u << min(kTcStages, nstages)) - 1u;
 
         // ---- this thread's row: query row, output location, key limit ------------------
         long long qoff = -1, ooff = -1;
@@ -313,22 +331,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         for (int si = 0; si < nstages; ++si) {
             const int st = si % kTcStages;
             const int t0 = kbeg + si * kTcTokens;
-            bool ok = mbar_wait_bounded(full_bar(st), (ph_full >> st) & 1u, kWaitLimitNs);
-            ph_full ^= 1u << st;
-            pending &= ~(1u << st);
-            // value rows past the key range -> zero (never fetched, or past the context)
-            const int nvalid = kend - t0;
-            if (nvalid < kTcTokens) {
-                const int rows = kTcTokens - nvalid;
-                for (int c = tid; c < L::kHalves * rows * 8; c += kTcThreads) {
-                    const int hf = c / (rows * 8), rem = c - hf * rows * 8;
-                    const uint32_t a = kbase(st) + L::kKVBytes + hf * L::kKVHalf +
-                                       (nvalid + rem / 8) * 128 + (rem % 8) * 16;
-                    asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(a), "r"(0)
-                                 : "memory");
-                }
-                fence_proxy_async_smem();
-            }
+            bool ok = mbar_wait_bounded(kbar(st), (ph_k >> st) & 1u, kWaitLimitNs);
+            ph_k ^= 1u << st;
+            pend_k &= ~(1u << st);
             if (__syncthreads_or(!ok)) {
                 aborted = true;
                 break;
@@ -355,8 +360,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 aborted = true;
                 break;
             }
+            // the K half of stage st is free: fetch the keys of tile si + 2
+            if (si + kTcStages < nstages) {
+                if (tid == 0) {
+                    lookup(si + kTcStages);
+                    issue(si + kTcStages, false);
+                }
+                pend_k |= 1u << st;
+            }
 
             // ---- softmax of this thread's row -------------------------------------------
+            // raw scores (q . k); the scale is applied inside the exponent
             float sv[kTcTokens];
 #pragma unroll
             for (int c = 0; c < kTcTokens / 32; ++c) {
@@ -366,12 +380,27 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 for (int i = 0; i < 32; ++i)
                     sv[c * 32 + i] = __uint_as_float(r[i]);
             }
-            float mx = -INFINITY;
+            if (lim < t0 + kTcTokens) {  // causal / range mask (diagonal and last tiles)
 #pragma unroll
-            for (int i = 0; i < kTcTokens; ++i) {
-                sv[i] = t0 + i < lim ? sv[i] * p.scale_log2 : -INFINITY;
-                mx = fmaxf(mx, sv[i]);
+                for (int i = 0; i < kTcTokens; ++i)
+                    sv[i] = t0 + i < lim ? sv[i] : -INFINITY;
             }
+            // maximum raw score (the scale is positive), as a tree
+            float e8[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                float x = sv[k];
+#pragma unroll
+                for (int i = k + 8; i < kTcTokens; i += 8)
+                    x = fmaxf(x, sv[i]);
+                e8[k] = x;
+            }
+#pragma unroll
+            for (int w = 4; w > 0; w >>= 1)
+#pragma unroll
+                for (int k = 0; k < w; ++k)
+                    e8[k] = fmaxf(e8[k], e8[k + w]);
+            const float mx = e8[0] * p.scale_log2;  // -inf for a fully masked row
             // the reference maximum moves only when a score passes it by 2^kSlack
             const bool moved = mx > m_ref + kSlack;
             float alpha = 1.f;
@@ -380,14 +409,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 m_ref = mx;
                 l_run *= alpha;
             }
-            const float mu = m_ref == -INFINITY ? 0.f : m_ref;
+            const float neg_mu = m_ref == -INFINITY ? 0.f : -m_ref;
             uint32_t pw[kTcTokens / 2];
+            float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int i = 0; i < kTcTokens / 2; ++i) {
-                const float p0 = exp2f(sv[2 * i] - mu), p1 = exp2f(sv[2 * i + 1] - mu);
-                l_run += p0 + p1;
+                const float p0 = exp2f(fmaf(sv[2 * i], p.scale_log2, neg_mu));
+                const float p1 = exp2f(fmaf(sv[2 * i + 1], p.scale_log2, neg_mu));
+                ls[i & 3] += p0 + p1;
                 pw[i] = MmaOp<T>::pack(p0, p1);
             }
+            l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
             tmem_st_32x32b_x32(tmem + lane_base, pw);  // P over S: columns [0, 32)
             // O was accumulated by earlier stages: rescale it in TMEM
             if (si > 0 && __any_sync(kFull, moved)) {
@@ -401,8 +433,28 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     tmem_st_32x32b_x32(tmem + lane_base + kTmemO + c * 32, r);
                 }
             }
+            // values of this tile landed; rows past the key range -> zero
+            // (never fetched, or past the context)
+            ok = mbar_wait_bounded(vbar(st), (ph_v >> st) & 1u, kWaitLimitNs);
+            ph_v ^= 1u << st;
+            pend_v &= ~(1u << st);
+            const int nvalid = kend - t0;
+            if (nvalid < kTcTokens) {
+                const int rows = kTcTokens - nvalid;
+                for (int c = tid; c < L::kHalves * rows * 8; c += kTcThreads) {
+                    const int hf = c / (rows * 8), rem = c - hf * rows * 8;
+                    const uint32_t a = kbase(st) + L::kKVBytes + hf * L::kKVHalf +
+                                       (nvalid + rem / 8) * 128 + (rem % 8) * 16;
+                    asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(a), "r"(0)
+                                 : "memory");
+                }
+                fence_proxy_async_smem();
+            }
             tc_fence_before();
-            __syncthreads();
+            if (__syncthreads_or(!ok)) {
+                aborted = true;
+                break;
+            }
 
             // O += P V (fp32 in TMEM columns [128, 128 + D))
             if (tid == 0) {
@@ -423,11 +475,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 aborted = true;
                 break;
             }
-            // stage st is free: refill it with tile si + 2
+            // the V half of stage st is free: fetch the values of tile si + 2
             if (si + kTcStages < nstages) {
                 if (tid == 0)
-                    issue(si + kTcStages);
-                pending |= 1u << st;
+                    issue(si + kTcStages, true);
+                pend_v |= 1u << st;
             }
         }
         if (aborted)
@@ -481,9 +533,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
     // ---- drain (only after an abort): fills still landing -------------------------------
     if (tid == 0) {
-        for (int st = 0; st < kTcStages; ++st)
-            if (pending & (1u << st))
-                mbar_wait_bounded(full_bar(st), (ph_full >> st) & 1u, kWaitLimitNs);
+        for (int st = 0; st < kTcStages; ++st) {
+            if (pend_k & (1u << st))
+                mbar_wait_bounded(kbar(st), (ph_k >> st) & 1u, kWaitLimitNs);
+            if (pend_v & (1u << st))
+                mbar_wait_bounded(vbar(st), (ph_v >> st) & 1u, kWaitLimitNs);
+        }
     }
     if (aborted && tid == 0)
         flag_error(p.error_word, PA_DEVERR_TIMEOUT);
@@ -523,23 +578,41 @@ static pa_status launch_mq(const MqParams &prm, const CUtensorMap &mk, const CUt
         if (smem > ks.smem_enabled) {
             e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      (int)smem);
+            // the whole unified L1/shared array as shared memory, so that the
+            // residency below is the one shared memory allows
+            if (e == cudaSuccess)
+                e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                         (int)cudaSharedmemCarveoutMaxShared);
             if (e != cudaSuccess)
                 return record_cuda(e);
             ks.smem_enabled = smem;
         }
         if (smem != ks.smem_queried) {
-            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&ks.per_sm, kernel,
-                                                              kTcThreads, smem);
+            // Residency from the kernel's own needs -- shared memory (plus the
+            // 1 KB the system reserves per CTA), registers, and tensor memory
+            // (kTmemCols of the SM's 512 columns per CTA).  (The runtime's
+            // occupancy query answers 1 for this kernel at any shared-memory
+            // size, while the launch itself fits two CTAs per SM.)
+            cudaFuncAttributes fa;
+            int smem_sm = 0, regs_sm = 0;
+            e = cudaFuncGetAttributes(&fa, kernel);
+            if (e == cudaSuccess)
+                e = cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor,
+                                           dev);
+            if (e == cudaSuccess)
+                e = cudaDeviceGetAttribute(&regs_sm, cudaDevAttrMaxRegistersPerMultiprocessor,
+                                           dev);
             if (e != cudaSuccess)
                 return record_cuda(e);
+            const int by_smem = smem_sm / (int)(smem + 1024);
+            const int by_regs = regs_sm / (((fa.numRegs + 7) & ~7) * kTcThreads);
+            ks.per_sm = std::min(std::min(by_smem, by_regs), (int)(512 / kTmemCols));
             ks.smem_queried = smem;
         }
         per_sm = ks.per_sm;
     }
     if (per_sm < 1)
         return PA_ERR_UNSUPPORTED;
-    // each CTA holds kTmemCols of the SM's 512 tensor-memory columns
-    per_sm = std::min(per_sm, (int)(512 / kTmemCols));
     long long grid = std::min<long long>((long long)info.sms * per_sm, max_units);
     if (grid < 1)
         grid = 1;
@@ -587,7 +660,8 @@ extern "C" pa_status pa_prefill_attention(void *out, const void *query, const vo
 {
     if (num_seqs < 0 || num_tokens < 0 || num_heads <= 0 || num_kv_heads <= 0 ||
         head_dim <= 0 || block_size <= 0 || num_blocks <= 0 || max_blocks_per_seq <= 0 ||
-        max_context_len < 0 || !std::isfinite(scale) || num_heads % num_kv_heads != 0)
+        max_context_len < 0 || !std::isfinite(scale) || !(scale > 0.f) ||
+        num_heads % num_kv_heads != 0)
         return PA_ERR_INVALID_ARG;
     if (dtype != PA_F16 && dtype != PA_BF16)
         return dtype == PA_FP8_E4M3 ? PA_ERR_UNSUPPORTED : PA_ERR_INVALID_ARG;
