@@ -50,7 +50,7 @@ constexpr int kTcThreads = 128;  // one thread per row
 constexpr int kTcTokens = 64;    // key/value tokens per stage (N of S = Q K^T)
 constexpr int kTcSubs = kTcTokens / kTileTokens;
 constexpr int kTcStages = 2;
-constexpr uint32_t kTmemCols = 256;  // S/P at column 0, O at column 128
+constexpr uint32_t kTmemCols = 256;  // S/P buffers at columns 0 and 64, O at column 128
 constexpr uint32_t kTmemO = 128;
 
 template <int D> struct TcLayout {
@@ -60,8 +60,8 @@ template <int D> struct TcLayout {
     static constexpr int kKVBytes = kHalves * kKVHalf;        // K (or V) of one stage
     static constexpr int kStageBytes = 2 * kKVBytes;          // K then V
     static constexpr int kQ = kTcStages * kStageBytes;
-    static constexpr int kBars = kQ + kHalves * kQHalf;       // k[2], v[2], s, o
-    static constexpr int kTmemSlot = kBars + 6 * 8;
+    static constexpr int kBars = kQ + kHalves * kQHalf;       // k[2], v[2], s[2], o
+    static constexpr int kTmemSlot = kBars + 8 * 8;
     static constexpr int kSeg = kTmemSlot + 16;               // int unit prefix[n + 1]
     static size_t bytes(int segments) { return 1024 + kSeg + 4 * ((size_t)segments + 1); }
     static_assert(kStageBytes % 1024 == 0 && kQ % 1024 == 0, "1024-byte aligned operands");
@@ -122,7 +122,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     int *pref = reinterpret_cast<int *>(smem + L::kSeg);
     auto kbar = [&](int st) { return sbase + L::kBars + st * 8; };       // K tile landed
     auto vbar = [&](int st) { return sbase + L::kBars + 16 + st * 8; };  // V tile landed
-    const uint32_t bar_s = sbase + L::kBars + 32, bar_o = sbase + L::kBars + 40;
+    auto sbar = [&](int b) { return sbase + L::kBars + 32 + b * 8; };  // S buffer b computed
+    const uint32_t bar_o = sbase + L::kBars + 48;                        // value product done
     auto kbase = [&](int st) { return sbase + st * L::kStageBytes; };
 
     const int tid = threadIdx.x, warp = tid >> 5;
@@ -134,7 +135,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             mbar_init(kbar(st), 1);
             mbar_init(vbar(st), 1);
         }
-        mbar_init(bar_s, 1);
+        mbar_init(sbar(0), 1);
+        mbar_init(sbar(1), 1);
         mbar_init(bar_o, 1);
         fence_barrier_init();
         prefetch_tensormap(&tmap_k);
@@ -179,8 +181,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     __syncthreads();
     const int total_units = pref[nseg] * Hkv;
 
-    uint32_t ph_k = 0, ph_v = 0, ph_s = 0, ph_o = 0;  // mbarrier parities
-    uint32_t pend_k = 0, pend_v = 0;  // stages with a K / V fill not yet waited for
+    // mbarrier parities (K fills are waited for by thread 0 alone)
+    uint32_t ph_k = 0, ph_v = 0, ph_s = 0, ph_o = 0;
+    uint32_t pend_k = 0, pend_v = 0;  // thread 0: stages with a fill not yet waited for
+    uint32_t pend_mma = 0;            // bit b: S buffer b committed, bit 2: value product
     bool aborted = false;
 
     for (int u = blockIdx.x; u < total_units && !aborted; u += gridDim.x) {
@@ -246,18 +250,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 flag_error(p.error_word, PA_DEVERR_PREFIX_PLAN);
         }
 
-        // thread 0: the physical blocks of tile `si` (up to 4 independent table
-        // loads), then the K or the V half of its fetch into stage si % 2.  K
-        // is refilled as soon as S = Q K^T of the tile two back has finished,
-        // V once its value product has: the key fetch gets a longer lead.
-        int ent[kTcSubs];
-        auto lookup = [&](int si) {
+        // thread 0: the physical blocks of a tile (up to 4 independent table
+        // loads, issued one tile ahead of their use), then the K or the V half
+        // of its fetch into stage si % 2.  K is refilled as soon as S = Q K^T
+        // of the tile two back has finished, V once the value product of the
+        // tile two back has.
+        auto lookup = [&](int si, int (&ent)[kTcSubs]) {
             const int t0 = kbeg + si * kTcTokens;
 #pragma unroll
             for (int sb = 0; sb < kTcSubs; ++sb) {
                 const int tok = t0 + sb * kTileTokens;
                 ent[sb] = tok < kend ? __ldg(table + (tok >> p.block_shift)) : 0;
             }
+        };
+        auto checked = [&](int (&ent)[kTcSubs]) {
 #pragma unroll
             for (int sb = 0; sb < kTcSubs; ++sb) {
                 if (ent[sb] < 0 || ent[sb] >= p.num_blocks) {
@@ -266,7 +272,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
             }
         };
-        auto issue = [&](int si, bool values) {
+        auto issue = [&](int si, bool values, const int (&ent)[kTcSubs]) {
             const int st = si % kTcStages;
             const int t0 = kbeg + si * kTcTokens;
             const int nsub = min(kTcSubs, (kend - t0 + kTileTokens - 1) / kTileTokens);
@@ -280,15 +286,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     tma_load_4d(dst + hf * L::kKVHalf + sb * 2048, values ? &tmap_v : &tmap_k,
                                 bar, hf * 64, kh, row, ent[sb]);
             }
+            if (values)
+                pend_v |= 1u << st;
+            else
+                pend_k |= 1u << st;
         };
+        int ent_cur[kTcSubs], ent_next[kTcSubs];  // thread 0: tiles si + 1 and si + 2
         if (tid == 0) {
             for (int si = 0; si < min(kTcStages, nstages); ++si) {
-                lookup(si);
-                issue(si, false);
-                issue(si, true);
+                lookup(si, ent_cur);
+                checked(ent_cur);
+                issue(si, false, ent_cur);
+                issue(si, true, ent_cur);
             }
         }
-        pend_k = pend_v = (1u << min(kTcStages, nstages)) - 1u;
 
         // ---- this thread's row: query row, output location, key limit ------------------
         long long qoff = -1, ooff = -1;
@@ -328,54 +339,52 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         fence_proxy_async_smem();
 
         float m_ref = -INFINITY, l_run = 0.f;
-        for (int si = 0; si < nstages; ++si) {
-            const int st = si % kTcStages;
-            const int t0 = kbeg + si * kTcTokens;
-            bool ok = mbar_wait_bounded(kbar(st), (ph_k >> st) & 1u, kWaitLimitNs);
+        bool ok = true;
+        // S = Q K^T of tile `si` into S buffer si % 2 (fp32, 64 columns);
+        // thread 0, once the keys have landed
+        auto issue_s = [&](int si) {
+            const int st = si % kTcStages, b = si & 1;
+            ok = mbar_wait_bounded(kbar(st), (ph_k >> st) & 1u, kWaitLimitNs) && ok;
             ph_k ^= 1u << st;
             pend_k &= ~(1u << st);
-            if (__syncthreads_or(!ok)) {
-                aborted = true;
-                break;
-            }
-
-            // S = Q K^T (fp32 in TMEM columns [0, 64))
-            if (tid == 0) {
-                tc_fence_after();
-#pragma unroll
-                for (int kk = 0; kk < KT; ++kk) {
-                    const uint64_t a = smem_desc_sw128(qbase + (kk >> 2) * L::kQHalf + (kk & 3) * 32,
-                                                       16, 1024);
-                    const uint64_t b = smem_desc_sw128(kbase(st) + (kk >> 2) * L::kKVHalf +
-                                                           (kk & 3) * 32,
-                                                       16, 1024);
-                    tc_mma_ss(tmem, a, b, kIdescS, kk > 0 ? 1u : 0u);
-                }
-                tc_commit(bar_s);
-            }
-            ok = mbar_wait_bounded(bar_s, ph_s, kWaitLimitNs);
-            ph_s ^= 1u;
             tc_fence_after();
-            if (__syncthreads_or(!ok)) {
-                aborted = true;
-                break;
+#pragma unroll
+            for (int kk = 0; kk < KT; ++kk) {
+                const uint64_t a = smem_desc_sw128(qbase + (kk >> 2) * L::kQHalf + (kk & 3) * 32,
+                                                   16, 1024);
+                const uint64_t bd = smem_desc_sw128(kbase(st) + (kk >> 2) * L::kKVHalf +
+                                                        (kk & 3) * 32,
+                                                    16, 1024);
+                tc_mma_ss(tmem + b * kTcTokens, a, bd, kIdescS, kk > 0 ? 1u : 0u);
             }
-            // the K half of stage st is free: fetch the keys of tile si + 2
-            if (si + kTcStages < nstages) {
-                if (tid == 0) {
-                    lookup(si + kTcStages);
-                    issue(si + kTcStages, false);
-                }
-                pend_k |= 1u << st;
-            }
+            tc_commit(sbar(b));
+        };
+        if (nstages > 0) {
+            __syncthreads();  // the query tile is in shared memory
+            if (tid == 0)
+                issue_s(0);
+            pend_mma |= 1u;
+        }
 
-            // ---- softmax of this thread's row -------------------------------------------
-            // raw scores (q . k); the scale is applied inside the exponent
+        for (int si = 0; si < nstages; ++si) {
+            const int st = si % kTcStages, b = si & 1;
+            const int t0 = kbeg + si * kTcTokens;
+            // thread 0: table entries of tile si + 2 (used after the MMAs below)
+            if (tid == 0 && si + kTcStages < nstages)
+                lookup(si + kTcStages, ent_next);
+            // 1. S of this tile
+            ok = mbar_wait_bounded(sbar(b), (ph_s >> b) & 1u, kWaitLimitNs) && ok;
+            ph_s ^= 1u << b;
+            pend_mma &= ~(1u << b);
+            tc_fence_after();
+
+            // 2. softmax of this thread's row: raw scores (q . k); the scale is
+            //    applied inside the exponent
             float sv[kTcTokens];
 #pragma unroll
             for (int c = 0; c < kTcTokens / 32; ++c) {
                 uint32_t r[32];
-                tmem_ld_32x32b_x32(tmem + lane_base + c * 32, r);
+                tmem_ld_32x32b_x32(tmem + lane_base + b * kTcTokens + c * 32, r);
 #pragma unroll
                 for (int i = 0; i < 32; ++i)
                     sv[c * 32 + i] = __uint_as_float(r[i]);
@@ -420,24 +429,36 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 pw[i] = MmaOp<T>::pack(p0, p1);
             }
             l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-            tmem_st_32x32b_x32(tmem + lane_base, pw);  // P over S: columns [0, 32)
-            // O was accumulated by earlier stages: rescale it in TMEM
-            if (si > 0 && __any_sync(kFull, moved)) {
+
+            // 3. the previous tile's value product has finished: O is final
+            //    for it, and its S buffer (the other one) is free
+            if (si > 0) {
+                ok = mbar_wait_bounded(bar_o, ph_o, kWaitLimitNs) && ok;
+                ph_o ^= 1u;
+                pend_mma &= ~4u;
+                tc_fence_after();
+                // 4. rescale O in TMEM when a row's reference maximum moved
+                if (__any_sync(kFull, moved)) {
 #pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
-                    uint32_t r[32];
-                    tmem_ld_32x32b_x32(tmem + lane_base + kTmemO + c * 32, r);
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint32_t r[32];
+                        tmem_ld_32x32b_x32(tmem + lane_base + kTmemO + c * 32, r);
 #pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-                    tmem_st_32x32b_x32(tmem + lane_base + kTmemO + c * 32, r);
+                        for (int i = 0; i < 32; ++i)
+                            r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+                        tmem_st_32x32b_x32(tmem + lane_base + kTmemO + c * 32, r);
+                    }
                 }
             }
-            // values of this tile landed; rows past the key range -> zero
-            // (never fetched, or past the context)
-            ok = mbar_wait_bounded(vbar(st), (ph_v >> st) & 1u, kWaitLimitNs);
+            // 5. P over this tile's S (A operand of the value product)
+            tmem_st_32x32b_x32(tmem + lane_base + b * kTcTokens, pw);
+
+            // 6. values of this tile; rows past the key range -> zero (never
+            //    fetched, or past the context)
+            ok = mbar_wait_bounded(vbar(st), (ph_v >> st) & 1u, kWaitLimitNs) && ok;
             ph_v ^= 1u << st;
-            pend_v &= ~(1u << st);
+            if (tid == 0)
+                pend_v &= ~(1u << st);
             const int nvalid = kend - t0;
             if (nvalid < kTcTokens) {
                 const int rows = kTcTokens - nvalid;
@@ -456,34 +477,48 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 break;
             }
 
-            // O += P V (fp32 in TMEM columns [128, 128 + D))
+            // 7. thread 0: O += P V of this tile; S of the next tile into the
+            //    other buffer (overlapping the next softmax); refills: K of tile
+            //    si + 2 into this stage (S of this tile is done), V of tile
+            //    si + 1 into the other stage (the value product of tile si - 1
+            //    is done)
             if (tid == 0) {
                 tc_fence_after();
 #pragma unroll
                 for (int ks = 0; ks < kTcTokens / 16; ++ks) {
-                    const uint64_t b = smem_desc_sw128(kbase(st) + L::kKVBytes + ks * 2048,
-                                                       L::kKVHalf, 1024);
-                    tc_mma_ts(tmem + kTmemO, tmem + ks * 8, b, kIdescO,
+                    const uint64_t bd = smem_desc_sw128(kbase(st) + L::kKVBytes + ks * 2048,
+                                                        L::kKVHalf, 1024);
+                    tc_mma_ts(tmem + kTmemO, tmem + b * kTcTokens + ks * 8, bd, kIdescO,
                               (si > 0 || ks > 0) ? 1u : 0u);
                 }
                 tc_commit(bar_o);
+                if (si + 1 < nstages)
+                    issue_s(si + 1);
+                if (si + kTcStages < nstages) {
+                    checked(ent_next);
+                    issue(si + kTcStages, false, ent_next);
+                }
+                if (si >= 1 && si + 1 < nstages)
+                    issue(si + 1, true, ent_cur);
+#pragma unroll
+                for (int sb = 0; sb < kTcSubs; ++sb)
+                    ent_cur[sb] = ent_next[sb];
             }
-            ok = mbar_wait_bounded(bar_o, ph_o, kWaitLimitNs);
+            pend_mma |= 4u | (si + 1 < nstages ? 1u << ((si + 1) & 1) : 0u);
+        }
+        if (aborted)
+            break;
+        // the last value product
+        if (nstages > 0) {
+            ok = mbar_wait_bounded(bar_o, ph_o, kWaitLimitNs) && ok;
             ph_o ^= 1u;
+            pend_mma &= ~4u;
             tc_fence_after();
             if (__syncthreads_or(!ok)) {
                 aborted = true;
                 break;
             }
-            // the V half of stage st is free: fetch the values of tile si + 2
-            if (si + kTcStages < nstages) {
-                if (tid == 0)
-                    issue(si + kTcStages, true);
-                pend_v |= 1u << st;
-            }
         }
-        if (aborted)
-            break;
 
         // ---- epilogue: this thread's row of O / l (TMEM loads are warp-wide) -----------
         const float inv = (nstages > 0 && l_run > 0.f) ? 1.f / l_run : 0.f;
@@ -539,6 +574,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (pend_v & (1u << st))
                 mbar_wait_bounded(vbar(st), (ph_v >> st) & 1u, kWaitLimitNs);
         }
+        // tensor-core work still committed (only after an abort)
+        for (int b = 0; b < 2; ++b)
+            if (pend_mma & (1u << b))
+                mbar_wait_bounded(sbar(b), (ph_s >> b) & 1u, kWaitLimitNs);
+        if (pend_mma & 4u)
+            mbar_wait_bounded(bar_o, ph_o, kWaitLimitNs);
     }
     if (aborted && tid == 0)
         flag_error(p.error_word, PA_DEVERR_TIMEOUT);
