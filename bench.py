@@ -45,8 +45,6 @@ METRIC = ("paged decode attention effective KV GB/s and % of GB300 HBM peak; "
 PREFILL_METRIC = "chunked-prefill paged attention TFLOP/s; tokens/s per step"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
-DECODE_SRC = os.path.join(ROOT, "paged_kv_cache_96_gb300", "csrc", "pa_decode.cu")
-TRAFFIC_SUMMARY = os.path.join(ROOT, "profiles", "decode_gqa70b_ncu.md")
 
 
 def parse_args(argv=None):
@@ -173,19 +171,60 @@ def measured_hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def recorded_traffic():
-    """DRAM bytes per launch of the decode kernel from the committed ncu
-    summary -- only if the kernel source is unchanged since the capture."""
+# Per workload: the committed ncu summary whose DRAM bytes per launch the
+# roofline's `traffic` reports, and the kernel sources it was captured from
+# (a changed source voids the figure).
+CSRC = os.path.join(ROOT, "paged_kv_cache_96_gb300", "csrc")
+DECODE_SOURCES = ["pa_decode.cu", "pa_decode_common.cuh", "pa_ptx.cuh"]
+PREFILL_SOURCES = ["pa_prefill.cu", "pa_tcgen05.cuh", "pa_decode_common.cuh", "pa_ptx.cuh"]
+TRAFFIC_SUMMARIES = {
+    "gqa70b": ("decode_gqa70b_ncu.md", DECODE_SOURCES),
+    "gqa70b-fp8": ("decode_gqa70b_fp8_ncu.md", DECODE_SOURCES),
+    "chunked": ("prefill_chunked_ncu.md", PREFILL_SOURCES),
+}
+
+
+def sources_sha256(names):
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(CSRC, n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def recorded_traffic(config: str, partition_is_default: bool = True):
+    """DRAM bytes per launch of the attention call from the committed ncu
+    summary of this workload -- only if its kernel sources are unchanged
+    since the capture and the launch configuration is the captured one."""
+    entry = TRAFFIC_SUMMARIES.get(config)
+    if entry is None or not partition_is_default:
+        return None
     try:
-        text = open(TRAFFIC_SUMMARY).read()
+        text = open(os.path.join(ROOT, "profiles", entry[0])).read()
     except OSError:
         return None
-    m_sha = re.search(r"kernel_source_sha256:\s*([0-9a-f]{64})", text)
+    m_sha = re.search(r"kernel_sources_sha256:\s*([0-9a-f]{64})", text)
     m_b = re.search(r"dram_bytes_per_launch_full_workload:\s*([0-9.eE+]+)", text)
     if not (m_sha and m_b):
         return None
-    sha = hashlib.sha256(open(DECODE_SRC, "rb").read()).hexdigest()
-    return float(m_b.group(1)) if sha == m_sha.group(1) else None
+    return float(m_b.group(1)) if sources_sha256(entry[1]) == m_sha.group(1) else None
+
+
+L2_BYTES = 129 * 1024 * 1024  # GB300 L2
+
+
+def step_bytes(w) -> int:
+    """Bytes one step touches: attended K/V (each physical block once) and the
+    step's queries and outputs."""
+    return w.unique_kv_bytes() + w.qo_bytes()
+
+
+def l2_note(w) -> str:
+    b = step_bytes(w)
+    if b < L2_BYTES:
+        return (f"step data {b / 1e6:.1f} MB < L2: L2 flushed before every timed step "
+                f"(write of {2 * L2_BYTES >> 20} MiB, outside the timed intervals)")
+    return f"inputs larger than L2: {b / 1e9:.2f} GB per step; no flush"
 
 
 def workload_config(w, partition_size, world=1):
@@ -197,7 +236,7 @@ def workload_config(w, partition_size, world=1):
             "head_dim": w.D, "block_size": w.bs, "num_blocks": w.num_blocks,
             "context_tokens": int(w.context_lens.sum()),
             "attention_flops_per_step": w.prefill_flops(),
-            "l2": "compute-bound step; K/V re-reads hit L2 by design, no flush",
+            "l2": l2_note(w),
             "parallelism": "replicas" if world > 1 else "single GPU",
             "kv_cache_dtype": w.dtype,
         }
@@ -206,7 +245,7 @@ def workload_config(w, partition_size, world=1):
         "num_seqs": w.S, "num_heads": w.H, "num_kv_heads": w.Hkv, "head_dim": w.D,
         "block_size": w.bs, "num_blocks": w.num_blocks, "partition_size": partition_size,
         "context_tokens": int(w.context_lens.sum()), "kv_bytes_per_step": kv,
-        "l2": f"inputs larger than L2: {kv / 1e9:.2f} GB of K/V read per step; no flush",
+        "l2": l2_note(w),
         "parallelism": "replicas" if world > 1 else "single GPU",
         "kv_cache_dtype": "fp8-e4m3" if w.fp8 else w.dtype,
     }
@@ -387,28 +426,33 @@ def run_ours(args):
         raise RuntimeError(f"device error word {int(st.error_word.item()):#x}")
 
     K = args.steps
+    ev_s = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     ev_a = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     ev_b = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    start = torch.cuda.Event(enable_timing=True)
-    end = torch.cuda.Event(enable_timing=True)
+    # A step whose data fits in L2 gets L2 flushed before it (a write of twice
+    # the L2 size, outside the timed intervals); larger steps need none.
+    flush = None
+    if step_bytes(w) < L2_BYTES:
+        flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize(dev)
     t_host0 = time.time()
-    start.record(stream)
     for i in range(K):
+        if flush is not None:
+            flush.zero_()
+        ev_s[i].record(stream)
         st.slot_mapping()
         st.reshape_and_cache()
         st.copy_blocks()
         ev_a[i].record(stream)
         st.attention()
         ev_b[i].record(stream)
-    end.record(stream)
     torch.cuda.synchronize(dev)
     t_host1 = time.time()
     if world > 1:
         torch.distributed.barrier()
-    step_s = start.elapsed_time(end) / 1e3
+    step_s = sum(a.elapsed_time(b) for a, b in zip(ev_s, ev_b)) / 1e3
     attn_s = sum(a.elapsed_time(b) for a, b in zip(ev_a, ev_b)) / 1e3 / K
     if sampler is not None:
         sampler.stop()
@@ -464,7 +508,8 @@ def run_ours(args):
             "us_per_step": per_step * 1e6,
             "attention_us": attn_s * 1e6,
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": tpeak,
-                         "unit": "TFLOP/s", "frac": achieved / tpeak, "traffic": None,
+                         "unit": "TFLOP/s", "frac": achieved / tpeak,
+                         "traffic": recorded_traffic(args.config),
                          "kernel": "pa_prefill_attention (paged_mq_kernel)",
                          "peak_kind": f"{tpeak_kind} bf16 (cuBLAS)",
                          "algorithmic_flops_per_launch": flops},
@@ -498,7 +543,9 @@ def run_ours(args):
         "unique_kv_gbs": w.unique_kv_bytes() * world / per_step / 1e9,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak,
-                     "traffic": None if st.cascade else recorded_traffic(),
+                     "traffic": recorded_traffic(
+                         args.config, args.partition is None
+                         or args.partition == w.spec.partition_size),
                      "kernel": kernel,
                      "peak_kind": f"{peak_kind} copy",
                      "algorithmic_bytes_per_launch": attn_bytes},
