@@ -57,7 +57,9 @@ typedef enum {
     PA_ERR_INVALID_ARG = 1,  /* null pointer, negative size, misalignment, ... */
     PA_ERR_UNSUPPORTED = 2,  /* valid but not implemented (head_dim, block_size, group) */
     PA_ERR_WORKSPACE = 3,    /* workspace missing or smaller than required */
-    PA_ERR_CUDA = 4          /* a CUDA runtime/driver call failed */
+    PA_ERR_CUDA = 4,         /* a CUDA runtime/driver call failed */
+    PA_ERR_OUT_OF_BLOCKS = 5, /* block manager: not enough free physical blocks */
+    PA_ERR_TABLE_FULL = 6    /* block manager: a table would pass max_blocks_per_seq */
 } pa_status;
 
 typedef enum {
@@ -366,6 +368,69 @@ PA_API pa_status pa_decode_attention_noalloc(void *out, const void *query,
                                              int head_dim, int block_size, int num_blocks,
                                              float scale, int partition_size, pa_dtype dtype,
                                              int32_t *error_word, void *stream);
+
+/*
+ * Host block manager -- the bookkeeping either side of the cache write and
+ * the block copy ([GAO] §1.3-§1.5, [FEI] "Block Table 实现" and
+ * "共享前缀的 Block 复用", [LAKE] §3.2 and §4.2, [P1] §3.1).  Host memory
+ * only; no call touches the GPU.  A manager owns the reference counts of a
+ * pool of num_blocks physical blocks of block_size tokens and one block table
+ * (logical block -> physical block) and token count per sequence:
+ *   - a token appended at position p of a sequence goes to a new block when
+ *     p % block_size == 0 (the lowest-numbered free block), otherwise into
+ *     the sequence's last block;
+ *   - fork gives the child the parent's table and token count, every block
+ *     gaining a reference (parallel samples, shared prefixes);
+ *   - appending into a last block that another table also names first copies
+ *     it (copy-on-write): a new block is allocated, the (old, new) pair is
+ *     returned for pa_copy_blocks -- which must run before the new tokens
+ *     are written -- the sequence's table names the new block and the old
+ *     one loses a reference;
+ *   - freeing a sequence drops one reference from each of its blocks; a block
+ *     no table names is free.
+ * Calls on one manager must not overlap (no internal locking).  Every call
+ * that fails leaves the manager unchanged.  Sequence ids are any values >= 0.
+ */
+typedef struct pa_block_manager pa_block_manager;
+
+/* A manager with every block free.  PA_ERR_INVALID_ARG for sizes <= 0 or a
+ * pool whose slots do not fit int32. */
+PA_API pa_status pa_bm_create(int num_blocks, int block_size, int max_blocks_per_seq,
+                              pa_block_manager **out);
+PA_API void pa_bm_destroy(pa_block_manager *bm);
+PA_API int pa_bm_num_free_blocks(const pa_block_manager *bm);
+/* A new, empty sequence (PA_ERR_INVALID_ARG if the id exists or is < 0). */
+PA_API pa_status pa_bm_add_sequence(pa_block_manager *bm, int seq_id);
+/* child_id gets parent_id's table and token count (PA_ERR_INVALID_ARG if the
+ * parent is unknown or the child exists). */
+PA_API pa_status pa_bm_fork(pa_block_manager *bm, int parent_id, int child_id);
+/* Append num_tokens tokens: slots[num_tokens] receive their cache slots
+ * (block * block_size + offset, [GAO] §1.5); cow_pairs[2 * cow_capacity]
+ * receive the (src, dst) copy-on-write pairs, *num_cow their count (at most
+ * 1 per call).  PA_ERR_OUT_OF_BLOCKS when the free blocks do not cover the
+ * new blocks and the copy, PA_ERR_TABLE_FULL past max_blocks_per_seq,
+ * PA_ERR_WORKSPACE when cow_capacity is too small. */
+PA_API pa_status pa_bm_append_tokens(pa_block_manager *bm, int seq_id, int num_tokens,
+                                     int32_t *slots, int32_t *cow_pairs, int cow_capacity,
+                                     int *num_cow);
+/* Blocks (new ones and a copy-on-write copy) an append of num_tokens would
+ * take, or -1 for an unknown sequence. */
+PA_API int pa_bm_blocks_needed(const pa_block_manager *bm, int seq_id, int num_tokens);
+PA_API pa_status pa_bm_free_sequence(pa_block_manager *bm, int seq_id);
+/* Token and block counts of a sequence. */
+PA_API pa_status pa_bm_sequence_info(const pa_block_manager *bm, int seq_id,
+                                     int *num_tokens, int *num_blocks);
+/* The sequence's table into row[capacity] (PA_ERR_WORKSPACE if shorter). */
+PA_API pa_status pa_bm_block_table(const pa_block_manager *bm, int seq_id, int32_t *row,
+                                   int capacity);
+/* Number of tables naming a block (-1 out of range). */
+PA_API int pa_bm_ref_count(const pa_block_manager *bm, int block);
+/* Step inputs for a batch: block_tables[n][max_blocks] (rows padded with
+ * pad_block) and context_lens[n] (token counts), host memory.
+ * PA_ERR_WORKSPACE if a table is longer than max_blocks. */
+PA_API pa_status pa_bm_build_batch(const pa_block_manager *bm, const int32_t *seq_ids, int n,
+                                   int32_t *block_tables, int max_blocks,
+                                   int32_t *context_lens, int32_t pad_block);
 
 /* Human-readable name of a status code (static storage). */
 PA_API const char *pa_status_string(pa_status status);

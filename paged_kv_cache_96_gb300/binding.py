@@ -19,7 +19,8 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.environ.get("PA_LIBRARY",
                            os.path.join(_HERE, "lib", "libpaged_attention.so"))
 
-PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_WORKSPACE, PA_ERR_CUDA = range(5)
+(PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_WORKSPACE, PA_ERR_CUDA,
+ PA_ERR_OUT_OF_BLOCKS, PA_ERR_TABLE_FULL) = range(7)
 PA_F16, PA_BF16, PA_FP8_E4M3 = 0, 1, 2
 
 DEVERR_SLOT_RANGE = 0x01
@@ -73,6 +74,18 @@ def _load() -> ctypes.CDLL:
         "pa_decode_attention_cascade": (i32, [P, P, P, P, P, i32, P, i32, i32, i32, i32, i32,
                                               i32, i32, f32, P, i32, i32, i32, P, sz, i32, P,
                                               P]),
+        "pa_bm_create": (i32, [i32, i32, i32, P]),
+        "pa_bm_destroy": (None, [P]),
+        "pa_bm_num_free_blocks": (i32, [P]),
+        "pa_bm_add_sequence": (i32, [P, i32]),
+        "pa_bm_fork": (i32, [P, i32, i32]),
+        "pa_bm_append_tokens": (i32, [P, i32, i32, P, P, i32, P]),
+        "pa_bm_blocks_needed": (i32, [P, i32, i32]),
+        "pa_bm_free_sequence": (i32, [P, i32]),
+        "pa_bm_sequence_info": (i32, [P, i32, P, P]),
+        "pa_bm_block_table": (i32, [P, i32, P, i32]),
+        "pa_bm_ref_count": (i32, [P, i32]),
+        "pa_bm_build_batch": (i32, [P, P, i32, P, i32, P, i32]),
         "pa_status_string": (ctypes.c_char_p, [i32]),
         "pa_last_cuda_error": (ctypes.c_char_p, []),
         "pa_version": (i32, []),
@@ -374,4 +387,86 @@ def pa_decode_attention_cascade(out: torch.Tensor, query: torch.Tensor,
         d, bs, N, float(scale), _dev(prefix_plan, "prefix_plan", torch.int32),
         int(num_groups), int(num_members), int(partition_size), ws_ptr, ws_bytes,
         _dtype_code(key_cache), _opt(error_word, "error_word"), _stream(stream)))
+
+
+class BlockManager:
+    """The library's host block manager (C++): block tables, reference
+    counts, copy-on-write decisions and slot mapping for a pool of
+    num_blocks blocks of block_size tokens.  Host memory only."""
+
+    def __init__(self, num_blocks: int, block_size: int, max_blocks_per_seq: int):
+        self._h = ctypes.c_void_p()
+        _check("pa_bm_create", _lib.pa_bm_create(num_blocks, block_size, max_blocks_per_seq,
+                                                 ctypes.byref(self._h)))
+        self.num_blocks, self.block_size = num_blocks, block_size
+        self.max_blocks_per_seq = max_blocks_per_seq
+
+    def close(self):
+        if self._h:
+            _lib.pa_bm_destroy(self._h)
+            self._h = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def num_free(self) -> int:
+        return int(_lib.pa_bm_num_free_blocks(self._h))
+
+    def add_sequence(self, seq: int) -> None:
+        _check("pa_bm_add_sequence", _lib.pa_bm_add_sequence(self._h, int(seq)))
+
+    def fork(self, parent: int, child: int) -> None:
+        _check("pa_bm_fork", _lib.pa_bm_fork(self._h, int(parent), int(child)))
+
+    def blocks_needed(self, seq: int, n: int) -> int:
+        return int(_lib.pa_bm_blocks_needed(self._h, int(seq), int(n)))
+
+    def append_tokens(self, seq: int, n: int):
+        """(slots int32 array [n], copy-on-write pairs [(src, dst)])."""
+        import numpy as np
+        slots = np.zeros(max(n, 1), dtype=np.int32)
+        pairs = np.zeros(2, dtype=np.int32)
+        ncow = ctypes.c_int(0)
+        _check("pa_bm_append_tokens", _lib.pa_bm_append_tokens(
+            self._h, int(seq), int(n), slots.ctypes.data_as(ctypes.c_void_p),
+            pairs.ctypes.data_as(ctypes.c_void_p), 1, ctypes.byref(ncow)))
+        return slots[:n], [(int(pairs[0]), int(pairs[1]))] if ncow.value else []
+
+    def free_sequence(self, seq: int) -> None:
+        _check("pa_bm_free_sequence", _lib.pa_bm_free_sequence(self._h, int(seq)))
+
+    def length(self, seq: int) -> int:
+        t, b = ctypes.c_int(0), ctypes.c_int(0)
+        _check("pa_bm_sequence_info", _lib.pa_bm_sequence_info(self._h, int(seq),
+                                                               ctypes.byref(t), ctypes.byref(b)))
+        return t.value
+
+    def table(self, seq: int):
+        import numpy as np
+        t, b = ctypes.c_int(0), ctypes.c_int(0)
+        _check("pa_bm_sequence_info", _lib.pa_bm_sequence_info(self._h, int(seq),
+                                                               ctypes.byref(t), ctypes.byref(b)))
+        row = np.zeros(max(b.value, 1), dtype=np.int32)
+        _check("pa_bm_block_table", _lib.pa_bm_block_table(
+            self._h, int(seq), row.ctypes.data_as(ctypes.c_void_p), b.value))
+        return row[:b.value].tolist()
+
+    def ref(self, block: int) -> int:
+        return int(_lib.pa_bm_ref_count(self._h, int(block)))
+
+    def build_batch(self, seqs, max_blocks: int, pad_block: int):
+        """(block_tables int32 [n, max_blocks], context_lens int32 [n])."""
+        import numpy as np
+        ids = np.ascontiguousarray(np.asarray(seqs, dtype=np.int32))
+        n = ids.shape[0]
+        tables = np.zeros((max(n, 1), max_blocks), dtype=np.int32)
+        lens = np.zeros(max(n, 1), dtype=np.int32)
+        _check("pa_bm_build_batch", _lib.pa_bm_build_batch(
+            self._h, ids.ctypes.data_as(ctypes.c_void_p), n,
+            tables.ctypes.data_as(ctypes.c_void_p), max_blocks,
+            lens.ctypes.data_as(ctypes.c_void_p), int(pad_block)))
+        return tables[:n], lens[:n]
 

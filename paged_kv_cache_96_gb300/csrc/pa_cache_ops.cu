@@ -321,6 +321,8 @@ extern "C" const char *pa_status_string(pa_status status)
     case PA_ERR_UNSUPPORTED: return "PA_ERR_UNSUPPORTED";
     case PA_ERR_WORKSPACE: return "PA_ERR_WORKSPACE";
     case PA_ERR_CUDA: return "PA_ERR_CUDA";
+    case PA_ERR_OUT_OF_BLOCKS: return "PA_ERR_OUT_OF_BLOCKS";
+    case PA_ERR_TABLE_FULL: return "PA_ERR_TABLE_FULL";
     }
     return "PA_UNKNOWN_STATUS";
 }
