@@ -413,6 +413,18 @@ PA_API pa_status pa_bm_fork(pa_block_manager *bm, int parent_id, int child_id);
 PA_API pa_status pa_bm_append_tokens(pa_block_manager *bm, int seq_id, int num_tokens,
                                      int32_t *slots, int32_t *cow_pairs, int cow_capacity,
                                      int *num_cow);
+/* One step's appends in one call: sequence seq_ids[i] gets counts[i] tokens
+ * (ids distinct); the result is that of pa_bm_append_tokens called for each
+ * in batch order.  slots[sum(counts)] receive the slots in batch order, and
+ * cow_pairs[2 * cow_capacity] / *num_cow the copy-on-write pairs of the whole
+ * batch (at most one per sequence; when every table naming a shared block
+ * appends, the last one writes in place).  All or nothing, checks in this
+ * order: a sequence unknown or repeated (PA_ERR_INVALID_ARG), past
+ * max_blocks_per_seq (PA_ERR_TABLE_FULL), more pairs than cow_capacity
+ * (PA_ERR_WORKSPACE), more blocks than are free (PA_ERR_OUT_OF_BLOCKS). */
+PA_API pa_status pa_bm_append_batch(pa_block_manager *bm, const int32_t *seq_ids,
+                                    const int32_t *counts, int n, int32_t *slots,
+                                    int32_t *cow_pairs, int cow_capacity, int *num_cow);
 /* Blocks (new ones and a copy-on-write copy) an append of num_tokens would
  * take, or -1 for an unknown sequence. */
 PA_API int pa_bm_blocks_needed(const pa_block_manager *bm, int seq_id, int num_tokens);

@@ -137,6 +137,33 @@ class BlockManager:
         self.lengths[seq] = length
         return slots, pairs
 
+    def append_batch(self, seqs: Sequence[int], counts: Sequence[int]
+                     ) -> Tuple[List[int], List[Tuple[int, int]]]:
+        """One step's appends: the appends of `seqs` in order, applied all or
+        nothing.  Refusals are checked in this order: an unknown or repeated
+        sequence (KeyError), a table past max_blocks_per_seq (TableFull),
+        then running out of blocks part-way (OutOfBlocks)."""
+        if len(set(seqs)) != len(seqs) or any(s not in self.tables for s in seqs):
+            raise KeyError(seqs)
+        bs = self.block_size
+        for s, n in zip(seqs, counts):
+            if n < 0:
+                raise KeyError(s)
+            if (self.lengths[s] + n + bs - 1) // bs > self.max_blocks_per_seq:
+                raise TableFull()
+        saved = (list(self.ref), {k: list(v) for k, v in self.tables.items()},
+                 dict(self.lengths))
+        slots, pairs = [], []
+        try:
+            for s, n in zip(seqs, counts):
+                sl, pr = self.append_tokens(s, n)
+                slots += sl
+                pairs += pr
+        except OutOfBlocks:
+            self.ref, self.tables, self.lengths = saved
+            raise
+        return slots, pairs
+
     # -- step inputs ------------------------------------------------------------
     def build_batch(self, seqs: Sequence[int], max_blocks: int,
                     pad_block: int) -> Tuple[List[List[int]], List[int]]:

@@ -80,6 +80,7 @@ def _load() -> ctypes.CDLL:
         "pa_bm_add_sequence": (i32, [P, i32]),
         "pa_bm_fork": (i32, [P, i32, i32]),
         "pa_bm_append_tokens": (i32, [P, i32, i32, P, P, i32, P]),
+        "pa_bm_append_batch": (i32, [P, P, P, i32, P, P, i32, P]),
         "pa_bm_blocks_needed": (i32, [P, i32, i32]),
         "pa_bm_free_sequence": (i32, [P, i32]),
         "pa_bm_sequence_info": (i32, [P, i32, P, P]),
@@ -434,6 +435,24 @@ class BlockManager:
             self._h, int(seq), int(n), slots.ctypes.data_as(ctypes.c_void_p),
             pairs.ctypes.data_as(ctypes.c_void_p), 1, ctypes.byref(ncow)))
         return slots[:n], [(int(pairs[0]), int(pairs[1]))] if ncow.value else []
+
+    def append_batch(self, seqs, counts):
+        """One step's appends in one call: (slots int32 array in batch order,
+        copy-on-write pairs [(src, dst)])."""
+        import numpy as np
+        ids = np.ascontiguousarray(np.asarray(seqs, dtype=np.int32))
+        cnt = np.ascontiguousarray(np.asarray(counts, dtype=np.int32))
+        total = int(cnt.sum()) if cnt.size else 0
+        slots = np.zeros(max(total, 1), dtype=np.int32)
+        cap = max(ids.shape[0], 1)
+        pairs = np.zeros(2 * cap, dtype=np.int32)
+        ncow = ctypes.c_int(0)
+        _check("pa_bm_append_batch", _lib.pa_bm_append_batch(
+            self._h, ids.ctypes.data_as(ctypes.c_void_p), cnt.ctypes.data_as(ctypes.c_void_p),
+            ids.shape[0], slots.ctypes.data_as(ctypes.c_void_p),
+            pairs.ctypes.data_as(ctypes.c_void_p), cap, ctypes.byref(ncow)))
+        return slots[:total], [(int(pairs[2 * i]), int(pairs[2 * i + 1]))
+                               for i in range(ncow.value)]
 
     def free_sequence(self, seq: int) -> None:
         _check("pa_bm_free_sequence", _lib.pa_bm_free_sequence(self._h, int(seq)))

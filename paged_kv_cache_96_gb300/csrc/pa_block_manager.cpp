@@ -155,6 +155,57 @@ extern "C" pa_status pa_bm_append_tokens(pa_block_manager *bm, int seq_id, int n
     return PA_OK;
 }
 
+extern "C" pa_status pa_bm_append_batch(pa_block_manager *bm, const int32_t *seq_ids,
+                                        const int32_t *counts, int n, int32_t *slots,
+                                        int32_t *cow_pairs, int cow_capacity, int *num_cow)
+{
+    if (!bm || n < 0 || !num_cow || cow_capacity < 0 ||
+        (n > 0 && (!seq_ids || !counts)))
+        return PA_ERR_INVALID_ARG;
+    *num_cow = 0;
+    // check the whole batch first: the call is all or nothing
+    std::unordered_map<int, int> seen;
+    // partly filled shared last blocks -> batch sequences appending into them
+    std::unordered_map<int32_t, int> sharers;
+    int64_t need = 0, total = 0;
+    const int64_t bs = bm->block_size;
+    for (int i = 0; i < n; ++i) {
+        auto it = bm->seqs.find(seq_ids[i]);
+        if (it == bm->seqs.end() || counts[i] < 0 || !seen.emplace(seq_ids[i], i).second)
+            return PA_ERR_INVALID_ARG;
+        const pa_block_manager::Seq &s = it->second;
+        if ((s.tokens + counts[i] + bs - 1) / bs > bm->max_blocks_per_seq)
+            return PA_ERR_TABLE_FULL;
+        need += (s.tokens + counts[i] + bs - 1) / bs - (s.tokens + bs - 1) / bs;
+        total += counts[i];
+        if (counts[i] > 0 && s.tokens % bs != 0 && bm->ref[s.table.back()] > 1)
+            ++sharers[s.table.back()];
+    }
+    if (total > 0 && !slots)
+        return PA_ERR_INVALID_ARG;
+    // in batch order, the first ref - 1 appenders into a shared block copy it;
+    // if every table naming it appends, the last one writes in place
+    int64_t cows = 0;
+    for (const auto &kv : sharers)
+        cows += std::min<int64_t>(kv.second, bm->ref[kv.first] - 1);
+    if (cows > cow_capacity || (cows > 0 && !cow_pairs))
+        return PA_ERR_WORKSPACE;
+    if (need + cows > (int64_t)bm->free_heap.size())
+        return PA_ERR_OUT_OF_BLOCKS;
+    int64_t k = 0;
+    for (int i = 0; i < n; ++i) {
+        int c = 0;
+        const pa_status st = pa_bm_append_tokens(bm, seq_ids[i], counts[i], slots + k,
+                                                 cow_pairs + 2 * *num_cow,
+                                                 cow_capacity - *num_cow, &c);
+        if (st != PA_OK)  // not reached: every condition was checked above
+            return st;
+        *num_cow += c;
+        k += counts[i];
+    }
+    return PA_OK;
+}
+
 extern "C" pa_status pa_bm_free_sequence(pa_block_manager *bm, int seq_id)
 {
     if (!bm)

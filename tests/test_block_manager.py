@@ -30,7 +30,7 @@ def test_random_sessions_match_reference(seed):
     bm, ref = B.BlockManager(N, bs, MB), M.BlockManager(N, bs, MB)
     live, nxt = [], 0
     for _ in range(400):
-        op = int(rng.integers(0, 5))
+        op = int(rng.integers(0, 6))
         if op == 0 or not live:
             bm.add_sequence(nxt)
             ref.add_sequence(nxt)
@@ -59,6 +59,25 @@ def test_random_sessions_match_reference(seed):
             else:
                 with pytest.raises(B.PAError) as ex:
                     bm.append_tokens(s, n)
+                assert ex.value.status == err
+        elif op == 4:
+            # one step's appends for a random subset (forked sharers included)
+            k = int(rng.integers(1, len(live) + 1))
+            seqs = [int(x) for x in rng.choice(live, size=k, replace=False)]
+            counts = [int(rng.integers(0, 2 * bs + 2)) for _ in seqs]
+            try:
+                want = ref.append_batch(seqs, counts)
+                err = None
+            except M.OutOfBlocks:
+                err = B.PA_ERR_OUT_OF_BLOCKS
+            except M.TableFull:
+                err = B.PA_ERR_TABLE_FULL
+            if err is None:
+                slots, pairs = bm.append_batch(seqs, counts)
+                assert slots.tolist() == want[0] and pairs == want[1]
+            else:
+                with pytest.raises(B.PAError) as ex:
+                    bm.append_batch(seqs, counts)
                 assert ex.value.status == err
         else:
             s = live.pop(int(rng.integers(0, len(live))))
@@ -99,6 +118,24 @@ def test_refusals_change_nothing():
     lib = B.lib()
     assert lib.pa_bm_create(0, 16, 4, None) == B.PA_ERR_INVALID_ARG
     assert lib.pa_bm_ref_count(bm._h, 4) == -1 and lib.pa_bm_blocks_needed(bm._h, 11, 1) == -1
+
+
+def test_batch_where_every_sharer_appends():
+    """Three tables on one partly filled block all append in one step: the
+    first two copy it, the last writes in place; a repeated id is refused."""
+    bm = B.BlockManager(16, 4, 8)
+    bm.add_sequence(0)
+    bm.append_tokens(0, 6)
+    bm.fork(0, 1)
+    bm.fork(0, 2)
+    shared = bm.table(0)[1]
+    slots, pairs = bm.append_batch([2, 0, 1], [1, 1, 1])
+    assert [p[0] for p in pairs] == [shared, shared]
+    assert bm.table(1)[1] == shared and bm.ref(shared) == 1
+    assert slots[2] == shared * 4 + 2
+    with pytest.raises(B.PAError) as ex:
+        bm.append_batch([0, 0], [1, 1])
+    assert ex.value.status == B.PA_ERR_INVALID_ARG
 
 
 def test_copy_on_write_needs_room_for_the_pair():

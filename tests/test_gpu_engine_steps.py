@@ -54,13 +54,13 @@ def test_engine_steps_with_block_manager(B):
 
     def append(seqs, counts):
         """Append tokens on both managers; write their K/V on both sides."""
-        all_slots, all_pairs = [], []
-        for s, n in zip(seqs, counts):
-            slots, pairs = bm.append_tokens(s, n)
-            want_s, want_p = ref.append_tokens(s, n)
-            assert slots.tolist() == want_s and pairs == want_p
-            all_slots += want_s
-            all_pairs += want_p
+        if len(seqs) == 1:
+            slots, pairs = bm.append_tokens(seqs[0], counts[0])
+            all_slots, all_pairs = ref.append_tokens(seqs[0], counts[0])
+        else:  # one step's appends in one call
+            slots, pairs = bm.append_batch(seqs, counts)
+            all_slots, all_pairs = ref.append_batch(seqs, counts)
+        assert slots.tolist() == all_slots and pairs == all_pairs
         T = len(all_slots)
         k, v = _bits(rng, (T, HKV, D)), _bits(rng, (T, HKV, D))
         sl = np.asarray(all_slots, np.int32)
