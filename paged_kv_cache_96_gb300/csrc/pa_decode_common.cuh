@@ -98,10 +98,19 @@ __device__ __forceinline__ int prefix_partitions(int start, int part_tokens)
 // independent, so a sequence with up to QG * kReduceUnroll partitions costs
 // two dependent trips to memory.
 constexpr int kReduceThreads = 256;
-constexpr int kReduceUnroll = 8;
+#ifndef PA_REDUCE_UNROLL
+#define PA_REDUCE_UNROLL 4
+#endif
+#ifndef PA_REDUCE_MINB
+#define PA_REDUCE_MINB 3
+#endif
+// partitions whose loads are issued together per thread; CTAs per SM the
+// register budget is sized for (3 x 256 threads, 85 registers; measured
+// against 2 to 8 CTAs and unrolls of 2 to 8)
+constexpr int kReduceUnroll = PA_REDUCE_UNROLL;
 
 template <typename T, int D>
-__global__ void __launch_bounds__(kReduceThreads)
+__global__ void __launch_bounds__(kReduceThreads, PA_REDUCE_MINB)
     paged_reduce_kernel(const __grid_constant__ DecodeParams p)
 {
     using Op = MmaOp<T>;
