@@ -459,12 +459,14 @@ def run_reference(args):
     from paged_kv_cache_96_gb300 import workloads as W
     w = W.build(W.CONFIGS[args.config])
     oc = OracleCache(w)
-    # per step: a bounded sample of sequences sized for ~2 s of CPU work
+    # per step: a bounded sample of sequences, sized so that the whole run
+    # (warm-up + timed steps) takes about 2.5 minutes of CPU work, at most 2 s
+    # per step
     cost = (lambda s: _seq_flops(w, s)) if w.prefill else (lambda s: int(w.context_lens[s]))
     t0 = time.perf_counter()
     oc.attention([0])
     per_unit = (time.perf_counter() - t0) / max(1, cost(0))
-    budget = 2.0
+    budget = min(2.0, 150.0 / max(1, args.steps + args.warmup))
     sample, toks, units = [], 0, 0
     for s in range(w.S):
         if sample and (units + cost(s)) * per_unit > budget:
