@@ -125,6 +125,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     auto sbar = [&](int b) { return sbase + L::kBars + 32 + b * 8; };  // S buffer b computed
     const uint32_t bar_o = sbase + L::kBars + 48;                        // value product done
     auto kbase = [&](int st) { return sbase + st * L::kStageBytes; };
+    // operand descriptors of stage 0 and of the query tile; other stages and
+    // k-steps add their byte offset / 16 to the start-address field
+    const uint64_t desc_q0 = smem_desc_sw128(qbase, 16, 1024);
+    const uint64_t desc_k0 = smem_desc_sw128(sbase, 16, 1024);
+    const uint64_t desc_v0 = smem_desc_sw128(sbase + L::kKVBytes, L::kKVHalf, 1024);
 
     const int tid = threadIdx.x, warp = tid >> 5;
     const int G = p.group, Hkv = p.num_kv_heads, H = p.num_heads;
@@ -250,52 +255,48 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 flag_error(p.error_word, PA_DEVERR_PREFIX_PLAN);
         }
 
-        // thread 0: the physical blocks of a tile (up to 4 independent table
-        // loads, issued one tile ahead of their use), then the K or the V half
-        // of its fetch into stage si % 2.  K is refilled as soon as S = Q K^T
-        // of the tile two back has finished, V once the value product of the
-        // tile two back has.
-        auto lookup = [&](int si, int (&ent)[kTcSubs]) {
-            const int t0 = kbeg + si * kTcTokens;
-#pragma unroll
-            for (int sb = 0; sb < kTcSubs; ++sb) {
-                const int tok = t0 + sb * kTileTokens;
-                ent[sb] = tok < kend ? __ldg(table + (tok >> p.block_shift)) : 0;
-            }
+        // warp 0 fetches: lane j < 2 * kTcSubs (j < kTcSubs for d = 64) owns
+        // the 16-token sub-tile j / halves and d-half j % halves of every tile,
+        // looks up its physical block one tile ahead of its use and issues its
+        // own 2 KB box, so the boxes of a K or V tile go out in one warp step.
+        // K is refilled as soon as S = Q K^T of the tile two back has
+        // finished, V once the value product of the tile two back has.
+        const int lane = tid & 31;
+        const int my_sb = lane / L::kHalves, my_hf = lane % L::kHalves;
+        auto lookup = [&](int si) {
+            const int tok = kbeg + si * kTcTokens + my_sb * kTileTokens;
+            return (my_sb < kTcSubs && tok < kend) ? __ldg(table + (tok >> p.block_shift)) : 0;
         };
-        auto checked = [&](int (&ent)[kTcSubs]) {
-#pragma unroll
-            for (int sb = 0; sb < kTcSubs; ++sb) {
-                if (ent[sb] < 0 || ent[sb] >= p.num_blocks) {
-                    flag_error(p.error_word, PA_DEVERR_BLOCK_RANGE);
-                    ent[sb] = 0;  // stays inside the pool; the row's output is undefined
-                }
+        auto checked = [&](int ent) {
+            if (ent < 0 || ent >= p.num_blocks) {
+                flag_error(p.error_word, PA_DEVERR_BLOCK_RANGE);
+                ent = 0;  // stays inside the pool; the row's output is undefined
             }
+            return ent;
         };
-        auto issue = [&](int si, bool values, const int (&ent)[kTcSubs]) {
+        auto issue = [&](int si, bool values, int ent) {  // warp 0, all lanes
             const int st = si % kTcStages;
             const int t0 = kbeg + si * kTcTokens;
             const int nsub = min(kTcSubs, (kend - t0 + kTileTokens - 1) / kTileTokens);
             const uint32_t bar = values ? vbar(st) : kbar(st);
-            const uint32_t dst = kbase(st) + (values ? L::kKVBytes : 0);
-            mbar_arrive_expect_tx(bar, (uint32_t)(nsub * L::kHalves * 2048));
-            for (int sb = 0; sb < nsub; ++sb) {
-                const int row = (t0 + sb * kTileTokens) & (p.block_size - 1);
-#pragma unroll
-                for (int hf = 0; hf < L::kHalves; ++hf)
-                    tma_load_4d(dst + hf * L::kKVHalf + sb * 2048, values ? &tmap_v : &tmap_k,
-                                bar, hf * 64, kh, row, ent[sb]);
+            if (lane == 0)
+                mbar_arrive_expect_tx(bar, (uint32_t)(nsub * L::kHalves * 2048));
+            __syncwarp();
+            if (my_sb < nsub) {
+                const int row = (t0 + my_sb * kTileTokens) & (p.block_size - 1);
+                tma_load_4d(kbase(st) + (values ? L::kKVBytes : 0) + my_hf * L::kKVHalf +
+                                my_sb * 2048,
+                            values ? &tmap_v : &tmap_k, bar, my_hf * 64, kh, row, ent);
             }
             if (values)
                 pend_v |= 1u << st;
             else
                 pend_k |= 1u << st;
         };
-        int ent_cur[kTcSubs], ent_next[kTcSubs];  // thread 0: tiles si + 1 and si + 2
-        if (tid == 0) {
+        int ent_cur = 0, ent_next = 0;  // warp 0: this lane's entry of tiles si + 1, si + 2
+        if (warp == 0) {
             for (int si = 0; si < min(kTcStages, nstages); ++si) {
-                lookup(si, ent_cur);
-                checked(ent_cur);
+                ent_cur = checked(lookup(si));
                 issue(si, false, ent_cur);
                 issue(si, true, ent_cur);
             }
@@ -341,27 +342,29 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         float m_ref = -INFINITY, l_run = 0.f;
         bool ok = true;
         // S = Q K^T of tile `si` into S buffer si % 2 (fp32, 64 columns);
-        // thread 0, once the keys have landed
+        // warp 0 (one elected lane issues), once the keys have landed
         auto issue_s = [&](int si) {
             const int st = si % kTcStages, b = si & 1;
             ok = mbar_wait_bounded(kbar(st), (ph_k >> st) & 1u, kWaitLimitNs) && ok;
             ph_k ^= 1u << st;
             pend_k &= ~(1u << st);
             tc_fence_after();
+            const uint64_t dk = desc_k0 + (uint64_t)((st * L::kStageBytes) >> 4);
+            if (elect_one()) {
 #pragma unroll
-            for (int kk = 0; kk < KT; ++kk) {
-                const uint64_t a = smem_desc_sw128(qbase + (kk >> 2) * L::kQHalf + (kk & 3) * 32,
-                                                   16, 1024);
-                const uint64_t bd = smem_desc_sw128(kbase(st) + (kk >> 2) * L::kKVHalf +
-                                                        (kk & 3) * 32,
-                                                    16, 1024);
-                tc_mma_ss(tmem + b * kTcTokens, a, bd, kIdescS, kk > 0 ? 1u : 0u);
+                for (int kk = 0; kk < KT; ++kk) {
+                    const uint32_t qo = ((kk >> 2) * L::kQHalf + (kk & 3) * 32) >> 4;
+                    const uint32_t ko = ((kk >> 2) * L::kKVHalf + (kk & 3) * 32) >> 4;
+                    tc_mma_ss(tmem + b * kTcTokens, desc_q0 + qo, dk + ko, kIdescS,
+                              kk > 0 ? 1u : 0u);
+                }
+                tc_commit(sbar(b));
             }
-            tc_commit(sbar(b));
+            __syncwarp();
         };
         if (nstages > 0) {
             __syncthreads();  // the query tile is in shared memory
-            if (tid == 0)
+            if (warp == 0)
                 issue_s(0);
             pend_mma |= 1u;
         }
@@ -369,9 +372,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         for (int si = 0; si < nstages; ++si) {
             const int st = si % kTcStages, b = si & 1;
             const int t0 = kbeg + si * kTcTokens;
-            // thread 0: table entries of tile si + 2 (used after the MMAs below)
-            if (tid == 0 && si + kTcStages < nstages)
-                lookup(si + kTcStages, ent_next);
+            // warp 0: table entries of tile si + 2 (used after the softmax below)
+            if (warp == 0 && si + kTcStages < nstages)
+                ent_next = lookup(si + kTcStages);
             // 1. S of this tile
             ok = mbar_wait_bounded(sbar(b), (ph_s >> b) & 1u, kWaitLimitNs) && ok;
             ph_s ^= 1u << b;
@@ -431,7 +434,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
 
             // 3. the previous tile's value product has finished: O is final
-            //    for it, and its S buffer (the other one) is free
+            //    for it, its S buffer (the other one) and its value stage are
+            //    free
             if (si > 0) {
                 ok = mbar_wait_bounded(bar_o, ph_o, kWaitLimitNs) && ok;
                 ph_o ^= 1u;
@@ -450,6 +454,24 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     }
                 }
             }
+            // warp 0: S of the next tile into the other buffer (thread 0), so
+            // the tensor core computes it while this tile's P is stored and its
+            // value product waits for the block; refills: K of tile si + 2
+            // into this stage (S of this tile is done), V of tile si + 1 into
+            // the other stage (the value product of tile si - 1 is done)
+            if (warp == 0) {
+                if (si + 1 < nstages)
+                    issue_s(si + 1);
+                if (si + kTcStages < nstages) {
+                    ent_next = checked(ent_next);
+                    issue(si + kTcStages, false, ent_next);
+                }
+                if (si >= 1 && si + 1 < nstages)
+                    issue(si + 1, true, ent_cur);
+                ent_cur = ent_next;
+            }
+            if (si + 1 < nstages)
+                pend_mma |= 1u << ((si + 1) & 1);
             // 5. P over this tile's S (A operand of the value product)
             tmem_st_32x32b_x32(tmem + lane_base + b * kTcTokens, pw);
 
@@ -477,34 +499,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 break;
             }
 
-            // 7. thread 0: O += P V of this tile; S of the next tile into the
-            //    other buffer (overlapping the next softmax); refills: K of tile
-            //    si + 2 into this stage (S of this tile is done), V of tile
-            //    si + 1 into the other stage (the value product of tile si - 1
-            //    is done)
-            if (tid == 0) {
+            // 7. thread 0: O += P V of this tile (queued behind S of the next
+            //    tile, so the next softmax can start while it runs)
+            if (warp == 0) {
                 tc_fence_after();
+                const uint64_t dv = desc_v0 + (uint64_t)((st * L::kStageBytes) >> 4);
+                if (elect_one()) {
 #pragma unroll
-                for (int ks = 0; ks < kTcTokens / 16; ++ks) {
-                    const uint64_t bd = smem_desc_sw128(kbase(st) + L::kKVBytes + ks * 2048,
-                                                        L::kKVHalf, 1024);
-                    tc_mma_ts(tmem + kTmemO, tmem + b * kTcTokens + ks * 8, bd, kIdescO,
-                              (si > 0 || ks > 0) ? 1u : 0u);
+                    for (int ks = 0; ks < kTcTokens / 16; ++ks)
+                        tc_mma_ts(tmem + kTmemO, tmem + b * kTcTokens + ks * 8,
+                                  dv + (uint64_t)((ks * 2048) >> 4), kIdescO,
+                                  (si > 0 || ks > 0) ? 1u : 0u);
+                    tc_commit(bar_o);
                 }
-                tc_commit(bar_o);
-                if (si + 1 < nstages)
-                    issue_s(si + 1);
-                if (si + kTcStages < nstages) {
-                    checked(ent_next);
-                    issue(si + kTcStages, false, ent_next);
-                }
-                if (si >= 1 && si + 1 < nstages)
-                    issue(si + 1, true, ent_cur);
-#pragma unroll
-                for (int sb = 0; sb < kTcSubs; ++sb)
-                    ent_cur[sb] = ent_next[sb];
+                __syncwarp();
             }
-            pend_mma |= 4u | (si + 1 < nstages ? 1u << ((si + 1) & 1) : 0u);
+            pend_mma |= 4u;
         }
         if (aborted)
             break;

@@ -32,6 +32,18 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols)
 }
 
 // Order tcgen05 operations against a thread synchronisation.
+// One lane of a converged warp (elect.sync over the full mask): the issuing
+// lane of tcgen05.mma / commit, with the operands computed warp-wide.
+__device__ __forceinline__ bool elect_one()
+{
+    uint32_t leader;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t.reg .b32 l;\n\t"
+        "elect.sync l|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(leader));
+    return leader != 0;
+}
+
 __device__ __forceinline__ void tc_fence_before()
 {
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
