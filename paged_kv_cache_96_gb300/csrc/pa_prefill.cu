@@ -18,21 +18,27 @@
 //
 // Design (GB300): a CTA takes 128 query rows of one KV head -- a chunk's
 // tokens times the G query heads of the group, or the members' decode
-// queries times G -- as the M = 128 dimension of tcgen05.mma tiles.  The
-// rows sit in shared memory as the K-major A operand (128-byte swizzle);
-// keys and values stream through a 2-stage ring of 64-token tiles fetched by
-// 4-D TMA loads (2 KB boxes, 128-byte swizzle) whose layout is directly the
-// K-major B operand of S = Q K^T and the MN-major B operand of O += P V.
-// S (128 x 64, fp32) and O (128 x d, fp32) live in tensor memory; one thread
-// per row reads its S row, applies the causal / range mask and the online
+// queries times G -- as the M = 128 dimension of tcgen05.mma tiles, and its
+// six warps split the work.  Warps 0-3 (one thread per row) write the rows
+// into shared memory as the K-major A operand (128-byte swizzle), read each
+// S row from tensor memory, apply the causal / range mask and the online
 // softmax (fp32, log2 units, a reference maximum that moves only when a
-// score exceeds it by 2^8, rescaling O in tensor memory then), and writes P
-// as bf16/fp16 pairs back over S, where it is the A operand of the value
-// product.  One elected thread issues the MMAs and commits them to
-// mbarriers; every wait is bounded in time, and tensor memory is released on
-// every exit path.  Value rows past the key range are zeroed in shared memory
-// before the value product, so a poisoned (NaN) slot never reaches the
-// output.
+// score exceeds it by 2^8, rescaling O in tensor memory then), and write P as
+// bf16/fp16 pairs back over S, where it is the A operand of the value
+// product.  Warp 4 looks up the physical blocks and streams keys and values
+// through a 2-stage ring of 64-token tiles by 4-D TMA loads (2 KB boxes,
+// 128-byte swizzle) whose layout is directly the K-major B operand of
+// S = Q K^T and the MN-major B operand of O += P V.  Warp 5 issues the MMAs
+// from one elected lane: S of tile g into S buffer g % 2 as soon as its keys
+// have landed and the buffer's previous P has been consumed, then the value
+// product of tile g - 1, and commits each to an mbarrier that frees the ring
+// stage or the S buffer it used.  S (128 x 64, fp32, double-buffered) and
+// O (128 x d, fp32) live in tensor memory (256 columns, so two CTAs share an
+// SM).  The roles meet only at mbarriers whose phase is the tile's index
+// over the CTA's units / 2; every wait is bounded in time, the first to run
+// out stops all roles, and tensor memory is released on every exit path.
+// Value rows past the key range are zeroed in shared memory before the value
+// product, so a poisoned (NaN) slot never reaches the output.
 #include <cuda.h>
 
 #include <algorithm>
@@ -46,7 +52,10 @@
 namespace pa {
 
 constexpr int kTcRows = 128;     // query rows per CTA (M of the MMAs)
-constexpr int kTcThreads = 128;  // one thread per row
+constexpr int kRowWarps = 4;     // warps 0-3: one thread per row (softmax, epilogue)
+constexpr int kFetchWarp = 4;    // table lookups and K/V fetches
+constexpr int kMmaWarp = 5;      // tensor-core issue
+constexpr int kTcThreads = 32 * (kRowWarps + 2);
 constexpr int kTcTokens = 64;    // key/value tokens per stage (N of S = Q K^T)
 constexpr int kTcSubs = kTcTokens / kTileTokens;
 constexpr int kTcStages = 2;
@@ -60,8 +69,9 @@ template <int D> struct TcLayout {
     static constexpr int kKVBytes = kHalves * kKVHalf;        // K (or V) of one stage
     static constexpr int kStageBytes = 2 * kKVBytes;          // K then V
     static constexpr int kQ = kTcStages * kStageBytes;
-    static constexpr int kBars = kQ + kHalves * kQHalf;       // k[2], v[2], s[2], o
-    static constexpr int kTmemSlot = kBars + 8 * 8;
+    static constexpr int kBars = kQ + kHalves * kQHalf;       // 12 mbarriers
+    static constexpr int kTmemSlot = kBars + 12 * 8;
+    static constexpr int kAbort = kTmemSlot + 8;
     static constexpr int kSeg = kTmemSlot + 16;               // int unit prefix[n + 1]
     static size_t bytes(int segments) { return 1024 + kSeg + 4 * ((size_t)segments + 1); }
     static_assert(kStageBytes % 1024 == 0 && kQ % 1024 == 0, "1024-byte aligned operands");
@@ -103,7 +113,7 @@ __device__ __forceinline__ int mq_segment_units(const MqParams &p, int seg)
 }
 
 template <typename T, int D>
-__global__ void __launch_bounds__(kTcThreads, 1)
+__global__ void __launch_bounds__(kTcThreads, 2)
     paged_mq_kernel(const __grid_constant__ MqParams p,
                     const __grid_constant__ CUtensorMap tmap_k,
                     const __grid_constant__ CUtensorMap tmap_v)
@@ -120,10 +130,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const uint32_t sbase = smem_addr(smem);
     const uint32_t qbase = sbase + L::kQ;
     int *pref = reinterpret_cast<int *>(smem + L::kSeg);
-    auto kbar = [&](int st) { return sbase + L::kBars + st * 8; };       // K tile landed
-    auto vbar = [&](int st) { return sbase + L::kBars + 16 + st * 8; };  // V tile landed
-    auto sbar = [&](int b) { return sbase + L::kBars + 32 + b * 8; };  // S buffer b computed
-    const uint32_t bar_o = sbase + L::kBars + 48;                        // value product done
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kAbort);
+    // mbarriers: K / V of stage st landed (fetch warp, transaction bytes);
+    // S of buffer b computed (its commit also frees K stage b); value product
+    // of stage st done (frees V stage st and S buffer st, makes O current);
+    // P of buffer b stored by the 4 row warps; query tile in shared memory
+    // (4 row warps); every tensor-core operation of the CTA done (drain)
+    auto bar = [&](int i) { return sbase + L::kBars + 8 * i; };
+    auto kfull = [&](int st) { return bar(st); };
+    auto vfull = [&](int st) { return bar(2 + st); };
+    auto sfull = [&](int b) { return bar(4 + b); };
+    auto vfree = [&](int st) { return bar(6 + st); };
+    auto pfull = [&](int b) { return bar(8 + b); };
+    const uint32_t qfull = bar(10), mma_drain = bar(11);
     auto kbase = [&](int st) { return sbase + st * L::kStageBytes; };
     // operand descriptors of stage 0 and of the query tile; other stages and
     // k-steps add their byte offset / 16 to the start-address field
@@ -131,18 +150,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const uint64_t desc_k0 = smem_desc_sw128(sbase, 16, 1024);
     const uint64_t desc_v0 = smem_desc_sw128(sbase + L::kKVBytes, L::kKVHalf, 1024);
 
-    const int tid = threadIdx.x, warp = tid >> 5;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int G = p.group, Hkv = p.num_kv_heads, H = p.num_heads;
     const int nseg = p.num_segments;
 
     if (tid == 0) {
         for (int st = 0; st < kTcStages; ++st) {
-            mbar_init(kbar(st), 1);
-            mbar_init(vbar(st), 1);
+            mbar_init(kfull(st), 1);
+            mbar_init(vfull(st), 1);
+            mbar_init(sfull(st), 1);
+            mbar_init(vfree(st), 1);
+            mbar_init(pfull(st), kRowWarps);
         }
-        mbar_init(sbar(0), 1);
-        mbar_init(sbar(1), 1);
-        mbar_init(bar_o, 1);
+        mbar_init(qfull, kRowWarps);
+        mbar_init(mma_drain, 1);
+        *abort_flag = 0;
         fence_barrier_init();
         prefetch_tensormap(&tmap_k);
         prefetch_tensormap(&tmap_v);
@@ -160,11 +182,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + L::kTmemSlot);
-    const uint32_t lane_base = (uint32_t)(32 * warp) << 16;  // this warp's TMEM lanes
 
     // ---- work units per segment and their prefix sums -------------------------------
     if (warp == 0) {
-        const int lane = tid & 31;
         int carry = 0;
         for (int base = 0; base < nseg; base += 32) {
             const int sg = base + lane;
@@ -186,16 +206,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     __syncthreads();
     const int total_units = pref[nseg] * Hkv;
 
-    // mbarrier parities (K fills are waited for by thread 0 alone)
-    uint32_t ph_k = 0, ph_v = 0, ph_s = 0, ph_o = 0;
-    uint32_t pend_k = 0, pend_v = 0;  // thread 0: stages with a fill not yet waited for
-    uint32_t pend_mma = 0;            // bit b: S buffer b committed, bit 2: value product
-    bool aborted = false;
-
-    for (int u = blockIdx.x; u < total_units && !aborted; u += gridDim.x) {
-        // ---- unit -> (segment, KV head, row tile, prefix partition) ---------------------
+    // ---- unit -> (segment, KV head, row tile, prefix partition, key range) -------------
+    // Every role walks the same units in the same order and counts the same
+    // 64-token tiles, so a tile's global index g (across this CTA's units)
+    // names its ring stage g % 2, its S buffer g % 2 and the phase g / 2 of
+    // every barrier of that stage.
+    struct Unit {
+        int seg, kh, rt, part, count, nrows, kbeg, kend, n;
+        const int32_t *table;
+    };
+    auto decode = [&](int u, Unit &w) {
         const int q = u / Hkv;
-        const int kh = u - q * Hkv;
+        w.kh = u - q * Hkv;
         int lo = 0, hi = nseg - 1;
         while (lo < hi) {
             const int mid = (lo + hi + 1) >> 1;
@@ -204,287 +226,345 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             else
                 hi = mid - 1;
         }
-        const int seg = lo;
-        const int count = mq_segment_count(p, seg);
-        const int tiles = (count * G + kTcRows - 1) / kTcRows;
-        const int idx = q - pref[seg];
-        const int rt = idx % tiles;     // row tile
-        const int part = idx / tiles;   // prefix partition (0 for prefill)
-        const int nrows = min(kTcRows, count * G - rt * kTcRows);
-
-        int table_seq, kbeg, kend;
+        w.seg = lo;
+        w.count = mq_segment_count(p, w.seg);
+        const int tiles = (w.count * G + kTcRows - 1) / kTcRows;
+        const int idx = q - pref[w.seg];
+        w.rt = idx % tiles;    // row tile
+        w.part = idx / tiles;  // prefix partition (0 for prefill)
+        w.nrows = min(kTcRows, w.count * G - w.rt * kTcRows);
+        int table_seq;
         if (p.prefix_mode) {
-            // a bad leader id is flagged by the plan check below
-            table_seq = min(max(p.group_members[p.group_start[seg]], 0), p.num_seqs - 1);
-            kbeg = part * p.part_tokens;
-            kend = min(mq_group_prefix(p, seg), kbeg + p.part_tokens);
+            // a bad leader id is flagged by the plan check of the row warps
+            table_seq = min(max(p.group_members[p.group_start[w.seg]], 0), p.num_seqs - 1);
+            w.kbeg = w.part * p.part_tokens;
+            w.kend = min(mq_group_prefix(p, w.seg), w.kbeg + p.part_tokens);
         } else {
-            table_seq = seg;
-            const int ctx = clamp_context_mq(p, seg);
-            const int last = (rt * kTcRows + nrows - 1) / G;  // chunk row of the last row
-            kbeg = 0;
-            kend = max(0, ctx - count + last + 1);
+            table_seq = w.seg;
+            const int ctx = clamp_context_mq(p, w.seg);
+            const int last = (w.rt * kTcRows + w.nrows - 1) / G;  // chunk row of the last row
+            w.kbeg = 0;
+            w.kend = max(0, ctx - w.count + last + 1);
         }
-        const int32_t *table = p.block_tables + (size_t)table_seq * p.max_blocks_per_seq;
-        const int nstages = kend > kbeg ? (kend - kbeg + kTcTokens - 1) / kTcTokens : 0;
+        w.table = p.block_tables + (size_t)table_seq * p.max_blocks_per_seq;
+        w.n = w.kend > w.kbeg ? (w.kend - w.kbeg + kTcTokens - 1) / kTcTokens : 0;
+    };
+    // a bounded wait, warp-uniform; the first one to run out stops every role
+    auto wait = [&](uint32_t b, uint32_t parity) -> bool {
+        bool ok = *abort_flag == 0 && mbar_wait_bounded(b, parity, kWaitLimitNs);
+        ok = __all_sync(kFull, ok);
+        if (!ok)
+            *abort_flag = 1;
+        return ok;
+    };
 
-        tc_fence_before();
-        __syncthreads();  // the previous unit is done with the stages, Q tile and TMEM
-        tc_fence_after();
-
-        // prefix pass, first KV head and partition: check the plan for this
-        // tile's members -- the prefix is on the tile grid and within every
-        // member's context, each member records it as its start, and each
-        // member's table names the leader's blocks for the whole prefix
-        if (p.prefix_mode && kh == 0 && part == 0 && tid < nrows &&
-            (rt * kTcRows + tid) % G == 0) {
-            const int s = p.group_members[p.group_start[seg] + (rt * kTcRows + tid) / G];
-            const int Lg = p.group_prefix[seg];
-            const int leader = p.group_members[p.group_start[seg]];
-            bool bad = s < 0 || s >= p.num_seqs || Lg <= 0 || (Lg & (kTileTokens - 1)) != 0 ||
-                       Lg > p.max_blocks_per_seq * p.block_size || leader < 0 ||
-                       leader >= p.num_seqs;
-            if (!bad) {
-                const int c = p.context_lens[s];
-                bad = c < Lg || c > p.max_context_len || p.seq_start[s] != Lg;
-                const int32_t *mine = p.block_tables + (size_t)s * p.max_blocks_per_seq;
-                for (int b = 0; !bad && b < (Lg >> p.block_shift); ++b)
-                    bad = __ldg(mine + b) != __ldg(table + b);
-            }
-            if (bad)
-                flag_error(p.error_word, PA_DEVERR_PREFIX_PLAN);
-        }
-
-        // warp 0 fetches: lane j < 2 * kTcSubs (j < kTcSubs for d = 64) owns
-        // the 16-token sub-tile j / halves and d-half j % halves of every tile,
-        // looks up its physical block one tile ahead of its use and issues its
-        // own 2 KB box, so the boxes of a K or V tile go out in one warp step.
-        // K is refilled as soon as S = Q K^T of the tile two back has
-        // finished, V once the value product of the tile two back has.
-        const int lane = tid & 31;
-        const int my_sb = lane / L::kHalves, my_hf = lane % L::kHalves;
-        auto lookup = [&](int si) {
-            const int tok = kbeg + si * kTcTokens + my_sb * kTileTokens;
-            return (my_sb < kTcSubs && tok < kend) ? __ldg(table + (tok >> p.block_shift)) : 0;
-        };
-        auto checked = [&](int ent) {
-            if (ent < 0 || ent >= p.num_blocks) {
-                flag_error(p.error_word, PA_DEVERR_BLOCK_RANGE);
-                ent = 0;  // stays inside the pool; the row's output is undefined
-            }
-            return ent;
-        };
-        auto issue = [&](int si, bool values, int ent) {  // warp 0, all lanes
-            const int st = si % kTcStages;
-            const int t0 = kbeg + si * kTcTokens;
-            const int nsub = min(kTcSubs, (kend - t0 + kTileTokens - 1) / kTileTokens);
-            const uint32_t bar = values ? vbar(st) : kbar(st);
-            if (lane == 0)
-                mbar_arrive_expect_tx(bar, (uint32_t)(nsub * L::kHalves * 2048));
-            __syncwarp();
-            if (my_sb < nsub) {
-                const int row = (t0 + my_sb * kTileTokens) & (p.block_size - 1);
-                tma_load_4d(kbase(st) + (values ? L::kKVBytes : 0) + my_hf * L::kKVHalf +
-                                my_sb * 2048,
-                            values ? &tmap_v : &tmap_k, bar, my_hf * 64, kh, row, ent);
-            }
-            if (values)
-                pend_v |= 1u << st;
-            else
-                pend_k |= 1u << st;
-        };
-        int ent_cur = 0, ent_next = 0;  // warp 0: this lane's entry of tiles si + 1, si + 2
-        if (warp == 0) {
-            for (int si = 0; si < min(kTcStages, nstages); ++si) {
-                ent_cur = checked(lookup(si));
-                issue(si, false, ent_cur);
-                issue(si, true, ent_cur);
-            }
-        }
-
-        // ---- this thread's row: query row, output location, key limit ------------------
-        long long qoff = -1, ooff = -1;
-        int lim = 0;
-        if (tid < nrows) {
-            const int r = rt * kTcRows + tid;
-            const int i = r / G, hg = r - (r / G) * G;
-            const int h = kh * G + hg;
-            if (p.prefix_mode) {
-                int s = p.group_members[p.group_start[seg] + i];
-                s = min(max(s, 0), p.num_seqs - 1);  // a bad member id is flagged above
-                qoff = ((long long)s * H + h) * D;
-                ooff = ((long long)s * H + h) * p.max_parts + part;
-                lim = kend;
-            } else {
-                const long long row = (long long)p.query_start[seg] + i;
-                qoff = (row * H + h) * D;
-                ooff = qoff;
-                const int last = (rt * kTcRows + nrows - 1) / G;
-                lim = max(0, kend - (last - i));
-            }
-        }
-        // query row -> shared memory (K-major, 128-byte swizzle; zeros past the tile)
-        {
-            const uint4 *src = reinterpret_cast<const uint4 *>(static_cast<const T *>(p.query) +
-                                                               (qoff < 0 ? 0 : qoff));
-#pragma unroll
-            for (int c = 0; c < D / 8; ++c) {
-                const uint4 v = qoff >= 0 ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
-                const uint32_t a = qbase + (c >> 3) * L::kQHalf + tid * 128 +
-                                   (((c & 7) ^ (tid & 7)) << 4);
-                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(v.x),
-                             "r"(v.y), "r"(v.z), "r"(v.w)
-                             : "memory");
-            }
-        }
-        fence_proxy_async_smem();
-
-        float m_ref = -INFINITY, l_run = 0.f;
+    if (warp < kRowWarps) {
+        // ===== row warps: query rows in, online softmax, P out, epilogue ===============
+        const uint32_t lane_base = (uint32_t)(32 * warp) << 16;  // this warp's TMEM lanes
+        uint32_t g = 0;
         bool ok = true;
-        // S = Q K^T of tile `si` into S buffer si % 2 (fp32, 64 columns);
-        // warp 0 (one elected lane issues), once the keys have landed
-        auto issue_s = [&](int si) {
-            const int st = si % kTcStages, b = si & 1;
-            ok = mbar_wait_bounded(kbar(st), (ph_k >> st) & 1u, kWaitLimitNs) && ok;
-            ph_k ^= 1u << st;
-            pend_k &= ~(1u << st);
-            tc_fence_after();
-            const uint64_t dk = desc_k0 + (uint64_t)((st * L::kStageBytes) >> 4);
-            if (elect_one()) {
-#pragma unroll
-                for (int kk = 0; kk < KT; ++kk) {
-                    const uint32_t qo = ((kk >> 2) * L::kQHalf + (kk & 3) * 32) >> 4;
-                    const uint32_t ko = ((kk >> 2) * L::kKVHalf + (kk & 3) * 32) >> 4;
-                    tc_mma_ss(tmem + b * kTcTokens, desc_q0 + qo, dk + ko, kIdescS,
-                              kk > 0 ? 1u : 0u);
+        for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x) {
+            Unit w;
+            decode(u, w);
+            // prefix pass, first KV head and partition: check the plan for this
+            // tile's members -- the prefix is on the tile grid and within every
+            // member's context, each member records it as its start, and each
+            // member's table names the leader's blocks for the whole prefix
+            if (p.prefix_mode && w.kh == 0 && w.part == 0 && tid < w.nrows &&
+                (w.rt * kTcRows + tid) % G == 0) {
+                const int s = p.group_members[p.group_start[w.seg] + (w.rt * kTcRows + tid) / G];
+                const int Lg = p.group_prefix[w.seg];
+                const int leader = p.group_members[p.group_start[w.seg]];
+                bool bad = s < 0 || s >= p.num_seqs || Lg <= 0 ||
+                           (Lg & (kTileTokens - 1)) != 0 ||
+                           Lg > p.max_blocks_per_seq * p.block_size || leader < 0 ||
+                           leader >= p.num_seqs;
+                if (!bad) {
+                    const int c = p.context_lens[s];
+                    bad = c < Lg || c > p.max_context_len || p.seq_start[s] != Lg;
+                    const int32_t *mine = p.block_tables + (size_t)s * p.max_blocks_per_seq;
+                    for (int bk = 0; !bad && bk < (Lg >> p.block_shift); ++bk)
+                        bad = __ldg(mine + bk) != __ldg(w.table + bk);
                 }
-                tc_commit(sbar(b));
+                if (bad)
+                    flag_error(p.error_word, PA_DEVERR_PREFIX_PLAN);
             }
-            __syncwarp();
-        };
-        if (nstages > 0) {
-            __syncthreads();  // the query tile is in shared memory
-            if (warp == 0)
-                issue_s(0);
-            pend_mma |= 1u;
-        }
 
-        for (int si = 0; si < nstages; ++si) {
-            const int st = si % kTcStages, b = si & 1;
-            const int t0 = kbeg + si * kTcTokens;
-            // warp 0: table entries of tile si + 2 (used after the softmax below)
-            if (warp == 0 && si + kTcStages < nstages)
-                ent_next = lookup(si + kTcStages);
-            // 1. S of this tile
-            ok = mbar_wait_bounded(sbar(b), (ph_s >> b) & 1u, kWaitLimitNs) && ok;
-            ph_s ^= 1u << b;
-            pend_mma &= ~(1u << b);
-            tc_fence_after();
+            // this thread's row: query row, output location, key limit
+            long long qoff = -1, ooff = -1;
+            int lim = 0;
+            if (tid < w.nrows) {
+                const int r = w.rt * kTcRows + tid;
+                const int i = r / G, hg = r - (r / G) * G;
+                const int h = w.kh * G + hg;
+                if (p.prefix_mode) {
+                    int sq = p.group_members[p.group_start[w.seg] + i];
+                    sq = min(max(sq, 0), p.num_seqs - 1);  // a bad member id is flagged above
+                    qoff = ((long long)sq * H + h) * D;
+                    ooff = ((long long)sq * H + h) * p.max_parts + w.part;
+                    lim = w.kend;
+                } else {
+                    const long long row = (long long)p.query_start[w.seg] + i;
+                    qoff = (row * H + h) * D;
+                    ooff = qoff;
+                    const int last = (w.rt * kTcRows + w.nrows - 1) / G;
+                    lim = max(0, w.kend - (last - i));
+                }
+            }
 
-            // 2. softmax of this thread's row: raw scores (q . k); the scale is
-            //    applied inside the exponent
-            float sv[kTcTokens];
+            float m_ref = -INFINITY, l_run = 0.f;
+            if (w.n > 0) {
+                // query row -> shared memory (K-major, 128-byte swizzle; zeros
+                // past the tile).  The previous unit's tensor-core work has
+                // finished (its last value product was waited for below).
+                const uint4 *src = reinterpret_cast<const uint4 *>(
+                    static_cast<const T *>(p.query) + (qoff < 0 ? 0 : qoff));
 #pragma unroll
-            for (int c = 0; c < kTcTokens / 32; ++c) {
-                uint32_t r[32];
-                tmem_ld_32x32b_x32(tmem + lane_base + b * kTcTokens + c * 32, r);
-#pragma unroll
-                for (int i = 0; i < 32; ++i)
-                    sv[c * 32 + i] = __uint_as_float(r[i]);
-            }
-            if (lim < t0 + kTcTokens) {  // causal / range mask (diagonal and last tiles)
-#pragma unroll
-                for (int i = 0; i < kTcTokens; ++i)
-                    sv[i] = t0 + i < lim ? sv[i] : -INFINITY;
-            }
-            // maximum raw score (the scale is positive), as a tree
-            float e8[8];
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                float x = sv[k];
-#pragma unroll
-                for (int i = k + 8; i < kTcTokens; i += 8)
-                    x = fmaxf(x, sv[i]);
-                e8[k] = x;
-            }
-#pragma unroll
-            for (int w = 4; w > 0; w >>= 1)
-#pragma unroll
-                for (int k = 0; k < w; ++k)
-                    e8[k] = fmaxf(e8[k], e8[k + w]);
-            const float mx = e8[0] * p.scale_log2;  // -inf for a fully masked row
-            // the reference maximum moves only when a score passes it by 2^kSlack
-            const bool moved = mx > m_ref + kSlack;
-            float alpha = 1.f;
-            if (moved) {
-                alpha = exp2f(m_ref - mx);  // 0 while m_ref is -inf
-                m_ref = mx;
-                l_run *= alpha;
-            }
-            const float neg_mu = m_ref == -INFINITY ? 0.f : -m_ref;
-            uint32_t pw[kTcTokens / 2];
-            float ls[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int i = 0; i < kTcTokens / 2; ++i) {
-                const float p0 = exp2f(fmaf(sv[2 * i], p.scale_log2, neg_mu));
-                const float p1 = exp2f(fmaf(sv[2 * i + 1], p.scale_log2, neg_mu));
-                ls[i & 3] += p0 + p1;
-                pw[i] = MmaOp<T>::pack(p0, p1);
-            }
-            l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+                for (int c = 0; c < D / 8; ++c) {
+                    const uint4 v = qoff >= 0 ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
+                    const uint32_t a = qbase + (c >> 3) * L::kQHalf + tid * 128 +
+                                       (((c & 7) ^ (tid & 7)) << 4);
+                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a),
+                                 "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                                 : "memory");
+                }
+                fence_proxy_async_smem();
+                tc_fence_before();  // and the epilogue's loads of O are complete
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(qfull);
 
-            // 3. the previous tile's value product has finished: O is final
-            //    for it, its S buffer (the other one) and its value stage are
-            //    free
-            if (si > 0) {
-                ok = mbar_wait_bounded(bar_o, ph_o, kWaitLimitNs) && ok;
-                ph_o ^= 1u;
-                pend_mma &= ~4u;
-                tc_fence_after();
-                // 4. rescale O in TMEM when a row's reference maximum moved
-                if (__any_sync(kFull, moved)) {
+                for (int si = 0; si < w.n; ++si) {
+                    const uint32_t gg = g + si, b = gg & 1;
+                    const int t0 = w.kbeg + si * kTcTokens;
+                    // 1. S of this tile
+                    ok = wait(sfull(b), (gg >> 1) & 1);
+                    if (!ok)
+                        break;
+                    tc_fence_after();
+
+                    // 2. softmax of this thread's row: raw scores (q . k); the
+                    //    scale is applied inside the exponent
+                    float sv[kTcTokens];
 #pragma unroll
-                    for (int c = 0; c < D / 32; ++c) {
+                    for (int c = 0; c < kTcTokens / 32; ++c) {
                         uint32_t r[32];
-                        tmem_ld_32x32b_x32(tmem + lane_base + kTmemO + c * 32, r);
+                        tmem_ld_32x32b_x32(tmem + lane_base + b * kTcTokens + c * 32, r);
 #pragma unroll
                         for (int i = 0; i < 32; ++i)
-                            r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-                        tmem_st_32x32b_x32(tmem + lane_base + kTmemO + c * 32, r);
+                            sv[c * 32 + i] = __uint_as_float(r[i]);
+                    }
+                    if (lim < t0 + kTcTokens) {  // causal / range mask (diagonal, last tiles)
+#pragma unroll
+                        for (int i = 0; i < kTcTokens; ++i)
+                            sv[i] = t0 + i < lim ? sv[i] : -INFINITY;
+                    }
+                    // maximum raw score (the scale is positive), as a tree
+                    float e8[8];
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        float x = sv[k];
+#pragma unroll
+                        for (int i = k + 8; i < kTcTokens; i += 8)
+                            x = fmaxf(x, sv[i]);
+                        e8[k] = x;
+                    }
+#pragma unroll
+                    for (int wd = 4; wd > 0; wd >>= 1)
+#pragma unroll
+                        for (int k = 0; k < wd; ++k)
+                            e8[k] = fmaxf(e8[k], e8[k + wd]);
+                    const float mx = e8[0] * p.scale_log2;  // -inf for a fully masked row
+                    // the reference maximum moves only when a score passes it by 2^kSlack
+                    const bool moved = mx > m_ref + kSlack;
+                    float alpha = 1.f;
+                    if (moved) {
+                        alpha = exp2f(m_ref - mx);  // 0 while m_ref is -inf
+                        m_ref = mx;
+                        l_run *= alpha;
+                    }
+                    const float neg_mu = m_ref == -INFINITY ? 0.f : -m_ref;
+                    uint32_t pw[kTcTokens / 2];
+                    float ls[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                    for (int i = 0; i < kTcTokens / 2; ++i) {
+                        const float p0 = exp2f(fmaf(sv[2 * i], p.scale_log2, neg_mu));
+                        const float p1 = exp2f(fmaf(sv[2 * i + 1], p.scale_log2, neg_mu));
+                        ls[i & 3] += p0 + p1;
+                        pw[i] = MmaOp<T>::pack(p0, p1);
+                    }
+                    l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+
+                    // 3. a row's reference maximum moved: rescale O in tensor
+                    //    memory once the previous tile's value product is done
+                    //    (the next one waits for this tile's P, below)
+                    if (si > 0 && __any_sync(kFull, moved)) {
+                        const uint32_t gp = gg - 1;
+                        ok = wait(vfree(gp & 1), (gp >> 1) & 1);
+                        if (!ok)
+                            break;
+                        tc_fence_after();
+#pragma unroll
+                        for (int c = 0; c < D / 32; ++c) {
+                            uint32_t r[32];
+                            tmem_ld_32x32b_x32(tmem + lane_base + kTmemO + c * 32, r);
+#pragma unroll
+                            for (int i = 0; i < 32; ++i)
+                                r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+                            tmem_st_32x32b_x32(tmem + lane_base + kTmemO + c * 32, r);
+                        }
+                    }
+                    // 4. P over this tile's S (A operand of the value product)
+                    tmem_st_32x32b_x32(tmem + lane_base + b * kTcTokens, pw);
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive(pfull(b));
+                }
+                // the unit's last value product
+                if (ok) {
+                    const uint32_t gl = g + w.n - 1;
+                    ok = wait(vfree(gl & 1), (gl >> 1) & 1);
+                    tc_fence_after();
+                }
+                if (!ok)
+                    break;
+            }
+
+            // epilogue: this thread's row of O / l (TMEM loads are warp-wide)
+            const float inv = (w.n > 0 && l_run > 0.f) ? 1.f / l_run : 0.f;
+            if (p.prefix_mode && ooff >= 0) {
+                p.part_m[ooff] = m_ref * kLn2;
+                p.part_l[ooff] = l_run;
+            }
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t r[32];
+                if (w.n > 0) {
+                    tmem_ld_32x32b_x32(tmem + lane_base + kTmemO + c * 32, r);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        r[i] = 0u;
+                }
+                if (ooff < 0)
+                    continue;
+                if (p.prefix_mode) {
+                    float4 *dst = reinterpret_cast<float4 *>(p.part_o + ooff * D) + c * 8;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        dst[i] = make_float4(__uint_as_float(r[4 * i]) * inv,
+                                             __uint_as_float(r[4 * i + 1]) * inv,
+                                             __uint_as_float(r[4 * i + 2]) * inv,
+                                             __uint_as_float(r[4 * i + 3]) * inv);
+                } else {
+                    uint4 *dst =
+                        reinterpret_cast<uint4 *>(static_cast<T *>(p.out) + ooff) + c * 4;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        uint4 v;
+                        v.x = MmaOp<T>::pack(__uint_as_float(r[8 * i]) * inv,
+                                             __uint_as_float(r[8 * i + 1]) * inv);
+                        v.y = MmaOp<T>::pack(__uint_as_float(r[8 * i + 2]) * inv,
+                                             __uint_as_float(r[8 * i + 3]) * inv);
+                        v.z = MmaOp<T>::pack(__uint_as_float(r[8 * i + 4]) * inv,
+                                             __uint_as_float(r[8 * i + 5]) * inv);
+                        v.w = MmaOp<T>::pack(__uint_as_float(r[8 * i + 6]) * inv,
+                                             __uint_as_float(r[8 * i + 7]) * inv);
+                        dst[i] = v;
                     }
                 }
             }
-            // warp 0: S of the next tile into the other buffer (thread 0), so
-            // the tensor core computes it while this tile's P is stored and its
-            // value product waits for the block; refills: K of tile si + 2
-            // into this stage (S of this tile is done), V of tile si + 1 into
-            // the other stage (the value product of tile si - 1 is done)
-            if (warp == 0) {
-                if (si + 1 < nstages)
-                    issue_s(si + 1);
-                if (si + kTcStages < nstages) {
-                    ent_next = checked(ent_next);
-                    issue(si + kTcStages, false, ent_next);
+            g += w.n;
+        }
+    } else if (warp == kFetchWarp) {
+        // ===== fetch warp: table lookups and K/V boxes into the 2-stage ring ===========
+        // Lane j < 2 * kTcSubs (j < kTcSubs for d = 64) owns the 16-token
+        // sub-tile j / halves and d-half j % halves of every tile: it looks up
+        // that sub-tile's physical block one tile ahead of its use and issues
+        // its own 2 KB box.  K of tile g goes out once S of tile g - 2 is done,
+        // V of tile g once the value product of tile g - 2 is.
+        const int my_sb = lane / L::kHalves, my_hf = lane % L::kHalves;
+        uint32_t g = 0;
+        int last_k0 = -1, last_k1 = -1, last_v0 = -1, last_v1 = -1;  // last fill per stage
+        bool ok = true;
+        for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x) {
+            Unit w;
+            decode(u, w);
+            auto lookup = [&](int si) {
+                const int tok = w.kbeg + si * kTcTokens + my_sb * kTileTokens;
+                int e = (my_sb < kTcSubs && tok < w.kend)
+                            ? __ldg(w.table + (tok >> p.block_shift))
+                            : 0;
+                return e;
+            };
+            auto checked = [&](int e) {
+                if (e < 0 || e >= p.num_blocks) {
+                    flag_error(p.error_word, PA_DEVERR_BLOCK_RANGE);
+                    e = 0;  // stays inside the pool; the row's output is undefined
                 }
-                if (si >= 1 && si + 1 < nstages)
-                    issue(si + 1, true, ent_cur);
-                ent_cur = ent_next;
+                return e;
+            };
+            auto issue = [&](int si, uint32_t st, bool values, int ent) {
+                const int t0 = w.kbeg + si * kTcTokens;
+                const int nsub = min(kTcSubs, (w.kend - t0 + kTileTokens - 1) / kTileTokens);
+                const uint32_t fb = values ? vfull(st) : kfull(st);
+                if (lane == 0)
+                    mbar_arrive_expect_tx(fb, (uint32_t)(nsub * L::kHalves * 2048));
+                __syncwarp();
+                if (my_sb < nsub) {
+                    const int row = (t0 + my_sb * kTileTokens) & (p.block_size - 1);
+                    tma_load_4d(kbase(st) + (values ? L::kKVBytes : 0) + my_hf * L::kKVHalf +
+                                    my_sb * 2048,
+                                values ? &tmap_v : &tmap_k, fb, my_hf * 64, w.kh, row, ent);
+                }
+            };
+            int ent_next = w.n > 0 ? lookup(0) : 0;
+            for (int si = 0; si < w.n; ++si) {
+                const uint32_t gg = g + si, st = gg & 1;
+                const int ent = checked(ent_next);
+                if (si + 1 < w.n)
+                    ent_next = lookup(si + 1);
+                if (gg >= kTcStages) {
+                    ok = wait(sfull(st), ((gg - 2) >> 1) & 1);  // S of tile gg - 2: K free
+                    if (!ok)
+                        break;
+                }
+                issue(si, st, false, ent);
+                (st ? last_k1 : last_k0) = (int)gg;
+                if (gg >= kTcStages) {
+                    ok = wait(vfree(st), ((gg - 2) >> 1) & 1);  // its value product: V free
+                    if (!ok)
+                        break;
+                }
+                issue(si, st, true, ent);
+                (st ? last_v1 : last_v0) = (int)gg;
             }
-            if (si + 1 < nstages)
-                pend_mma |= 1u << ((si + 1) & 1);
-            // 5. P over this tile's S (A operand of the value product)
-            tmem_st_32x32b_x32(tmem + lane_base + b * kTcTokens, pw);
-
-            // 6. values of this tile; rows past the key range -> zero (never
-            //    fetched, or past the context)
-            ok = mbar_wait_bounded(vbar(st), (ph_v >> st) & 1u, kWaitLimitNs) && ok;
-            ph_v ^= 1u << st;
-            if (tid == 0)
-                pend_v &= ~(1u << st);
-            const int nvalid = kend - t0;
+            g += w.n;
+        }
+        // fills still landing (only after an abort: the MMA warp waited the rest)
+        if (last_k0 >= 0)
+            mbar_wait_bounded(kfull(0), (last_k0 >> 1) & 1, kWaitLimitNs);
+        if (last_k1 >= 0)
+            mbar_wait_bounded(kfull(1), (last_k1 >> 1) & 1, kWaitLimitNs);
+        if (last_v0 >= 0)
+            mbar_wait_bounded(vfull(0), (last_v0 >> 1) & 1, kWaitLimitNs);
+        if (last_v1 >= 0)
+            mbar_wait_bounded(vfull(1), (last_v1 >> 1) & 1, kWaitLimitNs);
+    } else if (warp == kMmaWarp) {
+        // ===== tensor-core warp: S = Q K^T and O += P V, one elected lane issues ========
+        uint32_t g = 0, nq = 0;
+        bool ok = true;
+        // O += P V of tile gg (tile si of unit w): P stored, V landed; value rows
+        // past the key range are zeroed first (never fetched, or past the context)
+        auto issue_pv = [&](const Unit &w, int si, uint32_t gg) -> bool {
+            const uint32_t st = gg & 1;
+            if (!wait(pfull(st), (gg >> 1) & 1) || !wait(vfull(st), (gg >> 1) & 1))
+                return false;
+            const int nvalid = w.kend - (w.kbeg + si * kTcTokens);
             if (nvalid < kTcTokens) {
                 const int rows = kTcTokens - nvalid;
-                for (int c = tid; c < L::kHalves * rows * 8; c += kTcThreads) {
+                for (int c = lane; c < L::kHalves * rows * 8; c += 32) {
                     const int hf = c / (rows * 8), rem = c - hf * rows * 8;
                     const uint32_t a = kbase(st) + L::kKVBytes + hf * L::kKVHalf +
                                        (nvalid + rem / 8) * 128 + (rem % 8) * 16;
@@ -492,109 +572,73 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                                  : "memory");
                 }
                 fence_proxy_async_smem();
-            }
-            tc_fence_before();
-            if (__syncthreads_or(!ok)) {
-                aborted = true;
-                break;
-            }
-
-            // 7. thread 0: O += P V of this tile (queued behind S of the next
-            //    tile, so the next softmax can start while it runs)
-            if (warp == 0) {
-                tc_fence_after();
-                const uint64_t dv = desc_v0 + (uint64_t)((st * L::kStageBytes) >> 4);
-                if (elect_one()) {
-#pragma unroll
-                    for (int ks = 0; ks < kTcTokens / 16; ++ks)
-                        tc_mma_ts(tmem + kTmemO, tmem + b * kTcTokens + ks * 8,
-                                  dv + (uint64_t)((ks * 2048) >> 4), kIdescO,
-                                  (si > 0 || ks > 0) ? 1u : 0u);
-                    tc_commit(bar_o);
-                }
                 __syncwarp();
             }
-            pend_mma |= 4u;
-        }
-        if (aborted)
-            break;
-        // the last value product
-        if (nstages > 0) {
-            ok = mbar_wait_bounded(bar_o, ph_o, kWaitLimitNs) && ok;
-            ph_o ^= 1u;
-            pend_mma &= ~4u;
             tc_fence_after();
-            if (__syncthreads_or(!ok)) {
-                aborted = true;
-                break;
-            }
-        }
-
-        // ---- epilogue: this thread's row of O / l (TMEM loads are warp-wide) -----------
-        const float inv = (nstages > 0 && l_run > 0.f) ? 1.f / l_run : 0.f;
-        if (p.prefix_mode && ooff >= 0) {
-            p.part_m[ooff] = m_ref * kLn2;
-            p.part_l[ooff] = l_run;
-        }
+            const uint64_t dv = desc_v0 + (uint64_t)((st * L::kStageBytes) >> 4);
+            if (elect_one()) {
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-            uint32_t r[32];
-            if (nstages > 0) {
-                tmem_ld_32x32b_x32(tmem + lane_base + kTmemO + c * 32, r);
-            } else {
-#pragma unroll
-                for (int i = 0; i < 32; ++i)
-                    r[i] = 0u;
+                for (int ks = 0; ks < kTcTokens / 16; ++ks)
+                    tc_mma_ts(tmem + kTmemO, tmem + st * kTcTokens + ks * 8,
+                              dv + (uint64_t)((ks * 2048) >> 4), kIdescO,
+                              (si > 0 || ks > 0) ? 1u : 0u);
+                tc_commit(vfree(st));
             }
-            if (ooff < 0)
+            __syncwarp();
+            return true;
+        };
+        for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x) {
+            Unit w;
+            decode(u, w);
+            if (w.n == 0)
                 continue;
-            if (p.prefix_mode) {
-                float4 *dst = reinterpret_cast<float4 *>(p.part_o + ooff * D) + c * 8;
+            ok = wait(qfull, nq & 1);  // this unit's queries; O read out by the last unit
+            ++nq;
+            if (!ok)
+                break;
+            tc_fence_after();
+            for (int si = 0; si < w.n && ok; ++si) {
+                const uint32_t gg = g + si, st = gg & 1;
+                // S of tile gg into buffer st: its keys landed, and the value
+                // product of tile gg - 2 (the buffer's P) is done
+                ok = wait(kfull(st), (gg >> 1) & 1);
+                if (ok && gg >= kTcStages)
+                    ok = wait(vfree(st), ((gg - 2) >> 1) & 1);
+                if (!ok)
+                    break;
+                tc_fence_after();
+                const uint64_t dk = desc_k0 + (uint64_t)((st * L::kStageBytes) >> 4);
+                if (elect_one()) {
 #pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    dst[i] = make_float4(__uint_as_float(r[4 * i]) * inv,
-                                         __uint_as_float(r[4 * i + 1]) * inv,
-                                         __uint_as_float(r[4 * i + 2]) * inv,
-                                         __uint_as_float(r[4 * i + 3]) * inv);
-            } else {
-                uint4 *dst = reinterpret_cast<uint4 *>(static_cast<T *>(p.out) + ooff) + c * 4;
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    uint4 w;
-                    w.x = MmaOp<T>::pack(__uint_as_float(r[8 * i]) * inv,
-                                         __uint_as_float(r[8 * i + 1]) * inv);
-                    w.y = MmaOp<T>::pack(__uint_as_float(r[8 * i + 2]) * inv,
-                                         __uint_as_float(r[8 * i + 3]) * inv);
-                    w.z = MmaOp<T>::pack(__uint_as_float(r[8 * i + 4]) * inv,
-                                         __uint_as_float(r[8 * i + 5]) * inv);
-                    w.w = MmaOp<T>::pack(__uint_as_float(r[8 * i + 6]) * inv,
-                                         __uint_as_float(r[8 * i + 7]) * inv);
-                    dst[i] = w;
+                    for (int kk = 0; kk < KT; ++kk) {
+                        const uint32_t qo = ((kk >> 2) * L::kQHalf + (kk & 3) * 32) >> 4;
+                        const uint32_t ko = ((kk >> 2) * L::kKVHalf + (kk & 3) * 32) >> 4;
+                        tc_mma_ss(tmem + st * kTcTokens, desc_q0 + qo, dk + ko, kIdescS,
+                                  kk > 0 ? 1u : 0u);
+                    }
+                    tc_commit(sfull(st));
                 }
+                __syncwarp();
+                // the previous tile's value product, queued behind this S
+                if (si > 0)
+                    ok = issue_pv(w, si - 1, gg - 1);
             }
+            if (ok)
+                ok = issue_pv(w, w.n - 1, g + w.n - 1);
+            g += w.n;
         }
+        // every tensor-core operation this warp issued has finished
+        if (elect_one())
+            tc_commit(mma_drain);
+        __syncwarp();
+        mbar_wait_bounded(mma_drain, 0, kWaitLimitNs);
     }
     pdl_launch_dependents();
 
-    // ---- drain (only after an abort): fills still landing -------------------------------
-    if (tid == 0) {
-        for (int st = 0; st < kTcStages; ++st) {
-            if (pend_k & (1u << st))
-                mbar_wait_bounded(kbar(st), (ph_k >> st) & 1u, kWaitLimitNs);
-            if (pend_v & (1u << st))
-                mbar_wait_bounded(vbar(st), (ph_v >> st) & 1u, kWaitLimitNs);
-        }
-        // tensor-core work still committed (only after an abort)
-        for (int b = 0; b < 2; ++b)
-            if (pend_mma & (1u << b))
-                mbar_wait_bounded(sbar(b), (ph_s >> b) & 1u, kWaitLimitNs);
-        if (pend_mma & 4u)
-            mbar_wait_bounded(bar_o, ph_o, kWaitLimitNs);
-    }
-    if (aborted && tid == 0)
-        flag_error(p.error_word, PA_DEVERR_TIMEOUT);
     tc_fence_before();
     __syncthreads();
+    if (tid == 0 && *abort_flag)
+        flag_error(p.error_word, PA_DEVERR_TIMEOUT);
     if (warp == 0) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
