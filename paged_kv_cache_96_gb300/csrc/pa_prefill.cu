@@ -53,9 +53,10 @@ namespace pa {
 
 constexpr int kTcRows = 128;     // query rows per CTA (M of the MMAs)
 constexpr int kRowWarps = 4;     // warps 0-3: one thread per row (softmax, epilogue)
-constexpr int kFetchWarp = 4;    // table lookups and K/V fetches
-constexpr int kMmaWarp = 5;      // tensor-core issue
-constexpr int kTcThreads = 32 * (kRowWarps + 2);
+constexpr int kKeyWarp = 4;      // table lookups and key fetches
+constexpr int kValueWarp = 5;    // table lookups and value fetches
+constexpr int kMmaWarp = 6;      // tensor-core issue
+constexpr int kTcThreads = 32 * (kRowWarps + 3);
 constexpr int kTcTokens = 64;    // key/value tokens per stage (N of S = Q K^T)
 constexpr int kTcSubs = kTcTokens / kTileTokens;
 constexpr int kTcStages = 2;
@@ -477,16 +478,17 @@ __global__ void __launch_bounds__(kTcThreads, 2)
             }
             g += w.n;
         }
-    } else if (warp == kFetchWarp) {
-        // ===== fetch warp: table lookups and K/V boxes into the 2-stage ring ===========
+    } else if (warp == kKeyWarp || warp == kValueWarp) {
+        // ===== fetch warps: keys (warp 4) and values (warp 5) into the 2-stage ring ====
         // Lane j < 2 * kTcSubs (j < kTcSubs for d = 64) owns the 16-token
         // sub-tile j / halves and d-half j % halves of every tile: it looks up
         // that sub-tile's physical block one tile ahead of its use and issues
         // its own 2 KB box.  K of tile g goes out once S of tile g - 2 is done,
         // V of tile g once the value product of tile g - 2 is.
+        const bool values = warp == kValueWarp;
         const int my_sb = lane / L::kHalves, my_hf = lane % L::kHalves;
         uint32_t g = 0;
-        int last_k0 = -1, last_k1 = -1, last_v0 = -1, last_v1 = -1;  // last fill per stage
+        int last0 = -1, last1 = -1;  // last fill per stage
         bool ok = true;
         for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x) {
             Unit w;
@@ -505,7 +507,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
                 }
                 return e;
             };
-            auto issue = [&](int si, uint32_t st, bool values, int ent) {
+            auto issue = [&](int si, uint32_t st, int ent) {
                 const int t0 = w.kbeg + si * kTcTokens;
                 const int nsub = min(kTcSubs, (w.kend - t0 + kTileTokens - 1) / kTileTokens);
                 const uint32_t fb = values ? vfull(st) : kfull(st);
@@ -525,32 +527,23 @@ __global__ void __launch_bounds__(kTcThreads, 2)
                 const int ent = checked(ent_next);
                 if (si + 1 < w.n)
                     ent_next = lookup(si + 1);
+                // the stage's tile gg - 2 is consumed: its S (keys), its
+                // value product (values)
                 if (gg >= kTcStages) {
-                    ok = wait(sfull(st), ((gg - 2) >> 1) & 1);  // S of tile gg - 2: K free
+                    ok = wait(values ? vfree(st) : sfull(st), ((gg - 2) >> 1) & 1);
                     if (!ok)
                         break;
                 }
-                issue(si, st, false, ent);
-                (st ? last_k1 : last_k0) = (int)gg;
-                if (gg >= kTcStages) {
-                    ok = wait(vfree(st), ((gg - 2) >> 1) & 1);  // its value product: V free
-                    if (!ok)
-                        break;
-                }
-                issue(si, st, true, ent);
-                (st ? last_v1 : last_v0) = (int)gg;
+                issue(si, st, ent);
+                (st ? last1 : last0) = (int)gg;
             }
             g += w.n;
         }
         // fills still landing (only after an abort: the MMA warp waited the rest)
-        if (last_k0 >= 0)
-            mbar_wait_bounded(kfull(0), (last_k0 >> 1) & 1, kWaitLimitNs);
-        if (last_k1 >= 0)
-            mbar_wait_bounded(kfull(1), (last_k1 >> 1) & 1, kWaitLimitNs);
-        if (last_v0 >= 0)
-            mbar_wait_bounded(vfull(0), (last_v0 >> 1) & 1, kWaitLimitNs);
-        if (last_v1 >= 0)
-            mbar_wait_bounded(vfull(1), (last_v1 >> 1) & 1, kWaitLimitNs);
+        if (last0 >= 0)
+            mbar_wait_bounded(values ? vfull(0) : kfull(0), (last0 >> 1) & 1, kWaitLimitNs);
+        if (last1 >= 0)
+            mbar_wait_bounded(values ? vfull(1) : kfull(1), (last1 >> 1) & 1, kWaitLimitNs);
     } else if (warp == kMmaWarp) {
         // ===== tensor-core warp: S = Q K^T and O += P V, one elected lane issues ========
         uint32_t g = 0, nq = 0;
