@@ -264,9 +264,12 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         const uint32_t lane_base = (uint32_t)(32 * warp) << 16;  // this warp's TMEM lanes
         uint32_t g = 0;
         bool ok = true;
-        for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x) {
-            Unit w;
-            decode(u, w);
+        // this thread's row of a unit: query row, output location, key limit
+        struct Row {
+            long long qoff, ooff;
+            int lim;
+        };
+        auto row_of = [&](const Unit &w, Row &r) {
             // prefix pass, first KV head and partition: check the plan for this
             // tile's members -- the prefix is on the tile grid and within every
             // member's context, each member records it as its start, and each
@@ -290,29 +293,48 @@ __global__ void __launch_bounds__(kTcThreads, 2)
                 if (bad)
                     flag_error(p.error_word, PA_DEVERR_PREFIX_PLAN);
             }
-
-            // this thread's row: query row, output location, key limit
-            long long qoff = -1, ooff = -1;
-            int lim = 0;
+            r.qoff = -1;
+            r.ooff = -1;
+            r.lim = 0;
             if (tid < w.nrows) {
-                const int r = w.rt * kTcRows + tid;
-                const int i = r / G, hg = r - (r / G) * G;
+                const int rr = w.rt * kTcRows + tid;
+                const int i = rr / G, hg = rr - (rr / G) * G;
                 const int h = w.kh * G + hg;
                 if (p.prefix_mode) {
                     int sq = p.group_members[p.group_start[w.seg] + i];
                     sq = min(max(sq, 0), p.num_seqs - 1);  // a bad member id is flagged above
-                    qoff = ((long long)sq * H + h) * D;
-                    ooff = ((long long)sq * H + h) * p.max_parts + w.part;
-                    lim = w.kend;
+                    r.qoff = ((long long)sq * H + h) * D;
+                    r.ooff = ((long long)sq * H + h) * p.max_parts + w.part;
+                    r.lim = w.kend;
                 } else {
                     const long long row = (long long)p.query_start[w.seg] + i;
-                    qoff = (row * H + h) * D;
-                    ooff = qoff;
+                    r.qoff = (row * H + h) * D;
+                    r.ooff = r.qoff;
                     const int last = (w.rt * kTcRows + w.nrows - 1) / G;
-                    lim = max(0, w.kend - (last - i));
+                    r.lim = max(0, w.kend - (last - i));
                 }
             }
-
+        };
+        // the next unit's query row is pulled into L2 while the current unit's
+        // last value product runs and its output is written
+        auto prefetch_q = [&](const Unit &w, const Row &r) {
+            if (w.n > 0 && r.qoff >= 0) {
+                const char *src = reinterpret_cast<const char *>(static_cast<const T *>(p.query) +
+                                                                 r.qoff);
+#pragma unroll
+                for (int c = 0; c < D * (int)sizeof(T); c += 128)
+                    asm volatile("prefetch.global.L2 [%0];" ::"l"(src + c));
+            }
+        };
+        Unit w;
+        Row rw;
+        if ((int)blockIdx.x < total_units) {
+            decode(blockIdx.x, w);
+            row_of(w, rw);
+        }
+        for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x) {
+            const long long qoff = rw.qoff, ooff = rw.ooff;
+            const int lim = rw.lim;
             float m_ref = -INFINITY, l_run = 0.f;
             if (w.n > 0) {
                 // query row -> shared memory (K-major, 128-byte swizzle; zeros
@@ -422,12 +444,26 @@ __global__ void __launch_bounds__(kTcThreads, 2)
                     if (lane == 0)
                         mbar_arrive(pfull(b));
                 }
-                // the unit's last value product
-                if (ok) {
-                    const uint32_t gl = g + w.n - 1;
-                    ok = wait(vfree(gl & 1), (gl >> 1) & 1);
-                    tc_fence_after();
-                }
+                if (!ok)
+                    break;
+            }
+            // the next unit's rows and query row
+            Unit wn;
+            Row rn;
+            if (u + (int)gridDim.x < total_units) {
+                decode(u + gridDim.x, wn);
+                row_of(wn, rn);
+                prefetch_q(wn, rn);
+            } else {
+                wn.n = 0;
+                rn.qoff = rn.ooff = -1;
+                rn.lim = 0;
+            }
+            // this unit's last value product
+            if (w.n > 0) {
+                const uint32_t gl = g + w.n - 1;
+                ok = wait(vfree(gl & 1), (gl >> 1) & 1);
+                tc_fence_after();
                 if (!ok)
                     break;
             }
@@ -477,6 +513,8 @@ __global__ void __launch_bounds__(kTcThreads, 2)
                 }
             }
             g += w.n;
+            w = wn;
+            rw = rn;
         }
     } else if (warp == kKeyWarp || warp == kValueWarp) {
         // ===== fetch warps: keys (warp 4) and values (warp 5) into the 2-stage ring ====
