@@ -207,11 +207,21 @@ def to_float(t: torch.Tensor) -> np.ndarray:
 
 
 class HostStepIO:
-    """A decode step driven from host memory: every call copies the step's
-    inputs (query, new K/V, their sequence ids and positions, block tables,
-    context lengths, copy-on-write pairs) from pinned host buffers to the
-    device, runs the step, and copies the attention output back to a pinned
-    host buffer.  The K/V pools stay resident on the device."""
+    """Decode steps driven from host memory, as a serving loop runs them:
+    every step copies its inputs (query, new K/V, their sequence ids and
+    positions, block tables, context lengths, copy-on-write pairs) from a
+    pinned host staging buffer to the device in one transfer, runs the step,
+    and copies the attention output back to a pinned host buffer.
+
+    Uploads and read-backs each run on a stream of their own and are
+    double-buffered: step i's inputs go into staging slot i % 2 (the step's
+    input tensors become views into it, each at a 256-byte aligned offset, so
+    the kernels read them in place) while step i - 1 computes, and step i's
+    output is read back while step i + 1 computes.  A slot's inputs are
+    refilled only after the step that last read them has finished, and its
+    output is rewritten only after it has been read back.  The K/V pools stay
+    resident on the device.  Bracket a run of steps with begin() and finish()
+    so that the transfer streams are ordered inside it."""
 
     def __init__(self, st: DecodeStep):
         self.st = st
@@ -223,19 +233,85 @@ class HostStepIO:
             names.append("query_start")
         if st.plan is not None:
             names.append("plan")
-        self.pairs = []
+        layout, total = [], 0
         for n in names:
-            dev = getattr(st, n)
-            host = torch.empty(dev.shape, dtype=dev.dtype, pin_memory=True)
-            host.copy_(dev)
-            self.pairs.append((host, dev))
-        self.host_out = torch.empty(st.out.shape, dtype=st.out.dtype, pin_memory=True)
-        self.h2d_bytes = sum(h.numel() * h.element_size() for h, _ in self.pairs)
-        self.d2h_bytes = self.host_out.numel() * self.host_out.element_size()
+            t = getattr(st, n)
+            nbytes = t.numel() * t.element_size()
+            layout.append((n, total, nbytes, t.dtype, t.shape))
+            total += (nbytes + 255) & ~255
+        self.dev_bufs = [torch.empty(total, dtype=torch.uint8, device=st.device)
+                         for _ in range(2)]
+        self.host_bufs = [torch.empty(total, dtype=torch.uint8, pin_memory=True)
+                          for _ in range(2)]
+        self.views = [{}, {}]
+        for slot in range(2):
+            for n, off, nbytes, dtype, shape in layout:
+                t = getattr(st, n)
+                self.host_bufs[slot][off:off + nbytes].view(dtype).view(shape).copy_(t)
+                self.views[slot][n] = self.dev_bufs[slot][off:off + nbytes].view(dtype).view(shape)
+        self.outs = [st.out, torch.empty_like(st.out)]
+        self.host_outs = [torch.empty(st.out.shape, dtype=st.out.dtype, pin_memory=True)
+                          for _ in range(2)]
+        self.h2d_bytes = total
+        self.d2h_bytes = self.host_outs[0].numel() * self.host_outs[0].element_size()
+        self.up = torch.cuda.Stream(device=st.device)
+        self.down = torch.cuda.Stream(device=st.device)
+        self.in_ready = [torch.cuda.Event() for _ in range(2)]
+        self.step_done = [torch.cuda.Event() for _ in range(2)]
+        self.out_read = [torch.cuda.Event() for _ in range(2)]
+        self.used = [False, False]
+        self.i = 0
+
+    def begin(self, stream: torch.cuda.Stream) -> None:
+        """Order the transfer streams after everything queued so far on `stream`."""
+        self.up.wait_stream(stream)
+        self.down.wait_stream(stream)
+
+    def finish(self, stream: torch.cuda.Stream) -> None:
+        """Order `stream` after the last upload and read-back."""
+        stream.wait_stream(self.up)
+        stream.wait_stream(self.down)
 
     def step(self) -> torch.Tensor:
-        for host, dev in self.pairs:
-            dev.copy_(host, non_blocking=True)
+        slot = self.i % 2
+        main = torch.cuda.current_stream(self.st.device)
+        with torch.cuda.stream(self.up):
+            if self.used[slot]:
+                self.up.wait_event(self.step_done[slot])  # step i - 2 read these inputs
+            self.dev_bufs[slot].copy_(self.host_bufs[slot], non_blocking=True)
+            self.in_ready[slot].record(self.up)
+        main.wait_event(self.in_ready[slot])
+        if self.used[slot]:
+            main.wait_event(self.out_read[slot])  # step i - 2's output has been read back
+        for n, v in self.views[slot].items():
+            setattr(self.st, n, v)
+        self.st.out = self.outs[slot]
         out = self.st.run()
-        self.host_out.copy_(out, non_blocking=True)
-        return self.host_out
+        self.step_done[slot].record(main)
+        self.used[slot] = True
+        with torch.cuda.stream(self.down):
+            self.down.wait_event(self.step_done[slot])
+            self.host_outs[slot].copy_(out, non_blocking=True)
+            self.out_read[slot].record(self.down)
+        self.i += 1
+        return self.host_outs[slot]
+
+    def capture(self, steps: int) -> None:
+        """Record `steps` consecutive steps (transfers, kernels, read-backs,
+        and their overlap) as one CUDA graph; replay() then runs them with a
+        single launch from the host.  Run a few steps eagerly first, so every
+        kernel's launch attributes are set before capture."""
+        torch.cuda.synchronize(self.st.device)
+        self.used = [False, False]  # dependencies inside one replay only
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph):
+            main = torch.cuda.current_stream(self.st.device)
+            self.begin(main)
+            for _ in range(steps):
+                self.step()
+            self.finish(main)
+        self.graph_steps = steps
+
+    def replay(self) -> None:
+        """The captured steps; replays of one graph never overlap each other."""
+        self.graph.replay()
