@@ -307,13 +307,18 @@ PA_API size_t pa_cascade_workspace_bytes(int num_seqs, int num_heads, int num_kv
  * from HBM once for all of its members instead of once per member.
  *   1. prefix pass: for every group g and KV head, the decode queries of all
  *      members (times the G query heads) attend the prefix [0, L_g), read
- *      through the leader's table, with tensor-core tiles of 64 query rows;
- *      each (member, head) gets partial 0 = (m, l, o) in the workspace.
+ *      through the leader's table, with tcgen05 tensor-core tiles of 128
+ *      query rows; each (member, head) gets partials 0 .. ceil(L_g / P) - 1
+ *      = (m, l, o) in the workspace, one per prefix partition of P =
+ *      partition_size tokens.
  *   2. partition pass: every sequence attends its own tokens [L, ctx) (L = 0
  *      outside any group) in partitions of partition_size tokens (0: one).
  *   3. reduce: log-sum-exp merge of each grouped or split sequence's
  *      partials; ungrouped single-partition sequences are written by step 2.
- * All three are queued on `stream` by this call.  prefix_plan is the device
+ * All three are queued on `stream` by this call, the prefix pass first; the
+ * partition pass reads nothing the prefix pass writes, so it runs alongside
+ * it (its grid finishes only after the prefix pass's), and the reduce waits
+ * for both.  prefix_plan is the device
  * copy of a prefix plan (num_groups, num_members as planned); an
  * inconsistent plan (a table that differs from the leader's on the prefix,
  * a prefix not below a member's context or off the 16-token grid, a

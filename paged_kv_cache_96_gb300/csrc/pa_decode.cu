@@ -128,8 +128,12 @@ __global__ void __launch_bounds__(NW * 32, MINB)
     }
     // Launched as a programmatic dependent of the kernel before it on the
     // stream: every global read below comes after the predecessor's writes
-    // are visible.
-    pdl_wait_primary();
+    // are visible.  Alongside the shared-prefix pass (which starts this one
+    // only once everything before it has finished, and writes only partial
+    // slots this pass leaves alone) the wait moves to the end, so that this
+    // grid -- and the reduce after it -- finishes after that pass.
+    if (!p.concurrent)
+        pdl_wait_primary();
 
     // ---- context lengths and partition prefix sums -----------------------
     for (int s = tid; s < S; s += kThreads) {
@@ -614,6 +618,8 @@ __global__ void __launch_bounds__(NW * 32, MINB)
             mbar_wait_bounded(bar_of(k), (last / NST) & 1u, kWaitLimitNs);
         }
     }
+    if (p.concurrent)
+        pdl_wait_primary();  // the shared-prefix pass has finished
 }
 
 // ---- host side -------------------------------------------------------------------
@@ -725,12 +731,21 @@ static pa_status launch_decode(const DecodeParams &prm, const CUtensorMap &mk,
                                long long max_units, const PrefixPass *prefix = nullptr)
 {
     constexpr int kStages = sizeof(KV) == 1 ? kStagesPerWarpFp8 : kStagesPerWarp;
-    pa_status st = launch_pass<T, KV, D, NT, kStages>(prm, mk, mv, stream, max_units);
+    // prefix-aware decode: the shared-prefix pass (tensor cores) goes first
+    // and the partition pass (memory-bound) runs alongside it
+    DecodeParams pass = prm;
+    pass.concurrent = 0;
+    if (prefix != nullptr) {
+        const pa_status ps = launch_prefix_pass(*prefix->prm, prefix->dtype, prefix->key_cache,
+                                                prefix->value_cache, D, stream,
+                                                prefix->max_units);
+        if (ps != PA_OK)
+            return ps;
+        pass.concurrent = 1;
+    }
+    pa_status st = launch_pass<T, KV, D, NT, kStages>(pass, mk, mv, stream, max_units);
     if (st == PA_ERR_UNSUPPORTED)
-        st = launch_pass<T, KV, D, NT, kStagesManySeqs>(prm, mk, mv, stream, max_units);
-    if (st == PA_OK && prefix != nullptr)
-        st = launch_prefix_pass(*prefix->prm, prefix->dtype, prefix->key_cache,
-                                prefix->value_cache, D, stream, prefix->max_units);
+        st = launch_pass<T, KV, D, NT, kStagesManySeqs>(pass, mk, mv, stream, max_units);
     if (st != PA_OK || prm.max_parts <= 1)
         return st;
     return launch_reduce<T, D>(prm, stream);

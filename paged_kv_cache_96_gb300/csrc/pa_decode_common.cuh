@@ -39,6 +39,9 @@ struct DecodeParams {
     int max_parts;    // partitions per sequence the workspace holds
     float scale_log2; // scale * log2(e) (times the K scale for FP8 pools)
     float out_scale;  // applied to the attention output (the V scale for FP8 pools)
+    int concurrent;   // 1: the kernel before it on the stream (the shared-prefix
+                      // pass) writes nothing this pass reads -- run alongside it
+                      // and wait for it only before finishing
 };
 
 // Clamped context length (same rule in both kernels).

@@ -174,6 +174,11 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     // stream has finished -- including an earlier launch of this kernel, so
     // the tensor memory below is never contended by one.
     pdl_wait_primary();
+    // the shared-prefix pass lets the partition pass after it start at once
+    // (that pass reads nothing this one writes, and waits for this grid
+    // before it finishes)
+    if (p.prefix_mode)
+        pdl_launch_dependents();
     // tensor memory: one warp allocates, every thread reads the address
     if (warp == 0) {
         tmem_alloc(sbase + L::kTmemSlot, kTmemCols);
