@@ -274,12 +274,12 @@ __global__ void __launch_bounds__(kTcThreads, 2)
             long long qoff, ooff;
             int lim;
         };
-        auto row_of = [&](const Unit &w, Row &r) {
+        auto row_of = [&](const Unit &w, Row &r, bool check) {
             // prefix pass, first KV head and partition: check the plan for this
             // tile's members -- the prefix is on the tile grid and within every
             // member's context, each member records it as its start, and each
             // member's table names the leader's blocks for the whole prefix
-            if (p.prefix_mode && w.kh == 0 && w.part == 0 && tid < w.nrows &&
+            if (check && p.prefix_mode && w.kh == 0 && w.part == 0 && tid < w.nrows &&
                 (w.rt * kTcRows + tid) % G == 0) {
                 const int s = p.group_members[p.group_start[w.seg] + (w.rt * kTcRows + tid) / G];
                 const int Lg = p.group_prefix[w.seg];
@@ -331,37 +331,49 @@ __global__ void __launch_bounds__(kTcThreads, 2)
                     asm volatile("prefetch.global.L2 [%0];" ::"l"(src + c));
             }
         };
+        // a unit's query rows -> shared memory (K-major, 128-byte swizzle;
+        // zeros past the tile), announced to the MMA warp.  Called once every
+        // S of the unit before has finished (they read the query tile).
+        auto write_q = [&](const Unit &w, const Row &r) {
+            if (w.n <= 0)
+                return;
+            const uint4 *src = reinterpret_cast<const uint4 *>(static_cast<const T *>(p.query) +
+                                                               (r.qoff < 0 ? 0 : r.qoff));
+#pragma unroll
+            for (int c = 0; c < D / 8; ++c) {
+                const uint4 v = r.qoff >= 0 ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
+                const uint32_t a = qbase + (c >> 3) * L::kQHalf + tid * 128 +
+                                   (((c & 7) ^ (tid & 7)) << 4);
+                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(v.x),
+                             "r"(v.y), "r"(v.z), "r"(v.w)
+                             : "memory");
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(qfull);
+        };
         Unit w;
         Row rw;
         if ((int)blockIdx.x < total_units) {
             decode(blockIdx.x, w);
-            row_of(w, rw);
+            row_of(w, rw, true);
+            write_q(w, rw);
         }
         for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x) {
             const long long qoff = rw.qoff, ooff = rw.ooff;
             const int lim = rw.lim;
+            const bool has_next = u + (int)gridDim.x < total_units;
+            if (has_next) {
+                // the next unit's query rows, pulled into L2 while this unit runs
+                Unit wn;
+                Row rn;
+                decode(u + gridDim.x, wn);
+                row_of(wn, rn, false);
+                prefetch_q(wn, rn);
+            }
             float m_ref = -INFINITY, l_run = 0.f;
             if (w.n > 0) {
-                // query row -> shared memory (K-major, 128-byte swizzle; zeros
-                // past the tile).  The previous unit's tensor-core work has
-                // finished (its last value product was waited for below).
-                const uint4 *src = reinterpret_cast<const uint4 *>(
-                    static_cast<const T *>(p.query) + (qoff < 0 ? 0 : qoff));
-#pragma unroll
-                for (int c = 0; c < D / 8; ++c) {
-                    const uint4 v = qoff >= 0 ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
-                    const uint32_t a = qbase + (c >> 3) * L::kQHalf + tid * 128 +
-                                       (((c & 7) ^ (tid & 7)) << 4);
-                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a),
-                                 "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
-                                 : "memory");
-                }
-                fence_proxy_async_smem();
-                tc_fence_before();  // and the epilogue's loads of O are complete
-                __syncwarp();
-                if (lane == 0)
-                    mbar_arrive(qfull);
-
                 for (int si = 0; si < w.n; ++si) {
                     const uint32_t gg = g + si, b = gg & 1;
                     const int t0 = w.kbeg + si * kTcTokens;
@@ -452,13 +464,15 @@ __global__ void __launch_bounds__(kTcThreads, 2)
                 if (!ok)
                     break;
             }
-            // the next unit's rows and query row
+            // every S of this unit has finished: the next unit's query rows go
+            // into shared memory now, so its first S can run during this unit's
+            // last value product and epilogue
             Unit wn;
             Row rn;
-            if (u + (int)gridDim.x < total_units) {
+            if (has_next) {
                 decode(u + gridDim.x, wn);
-                row_of(wn, rn);
-                prefetch_q(wn, rn);
+                row_of(wn, rn, true);
+                write_q(wn, rn);
             } else {
                 wn.n = 0;
                 rn.qoff = rn.ooff = -1;
