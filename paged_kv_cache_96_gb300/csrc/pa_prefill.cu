@@ -256,7 +256,10 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         w.n = w.kend > w.kbeg ? (w.kend - w.kbeg + kTcTokens - 1) / kTcTokens : 0;
     };
     // a bounded wait, warp-uniform; the first one to run out stops every role
+    // (the abort flag is read only when the phase is not already complete)
     auto wait = [&](uint32_t b, uint32_t parity) -> bool {
+        if (__all_sync(kFull, mbar_try_wait(b, parity)))
+            return true;
         bool ok = *abort_flag == 0 && mbar_wait_bounded(b, parity, kWaitLimitNs);
         ok = __all_sync(kFull, ok);
         if (!ok)
@@ -634,7 +637,6 @@ __global__ void __launch_bounds__(kTcThreads, 2)
                               (si > 0 || ks > 0) ? 1u : 0u);
                 tc_commit(vfree(st));
             }
-            __syncwarp();
             return true;
         };
         for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x) {
@@ -668,7 +670,6 @@ __global__ void __launch_bounds__(kTcThreads, 2)
                     }
                     tc_commit(sfull(st));
                 }
-                __syncwarp();
                 // the previous tile's value product, queued behind this S
                 if (si > 0)
                     ok = issue_pv(w, si - 1, gg - 1);
