@@ -51,6 +51,45 @@
 
 namespace pa {
 
+// ---- fp32 helpers for the softmax ---------------------------------------------
+
+// Maximum of three (max.f32 with three sources; a NaN source is ignored as
+// in fmaxf).
+__device__ __forceinline__ float fmax3(float a, float b, float c)
+{
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
+// Two fp32 values in one 64-bit register, and packed fp32 FMA / add on them
+// (fma.rn.f32x2 / add.rn.f32x2: each lane rounds as its scalar form).
+__device__ __forceinline__ uint64_t pack_f32x2(float lo, float hi)
+{
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+
+__device__ __forceinline__ void unpack_f32x2(uint64_t v, float &lo, float &hi)
+{
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+
+__device__ __forceinline__ uint64_t ffma_f32x2(uint64_t a, uint64_t b, uint64_t c)
+{
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+
+__device__ __forceinline__ uint64_t fadd_f32x2(uint64_t a, uint64_t b)
+{
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+
 constexpr int kTcRows = 128;     // query rows per CTA (M of the MMAs)
 constexpr int kRowWarps = 4;     // warps 0-3: one thread per row (softmax, epilogue)
 constexpr int kKeyWarp = 4;      // table lookups and key fetches
@@ -402,22 +441,21 @@ __global__ void __launch_bounds__(kTcThreads, 2)
                         for (int i = 0; i < kTcTokens; ++i)
                             sv[i] = t0 + i < lim ? sv[i] : -INFINITY;
                     }
-                    // maximum raw score (the scale is positive), as a tree
-                    float e8[8];
+                    // maximum raw score (the scale is positive): a tree of
+                    // three-input maxima, 64 -> 22 -> 8 -> 3 -> 1
+                    static_assert(kTcTokens == 64, "max tree sized for 64 keys");
+                    float m22[22], m8[8];
 #pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        float x = sv[k];
+                    for (int k = 0; k < 21; ++k)
+                        m22[k] = fmax3(sv[3 * k], sv[3 * k + 1], sv[3 * k + 2]);
+                    m22[21] = sv[63];
 #pragma unroll
-                        for (int i = k + 8; i < kTcTokens; i += 8)
-                            x = fmaxf(x, sv[i]);
-                        e8[k] = x;
-                    }
-#pragma unroll
-                    for (int wd = 4; wd > 0; wd >>= 1)
-#pragma unroll
-                        for (int k = 0; k < wd; ++k)
-                            e8[k] = fmaxf(e8[k], e8[k + wd]);
-                    const float mx = e8[0] * p.scale_log2;  // -inf for a fully masked row
+                    for (int k = 0; k < 7; ++k)
+                        m8[k] = fmax3(m22[3 * k], m22[3 * k + 1], m22[3 * k + 2]);
+                    m8[7] = m22[21];
+                    const float mx = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]),
+                                           fmaxf(m8[6], m8[7])) *
+                                     p.scale_log2;  // -inf for a fully masked row
                     // the reference maximum moves only when a score passes it by 2^kSlack
                     const bool moved = mx > m_ref + kSlack;
                     float alpha = 1.f;
@@ -427,16 +465,27 @@ __global__ void __launch_bounds__(kTcThreads, 2)
                         l_run *= alpha;
                     }
                     const float neg_mu = m_ref == -INFINITY ? 0.f : -m_ref;
+                    // exponents two at a time (packed fp32 FMA), weights
+                    // summed in two packed accumulators
                     uint32_t pw[kTcTokens / 2];
-                    float ls[4] = {0.f, 0.f, 0.f, 0.f};
+                    const uint64_t sl2 = pack_f32x2(p.scale_log2, p.scale_log2);
+                    const uint64_t nm2 = pack_f32x2(neg_mu, neg_mu);
+                    uint64_t acc[2] = {pack_f32x2(0.f, 0.f), pack_f32x2(0.f, 0.f)};
 #pragma unroll
                     for (int i = 0; i < kTcTokens / 2; ++i) {
-                        const float p0 = exp2f(fmaf(sv[2 * i], p.scale_log2, neg_mu));
-                        const float p1 = exp2f(fmaf(sv[2 * i + 1], p.scale_log2, neg_mu));
-                        ls[i & 3] += p0 + p1;
+                        float e0, e1;
+                        unpack_f32x2(ffma_f32x2(pack_f32x2(sv[2 * i], sv[2 * i + 1]), sl2, nm2),
+                                     e0, e1);
+                        const float p0 = exp2f(e0), p1 = exp2f(e1);
+                        acc[i & 1] = fadd_f32x2(acc[i & 1], pack_f32x2(p0, p1));
                         pw[i] = MmaOp<T>::pack(p0, p1);
                     }
-                    l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+                    {
+                        float a0, a1, b0, b1;
+                        unpack_f32x2(acc[0], a0, a1);
+                        unpack_f32x2(acc[1], b0, b1);
+                        l_run += (a0 + a1) + (b0 + b1);
+                    }
 
                     // 3. a row's reference maximum moved: rescale O in tensor
                     //    memory once the previous tile's value product is done
