@@ -428,13 +428,12 @@ __global__ void __launch_bounds__(kTcThreads, 2)
                     // 2. softmax of this thread's row: raw scores (q . k); the
                     //    scale is applied inside the exponent
                     float sv[kTcTokens];
+                    {
+                        uint32_t r[kTcTokens];
+                        tmem_ld_32x32b_x64(tmem + lane_base + b * kTcTokens, r);
 #pragma unroll
-                    for (int c = 0; c < kTcTokens / 32; ++c) {
-                        uint32_t r[32];
-                        tmem_ld_32x32b_x32(tmem + lane_base + b * kTcTokens + c * 32, r);
-#pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            sv[c * 32 + i] = __uint_as_float(r[i]);
+                        for (int i = 0; i < kTcTokens; ++i)
+                            sv[i] = __uint_as_float(r[i]);
                     }
                     if (lim < t0 + kTcTokens) {  // causal / range mask (diagonal, last tiles)
 #pragma unroll
@@ -546,30 +545,30 @@ __global__ void __launch_bounds__(kTcThreads, 2)
                 p.part_l[ooff] = l_run;
             }
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-                uint32_t r[32];
+            for (int c = 0; c < D / 64; ++c) {
+                uint32_t r[64];
                 if (w.n > 0) {
-                    tmem_ld_32x32b_x32(tmem + lane_base + kTmemO + c * 32, r);
+                    tmem_ld_32x32b_x64(tmem + lane_base + kTmemO + c * 64, r);
                 } else {
 #pragma unroll
-                    for (int i = 0; i < 32; ++i)
+                    for (int i = 0; i < 64; ++i)
                         r[i] = 0u;
                 }
                 if (ooff < 0)
                     continue;
                 if (p.prefix_mode) {
-                    float4 *dst = reinterpret_cast<float4 *>(p.part_o + ooff * D) + c * 8;
+                    float4 *dst = reinterpret_cast<float4 *>(p.part_o + ooff * D) + c * 16;
 #pragma unroll
-                    for (int i = 0; i < 8; ++i)
+                    for (int i = 0; i < 16; ++i)
                         dst[i] = make_float4(__uint_as_float(r[4 * i]) * inv,
                                              __uint_as_float(r[4 * i + 1]) * inv,
                                              __uint_as_float(r[4 * i + 2]) * inv,
                                              __uint_as_float(r[4 * i + 3]) * inv);
                 } else {
                     uint4 *dst =
-                        reinterpret_cast<uint4 *>(static_cast<T *>(p.out) + ooff) + c * 4;
+                        reinterpret_cast<uint4 *>(static_cast<T *>(p.out) + ooff) + c * 8;
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
+                    for (int i = 0; i < 8; ++i) {
                         uint4 v;
                         v.x = MmaOp<T>::pack(__uint_as_float(r[8 * i]) * inv,
                                              __uint_as_float(r[8 * i + 1]) * inv);
