@@ -553,8 +553,7 @@ def run_ours(args):
         if flush is not None:
             flush.zero_()
         ev_s[i].record(stream)
-        st.slot_mapping()
-        st.reshape_and_cache()
+        st.slot_mapping_and_cache()
         st.copy_blocks()
         ev_a[i].record(stream)
         st.attention()

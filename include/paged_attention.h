@@ -130,6 +130,36 @@ PA_API pa_status pa_reshape_and_cache_fp8(const void *key, const void *value,
                                           float v_scale, int32_t *error_word, void *stream);
 
 /*
+ * pa_slot_mapping_and_cache, pa_slot_mapping_and_cache_fp8 -- one launch for
+ * the two steps before attention: the slot of each new token as
+ * pa_slot_mapping computes it ([GAO] §1.5; same checks, slot -1 and the same
+ * error flags for a bad token or table entry), stored to slot_mapping, and
+ * its K/V written there as pa_reshape_and_cache / pa_reshape_and_cache_fp8
+ * write them (same layouts, dtypes, scales and rules).  The pools and
+ * slot_mapping end bit-identical to the two calls made in turn.
+ */
+PA_API pa_status pa_slot_mapping_and_cache(int32_t *slot_mapping, const int32_t *block_tables,
+                                           int max_blocks_per_seq, const int32_t *token_seq,
+                                           const int32_t *token_pos, int num_tokens,
+                                           int num_seqs, const void *key, const void *value,
+                                           void *key_cache, void *value_cache, int num_blocks,
+                                           int block_size, int num_kv_heads, int head_dim,
+                                           pa_dtype dtype, int32_t *error_word, void *stream);
+
+PA_API pa_status pa_slot_mapping_and_cache_fp8(int32_t *slot_mapping,
+                                               const int32_t *block_tables,
+                                               int max_blocks_per_seq,
+                                               const int32_t *token_seq,
+                                               const int32_t *token_pos, int num_tokens,
+                                               int num_seqs, const void *key,
+                                               const void *value, void *key_cache,
+                                               void *value_cache, int num_blocks,
+                                               int block_size, int num_kv_heads, int head_dim,
+                                               pa_dtype src_dtype, float k_scale,
+                                               float v_scale, int32_t *error_word,
+                                               void *stream);
+
+/*
  * pa_copy_blocks -- the "copy the contents" step of copy-on-write
  * ([LAKE] §3.2).  block_mapping: int32 [num_pairs][2] = (src, dst); for every
  * pair, K block dst := K block src and V block dst := V block src (whole

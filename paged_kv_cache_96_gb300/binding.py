@@ -64,6 +64,10 @@ def _load() -> ctypes.CDLL:
                                               i32, i32, i32, f32, i32, i32, P, P]),
         "pa_reshape_and_cache_fp8": (i32, [P, P, P, P, P, i32, i32, i32, i32, i32, i32, f32,
                                            f32, P, P]),
+        "pa_slot_mapping_and_cache": (i32, [P, P, i32, P, P, i32, i32, P, P, P, P, i32, i32,
+                                            i32, i32, i32, P, P]),
+        "pa_slot_mapping_and_cache_fp8": (i32, [P, P, i32, P, P, i32, i32, P, P, P, P, i32,
+                                                i32, i32, i32, i32, f32, f32, P, P]),
         "pa_decode_attention_fp8": (i32, [P, P, P, P, P, i32, P, i32, i32, i32, i32, i32,
                                           i32, i32, f32, f32, f32, i32, P, sz, i32, P, P]),
         "pa_prefill_attention": (i32, [P, P, P, P, P, i32, P, P, i32, i32, i32, i32, i32,
@@ -176,6 +180,41 @@ def pa_reshape_and_cache(key: torch.Tensor, value: torch.Tensor,
         _dev(key_cache, "key_cache"), _dev(value_cache, "value_cache", key_cache.dtype),
         _dev(slot_mapping, "slot_mapping", torch.int32), T, N, bs, Hkv, d, dt,
         _opt(error_word, "error_word"), _stream(stream)))
+
+
+def pa_slot_mapping_and_cache(slot_mapping: torch.Tensor, block_tables: torch.Tensor,
+                              token_seq: torch.Tensor, token_pos: torch.Tensor,
+                              key: torch.Tensor, value: torch.Tensor,
+                              key_cache: torch.Tensor, value_cache: torch.Tensor,
+                              k_scale: float = 1.0, v_scale: float = 1.0,
+                              error_word: Optional[torch.Tensor] = None,
+                              stream=None) -> None:
+    """pa_slot_mapping and the cache write in one launch: slot_mapping gets
+    the slots, the pools the new tokens' K/V (e4m3 codes with the scales when
+    the pools are uint8)."""
+    S, MB = block_tables.shape
+    T, Hkv, d = key.shape
+    N, bs, Hkv2, d2 = key_cache.shape
+    if (Hkv, d) != (Hkv2, d2) or value.shape != key.shape or value_cache.shape != key_cache.shape:
+        raise ValueError("shape mismatch between new tokens and pools")
+    if token_seq.shape[0] != T or token_pos.shape[0] != T or slot_mapping.shape[0] != T:
+        raise ValueError("one sequence id, position and slot per new token expected")
+    head = (_dev(slot_mapping, "slot_mapping", torch.int32),
+            _dev(block_tables, "block_tables", torch.int32), MB,
+            _dev(token_seq, "token_seq", torch.int32), _dev(token_pos, "token_pos", torch.int32),
+            T, S)
+    if key_cache.dtype == torch.uint8:
+        _check("pa_slot_mapping_and_cache_fp8", _lib.pa_slot_mapping_and_cache_fp8(
+            *head, _dev(key, "key"), _dev(value, "value", key.dtype),
+            _dev(key_cache, "key_cache", torch.uint8),
+            _dev(value_cache, "value_cache", torch.uint8), N, bs, Hkv, d, _dtype_code(key),
+            float(k_scale), float(v_scale), _opt(error_word, "error_word"), _stream(stream)))
+        return
+    _check("pa_slot_mapping_and_cache", _lib.pa_slot_mapping_and_cache(
+        *head, _dev(key, "key", key_cache.dtype), _dev(value, "value", key_cache.dtype),
+        _dev(key_cache, "key_cache"), _dev(value_cache, "value_cache", key_cache.dtype),
+        N, bs, Hkv, d, _dtype_code(key_cache), _opt(error_word, "error_word"),
+        _stream(stream)))
 
 
 def pa_copy_blocks(key_cache: torch.Tensor, value_cache: torch.Tensor,

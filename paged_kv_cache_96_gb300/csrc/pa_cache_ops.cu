@@ -31,7 +31,31 @@ pa_status record_cuda(cudaError_t err)
 
 // ---- slot mapping ------------------------------------------------------------
 
-// One thread per token: slot = table[s][p / bs] * bs + p % bs.
+// The slot of token t: table[s][p / bs] * bs + p % bs, or -1 (flagged) for a
+// token outside the batch or the table, or a table entry outside the pool.
+__device__ __forceinline__ int32_t token_slot(const int32_t *__restrict__ block_tables,
+                                              int max_blocks_per_seq,
+                                              const int32_t *__restrict__ token_seq,
+                                              const int32_t *__restrict__ token_pos, int t,
+                                              int num_seqs, int block_size, int num_blocks,
+                                              int32_t *error_word)
+{
+    const int s = token_seq[t];
+    const int p = token_pos[t];
+    if (s < 0 || s >= num_seqs || p < 0 || p / block_size >= max_blocks_per_seq) {
+        flag_error(error_word, PA_DEVERR_TOKEN_RANGE);
+        return -1;
+    }
+    const int32_t block =
+        block_tables[static_cast<int64_t>(s) * max_blocks_per_seq + p / block_size];
+    if (block < 0 || block >= num_blocks) {
+        flag_error(error_word, PA_DEVERR_BLOCK_RANGE);
+        return -1;
+    }
+    return block * block_size + p % block_size;
+}
+
+// One thread per token.
 __global__ void slot_mapping_kernel(int32_t *__restrict__ slot_mapping,
                                     const int32_t *__restrict__ block_tables,
                                     int max_blocks_per_seq,
@@ -45,20 +69,36 @@ __global__ void slot_mapping_kernel(int32_t *__restrict__ slot_mapping,
     const int t = blockIdx.x * blockDim.x + threadIdx.x;
     if (t >= num_tokens)
         return;
-    const int s = token_seq[t];
-    const int p = token_pos[t];
-    int32_t slot = -1;
-    if (s < 0 || s >= num_seqs || p < 0 || p / block_size >= max_blocks_per_seq) {
-        flag_error(error_word, PA_DEVERR_TOKEN_RANGE);
-    } else {
-        const int32_t block =
-            block_tables[static_cast<int64_t>(s) * max_blocks_per_seq + p / block_size];
-        if (block < 0 || block >= num_blocks)
-            flag_error(error_word, PA_DEVERR_BLOCK_RANGE);
-        else
-            slot = block * block_size + p % block_size;
+    slot_mapping[t] = token_slot(block_tables, max_blocks_per_seq, token_seq, token_pos, t,
+                                 num_seqs, block_size, num_blocks, error_word);
+}
+
+// Where a cache-write CTA finds its token's slot: in slot_mapping (written
+// by slot_mapping_kernel), or -- fused -- computed here from the token's
+// sequence and position (thread 0), stored to slot_mapping and shared.
+struct SlotSource {
+    int32_t *slot_mapping;
+    const int32_t *block_tables;  // null: read slot_mapping
+    const int32_t *token_seq;
+    const int32_t *token_pos;
+    int max_blocks_per_seq, num_seqs, block_size, num_blocks;
+};
+
+__device__ __forceinline__ int64_t cta_token_slot(const SlotSource &src, int t,
+                                                  int32_t *error_word)
+{
+    if (src.block_tables == nullptr)
+        return src.slot_mapping[t];
+    __shared__ int32_t slot_s;
+    if (threadIdx.x == 0) {
+        const int32_t slot = token_slot(src.block_tables, src.max_blocks_per_seq,
+                                        src.token_seq, src.token_pos, t, src.num_seqs,
+                                        src.block_size, src.num_blocks, error_word);
+        src.slot_mapping[t] = slot;
+        slot_s = slot;
     }
-    slot_mapping[t] = slot;
+    __syncthreads();
+    return slot_s;
 }
 
 // ---- reshape_and_cache --------------------------------------------------------
@@ -69,14 +109,13 @@ __global__ void reshape_and_cache_kernel(const uint4 *__restrict__ key,
                                          const uint4 *__restrict__ value,
                                          uint4 *__restrict__ key_cache,
                                          uint4 *__restrict__ value_cache,
-                                         const int32_t *__restrict__ slot_mapping,
-                                         int64_t num_slots, int words_per_token,
-                                         int32_t *error_word)
+                                         const SlotSource slots, int64_t num_slots,
+                                         int words_per_token, int32_t *error_word)
 {
     pdl_wait_primary();
     pdl_launch_dependents();
     const int t = blockIdx.x;
-    const int64_t slot = slot_mapping[t];
+    const int64_t slot = cta_token_slot(slots, t, error_word);
     if (slot < 0)
         return;
     if (slot >= num_slots) {
@@ -108,15 +147,14 @@ __global__ void reshape_and_cache_fp8_kernel(const uint4 *__restrict__ key,
                                              const uint4 *__restrict__ value,
                                              uint2 *__restrict__ key_cache,
                                              uint2 *__restrict__ value_cache,
-                                             const int32_t *__restrict__ slot_mapping,
-                                             int64_t num_slots, int words_per_token,
-                                             float k_inv_scale, float v_inv_scale,
-                                             int32_t *error_word)
+                                             const SlotSource slots, int64_t num_slots,
+                                             int words_per_token, float k_inv_scale,
+                                             float v_inv_scale, int32_t *error_word)
 {
     pdl_wait_primary();
     pdl_launch_dependents();
     const int t = blockIdx.x;
-    const int64_t slot = slot_mapping[t];
+    const int64_t slot = cta_token_slot(slots, t, error_word);
     if (slot < 0)
         return;
     if (slot >= num_slots) {
@@ -211,19 +249,19 @@ extern "C" pa_status pa_slot_mapping(int32_t *slot_mapping, const int32_t *block
                       num_tokens, num_seqs, block_size, num_blocks, error_word);
 }
 
-extern "C" pa_status pa_reshape_and_cache(const void *key, const void *value,
-                                          void *key_cache, void *value_cache,
-                                          const int32_t *slot_mapping, int num_tokens,
-                                          int num_blocks, int block_size,
-                                          int num_kv_heads, int head_dim, pa_dtype dtype,
-                                          int32_t *error_word, void *stream)
+// The cache writes of both entry forms (slots given, or computed in the
+// same launch).
+static pa_status cache_write(const void *key, const void *value, void *key_cache,
+                             void *value_cache, const SlotSource &src, int num_tokens,
+                             int num_blocks, int block_size, int num_kv_heads, int head_dim,
+                             pa_dtype dtype, int32_t *error_word, void *stream)
 {
     if (num_tokens < 0 || num_blocks <= 0 || block_size <= 0 || num_kv_heads <= 0 ||
         head_dim <= 0 || (dtype != PA_F16 && dtype != PA_BF16))
         return PA_ERR_INVALID_ARG;
     if (num_tokens == 0)
         return PA_OK;
-    if (!key || !value || !key_cache || !value_cache || !slot_mapping)
+    if (!key || !value || !key_cache || !value_cache || !src.slot_mapping)
         return PA_ERR_INVALID_ARG;
     if (!aligned16(key) || !aligned16(value) || !aligned16(key_cache) ||
         !aligned16(value_cache))
@@ -236,18 +274,15 @@ extern "C" pa_status pa_reshape_and_cache(const void *key, const void *value,
     return launch_pdl(reshape_and_cache_kernel, dim3(num_tokens), dim3(threads), 0,
                       as_stream(stream), static_cast<const uint4 *>(key),
                       static_cast<const uint4 *>(value), static_cast<uint4 *>(key_cache),
-                      static_cast<uint4 *>(value_cache), slot_mapping,
+                      static_cast<uint4 *>(value_cache), src,
                       static_cast<int64_t>(num_blocks) * block_size, words, error_word);
 }
 
-extern "C" pa_status pa_reshape_and_cache_fp8(const void *key, const void *value,
-                                              void *key_cache, void *value_cache,
-                                              const int32_t *slot_mapping, int num_tokens,
-                                              int num_blocks, int block_size,
-                                              int num_kv_heads, int head_dim,
-                                              pa_dtype src_dtype, float k_scale,
-                                              float v_scale, int32_t *error_word,
-                                              void *stream)
+static pa_status cache_write_fp8(const void *key, const void *value, void *key_cache,
+                                 void *value_cache, const SlotSource &src, int num_tokens,
+                                 int num_blocks, int block_size, int num_kv_heads,
+                                 int head_dim, pa_dtype src_dtype, float k_scale,
+                                 float v_scale, int32_t *error_word, void *stream)
 {
     if (num_tokens < 0 || num_blocks <= 0 || block_size <= 0 || num_kv_heads <= 0 ||
         head_dim <= 0 || (src_dtype != PA_F16 && src_dtype != PA_BF16) ||
@@ -256,7 +291,7 @@ extern "C" pa_status pa_reshape_and_cache_fp8(const void *key, const void *value
         return PA_ERR_INVALID_ARG;
     if (num_tokens == 0)
         return PA_OK;
-    if (!key || !value || !key_cache || !value_cache || !slot_mapping)
+    if (!key || !value || !key_cache || !value_cache || !src.slot_mapping)
         return PA_ERR_INVALID_ARG;
     if (!aligned16(key) || !aligned16(value) || !aligned16(key_cache) ||
         !aligned16(value_cache))
@@ -273,13 +308,96 @@ extern "C" pa_status pa_reshape_and_cache_fp8(const void *key, const void *value
         return launch_pdl(reshape_and_cache_fp8_kernel<__nv_bfloat16>, dim3(num_tokens),
                           dim3(threads), 0, as_stream(stream), static_cast<const uint4 *>(key),
                           static_cast<const uint4 *>(value), static_cast<uint2 *>(key_cache),
-                          static_cast<uint2 *>(value_cache), slot_mapping, slots, words, k_inv,
-                          v_inv, error_word);
+                          static_cast<uint2 *>(value_cache), src, slots, words, k_inv, v_inv,
+                          error_word);
     return launch_pdl(reshape_and_cache_fp8_kernel<__half>, dim3(num_tokens), dim3(threads), 0,
                       as_stream(stream), static_cast<const uint4 *>(key),
                       static_cast<const uint4 *>(value), static_cast<uint2 *>(key_cache),
-                      static_cast<uint2 *>(value_cache), slot_mapping, slots, words, k_inv,
-                      v_inv, error_word);
+                      static_cast<uint2 *>(value_cache), src, slots, words, k_inv, v_inv,
+                      error_word);
+}
+
+// Slots computed in the cache-write launch: the tables and token arrays are
+// checked as pa_slot_mapping checks them.
+static pa_status fused_source(SlotSource *src, int32_t *slot_mapping,
+                              const int32_t *block_tables, int max_blocks_per_seq,
+                              const int32_t *token_seq, const int32_t *token_pos,
+                              int num_tokens, int num_seqs, int block_size, int num_blocks)
+{
+    if (num_tokens < 0 || num_seqs < 0 || max_blocks_per_seq <= 0 || block_size <= 0 ||
+        num_blocks <= 0)
+        return PA_ERR_INVALID_ARG;
+    if (num_tokens > 0 && (!slot_mapping || !block_tables || !token_seq || !token_pos))
+        return PA_ERR_INVALID_ARG;
+    if (static_cast<int64_t>(num_blocks) * block_size > INT32_MAX)
+        return PA_ERR_UNSUPPORTED;
+    *src = SlotSource{slot_mapping, block_tables, token_seq, token_pos,
+                      max_blocks_per_seq, num_seqs, block_size, num_blocks};
+    return PA_OK;
+}
+
+extern "C" pa_status pa_reshape_and_cache(const void *key, const void *value,
+                                          void *key_cache, void *value_cache,
+                                          const int32_t *slot_mapping, int num_tokens,
+                                          int num_blocks, int block_size,
+                                          int num_kv_heads, int head_dim, pa_dtype dtype,
+                                          int32_t *error_word, void *stream)
+{
+    const SlotSource src{const_cast<int32_t *>(slot_mapping), nullptr, nullptr, nullptr,
+                         0, 0, 0, 0};
+    return cache_write(key, value, key_cache, value_cache, src, num_tokens, num_blocks,
+                       block_size, num_kv_heads, head_dim, dtype, error_word, stream);
+}
+
+extern "C" pa_status pa_reshape_and_cache_fp8(const void *key, const void *value,
+                                              void *key_cache, void *value_cache,
+                                              const int32_t *slot_mapping, int num_tokens,
+                                              int num_blocks, int block_size,
+                                              int num_kv_heads, int head_dim,
+                                              pa_dtype src_dtype, float k_scale,
+                                              float v_scale, int32_t *error_word,
+                                              void *stream)
+{
+    const SlotSource src{const_cast<int32_t *>(slot_mapping), nullptr, nullptr, nullptr,
+                         0, 0, 0, 0};
+    return cache_write_fp8(key, value, key_cache, value_cache, src, num_tokens, num_blocks,
+                           block_size, num_kv_heads, head_dim, src_dtype, k_scale, v_scale,
+                           error_word, stream);
+}
+
+extern "C" pa_status pa_slot_mapping_and_cache(
+    int32_t *slot_mapping, const int32_t *block_tables, int max_blocks_per_seq,
+    const int32_t *token_seq, const int32_t *token_pos, int num_tokens, int num_seqs,
+    const void *key, const void *value, void *key_cache, void *value_cache, int num_blocks,
+    int block_size, int num_kv_heads, int head_dim, pa_dtype dtype, int32_t *error_word,
+    void *stream)
+{
+    SlotSource src;
+    const pa_status st = fused_source(&src, slot_mapping, block_tables, max_blocks_per_seq,
+                                      token_seq, token_pos, num_tokens, num_seqs, block_size,
+                                      num_blocks);
+    if (st != PA_OK)
+        return st;
+    return cache_write(key, value, key_cache, value_cache, src, num_tokens, num_blocks,
+                       block_size, num_kv_heads, head_dim, dtype, error_word, stream);
+}
+
+extern "C" pa_status pa_slot_mapping_and_cache_fp8(
+    int32_t *slot_mapping, const int32_t *block_tables, int max_blocks_per_seq,
+    const int32_t *token_seq, const int32_t *token_pos, int num_tokens, int num_seqs,
+    const void *key, const void *value, void *key_cache, void *value_cache, int num_blocks,
+    int block_size, int num_kv_heads, int head_dim, pa_dtype src_dtype, float k_scale,
+    float v_scale, int32_t *error_word, void *stream)
+{
+    SlotSource src;
+    const pa_status st = fused_source(&src, slot_mapping, block_tables, max_blocks_per_seq,
+                                      token_seq, token_pos, num_tokens, num_seqs, block_size,
+                                      num_blocks);
+    if (st != PA_OK)
+        return st;
+    return cache_write_fp8(key, value, key_cache, value_cache, src, num_tokens, num_blocks,
+                           block_size, num_kv_heads, head_dim, src_dtype, k_scale, v_scale,
+                           error_word, stream);
 }
 
 extern "C" pa_status pa_copy_blocks(void *key_cache, void *value_cache,

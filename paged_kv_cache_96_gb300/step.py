@@ -169,21 +169,27 @@ class DecodeStep:
                                   self.max_context_len, self.w.scale, P, ws,
                                   error_word=self.error_word, stream=stream)
 
+    def slot_mapping_and_cache(self, stream=None) -> None:
+        """Steps 1 and 2 in one launch (slots computed where they are used)."""
+        B.pa_slot_mapping_and_cache(self.slots, self.block_tables, self.new_seq, self.new_pos,
+                                    self.new_key, self.new_value, self.key_cache,
+                                    self.value_cache, self.kv_scale, self.kv_scale,
+                                    error_word=self.error_word, stream=stream)
+
     def run(self, stream=None) -> torch.Tensor:
         """One whole decode step; returns the attention output tensor."""
-        self.slot_mapping(stream)
-        self.reshape_and_cache(stream)
+        self.slot_mapping_and_cache(stream)
         self.copy_blocks(stream)
         self.attention(stream)
         return self.out
 
     def launches_per_step(self) -> int:
-        """Kernels one run() launches: slot mapping, cache write, block copy
-        (when the step has copy-on-write pairs), the attention pass, the
+        """Kernels one run() launches: slot mapping with the cache write, block
+        copy (when the step has copy-on-write pairs), the attention pass, the
         shared-prefix pass (prefix-aware decode with at least one group), and
         the reduce (when some context spans more than one partition, or a
         prefix group exists)."""
-        n = 3 + (1 if self.cow_pairs is not None else 0)
+        n = 2 + (1 if self.cow_pairs is not None else 0)
         if self.cascade and self.num_groups > 0:
             n += 2
         elif self.workspace is not None and not self.cascade:
