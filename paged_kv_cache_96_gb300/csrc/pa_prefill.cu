@@ -403,7 +403,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
             write_q(w, rw);
         }
         for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x) {
-            const long long qoff = rw.qoff, ooff = rw.ooff;
+            const long long ooff = rw.ooff;
             const int lim = rw.lim;
             const bool has_next = u + (int)gridDim.x < total_units;
             if (has_next) {
