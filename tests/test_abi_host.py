@@ -104,6 +104,29 @@ def test_cache_op_argument_checks(B):
         B.PA_ERR_INVALID_ARG
 
 
+def test_fused_cache_argument_checks(B):
+    """pa_slot_mapping_and_cache(_fp8): the slot-mapping checks, then the
+    cache-write checks, all before any launch."""
+    L = B.lib()
+    f = L.pa_slot_mapping_and_cache
+    f8 = L.pa_slot_mapping_and_cache_fp8
+    # (slots, tables, mb, seq, pos, T, S, key, value, kc, vc, N, bs, Hkv, d, dtype, err, stream)
+    ok = (FAKE, FAKE, 4, FAKE, FAKE, 3, 2, FAKE, FAKE, FAKE, FAKE, 8, 16, 2, 128, 1, None, None)
+    assert f(*ok[:5], 0, *ok[6:]) == B.PA_OK                          # no tokens
+    assert f(None, *ok[1:]) == B.PA_ERR_INVALID_ARG                   # no slot array
+    assert f(*ok[:3], None, *ok[4:]) == B.PA_ERR_INVALID_ARG          # no sequence ids
+    assert f(*ok[:2], 0, *ok[3:]) == B.PA_ERR_INVALID_ARG             # empty table rows
+    assert f(*ok[:7], FAKE_ODD, *ok[8:]) == B.PA_ERR_INVALID_ARG      # unaligned keys
+    assert f(*ok[:13], 1, 4, *ok[15:]) == B.PA_ERR_UNSUPPORTED        # 8-byte rows
+    assert f(*ok[:15], 5, *ok[16:]) == B.PA_ERR_INVALID_ARG           # not a 16-bit type
+    assert f(*ok[:11], 1 << 20, 1 << 12, *ok[13:]) == B.PA_ERR_UNSUPPORTED  # 2^32 slots
+    ok8 = ok[:16] + (0.5, 0.5) + ok[16:]
+    assert f8(*ok8[:5], 0, *ok8[6:]) == B.PA_OK
+    assert f8(*ok8[:16], 0.0, 0.5, *ok8[18:]) == B.PA_ERR_INVALID_ARG  # zero K scale
+    assert f8(*ok8[:16], 0.5, float("inf"), *ok8[18:]) == B.PA_ERR_INVALID_ARG
+    assert f8(*ok8[:3], None, *ok8[4:]) == B.PA_ERR_INVALID_ARG
+
+
 def test_workspace_layout_sizes(B):
     L = B.lib()
     a256 = lambda x: (x + 255) // 256 * 256  # noqa: E731
