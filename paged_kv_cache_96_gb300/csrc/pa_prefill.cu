@@ -19,26 +19,27 @@
 // Design (GB300): a CTA takes 128 query rows of one KV head -- a chunk's
 // tokens times the G query heads of the group, or the members' decode
 // queries times G -- as the M = 128 dimension of tcgen05.mma tiles, and its
-// six warps split the work.  Warps 0-3 (one thread per row) write the rows
+// seven warps split the work.  Warps 0-3 (one thread per row) write the rows
 // into shared memory as the K-major A operand (128-byte swizzle), read each
 // S row from tensor memory, apply the causal / range mask and the online
 // softmax (fp32, log2 units, a reference maximum that moves only when a
 // score exceeds it by 2^8, rescaling O in tensor memory then), and write P as
 // bf16/fp16 pairs back over S, where it is the A operand of the value
-// product.  Warp 4 looks up the physical blocks and streams keys and values
-// through a 2-stage ring of 64-token tiles by 4-D TMA loads (2 KB boxes,
-// 128-byte swizzle) whose layout is directly the K-major B operand of
-// S = Q K^T and the MN-major B operand of O += P V.  Warp 5 issues the MMAs
-// from one elected lane: S of tile g into S buffer g % 2 as soon as its keys
-// have landed and the buffer's previous P has been consumed, then the value
-// product of tile g - 1, and commits each to an mbarrier that frees the ring
-// stage or the S buffer it used.  S (128 x 64, fp32, double-buffered) and
-// O (128 x d, fp32) live in tensor memory (256 columns, so two CTAs share an
-// SM).  The roles meet only at mbarriers whose phase is the tile's index
-// over the CTA's units / 2; every wait is bounded in time, the first to run
-// out stops all roles, and tensor memory is released on every exit path.
-// Value rows past the key range are zeroed in shared memory before the value
-// product, so a poisoned (NaN) slot never reaches the output.
+// product.  Warps 4 and 5 look up the physical blocks and stream the keys,
+// resp. the values, through a 2-stage ring of 64-token tiles by 4-D TMA loads
+// (2 KB boxes, 128-byte swizzle) whose layout is directly the K-major B
+// operand of S = Q K^T and the MN-major B operand of O += P V.  Warp 6 issues
+// the MMAs from one elected lane: S of tile g into S buffer g % 2 as soon as
+// its keys have landed and the buffer's previous P has been consumed, then
+// the value product of tile g - 1, and commits each to an mbarrier that frees
+// the ring stage or the S buffer it used.  S (128 x 64, fp32,
+// double-buffered) and O (128 x d, fp32) live in tensor memory (256 columns,
+// so two CTAs share an SM).  The roles meet only at mbarriers whose phase is
+// the tile's index over the CTA's units / 2; every wait is bounded in time,
+// the first to run out stops all roles, and tensor memory is released on
+// every exit path.  Value rows past the key range are zeroed in shared
+// memory before the value product, so a poisoned (NaN) slot never reaches
+// the output.
 #include <cuda.h>
 
 #include <algorithm>
