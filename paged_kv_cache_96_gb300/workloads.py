@@ -401,7 +401,7 @@ CONFIGS["chunked"] = WorkloadSpec(
     context_lens=_fixed([512, 1024, 1536, 2048]), query_lens=_fixed_q([512] * 4),
     partition_size=0)
 CONFIGS["prefix-cascade"] = dataclasses.replace(
-    CONFIGS["prefix"], name="prefix-cascade", cascade=True, partition_size=512,
+    CONFIGS["prefix"], name="prefix-cascade", cascade=True, partition_size=1024,
     description=CONFIGS["prefix"].description + "; prefix-aware decode (shared "
     "prefix read once per group)")
 
