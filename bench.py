@@ -2,12 +2,17 @@
 """Paged decode step benchmark on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME]
-                    [--partition P] [--impl ours|reference]
+                    [--partition P] [--separate-append] [--impl ours|reference]
 
 A step is one pass of the whole hot path over one batch: slot mapping of
 the step's new tokens, reshape_and_cache of their K/V, copy-on-write block
 copies (when the workload has them) and paged decode attention (split-context
-partitions merged in the same launch).  Default workload: the GQA 70B-like
+partitions merged by a reduce launch).  A decode step with one new token per
+sequence copies its copy-on-write blocks first and then runs the slot
+mapping, the cache write and attention as one call
+(pa_decode_attention_append); `--separate-append` times the unfused order
+instead (one launch for slot mapping and cache write, then copy-on-write,
+then attention).  Default workload: the GQA 70B-like
 decode layer (128 sequences, lognormal contexts, 64 query heads over 8 KV
 heads, d 128, block 16, bf16).
 
@@ -58,6 +63,9 @@ def parse_args(argv=None):
                              "longctx-fp8", "prefix-cascade", "mixed", "chunked"])
     ap.add_argument("--partition", type=int, default=None,
                     help="split-context partition tokens (0 = single pass)")
+    ap.add_argument("--separate-append", action="store_true",
+                    help="decode steps: write the new tokens with their own launch "
+                         "before attention instead of inside it")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
@@ -520,6 +528,8 @@ def run_ours(args):
     from paged_kv_cache_96_gb300 import workloads as W
     w = W.build(W.CONFIGS[args.config])
     st = S.DecodeStep(w, device=str(dev), partition_size=args.partition)
+    if args.separate_append:
+        st.fused_append = False
     stream = torch.cuda.current_stream(dev)
     torch.cuda.synchronize(dev)
 
@@ -553,10 +563,16 @@ def run_ours(args):
         if flush is not None:
             flush.zero_()
         ev_s[i].record(stream)
-        st.slot_mapping_and_cache()
-        st.copy_blocks()
-        ev_a[i].record(stream)
-        st.attention()
+        if st.fused_append:
+            # copy-on-write, then the new tokens' append fused into attention
+            st.copy_blocks()
+            ev_a[i].record(stream)
+            st.append_attention()
+        else:
+            st.slot_mapping_and_cache()
+            st.copy_blocks()
+            ev_a[i].record(stream)
+            st.attention()
         ev_b[i].record(stream)
     torch.cuda.synchronize(dev)
     t_host1 = time.time()
@@ -655,6 +671,9 @@ def run_ours(args):
     attn_bytes = w.unique_kv_bytes() + w.qo_bytes()
     achieved = attn_bytes / attn_s / 1e9
     kernel = "pa_decode_attention (paged_decode_kernel + paged_reduce_kernel)"
+    if st.fused_append:
+        kernel = ("pa_decode_attention_append (paged_decode_kernel with the new tokens' "
+                  "append + paged_reduce_kernel)")
     if st.cascade:
         kernel = ("pa_decode_attention_cascade (paged_decode_kernel + paged_mq_kernel "
                   "prefix pass + paged_reduce_kernel)")

@@ -251,6 +251,50 @@ PA_API pa_status pa_decode_attention_fp8(void *out, const void *query, const voi
                                          int32_t *error_word, void *stream);
 
 /*
+ * pa_decode_attention_append, pa_decode_attention_append_fp8 -- one decode
+ * step in one call: the slot mapping and reshape_and_cache of each running
+ * sequence's new token ([GAO] §1.5 and §1.6: the token's K/V go to slot
+ * block_table[pos // block_size] * block_size + pos % block_size) fused into
+ * pa_decode_attention / pa_decode_attention_fp8.  The new token of sequence
+ * s is at position pos = context_lens[s] - 1 (context_lens counts it):
+ *   new_key, new_value : [num_seqs][num_kv_heads][head_dim], dtype (16-bit),
+ *                        device, 16-byte aligned.
+ *   key_cache, value_cache : written at the slot of pos -- the 16-bit rows
+ *                        verbatim, or (FP8 pools) the e4m3 codes
+ *                        e4m3(x * (1 / k_scale)) / e4m3(x * (1 / v_scale)),
+ *                        bit for bit what pa_reshape_and_cache(_fp8) writes.
+ *   slot_mapping       : int32 [num_seqs] (device) or NULL: receives each
+ *                        sequence's slot (-1 for a context of 0, which
+ *                        appends nothing).
+ * Attention then covers positions [0, context_lens[s]): the cached ones
+ * from the pools and pos from the new rows as the pools now hold them (for
+ * FP8 pools, the codes), so out equals that of pa_slot_mapping +
+ * pa_reshape_and_cache(_fp8) + pa_decode_attention(_fp8) on the same inputs
+ * up to fp32 rounding order (the new token's term joins the softmax sums in
+ * the pass's end-of-partition merge rather than inside a 16-token tile).
+ * The block holding pos must belong to sequence s alone (copy-on-write
+ * first, as the engine does before any write into a shared block); other
+ * arguments, workspace and errors as pa_decode_attention(_fp8).  A table
+ * entry of pos outside [0, num_blocks) flags PA_DEVERR_BLOCK_RANGE and
+ * nothing is written there.
+ */
+PA_API pa_status pa_decode_attention_append(
+    void *out, const void *query, void *key_cache, void *value_cache, const void *new_key,
+    const void *new_value, int32_t *slot_mapping, const int32_t *block_tables,
+    int max_blocks_per_seq, const int32_t *context_lens, int max_context_len, int num_seqs,
+    int num_heads, int num_kv_heads, int head_dim, int block_size, int num_blocks, float scale,
+    int partition_size, void *workspace, size_t workspace_bytes, pa_dtype dtype,
+    int32_t *error_word, void *stream);
+
+PA_API pa_status pa_decode_attention_append_fp8(
+    void *out, const void *query, void *key_cache, void *value_cache, const void *new_key,
+    const void *new_value, int32_t *slot_mapping, const int32_t *block_tables,
+    int max_blocks_per_seq, const int32_t *context_lens, int max_context_len, int num_seqs,
+    int num_heads, int num_kv_heads, int head_dim, int block_size, int num_blocks, float scale,
+    float k_scale, float v_scale, int partition_size, void *workspace, size_t workspace_bytes,
+    pa_dtype dtype, int32_t *error_word, void *stream);
+
+/*
  * pa_prefill_attention -- chunked prefill and mixed batches over the paged
  * pool, [GAO] §2.4 (prefill processes a prompt's tokens in parallel; a batch
  * mixes decode requests of one token with prefill requests of many) and

@@ -70,6 +70,11 @@ def _load() -> ctypes.CDLL:
                                                 i32, i32, i32, i32, f32, f32, P, P]),
         "pa_decode_attention_fp8": (i32, [P, P, P, P, P, i32, P, i32, i32, i32, i32, i32,
                                           i32, i32, f32, f32, f32, i32, P, sz, i32, P, P]),
+        "pa_decode_attention_append": (i32, [P, P, P, P, P, P, P, P, i32, P, i32, i32, i32,
+                                             i32, i32, i32, i32, f32, i32, P, sz, i32, P, P]),
+        "pa_decode_attention_append_fp8": (i32, [P, P, P, P, P, P, P, P, i32, P, i32, i32,
+                                                 i32, i32, i32, i32, i32, f32, f32, f32, i32,
+                                                 P, sz, i32, P, P]),
         "pa_prefill_attention": (i32, [P, P, P, P, P, i32, P, P, i32, i32, i32, i32, i32,
                                        i32, i32, i32, f32, i32, P, P]),
         "pa_prefix_plan_ints": (sz, [i32, i32, i32]),
@@ -332,6 +337,53 @@ def pa_decode_attention_fp8(out: torch.Tensor, query: torch.Tensor,
         d, bs, N, float(scale), float(k_scale), float(v_scale), int(partition_size),
         ws_ptr, ws_bytes, _dtype_code(query), _opt(error_word, "error_word"),
         _stream(stream)))
+
+
+def pa_decode_attention_append(out: torch.Tensor, query: torch.Tensor,
+                               key_cache: torch.Tensor, value_cache: torch.Tensor,
+                               new_key: torch.Tensor, new_value: torch.Tensor,
+                               block_tables: torch.Tensor, context_lens: torch.Tensor,
+                               max_context_len: int, scale: float, partition_size: int = 0,
+                               workspace: Optional[torch.Tensor] = None,
+                               slot_mapping: Optional[torch.Tensor] = None,
+                               k_scale: float = 1.0, v_scale: float = 1.0,
+                               error_word: Optional[torch.Tensor] = None,
+                               stream=None) -> None:
+    """One decode step in one call: each sequence's new token (new_key /
+    new_value [S, Hkv, d], at position context_lens[s] - 1) is written to the
+    pools, then attention runs over the whole context.  uint8 pools take the
+    e4m3 path with k_scale / v_scale."""
+    S, H, d = query.shape
+    N, bs, Hkv, d2 = key_cache.shape
+    MB = block_tables.shape[1]
+    if d != d2 or out.shape != query.shape:
+        raise ValueError("shape mismatch")
+    if new_key.shape != (S, Hkv, d) or new_value.shape != new_key.shape:
+        raise ValueError("new_key / new_value must be [num_seqs, num_kv_heads, head_dim]")
+    if slot_mapping is not None and slot_mapping.shape[0] != S:
+        raise ValueError("one slot per sequence expected")
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not None:
+        ws_ptr = _dev(workspace, "workspace")
+        ws_bytes = workspace.numel() * workspace.element_size()
+    fp8 = key_cache.dtype == torch.uint8
+    head = (_dev(out, "out", query.dtype), _dev(query, "query"),
+            _dev(key_cache, "key_cache"), _dev(value_cache, "value_cache", key_cache.dtype),
+            _dev(new_key, "new_key", query.dtype), _dev(new_value, "new_value", query.dtype),
+            _opt(slot_mapping, "slot_mapping"),
+            _dev(block_tables, "block_tables", torch.int32), MB,
+            _dev(context_lens, "context_lens", torch.int32), int(max_context_len), S, H, Hkv,
+            d, bs, N, float(scale))
+    if fp8:
+        _check("pa_decode_attention_append_fp8", _lib.pa_decode_attention_append_fp8(
+            *head, float(k_scale), float(v_scale), int(partition_size), ws_ptr, ws_bytes,
+            _dtype_code(query), _opt(error_word, "error_word"), _stream(stream)))
+        return
+    if query.dtype != key_cache.dtype:
+        raise TypeError("query and pools must share one 16-bit type")
+    _check("pa_decode_attention_append", _lib.pa_decode_attention_append(
+        *head, int(partition_size), ws_ptr, ws_bytes, _dtype_code(key_cache),
+        _opt(error_word, "error_word"), _stream(stream)))
 
 
 def alloc_workspace(num_seqs: int, num_heads: int, num_kv_heads: int, head_dim: int,

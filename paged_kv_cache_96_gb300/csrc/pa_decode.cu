@@ -63,7 +63,10 @@ template <int D, int NT, int NW, int NST, int EB> struct Layout {
     static constexpr int kMergeO = kStages + NW * NST * kStageBytes;
     static constexpr int kMergeM = kMergeO + NW * kHeads * kPitch * 4;
     static constexpr int kMergeL = kMergeM + NW * kHeads * 4;
-    static constexpr int kBars = kMergeL + NW * kHeads * 4;
+    // fused append: the new token's value row (fp32) and per-head scores
+    static constexpr int kAppV = kMergeL + NW * kHeads * 4;
+    static constexpr int kAppM = kAppV + D * 4;
+    static constexpr int kBars = kAppM + kHeads * 4;
     static constexpr int kFlags = kBars + NW * NST * 8;
     static constexpr int kSeq = kFlags + NW * NST * 4;  // int ctx[S], prefix[S + 1], start[S]
     static size_t bytes(int num_seqs) { return 1024 + kSeq + 4 * (3 * (size_t)num_seqs + 1); }
@@ -74,8 +77,122 @@ template <int D, int NT, int NW, int NST, int EB> struct Layout {
 // T: query/output type.  KV: cached element type -- T itself, or uint8_t
 // for FP8 (e4m3) pools, whose tiles are widened to fp16 in registers (the
 // tensor-core products then run in fp16).
+// Fused append, one warp, once per (sequence s, KV head kh) at the start of
+// the sequence's last unit: the new token at position pos goes to its pool
+// slot (the 16-bit row verbatim, or its e4m3 codes computed as
+// reshape_and_cache_fp8 computes them) and its merge record is staged --
+// app_v = the value row as attention sees it (the codes, widened, for FP8
+// pools: the V scale is applied with the output), app_m[jh] = the score of
+// query head kh * G + jh in log2 units.  The tiles of the unit stop before
+// pos, so the record enters the softmax exactly once, in the end-of-unit
+// merge.  Each lane holds D / 32 consecutive elements; every load is issued
+// before the first use (one round trip).  NH: query heads the kernel
+// instance serves per KV head (>= the group).
+template <typename T, bool kFp8, int D, int NH>
+__device__ __noinline__ void append_token(const DecodeParams &p, int s, int kh, int pos,
+                                          float *app_v, float *app_m, int lane)
+{
+    constexpr int E = D / 32;
+    using Raw = typename std::conditional<E == 4, uint2, uint32_t>::type;
+    auto f = [](T x) -> float {
+        if constexpr (std::is_same<T, __half>::value)
+            return __half2float(x);
+        else
+            return __bfloat162float(x);
+    };
+    const int G = p.group;
+    const size_t row = ((size_t)s * p.num_kv_heads + kh) * D + (size_t)lane * E;
+    const Raw kr = __ldg(reinterpret_cast<const Raw *>(static_cast<const T *>(p.new_key) + row));
+    const Raw vr = __ldg(reinterpret_cast<const Raw *>(static_cast<const T *>(p.new_value) + row));
+    const int32_t ent =
+        __ldg(p.block_tables + (size_t)s * p.max_blocks_per_seq + (pos >> p.block_shift));
+    Raw qr[NH];
+    const T *q0 = static_cast<const T *>(p.query) +
+                  ((size_t)s * p.num_heads + (size_t)kh * G) * D + (size_t)lane * E;
+#pragma unroll
+    for (int jh = 0; jh < NH; ++jh)
+        qr[jh] = jh < G ? __ldg(reinterpret_cast<const Raw *>(q0 + (size_t)jh * D)) : Raw{};
+    const T *ke = reinterpret_cast<const T *>(&kr);
+    const T *ve = reinterpret_cast<const T *>(&vr);
+    float kf[E], vf[E];
+    const bool ok = ent >= 0 && ent < p.num_blocks;
+    const int64_t slot = ok ? (int64_t)ent * p.block_size + (pos & (p.block_size - 1)) : -1;
+    const size_t elem = ((size_t)slot * p.num_kv_heads + kh) * D + (size_t)lane * E;
+    if constexpr (kFp8) {
+        static_assert(E == 4, "FP8 pools have head_dim 128");
+        const uint32_t kc = (uint32_t)f32x2_to_e4m3x2(f(ke[0]) * p.k_inv_scale,
+                                                      f(ke[1]) * p.k_inv_scale) |
+                            ((uint32_t)f32x2_to_e4m3x2(f(ke[2]) * p.k_inv_scale,
+                                                       f(ke[3]) * p.k_inv_scale) << 16);
+        const uint32_t vc = (uint32_t)f32x2_to_e4m3x2(f(ve[0]) * p.v_inv_scale,
+                                                      f(ve[1]) * p.v_inv_scale) |
+                            ((uint32_t)f32x2_to_e4m3x2(f(ve[2]) * p.v_inv_scale,
+                                                       f(ve[3]) * p.v_inv_scale) << 16);
+        if (ok) {
+            *reinterpret_cast<uint32_t *>(static_cast<uint8_t *>(p.key_cache) + elem) = kc;
+            *reinterpret_cast<uint32_t *>(static_cast<uint8_t *>(p.value_cache) + elem) = vc;
+        }
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const uint32_t kw = e4m3x2_to_f16x2((uint16_t)(kc >> (16 * h)));
+            const uint32_t vw = e4m3x2_to_f16x2((uint16_t)(vc >> (16 * h)));
+            kf[2 * h] = __half2float(__ushort_as_half((unsigned short)(kw & 0xffffu)));
+            kf[2 * h + 1] = __half2float(__ushort_as_half((unsigned short)(kw >> 16)));
+            vf[2 * h] = __half2float(__ushort_as_half((unsigned short)(vw & 0xffffu)));
+            vf[2 * h + 1] = __half2float(__ushort_as_half((unsigned short)(vw >> 16)));
+        }
+    } else {
+        if (ok) {
+            *reinterpret_cast<Raw *>(static_cast<T *>(p.key_cache) + elem) = kr;
+            *reinterpret_cast<Raw *>(static_cast<T *>(p.value_cache) + elem) = vr;
+        }
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+            kf[e] = f(ke[e]);
+            vf[e] = f(ve[e]);
+        }
+    }
+    if (lane == 0) {
+        if (!ok)
+            flag_error(p.error_word, PA_DEVERR_BLOCK_RANGE);
+        if (kh == 0 && p.slot_out != nullptr)
+            p.slot_out[s] = (int32_t)slot;
+    }
+#pragma unroll
+    for (int e = 0; e < E; ++e)
+        app_v[lane * E + e] = vf[e];
+#pragma unroll
+    for (int jh = 0; jh < NH; ++jh) {
+        if (jh >= G)
+            break;
+        const T *qe = reinterpret_cast<const T *>(&qr[jh]);
+        float dot = 0.f;
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+            // FP8 pools take the query in fp16, as the tiles' products do
+            const float q = kFp8 ? __half2float(__float2half_rn(f(qe[e]))) : f(qe[e]);
+            dot = fmaf(q, kf[e], dot);
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1)
+            dot += __shfl_xor_sync(kFull, dot, off);
+        if (lane == 0)
+            app_m[jh] = dot * p.scale_log2;
+    }
+}
+
+// Register budget for MINB resident CTAs of NW warps: an SM's 64K registers
+// sit in four 16K sub-partition files and each warp lives in one of them, so
+// the binding limit is the fullest file (ceil(NW * MINB / 4) warps).  The
+// thread count given to __launch_bounds__ is the one whose even split over
+// MINB CTAs yields that per-warp budget (the block itself is NW warps).
+constexpr int bound_threads(int NW, int MINB)
+{
+    return 128 * ((NW * MINB + 3) / 4) / MINB;
+}
+
 template <typename T, typename KV, int D, int NT, int NW, int NST, int MINB>
-__global__ void __launch_bounds__(NW * 32, MINB)
+__global__ void __launch_bounds__(bound_threads(NW, MINB), MINB)
     paged_decode_kernel(const __grid_constant__ DecodeParams p,
                         const __grid_constant__ CUtensorMap tmap_k,
                         const __grid_constant__ CUtensorMap tmap_v)
@@ -104,6 +221,9 @@ __global__ void __launch_bounds__(NW * 32, MINB)
     const int Hkv = p.num_kv_heads;
     const int G = p.group;
     const int P = p.part_tokens;
+    // Fused append: each sequence's last position holds the new token, whose
+    // K/V come from new_key/new_value; the tiles cover the positions before it.
+    const int napp = p.new_key != nullptr ? 1 : 0;
 
     int *ctx_s = reinterpret_cast<int *>(smem + L::kSeq);
     int *pref = ctx_s + S;
@@ -112,6 +232,8 @@ __global__ void __launch_bounds__(NW * 32, MINB)
     float *merge_o = reinterpret_cast<float *>(smem + L::kMergeO);
     float *merge_m = reinterpret_cast<float *>(smem + L::kMergeM);
     float *merge_l = reinterpret_cast<float *>(smem + L::kMergeL);
+    float *app_v = reinterpret_cast<float *>(smem + L::kAppV);
+    float *app_m = reinterpret_cast<float *>(smem + L::kAppM);
     auto bar_of = [&](int stage) { return sbase + L::kBars + (warp * NST + stage) * 8; };
     auto stage_of = [&](int stage) {
         return sbase + L::kStages + (warp * NST + stage) * L::kStageBytes;
@@ -168,6 +290,8 @@ __global__ void __launch_bounds__(NW * 32, MINB)
     for (int s = blockIdx.x; s < S; s += gridDim.x) {
         if (ctx_s[s] != 0)
             continue;
+        if (tid == 0 && p.new_key != nullptr && p.slot_out != nullptr)
+            p.slot_out[s] = -1;  // nothing to append
         uint4 *row = reinterpret_cast<uint4 *>(static_cast<T *>(p.out) +
                                                (size_t)s * p.num_heads * D);
         for (int i = tid; i < p.num_heads * D / 8; i += kThreads)
@@ -190,7 +314,7 @@ __global__ void __launch_bounds__(NW * 32, MINB)
         s = lo;
         j = q - pref[s];
         tok0 = start_s[s] + j * P;
-        const int tok_end = min(ctx_s[s], tok0 + P);
+        const int tok_end = min(ctx_s[s] - napp, tok0 + P);
         ntiles = (tok_end - tok0 + kTileTokens - 1) / kTileTokens;
     };
 
@@ -325,7 +449,9 @@ __global__ void __launch_bounds__(NW * 32, MINB)
     for (int u = blockIdx.x; u < total_units; u += gridDim.x) {
         int s, kh, j, tok0, ntiles;
         decode_unit(u, s, kh, j, tok0, ntiles);
-        const int tok_end = min(ctx_s[s], tok0 + P);
+        const int tok_end = min(ctx_s[s] - napp, tok0 + P);
+        // fused append: the sequence's last unit also takes the new token
+        const bool app = napp != 0 && tok0 + P >= ctx_s[s];
         const int nparts = pref[s + 1] - pref[s];
         // the first partials belong to the prefix pass
         const int pbase = prefix_partitions(start_s[s], P);
@@ -340,6 +466,10 @@ __global__ void __launch_bounds__(NW * 32, MINB)
             for (int mt = 0; mt < KT; ++mt)
                 o[mt][nt][0] = o[mt][nt][1] = o[mt][nt][2] = o[mt][nt][3] = 0.f;
         }
+        // the new token counts as tile ntiles of the round-robin deal: its
+        // warp is one with a tile fewer than the others (or the first)
+        if (app && warp == ntiles % NW)
+            append_token<T, kFp8, D, kHeads>(p, s, kh, ctx_s[s] - 1, app_v, app_m, lane);
 
         for (int tile = warp; tile < ntiles; tile += NW) {
             const int stage = consumed % NST;
@@ -568,6 +698,8 @@ __global__ void __launch_bounds__(NW * 32, MINB)
 #pragma unroll
             for (int w = 0; w < NW; ++w)
                 mmax = fmaxf(mmax, merge_m[w * kHeads + jh]);
+            if (app)
+                mmax = fmaxf(mmax, app_m[jh]);
             const float mu = mmax == -INFINITY ? 0.f : mmax;
             float lsum = 0.f;
             float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
@@ -580,6 +712,14 @@ __global__ void __launch_bounds__(NW * 32, MINB)
                 const float4 x0 = src[0], x1 = src[1];
                 acc[0] += wgt * x0.x; acc[1] += wgt * x0.y; acc[2] += wgt * x0.z; acc[3] += wgt * x0.w;
                 acc[4] += wgt * x1.x; acc[5] += wgt * x1.y; acc[6] += wgt * x1.z; acc[7] += wgt * x1.w;
+            }
+            if (app) {
+                // the new token: m = its score, l = 1, o = its value row
+                const float wgt = exp2f(app_m[jh] - mu);
+                lsum += wgt;
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    acc[e] += wgt * app_v[d0 + e];
             }
             const float inv = p.out_scale / lsum;
             const size_t h = (size_t)kh * G + jh;
@@ -631,7 +771,7 @@ __global__ void __launch_bounds__(NW * 32, MINB)
 #define PA_DECODE_STAGES 2
 #endif
 #ifndef PA_DECODE_MINB
-#define PA_DECODE_MINB 1
+#define PA_DECODE_MINB 2
 #endif
 #ifndef PA_DECODE_WARPS_FP8
 #define PA_DECODE_WARPS_FP8 4
@@ -766,6 +906,84 @@ extern "C" size_t pa_decode_workspace_bytes(int num_seqs, int num_heads, int num
     return workspace_layout(num_seqs, num_heads, head_dim, parts).total;
 }
 
+// 16-bit pools: tensor maps, then the kernel instance for (dtype, d, group).
+static pa_status run_decode16(const DecodeParams &prm, const void *key_cache,
+                              const void *value_cache, pa_dtype dtype, int num_seqs,
+                              int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                              void *stream)
+{
+    CUtensorMap mk, mv;
+    if (!encode_pool_map(&mk, key_cache, dtype, num_blocks, block_size, num_kv_heads,
+                         head_dim) ||
+        !encode_pool_map(&mv, value_cache, dtype, num_blocks, block_size, num_kv_heads,
+                         head_dim))
+        return PA_ERR_CUDA;
+
+    const long long max_units = (long long)num_seqs * num_kv_heads * prm.max_parts;
+    cudaStream_t st = as_stream(stream);
+    const bool bf = dtype == PA_BF16;
+    const bool wide = prm.group > 8;
+    using B16 = __nv_bfloat16;
+    using F16 = __half;
+    if (head_dim == 128) {
+        if (bf)
+            return wide ? launch_decode<B16, B16, 128, 2>(prm, mk, mv, st, max_units)
+                        : launch_decode<B16, B16, 128, 1>(prm, mk, mv, st, max_units);
+        return wide ? launch_decode<F16, F16, 128, 2>(prm, mk, mv, st, max_units)
+                    : launch_decode<F16, F16, 128, 1>(prm, mk, mv, st, max_units);
+    }
+    if (bf)
+        return wide ? launch_decode<B16, B16, 64, 2>(prm, mk, mv, st, max_units)
+                    : launch_decode<B16, B16, 64, 1>(prm, mk, mv, st, max_units);
+    return wide ? launch_decode<F16, F16, 64, 2>(prm, mk, mv, st, max_units)
+                : launch_decode<F16, F16, 64, 1>(prm, mk, mv, st, max_units);
+}
+
+// FP8 (e4m3) pools, head_dim 128: scores use the K codes (the K scale folded
+// into the exponent's scale), outputs and partials get the V scale.
+static pa_status run_decode_fp8(DecodeParams &prm, const void *key_cache,
+                                const void *value_cache, pa_dtype dtype, int num_seqs,
+                                int num_kv_heads, int block_size, int num_blocks, float scale,
+                                float k_scale, float v_scale, void *stream)
+{
+    prm.scale_log2 = scale * k_scale * kLog2e;
+    prm.out_scale = v_scale;
+    CUtensorMap mk, mv;
+    if (!encode_pool_map(&mk, key_cache, PA_FP8_E4M3, num_blocks, block_size, num_kv_heads,
+                         128) ||
+        !encode_pool_map(&mv, value_cache, PA_FP8_E4M3, num_blocks, block_size, num_kv_heads,
+                         128))
+        return PA_ERR_CUDA;
+    const long long max_units = (long long)num_seqs * num_kv_heads * prm.max_parts;
+    cudaStream_t st = as_stream(stream);
+    const bool wide = prm.group > 8;
+    using U8 = uint8_t;
+    if (dtype == PA_BF16)
+        return wide ? launch_decode<__nv_bfloat16, U8, 128, 2>(prm, mk, mv, st, max_units)
+                    : launch_decode<__nv_bfloat16, U8, 128, 1>(prm, mk, mv, st, max_units);
+    return wide ? launch_decode<__half, U8, 128, 2>(prm, mk, mv, st, max_units)
+                : launch_decode<__half, U8, 128, 1>(prm, mk, mv, st, max_units);
+}
+
+static bool valid_fp8_scales(float k_scale, float v_scale)
+{
+    return std::isfinite(k_scale) && std::isfinite(v_scale) && k_scale > 0.f && v_scale > 0.f;
+}
+
+// The fused append's arguments: both new-row buffers, 16-byte aligned.
+static pa_status set_append(DecodeParams *prm, void *key_cache, void *value_cache,
+                            const void *new_key, const void *new_value, int32_t *slot_mapping)
+{
+    if (!new_key || !new_value || !aligned16(new_key) || !aligned16(new_value))
+        return PA_ERR_INVALID_ARG;
+    prm->key_cache = key_cache;
+    prm->value_cache = value_cache;
+    prm->new_key = new_key;
+    prm->new_value = new_value;
+    prm->slot_out = slot_mapping;
+    return PA_OK;
+}
+
 extern "C" pa_status pa_decode_attention(void *out, const void *query, const void *key_cache,
                                          const void *value_cache, const int32_t *block_tables,
                                          int max_blocks_per_seq, const int32_t *context_lens,
@@ -785,34 +1003,33 @@ extern "C" pa_status pa_decode_attention(void *out, const void *query, const voi
         error_word);
     if (ok != PA_OK || num_seqs == 0)
         return ok;
-    const int group = prm.group;
-    const int parts = prm.max_parts;
+    return run_decode16(prm, key_cache, value_cache, dtype, num_seqs, num_kv_heads, head_dim,
+                        block_size, num_blocks, stream);
+}
 
-    CUtensorMap mk, mv;
-    if (!encode_pool_map(&mk, key_cache, dtype, num_blocks, block_size, num_kv_heads,
-                         head_dim) ||
-        !encode_pool_map(&mv, value_cache, dtype, num_blocks, block_size, num_kv_heads,
-                         head_dim))
-        return PA_ERR_CUDA;
-
-    const long long max_units = (long long)num_seqs * num_kv_heads * parts;
-    cudaStream_t st = as_stream(stream);
-    const bool bf = dtype == PA_BF16;
-    const bool wide = group > 8;
-    using B16 = __nv_bfloat16;
-    using F16 = __half;
-    if (head_dim == 128) {
-        if (bf)
-            return wide ? launch_decode<B16, B16, 128, 2>(prm, mk, mv, st, max_units)
-                        : launch_decode<B16, B16, 128, 1>(prm, mk, mv, st, max_units);
-        return wide ? launch_decode<F16, F16, 128, 2>(prm, mk, mv, st, max_units)
-                    : launch_decode<F16, F16, 128, 1>(prm, mk, mv, st, max_units);
-    }
-    if (bf)
-        return wide ? launch_decode<B16, B16, 64, 2>(prm, mk, mv, st, max_units)
-                    : launch_decode<B16, B16, 64, 1>(prm, mk, mv, st, max_units);
-    return wide ? launch_decode<F16, F16, 64, 2>(prm, mk, mv, st, max_units)
-                : launch_decode<F16, F16, 64, 1>(prm, mk, mv, st, max_units);
+extern "C" pa_status pa_decode_attention_append(
+    void *out, const void *query, void *key_cache, void *value_cache, const void *new_key,
+    const void *new_value, int32_t *slot_mapping, const int32_t *block_tables,
+    int max_blocks_per_seq, const int32_t *context_lens, int max_context_len, int num_seqs,
+    int num_heads, int num_kv_heads, int head_dim, int block_size, int num_blocks, float scale,
+    int partition_size, void *workspace, size_t workspace_bytes, pa_dtype dtype,
+    int32_t *error_word, void *stream)
+{
+    if (dtype != PA_F16 && dtype != PA_BF16)
+        return PA_ERR_INVALID_ARG;
+    DecodeParams prm{};
+    pa_status ok = prepare_decode(&prm, out, query, key_cache, value_cache, block_tables,
+                                  max_blocks_per_seq, context_lens, max_context_len, num_seqs,
+                                  num_heads, num_kv_heads, head_dim, block_size, num_blocks,
+                                  scale, partition_size, workspace, workspace_bytes,
+                                  error_word);
+    if (ok != PA_OK || num_seqs == 0)
+        return ok;
+    ok = set_append(&prm, key_cache, value_cache, new_key, new_value, slot_mapping);
+    if (ok != PA_OK)
+        return ok;
+    return run_decode16(prm, key_cache, value_cache, dtype, num_seqs, num_kv_heads, head_dim,
+                        block_size, num_blocks, stream);
 }
 
 extern "C" pa_status pa_decode_attention_fp8(
@@ -823,8 +1040,7 @@ extern "C" pa_status pa_decode_attention_fp8(
     int partition_size, void *workspace, size_t workspace_bytes, pa_dtype dtype,
     int32_t *error_word, void *stream)
 {
-    if ((dtype != PA_F16 && dtype != PA_BF16) || !std::isfinite(k_scale) ||
-        !std::isfinite(v_scale) || k_scale <= 0.f || v_scale <= 0.f)
+    if ((dtype != PA_F16 && dtype != PA_BF16) || !valid_fp8_scales(k_scale, v_scale))
         return PA_ERR_INVALID_ARG;
     DecodeParams prm{};
     const pa_status ok = prepare_decode(
@@ -836,26 +1052,38 @@ extern "C" pa_status pa_decode_attention_fp8(
         return ok;
     if (head_dim != 128)
         return PA_ERR_UNSUPPORTED;
-    // scores use the K codes: fold the K scale into the exponent's scale;
-    // outputs (and partials) get the V scale
-    prm.scale_log2 = scale * k_scale * kLog2e;
-    prm.out_scale = v_scale;
+    return run_decode_fp8(prm, key_cache, value_cache, dtype, num_seqs, num_kv_heads,
+                          block_size, num_blocks, scale, k_scale, v_scale, stream);
+}
 
-    CUtensorMap mk, mv;
-    if (!encode_pool_map(&mk, key_cache, PA_FP8_E4M3, num_blocks, block_size, num_kv_heads,
-                         head_dim) ||
-        !encode_pool_map(&mv, value_cache, PA_FP8_E4M3, num_blocks, block_size, num_kv_heads,
-                         head_dim))
-        return PA_ERR_CUDA;
-    const long long max_units = (long long)num_seqs * num_kv_heads * prm.max_parts;
-    cudaStream_t st = as_stream(stream);
-    const bool wide = prm.group > 8;
-    using U8 = uint8_t;
-    if (dtype == PA_BF16)
-        return wide ? launch_decode<__nv_bfloat16, U8, 128, 2>(prm, mk, mv, st, max_units)
-                    : launch_decode<__nv_bfloat16, U8, 128, 1>(prm, mk, mv, st, max_units);
-    return wide ? launch_decode<__half, U8, 128, 2>(prm, mk, mv, st, max_units)
-                : launch_decode<__half, U8, 128, 1>(prm, mk, mv, st, max_units);
+extern "C" pa_status pa_decode_attention_append_fp8(
+    void *out, const void *query, void *key_cache, void *value_cache, const void *new_key,
+    const void *new_value, int32_t *slot_mapping, const int32_t *block_tables,
+    int max_blocks_per_seq, const int32_t *context_lens, int max_context_len, int num_seqs,
+    int num_heads, int num_kv_heads, int head_dim, int block_size, int num_blocks, float scale,
+    float k_scale, float v_scale, int partition_size, void *workspace, size_t workspace_bytes,
+    pa_dtype dtype, int32_t *error_word, void *stream)
+{
+    if ((dtype != PA_F16 && dtype != PA_BF16) || !valid_fp8_scales(k_scale, v_scale))
+        return PA_ERR_INVALID_ARG;
+    DecodeParams prm{};
+    pa_status ok = prepare_decode(&prm, out, query, key_cache, value_cache, block_tables,
+                                  max_blocks_per_seq, context_lens, max_context_len, num_seqs,
+                                  num_heads, num_kv_heads, head_dim, block_size, num_blocks,
+                                  scale, partition_size, workspace, workspace_bytes,
+                                  error_word);
+    if (ok != PA_OK || num_seqs == 0)
+        return ok;
+    if (head_dim != 128)
+        return PA_ERR_UNSUPPORTED;
+    ok = set_append(&prm, key_cache, value_cache, new_key, new_value, slot_mapping);
+    if (ok != PA_OK)
+        return ok;
+    // the codes' contract: e4m3(x * (1 / scale)), the reciprocal taken in fp32
+    prm.k_inv_scale = 1.0f / k_scale;
+    prm.v_inv_scale = 1.0f / v_scale;
+    return run_decode_fp8(prm, key_cache, value_cache, dtype, num_seqs, num_kv_heads,
+                          block_size, num_blocks, scale, k_scale, v_scale, stream);
 }
 
 extern "C" size_t pa_prefix_plan_ints(int num_seqs, int num_groups, int num_members)

@@ -42,6 +42,18 @@ struct DecodeParams {
     int concurrent;   // 1: the kernel before it on the stream (the shared-prefix
                       // pass) writes nothing this pass reads -- run alongside it
                       // and wait for it only before finishing
+    // Decode step with the append fused in (null new_key: attention only).
+    // Sequence s's new token sits at position context_lens[s] - 1; its rows
+    // new_key/new_value [num_seqs][num_kv_heads][head_dim] (16-bit, type T)
+    // are written to the pools at that position's slot (as e4m3 codes times
+    // k_inv_scale / v_inv_scale for FP8 pools) and attended from the copy in
+    // shared memory; slot_out (optional) receives each sequence's slot.
+    void *key_cache;
+    void *value_cache;
+    const void *new_key;
+    const void *new_value;
+    int32_t *slot_out;
+    float k_inv_scale, v_inv_scale;
 };
 
 // Clamped context length (same rule in both kernels).

@@ -13,6 +13,10 @@ Batching" §1.5, §1.6, §2.4, §2.5):
      prefix plan, each group's shared prefix read once), or, for a prefill
      step, each chunk row over the context up to its own position.
 
+A decode step with one new token per sequence runs 3 first and then 1, 2
+and 4 in one call (the append fused into the attention pass), the order in
+which the engine copies a shared block before writing into it.
+
 Torch provides device memory and the stream; every step above is a kernel
 of ``libpaged_attention.so``.
 """
@@ -91,6 +95,18 @@ class DecodeStep:
         else:
             self.workspace = B.alloc_workspace(w.S, w.H, w.Hkv, w.D, self.max_context_len,
                                                self.partition_size, device=self.device)
+        # Decode with one new token per sequence, at its last position, and
+        # that position in the same block before and after copy-on-write: the
+        # append runs inside the attention call.
+        self.fused_append = False
+        if not w.prefill and not self.cascade and w.new_seq.shape[0] == w.S:
+            last = w.context_lens.astype(np.int64) - 1
+            if (np.array_equal(w.new_seq, np.arange(w.S)) and
+                    np.array_equal(w.new_pos, last) and bool((last >= 0).all())):
+                rows = np.arange(w.S)
+                lb = last // w.bs
+                self.fused_append = bool(np.array_equal(w.block_tables[rows, lb],
+                                                        w.step_block_tables[rows, lb]))
         if build_pools:
             self.write_history()
 
@@ -176,20 +192,46 @@ class DecodeStep:
                                     self.value_cache, self.kv_scale, self.kv_scale,
                                     error_word=self.error_word, stream=stream)
 
+    def append_attention(self, stream=None, partition_size: Optional[int] = None) -> None:
+        """Steps 1, 2 and 4 of a decode step in one call: each sequence's new
+        token goes to the pools inside the attention pass."""
+        if not self.fused_append:
+            raise RuntimeError("this step's new tokens are not one per sequence at its end")
+        w = self.w
+        P = self.partition_size if partition_size is None else partition_size
+        ws = self.workspace
+        if P != self.partition_size:
+            ws = B.alloc_workspace(w.S, w.H, w.Hkv, w.D, self.max_context_len, P,
+                                   device=self.device)
+        B.pa_decode_attention_append(self.out, self.query, self.key_cache, self.value_cache,
+                                     self.new_key, self.new_value, self.step_block_tables,
+                                     self.context_lens, self.max_context_len, w.scale, P, ws,
+                                     slot_mapping=self.slots, k_scale=self.kv_scale,
+                                     v_scale=self.kv_scale, error_word=self.error_word,
+                                     stream=stream)
+
     def run(self, stream=None) -> torch.Tensor:
-        """One whole decode step; returns the attention output tensor."""
+        """One whole decode step; returns the attention output tensor.  A
+        decode step whose new tokens are one per sequence copies its
+        copy-on-write blocks first and then appends and attends in one call;
+        other steps write, copy, then attend."""
+        if self.fused_append:
+            self.copy_blocks(stream)
+            self.append_attention(stream)
+            return self.out
         self.slot_mapping_and_cache(stream)
         self.copy_blocks(stream)
         self.attention(stream)
         return self.out
 
     def launches_per_step(self) -> int:
-        """Kernels one run() launches: slot mapping with the cache write, block
-        copy (when the step has copy-on-write pairs), the attention pass, the
+        """Kernels one run() launches: slot mapping with the cache write (unless
+        fused into the attention pass), block copy (when the step has
+        copy-on-write pairs), the attention pass, the
         shared-prefix pass (prefix-aware decode with at least one group), and
         the reduce (when some context spans more than one partition, or a
         prefix group exists)."""
-        n = 2 + (1 if self.cow_pairs is not None else 0)
+        n = (1 if self.fused_append else 2) + (1 if self.cow_pairs is not None else 0)
         if self.cascade and self.num_groups > 0:
             n += 2
         elif self.workspace is not None and not self.cascade:

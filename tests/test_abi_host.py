@@ -127,6 +127,31 @@ def test_fused_cache_argument_checks(B):
     assert f8(*ok8[:3], None, *ok8[4:]) == B.PA_ERR_INVALID_ARG
 
 
+def test_append_argument_checks(B):
+    """pa_decode_attention_append(_fp8): the decode checks, then the new-row
+    buffers, all before any launch."""
+    L = B.lib()
+    f = L.pa_decode_attention_append
+    f8 = L.pa_decode_attention_append_fp8
+    # (out, query, kc, vc, new_key, new_value, slots, tables, mb, ctx, maxctx, S, H, Hkv,
+    #  d, bs, N, scale, P, ws, ws_bytes, dtype, err, stream)
+    ok = (FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, 4, FAKE, 64, 2, 8, 2, 128, 16, 8,
+          0.1, 0, None, 0, 1, None, None)
+    assert f(*ok[:11], 0, *ok[12:]) == B.PA_OK                        # no sequences
+    assert f(*ok[:4], None, *ok[5:]) == B.PA_ERR_INVALID_ARG          # no new keys
+    assert f(*ok[:5], None, *ok[6:]) == B.PA_ERR_INVALID_ARG          # no new values
+    assert f(*ok[:4], FAKE_ODD, *ok[5:]) == B.PA_ERR_INVALID_ARG      # unaligned rows
+    assert f(*ok[:21], 7, *ok[22:]) == B.PA_ERR_INVALID_ARG           # not a 16-bit type
+    assert f(*ok[:14], 96, *ok[15:]) == B.PA_ERR_UNSUPPORTED          # head_dim 96
+    assert f(*ok[:18], 16, *ok[19:]) == B.PA_ERR_WORKSPACE            # split, no workspace
+    ok8 = ok[:18] + (0.5, 0.5) + ok[18:]
+    assert f8(*ok8[:11], 0, *ok8[12:]) == B.PA_OK
+    assert f8(*ok8[:18], 0.0, 0.5, *ok8[20:]) == B.PA_ERR_INVALID_ARG  # zero K scale
+    assert f8(*ok8[:18], 0.5, float("nan"), *ok8[20:]) == B.PA_ERR_INVALID_ARG
+    assert f8(*ok8[:14], 64, *ok8[15:]) == B.PA_ERR_UNSUPPORTED         # FP8: d 128 only
+    assert f8(*ok8[:5], None, *ok8[6:]) == B.PA_ERR_INVALID_ARG
+
+
 def test_workspace_layout_sizes(B):
     L = B.lib()
     a256 = lambda x: (x + 255) // 256 * 256  # noqa: E731
