@@ -677,6 +677,9 @@ def run_ours(args):
     if st.cascade:
         kernel = ("pa_decode_attention_cascade (paged_decode_kernel + paged_mq_kernel "
                   "prefix pass + paged_reduce_kernel)")
+        if st.fused_append:
+            kernel = ("pa_decode_attention_cascade_append (paged_decode_kernel with the new "
+                      "tokens' append + paged_mq_kernel prefix pass + paged_reduce_kernel)")
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": per_step * 1e3, "higher_is_better": True,

@@ -416,6 +416,28 @@ PA_API pa_status pa_decode_attention_cascade(void *out, const void *query, const
                                              int32_t *error_word, void *stream);
 
 /*
+ * pa_decode_attention_cascade_append -- pa_decode_attention_cascade with the
+ * decode step's append fused into its partition pass, as
+ * pa_decode_attention_append does for pa_decode_attention: new_key /
+ * new_value [num_seqs][num_kv_heads][head_dim] (dtype) are written at the
+ * slot of position context_lens[s] - 1 (slot_mapping, optional, receives the
+ * slots) and attended.  Every member's shared prefix must end before its new
+ * token (prefix_plan's seq_start[s] < context_lens[s], as
+ * pa_plan_prefix_groups plans it; otherwise PA_DEVERR_PREFIX_PLAN), so the
+ * block written is the sequence's own and the prefix pass never reads it.
+ * With num_groups == 0 this is pa_decode_attention_append.  Other arguments,
+ * workspace (pa_cascade_workspace_bytes) and errors as
+ * pa_decode_attention_cascade.
+ */
+PA_API pa_status pa_decode_attention_cascade_append(
+    void *out, const void *query, void *key_cache, void *value_cache, const void *new_key,
+    const void *new_value, int32_t *slot_mapping, const int32_t *block_tables,
+    int max_blocks_per_seq, const int32_t *context_lens, int max_context_len, int num_seqs,
+    int num_heads, int num_kv_heads, int head_dim, int block_size, int num_blocks, float scale,
+    const int32_t *prefix_plan, int num_groups, int num_members, int partition_size,
+    void *workspace, size_t workspace_bytes, pa_dtype dtype, int32_t *error_word, void *stream);
+
+/*
  * pa_decode_attention_noalloc -- no counterpart on the pages: an addition
  * for callers that may not allocate device memory on their decode path (a
  * plugin whose host engine owns all device memory through its own pool, a

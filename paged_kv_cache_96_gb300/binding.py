@@ -83,6 +83,9 @@ def _load() -> ctypes.CDLL:
         "pa_decode_attention_cascade": (i32, [P, P, P, P, P, i32, P, i32, i32, i32, i32, i32,
                                               i32, i32, f32, P, i32, i32, i32, P, sz, i32, P,
                                               P]),
+        "pa_decode_attention_cascade_append": (i32, [P, P, P, P, P, P, P, P, i32, P, i32,
+                                                     i32, i32, i32, i32, i32, i32, f32, P,
+                                                     i32, i32, i32, P, sz, i32, P, P]),
         "pa_bm_create": (i32, [i32, i32, i32, P]),
         "pa_bm_destroy": (None, [P]),
         "pa_bm_num_free_blocks": (i32, [P]),
@@ -475,6 +478,46 @@ def pa_decode_attention_cascade(out: torch.Tensor, query: torch.Tensor,
         _dev(out, "out", query.dtype), _dev(query, "query", key_cache.dtype),
         _dev(key_cache, "key_cache"), _dev(value_cache, "value_cache", key_cache.dtype),
         _dev(block_tables, "block_tables", torch.int32), MB,
+        _dev(context_lens, "context_lens", torch.int32), int(max_context_len), S, H, Hkv,
+        d, bs, N, float(scale), _dev(prefix_plan, "prefix_plan", torch.int32),
+        int(num_groups), int(num_members), int(partition_size), ws_ptr, ws_bytes,
+        _dtype_code(key_cache), _opt(error_word, "error_word"), _stream(stream)))
+
+
+def pa_decode_attention_cascade_append(out: torch.Tensor, query: torch.Tensor,
+                                       key_cache: torch.Tensor, value_cache: torch.Tensor,
+                                       new_key: torch.Tensor, new_value: torch.Tensor,
+                                       block_tables: torch.Tensor, context_lens: torch.Tensor,
+                                       max_context_len: int, scale: float,
+                                       prefix_plan: torch.Tensor, num_groups: int,
+                                       num_members: int, partition_size: int,
+                                       workspace: torch.Tensor,
+                                       slot_mapping: Optional[torch.Tensor] = None,
+                                       error_word: Optional[torch.Tensor] = None,
+                                       stream=None) -> None:
+    """Prefix-aware decode step in one call: each sequence's new token
+    (new_key / new_value [S, Hkv, d], position context_lens[s] - 1) written
+    to the pools and attended, each planned group's shared prefix read once."""
+    S, H, d = query.shape
+    N, bs, Hkv, d2 = key_cache.shape
+    MB = block_tables.shape[1]
+    if d != d2 or out.shape != query.shape:
+        raise ValueError("shape mismatch")
+    if new_key.shape != (S, Hkv, d) or new_value.shape != new_key.shape:
+        raise ValueError("new_key / new_value must be [num_seqs, num_kv_heads, head_dim]")
+    if slot_mapping is not None and slot_mapping.shape[0] != S:
+        raise ValueError("one slot per sequence expected")
+    if key_cache.dtype == torch.uint8:
+        raise TypeError("FP8 pools are not supported by the prefix-aware decode")
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not None:
+        ws_ptr = _dev(workspace, "workspace")
+        ws_bytes = workspace.numel() * workspace.element_size()
+    _check("pa_decode_attention_cascade_append", _lib.pa_decode_attention_cascade_append(
+        _dev(out, "out", query.dtype), _dev(query, "query", key_cache.dtype),
+        _dev(key_cache, "key_cache"), _dev(value_cache, "value_cache", key_cache.dtype),
+        _dev(new_key, "new_key", key_cache.dtype), _dev(new_value, "new_value", key_cache.dtype),
+        _opt(slot_mapping, "slot_mapping"), _dev(block_tables, "block_tables", torch.int32), MB,
         _dev(context_lens, "context_lens", torch.int32), int(max_context_len), S, H, Hkv,
         d, bs, N, float(scale), _dev(prefix_plan, "prefix_plan", torch.int32),
         int(num_groups), int(num_members), int(partition_size), ws_ptr, ws_bytes,

@@ -262,6 +262,10 @@ __global__ void __launch_bounds__(bound_threads(NW, MINB), MINB)
         const int c = clamp_context(p, s, blockIdx.x == 0);
         ctx_s[s] = c;
         start_s[s] = seq_start_of(p, s, c);
+        // with the append fused in, a shared prefix must end before the new
+        // token (which is then in a block of the sequence's own)
+        if (napp != 0 && c > 0 && start_s[s] >= c && blockIdx.x == 0)
+            flag_error(p.error_word, PA_DEVERR_PREFIX_PLAN);
     }
     __syncthreads();
     if (warp == 0) {
@@ -1104,35 +1108,52 @@ extern "C" size_t pa_cascade_workspace_bytes(int num_seqs, int num_heads, int nu
     return workspace_layout(num_seqs, num_heads, head_dim, parts).total;
 }
 
-extern "C" pa_status pa_decode_attention_cascade(
-    void *out, const void *query, const void *key_cache, const void *value_cache,
-    const int32_t *block_tables, int max_blocks_per_seq, const int32_t *context_lens,
-    int max_context_len, int num_seqs, int num_heads, int num_kv_heads, int head_dim,
-    int block_size, int num_blocks, float scale, const int32_t *prefix_plan, int num_groups,
-    int num_members, int partition_size, void *workspace, size_t workspace_bytes,
-    pa_dtype dtype, int32_t *error_word, void *stream)
+// Prefix-aware decode; with new_key non-null, the decode step's append fused
+// into its partition pass (the prefix pass reads only shared blocks, which
+// never hold a new token).
+static pa_status run_cascade(void *out, const void *query, void *key_cache, void *value_cache,
+                             const void *new_key, const void *new_value, int32_t *slot_mapping,
+                             const int32_t *block_tables, int max_blocks_per_seq,
+                             const int32_t *context_lens, int max_context_len, int num_seqs,
+                             int num_heads, int num_kv_heads, int head_dim, int block_size,
+                             int num_blocks, float scale, const int32_t *prefix_plan,
+                             int num_groups, int num_members, int partition_size,
+                             void *workspace, size_t workspace_bytes, pa_dtype dtype,
+                             int32_t *error_word, void *stream)
 {
     if (dtype != PA_F16 && dtype != PA_BF16)
         return dtype == PA_FP8_E4M3 ? PA_ERR_UNSUPPORTED : PA_ERR_INVALID_ARG;
     if (num_groups < 0 || num_members < 0 || (num_groups > 0 && num_members < 2 * num_groups) ||
         !(scale > 0.f))
         return PA_ERR_INVALID_ARG;
-    if (num_groups == 0)
-        return pa_decode_attention(out, query, key_cache, value_cache, block_tables,
-                                   max_blocks_per_seq, context_lens, max_context_len, num_seqs,
-                                   num_heads, num_kv_heads, head_dim, block_size, num_blocks,
-                                   scale, partition_size, workspace, workspace_bytes, dtype,
-                                   error_word, stream);
+    if (num_groups == 0) {
+        if (new_key == nullptr)
+            return pa_decode_attention(out, query, key_cache, value_cache, block_tables,
+                                       max_blocks_per_seq, context_lens, max_context_len,
+                                       num_seqs, num_heads, num_kv_heads, head_dim, block_size,
+                                       num_blocks, scale, partition_size, workspace,
+                                       workspace_bytes, dtype, error_word, stream);
+        return pa_decode_attention_append(
+            out, query, key_cache, value_cache, new_key, new_value, slot_mapping, block_tables,
+            max_blocks_per_seq, context_lens, max_context_len, num_seqs, num_heads,
+            num_kv_heads, head_dim, block_size, num_blocks, scale, partition_size, workspace,
+            workspace_bytes, dtype, error_word, stream);
+    }
     DecodeParams prm{};
-    const pa_status ok = prepare_decode(
-        &prm, out, query, key_cache, value_cache, block_tables, max_blocks_per_seq,
-        context_lens, max_context_len, num_seqs, num_heads, num_kv_heads, head_dim,
-        block_size, num_blocks, scale, partition_size, workspace, workspace_bytes,
-        error_word);
+    pa_status ok = prepare_decode(&prm, out, query, key_cache, value_cache, block_tables,
+                                  max_blocks_per_seq, context_lens, max_context_len, num_seqs,
+                                  num_heads, num_kv_heads, head_dim, block_size, num_blocks,
+                                  scale, partition_size, workspace, workspace_bytes,
+                                  error_word);
     if (ok != PA_OK || num_seqs == 0)
         return ok;
     if (prefix_plan == nullptr)
         return PA_ERR_INVALID_ARG;
+    if (new_key != nullptr) {
+        ok = set_append(&prm, key_cache, value_cache, new_key, new_value, slot_mapping);
+        if (ok != PA_OK)
+            return ok;
+    }
     // the shared prefix [0, L) and the own tokens [L, ctx) are each cut into
     // partitions of part_tokens: ceil(L / P) + ceil((ctx - L) / P) <=
     // ceil(ctx / P) + 1 partials per (sequence, head)
@@ -1203,4 +1224,37 @@ extern "C" pa_status pa_decode_attention_cascade(
                     : launch_decode<B16, B16, 64, 1>(prm, mk, mv, st, max_units, &pp);
     return wide ? launch_decode<F16, F16, 64, 2>(prm, mk, mv, st, max_units, &pp)
                 : launch_decode<F16, F16, 64, 1>(prm, mk, mv, st, max_units, &pp);
+}
+
+extern "C" pa_status pa_decode_attention_cascade(
+    void *out, const void *query, const void *key_cache, const void *value_cache,
+    const int32_t *block_tables, int max_blocks_per_seq, const int32_t *context_lens,
+    int max_context_len, int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+    int block_size, int num_blocks, float scale, const int32_t *prefix_plan, int num_groups,
+    int num_members, int partition_size, void *workspace, size_t workspace_bytes,
+    pa_dtype dtype, int32_t *error_word, void *stream)
+{
+    return run_cascade(out, query, const_cast<void *>(key_cache),
+                       const_cast<void *>(value_cache), nullptr, nullptr, nullptr,
+                       block_tables, max_blocks_per_seq, context_lens, max_context_len,
+                       num_seqs, num_heads, num_kv_heads, head_dim, block_size, num_blocks,
+                       scale, prefix_plan, num_groups, num_members, partition_size, workspace,
+                       workspace_bytes, dtype, error_word, stream);
+}
+
+extern "C" pa_status pa_decode_attention_cascade_append(
+    void *out, const void *query, void *key_cache, void *value_cache, const void *new_key,
+    const void *new_value, int32_t *slot_mapping, const int32_t *block_tables,
+    int max_blocks_per_seq, const int32_t *context_lens, int max_context_len, int num_seqs,
+    int num_heads, int num_kv_heads, int head_dim, int block_size, int num_blocks, float scale,
+    const int32_t *prefix_plan, int num_groups, int num_members, int partition_size,
+    void *workspace, size_t workspace_bytes, pa_dtype dtype, int32_t *error_word, void *stream)
+{
+    if (num_seqs > 0 && (new_key == nullptr || new_value == nullptr))
+        return PA_ERR_INVALID_ARG;
+    return run_cascade(out, query, key_cache, value_cache, new_key, new_value, slot_mapping,
+                       block_tables, max_blocks_per_seq, context_lens, max_context_len,
+                       num_seqs, num_heads, num_kv_heads, head_dim, block_size, num_blocks,
+                       scale, prefix_plan, num_groups, num_members, partition_size, workspace,
+                       workspace_bytes, dtype, error_word, stream);
 }

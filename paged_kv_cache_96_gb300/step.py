@@ -99,7 +99,7 @@ class DecodeStep:
         # that position in the same block before and after copy-on-write: the
         # append runs inside the attention call.
         self.fused_append = False
-        if not w.prefill and not self.cascade and w.new_seq.shape[0] == w.S:
+        if not w.prefill and w.new_seq.shape[0] == w.S:
             last = w.context_lens.astype(np.int64) - 1
             if (np.array_equal(w.new_seq, np.arange(w.S)) and
                     np.array_equal(w.new_pos, last) and bool((last >= 0).all())):
@@ -200,6 +200,16 @@ class DecodeStep:
         w = self.w
         P = self.partition_size if partition_size is None else partition_size
         ws = self.workspace
+        if self.cascade:
+            if P != self.partition_size:
+                n = B.pa_cascade_workspace_bytes(w.S, w.H, w.Hkv, w.D, self.max_context_len, P)
+                ws = torch.zeros(n, dtype=torch.uint8, device=self.device)
+            B.pa_decode_attention_cascade_append(
+                self.out, self.query, self.key_cache, self.value_cache, self.new_key,
+                self.new_value, self.step_block_tables, self.context_lens, self.max_context_len,
+                w.scale, self.plan, self.num_groups, self.num_members, P, ws,
+                slot_mapping=self.slots, error_word=self.error_word, stream=stream)
+            return
         if P != self.partition_size:
             ws = B.alloc_workspace(w.S, w.H, w.Hkv, w.D, self.max_context_len, P,
                                    device=self.device)

@@ -152,6 +152,21 @@ def test_append_argument_checks(B):
     assert f8(*ok8[:5], None, *ok8[6:]) == B.PA_ERR_INVALID_ARG
 
 
+def test_cascade_append_argument_checks(B):
+    L = B.lib()
+    f = L.pa_decode_attention_cascade_append
+    # (out, query, kc, vc, new_key, new_value, slots, tables, mb, ctx, maxctx, S, H, Hkv,
+    #  d, bs, N, scale, plan, groups, members, P, ws, ws_bytes, dtype, err, stream)
+    ok = (FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, 4, FAKE, 64, 2, 8, 2, 128, 16, 8,
+          0.1, FAKE, 1, 2, 16, None, 0, 1, None, None)
+    assert f(*ok[:4], None, *ok[5:]) == B.PA_ERR_INVALID_ARG          # no new keys
+    assert f(*ok[:5], None, *ok[6:]) == B.PA_ERR_INVALID_ARG          # no new values
+    assert f(*ok[:24], 2, *ok[25:]) == B.PA_ERR_UNSUPPORTED           # FP8 pools
+    assert f(*ok[:19], 1, 1, *ok[21:]) == B.PA_ERR_INVALID_ARG        # group of one
+    assert f(*ok[:18], None, *ok[19:]) == B.PA_ERR_WORKSPACE          # no workspace first
+    assert f(*ok[:11], 0, *ok[12:]) == B.PA_OK                        # no sequences
+
+
 def test_workspace_layout_sizes(B):
     L = B.lib()
     a256 = lambda x: (x + 255) // 256 * 256  # noqa: E731

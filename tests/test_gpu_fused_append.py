@@ -9,7 +9,9 @@ partition, and in the last partition of both single- and multi-partition
 sequences).  The oracle comparison of the fused step itself is the step
 parity test, whose run() takes this path.  Edge rows: a context of 0
 (nothing appended, slot -1, a zero output row) and a new token whose block
-is outside the pool (slot -1, nothing written, PA_DEVERR_BLOCK_RANGE)."""
+is outside the pool (slot -1, nothing written, PA_DEVERR_BLOCK_RANGE); for
+the prefix-aware form, a plan whose shared prefix reaches a new token
+(PA_DEVERR_PREFIX_PLAN)."""
 import numpy as np
 import pytest
 import torch
@@ -19,7 +21,7 @@ pytestmark = pytest.mark.gpu
 from paged_kv_cache_96_gb300 import workloads as W  # noqa: E402
 from stepping import assert_attention_close  # noqa: E402
 
-NAMES = ["tiny", "mha7b", "gqa70b", "longctx", "prefix",
+NAMES = ["tiny", "mha7b", "gqa70b", "longctx", "prefix", "prefix-cascade",
          "gqa70b-fp8", "longctx-fp8", "prefix-fp8"]
 
 
@@ -132,3 +134,22 @@ def test_append_argument_checks(B, S):
         B.pa_decode_attention_append(st.out, st.query, st.key_cache, st.value_cache,
                                      st.new_key, st.new_value, st.step_block_tables,
                                      st.context_lens, st.max_context_len, float("nan"))
+
+
+def test_cascade_append_prefix_must_end_before_new_token(B, S):
+    w = W.build(W.small_variant("prefix-cascade"))
+    st = S.DecodeStep(w)
+    assert st.cascade and st.fused_append and st.num_groups >= 1
+    ng = st.num_groups
+    plan = st.plan.cpu().numpy()
+    member = int(plan[w.S + 2 * ng + 1 + 1])   # a group's second member
+    ctx = st.context_lens.clone()
+    ctx[member] = int(plan[member])            # its context now ends with the prefix
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    B.pa_decode_attention_cascade_append(st.out, st.query, st.key_cache, st.value_cache,
+                                         st.new_key, st.new_value, st.step_block_tables, ctx,
+                                         st.max_context_len, w.scale, st.plan, ng,
+                                         st.num_members, st.partition_size, st.workspace,
+                                         error_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & B.DEVERR_PREFIX_PLAN
