@@ -178,3 +178,34 @@ def test_workspace_layout_sizes(B):
     assert L.pa_decode_workspace_bytes(S, H, Hkv, D, 512, 512) == 0
     assert L.pa_decode_workspace_bytes(S, H, Hkv, D, 32768, 0) == 0
     assert L.pa_decode_workspace_bytes(-1, H, Hkv, D, 32768, 512) == 0
+
+
+@pytest.mark.parametrize("name,fused", [("tiny", True), ("mha7b", True), ("gqa70b", True),
+                                        ("longctx", True), ("prefix", True),
+                                        ("prefix-cascade", True), ("gqa70b-fp8", True),
+                                        ("chunked", False), ("mixed", False)])
+def test_step_takes_the_fused_append(lib, name, fused):
+    """Host logic of the step: a decode step whose new tokens are one per
+    sequence at its last position (in the same block before and after
+    copy-on-write) runs the fused append; prefill steps, a second new token
+    or a remapped last block send it back to the separate write."""
+    from paged_kv_cache_96_gb300 import step as S
+    from paged_kv_cache_96_gb300 import workloads as W
+    w = W.build(W.small_variant(name))
+    st = S.DecodeStep(w, device="cpu", build_pools=False)
+    assert st.fused_append is fused
+    n_attn = st.launches_per_step()
+    assert n_attn >= (1 if fused else 2)
+    if not fused:
+        return
+    # a step whose new token is not the last position
+    w2 = W.build(W.small_variant(name))
+    w2.new_pos = w2.new_pos - 1
+    assert S.DecodeStep(w2, device="cpu", build_pools=False).fused_append is False
+    # a step whose copy-on-write remaps the block holding a new token
+    w3 = W.build(W.small_variant(name))
+    s0 = 0
+    lb = (int(w3.context_lens[s0]) - 1) // w3.bs
+    w3.step_block_tables = w3.step_block_tables.copy()
+    w3.step_block_tables[s0, lb] = (int(w3.step_block_tables[s0, lb]) + 1) % w3.num_blocks
+    assert S.DecodeStep(w3, device="cpu", build_pools=False).fused_append is False
