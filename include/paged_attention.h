@@ -265,7 +265,7 @@ PA_API pa_status pa_decode_attention_fp8(void *out, const void *query, const voi
  *                        bit for bit what pa_reshape_and_cache(_fp8) writes.
  *   slot_mapping       : int32 [num_seqs] (device) or NULL: receives each
  *                        sequence's slot (-1 for a context of 0, which
- *                        appends nothing).
+ *                        appends nothing, and for a block outside the pool).
  * Attention then covers positions [0, context_lens[s]): the cached ones
  * from the pools and pos from the new rows as the pools now hold them (for
  * FP8 pools, the codes), so out equals that of pa_slot_mapping +
