@@ -175,4 +175,128 @@ def pin_random_invariants(M):
                 assert len(t) == -(-bm.length(s) // bs) and len(set(t)) == len(t)
 
 
+def _state(bm):
+    return (list(bm.ref), {k: list(v) for k, v in bm.tables.items()}, dict(bm.lengths))
+
+
+def _session(M, seed, num_blocks, bs):
+    """A manager with a few sequences, some forked (shared, partly filled
+    last blocks), built by single-sequence appends only."""
+    rng = np.random.default_rng(seed)
+    bm = M.BlockManager(num_blocks, bs, 12)
+    bm.add_sequence(0)
+    bm.append_tokens(0, int(rng.integers(1, 3 * bs)))
+    nxt = 1
+    for _ in range(5):
+        if rng.integers(0, 2):
+            bm.fork(int(rng.integers(0, nxt)), nxt)
+        else:
+            bm.add_sequence(nxt)
+            bm.append_tokens(nxt, int(rng.integers(1, 2 * bs)))
+        nxt += 1
+    return bm, rng
+
+
+def pin_append_batch_is_sequential_appends(M):
+    """A step's batch append equals single-sequence appends made one after
+    another in batch order ([FEI] "Block Table 实现", [LAKE] §3.2): same
+    slots, same copy-on-write pairs, same tables, counts and lengths.  The
+    single appends run on an independent deep copy of the manager."""
+    import copy
+    cow = 0
+    for seed in range(12):
+        bm, rng = _session(M, 100 + seed, 64, int(rng_bs(seed)))
+        ref_bm = copy.deepcopy(bm)
+        seqs = [int(s) for s in rng.permutation(sorted(bm.tables))]
+        counts = [int(rng.integers(0, 2 * bm.block_size)) for _ in seqs]
+        slots, pairs = bm.append_batch(seqs, counts)
+        want_slots, want_pairs = [], []
+        for s, n in zip(seqs, counts):
+            sl, pr = ref_bm.append_tokens(s, n)
+            want_slots += sl
+            want_pairs += pr
+        assert slots == want_slots and pairs == want_pairs, seed
+        assert _state(bm) == _state(ref_bm), seed
+        assert recount(bm) == bm.ref
+        cow += len(pairs)
+    assert cow > 0, "the sessions must exercise copy-on-write"
+
+
+def rng_bs(seed):
+    return (1, 2, 4, 16)[seed % 4]
+
+
+def pin_append_batch_rolls_back(M):
+    """All or nothing: a batch that runs out of blocks part-way -- after
+    earlier sequences of the batch have taken blocks and copy-on-write
+    copies -- leaves every count, table and length exactly as before."""
+    bs = 4
+    bm = M.BlockManager(7, bs, 8)
+    bm.add_sequence(0)
+    bm.append_tokens(0, 6)          # 2 blocks, last one half full
+    bm.fork(0, 1)                   # shares both
+    bm.add_sequence(2)
+    bm.append_tokens(2, 4)          # 1 full block; 4 blocks free
+    before = _state(bm)
+    # seq 1: copy-on-write (1 block) + 1 new; seq 2: 2 new; seq 0: 2 more
+    # -> 6 blocks wanted, 4 free: the first two succeed, the third fails
+    try:
+        bm.append_batch([1, 2, 0], [3, 8, 8])
+        raise AssertionError("batch must fail")
+    except M.OutOfBlocks:
+        pass
+    assert _state(bm) == before
+    assert recount(bm) == bm.ref
+    # the same batch without its last member goes through
+    slots, pairs = bm.append_batch([1, 2], [3, 8])
+    assert len(pairs) == 1 and len(slots) == 11
+
+
+def pin_append_batch_refusal_order(M):
+    """Refusals come in a fixed order, each leaving the manager unchanged:
+    an unknown or repeated sequence first, then a table past
+    max_blocks_per_seq (checked for the whole batch before any append),
+    then running out of blocks."""
+    bm = M.BlockManager(4, 2, 3)
+    bm.add_sequence(0)
+    bm.add_sequence(1)
+    bm.append_tokens(0, 3)          # 2 blocks; 2 free
+    before = _state(bm)
+    cases = [
+        # an unknown id beside a table-full and an out-of-blocks member
+        (([0, 9, 1], [4, 1, 6]), KeyError),
+        # a repeated id whose total would also pass the table limit
+        (([1, 1], [7, 1]), KeyError),
+        # seq 1 alone would run out of blocks (3 wanted, 2 free), seq 0
+        # would pass the table (7 tokens = 4 blocks > 3): the table wins
+        (([1, 0], [6, 4]), M.TableFull),
+        # seq 0 takes a block, then seq 1 wants 2 with 1 left
+        (([0, 1], [2, 3]), M.OutOfBlocks),
+    ]
+    for (seqs, counts), exc in cases:
+        try:
+            bm.append_batch(seqs, counts)
+            raise AssertionError(f"{seqs} {counts} must fail")
+        except exc:
+            pass
+        assert _state(bm) == before, (seqs, counts)
+
+
+def pin_build_batch_rows(M):
+    """Step inputs ([GAO] §1.4): row i is the table of seqs[i] followed by
+    pad_block up to max_blocks, and the context length is the sequence's
+    token count (not the FEI sketch's len(blocks) * block_size)."""
+    bm, rng = _session(M, 7, 64, 4)
+    seqs = [int(s) for s in rng.permutation(sorted(bm.tables))]
+    width = max(len(bm.table(s)) for s in seqs) + 3
+    tables, lens = bm.build_batch(seqs, width, -5)
+    assert len(tables) == len(seqs) and len(lens) == len(seqs)
+    for i, s in enumerate(seqs):
+        t = bm.table(s)
+        assert tables[i] == t + [-5] * (width - len(t)), s
+        assert lens[i] == bm.length(s)
+    # token counts that are not whole blocks are kept as counts
+    assert any(n % bm.block_size for n in lens)
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -234,6 +234,26 @@ def pin_copy_blocks(lib):
     assert np.array_equal(kc[others], k0[others]) and np.array_equal(vc[others], v0[others])
 
 
+def pin_copy_blocks_u8(lib):
+    """"vLLM源码解析(二)" §3.2 on 1-byte (FP8) pools: the result equals numpy
+    whole-block slice copies made pair by pair -- every destination block
+    holds the source block's K and V codes, byte for byte over the whole
+    block, and every other block keeps its bytes.  Several shapes, so that a
+    block length taken from the wrong sizes (or halved) shows."""
+    rng = np.random.default_rng(17)
+    for N, bs, Hkv, d, npairs in ((12, 4, 2, 8, 3), (9, 16, 3, 128, 4), (20, 1, 1, 16, 7)):
+        kc = rng.integers(0, 256, size=(N, bs, Hkv, d)).astype(np.uint8)
+        vc = rng.integers(0, 256, size=(N, bs, Hkv, d)).astype(np.uint8)
+        ids = rng.permutation(N)[:2 * npairs]
+        pairs = np.stack([ids[:npairs], ids[npairs:]], axis=1).astype(np.int32)
+        want_k, want_v = kc.copy(), vc.copy()
+        for src, dst in pairs:
+            want_k[dst] = want_k[src]
+            want_v[dst] = want_v[src]
+        oracle.copy_blocks_u8(kc, vc, pairs, lib=lib)
+        assert np.array_equal(kc, want_k) and np.array_equal(vc, want_v), (N, bs, Hkv, d)
+
+
 def pin_attention_matches_sdpa(lib):
     """§1.6 on random GQA inputs with shuffled blocks equals torch's
     float64 scaled-dot-product attention on the gathered contiguous K/V."""

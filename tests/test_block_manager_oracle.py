@@ -27,6 +27,25 @@ MUTANTS = [
     ("slot_offset_logical", "    return table[position // block_size] * block_size + position % block_size",
      "    return table[position // block_size] * block_size + position // block_size"),
     ("append_not_atomic", "        if self.blocks_needed(seq, n) > self.num_free():\n            raise OutOfBlocks()\n", ""),
+    ("batch_no_rollback", "            self.ref, self.tables, self.lengths = saved\n", ""),
+    ("batch_rollback_keeps_tables",
+     "            self.ref, self.tables, self.lengths = saved\n",
+     "            self.ref, self.lengths = saved[0], saved[2]\n"),
+    ("batch_repeat_allowed",
+     "        if len(set(seqs)) != len(seqs) or any(s not in self.tables for s in seqs):",
+     "        if any(s not in self.tables for s in seqs):"),
+    ("batch_table_check_late",
+     "            if (self.lengths[s] + n + bs - 1) // bs > self.max_blocks_per_seq:\n                raise TableFull()\n",
+     ""),
+    ("batch_reversed_order",
+     "            for s, n in zip(seqs, counts):\n                sl, pr = self.append_tokens(s, n)",
+     "            for s, n in reversed(list(zip(seqs, counts))):\n                sl, pr = self.append_tokens(s, n)"),
+    ("build_batch_pads_zero",
+     "[pad_block] * (max_blocks - len(self.tables[s]))",
+     "[0] * (max_blocks - len(self.tables[s]))"),
+    ("build_batch_length_in_blocks",
+     "            lens.append(self.lengths[s])",
+     "            lens.append(len(self.tables[s]) * self.block_size)"),
 ]
 
 

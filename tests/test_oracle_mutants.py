@@ -116,6 +116,25 @@ MUTANTS = [
     ("fp8_cache_swaps_scales",
      "                             dtype, k_inv_scale);",
      "                             dtype, v_inv_scale);", 0),
+    ("copy_blocks_u8_swapped",
+     "        memcpy(key_cache + dst * block_elems, key_cache + src * block_elems,",
+     "        memcpy(key_cache + src * block_elems, key_cache + dst * block_elems,", 0),
+    ("copy_blocks_u8_half_block",
+     "        memcpy(value_cache + dst * block_elems, value_cache + src * block_elems,\n"
+     "               (size_t)block_elems);",
+     "        memcpy(value_cache + dst * block_elems, value_cache + src * block_elems,\n"
+     "               (size_t)block_elems / 2);", 0),
+    ("copy_blocks_u8_only_keys",
+     "        memcpy(value_cache + dst * block_elems, value_cache + src * block_elems,\n"
+     "               (size_t)block_elems);\n",
+     "", 0),
+    ("copy_blocks_u8_block_without_heads",
+     "    int64_t block_elems = (int64_t)block_size * num_kv_heads * head_dim;\n"
+     "    for (int p = 0; p < num_pairs; ++p) {\n        int64_t src = block_mapping[2 * p];\n"
+     "        int64_t dst = block_mapping[2 * p + 1];\n        memcpy(",
+     "    int64_t block_elems = (int64_t)block_size * head_dim;\n"
+     "    for (int p = 0; p < num_pairs; ++p) {\n        int64_t src = block_mapping[2 * p];\n"
+     "        int64_t dst = block_mapping[2 * p + 1];\n        memcpy(", 0),
 ]
 
 RUNNER = r"""
