@@ -102,28 +102,60 @@ class ClockSampler:
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    PERIOD_MS = 20
 
-    def __init__(self, gpu_id: str):
+    def __init__(self, gpu_ids):
+        """Samples nvidia-smi for the first of `gpu_ids` (UUID, then index)
+        that nvidia-smi accepts."""
         self.samples = []
         self.proc = None
         self.thread = None
         self.error = None
-        try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100", "-i", gpu_id],
-                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-        except (OSError, ValueError) as e:
-            self.error = str(e)
+        self.ids = [g for g in gpu_ids if g]
+        self._start_next()
+
+    def _start_next(self):
+        while self.ids:
+            gid = self.ids.pop(0)
+            try:
+                self.proc = subprocess.Popen(
+                    ["nvidia-smi", f"--query-gpu={self.FIELDS}",
+                     "--format=csv,noheader,nounits", "-lms", str(self.PERIOD_MS), "-i", gid],
+                    stdout=subprocess.PIPE, stderr=subprocess.PIPE, text=True)
+            except (OSError, ValueError) as e:
+                self.error = str(e)
+                continue
+            self.gpu_id = gid
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
             return
-        self.thread = threading.Thread(target=self._read, daemon=True)
-        self.thread.start()
+        self.proc = None
 
     def _read(self):
         for line in self.proc.stdout:
             parts = [p.strip() for p in line.split(",")]
             if len(parts) >= 9:
                 self.samples.append((time.time(), parts))
+
+    def wait_first(self, timeout: float = 10.0) -> bool:
+        """Block until the first sample arrives (nvidia-smi takes a moment to
+        start); try the next id if nvidia-smi refuses this one."""
+        t_end = time.time() + timeout
+        while time.time() < t_end:
+            if self.samples:
+                return True
+            if self.proc is None:
+                return False
+            if self.proc.poll() is not None:  # refused this id
+                err = self.proc.stderr.read().strip() if self.proc.stderr else ""
+                self.error = f"nvidia-smi -i {self.gpu_id}: {err[:160]}"
+                self._start_next()
+                continue
+            time.sleep(0.01)
+        return bool(self.samples)
+
+    def count(self, t0: float, t1: float) -> int:
+        return sum(1 for (t, _) in self.samples if t0 <= t <= t1)
 
     def stop(self):
         if self.proc is not None:
@@ -133,15 +165,15 @@ class ClockSampler:
             except subprocess.TimeoutExpired:
                 self.proc.kill()
 
-    def summary(self, t0: float, t1: float):
-        if self.error or not self.samples:
+    def summary(self, t0: float, t1: float, note: str = ""):
+        if not self.samples:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [],
                     "note": self.error or "no nvidia-smi samples"}
-        window = [p for (t, p) in self.samples if t0 <= t <= t1 + 0.15]
-        note = "sampled during the timed region (100 ms period)"
+        window = [p for (t, p) in self.samples if t0 <= t <= t1]
+        note = note or f"sampled during the timed region ({self.PERIOD_MS} ms period)"
         if not window:
             window = [p for (_, p) in self.samples]
-            note = "timed region shorter than the sampling period: samples span warm-up + timing"
+            note = "no sample inside the timed region: samples span the whole run"
 
         def num(x):
             try:
@@ -157,7 +189,22 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(mx) if mx else None,
                 "power_w_max": max(pw) if pw else None,
-                "reasons": reasons, "samples": len(window), "note": note}
+                "reasons": reasons, "samples": len(window), "note": note,
+                "gpu": self.gpu_id}
+
+
+def gpu_ids_for(torch, dev, local_rank):
+    """nvidia-smi ids of a torch device: its UUID, then the physical index
+    (CUDA_VISIBLE_DEVICES maps torch's index to it)."""
+    ids = []
+    uuid = str(getattr(torch.cuda.get_device_properties(dev), "uuid", "") or "")
+    if uuid:
+        ids.append(uuid if uuid.startswith("GPU-") or not re.fullmatch(r"[0-9a-f-]{36}", uuid)
+                   else "GPU-" + uuid)
+    vis = [v.strip() for v in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if v.strip()]
+    idx = dev.index or 0
+    ids.append(vis[idx] if idx < len(vis) else str(idx))
+    return ids
 
 
 # ---------------------------------------------------------------------------
@@ -359,18 +406,20 @@ def cpu_baseline_sample(w, target_s: float, keep: bool = False):
 _MC = {}
 
 
-def _mc_init(kpath, vpath, shape, dtype, fields):
+def _mc_init(folder, fields):
     import types
 
     import oracle
     oracle.load()
-    w = types.SimpleNamespace(**fields)
+    arrays = {n: np.load(os.path.join(folder, n + ".npy"), mmap_mode="r")
+              for n in ("query", "query_start", "step_block_tables", "context_lens", "kc", "vc")}
+    w = types.SimpleNamespace(**fields, **{k: arrays[k] for k in (
+        "query", "query_start", "step_block_tables", "context_lens")})
     w.spec = types.SimpleNamespace(kv_scale=fields["kv_scale"])
     oc = OracleCache.__new__(OracleCache)
     oc.o, oc.w = oracle, w
     oc.dt = oracle.F16 if w.dtype == "f16" else oracle.BF16
-    oc.kc = np.memmap(kpath, dtype=dtype, mode="r", shape=shape)
-    oc.vc = np.memmap(vpath, dtype=dtype, mode="r", shape=shape)
+    oc.kc, oc.vc = arrays["kc"], arrays["vc"]
     _MC["oc"] = oc
 
 
@@ -385,18 +434,19 @@ def cpu_baseline_multicore(oc, w, cores: int):
     import multiprocessing
     import shutil
     import tempfile
-    d = tempfile.mkdtemp(prefix="pa_oracle_")
+    d = tempfile.mkdtemp(prefix="pa_oracle_",
+                         dir="/dev/shm" if os.path.isdir("/dev/shm") else None)
     try:
-        kpath, vpath = os.path.join(d, "k.bin"), os.path.join(d, "v.bin")
-        for path, arr in ((kpath, oc.kc), (vpath, oc.vc)):
-            mm = np.memmap(path, dtype=arr.dtype, mode="w+", shape=arr.shape)
-            mm[...] = arr
-            mm.flush()
-            del mm
+        # every array through a file the workers map (start arguments go
+        # through a pipe each child reads only after its imports, so large
+        # ones would start the workers one by one)
+        for name, arr in (("kc", oc.kc), ("vc", oc.vc), ("query", w.query),
+                          ("query_start", w.query_start),
+                          ("step_block_tables", w.step_block_tables),
+                          ("context_lens", w.context_lens)):
+            np.save(os.path.join(d, name + ".npy"), np.ascontiguousarray(arr))
         fields = {"prefill": w.prefill, "fp8": w.fp8, "dtype": w.dtype, "scale": w.scale,
-                  "kv_scale": float(w.spec.kv_scale), "query": w.query,
-                  "query_start": w.query_start, "step_block_tables": w.step_block_tables,
-                  "context_lens": w.context_lens}
+                  "kv_scale": float(w.spec.kv_scale)}
         cost = [(_seq_flops(w, s) if w.prefill else int(w.context_lens[s]), s)
                 for s in range(w.S)]
         cost.sort(reverse=True)
@@ -408,8 +458,7 @@ def cpu_baseline_multicore(oc, w, cores: int):
             load[i] += c
         chunks = [c for c in chunks if c]
         ctx = multiprocessing.get_context("spawn")
-        with ctx.Pool(cores, initializer=_mc_init,
-                      initargs=(kpath, vpath, oc.kc.shape, oc.kc.dtype.str, fields)) as pool:
+        with ctx.Pool(cores, initializer=_mc_init, initargs=(d, fields)) as pool:
             # every worker started and loaded (bounded: a pool whose workers
             # cannot start would otherwise restart them for ever)
             pool.map_async(_mc_task, [[0]] * cores).get(timeout=120)
@@ -523,6 +572,8 @@ def run_ours(args):
         dist.init_process_group("nccl")
     dev = torch.device("cuda", local_rank if world > 1 else 0)
     torch.cuda.set_device(dev)
+    # clocks: started now, so that nvidia-smi is sampling before warm-up
+    sampler = ClockSampler(gpu_ids_for(torch, dev, local_rank)) if rank == 0 else None
 
     from paged_kv_cache_96_gb300 import step as S
     from paged_kv_cache_96_gb300 import workloads as W
@@ -533,16 +584,11 @@ def run_ours(args):
     stream = torch.cuda.current_stream(dev)
     torch.cuda.synchronize(dev)
 
-    sampler = None
-    if rank == 0:
-        gpu_id = str(getattr(torch.cuda.get_device_properties(dev), "uuid", local_rank))
-        if not gpu_id.startswith("GPU-") and re.fullmatch(r"[0-9a-f-]{36}", gpu_id):
-            gpu_id = "GPU-" + gpu_id
-        sampler = ClockSampler(gpu_id)
-
     for _ in range(max(args.warmup, 3)):
         st.run()
     torch.cuda.synchronize(dev)
+    if sampler is not None:
+        sampler.wait_first()
     if st.error_word.item() != 0:
         raise RuntimeError(f"device error word {int(st.error_word.item()):#x}")
 
@@ -580,9 +626,24 @@ def run_ours(args):
         torch.distributed.barrier()
     step_s = sum(a.elapsed_time(b) for a, b in zip(ev_s, ev_b)) / 1e3
     attn_s = sum(a.elapsed_time(b) for a, b in zip(ev_a, ev_b)) / 1e3 / K
+    clocks = None
     if sampler is not None:
+        t_end, note = t_host1, ""
+        if sampler.samples and sampler.count(t_host0, t_host1) < 3:
+            # a timed region shorter than a few sampling periods: the same
+            # steps keep running (untimed) until three samples have been
+            # taken under that load, at most one second
+            t_stop = time.time() + 1.0
+            while sampler.count(t_host0, time.time()) < 3 and time.time() < t_stop:
+                for _ in range(8):
+                    st.run()
+                torch.cuda.synchronize(dev)
+            t_end = time.time()
+            note = (f"timed region {1e3 * (t_host1 - t_host0):.1f} ms: sampled over it and "
+                    f"the same steps run on, untimed, to {1e3 * (t_end - t_host0):.0f} ms "
+                    f"({ClockSampler.PERIOD_MS} ms period)")
         sampler.stop()
-    clocks = sampler.summary(t_host0, t_host1) if sampler else None
+        clocks = sampler.summary(t_host0, t_end, note)
 
     kv = w.kv_bytes()
     if w.prefill:

@@ -451,9 +451,14 @@ PA_API pa_status pa_decode_attention_cascade_append(
  *   - Sizes whose workspace (pa_decode_workspace_bytes) exceeds
  *     PA_NOALLOC_WORKSPACE_BYTES are rejected with PA_ERR_WORKSPACE before
  *     anything is launched.
+ *   - Arguments are checked first, with pa_decode_attention's statuses; a
+ *     valid call whose partials need more than the array is then refused.
  *   - The first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress, once per device, with that device current);
- *     make that first call before any stream capture.
+ *     make that first call before any stream capture.  The address is kept
+ *     with the unique id of the CUDA context it belongs to: after a
+ *     cudaDeviceReset (a new context), the next call looks it up again, so
+ *     make that call, too, before any capture.
  *   - Every call on a device shares the one array and leaves its last
  *     contents there; no part of it needs to start at zero (each call
  *     writes every partial it later reads).  Calls whose GPU work overlaps
@@ -553,6 +558,34 @@ PA_API const char *pa_last_cuda_error(void);
 
 /* ABI version: major * 10000 + minor * 100 + patch. */
 PA_API int pa_version(void);
+
+/*
+ * Stage-wait limit -- no counterpart on the pages: the watchdog of the
+ * attention kernels (pa_decode_attention*, pa_prefill_attention, the prefix
+ * pass of pa_decode_attention_cascade*).  Each wait of such a kernel for
+ * staged data (a K/V tile landing in shared memory, a tensor-core result)
+ * gives up after limit_ns nanoseconds: the kernel then stops issuing work,
+ * waits (up to the default limit) for the copies and tensor-core operations
+ * it already started, releases its tensor memory, ORs PA_DEVERR_TIMEOUT into
+ * the error word and returns; the outputs of that call are undefined, and
+ * later calls on the stream are unaffected.  The setting is process-wide,
+ * read when a call launches its kernels (calls already queued keep theirs).
+ * limit_ns == 0 restores the default of one second.
+ */
+PA_API void pa_set_stage_wait_limit_ns(uint64_t limit_ns);
+PA_API uint64_t pa_stage_wait_limit_ns(void);
+
+/*
+ * pa_debug_withhold_first_fill -- test hook of the time-out path above, no
+ * counterpart on the pages.  While enabled (enable != 0; process-wide, read
+ * at launch), every CTA of every attention kernel launched leaves its first
+ * K/V fill unissued: nothing completes that stage, so the wait for it
+ * runs out after the stage-wait limit and the kernel returns through its
+ * time-out path (PA_DEVERR_TIMEOUT, undefined outputs of that call).  No
+ * fault, no hang: every other copy the kernel issued is waited for.  Off by
+ * default; meant only for tests of the watchdog.
+ */
+PA_API void pa_debug_withhold_first_fill(int enable);
 
 #ifdef __cplusplus
 }

@@ -102,6 +102,9 @@ def _load() -> ctypes.CDLL:
         "pa_status_string": (ctypes.c_char_p, [i32]),
         "pa_last_cuda_error": (ctypes.c_char_p, []),
         "pa_version": (i32, []),
+        "pa_set_stage_wait_limit_ns": (None, [ctypes.c_uint64]),
+        "pa_stage_wait_limit_ns": (ctypes.c_uint64, []),
+        "pa_debug_withhold_first_fill": (None, [i32]),
     }
     for name, (res, args) in sigs.items():
         fn = getattr(lib, name)
@@ -116,6 +119,22 @@ _lib = _load()
 def lib() -> ctypes.CDLL:
     """The loaded C library (for callers that pass raw pointers)."""
     return _lib
+
+
+def pa_set_stage_wait_limit_ns(limit_ns: int) -> None:
+    """Process-wide limit of one stage wait in the attention kernels (0: the
+    default of one second)."""
+    _lib.pa_set_stage_wait_limit_ns(int(limit_ns))
+
+
+def pa_stage_wait_limit_ns() -> int:
+    return int(_lib.pa_stage_wait_limit_ns())
+
+
+def pa_debug_withhold_first_fill(enable: bool) -> None:
+    """Test hook of the time-out path: while enabled, every CTA of each
+    attention launch leaves its first K/V fill unissued, so its wait runs out."""
+    _lib.pa_debug_withhold_first_fill(1 if enable else 0)
 
 
 # ---------------------------------------------------------------------------

@@ -3,6 +3,7 @@
 // Batching" §1.5; "vLLM 架构详解", "Block Table 实现") and the copy-on-write
 // block copy ("vLLM源码解析(二)" §3.2).  All three are bit-exact: they move
 // 16-byte words or compute integers.
+#include <atomic>
 #include <cstdio>
 #include <cstring>
 
@@ -18,7 +19,14 @@ namespace pa {
 
 namespace {
 thread_local char g_last_error[256] = "no error";
+// Time limit of one wait on staged data in the attention kernels, read when
+// a call launches them.
+std::atomic<uint64_t> g_stage_wait_ns{kDefaultStageWaitNs};
+std::atomic<int> g_withhold_fill{0};
 }
+
+uint64_t stage_wait_limit_ns() { return g_stage_wait_ns.load(std::memory_order_relaxed); }
+int withhold_first_fill() { return g_withhold_fill.load(std::memory_order_relaxed); }
 
 pa_status record_cuda(cudaError_t err)
 {
@@ -448,3 +456,16 @@ extern "C" const char *pa_status_string(pa_status status)
 extern "C" const char *pa_last_cuda_error(void) { return g_last_error; }
 
 extern "C" int pa_version(void) { return 100; }
+
+extern "C" void pa_set_stage_wait_limit_ns(uint64_t limit_ns)
+{
+    g_stage_wait_ns.store(limit_ns == 0 ? kDefaultStageWaitNs : limit_ns,
+                          std::memory_order_relaxed);
+}
+
+extern "C" uint64_t pa_stage_wait_limit_ns(void) { return stage_wait_limit_ns(); }
+
+extern "C" void pa_debug_withhold_first_fill(int enable)
+{
+    g_withhold_fill.store(enable ? 1 : 0, std::memory_order_relaxed);
+}

@@ -15,6 +15,17 @@ namespace pa {
 // (or PA_OK when err == cudaSuccess).
 pa_status record_cuda(cudaError_t err);
 
+// A wait of an attention kernel on staged data (a tile landing, a
+// tensor-core result) gives up after this many nanoseconds and flags
+// PA_DEVERR_TIMEOUT; the process-wide setting (pa_set_stage_wait_limit_ns)
+// is read at each launch.  Waits that drain copies still in flight before a
+// kernel exits always use the default.
+constexpr uint64_t kDefaultStageWaitNs = 1000000000ull;  // one second
+uint64_t stage_wait_limit_ns();
+// Test hook of that time-out path (pa_debug_withhold_first_fill): 1 while
+// every CTA of each attention launch leaves its first K/V fill unissued.
+int withhold_first_fill();
+
 inline bool aligned16(const void *p)
 {
     return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;

@@ -359,7 +359,10 @@ __global__ void __launch_bounds__(bound_threads(NW, MINB), MINB)
         if (pdone || aborted)
             return;
         const int stage = issued % NST;
-        if (lane == 0) {
+        // test hook of the time-out path: a fill that is never issued, so
+        // nothing completes the stage's phase and its wait runs out
+        const bool withheld = p.withhold_fill != 0 && warp == 0 && issued == 0;
+        if (lane == 0 && !withheld) {
             const bool ok = pphys >= 0 && pphys < p.num_blocks;
             flags[warp * NST + stage] = ok;
             if (ok) {
@@ -384,7 +387,8 @@ __global__ void __launch_bounds__(bound_threads(NW, MINB), MINB)
                 mbar_arrive(bar_of(stage));
             }
         }
-        inflight |= 1u << stage;
+        if (!withheld)
+            inflight |= 1u << stage;
         ++issued;
         ptile += NW;
         skip_empty();
@@ -480,7 +484,7 @@ __global__ void __launch_bounds__(bound_threads(NW, MINB), MINB)
             const uint32_t parity = (consumed / NST) & 1u;
             bool ready = false;
             if (!aborted) {
-                ready = __all_sync(kFull, mbar_wait_bounded(bar_of(stage), parity, kWaitLimitNs));
+                ready = __all_sync(kFull, mbar_wait_bounded(bar_of(stage), parity, p.wait_ns));
                 if (ready) {
                     inflight &= ~(1u << stage);
                 } else {
@@ -759,7 +763,7 @@ __global__ void __launch_bounds__(bound_threads(NW, MINB), MINB)
             // the most recent fetch into stage k was issue number
             // issued - 1 - ((issued - 1 - k) % NST)
             const uint32_t last = issued - 1 - ((issued - 1 - k) % NST);
-            mbar_wait_bounded(bar_of(k), (last / NST) & 1u, kWaitLimitNs);
+            mbar_wait_bounded(bar_of(k), (last / NST) & 1u, kDrainWaitNs);
         }
     }
     if (p.concurrent)
@@ -1181,6 +1185,8 @@ static pa_status run_cascade(void *out, const void *query, void *key_cache, void
     mq.part_l = prm.part_l;
     mq.part_o = prm.part_o;
     mq.error_word = error_word;
+    mq.wait_ns = prm.wait_ns;
+    mq.withhold_fill = prm.withhold_fill;
     mq.prefix_mode = 1;
     mq.num_segments = num_groups;
     mq.num_seqs = num_seqs;

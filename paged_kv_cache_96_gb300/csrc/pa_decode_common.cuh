@@ -16,7 +16,7 @@
 namespace pa {
 
 constexpr int kTileTokens = 16;
-constexpr uint64_t kWaitLimitNs = 1000000000ull;  // one second per stage wait
+constexpr uint64_t kDrainWaitNs = kDefaultStageWaitNs;  // waits for copies in flight at exit
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr unsigned kFull = 0xffffffffu;
@@ -32,6 +32,8 @@ struct DecodeParams {
     float *part_l;
     float *part_o;
     int32_t *error_word;
+    uint64_t wait_ns;  // limit of one stage wait (PA_DEVERR_TIMEOUT past it)
+    int withhold_fill; // test hook: warp 0 of each CTA never issues its first fill
     int num_seqs, num_heads, num_kv_heads, group;
     int max_blocks_per_seq, num_blocks, block_size, max_context_len;
     int block_shift;  // log2(block_size)
@@ -422,6 +424,8 @@ static pa_status prepare_decode(DecodeParams *prm, void *out, const void *query,
     prm->part_l = wl.total ? reinterpret_cast<float *>(ws + wl.l_off) : nullptr;
     prm->part_o = wl.total ? reinterpret_cast<float *>(ws + wl.o_off) : nullptr;
     prm->error_word = error_word;
+    prm->wait_ns = stage_wait_limit_ns();
+    prm->withhold_fill = withhold_first_fill();
     prm->num_seqs = num_seqs;
     prm->num_heads = num_heads;
     prm->num_kv_heads = num_kv_heads;

@@ -300,7 +300,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     auto wait = [&](uint32_t b, uint32_t parity) -> bool {
         if (__all_sync(kFull, mbar_try_wait(b, parity)))
             return true;
-        bool ok = *abort_flag == 0 && mbar_wait_bounded(b, parity, kWaitLimitNs);
+        bool ok = *abort_flag == 0 && mbar_wait_bounded(b, parity, p.wait_ns);
         ok = __all_sync(kFull, ok);
         if (!ok)
             *abort_flag = 1;
@@ -643,6 +643,10 @@ __global__ void __launch_bounds__(kTcThreads, 2)
                     if (!ok)
                         break;
                 }
+                // test hook of the time-out path: a CTA's first key fill is
+                // never issued, so the wait for it runs out
+                if (p.withhold_fill != 0 && !values && gg == 0)
+                    continue;
                 issue(si, st, ent);
                 (st ? last1 : last0) = (int)gg;
             }
@@ -650,9 +654,9 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         }
         // fills still landing (only after an abort: the MMA warp waited the rest)
         if (last0 >= 0)
-            mbar_wait_bounded(values ? vfull(0) : kfull(0), (last0 >> 1) & 1, kWaitLimitNs);
+            mbar_wait_bounded(values ? vfull(0) : kfull(0), (last0 >> 1) & 1, kDrainWaitNs);
         if (last1 >= 0)
-            mbar_wait_bounded(values ? vfull(1) : kfull(1), (last1 >> 1) & 1, kWaitLimitNs);
+            mbar_wait_bounded(values ? vfull(1) : kfull(1), (last1 >> 1) & 1, kDrainWaitNs);
     } else if (warp == kMmaWarp) {
         // ===== tensor-core warp: S = Q K^T and O += P V, one elected lane issues ========
         uint32_t g = 0, nq = 0;
@@ -731,7 +735,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         if (elect_one())
             tc_commit(mma_drain);
         __syncwarp();
-        mbar_wait_bounded(mma_drain, 0, kWaitLimitNs);
+        mbar_wait_bounded(mma_drain, 0, kDrainWaitNs);
     }
     pdl_launch_dependents();
 
@@ -882,6 +886,8 @@ extern "C" pa_status pa_prefill_attention(void *out, const void *query, const vo
     prm.context_lens = context_lens;
     prm.query_start = query_start;
     prm.error_word = error_word;
+    prm.wait_ns = stage_wait_limit_ns();
+    prm.withhold_fill = withhold_first_fill();
     prm.prefix_mode = 0;
     prm.num_segments = num_seqs;
     prm.num_seqs = num_seqs;

@@ -21,6 +21,8 @@ struct MqParams {
     float *part_l;
     float *part_o;
     int32_t *error_word;
+    uint64_t wait_ns;  // limit of one stage wait (PA_DEVERR_TIMEOUT past it)
+    int withhold_fill; // test hook: each CTA's key warp never issues its first fill
     int prefix_mode;   // 0: chunked prefill, 1: shared-prefix pass
     int num_segments;  // sequences (prefill) or groups (prefix pass)
     int num_seqs, num_heads, num_kv_heads, group;

@@ -7,6 +7,11 @@ same seeded workload arrays; nothing flows from the GPU into the oracle.
 """
 from __future__ import annotations
 
+import os
+import shutil
+import tempfile
+import types
+
 import numpy as np
 
 import oracle
@@ -94,3 +99,102 @@ def assert_attention_close(got: np.ndarray, want: np.ndarray, what: str = ""):
                              f"first {idx}: gpu {got[idx]} oracle {want[idx]}")
     rel = err / np.maximum(np.abs(want), 1e-6)
     return float(err.max()), float(np.median(rel))
+
+
+# ---- the oracle on every host core -------------------------------------------------
+#
+# Whole-step comparisons at full size: a spawn-context process pool (safe
+# after CUDA has started in the test process) runs the unchanged oracle over
+# disjoint, cost-balanced sets of sequences -- or, for a prefill step, of
+# chunk rows -- against the OracleStep's pools, shared through files the
+# workers map read-only.
+
+_WORKER = {}
+
+
+def _worker_init(folder, fields):
+    import oracle as _oracle
+    _oracle.load()
+    arrays = {}
+    for name in ("query", "query_start", "step_block_tables", "context_lens", "kc", "vc"):
+        arrays[name] = np.load(os.path.join(folder, name + ".npy"), mmap_mode="r")
+    w = types.SimpleNamespace(**fields, **{k: arrays[k] for k in (
+        "query", "query_start", "step_block_tables", "context_lens")})
+    w.spec = types.SimpleNamespace(kv_scale=fields["kv_scale"])
+    ref = OracleStep.__new__(OracleStep)
+    ref.w = w
+    ref.key_cache = arrays["kc"]
+    ref.value_cache = arrays["vc"]
+    _WORKER["ref"] = ref
+
+
+def _worker_task(job):
+    kind, items = job
+    ref = _WORKER["ref"]
+    if kind == "rows":
+        return items, ref.attention(rows=items)
+    return items, ref.attention(seqs=items)[items]
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def attention_all(ref: OracleStep, workers: int = 0) -> np.ndarray:
+    """The oracle's attention output of every sequence (decode, [S, H, d])
+    or every chunk row (prefill, [T, H, d]), computed on `workers` processes
+    (all host cores by default)."""
+    import multiprocessing
+    w = ref.w
+    workers = workers or host_cores()
+    if w.prefill:
+        # a row's cost is its position + 1 keys; cut the rows into chunks of
+        # similar cost
+        qs = w.query_start.astype(np.int64)
+        seq_of = np.searchsorted(qs, np.arange(w.T), side="right") - 1
+        pos = w.context_lens[seq_of] - (qs[seq_of + 1] - qs[seq_of]) + (np.arange(w.T) - qs[seq_of])
+        cost = np.maximum(pos + 1, 1).astype(np.float64)
+        edges = np.searchsorted(np.cumsum(cost), np.linspace(0, cost.sum(), 8 * workers + 1)[1:-1])
+        jobs = [("rows", [int(r) for r in c]) for c in np.split(np.arange(w.T), edges) if len(c)]
+        out = np.full((w.T, w.H, w.D), np.nan)
+    else:
+        order = sorted(range(w.S), key=lambda s: -int(w.context_lens[s]))
+        chunks = [[] for _ in range(min(w.S, 4 * workers))]
+        load = [0] * len(chunks)
+        for s in order:  # heaviest sequence to the lightest chunk
+            i = load.index(min(load))
+            chunks[i].append(s)
+            load[i] += int(w.context_lens[s]) + 1
+        jobs = [("seqs", sorted(c)) for c in chunks if c]
+        out = np.full((w.S, w.H, w.D), np.nan)
+    if workers <= 1:
+        for kind, items in jobs:
+            res = ref.attention(rows=items) if kind == "rows" else ref.attention(seqs=items)[items]
+            out[items] = res
+        return out
+    base = "/dev/shm" if os.path.isdir("/dev/shm") else None
+    d = tempfile.mkdtemp(prefix="pa_oracle_", dir=base)
+    try:
+        # every array goes through a file the workers map: arguments of the
+        # workers' start are pickled into a pipe each child reads only once
+        # it has imported this module, so large ones would start them one by
+        # one
+        for name, arr in (("kc", ref.key_cache), ("vc", ref.value_cache), ("query", w.query),
+                          ("query_start", w.query_start),
+                          ("step_block_tables", w.step_block_tables),
+                          ("context_lens", w.context_lens)):
+            np.save(os.path.join(d, name + ".npy"), np.ascontiguousarray(arr))
+        fields = {"prefill": w.prefill, "fp8": w.fp8, "dtype": w.dtype, "scale": w.scale,
+                  "kv_scale": float(w.spec.kv_scale)}
+        ctx = multiprocessing.get_context("spawn")
+        with ctx.Pool(workers, initializer=_worker_init, initargs=(d, fields)) as pool:
+            # bounded: a pool whose workers cannot start would restart them
+            # for ever
+            for items, res in pool.map_async(_worker_task, jobs).get(timeout=1800):
+                out[items] = res
+        return out
+    finally:
+        shutil.rmtree(d, ignore_errors=True)

@@ -209,3 +209,45 @@ def test_step_takes_the_fused_append(lib, name, fused):
     w3.step_block_tables = w3.step_block_tables.copy()
     w3.step_block_tables[s0, lb] = (int(w3.step_block_tables[s0, lb]) + 1) % w3.num_blocks
     assert S.DecodeStep(w3, device="cpu", build_pools=False).fused_append is False
+
+
+def test_stage_wait_limit_setting(B):
+    """The watchdog limit is process-wide, settable, and 0 restores the
+    default of one second."""
+    default = B.pa_stage_wait_limit_ns()
+    assert default == 1_000_000_000
+    try:
+        B.pa_set_stage_wait_limit_ns(250)
+        assert B.pa_stage_wait_limit_ns() == 250
+        B.pa_set_stage_wait_limit_ns(0)
+        assert B.pa_stage_wait_limit_ns() == default
+    finally:
+        B.pa_set_stage_wait_limit_ns(0)
+
+
+def test_noalloc_checks_arguments_before_its_size(B):
+    """The allocation-free entry point answers bad arguments as
+    pa_decode_attention does, even where their workspace would not fit its
+    array; only valid sizes that do not fit are refused for their size."""
+    L = B.lib()
+
+    def call(**kw):
+        a = dict(out=FAKE, query=FAKE, kc=FAKE, vc=FAKE, bt=FAKE, mb=1 << 14, ctx=FAKE,
+                 maxctx=1 << 18, S=64, H=32, Hkv=8, D=128, bs=16, N=1 << 16, scale=0.1, P=16,
+                 dt=1)
+        a.update(kw)
+        return L.pa_decode_attention_noalloc(
+            a["out"], a["query"], a["kc"], a["vc"], a["bt"], a["mb"], a["ctx"], a["maxctx"],
+            a["S"], a["H"], a["Hkv"], a["D"], a["bs"], a["N"], a["scale"], a["P"], a["dt"],
+            None, None)
+
+    need = B.pa_decode_workspace_bytes(64, 32, 8, 128, 1 << 18, 16)
+    assert need > B.NOALLOC_WORKSPACE_BYTES
+    assert call() == B.PA_ERR_WORKSPACE
+    assert call(P=24) == B.PA_ERR_UNSUPPORTED        # not a multiple of 16 tokens
+    assert call(D=96) == B.PA_ERR_UNSUPPORTED
+    assert call(out=None) == B.PA_ERR_INVALID_ARG
+    assert call(query=FAKE_ODD) == B.PA_ERR_INVALID_ARG
+    assert call(H=30) == B.PA_ERR_INVALID_ARG         # not a multiple of the KV heads
+    assert call(dt=2) == B.PA_ERR_INVALID_ARG
+    assert call(S=0) == B.PA_OK

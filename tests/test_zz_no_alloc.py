@@ -4,12 +4,15 @@ pa_decode_attention_noalloc serves callers that may not allocate device
 memory on their decode path (a plugin inside an engine that owns every
 device allocation, a loop that cannot take an allocation's implicit
 synchronisation, a C interface with no way to pass a workspace).  It keeps
-its split-context partials in a fixed-size device array inside the library.
-This test checks, on two calls in a row, that its output matches the
-regular entry point's (same kernels, caller-provided workspace) within the
-attention tolerance, and that sizes needing more scratch than the array
-holds are refused before anything runs.  The file is named so that pytest
-collects it last.
+its split-context partials in a fixed-size device array inside the library,
+shared by every call.  This test runs it on workloads of different sizes one
+after another -- long context, then GQA, then long context again, so that a
+call finds the array holding another call's partials -- through the raw C
+ABI and through the Python binding, and checks each output bit for bit
+against the regular entry point's (the same kernels with a caller-provided
+workspace and the same partitions give the same bits); it also checks that
+sizes needing more scratch than the array holds are refused before anything
+runs.  The file is named so that pytest collects it last.
 """
 import ctypes
 
@@ -20,7 +23,6 @@ import torch
 pytestmark = pytest.mark.gpu
 
 from paged_kv_cache_96_gb300 import workloads as W  # noqa: E402
-from stepping import ATOL, RTOL  # noqa: E402
 
 
 @pytest.fixture(scope="module")
@@ -42,25 +44,33 @@ def _raw_noalloc(L, st, P, stream):
         None, ctypes.c_void_p(stream.cuda_stream))
 
 
-@pytest.mark.parametrize("name", ["longctx", "gqa70b"])
-def test_noalloc_matches_workspace_entry_point(B, name):
+def _step(name, P):
     from paged_kv_cache_96_gb300 import step as S
     w = W.build(W.small_variant(name))
-    P = 32  # several partitions per sequence, so the scratch array is used
     st = S.DecodeStep(w, partition_size=P)
-    st.run()
+    st.run()  # the step's writes; then attention alone through each entry point
     st.attention(partition_size=P)
     torch.cuda.synchronize()
-    ref = S.to_float(st.out)
+    return st, st.out.clone()
+
+
+def test_noalloc_matches_workspace_entry_point(B):
+    P = 32  # several partitions per sequence, so the scratch array is used
+    steps = {n: _step(n, P) for n in ("longctx", "gqa70b")}
     L = B.lib()
     stream = torch.cuda.current_stream()
-    for call in range(2):
+    for call, name in enumerate(["longctx", "gqa70b", "longctx"]):
+        st, ref = steps[name]
         st.out.fill_(float("nan"))
-        assert _raw_noalloc(L, st, P, stream) == B.PA_OK, call
+        if call == 1:
+            B.pa_decode_attention_noalloc(st.out, st.query, st.key_cache, st.value_cache,
+                                          st.step_block_tables, st.context_lens,
+                                          st.max_context_len, st.w.scale, P)
+        else:
+            assert _raw_noalloc(L, st, P, stream) == B.PA_OK, call
         torch.cuda.synchronize()
-        got = S.to_float(st.out)
-        assert np.isfinite(got).all(), call
-        assert (np.abs(got - ref) <= ATOL + RTOL * np.abs(ref)).all(), call
+        assert torch.isfinite(st.out.float()).all(), (call, name)
+        assert torch.equal(st.out, ref), (call, name)
 
 
 def test_noalloc_refuses_oversized_workspace(B):
