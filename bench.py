@@ -731,10 +731,10 @@ def run_ours(args):
     # HBM minimum: each physical block once (a shared prefix counts once)
     attn_bytes = w.unique_kv_bytes() + w.qo_bytes()
     achieved = attn_bytes / attn_s / 1e9
-    kernel = "pa_decode_attention (paged_decode_kernel + paged_reduce_kernel)"
+    kernel = "pa_decode_attention (paged_decode_kernel, split contexts merged in the pass)"
     if st.fused_append:
         kernel = ("pa_decode_attention_append (paged_decode_kernel with the new tokens' "
-                  "append + paged_reduce_kernel)")
+                  "append, split contexts merged in the pass)")
     if st.cascade:
         kernel = ("pa_decode_attention_cascade (paged_decode_kernel + paged_mq_kernel "
                   "prefix pass + paged_reduce_kernel)")

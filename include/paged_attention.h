@@ -180,13 +180,18 @@ PA_API pa_status pa_copy_blocks(void *key_cache, void *value_cache,
  * needs for these sizes (0 when partition_size == 0 or every context fits in
  * one partition).  Layout, with P = ceil(max_context_len / partition_size)
  * and every region starting on a 256-byte boundary, in this order:
+ *     int32 counters[max(2^18, num_seqs * num_kv_heads)]  arrival counters
  *     float part_m[num_seqs][num_heads][P]            partition stabiliser m_j
  *     float part_l[num_seqs][num_heads][P]            sum_p exp(score_p - m_j)
  *     float part_o[num_seqs][num_heads][P][head_dim]  partition output / l_j
  * score_p = scale * q . k_p (natural-log units).  m_j is a stabiliser: the
  * partition's log-sum-exp is m_j + log(l_j).  Partials are written only for
- * sequences that span more than one partition.  num_kv_heads is accepted for
- * symmetry with pa_decode_attention.  Returns 0 for invalid sizes.
+ * sequences that span more than one partition.  The counters must hold
+ * zeros before a workspace is first used (cudaMemsetAsync once after
+ * allocating it); every call leaves them at zero.  The counter region has
+ * the same size for every call with num_seqs * num_kv_heads <= 2^18, so one
+ * workspace, zeroed once, serves calls of any such sizes; a call with more
+ * needs its whole counter region zeroed first.  Returns 0 for invalid sizes.
  */
 PA_API size_t pa_decode_workspace_bytes(int num_seqs, int num_heads, int num_kv_heads,
                                  int head_dim, int max_context_len,
@@ -209,13 +214,18 @@ PA_API size_t pa_decode_workspace_bytes(int num_seqs, int num_heads, int num_kv_
  *                  head); otherwise a multiple of 16 tokens: contexts are
  *                  split into partitions of that many tokens.  The partition
  *                  pass writes a partial (m, l, o) per partition to the
- *                  workspace, and a reduce kernel, queued behind it on the
- *                  same stream by this call, merges them by log-sum-exp
- *                  weights l_j * exp(m_j - max m).  A sequence that fits one
- *                  partition is written by the pass directly.
+ *                  workspace and merges a sequence's partials by
+ *                  log-sum-exp weights l_j * exp(m_j - max m): in the same
+ *                  kernel, as soon as the last of them is written (an
+ *                  arrival counter per sequence and KV head), for sequences
+ *                  of up to 8 partitions; in a reduce kernel queued behind
+ *                  it by this call for longer ones.  A sequence that fits
+ *                  one partition is written by the pass directly.
  *   workspace    : device, 256-byte aligned, >= pa_decode_workspace_bytes(...)
- *                  bytes; no initial contents needed.  May be NULL when that
- *                  size is 0.  Calls sharing one workspace must not overlap.
+ *                  bytes, its counter region zeroed before first use (see
+ *                  pa_decode_workspace_bytes); the partial regions need no
+ *                  initial contents.  May be NULL when that size is 0.
+ *                  Calls sharing one workspace must not overlap.
  * Supported: head_dim 64 or 128; block_size a power of two from 16 to 256;
  * num_heads / num_kv_heads in 1..16; num_blocks * block_size < 2^31.
  */
@@ -369,7 +379,8 @@ PA_API pa_status pa_plan_prefix_groups(const int32_t *block_tables, int max_bloc
  * pa_cascade_workspace_bytes -- workspace of pa_decode_attention_cascade:
  * the layout of pa_decode_workspace_bytes with P = 1 + ceil(max_context_len
  * / partition_size) (1 + 1 for partition_size 0) partials per (sequence,
- * head); partial 0 is the shared prefix's.
+ * head); the first partials of a grouped sequence are its shared prefix's.
+ * Counter region as for pa_decode_workspace_bytes (zero before first use).
  */
 PA_API size_t pa_cascade_workspace_bytes(int num_seqs, int num_heads, int num_kv_heads,
                                          int head_dim, int max_context_len,
@@ -460,7 +471,10 @@ PA_API pa_status pa_decode_attention_cascade_append(
  *     cudaDeviceReset (a new context), the next call looks it up again, so
  *     make that call, too, before any capture.
  *   - Every call on a device shares the one array and leaves its last
- *     contents there; no part of it needs to start at zero (each call
+ *     contents there.  Its counter region (the workspace layout of
+ *     pa_decode_workspace_bytes) starts at zero, since the array is
+ *     zero-filled when the library's device code is loaded, and every call
+ *     leaves it at zero; the partials need no initial contents (each call
  *     writes every partial it later reads).  Calls whose GPU work overlaps
  *     in time (for instance on two streams) race on the array.
  */

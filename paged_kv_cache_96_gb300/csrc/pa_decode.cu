@@ -63,10 +63,11 @@ template <int D, int NT, int NW, int NST, int EB> struct Layout {
     static constexpr int kMergeO = kStages + NW * NST * kStageBytes;
     static constexpr int kMergeM = kMergeO + NW * kHeads * kPitch * 4;
     static constexpr int kMergeL = kMergeM + NW * kHeads * 4;
-    // fused append: the new token's value row (fp32) and per-head scores
+    // fused append: the new token's value row (fp32) and per-head scores,
+    // one buffer per parity of the CTA's unit count
     static constexpr int kAppV = kMergeL + NW * kHeads * 4;
-    static constexpr int kAppM = kAppV + D * 4;
-    static constexpr int kBars = kAppM + kHeads * 4;
+    static constexpr int kAppM = kAppV + 2 * D * 4;
+    static constexpr int kBars = kAppM + 2 * kHeads * 4;  // NW * NST stage barriers
     static constexpr int kFlags = kBars + NW * NST * 8;
     static constexpr int kSeq = kFlags + NW * NST * 4;  // int ctx[S], prefix[S + 1], start[S]
     static size_t bytes(int num_seqs) { return 1024 + kSeq + 4 * (3 * (size_t)num_seqs + 1); }
@@ -185,14 +186,16 @@ __device__ __noinline__ void append_token(const DecodeParams &p, int s, int kh, 
 // sit in four 16K sub-partition files and each warp lives in one of them, so
 // the binding limit is the fullest file (ceil(NW * MINB / 4) warps).  The
 // thread count given to __launch_bounds__ is the one whose even split over
-// MINB CTAs yields that per-warp budget (the block itself is NW warps).
+// MINB CTAs yields that per-warp budget, in whole warps (the compiler rounds
+// a partial warp up, which would shrink the budget); the block itself is NW
+// warps.
 constexpr int bound_threads(int NW, int MINB)
 {
-    return 128 * ((NW * MINB + 3) / 4) / MINB;
+    return 128 * ((NW * MINB + 3) / 4) / MINB / 32 * 32;
 }
 
 template <typename T, typename KV, int D, int NT, int NW, int NST, int MINB>
-__global__ void __launch_bounds__(bound_threads(NW, MINB), MINB)
+__global__ void __launch_bounds__(bound_threads(NW + 1, MINB), MINB)
     paged_decode_kernel(const __grid_constant__ DecodeParams p,
                         const __grid_constant__ CUtensorMap tmap_k,
                         const __grid_constant__ CUtensorMap tmap_v)
@@ -204,7 +207,8 @@ __global__ void __launch_bounds__(bound_threads(NW, MINB), MINB)
     using Op = MmaOp<MT>;
     constexpr int KT = D / 16;  // k-steps of the score product, m-tiles of the output
     constexpr int kHeads = L::kHeads;
-    constexpr int kThreads = NW * 32;
+    constexpr int kThreads = (NW + 1) * 32;  // NW tile warps, then the merge warp
+    static_assert(bound_threads(NW + 1, MINB) >= kThreads, "launch bound below the block size");
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_addr(smem_raw);
@@ -238,8 +242,7 @@ __global__ void __launch_bounds__(bound_threads(NW, MINB), MINB)
     auto stage_of = [&](int stage) {
         return sbase + L::kStages + (warp * NST + stage) * L::kStageBytes;
     };
-
-    if (lane == 0) {
+    if (lane == 0 && warp < NW) {
         for (int k = 0; k < NST; ++k)
             mbar_init(bar_of(k), 1);
         fence_barrier_init();
@@ -324,7 +327,7 @@ __global__ void __launch_bounds__(bound_threads(NW, MINB), MINB)
 
     // ---- this warp's fetch cursor: its next tile, possibly in a later unit ----
     int pu = blockIdx.x, ps = 0, pkh = 0, pj = 0, ptok0 = 0, pnt = 0, ptile = warp;
-    bool pdone = pu >= total_units;
+    bool pdone = pu >= total_units || warp >= NW;  // the merge warp fetches nothing
     if (!pdone)
         decode_unit(pu, ps, pkh, pj, ptok0, pnt);
     auto skip_empty = [&]() {
@@ -447,311 +450,346 @@ __global__ void __launch_bounds__(bound_threads(NW, MINB), MINB)
             }
         }
     };
-    if (blockIdx.x < total_units) {
+    if (blockIdx.x < total_units && warp < NW) {
         int s, kh, j, tok0, ntiles;
         decode_unit(blockIdx.x, s, kh, j, tok0, ntiles);
         load_query(s, kh);
     }
 
     // ---- units --------------------------------------------------------------------
-    for (int u = blockIdx.x; u < total_units; u += gridDim.x) {
-        int s, kh, j, tok0, ntiles;
-        decode_unit(u, s, kh, j, tok0, ntiles);
-        const int tok_end = min(ctx_s[s] - napp, tok0 + P);
-        // fused append: the sequence's last unit also takes the new token
-        const bool app = napp != 0 && tok0 + P >= ctx_s[s];
-        const int nparts = pref[s + 1] - pref[s];
-        // the first partials belong to the prefix pass
-        const int pbase = prefix_partitions(start_s[s], P);
+    // The tile warps stream a unit's tiles and hand their (m, l, O) to the
+    // merge warp through shared memory; the merge warp combines them (and the
+    // appended token's record), writes the output row or the partition's
+    // partial, and -- for split sequences -- arrives on the sequence's counter
+    // and merges the partials when its arrival completes them.  The two sides
+    // meet only at two named barriers per unit ("records written": the tile
+    // warps arrive, the merge warp waits; "records read": the other way
+    // round, skipped after the CTA's last unit), so tile warps never wait for
+    // each other at a unit's end and the merge warp sleeps in hardware.
+    constexpr int kRecFull = 1, kRecFree = 2;  // named barrier ids (0 is __syncthreads)
+    if (warp < NW) {
+        int k_unit = 0;          // units of this CTA so far
+        bool rec_aborted = false;
+        for (int u = blockIdx.x; u < total_units; u += gridDim.x, ++k_unit) {
+            int s, kh, j, tok0, ntiles;
+            decode_unit(u, s, kh, j, tok0, ntiles);
+            const int tok_end = min(ctx_s[s] - napp, tok0 + P);
+            // fused append: the sequence's last unit also takes the new token
+            const bool app = napp != 0 && tok0 + P >= ctx_s[s];
 
-        float o[KT][NT][4];
-        float mrun[NT][2], lrun[NT][2];
+            float o[KT][NT][4];
+            float mrun[NT][2], lrun[NT][2];
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-            mrun[nt][0] = mrun[nt][1] = -INFINITY;
-            lrun[nt][0] = lrun[nt][1] = 0.f;
+            for (int nt = 0; nt < NT; ++nt) {
+                mrun[nt][0] = mrun[nt][1] = -INFINITY;
+                lrun[nt][0] = lrun[nt][1] = 0.f;
 #pragma unroll
-            for (int mt = 0; mt < KT; ++mt)
-                o[mt][nt][0] = o[mt][nt][1] = o[mt][nt][2] = o[mt][nt][3] = 0.f;
-        }
-        // the new token counts as tile ntiles of the round-robin deal: its
-        // warp is one with a tile fewer than the others (or the first)
-        if (app && warp == ntiles % NW)
-            append_token<T, kFp8, D, kHeads>(p, s, kh, ctx_s[s] - 1, app_v, app_m, lane);
-
-        for (int tile = warp; tile < ntiles; tile += NW) {
-            const int stage = consumed % NST;
-            const uint32_t parity = (consumed / NST) & 1u;
-            bool ready = false;
-            if (!aborted) {
-                ready = __all_sync(kFull, mbar_wait_bounded(bar_of(stage), parity, p.wait_ns));
-                if (ready) {
-                    inflight &= ~(1u << stage);
-                } else {
-                    aborted = true;
-                    if (lane == 0)
-                        flag_error(p.error_word, PA_DEVERR_TIMEOUT);
-                }
+                for (int mt = 0; mt < KT; ++mt)
+                    o[mt][nt][0] = o[mt][nt][1] = o[mt][nt][2] = o[mt][nt][3] = 0.f;
             }
-            if (ready && flags[warp * NST + stage] != 0) {
-                const uint32_t kbase = stage_of(stage);
-                const uint32_t vbase = kbase + L::kTileBytes;
-                const int nv = tok_end - (tok0 + tile * kTileTokens);  // valid rows
-                const bool partial = nv < kTileTokens;
+            // the new token counts as tile ntiles of the round-robin deal: its
+            // warp is one with a tile fewer than the others (or the first)
+            if (app && warp == ntiles % NW)
+                append_token<T, kFp8, D, kHeads>(p, s, kh, ctx_s[s] - 1, app_v + (k_unit & 1) * D,
+                                                 app_m + (k_unit & 1) * kHeads, lane);
 
-                // scores S[token][head] = K . Q^T in independent accumulator
-                // chains (k-step kk feeds chain kk % kChains), summed at the end
-                constexpr int kChains = KT >= 4 ? 4 : KT;
-                float part[kChains][NT][4];
+            for (int tile = warp; tile < ntiles; tile += NW) {
+                const int stage = consumed % NST;
+                const uint32_t parity = (consumed / NST) & 1u;
+                bool ready = false;
+                if (!aborted) {
+                    ready = __all_sync(kFull, mbar_wait_bounded(bar_of(stage), parity, p.wait_ns));
+                    if (ready) {
+                        inflight &= ~(1u << stage);
+                    } else {
+                        aborted = true;
+                        if (lane == 0)
+                            flag_error(p.error_word, PA_DEVERR_TIMEOUT);
+                    }
+                }
+                if (ready && flags[warp * NST + stage] != 0) {
+                    const uint32_t kbase = stage_of(stage);
+                    const uint32_t vbase = kbase + L::kTileBytes;
+                    const int nv = tok_end - (tok0 + tile * kTileTokens);  // valid rows
+                    const bool partial = nv < kTileTokens;
+
+                    // scores S[token][head] = K . Q^T in independent accumulator
+                    // chains (k-step kk feeds chain kk % kChains), summed at the end
+                    constexpr int kChains = KT >= 4 ? 4 : KT;
+                    float part[kChains][NT][4];
 #pragma unroll
-                for (int c = 0; c < kChains; ++c)
+                    for (int c = 0; c < kChains; ++c)
 #pragma unroll
-                    for (int nt = 0; nt < NT; ++nt)
-                        part[c][nt][0] = part[c][nt][1] = part[c][nt][2] = part[c][nt][3] = 0.f;
-                if constexpr (kFp8) {
-                    // one ldmatrix brings two 16-d chunks of 16 tokens as byte
-                    // pairs: thread (g, t4) gets d = 16c + 4t4 .. +3 of tokens g
-                    // and g + 8; widening gives the (permuted-k) A fragment
+                        for (int nt = 0; nt < NT; ++nt)
+                            part[c][nt][0] = part[c][nt][1] = part[c][nt][2] = part[c][nt][3] = 0.f;
+                    if constexpr (kFp8) {
+                        // one ldmatrix brings two 16-d chunks of 16 tokens as byte
+                        // pairs: thread (g, t4) gets d = 16c + 4t4 .. +3 of tokens g
+                        // and g + 8; widening gives the (permuted-k) A fragment
 #pragma unroll
-                    for (int kp = 0; kp < KT / 2; ++kp) {
-                        uint32_t r[4];
-                        ldmatrix_x4(tile_addr(kbase, k_row, 0, 2 * kp + k_cj), r);
+                        for (int kp = 0; kp < KT / 2; ++kp) {
+                            uint32_t r[4];
+                            ldmatrix_x4(tile_addr(kbase, k_row, 0, 2 * kp + k_cj), r);
 #pragma unroll
-                        for (int h = 0; h < 2; ++h) {
-                            const int kk = 2 * kp + h;
-                            const uint32_t w0 = r[2 * h], w1 = r[2 * h + 1];
+                            for (int h = 0; h < 2; ++h) {
+                                const int kk = 2 * kp + h;
+                                const uint32_t w0 = r[2 * h], w1 = r[2 * h + 1];
+                                uint32_t a[4];
+                                a[0] = e4m3x2_to_f16x2((uint16_t)(w0 & 0xffffu));
+                                a[1] = e4m3x2_to_f16x2((uint16_t)(w1 & 0xffffu));
+                                a[2] = e4m3x2_to_f16x2((uint16_t)(w0 >> 16));
+                                a[3] = e4m3x2_to_f16x2((uint16_t)(w1 >> 16));
+#pragma unroll
+                                for (int nt = 0; nt < NT; ++nt)
+                                    Op::run(part[kk % kChains][nt], a, qf[nt][kk][0], qf[nt][kk][1]);
+                            }
+                        }
+                    } else {
+#pragma unroll
+                        for (int kk = 0; kk < KT; ++kk) {
                             uint32_t a[4];
-                            a[0] = e4m3x2_to_f16x2((uint16_t)(w0 & 0xffffu));
-                            a[1] = e4m3x2_to_f16x2((uint16_t)(w1 & 0xffffu));
-                            a[2] = e4m3x2_to_f16x2((uint16_t)(w0 >> 16));
-                            a[3] = e4m3x2_to_f16x2((uint16_t)(w1 >> 16));
+                            ldmatrix_x4(tile_addr(kbase, k_row, kk >> 2, (kk & 3) * 2 + k_cj), a);
 #pragma unroll
                             for (int nt = 0; nt < NT; ++nt)
                                 Op::run(part[kk % kChains][nt], a, qf[nt][kk][0], qf[nt][kk][1]);
                         }
                     }
-                } else {
-#pragma unroll
-                    for (int kk = 0; kk < KT; ++kk) {
-                        uint32_t a[4];
-                        ldmatrix_x4(tile_addr(kbase, k_row, kk >> 2, (kk & 3) * 2 + k_cj), a);
-#pragma unroll
-                        for (int nt = 0; nt < NT; ++nt)
-                            Op::run(part[kk % kChains][nt], a, qf[nt][kk][0], qf[nt][kk][1]);
-                    }
-                }
-                float sc[NT][4];
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        float x = part[0][nt][e];
-#pragma unroll
-                        for (int c = 1; c < kChains; ++c)
-                            x += part[c][nt][e];
-                        sc[nt][e] = x;
-                    }
-
-                // V^T fragments (their latency overlaps the softmax); rows past
-                // the context are zeroed so NaN padding never meets a zero weight
-                uint32_t va[KT][4];
-                if constexpr (kFp8) {
-                    // transposed byte-pair loads: thread (g, t4) gets tokens 2t4,
-                    // 2t4+1 (and +8, +9) at d = 16c + 2g, 2g+1; fragment row g is
-                    // d = 16c + 2g and row g + 8 is d = 16c + 2g + 1
-#pragma unroll
-                    for (int mp = 0; mp < KT / 2; ++mp) {
-                        uint32_t r[4];
-                        ldmatrix_x4_trans(tile_addr(vbase, k_row, 0, 2 * mp + k_cj), r);
-#pragma unroll
-                        for (int h = 0; h < 2; ++h) {
-                            const uint32_t p0 = byte_perm(r[2 * h], 0u, 0x3120u);
-                            const uint32_t p1 = byte_perm(r[2 * h + 1], 0u, 0x3120u);
-                            va[2 * mp + h][0] = e4m3x2_to_f16x2((uint16_t)(p0 & 0xffffu));
-                            va[2 * mp + h][1] = e4m3x2_to_f16x2((uint16_t)(p0 >> 16));
-                            va[2 * mp + h][2] = e4m3x2_to_f16x2((uint16_t)(p1 & 0xffffu));
-                            va[2 * mp + h][3] = e4m3x2_to_f16x2((uint16_t)(p1 >> 16));
-                        }
-                    }
-                } else {
-#pragma unroll
-                    for (int mt = 0; mt < KT; ++mt)
-                        ldmatrix_x4_trans(tile_addr(vbase, v_row, mt >> 2, (mt & 3) * 2 + v_cj),
-                                          va[mt]);
-                }
-                if (partial) {
-                    const uint32_t m01 = (2 * t4 < nv ? 0x0000ffffu : 0u) |
-                                         (2 * t4 + 1 < nv ? 0xffff0000u : 0u);
-                    const uint32_t m89 = (2 * t4 + 8 < nv ? 0x0000ffffu : 0u) |
-                                         (2 * t4 + 9 < nv ? 0xffff0000u : 0u);
-#pragma unroll
-                    for (int mt = 0; mt < KT; ++mt) {
-                        va[mt][0] &= m01;
-                        va[mt][1] &= m01;
-                        va[mt][2] &= m89;
-                        va[mt][3] &= m89;
-                    }
-                }
-
-                // online softmax; P^T fragments for the value product
-                uint32_t pb[NT][2];
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt) {
-                    float s0 = sc[nt][0] * p.scale_log2, s1 = sc[nt][1] * p.scale_log2;
-                    float s2 = sc[nt][2] * p.scale_log2, s3 = sc[nt][3] * p.scale_log2;
-                    if (partial) {
-                        if (g >= nv)
-                            s0 = s1 = -INFINITY;
-                        if (g + 8 >= nv)
-                            s2 = s3 = -INFINITY;
-                    }
-                    // mrun is a reference point, not necessarily the running max:
-                    // while every score of the tile stays within kSlack of it
-                    // (weights <= 2^kSlack) it is kept, which skips the
-                    // cross-lane max and the rescale; otherwise it moves up to
-                    // the running max and l and O are rescaled.
-                    const bool fits = s0 <= mrun[nt][0] + kSlack && s2 <= mrun[nt][0] + kSlack &&
-                                      s1 <= mrun[nt][1] + kSlack && s3 <= mrun[nt][1] + kSlack;
-                    if (!__all_sync(kFull, fits)) {
-                        float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
-#pragma unroll
-                        for (int off = 4; off < 32; off <<= 1) {
-                            mx0 = fmaxf(mx0, __shfl_xor_sync(kFull, mx0, off));
-                            mx1 = fmaxf(mx1, __shfl_xor_sync(kFull, mx1, off));
-                        }
-                        const float mn0 = fmaxf(mrun[nt][0], mx0);
-                        const float mn1 = fmaxf(mrun[nt][1], mx1);
-                        const float al0 = mn0 == -INFINITY ? 1.f : exp2f(mrun[nt][0] - mn0);
-                        const float al1 = mn1 == -INFINITY ? 1.f : exp2f(mrun[nt][1] - mn1);
-                        lrun[nt][0] *= al0;
-                        lrun[nt][1] *= al1;
-#pragma unroll
-                        for (int mt = 0; mt < KT; ++mt) {
-                            o[mt][nt][0] *= al0;
-                            o[mt][nt][1] *= al1;
-                            o[mt][nt][2] *= al0;
-                            o[mt][nt][3] *= al1;
-                        }
-                        mrun[nt][0] = mn0;
-                        mrun[nt][1] = mn1;
-                    }
-                    const float mu0 = mrun[nt][0] == -INFINITY ? 0.f : mrun[nt][0];
-                    const float mu1 = mrun[nt][1] == -INFINITY ? 0.f : mrun[nt][1];
-                    const float p0 = exp2f(s0 - mu0), p2 = exp2f(s2 - mu0);
-                    const float p1 = exp2f(s1 - mu1), p3 = exp2f(s3 - mu1);
-                    lrun[nt][0] += p0 + p2;
-                    lrun[nt][1] += p1 + p3;
-                    pb[nt][0] = movmatrix_trans(Op::pack(p0, p1));
-                    pb[nt][1] = movmatrix_trans(Op::pack(p2, p3));
-                }
-
-                // O^T[d][head] += V^T . P^T
-#pragma unroll
-                for (int mt = 0; mt < KT; ++mt)
+                    float sc[NT][4];
 #pragma unroll
                     for (int nt = 0; nt < NT; ++nt)
-                        Op::run(o[mt][nt], va[mt], pb[nt][0], pb[nt][1]);
-            }
-            __syncwarp();
-            ++consumed;
-            produce();  // refill the stage just consumed
-        }
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            float x = part[0][nt][e];
+#pragma unroll
+                            for (int c = 1; c < kChains; ++c)
+                                x += part[c][nt][e];
+                            sc[nt][e] = x;
+                        }
 
-        // Next unit's query: its loads land while this unit's merge runs.
-        if (u + (int)gridDim.x < total_units) {
-            int sn, khn, jn, tn, ntn;
-            decode_unit(u + gridDim.x, sn, khn, jn, tn, ntn);
-            load_query(sn, khn);
-        }
+                    // V^T fragments (their latency overlaps the softmax); rows past
+                    // the context are zeroed so NaN padding never meets a zero weight
+                    uint32_t va[KT][4];
+                    if constexpr (kFp8) {
+                        // transposed byte-pair loads: thread (g, t4) gets tokens 2t4,
+                        // 2t4+1 (and +8, +9) at d = 16c + 2g, 2g+1; fragment row g is
+                        // d = 16c + 2g and row g + 8 is d = 16c + 2g + 1
+#pragma unroll
+                        for (int mp = 0; mp < KT / 2; ++mp) {
+                            uint32_t r[4];
+                            ldmatrix_x4_trans(tile_addr(vbase, k_row, 0, 2 * mp + k_cj), r);
+#pragma unroll
+                            for (int h = 0; h < 2; ++h) {
+                                const uint32_t p0 = byte_perm(r[2 * h], 0u, 0x3120u);
+                                const uint32_t p1 = byte_perm(r[2 * h + 1], 0u, 0x3120u);
+                                va[2 * mp + h][0] = e4m3x2_to_f16x2((uint16_t)(p0 & 0xffffu));
+                                va[2 * mp + h][1] = e4m3x2_to_f16x2((uint16_t)(p0 >> 16));
+                                va[2 * mp + h][2] = e4m3x2_to_f16x2((uint16_t)(p1 & 0xffffu));
+                                va[2 * mp + h][3] = e4m3x2_to_f16x2((uint16_t)(p1 >> 16));
+                            }
+                        }
+                    } else {
+#pragma unroll
+                        for (int mt = 0; mt < KT; ++mt)
+                            ldmatrix_x4_trans(tile_addr(vbase, v_row, mt >> 2, (mt & 3) * 2 + v_cj),
+                                              va[mt]);
+                    }
+                    if (partial) {
+                        const uint32_t m01 = (2 * t4 < nv ? 0x0000ffffu : 0u) |
+                                             (2 * t4 + 1 < nv ? 0xffff0000u : 0u);
+                        const uint32_t m89 = (2 * t4 + 8 < nv ? 0x0000ffffu : 0u) |
+                                             (2 * t4 + 9 < nv ? 0xffff0000u : 0u);
+#pragma unroll
+                        for (int mt = 0; mt < KT; ++mt) {
+                            va[mt][0] &= m01;
+                            va[mt][1] &= m01;
+                            va[mt][2] &= m89;
+                            va[mt][3] &= m89;
+                        }
+                    }
 
-        // ---- end of unit: merge the warps' (m, l, O) ------------------------------
+                    // online softmax; P^T fragments for the value product
+                    uint32_t pb[NT][2];
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
+                    for (int nt = 0; nt < NT; ++nt) {
+                        float s0 = sc[nt][0] * p.scale_log2, s1 = sc[nt][1] * p.scale_log2;
+                        float s2 = sc[nt][2] * p.scale_log2, s3 = sc[nt][3] * p.scale_log2;
+                        if (partial) {
+                            if (g >= nv)
+                                s0 = s1 = -INFINITY;
+                            if (g + 8 >= nv)
+                                s2 = s3 = -INFINITY;
+                        }
+                        // mrun is a reference point, not necessarily the running max:
+                        // while every score of the tile stays within kSlack of it
+                        // (weights <= 2^kSlack) it is kept, which skips the
+                        // cross-lane max and the rescale; otherwise it moves up to
+                        // the running max and l and O are rescaled.
+                        const bool fits = s0 <= mrun[nt][0] + kSlack && s2 <= mrun[nt][0] + kSlack &&
+                                          s1 <= mrun[nt][1] + kSlack && s3 <= mrun[nt][1] + kSlack;
+                        if (!__all_sync(kFull, fits)) {
+                            float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
 #pragma unroll
-            for (int k = 0; k < 2; ++k)
+                            for (int off = 4; off < 32; off <<= 1) {
+                                mx0 = fmaxf(mx0, __shfl_xor_sync(kFull, mx0, off));
+                                mx1 = fmaxf(mx1, __shfl_xor_sync(kFull, mx1, off));
+                            }
+                            const float mn0 = fmaxf(mrun[nt][0], mx0);
+                            const float mn1 = fmaxf(mrun[nt][1], mx1);
+                            const float al0 = mn0 == -INFINITY ? 1.f : exp2f(mrun[nt][0] - mn0);
+                            const float al1 = mn1 == -INFINITY ? 1.f : exp2f(mrun[nt][1] - mn1);
+                            lrun[nt][0] *= al0;
+                            lrun[nt][1] *= al1;
 #pragma unroll
-                for (int off = 4; off < 32; off <<= 1)
-                    lrun[nt][k] += __shfl_xor_sync(kFull, lrun[nt][k], off);
-        {
-            float *mo = merge_o + warp * kHeads * L::kPitch;
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-                const int h0 = nt * 8 + 2 * t4;
-#pragma unroll
-                for (int mt = 0; mt < KT; ++mt) {
-                    // fragment rows g, g + 8 are d = 16mt + g, + 8 (16-bit pools)
-                    // or d = 16mt + 2g, + 1 (FP8 pools)
-                    const int d0 = kFp8 ? mt * 16 + 2 * g : mt * 16 + g;
-                    const int d1 = kFp8 ? d0 + 1 : d0 + 8;
-                    mo[h0 * L::kPitch + d0] = o[mt][nt][0];
-                    mo[(h0 + 1) * L::kPitch + d0] = o[mt][nt][1];
-                    mo[h0 * L::kPitch + d1] = o[mt][nt][2];
-                    mo[(h0 + 1) * L::kPitch + d1] = o[mt][nt][3];
-                }
-                if (g == 0) {
-                    merge_m[warp * kHeads + h0] = mrun[nt][0];
-                    merge_m[warp * kHeads + h0 + 1] = mrun[nt][1];
-                    merge_l[warp * kHeads + h0] = lrun[nt][0];
-                    merge_l[warp * kHeads + h0 + 1] = lrun[nt][1];
-                }
-            }
-        }
-        __syncthreads();
+                            for (int mt = 0; mt < KT; ++mt) {
+                                o[mt][nt][0] *= al0;
+                                o[mt][nt][1] *= al1;
+                                o[mt][nt][2] *= al0;
+                                o[mt][nt][3] *= al1;
+                            }
+                            mrun[nt][0] = mn0;
+                            mrun[nt][1] = mn1;
+                        }
+                        const float mu0 = mrun[nt][0] == -INFINITY ? 0.f : mrun[nt][0];
+                        const float mu1 = mrun[nt][1] == -INFINITY ? 0.f : mrun[nt][1];
+                        const float p0 = exp2f(s0 - mu0), p2 = exp2f(s2 - mu0);
+                        const float p1 = exp2f(s1 - mu1), p3 = exp2f(s3 - mu1);
+                        lrun[nt][0] += p0 + p2;
+                        lrun[nt][1] += p1 + p3;
+                        pb[nt][0] = movmatrix_trans(Op::pack(p0, p1));
+                        pb[nt][1] = movmatrix_trans(Op::pack(p2, p3));
+                    }
 
-        const int items = G * (D / 8);
-        for (int it = tid; it < items; it += kThreads) {
-            const int jh = it / (D / 8);
-            const int d0 = (it - jh * (D / 8)) * 8;
-            float mmax = -INFINITY;
+                    // O^T[d][head] += V^T . P^T
 #pragma unroll
-            for (int w = 0; w < NW; ++w)
-                mmax = fmaxf(mmax, merge_m[w * kHeads + jh]);
-            if (app)
-                mmax = fmaxf(mmax, app_m[jh]);
-            const float mu = mmax == -INFINITY ? 0.f : mmax;
-            float lsum = 0.f;
-            float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                    for (int mt = 0; mt < KT; ++mt)
 #pragma unroll
-            for (int w = 0; w < NW; ++w) {
-                const float wgt = exp2f(merge_m[w * kHeads + jh] - mu);
-                lsum += wgt * merge_l[w * kHeads + jh];
-                const float4 *src = reinterpret_cast<const float4 *>(
-                    merge_o + (w * kHeads + jh) * L::kPitch + d0);
-                const float4 x0 = src[0], x1 = src[1];
-                acc[0] += wgt * x0.x; acc[1] += wgt * x0.y; acc[2] += wgt * x0.z; acc[3] += wgt * x0.w;
-                acc[4] += wgt * x1.x; acc[5] += wgt * x1.y; acc[6] += wgt * x1.z; acc[7] += wgt * x1.w;
+                        for (int nt = 0; nt < NT; ++nt)
+                            Op::run(o[mt][nt], va[mt], pb[nt][0], pb[nt][1]);
+                }
+                __syncwarp();
+                ++consumed;
+                produce();  // refill the stage just consumed
             }
-            if (app) {
-                // the new token: m = its score, l = 1, o = its value row
-                const float wgt = exp2f(app_m[jh] - mu);
-                lsum += wgt;
-#pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    acc[e] += wgt * app_v[d0 + e];
+
+            // Next unit's query: its loads land while this unit's records go out.
+            if (u + (int)gridDim.x < total_units) {
+                int sn, khn, jn, tn, ntn;
+                decode_unit(u + gridDim.x, sn, khn, jn, tn, ntn);
+                load_query(sn, khn);
             }
-            const float inv = p.out_scale / lsum;
-            const size_t h = (size_t)kh * G + jh;
-            if (nparts == 1 && pbase == 0) {
-                T vals[8];
+
+            // ---- end of unit: this warp's (m, l, O) to the merge warp -------------------
 #pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    vals[e] = MmaOp<T>::from_float(acc[e] * inv);
-                *reinterpret_cast<uint4 *>(static_cast<T *>(p.out) +
-                                           ((size_t)s * p.num_heads + h) * D + d0) =
-                    *reinterpret_cast<const uint4 *>(vals);
-            } else {
-                // partial of partition j, merged by the reduce kernel
-                const size_t idx = ((size_t)s * p.num_heads + h) * p.max_parts + pbase + j;
-                float4 *dst = reinterpret_cast<float4 *>(p.part_o + idx * D + d0);
-                dst[0] = make_float4(acc[0] * inv, acc[1] * inv, acc[2] * inv, acc[3] * inv);
-                dst[1] = make_float4(acc[4] * inv, acc[5] * inv, acc[6] * inv, acc[7] * inv);
-                if (d0 == 0) {
-                    p.part_m[idx] = mmax * kLn2;
-                    p.part_l[idx] = lsum;
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int k = 0; k < 2; ++k)
+#pragma unroll
+                    for (int off = 4; off < 32; off <<= 1)
+                        lrun[nt][k] += __shfl_xor_sync(kFull, lrun[nt][k], off);
+            // the merge warp has read the previous unit's records
+            if (k_unit > 0)
+                named_barrier_sync(kRecFree, kThreads);
+            {
+                float *mo = merge_o + warp * kHeads * L::kPitch;
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    const int h0 = nt * 8 + 2 * t4;
+#pragma unroll
+                    for (int mt = 0; mt < KT; ++mt) {
+                        // fragment rows g, g + 8 are d = 16mt + g, + 8 (16-bit pools)
+                        // or d = 16mt + 2g, + 1 (FP8 pools)
+                        const int d0 = kFp8 ? mt * 16 + 2 * g : mt * 16 + g;
+                        const int d1 = kFp8 ? d0 + 1 : d0 + 8;
+                        mo[h0 * L::kPitch + d0] = o[mt][nt][0];
+                        mo[(h0 + 1) * L::kPitch + d0] = o[mt][nt][1];
+                        mo[h0 * L::kPitch + d1] = o[mt][nt][2];
+                        mo[(h0 + 1) * L::kPitch + d1] = o[mt][nt][3];
+                    }
+                    if (g == 0) {
+                        merge_m[warp * kHeads + h0] = mrun[nt][0];
+                        merge_m[warp * kHeads + h0 + 1] = mrun[nt][1];
+                        merge_l[warp * kHeads + h0] = lrun[nt][0];
+                        merge_l[warp * kHeads + h0 + 1] = lrun[nt][1];
+                    }
                 }
             }
+            named_barrier_arrive(kRecFull, kThreads);  // this unit's records are written
         }
-        __syncthreads();  // merge scratch is reused by the next unit
+    } else {
+        // ===== the merge warp ======================================================
+        int k_unit = 0;
+        for (int u = blockIdx.x; u < total_units; u += gridDim.x, ++k_unit) {
+            int s, kh, j, tok0, ntiles;
+            decode_unit(u, s, kh, j, tok0, ntiles);
+            const bool app = napp != 0 && tok0 + P >= ctx_s[s];
+            const int nparts = pref[s + 1] - pref[s];
+            // the first partials belong to the prefix pass
+            const int pbase = prefix_partitions(start_s[s], P);
+            const bool split = nparts > 1 || pbase > 0;
+            named_barrier_sync(kRecFull, kThreads);  // every tile warp's records are in
+            const float *av = app_v + (k_unit & 1) * D;
+            const float *am = app_m + (k_unit & 1) * kHeads;
+            const int items = G * (D / 8);
+            for (int it = lane; it < items; it += 32) {
+                const int jh = it / (D / 8);
+                const int d0 = (it - jh * (D / 8)) * 8;
+                float mmax = -INFINITY;
+#pragma unroll
+                for (int w = 0; w < NW; ++w)
+                    mmax = fmaxf(mmax, merge_m[w * kHeads + jh]);
+                if (app)
+                    mmax = fmaxf(mmax, am[jh]);
+                const float mu = mmax == -INFINITY ? 0.f : mmax;
+                float lsum = 0.f;
+                float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int w = 0; w < NW; ++w) {
+                    const float wgt = exp2f(merge_m[w * kHeads + jh] - mu);
+                    lsum += wgt * merge_l[w * kHeads + jh];
+                    const float4 *src = reinterpret_cast<const float4 *>(
+                        merge_o + (w * kHeads + jh) * L::kPitch + d0);
+                    const float4 x0 = src[0], x1 = src[1];
+                    acc[0] += wgt * x0.x; acc[1] += wgt * x0.y; acc[2] += wgt * x0.z; acc[3] += wgt * x0.w;
+                    acc[4] += wgt * x1.x; acc[5] += wgt * x1.y; acc[6] += wgt * x1.z; acc[7] += wgt * x1.w;
+                }
+                if (app) {
+                    // the new token: m = its score, l = 1, o = its value row
+                    const float wgt = exp2f(am[jh] - mu);
+                    lsum += wgt;
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        acc[e] += wgt * av[d0 + e];
+                }
+                const float inv = p.out_scale / lsum;
+                const size_t h = (size_t)kh * G + jh;
+                if (!split) {
+                    T vals[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        vals[e] = MmaOp<T>::from_float(acc[e] * inv);
+                    *reinterpret_cast<uint4 *>(static_cast<T *>(p.out) +
+                                               ((size_t)s * p.num_heads + h) * D + d0) =
+                        *reinterpret_cast<const uint4 *>(vals);
+                } else {
+                    // partial of partition j, merged below (or by the reduce kernel)
+                    const size_t idx = ((size_t)s * p.num_heads + h) * p.max_parts + pbase + j;
+                    float4 *dst = reinterpret_cast<float4 *>(p.part_o + idx * D + d0);
+                    dst[0] = make_float4(acc[0] * inv, acc[1] * inv, acc[2] * inv, acc[3] * inv);
+                    dst[1] = make_float4(acc[4] * inv, acc[5] * inv, acc[6] * inv, acc[7] * inv);
+                    if (d0 == 0) {
+                        p.part_m[idx] = mmax * kLn2;
+                        p.part_l[idx] = lsum;
+                    }
+                }
+            }
+            // the records (and the append buffer) may be rewritten; the tile
+            // warps wait for this only from their next unit on
+            if (u + (int)gridDim.x < total_units)
+                named_barrier_arrive(kRecFree, kThreads);
+            if (split && p.counters != nullptr && pbase + nparts <= kMergeMax)
+                // records loaded per lane at once: fewer under the FP8 register cap
+                arrive_and_merge<T, D, kHeads, kFp8 ? 2 : 8>(p, s, kh, pbase + nparts, lane);
+        }
     }
     pdl_launch_dependents();
 
@@ -785,13 +823,13 @@ __global__ void __launch_bounds__(bound_threads(NW, MINB), MINB)
 #define PA_DECODE_WARPS_FP8 4
 #endif
 #ifndef PA_DECODE_STAGES_FP8
-#define PA_DECODE_STAGES_FP8 2
+#define PA_DECODE_STAGES_FP8 3
 #endif
 #ifndef PA_DECODE_MINB_FP8
-#define PA_DECODE_MINB_FP8 4
+#define PA_DECODE_MINB_FP8 3
 #endif
-// 16-bit pools: warps per CTA, ring stages per warp, CTAs per SM the
-// register budget is sized for.
+// 16-bit pools: tile warps per CTA (the merge warp comes on top), ring
+// stages per warp, CTAs per SM the register budget is sized for.
 constexpr int kWarps = PA_DECODE_WARPS;
 constexpr int kStagesPerWarp = PA_DECODE_STAGES;
 constexpr int kMinBlocks = PA_DECODE_MINB;
@@ -814,7 +852,7 @@ static pa_status launch_pass(const DecodeParams &prm, const CUtensorMap &mk,
     constexpr int MINB = NT > 1 ? 1 : kFp8 ? kMinBlocksFp8 : kMinBlocks;
     using L = Layout<D, NT, NW, NST, sizeof(KV)>;
     auto kernel = paged_decode_kernel<T, KV, D, NT, NW, NST, MINB>;
-    constexpr int kThreads = NW * 32;
+    constexpr int kThreads = (NW + 1) * 32;
     static KernelSetting setting[kMaxDevices];
     static std::mutex mu;
     const size_t smem = L::bytes(prm.num_seqs);
@@ -894,7 +932,10 @@ static pa_status launch_decode(const DecodeParams &prm, const CUtensorMap &mk,
     pa_status st = launch_pass<T, KV, D, NT, kStages>(pass, mk, mv, stream, max_units);
     if (st == PA_ERR_UNSUPPORTED)
         st = launch_pass<T, KV, D, NT, kStagesManySeqs>(pass, mk, mv, stream, max_units);
-    if (st != PA_OK || prm.max_parts <= 1)
+    // the pass merges split sequences of up to kMergeMax partials itself when
+    // it has arrival counters; the reduce kernel merges the rest
+    if (st != PA_OK || prm.max_parts <= 1 ||
+        (prm.counters != nullptr && prm.max_parts <= kMergeMax))
         return st;
     return launch_reduce<T, D>(prm, stream);
 }
@@ -911,7 +952,7 @@ extern "C" size_t pa_decode_workspace_bytes(int num_seqs, int num_heads, int num
         max_context_len < 0 || partition_size < 0)
         return 0;
     const int parts = num_parts(max_context_len, partition_size);
-    return workspace_layout(num_seqs, num_heads, head_dim, parts).total;
+    return workspace_layout(num_seqs, num_heads, num_kv_heads, head_dim, parts).total;
 }
 
 // 16-bit pools: tensor maps, then the kernel instance for (dtype, d, group).
@@ -1109,7 +1150,7 @@ extern "C" size_t pa_cascade_workspace_bytes(int num_seqs, int num_heads, int nu
         max_context_len < 0 || partition_size < 0)
         return 0;
     const int parts = num_parts(max_context_len, partition_size) + 1;
-    return workspace_layout(num_seqs, num_heads, head_dim, parts).total;
+    return workspace_layout(num_seqs, num_heads, num_kv_heads, head_dim, parts).total;
 }
 
 // Prefix-aware decode; with new_key non-null, the decode step's append fused
@@ -1162,7 +1203,8 @@ static pa_status run_cascade(void *out, const void *query, void *key_cache, void
     // partitions of part_tokens: ceil(L / P) + ceil((ctx - L) / P) <=
     // ceil(ctx / P) + 1 partials per (sequence, head)
     const int parts = prm.max_parts + 1;
-    const WorkspaceLayout wl = workspace_layout(num_seqs, num_heads, head_dim, parts);
+    const WorkspaceLayout wl = workspace_layout(num_seqs, num_heads, num_kv_heads, head_dim,
+                                                parts);
     if (workspace == nullptr || workspace_bytes < wl.total ||
         (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
         return PA_ERR_WORKSPACE;
@@ -1171,6 +1213,8 @@ static pa_status run_cascade(void *out, const void *query, void *key_cache, void
     prm.part_l = reinterpret_cast<float *>(ws + wl.l_off);
     prm.part_o = reinterpret_cast<float *>(ws + wl.o_off);
     prm.max_parts = parts;
+    // the reduce kernel merges the prefix pass's partials with the members' own
+    prm.counters = nullptr;
     prm.seq_start = prefix_plan;
 
     MqParams mq{};

@@ -16,6 +16,11 @@
 namespace pa {
 
 constexpr int kTileTokens = 16;
+// Partials of a sequence the partition pass merges itself, at most.
+constexpr int kMergeMax = 8;
+// Arrival counters a workspace holds at least (1 MB; one per sequence and
+// KV head).
+constexpr size_t kCounterWords = size_t(1) << 18;
 constexpr uint64_t kDrainWaitNs = kDefaultStageWaitNs;  // waits for copies in flight at exit
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -31,6 +36,9 @@ struct DecodeParams {
     float *part_m;
     float *part_l;
     float *part_o;
+    // Arrival counters of the merge fused into the pass, one per (sequence,
+    // KV head) (null: the reduce kernel merges every split sequence).
+    int32_t *counters;
     int32_t *error_word;
     uint64_t wait_ns;  // limit of one stage wait (PA_DEVERR_TIMEOUT past it)
     int withhold_fill; // test hook: warp 0 of each CTA never issues its first fill
@@ -146,6 +154,8 @@ __global__ void __launch_bounds__(kReduceThreads, PA_REDUCE_MINB)
                        prefix_partitions(start, p.part_tokens);
     if (nparts == 0 || (nparts == 1 && start == 0))
         return;  // nothing to merge: the partition pass wrote the row
+    if (p.counters != nullptr && nparts <= kMergeMax)
+        return;  // merged by the partition pass
 
     // G * D / 8 <= 16 * 128 / 8 = kReduceThreads: one (item, qg) per thread.
     static_assert(16 * D / 8 <= kReduceThreads, "one work item per thread");
@@ -250,6 +260,136 @@ __global__ void __launch_bounds__(kReduceThreads, PA_REDUCE_MINB)
         *reinterpret_cast<const uint4 *>(vals);
 }
 
+// ---- the split-context merge fused into the pass ------------------------------------
+//
+// A partition unit of a sequence that spans several partitions leaves its
+// partial (m, l, o) in the workspace and then arrives on the (sequence, KV
+// head) counter; the warp whose arrival completes the count merges the
+// partials -- by log-sum-exp weights, as paged_reduce_kernel does -- and
+// writes the output row, so no reduce kernel runs after the pass.  The
+// arrival is one acquire-release atomic by lane 0 after a warp barrier (the
+// warp's partial stores come before it; the last arrival sees everyone's),
+// the partials are read through L2, and the counter goes back to zero once
+// its last arrival is in.  Merges are kept to at most kMergeMax partials:
+// each costs the merging warp a round trip to L2 per batch of partials, and
+// the pass's tile warps wait for the merge warp at their next unit's end;
+// sequences with more partials are left to paged_reduce_kernel.
+
+// The n (<= kMergeMax) partials of (s, kh) merged in index order by one warp
+// into the output row.  Lane l takes items l, l + 32, ... (item = a query
+// head's 8 consecutive elements of d); up to REC partial records per lane
+// (at least one per item) are loaded before any is used.
+template <typename T, int D, int NH, int REC>
+__device__ __forceinline__ void warp_merge(const DecodeParams &p, int s, int kh, int n, int lane)
+{
+    constexpr int IPL = NH * (D / 8) / 32;          // items per lane, at most
+    constexpr int QB = IPL >= REC ? 1 : REC / IPL;  // partials per item and batch
+    static_assert(IPL >= 1 && NH * (D / 8) % 32 == 0, "whole items per lane");
+    const int G = p.group;
+    const int items = G * (D / 8);
+    float mt[IPL], lt[IPL], acc[IPL][8];
+    size_t hrow[IPL];
+    int d0[IPL];
+#pragma unroll
+    for (int k = 0; k < IPL; ++k) {
+        const int it = lane + 32 * k;
+        const int jh = it / (D / 8);
+        d0[k] = (it - jh * (D / 8)) * 8;
+        hrow[k] = ((size_t)s * p.num_heads + (size_t)kh * G + jh) * p.max_parts;
+        mt[k] = -INFINITY;
+        lt[k] = 0.f;
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+            acc[k][e] = 0.f;
+    }
+    for (int qb = 0; qb < n; qb += QB) {
+        float cm[IPL][QB], cl[IPL][QB];
+        float4 lo[IPL][QB], hi[IPL][QB];
+#pragma unroll
+        for (int k = 0; k < IPL; ++k)
+#pragma unroll
+            for (int b = 0; b < QB; ++b) {
+                const int q = qb + b;
+                if (lane + 32 * k < items && q < n) {
+                    const size_t idx = hrow[k] + q;
+                    cm[k][b] = __ldcg(p.part_m + idx);
+                    cl[k][b] = __ldcg(p.part_l + idx);
+                    const float4 *src = reinterpret_cast<const float4 *>(p.part_o + idx * D + d0[k]);
+                    lo[k][b] = __ldcg(src);
+                    hi[k][b] = __ldcg(src + 1);
+                } else {
+                    cm[k][b] = -INFINITY;
+                    cl[k][b] = 0.f;
+                    lo[k][b] = hi[k][b] = make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+            }
+#pragma unroll
+        for (int k = 0; k < IPL; ++k) {
+            float mn = mt[k];
+#pragma unroll
+            for (int b = 0; b < QB; ++b)
+                mn = fmaxf(mn, cm[k][b]);
+            if (mn == -INFINITY)
+                continue;  // no partial of this item in the batch
+            const float alpha = exp2f((mt[k] - mn) * kLog2e);  // 0 while mt is -inf
+            lt[k] *= alpha;
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                acc[k][e] *= alpha;
+#pragma unroll
+            for (int b = 0; b < QB; ++b) {
+                const float w = cl[k][b] * exp2f((cm[k][b] - mn) * kLog2e);
+                lt[k] += w;
+                acc[k][0] += w * lo[k][b].x; acc[k][1] += w * lo[k][b].y;
+                acc[k][2] += w * lo[k][b].z; acc[k][3] += w * lo[k][b].w;
+                acc[k][4] += w * hi[k][b].x; acc[k][5] += w * hi[k][b].y;
+                acc[k][6] += w * hi[k][b].z; acc[k][7] += w * hi[k][b].w;
+            }
+            mt[k] = mn;
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < IPL; ++k) {
+        const int it = lane + 32 * k;
+        if (it >= items)
+            continue;
+        const int jh = it / (D / 8);
+        const float inv = 1.f / lt[k];
+        T vals[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+            vals[e] = MmaOp<T>::from_float(acc[k][e] * inv);
+        *reinterpret_cast<uint4 *>(static_cast<T *>(p.out) +
+                                   ((size_t)s * p.num_heads + (size_t)kh * G + jh) * D + d0[k]) =
+            *reinterpret_cast<const uint4 *>(vals);
+    }
+}
+
+// The arrival of one of the ntot (<= kMergeMax) partials of (s, kh), made by
+// a whole warp right after that warp stored the partial; the warp completing
+// the count writes the output row.
+template <typename T, int D, int NH, int REC>
+__device__ __forceinline__ void arrive_and_merge(const DecodeParams &p, int s, int kh, int ntot,
+                                                 int lane)
+{
+    int32_t *cnt = p.counters + (size_t)s * p.num_kv_heads + kh;
+    __syncwarp();  // the warp's partial stores come before lane 0's release
+    int last = 0;
+    if (lane == 0) {
+        int old;
+        asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;"
+                     : "=r"(old)
+                     : "l"(cnt)
+                     : "memory");
+        last = old == ntot - 1;
+        if (last)
+            *cnt = 0;  // every arrival is in: zero for the next call
+    }
+    last = __shfl_sync(kFull, last, 0);  // the lanes' loads come after lane 0's acquire
+    if (last)
+        warp_merge<T, D, NH, REC>(p, s, kh, ntot, lane);
+}
+
 // ---- host side -------------------------------------------------------------------
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
@@ -351,19 +491,24 @@ static pa_status launch_reduce(const DecodeParams &prm, cudaStream_t stream)
 
 static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
+// Workspace of the split path: the arrival counters first (a region of at
+// least kCounterWords words, so that calls of different sizes reusing one
+// workspace find theirs at the same place, zero), then the partials.
 struct WorkspaceLayout {
-    size_t m_off, l_off, o_off, total;
+    size_t cnt_off, m_off, l_off, o_off, total;
 };
 
-static WorkspaceLayout workspace_layout(int S, int H, int D, int parts)
+static WorkspaceLayout workspace_layout(int S, int H, int Hkv, int D, int parts)
 {
     WorkspaceLayout w{};
     if (parts <= 1)
         return w;
+    const size_t words = std::max<size_t>(kCounterWords, (size_t)S * Hkv);
     const size_t ml = align256((size_t)S * H * parts * 4);
-    w.m_off = 0;
-    w.l_off = ml;
-    w.o_off = 2 * ml;
+    w.cnt_off = 0;
+    w.m_off = align256(words * 4);
+    w.l_off = w.m_off + ml;
+    w.o_off = w.l_off + ml;
     w.total = w.o_off + align256((size_t)S * H * parts * D * 4);
     return w;
 }
@@ -410,7 +555,8 @@ static pa_status prepare_decode(DecodeParams *prm, void *out, const void *query,
         return PA_ERR_UNSUPPORTED;
 
     const int parts = num_parts(max_context_len, partition_size);
-    const WorkspaceLayout wl = workspace_layout(num_seqs, num_heads, head_dim, parts);
+    const WorkspaceLayout wl = workspace_layout(num_seqs, num_heads, num_kv_heads, head_dim,
+                                                parts);
     if (wl.total > 0 && (workspace == nullptr || workspace_bytes < wl.total ||
                          (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0))
         return PA_ERR_WORKSPACE;
@@ -423,6 +569,7 @@ static pa_status prepare_decode(DecodeParams *prm, void *out, const void *query,
     prm->part_m = wl.total ? reinterpret_cast<float *>(ws + wl.m_off) : nullptr;
     prm->part_l = wl.total ? reinterpret_cast<float *>(ws + wl.l_off) : nullptr;
     prm->part_o = wl.total ? reinterpret_cast<float *>(ws + wl.o_off) : nullptr;
+    prm->counters = wl.total ? reinterpret_cast<int32_t *>(ws + wl.cnt_off) : nullptr;
     prm->error_word = error_word;
     prm->wait_ns = stage_wait_limit_ns();
     prm->withhold_fill = withhold_first_fill();

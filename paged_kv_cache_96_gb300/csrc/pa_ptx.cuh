@@ -77,6 +77,22 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
     }
 }
 
+// ---- named barriers (bar.sync / bar.arrive) ------------------------------------
+
+// Wait at CTA barrier `id` until `count` threads (a multiple of 32) have
+// arrived or waited there; whole warps call it.
+__device__ __forceinline__ void named_barrier_sync(int id, int count)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// Arrive at CTA barrier `id` without waiting (memory accesses before it are
+// performed for the threads waiting there); whole warps call it.
+__device__ __forceinline__ void named_barrier_arrive(int id, int count)
+{
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 // ---- TMA -------------------------------------------------------------------
 
 // 4-D tiled bulk tensor load global -> shared, completion on an mbarrier.

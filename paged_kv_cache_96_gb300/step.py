@@ -237,19 +237,12 @@ class DecodeStep:
     def launches_per_step(self) -> int:
         """Kernels one run() launches: slot mapping with the cache write (unless
         fused into the attention pass), block copy (when the step has
-        copy-on-write pairs), the attention pass, the
-        shared-prefix pass (prefix-aware decode with at least one group), and
-        the reduce (when some context spans more than one partition, or a
-        prefix group exists)."""
+        copy-on-write pairs), the attention pass (which merges split
+        contexts itself), and, for prefix-aware decode with at least one
+        group, the shared-prefix pass and the reduce."""
         n = (1 if self.fused_append else 2) + (1 if self.cow_pairs is not None else 0)
         if self.cascade and self.num_groups > 0:
             n += 2
-        elif self.workspace is not None and not self.cascade:
-            n += 1
-        elif self.cascade and B.pa_decode_workspace_bytes(
-                self.w.S, self.w.H, self.w.Hkv, self.w.D, self.max_context_len,
-                self.partition_size) > 0:
-            n += 1
         return n
 
 

@@ -172,8 +172,15 @@ def test_workspace_layout_sizes(B):
     a256 = lambda x: (x + 255) // 256 * 256  # noqa: E731
     # long-context workload: 16 seqs, 32 heads over 8, d 128, 32768 tokens / 512
     S, H, Hkv, D, P = 16, 32, 8, 128, 64
-    want = 2 * a256(S * H * P * 4) + a256(S * H * P * D * 4)
+    counters = a256(4 * max(1 << 18, S * Hkv))
+    want = counters + 2 * a256(S * H * P * 4) + a256(S * H * P * D * 4)
     assert L.pa_decode_workspace_bytes(S, H, Hkv, D, 32768, 512) == want
+    # a batch whose counters pass the fixed region
+    S2, P2 = 40000, 3
+    counters2 = a256(4 * S2 * Hkv)
+    assert counters2 > 4 << 18
+    assert L.pa_decode_workspace_bytes(S2, H, Hkv, D, 3 * 512, 512) == \
+        counters2 + 2 * a256(S2 * H * P2 * 4) + a256(S2 * H * P2 * D * 4)
     # everything fits one partition, or single pass: no workspace
     assert L.pa_decode_workspace_bytes(S, H, Hkv, D, 512, 512) == 0
     assert L.pa_decode_workspace_bytes(S, H, Hkv, D, 32768, 0) == 0

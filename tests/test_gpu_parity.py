@@ -107,10 +107,14 @@ def test_partition_partials_match_oracle(B, S, small, name):
 
     def a256(x):
         return (x + 255) // 256 * 256
+    # the arrival counters come first (and are back at zero after the call)
+    n_cnt = max(1 << 18, S_ * w.Hkv)
+    assert int(ws[:4 * n_cnt].view(torch.int32).abs().sum().item()) == 0
+    base = a256(4 * n_cnt)
     n_ml = S_ * H * Pm
-    m_g = region(0, n_ml).reshape(S_, H, Pm)
-    l_g = region(a256(4 * n_ml), n_ml).reshape(S_, H, Pm)
-    o_g = region(2 * a256(4 * n_ml), n_ml * D).reshape(S_, H, Pm, D)
+    m_g = region(base, n_ml).reshape(S_, H, Pm)
+    l_g = region(base + a256(4 * n_ml), n_ml).reshape(S_, H, Pm)
+    o_g = region(base + 2 * a256(4 * n_ml), n_ml * D).reshape(S_, H, Pm, D)
     multi = [s for s in range(S_) if oracle.num_partitions(int(w.context_lens[s]), P) > 1]
     assert multi, "reduced workload should have multi-partition sequences"
     for s in multi:

@@ -169,12 +169,16 @@ def test_cascade_prefix_partial_matches_oracle(B, S, small):
     def a256(x):
         return (x + 255) // 256 * 256
     n_ml = Sn * H * parts
+    # the arrival counters come first (zero before and after the call)
+    n_cnt = max(1 << 18, Sn * w.Hkv)
+    assert int(ws[:4 * n_cnt].view(torch.int32).abs().sum().item()) == 0
+    base = a256(4 * n_cnt)
 
     def region(off, count):
         return ws[off:off + 4 * count].view(torch.float32).cpu().numpy().astype(np.float64)
-    m_g = region(0, n_ml).reshape(Sn, H, parts)
-    l_g = region(a256(4 * n_ml), n_ml).reshape(Sn, H, parts)
-    o_g = region(2 * a256(4 * n_ml), n_ml * D).reshape(Sn, H, parts, D)
+    m_g = region(base, n_ml).reshape(Sn, H, parts)
+    l_g = region(base + a256(4 * n_ml), n_ml).reshape(Sn, H, parts)
+    o_g = region(base + 2 * a256(4 * n_ml), n_ml * D).reshape(Sn, H, parts, D)
     for g in range(ng):
         L = int(gprefix[g])
         mem = members[gstart[g]:gstart[g + 1]].tolist()
