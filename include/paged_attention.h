@@ -398,12 +398,16 @@ PA_API size_t pa_cascade_workspace_bytes(int num_seqs, int num_heads, int num_kv
  *      partition_size tokens.
  *   2. partition pass: every sequence attends its own tokens [L, ctx) (L = 0
  *      outside any group) in partitions of partition_size tokens (0: one).
- *   3. reduce: log-sum-exp merge of each grouped or split sequence's
- *      partials; ungrouped single-partition sequences are written by step 2.
- * All three are queued on `stream` by this call, the prefix pass first; the
- * partition pass reads nothing the prefix pass writes, so it runs alongside
- * it (its grid finishes only after the prefix pass's), and the reduce waits
- * for both.  prefix_plan is the device
+ *   3. merge: log-sum-exp merge of each grouped or split sequence's
+ *      partials, by whichever of the two passes stores the sequence's last
+ *      partial (an arrival counter per sequence and KV head in the
+ *      workspace), for sequences of up to 8 partials; by a reduce kernel
+ *      queued behind the passes for longer ones.  Ungrouped single-partition
+ *      sequences are written by step 2.
+ * The passes are queued on `stream` by this call, the prefix pass first; the
+ * partition pass reads none of the prefix pass's partials before its
+ * arrival shows they are all stored, so it runs alongside it (its grid
+ * finishes only after the prefix pass's).  prefix_plan is the device
  * copy of a prefix plan (num_groups, num_members as planned); an
  * inconsistent plan (a table that differs from the leader's on the prefix,
  * a prefix not below a member's context or off the 16-token grid, a

@@ -1213,8 +1213,7 @@ static pa_status run_cascade(void *out, const void *query, void *key_cache, void
     prm.part_l = reinterpret_cast<float *>(ws + wl.l_off);
     prm.part_o = reinterpret_cast<float *>(ws + wl.o_off);
     prm.max_parts = parts;
-    // the reduce kernel merges the prefix pass's partials with the members' own
-    prm.counters = nullptr;
+    prm.counters = reinterpret_cast<int32_t *>(ws + wl.cnt_off);
     prm.seq_start = prefix_plan;
 
     MqParams mq{};
@@ -1228,6 +1227,10 @@ static pa_status run_cascade(void *out, const void *query, void *key_cache, void
     mq.part_m = prm.part_m;
     mq.part_l = prm.part_l;
     mq.part_o = prm.part_o;
+    // sequences of up to kMergeMax partials are merged by whichever pass
+    // completes their arrival counter, into the decode output
+    mq.counters = prm.counters;
+    mq.out = out;
     mq.error_word = error_word;
     mq.wait_ns = prm.wait_ns;
     mq.withhold_fill = prm.withhold_fill;

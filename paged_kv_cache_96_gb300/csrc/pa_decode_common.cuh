@@ -277,114 +277,142 @@ __global__ void __launch_bounds__(kReduceThreads, PA_REDUCE_MINB)
 
 // The n (<= kMergeMax) partials of (s, kh) merged in index order by one warp
 // into the output row.  Lane l takes items l, l + 32, ... (item = a query
-// head's 8 consecutive elements of d); up to REC partial records per lane
-// (at least one per item) are loaded before any is used.
-template <typename T, int D, int NH, int REC>
-__device__ __forceinline__ void warp_merge(const DecodeParams &p, int s, int kh, int n, int lane)
+// head's 8 consecutive elements of d), in blocks of up to 4 per lane; up to
+// REC partial records per lane (at least one per item) are loaded before any
+// is used.  NH: query heads per KV head the caller's kernel serves, at most.
+// PT: the caller's parameters (part_m/l/o, out, num_heads, group,
+// max_parts).
+template <typename T, int D, int NH, int REC, typename PT>
+__device__ __forceinline__ void warp_merge(const PT &p, int s, int kh, int n, int lane)
 {
     constexpr int IPL = NH * (D / 8) / 32;          // items per lane, at most
-    constexpr int QB = IPL >= REC ? 1 : REC / IPL;  // partials per item and batch
-    static_assert(IPL >= 1 && NH * (D / 8) % 32 == 0, "whole items per lane");
+    constexpr int IB = IPL < 4 ? IPL : 4;           // items per lane and block
+    constexpr int QB = IB >= REC ? 1 : REC / IB;    // partials per item and batch
+    static_assert(IPL >= 1 && NH * (D / 8) % 32 == 0 && IPL % IB == 0, "whole items per lane");
     const int G = p.group;
     const int items = G * (D / 8);
-    float mt[IPL], lt[IPL], acc[IPL][8];
-    size_t hrow[IPL];
-    int d0[IPL];
+#pragma unroll 1
+    for (int kb = 0; kb < IPL; kb += IB) {
+        if (lane + 32 * kb >= items)
+            break;
+        float mt[IB], lt[IB], acc[IB][8];
+        size_t hrow[IB];
+        int d0[IB];
 #pragma unroll
-    for (int k = 0; k < IPL; ++k) {
-        const int it = lane + 32 * k;
-        const int jh = it / (D / 8);
-        d0[k] = (it - jh * (D / 8)) * 8;
-        hrow[k] = ((size_t)s * p.num_heads + (size_t)kh * G + jh) * p.max_parts;
-        mt[k] = -INFINITY;
-        lt[k] = 0.f;
-#pragma unroll
-        for (int e = 0; e < 8; ++e)
-            acc[k][e] = 0.f;
-    }
-    for (int qb = 0; qb < n; qb += QB) {
-        float cm[IPL][QB], cl[IPL][QB];
-        float4 lo[IPL][QB], hi[IPL][QB];
-#pragma unroll
-        for (int k = 0; k < IPL; ++k)
-#pragma unroll
-            for (int b = 0; b < QB; ++b) {
-                const int q = qb + b;
-                if (lane + 32 * k < items && q < n) {
-                    const size_t idx = hrow[k] + q;
-                    cm[k][b] = __ldcg(p.part_m + idx);
-                    cl[k][b] = __ldcg(p.part_l + idx);
-                    const float4 *src = reinterpret_cast<const float4 *>(p.part_o + idx * D + d0[k]);
-                    lo[k][b] = __ldcg(src);
-                    hi[k][b] = __ldcg(src + 1);
-                } else {
-                    cm[k][b] = -INFINITY;
-                    cl[k][b] = 0.f;
-                    lo[k][b] = hi[k][b] = make_float4(0.f, 0.f, 0.f, 0.f);
-                }
-            }
-#pragma unroll
-        for (int k = 0; k < IPL; ++k) {
-            float mn = mt[k];
-#pragma unroll
-            for (int b = 0; b < QB; ++b)
-                mn = fmaxf(mn, cm[k][b]);
-            if (mn == -INFINITY)
-                continue;  // no partial of this item in the batch
-            const float alpha = exp2f((mt[k] - mn) * kLog2e);  // 0 while mt is -inf
-            lt[k] *= alpha;
+        for (int k = 0; k < IB; ++k) {
+            const int it = lane + 32 * (kb + k);
+            const int jh = it / (D / 8);
+            d0[k] = (it - jh * (D / 8)) * 8;
+            hrow[k] = ((size_t)s * p.num_heads + (size_t)kh * G + jh) * p.max_parts;
+            mt[k] = -INFINITY;
+            lt[k] = 0.f;
 #pragma unroll
             for (int e = 0; e < 8; ++e)
-                acc[k][e] *= alpha;
-#pragma unroll
-            for (int b = 0; b < QB; ++b) {
-                const float w = cl[k][b] * exp2f((cm[k][b] - mn) * kLog2e);
-                lt[k] += w;
-                acc[k][0] += w * lo[k][b].x; acc[k][1] += w * lo[k][b].y;
-                acc[k][2] += w * lo[k][b].z; acc[k][3] += w * lo[k][b].w;
-                acc[k][4] += w * hi[k][b].x; acc[k][5] += w * hi[k][b].y;
-                acc[k][6] += w * hi[k][b].z; acc[k][7] += w * hi[k][b].w;
-            }
-            mt[k] = mn;
+                acc[k][e] = 0.f;
         }
-    }
+        for (int qb = 0; qb < n; qb += QB) {
+            float cm[IB][QB], cl[IB][QB];
+            float4 lo[IB][QB], hi[IB][QB];
 #pragma unroll
-    for (int k = 0; k < IPL; ++k) {
-        const int it = lane + 32 * k;
-        if (it >= items)
-            continue;
-        const int jh = it / (D / 8);
-        const float inv = 1.f / lt[k];
-        T vals[8];
+            for (int k = 0; k < IB; ++k)
 #pragma unroll
-        for (int e = 0; e < 8; ++e)
-            vals[e] = MmaOp<T>::from_float(acc[k][e] * inv);
-        *reinterpret_cast<uint4 *>(static_cast<T *>(p.out) +
-                                   ((size_t)s * p.num_heads + (size_t)kh * G + jh) * D + d0[k]) =
-            *reinterpret_cast<const uint4 *>(vals);
+                for (int b = 0; b < QB; ++b) {
+                    const int q = qb + b;
+                    if (lane + 32 * (kb + k) < items && q < n) {
+                        const size_t idx = hrow[k] + q;
+                        cm[k][b] = __ldcg(p.part_m + idx);
+                        cl[k][b] = __ldcg(p.part_l + idx);
+                        const float4 *src =
+                            reinterpret_cast<const float4 *>(p.part_o + idx * D + d0[k]);
+                        lo[k][b] = __ldcg(src);
+                        hi[k][b] = __ldcg(src + 1);
+                    } else {
+                        cm[k][b] = -INFINITY;
+                        cl[k][b] = 0.f;
+                        lo[k][b] = hi[k][b] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    }
+                }
+#pragma unroll
+            for (int k = 0; k < IB; ++k) {
+                float mn = mt[k];
+#pragma unroll
+                for (int b = 0; b < QB; ++b)
+                    mn = fmaxf(mn, cm[k][b]);
+                if (mn == -INFINITY)
+                    continue;  // no partial of this item in the batch
+                const float alpha = exp2f((mt[k] - mn) * kLog2e);  // 0 while mt is -inf
+                lt[k] *= alpha;
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    acc[k][e] *= alpha;
+#pragma unroll
+                for (int b = 0; b < QB; ++b) {
+                    const float w = cl[k][b] * exp2f((cm[k][b] - mn) * kLog2e);
+                    lt[k] += w;
+                    acc[k][0] += w * lo[k][b].x; acc[k][1] += w * lo[k][b].y;
+                    acc[k][2] += w * lo[k][b].z; acc[k][3] += w * lo[k][b].w;
+                    acc[k][4] += w * hi[k][b].x; acc[k][5] += w * hi[k][b].y;
+                    acc[k][6] += w * hi[k][b].z; acc[k][7] += w * hi[k][b].w;
+                }
+                mt[k] = mn;
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < IB; ++k) {
+            const int it = lane + 32 * (kb + k);
+            if (it >= items)
+                continue;
+            const int jh = it / (D / 8);
+            const float inv = 1.f / lt[k];
+            T vals[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                vals[e] = MmaOp<T>::from_float(acc[k][e] * inv);
+            *reinterpret_cast<uint4 *>(static_cast<T *>(p.out) +
+                                       ((size_t)s * p.num_heads + (size_t)kh * G + jh) * D +
+                                       d0[k]) = *reinterpret_cast<const uint4 *>(vals);
+        }
     }
 }
 
-// The arrival of one of the ntot (<= kMergeMax) partials of (s, kh), made by
-// a whole warp right after that warp stored the partial; the warp completing
-// the count writes the output row.
+// Partials of sequence s in all: the prefix pass's partitions of its shared
+// prefix [0, start) and its own partitions of [start, ctx) (the rule of the
+// partition pass, with the same clamped context and checked start).
+__device__ __forceinline__ int total_partitions(int ctx, int start, int part_tokens)
+{
+    return prefix_partitions(start, part_tokens) + own_partitions(ctx, start, part_tokens);
+}
+
+// One arrival of `add` head-rows of partials of (s, kh) (the counter of a
+// sequence with n partials completes at n * G), made with an acquire-release
+// atomic by the calling lane after its rows' stores are ordered before it
+// (its own stores, or its warp's behind a __syncwarp).  Returns whether this
+// arrival completed the count; the counter is then zero again.
+__device__ __forceinline__ bool arrive_rows(int32_t *cnt, int add, int total)
+{
+    int old;
+    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;"
+                 : "=r"(old)
+                 : "l"(cnt), "r"(add)
+                 : "memory");
+    const bool last = old + add == total;
+    if (last)
+        *cnt = 0;  // every arrival is in: zero for the next call
+    return last;
+}
+
+// The partition pass's arrival of one partial of (s, kh), all G heads, made
+// by the merge warp right after it stored them; the warp completing the
+// count writes the output row.
 template <typename T, int D, int NH, int REC>
 __device__ __forceinline__ void arrive_and_merge(const DecodeParams &p, int s, int kh, int ntot,
                                                  int lane)
 {
-    int32_t *cnt = p.counters + (size_t)s * p.num_kv_heads + kh;
     __syncwarp();  // the warp's partial stores come before lane 0's release
     int last = 0;
-    if (lane == 0) {
-        int old;
-        asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;"
-                     : "=r"(old)
-                     : "l"(cnt)
-                     : "memory");
-        last = old == ntot - 1;
-        if (last)
-            *cnt = 0;  // every arrival is in: zero for the next call
-    }
+    if (lane == 0)
+        last = arrive_rows(p.counters + (size_t)s * p.num_kv_heads + kh, p.group,
+                           ntot * p.group);
     last = __shfl_sync(kFull, last, 0);  // the lanes' loads come after lane 0's acquire
     if (last)
         warp_merge<T, D, NH, REC>(p, s, kh, ntot, lane);

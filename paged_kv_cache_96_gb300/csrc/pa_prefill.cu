@@ -315,7 +315,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         // this thread's row of a unit: query row, output location, key limit
         struct Row {
             long long qoff, ooff;
-            int lim;
+            int lim, seq;
         };
         auto row_of = [&](const Unit &w, Row &r, bool check) {
             // prefix pass, first KV head and partition: check the plan for this
@@ -344,6 +344,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
             r.qoff = -1;
             r.ooff = -1;
             r.lim = 0;
+            r.seq = -1;
             if (tid < w.nrows) {
                 const int rr = w.rt * kTcRows + tid;
                 const int i = rr / G, hg = rr - (rr / G) * G;
@@ -351,6 +352,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
                 if (p.prefix_mode) {
                     int sq = p.group_members[p.group_start[w.seg] + i];
                     sq = min(max(sq, 0), p.num_seqs - 1);  // a bad member id is flagged above
+                    r.seq = sq;
                     r.qoff = ((long long)sq * H + h) * D;
                     r.ooff = ((long long)sq * H + h) * p.max_parts + w.part;
                     r.lim = w.kend;
@@ -529,6 +531,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
                 wn.n = 0;
                 rn.qoff = rn.ooff = -1;
                 rn.lim = 0;
+                rn.seq = -1;
             }
             // this unit's last value product
             if (w.n > 0) {
@@ -581,6 +584,32 @@ __global__ void __launch_bounds__(kTcThreads, 2)
                                              __uint_as_float(r[8 * i + 7]) * inv);
                         dst[i] = v;
                     }
+                }
+            }
+            // prefix pass: this row's partial is stored; arrive on the
+            // sequence's counter (one head-row), and a warp whose lane
+            // completed a count merges that sequence's partials into its
+            // output row
+            if (p.prefix_mode && p.counters != nullptr) {
+                const int sq = rw.seq;
+                int ntot = 0;
+                bool last = false;
+                if (ooff >= 0) {
+                    const int limit = min(p.max_context_len, p.max_blocks_per_seq * p.block_size);
+                    const int c = min(max(p.context_lens[sq], 0), limit);
+                    int st = p.seq_start[sq];
+                    st = (st < 0 || st > c || (st & (kTileTokens - 1)) != 0) ? 0 : st;
+                    ntot = total_partitions(c, st, p.part_tokens);
+                    if (ntot <= kMergeMax)
+                        last = arrive_rows(p.counters + (size_t)sq * Hkv + w.kh, 1, ntot * G);
+                }
+                unsigned todo = __ballot_sync(kFull, last);
+                while (todo != 0) {
+                    const int src = __ffs(todo) - 1;
+                    todo &= todo - 1;
+                    const int ms = __shfl_sync(kFull, sq, src);
+                    const int mn = __shfl_sync(kFull, ntot, src);
+                    warp_merge<T, D, 16, 4>(p, ms, w.kh, mn, lane);
                 }
             }
             g += w.n;

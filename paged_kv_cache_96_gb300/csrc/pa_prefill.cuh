@@ -20,6 +20,9 @@ struct MqParams {
     float *part_m;
     float *part_l;
     float *part_o;
+    // prefix pass: the partition pass's arrival counters (null: the reduce
+    // kernel merges); out is then the decode output [S][H][D]
+    int32_t *counters;
     int32_t *error_word;
     uint64_t wait_ns;  // limit of one stage wait (PA_DEVERR_TIMEOUT past it)
     int withhold_fill; // test hook: each CTA's key warp never issues its first fill

@@ -237,12 +237,20 @@ class DecodeStep:
     def launches_per_step(self) -> int:
         """Kernels one run() launches: slot mapping with the cache write (unless
         fused into the attention pass), block copy (when the step has
-        copy-on-write pairs), the attention pass (which merges split
-        contexts itself), and, for prefix-aware decode with at least one
-        group, the shared-prefix pass and the reduce."""
+        copy-on-write pairs), the attention pass (which merges split contexts
+        of up to 8 partials itself), the shared-prefix pass (prefix-aware
+        decode with at least one group), and the reduce (when a sequence may
+        have more than 8 partials)."""
         n = (1 if self.fused_append else 2) + (1 if self.cow_pairs is not None else 0)
+        if self.w.prefill:
+            return n
+        P = self.partition_size
+        parts = -(-self.max_context_len // P) if P > 0 and self.max_context_len > 0 else 1
         if self.cascade and self.num_groups > 0:
-            n += 2
+            n += 1
+            parts += 1  # the shared prefix's partial
+        if parts > 8:
+            n += 1
         return n
 
 
