@@ -76,6 +76,7 @@ typedef enum {
 #define PA_DEVERR_TOKEN_RANGE   0x10 /* token's sequence or position outside its table */
 #define PA_DEVERR_TIMEOUT       0x20 /* a bounded wait on staged data gave up */
 #define PA_DEVERR_PREFIX_PLAN   0x40 /* prefix plan inconsistent with the tables or contexts */
+#define PA_DEVERR_QUERY_RANGE   0x80 /* FP8 pools: a bf16 query element beyond the fp16 range */
 
 /*
  * pa_slot_mapping -- [GAO] §1.5.  For every token t, writes
@@ -245,10 +246,12 @@ PA_API pa_status pa_decode_attention(void *out, const void *query,
  * pa_reshape_and_cache_fp8: K and V elements are e4m3 codes standing for
  * e4m3(code) * k_scale and * v_scale.  query and out are dtype (PA_F16 or
  * PA_BF16).  Codes are widened to fp16 and the query is rounded to fp16 for
- * the tensor-core products (|q| must stay below 65504); scores and weights
+ * the tensor-core products: a bf16 query element with |q| > 65504 overflows
+ * there, and is flagged PA_DEVERR_QUERY_RANGE (its rows' outputs are then
+ * not finite); scores and weights
  * accumulate in fp32 as in pa_decode_attention; the V scale is applied to
  * the output.  Workspace, partitions and errors as pa_decode_attention
- * (same workspace size).  Supported: head_dim 128.
+ * (same workspace size).  Supported: head_dim 64 or 128.
  */
 PA_API pa_status pa_decode_attention_fp8(void *out, const void *query, const void *key_cache,
                                          const void *value_cache, const int32_t *block_tables,

@@ -30,6 +30,7 @@ DEVERR_CONTEXT_RANGE = 0x08
 DEVERR_TOKEN_RANGE = 0x10
 DEVERR_TIMEOUT = 0x20
 DEVERR_PREFIX_PLAN = 0x40
+DEVERR_QUERY_RANGE = 0x80
 
 
 class PAError(RuntimeError):

@@ -120,21 +120,29 @@ __device__ __noinline__ void append_token(const DecodeParams &p, int s, int kh, 
     const int64_t slot = ok ? (int64_t)ent * p.block_size + (pos & (p.block_size - 1)) : -1;
     const size_t elem = ((size_t)slot * p.num_kv_heads + kh) * D + (size_t)lane * E;
     if constexpr (kFp8) {
-        static_assert(E == 4, "FP8 pools have head_dim 128");
-        const uint32_t kc = (uint32_t)f32x2_to_e4m3x2(f(ke[0]) * p.k_inv_scale,
-                                                      f(ke[1]) * p.k_inv_scale) |
-                            ((uint32_t)f32x2_to_e4m3x2(f(ke[2]) * p.k_inv_scale,
-                                                       f(ke[3]) * p.k_inv_scale) << 16);
-        const uint32_t vc = (uint32_t)f32x2_to_e4m3x2(f(ve[0]) * p.v_inv_scale,
-                                                      f(ve[1]) * p.v_inv_scale) |
-                            ((uint32_t)f32x2_to_e4m3x2(f(ve[2]) * p.v_inv_scale,
-                                                       f(ve[3]) * p.v_inv_scale) << 16);
+        // the e4m3 codes of this lane's E elements, as reshape_and_cache_fp8
+        // computes them, stored E bytes at a time
+        uint32_t kc = 0, vc = 0;
+#pragma unroll
+        for (int h = 0; h < E / 2; ++h) {
+            kc |= (uint32_t)f32x2_to_e4m3x2(f(ke[2 * h]) * p.k_inv_scale,
+                                            f(ke[2 * h + 1]) * p.k_inv_scale) << (16 * h);
+            vc |= (uint32_t)f32x2_to_e4m3x2(f(ve[2 * h]) * p.v_inv_scale,
+                                            f(ve[2 * h + 1]) * p.v_inv_scale) << (16 * h);
+        }
         if (ok) {
-            *reinterpret_cast<uint32_t *>(static_cast<uint8_t *>(p.key_cache) + elem) = kc;
-            *reinterpret_cast<uint32_t *>(static_cast<uint8_t *>(p.value_cache) + elem) = vc;
+            uint8_t *kd = static_cast<uint8_t *>(p.key_cache) + elem;
+            uint8_t *vd = static_cast<uint8_t *>(p.value_cache) + elem;
+            if constexpr (E == 4) {
+                *reinterpret_cast<uint32_t *>(kd) = kc;
+                *reinterpret_cast<uint32_t *>(vd) = vc;
+            } else {
+                *reinterpret_cast<uint16_t *>(kd) = (uint16_t)kc;
+                *reinterpret_cast<uint16_t *>(vd) = (uint16_t)vc;
+            }
         }
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
+        for (int h = 0; h < E / 2; ++h) {
             const uint32_t kw = e4m3x2_to_f16x2((uint16_t)(kc >> (16 * h)));
             const uint32_t vw = e4m3x2_to_f16x2((uint16_t)(vc >> (16 * h)));
             kf[2 * h] = __half2float(__ushort_as_half((unsigned short)(kw & 0xffffu)));
@@ -201,7 +209,6 @@ __global__ void __launch_bounds__(bound_threads(NW + 1, MINB), MINB)
                         const __grid_constant__ CUtensorMap tmap_v)
 {
     constexpr bool kFp8 = sizeof(KV) == 1;
-    static_assert(!kFp8 || D == 128, "FP8 pools are supported with head_dim 128");
     using L = Layout<D, NT, NW, NST, sizeof(KV)>;
     using MT = typename std::conditional<kFp8, __half, T>::type;  // tensor-core input type
     using Op = MmaOp<MT>;
@@ -409,7 +416,10 @@ __global__ void __launch_bounds__(bound_threads(NW + 1, MINB), MINB)
     // c ^ (r & 7) (the TMA's 128-byte swizzle).
     auto tile_addr = [&](uint32_t base, int token, int half, int chunk) -> uint32_t {
         if constexpr (kFp8) {
-            const int r = token;  // FP8: one 128-byte row per token, chunk 0..7
+            const int r = token;
+            if constexpr (D == 64)  // one 64-byte row per token, chunk 0..3, 64-byte swizzle
+                return base + r * 64 + ((chunk ^ ((r >> 1) & 3)) << 4);
+            // one 128-byte row per token, chunk 0..7
             return base + r * 128 + (((chunk + 4 * half) ^ (r & 7)) << 4);
         }
         const int r = half * kTileTokens + token;
@@ -422,6 +432,7 @@ __global__ void __launch_bounds__(bound_threads(NW + 1, MINB), MINB)
     // FP8 tile fragments -- k-steps 2t4, 2t4+1 <- d = 16kk + 4t4 (+1) and
     // k-steps 2t4+8, 2t4+9 <- d = 16kk + 4t4 + 2 (+3) -- in fp16.
     uint32_t qf[NT][KT][2];
+    bool q_over = false;  // FP8 pools: a bf16 query element past the fp16 range
     auto load_query = [&](int s, int kh) {
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
@@ -439,8 +450,13 @@ __global__ void __launch_bounds__(bound_threads(NW + 1, MINB), MINB)
                         qf[nt][kk][1] = w.y;
                     } else {
                         const T *e = reinterpret_cast<const T *>(&w);
-                        qf[nt][kk][0] = pack_f16x2(__bfloat162float(e[0]), __bfloat162float(e[1]));
-                        qf[nt][kk][1] = pack_f16x2(__bfloat162float(e[2]), __bfloat162float(e[3]));
+                        const float x0 = __bfloat162float(e[0]), x1 = __bfloat162float(e[1]);
+                        const float x2 = __bfloat162float(e[2]), x3 = __bfloat162float(e[3]);
+                        // the fp16 products need |q| within the fp16 range
+                        q_over |= fmaxf(fmaxf(fabsf(x0), fabsf(x1)), fmaxf(fabsf(x2), fabsf(x3))) >
+                                  65504.f;
+                        qf[nt][kk][0] = pack_f16x2(x0, x1);
+                        qf[nt][kk][1] = pack_f16x2(x2, x3);
                     }
                 } else {
                     const uint32_t *qw = reinterpret_cast<const uint32_t *>(qrow);
@@ -791,6 +807,8 @@ __global__ void __launch_bounds__(bound_threads(NW + 1, MINB), MINB)
                 arrive_and_merge<T, D, kHeads, kFp8 ? 2 : 8>(p, s, kh, pbase + nparts, lane);
         }
     }
+    if (kFp8 && __any_sync(kFull, q_over) && lane == 0)
+        flag_error(p.error_word, PA_DEVERR_QUERY_RANGE);
     pdl_launch_dependents();
 
     // ---- drain: wait (bounded) for any fetch still landing in this warp's ring ----
@@ -992,26 +1010,34 @@ static pa_status run_decode16(const DecodeParams &prm, const void *key_cache,
 // into the exponent's scale), outputs and partials get the V scale.
 static pa_status run_decode_fp8(DecodeParams &prm, const void *key_cache,
                                 const void *value_cache, pa_dtype dtype, int num_seqs,
-                                int num_kv_heads, int block_size, int num_blocks, float scale,
-                                float k_scale, float v_scale, void *stream)
+                                int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                                float scale, float k_scale, float v_scale, void *stream)
 {
     prm.scale_log2 = scale * k_scale * kLog2e;
     prm.out_scale = v_scale;
     CUtensorMap mk, mv;
     if (!encode_pool_map(&mk, key_cache, PA_FP8_E4M3, num_blocks, block_size, num_kv_heads,
-                         128) ||
+                         head_dim) ||
         !encode_pool_map(&mv, value_cache, PA_FP8_E4M3, num_blocks, block_size, num_kv_heads,
-                         128))
+                         head_dim))
         return PA_ERR_CUDA;
     const long long max_units = (long long)num_seqs * num_kv_heads * prm.max_parts;
     cudaStream_t st = as_stream(stream);
     const bool wide = prm.group > 8;
     using U8 = uint8_t;
+    using B16 = __nv_bfloat16;
+    if (head_dim == 128) {
+        if (dtype == PA_BF16)
+            return wide ? launch_decode<B16, U8, 128, 2>(prm, mk, mv, st, max_units)
+                        : launch_decode<B16, U8, 128, 1>(prm, mk, mv, st, max_units);
+        return wide ? launch_decode<__half, U8, 128, 2>(prm, mk, mv, st, max_units)
+                    : launch_decode<__half, U8, 128, 1>(prm, mk, mv, st, max_units);
+    }
     if (dtype == PA_BF16)
-        return wide ? launch_decode<__nv_bfloat16, U8, 128, 2>(prm, mk, mv, st, max_units)
-                    : launch_decode<__nv_bfloat16, U8, 128, 1>(prm, mk, mv, st, max_units);
-    return wide ? launch_decode<__half, U8, 128, 2>(prm, mk, mv, st, max_units)
-                : launch_decode<__half, U8, 128, 1>(prm, mk, mv, st, max_units);
+        return wide ? launch_decode<B16, U8, 64, 2>(prm, mk, mv, st, max_units)
+                    : launch_decode<B16, U8, 64, 1>(prm, mk, mv, st, max_units);
+    return wide ? launch_decode<__half, U8, 64, 2>(prm, mk, mv, st, max_units)
+                : launch_decode<__half, U8, 64, 1>(prm, mk, mv, st, max_units);
 }
 
 static bool valid_fp8_scales(float k_scale, float v_scale)
@@ -1099,9 +1125,7 @@ extern "C" pa_status pa_decode_attention_fp8(
         error_word);
     if (ok != PA_OK || num_seqs == 0)
         return ok;
-    if (head_dim != 128)
-        return PA_ERR_UNSUPPORTED;
-    return run_decode_fp8(prm, key_cache, value_cache, dtype, num_seqs, num_kv_heads,
+    return run_decode_fp8(prm, key_cache, value_cache, dtype, num_seqs, num_kv_heads, head_dim,
                           block_size, num_blocks, scale, k_scale, v_scale, stream);
 }
 
@@ -1123,15 +1147,13 @@ extern "C" pa_status pa_decode_attention_append_fp8(
                                   error_word);
     if (ok != PA_OK || num_seqs == 0)
         return ok;
-    if (head_dim != 128)
-        return PA_ERR_UNSUPPORTED;
     ok = set_append(&prm, key_cache, value_cache, new_key, new_value, slot_mapping);
     if (ok != PA_OK)
         return ok;
     // the codes' contract: e4m3(x * (1 / scale)), the reciprocal taken in fp32
     prm.k_inv_scale = 1.0f / k_scale;
     prm.v_inv_scale = 1.0f / v_scale;
-    return run_decode_fp8(prm, key_cache, value_cache, dtype, num_seqs, num_kv_heads,
+    return run_decode_fp8(prm, key_cache, value_cache, dtype, num_seqs, num_kv_heads, head_dim,
                           block_size, num_blocks, scale, k_scale, v_scale, stream);
 }
 

@@ -445,8 +445,8 @@ static EncodeTiledFn get_encode_fn()
 // (dims d, head, token, block).  16-bit pools: a box of 64 elements x 1 head
 // x 16 tokens x 1 block lands as 16 rows of 128 bytes with the 128-byte
 // swizzle; a 16-token tile of one KV head takes head_dim / 64 boxes.  FP8
-// pools: a box of 128 one-byte elements (one 128-byte row) x 1 head x 16
-// tokens x 1 block.
+// pools: a box of head_dim one-byte elements (one row of 128 bytes, 128-byte
+// swizzle; or of 64 bytes, 64-byte swizzle) x 1 head x 16 tokens x 1 block.
 static bool encode_pool_map(CUtensorMap *map, const void *pool, pa_dtype dtype,
                             int num_blocks, int block_size, int num_kv_heads,
                             int head_dim)
@@ -464,10 +464,12 @@ static bool encode_pool_map(CUtensorMap *map, const void *pool, pa_dtype dtype,
     const cuuint64_t strides[3] = {(cuuint64_t)head_dim * e,
                                    (cuuint64_t)num_kv_heads * head_dim * e,
                                    (cuuint64_t)block_size * num_kv_heads * head_dim * e};
-    const cuuint32_t box[4] = {fp8 ? 128u : 64u, 1, (cuuint32_t)kTileTokens, 1};
+    const cuuint32_t box[4] = {fp8 ? (cuuint32_t)head_dim : 64u, 1, (cuuint32_t)kTileTokens, 1};
     const cuuint32_t estr[4] = {1, 1, 1, 1};
+    const CUtensorMapSwizzle swz =
+        fp8 && head_dim == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B;
     return fn(map, ty, 4, const_cast<void *>(pool), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }

@@ -148,7 +148,7 @@ def test_append_argument_checks(B):
     assert f8(*ok8[:11], 0, *ok8[12:]) == B.PA_OK
     assert f8(*ok8[:18], 0.0, 0.5, *ok8[20:]) == B.PA_ERR_INVALID_ARG  # zero K scale
     assert f8(*ok8[:18], 0.5, float("nan"), *ok8[20:]) == B.PA_ERR_INVALID_ARG
-    assert f8(*ok8[:14], 64, *ok8[15:]) == B.PA_ERR_UNSUPPORTED         # FP8: d 128 only
+    assert f8(*ok8[:14], 96, *ok8[15:]) == B.PA_ERR_UNSUPPORTED         # FP8: d 64 or 128
     assert f8(*ok8[:5], None, *ok8[6:]) == B.PA_ERR_INVALID_ARG
 
 

@@ -75,6 +75,7 @@ SPECS = {
         query_lens=_fixed_q([100, 64, 129, 1]), partition_size=0),
 }
 SPECS["gqa-fp8"] = W.fp8_variant(SPECS["gqa"])
+SPECS["d64-fp8"] = W.fp8_variant(SPECS["d64"])
 
 DOMINANT_SCORE = 20.0
 VROW = np.array([3.0, 3.25, 3.5, 3.75])   # exact in fp16 and bf16
@@ -227,7 +228,7 @@ def _run(S, w, P, how):
     return S.to_float(st.out)
 
 
-DECODE_CASES = [(n, P, how) for n in ("gqa", "d64", "gqa-fp8")
+DECODE_CASES = [(n, P, how) for n in ("gqa", "d64", "gqa-fp8", "d64-fp8")
                 for P in (0, SPECS[n].partition_size, 16)
                 for how in ("append", "separate")]
 

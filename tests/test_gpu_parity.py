@@ -316,3 +316,19 @@ def test_host_argument_errors(B, S, small):
                               st.step_block_tables, st.context_lens, st.max_context_len,
                               w.scale, 24, None)
     assert e.value.status == B.PA_ERR_UNSUPPORTED
+
+
+def test_fp8_query_beyond_fp16_range_is_flagged(B, S, small):
+    """FP8 pools take the query in fp16 for the tensor-core products: a bf16
+    query element past the fp16 range is flagged on the device (and a query
+    inside it is not)."""
+    w, _ = small("gqa70b-fp8")
+    st = S.DecodeStep(w, partition_size=w.spec.partition_size)
+    st.run()
+    torch.cuda.synchronize()
+    assert int(st.error_word.item()) == 0
+    assert st.query.dtype == torch.bfloat16
+    st.query[1, 3, 17] = 1.0e5   # bf16 holds it, fp16 does not
+    st.attention()
+    torch.cuda.synchronize()
+    assert int(st.error_word.item()) & B.DEVERR_QUERY_RANGE

@@ -1,7 +1,8 @@
 """Shapes the five workloads do not reach, against the oracle: query-head
 groups that do not fill an 8-head tile (2, 3, 5, 12) and the 16-head tile
 variant, head_dim 64 and 128 in both 16-bit types, block sizes 16 to 256,
-several partition sizes, FP8 pools with wide and odd groups, chunked prefill
+several partition sizes, FP8 pools with wide and odd groups at head_dim 64
+and 128 (fp16 and bf16 queries), chunked prefill
 with the same groups and block sizes, and batches of thousands of sequences
 (past 10,000 the decode pass falls back to one ring stage per warp to fit
 the per-sequence arrays in shared memory).  Slots and pools bit-exact;
@@ -59,9 +60,14 @@ def test_decode_shapes(case):
 
 
 FP8 = [
-    ("fp8_g16_bs16", 4, 32, 2, 16, (0, 64)),
-    ("fp8_g3_bs64", 5, 6, 2, 64, (0, 128)),
-    ("fp8_g1_bs32", 4, 4, 4, 32, (0, 32)),
+    # (name, S, H, Hkv, bs, partitions, head_dim, query dtype)
+    ("fp8_g16_bs16", 4, 32, 2, 16, (0, 64), 128, "bf16"),
+    ("fp8_g3_bs64", 5, 6, 2, 64, (0, 128), 128, "bf16"),
+    ("fp8_g1_bs32", 4, 4, 4, 32, (0, 32), 128, "bf16"),
+    ("fp8_d64_g8_bs16", 5, 16, 2, 16, (0, 64), 64, "bf16"),
+    ("fp8_d64_g4_bs32_f16", 4, 8, 2, 32, (0, 96), 64, "f16"),
+    ("fp8_d64_g16_bs16", 4, 16, 1, 16, (0, 48), 64, "bf16"),
+    ("fp8_d64_g3_bs64", 5, 9, 3, 64, (0, 128), 64, "f16"),
 ]
 
 
@@ -70,8 +76,8 @@ def test_fp8_decode_shapes(case):
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     from paged_kv_cache_96_gb300 import step as St
-    name, S, H, Hkv, bs, parts = case
-    w = W.build(_spec(name, S, H, Hkv, 128, bs, "bf16", _uni(S, 1, 600), kv="fp8"))
+    name, S, H, Hkv, bs, parts, D, dt = case
+    w = W.build(_spec(name, S, H, Hkv, D, bs, dt, _uni(S, 1, 600), kv="fp8"))
     ref = OracleStep(w)
     want = ref.attention()
     for P in parts:
