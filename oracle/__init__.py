@@ -91,6 +91,8 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
         "oracle_paged_attention_fp8": (None, [P, P, P, P, P, i32, P, i32, i32, i32, i32,
                                               i32, dbl, i32, dbl, dbl, P, i32]),
         "oracle_copy_blocks_u8": (None, [P, P, P, i32, i32, i32, i32]),
+        "oracle_prefill_attention_fp8": (None, [P, P, P, P, P, i32, P, P, i32, i32, i32,
+                                                i32, i32, dbl, i32, dbl, dbl]),
         "oracle_prefill_attention": (None, [P, P, P, P, P, i32, P, P, i32, i32, i32,
                                             i32, i32, dbl, i32]),
     }
@@ -378,3 +380,27 @@ def copy_blocks_u8(key_cache: np.ndarray, value_cache: np.ndarray,
     bm = _i32(block_mapping).reshape(-1, 2)
     N, bs, Hkv, d = kc.shape
     lib.oracle_copy_blocks_u8(_ptr(kc), _ptr(vc), _ptr(bm), bm.shape[0], bs, Hkv, d)
+
+
+def prefill_attention_fp8(query: np.ndarray, key_cache: np.ndarray, value_cache: np.ndarray,
+                          block_tables: np.ndarray, query_start: np.ndarray,
+                          context_lens: np.ndarray, scale: float, dtype: int,
+                          k_scale: float, v_scale: float, lib=None) -> np.ndarray:
+    """Chunked prefill over FP8 pools (uint8 e4m3 codes, one scale per
+    pool): fp64 output [T, H, d], as prefill_attention with K and V the
+    dequantised codes."""
+    lib = lib or load()
+    q = _u16(query)
+    kc = np.ascontiguousarray(key_cache, dtype=np.uint8)
+    vc = np.ascontiguousarray(value_cache, dtype=np.uint8)
+    bt, qs, cl = _i32(block_tables), _i32(query_start), _i32(context_lens)
+    T, H, d = q.shape
+    N, bs, Hkv, d2 = kc.shape
+    S = cl.shape[0]
+    assert d == d2 and H % Hkv == 0 and qs.shape[0] == S + 1 and int(qs[-1]) == T
+    out = np.full((T, H, d), np.nan, dtype=np.float64)
+    lib.oracle_prefill_attention_fp8(_ptr(out), _ptr(q), _ptr(kc), _ptr(vc), _ptr(bt),
+                                     bt.shape[1], _ptr(qs), _ptr(cl), S, H, Hkv, d, bs,
+                                     float(scale), dtype, float(np.float32(k_scale)),
+                                     float(np.float32(v_scale)))
+    return out

@@ -467,6 +467,65 @@ void oracle_paged_attention_fp8(double *out, const uint16_t *query,
     }
 }
 
+/* Chunked prefill over FP8 pools: oracle_prefill_attention with K and V the
+ * dequantised codes (code value * k_scale, * v_scale).  Row i of sequence
+ * s's chunk sits at pos = context_len - q_len + i and attends [0, pos]; a
+ * negative position gives a zero row. */
+void oracle_prefill_attention_fp8(double *out, const uint16_t *query,
+                                  const uint8_t *key_cache, const uint8_t *value_cache,
+                                  const int32_t *block_tables, int max_blocks_per_seq,
+                                  const int32_t *query_start, const int32_t *context_lens,
+                                  int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                                  int block_size, double scale, int dtype, double k_scale,
+                                  double v_scale)
+{
+    int group = num_heads / num_kv_heads;
+    for (int s = 0; s < num_seqs; ++s) {
+        const int32_t *row = block_tables + (int64_t)s * max_blocks_per_seq;
+        int64_t q0 = query_start[s], q_len = query_start[s + 1] - query_start[s];
+        int64_t ctx = context_lens[s];
+        for (int64_t i = 0; i < q_len; ++i) {
+            int64_t pos = ctx - q_len + i;
+            for (int h = 0; h < num_heads; ++h) {
+                int64_t r = (q0 + i) * num_heads + h;
+                double *o = out + r * head_dim;
+                for (int k = 0; k < head_dim; ++k)
+                    o[k] = 0.0;
+                if (pos < 0)
+                    continue;
+                const uint16_t *q_row = query + r * head_dim;
+                int kh = h / group;
+                int64_t n = pos + 1;
+                double *scores = (double *)malloc(sizeof(double) * (size_t)n);
+                double m = -INFINITY;
+                for (int64_t p = 0; p < n; ++p) {
+                    int64_t k = cache_row(row, p, kh, num_kv_heads, head_dim, block_size);
+                    double dot = 0.0;
+                    for (int c = 0; c < head_dim; ++c)
+                        dot += decode(q_row[c], dtype) *
+                               (decode_e4m3(key_cache[k + c]) * k_scale);
+                    scores[p] = scale * dot;
+                    if (scores[p] > m)
+                        m = scores[p];
+                }
+                double l = 0.0;
+                for (int64_t p = 0; p < n; ++p) {
+                    scores[p] = exp(scores[p] - m);
+                    l += scores[p];
+                }
+                for (int64_t p = 0; p < n; ++p) {
+                    int64_t v = cache_row(row, p, kh, num_kv_heads, head_dim, block_size);
+                    for (int c = 0; c < head_dim; ++c)
+                        o[c] += scores[p] * (decode_e4m3(value_cache[v + c]) * v_scale);
+                }
+                for (int c = 0; c < head_dim; ++c)
+                    o[c] /= l;
+                free(scores);
+            }
+        }
+    }
+}
+
 /* Block copies of 1-byte (FP8) pools, pairs applied in order. */
 void oracle_copy_blocks_u8(uint8_t *key_cache, uint8_t *value_cache,
                            const int32_t *block_mapping, int num_pairs, int block_size,

@@ -637,6 +637,36 @@ def pin_prefill_matches_causal_sdpa(lib):
         _close(got, want, 1e-11, 1e-12, f"causal sdpa {dtype} {H}/{Hkv}")
 
 
+def pin_fp8_prefill_matches_causal_sdpa(lib):
+    """Chunked prefill over FP8 pools (the FP8 KV cache of "vLLM 架构详解"'s
+    deployment options, read by GAO §2.4/§2.5's chunk rows): torch float64
+    SDPA with the causal mask on the dequantised gathered codes (torch's e4m3
+    values times each pool's scale); a mixed batch with decode rows, whole
+    prompts, mid-context chunks and an empty chunk."""
+    rng = np.random.default_rng(61)
+    table = _e4m3_values()
+    ks, vs = 0.011, 0.013
+    for dtype, (H, Hkv, d, bs) in (("bf16", (4, 2, 16, 4)), ("f16", (6, 3, 8, 8))):
+        ctxs, q_lens = [7, 5, 20, 33, 9], [1, 5, 3, 16, 0]
+        c = _prefill_case(rng, ctxs, q_lens, H, Hkv, d, bs, dtype)
+        kl = [_torch_e4m3(rng.standard_normal((n, Hkv, d)).astype(np.float32) * 60)
+              for n in ctxs]
+        vl = [_torch_e4m3(rng.standard_normal((n, Hkv, d)).astype(np.float32) * 60)
+              for n in ctxs]
+        kc = place_sequences(kl, c["tables"], c["N"], bs, fill=np.uint8(0x7F)).astype(np.uint8)
+        vc = place_sequences(vl, c["tables"], c["N"], bs, fill=np.uint8(0x7F)).astype(np.uint8)
+        scale = 1.0 / math.sqrt(d)
+        dt = oracle.F16 if dtype == "f16" else oracle.BF16
+        got = oracle.prefill_attention_fp8(c["qrows"], kc, vc, c["tables"], c["qs"], c["ctx"],
+                                           scale, dt, ks, vs, lib=lib)
+        # the same rows through the mask-based reference, K/V dequantised
+        c2 = dict(c, kl=[table[k] * float(np.float32(ks)) for k in kl],
+                  vl=[table[v] * float(np.float32(vs)) for v in vl])
+        want = _causal_sdpa(c2, scale, lambda x, dd=_dec(dtype): (
+            x if x.dtype == np.float64 else dd(x)))
+        _close(got, want, 1e-11, 1e-12, f"fp8 causal sdpa {dtype} {H}/{Hkv}")
+
+
 def pin_prefill_causal_closed_forms(lib):
     """A whole prompt as one chunk: its first row sees only token 0, so its
     output is v_0 exactly; poisoning (NaN) the K/V of the last token leaves

@@ -116,6 +116,15 @@ MUTANTS = [
     ("fp8_cache_swaps_scales",
      "                             dtype, k_inv_scale);",
      "                             dtype, v_inv_scale);", 0),
+    ("fp8_prefill_excludes_own_token",
+     "                int64_t n = pos + 1;\n                double *scores = (double *)malloc(sizeof(double) * (size_t)n);",
+     "                int64_t n = pos;\n                double *scores = (double *)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1));", 0),
+    ("fp8_prefill_value_scale_is_k_scale",
+     "o[c] += scores[p] * (decode_e4m3(value_cache[v + c]) * v_scale);",
+     "o[c] += scores[p] * (decode_e4m3(value_cache[v + c]) * k_scale);", 0),
+    ("fp8_prefill_positions_from_chunk_start",
+     "            int64_t pos = ctx - q_len + i;\n            for (int h = 0; h < num_heads; ++h) {\n                int64_t r = (q0 + i) * num_heads + h;\n                double *o = out + r * head_dim;\n                for (int k = 0; k < head_dim; ++k)",
+     "            int64_t pos = i;\n            for (int h = 0; h < num_heads; ++h) {\n                int64_t r = (q0 + i) * num_heads + h;\n                double *o = out + r * head_dim;\n                for (int k = 0; k < head_dim; ++k)", 0),
     ("copy_blocks_u8_swapped",
      "        memcpy(key_cache + dst * block_elems, key_cache + src * block_elems,",
      "        memcpy(key_cache + src * block_elems, key_cache + dst * block_elems,", 0),
