@@ -60,7 +60,8 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--config", default="gqa70b",
                     choices=["tiny", "mha7b", "gqa70b", "longctx", "prefix", "gqa70b-fp8",
-                             "longctx-fp8", "prefix-cascade", "mixed", "chunked"])
+                             "longctx-fp8", "prefix-cascade", "prefix-cascade-fp8", "mixed",
+                             "chunked", "chunked-fp8"])
     ap.add_argument("--partition", type=int, default=None,
                     help="split-context partition tokens (0 = single pass)")
     ap.add_argument("--separate-append", action="store_true",
@@ -293,7 +294,7 @@ def workload_config(w, partition_size, world=1):
             "attention_flops_per_step": w.prefill_flops(),
             "l2": l2_note(w),
             "parallelism": "replicas" if world > 1 else "single GPU",
-            "kv_cache_dtype": w.dtype,
+            "kv_cache_dtype": "fp8-e4m3" if w.fp8 else w.dtype,
         }
     return {
         "workload": f"{w.spec.name}: {w.spec.description}",
@@ -348,10 +349,12 @@ class OracleCache:
             sq = np.asarray(seqs, dtype=np.int64)
             sub_qs = np.zeros(len(seqs) + 1, dtype=np.int32)
             sub_qs[1:] = np.cumsum(qs[sq + 1] - qs[sq])
-            return o.prefill_attention(np.ascontiguousarray(w.query[rows]), self.kc, self.vc,
-                                       np.ascontiguousarray(w.step_block_tables[sq]), sub_qs,
-                                       np.ascontiguousarray(w.context_lens[sq]), w.scale,
-                                       self.dt)
+            args = (np.ascontiguousarray(w.query[rows]), self.kc, self.vc,
+                    np.ascontiguousarray(w.step_block_tables[sq]), sub_qs,
+                    np.ascontiguousarray(w.context_lens[sq]), w.scale, self.dt)
+            if w.fp8:
+                return o.prefill_attention_fp8(*args, w.spec.kv_scale, w.spec.kv_scale)
+            return o.prefill_attention(*args)
         if w.fp8:
             return o.paged_attention_fp8(w.query, self.kc, self.vc, w.step_block_tables,
                                          w.context_lens, w.scale, self.dt, w.spec.kv_scale,
@@ -709,7 +712,9 @@ def run_ours(args):
             "metric": PREFILL_METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
             "steps": K, "warmup": args.warmup, "ms_per_step": per_step * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": f"{w.dtype} mma.sync, fp32 accumulate", "data": "synthetic",
+            "dtype": ("fp8-e4m3 KV widened to fp16, tcgen05 kind::f16, fp32 accumulate"
+                      if w.fp8 else f"{w.dtype} tcgen05 kind::f16, fp32 accumulate"),
+            "data": "synthetic",
             "config": workload_config(w, 0, world),
             "tokens_per_s": w.T * world / per_step,
             "us_per_step": per_step * 1e6,
@@ -737,10 +742,14 @@ def run_ours(args):
                   "append, split contexts merged in the pass)")
     if st.cascade:
         kernel = ("pa_decode_attention_cascade (paged_decode_kernel + paged_mq_kernel "
-                  "prefix pass + paged_reduce_kernel)")
+                  "prefix pass, merges in whichever pass completes a sequence)")
         if st.fused_append:
             kernel = ("pa_decode_attention_cascade_append (paged_decode_kernel with the new "
-                      "tokens' append + paged_mq_kernel prefix pass + paged_reduce_kernel)")
+                      "tokens' append + paged_mq_kernel prefix pass, merges in whichever "
+                      "pass completes a sequence)")
+    if st.launches_per_step() > (1 if st.fused_append else 2) + \
+            (1 if st.cow_pairs is not None else 0) + (1 if st.cascade and st.num_groups else 0):
+        kernel += " + paged_reduce_kernel"
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": per_step * 1e3, "higher_is_better": True,

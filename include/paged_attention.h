@@ -332,7 +332,7 @@ PA_API pa_status pa_decode_attention_append_fp8(
  *                 (chunk longer than the context) gets a zero row.
  * scale must be positive (PA_ERR_INVALID_ARG otherwise).  Accumulation fp32
  * (online softmax), output rounded to nearest even.  No workspace.
- * Supported: as pa_decode_attention (FP8 pools: PA_ERR_UNSUPPORTED).
+ * Supported: as pa_decode_attention (FP8 pools: pa_prefill_attention_fp8).
  */
 PA_API pa_status pa_prefill_attention(void *out, const void *query, const void *key_cache,
                                       const void *value_cache, const int32_t *block_tables,
@@ -342,6 +342,29 @@ PA_API pa_status pa_prefill_attention(void *out, const void *query, const void *
                                       int num_kv_heads, int head_dim, int block_size,
                                       int num_blocks, float scale, pa_dtype dtype,
                                       int32_t *error_word, void *stream);
+
+/*
+ * pa_prefill_attention_fp8 -- pa_prefill_attention over FP8 pools written by
+ * pa_reshape_and_cache_fp8 (K and V elements are e4m3 codes standing for
+ * e4m3(code) * k_scale and * v_scale), as pa_decode_attention_fp8 is to
+ * pa_decode_attention: the tensor-core tiles take the codes widened to fp16
+ * (exact) and the query rounded to fp16 (a bf16 query element with |q| >
+ * 65504 is flagged PA_DEVERR_QUERY_RANGE and its rows are not finite); k_scale
+ * joins the softmax scale, v_scale multiplies the output.  query and out are
+ * dtype (PA_F16 or PA_BF16); k_scale and v_scale must be positive and finite
+ * (PA_ERR_INVALID_ARG).  Supported: head_dim 128 (PA_ERR_UNSUPPORTED
+ * otherwise); other limits, arguments, rows and errors as
+ * pa_prefill_attention.
+ */
+PA_API pa_status pa_prefill_attention_fp8(void *out, const void *query, const void *key_cache,
+                                          const void *value_cache, const int32_t *block_tables,
+                                          int max_blocks_per_seq, const int32_t *query_start,
+                                          const int32_t *context_lens, int max_context_len,
+                                          int num_seqs, int num_tokens, int num_heads,
+                                          int num_kv_heads, int head_dim, int block_size,
+                                          int num_blocks, float scale, float k_scale,
+                                          float v_scale, pa_dtype dtype, int32_t *error_word,
+                                          void *stream);
 
 /*
  * Prefix plan -- which sequences of a decode batch share leading physical
@@ -418,7 +441,7 @@ PA_API size_t pa_cascade_workspace_bytes(int num_seqs, int num_heads, int num_kv
  * PA_DEVERR_PREFIX_PLAN and leaves those rows undefined.  num_groups == 0
  * is plain split decode.  scale must be positive (PA_ERR_INVALID_ARG
  * otherwise).  Other arguments, limits and errors as pa_decode_attention
- * (16-bit pools).
+ * (16-bit pools; FP8 pools: pa_decode_attention_cascade_fp8).
  */
 PA_API pa_status pa_decode_attention_cascade(void *out, const void *query, const void *key_cache,
                                              const void *value_cache,
@@ -454,6 +477,36 @@ PA_API pa_status pa_decode_attention_cascade_append(
     int num_heads, int num_kv_heads, int head_dim, int block_size, int num_blocks, float scale,
     const int32_t *prefix_plan, int num_groups, int num_members, int partition_size,
     void *workspace, size_t workspace_bytes, pa_dtype dtype, int32_t *error_word, void *stream);
+
+/*
+ * pa_decode_attention_cascade_fp8, pa_decode_attention_cascade_append_fp8 --
+ * the prefix-aware decode (and its fused append) over FP8 pools written by
+ * pa_reshape_and_cache_fp8, with the arithmetic of pa_decode_attention_fp8
+ * in both passes (codes widened to fp16, query rounded to fp16 and flagged
+ * PA_DEVERR_QUERY_RANGE beyond it, k_scale in the softmax scale, v_scale on
+ * the output) and the append's codes as pa_decode_attention_append_fp8
+ * writes them.  k_scale, v_scale positive and finite (PA_ERR_INVALID_ARG).
+ * Supported with groups: head_dim 128 (PA_ERR_UNSUPPORTED otherwise); with
+ * num_groups == 0 these are pa_decode_attention_fp8 /
+ * pa_decode_attention_append_fp8.  Other arguments, workspace and errors as
+ * pa_decode_attention_cascade(_append).
+ */
+PA_API pa_status pa_decode_attention_cascade_fp8(
+    void *out, const void *query, const void *key_cache, const void *value_cache,
+    const int32_t *block_tables, int max_blocks_per_seq, const int32_t *context_lens,
+    int max_context_len, int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+    int block_size, int num_blocks, float scale, float k_scale, float v_scale,
+    const int32_t *prefix_plan, int num_groups, int num_members, int partition_size,
+    void *workspace, size_t workspace_bytes, pa_dtype dtype, int32_t *error_word, void *stream);
+
+PA_API pa_status pa_decode_attention_cascade_append_fp8(
+    void *out, const void *query, void *key_cache, void *value_cache, const void *new_key,
+    const void *new_value, int32_t *slot_mapping, const int32_t *block_tables,
+    int max_blocks_per_seq, const int32_t *context_lens, int max_context_len, int num_seqs,
+    int num_heads, int num_kv_heads, int head_dim, int block_size, int num_blocks, float scale,
+    float k_scale, float v_scale, const int32_t *prefix_plan, int num_groups, int num_members,
+    int partition_size, void *workspace, size_t workspace_bytes, pa_dtype dtype,
+    int32_t *error_word, void *stream);
 
 /*
  * pa_decode_attention_noalloc -- no counterpart on the pages: an addition

@@ -78,6 +78,8 @@ def _load() -> ctypes.CDLL:
                                                  P, sz, i32, P, P]),
         "pa_prefill_attention": (i32, [P, P, P, P, P, i32, P, P, i32, i32, i32, i32, i32,
                                        i32, i32, i32, f32, i32, P, P]),
+        "pa_prefill_attention_fp8": (i32, [P, P, P, P, P, i32, P, P, i32, i32, i32, i32,
+                                           i32, i32, i32, i32, f32, f32, f32, i32, P, P]),
         "pa_prefix_plan_ints": (sz, [i32, i32, i32]),
         "pa_plan_prefix_groups": (i32, [P, i32, P, i32, i32, i32, P, sz, P, P]),
         "pa_cascade_workspace_bytes": (sz, [i32, i32, i32, i32, i32, i32]),
@@ -87,6 +89,13 @@ def _load() -> ctypes.CDLL:
         "pa_decode_attention_cascade_append": (i32, [P, P, P, P, P, P, P, P, i32, P, i32,
                                                      i32, i32, i32, i32, i32, i32, f32, P,
                                                      i32, i32, i32, P, sz, i32, P, P]),
+        "pa_decode_attention_cascade_fp8": (i32, [P, P, P, P, P, i32, P, i32, i32, i32, i32,
+                                                  i32, i32, i32, f32, f32, f32, P, i32, i32,
+                                                  i32, P, sz, i32, P, P]),
+        "pa_decode_attention_cascade_append_fp8": (i32, [P, P, P, P, P, P, P, P, i32, P, i32,
+                                                         i32, i32, i32, i32, i32, i32, f32,
+                                                         f32, f32, P, i32, i32, i32, P, sz,
+                                                         i32, P, P]),
         "pa_bm_create": (i32, [i32, i32, i32, P]),
         "pa_bm_destroy": (None, [P]),
         "pa_bm_num_free_blocks": (i32, [P]),
@@ -424,25 +433,34 @@ def pa_prefill_attention(out: torch.Tensor, query: torch.Tensor, key_cache: torc
                          value_cache: torch.Tensor, block_tables: torch.Tensor,
                          query_start: torch.Tensor, context_lens: torch.Tensor,
                          max_context_len: int, scale: float,
-                         error_word: Optional[torch.Tensor] = None, stream=None) -> None:
+                         error_word: Optional[torch.Tensor] = None, stream=None,
+                         k_scale: float = 1.0, v_scale: float = 1.0) -> None:
     """Chunked prefill / mixed batch: out and query are [T, H, d]; sequence s
-    owns rows [query_start[s], query_start[s+1]), its newest tokens."""
+    owns rows [query_start[s], query_start[s+1]), its newest tokens.  uint8
+    pools take the e4m3 path (pa_prefill_attention_fp8) with k_scale /
+    v_scale."""
     T, H, d = query.shape
     N, bs, Hkv, d2 = key_cache.shape
     MB = block_tables.shape[1]
     S = context_lens.shape[0]
     if d != d2 or out.shape != query.shape or query_start.shape[0] != S + 1:
         raise ValueError("shape mismatch")
-    if key_cache.dtype == torch.uint8:
-        raise TypeError("FP8 pools are not supported by pa_prefill_attention")
+    fp8 = key_cache.dtype == torch.uint8
+    if not fp8 and query.dtype != key_cache.dtype:
+        raise TypeError("query and pools must share one 16-bit type")
+    head = (_dev(out, "out", query.dtype), _dev(query, "query"),
+            _dev(key_cache, "key_cache"), _dev(value_cache, "value_cache", key_cache.dtype),
+            _dev(block_tables, "block_tables", torch.int32), MB,
+            _dev(query_start, "query_start", torch.int32),
+            _dev(context_lens, "context_lens", torch.int32), int(max_context_len), S, T, H,
+            Hkv, d, bs, N, float(scale))
+    if fp8:
+        _check("pa_prefill_attention_fp8", _lib.pa_prefill_attention_fp8(
+            *head, float(k_scale), float(v_scale), _dtype_code(query),
+            _opt(error_word, "error_word"), _stream(stream)))
+        return
     _check("pa_prefill_attention", _lib.pa_prefill_attention(
-        _dev(out, "out", query.dtype), _dev(query, "query", key_cache.dtype),
-        _dev(key_cache, "key_cache"), _dev(value_cache, "value_cache", key_cache.dtype),
-        _dev(block_tables, "block_tables", torch.int32), MB,
-        _dev(query_start, "query_start", torch.int32),
-        _dev(context_lens, "context_lens", torch.int32), int(max_context_len), S, T, H, Hkv,
-        d, bs, N, float(scale), _dtype_code(key_cache), _opt(error_word, "error_word"),
-        _stream(stream)))
+        *head, _dtype_code(key_cache), _opt(error_word, "error_word"), _stream(stream)))
 
 
 def pa_plan_prefix_groups(block_tables, context_lens, block_size: int,
@@ -480,28 +498,36 @@ def pa_decode_attention_cascade(out: torch.Tensor, query: torch.Tensor,
                                 num_groups: int, num_members: int, partition_size: int,
                                 workspace: torch.Tensor,
                                 error_word: Optional[torch.Tensor] = None,
-                                stream=None) -> None:
+                                stream=None, k_scale: float = 1.0,
+                                v_scale: float = 1.0) -> None:
     """Prefix-aware decode: pa_decode_attention's result with each planned
-    group's shared prefix read once (prefix_plan on the device)."""
+    group's shared prefix read once (prefix_plan on the device).  uint8
+    pools take the e4m3 path with k_scale / v_scale."""
     S, H, d = query.shape
     N, bs, Hkv, d2 = key_cache.shape
     MB = block_tables.shape[1]
     if d != d2 or out.shape != query.shape:
         raise ValueError("shape mismatch")
-    if key_cache.dtype == torch.uint8:
-        raise TypeError("FP8 pools are not supported by pa_decode_attention_cascade")
+    fp8 = key_cache.dtype == torch.uint8
+    if not fp8 and query.dtype != key_cache.dtype:
+        raise TypeError("query and pools must share one 16-bit type")
     ws_ptr, ws_bytes = None, 0
     if workspace is not None:
         ws_ptr = _dev(workspace, "workspace")
         ws_bytes = workspace.numel() * workspace.element_size()
-    _check("pa_decode_attention_cascade", _lib.pa_decode_attention_cascade(
-        _dev(out, "out", query.dtype), _dev(query, "query", key_cache.dtype),
-        _dev(key_cache, "key_cache"), _dev(value_cache, "value_cache", key_cache.dtype),
-        _dev(block_tables, "block_tables", torch.int32), MB,
-        _dev(context_lens, "context_lens", torch.int32), int(max_context_len), S, H, Hkv,
-        d, bs, N, float(scale), _dev(prefix_plan, "prefix_plan", torch.int32),
-        int(num_groups), int(num_members), int(partition_size), ws_ptr, ws_bytes,
-        _dtype_code(key_cache), _opt(error_word, "error_word"), _stream(stream)))
+    head = (_dev(out, "out", query.dtype), _dev(query, "query"),
+            _dev(key_cache, "key_cache"), _dev(value_cache, "value_cache", key_cache.dtype),
+            _dev(block_tables, "block_tables", torch.int32), MB,
+            _dev(context_lens, "context_lens", torch.int32), int(max_context_len), S, H, Hkv,
+            d, bs, N, float(scale))
+    tail = (_dev(prefix_plan, "prefix_plan", torch.int32), int(num_groups),
+            int(num_members), int(partition_size), ws_ptr, ws_bytes, _dtype_code(query),
+            _opt(error_word, "error_word"), _stream(stream))
+    if fp8:
+        _check("pa_decode_attention_cascade_fp8", _lib.pa_decode_attention_cascade_fp8(
+            *head, float(k_scale), float(v_scale), *tail))
+        return
+    _check("pa_decode_attention_cascade", _lib.pa_decode_attention_cascade(*head, *tail))
 
 
 def pa_decode_attention_cascade_append(out: torch.Tensor, query: torch.Tensor,
@@ -514,10 +540,12 @@ def pa_decode_attention_cascade_append(out: torch.Tensor, query: torch.Tensor,
                                        workspace: torch.Tensor,
                                        slot_mapping: Optional[torch.Tensor] = None,
                                        error_word: Optional[torch.Tensor] = None,
-                                       stream=None) -> None:
+                                       stream=None, k_scale: float = 1.0,
+                                       v_scale: float = 1.0) -> None:
     """Prefix-aware decode step in one call: each sequence's new token
     (new_key / new_value [S, Hkv, d], position context_lens[s] - 1) written
-    to the pools and attended, each planned group's shared prefix read once."""
+    to the pools and attended, each planned group's shared prefix read once.
+    uint8 pools take the e4m3 path with k_scale / v_scale."""
     S, H, d = query.shape
     N, bs, Hkv, d2 = key_cache.shape
     MB = block_tables.shape[1]
@@ -527,21 +555,29 @@ def pa_decode_attention_cascade_append(out: torch.Tensor, query: torch.Tensor,
         raise ValueError("new_key / new_value must be [num_seqs, num_kv_heads, head_dim]")
     if slot_mapping is not None and slot_mapping.shape[0] != S:
         raise ValueError("one slot per sequence expected")
-    if key_cache.dtype == torch.uint8:
-        raise TypeError("FP8 pools are not supported by the prefix-aware decode")
+    fp8 = key_cache.dtype == torch.uint8
+    if not fp8 and query.dtype != key_cache.dtype:
+        raise TypeError("query and pools must share one 16-bit type")
     ws_ptr, ws_bytes = None, 0
     if workspace is not None:
         ws_ptr = _dev(workspace, "workspace")
         ws_bytes = workspace.numel() * workspace.element_size()
-    _check("pa_decode_attention_cascade_append", _lib.pa_decode_attention_cascade_append(
-        _dev(out, "out", query.dtype), _dev(query, "query", key_cache.dtype),
-        _dev(key_cache, "key_cache"), _dev(value_cache, "value_cache", key_cache.dtype),
-        _dev(new_key, "new_key", key_cache.dtype), _dev(new_value, "new_value", key_cache.dtype),
-        _opt(slot_mapping, "slot_mapping"), _dev(block_tables, "block_tables", torch.int32), MB,
-        _dev(context_lens, "context_lens", torch.int32), int(max_context_len), S, H, Hkv,
-        d, bs, N, float(scale), _dev(prefix_plan, "prefix_plan", torch.int32),
-        int(num_groups), int(num_members), int(partition_size), ws_ptr, ws_bytes,
-        _dtype_code(key_cache), _opt(error_word, "error_word"), _stream(stream)))
+    head = (_dev(out, "out", query.dtype), _dev(query, "query"),
+            _dev(key_cache, "key_cache"), _dev(value_cache, "value_cache", key_cache.dtype),
+            _dev(new_key, "new_key", query.dtype), _dev(new_value, "new_value", query.dtype),
+            _opt(slot_mapping, "slot_mapping"), _dev(block_tables, "block_tables", torch.int32),
+            MB, _dev(context_lens, "context_lens", torch.int32), int(max_context_len), S, H,
+            Hkv, d, bs, N, float(scale))
+    tail = (_dev(prefix_plan, "prefix_plan", torch.int32), int(num_groups),
+            int(num_members), int(partition_size), ws_ptr, ws_bytes, _dtype_code(query),
+            _opt(error_word, "error_word"), _stream(stream))
+    if fp8:
+        _check("pa_decode_attention_cascade_append_fp8",
+               _lib.pa_decode_attention_cascade_append_fp8(*head, float(k_scale),
+                                                           float(v_scale), *tail))
+        return
+    _check("pa_decode_attention_cascade_append",
+           _lib.pa_decode_attention_cascade_append(*head, *tail))
 
 
 class BlockManager:

@@ -924,7 +924,8 @@ static pa_status launch_pass(const DecodeParams &prm, const CUtensorMap &mk,
 // dependent of the one before.
 struct PrefixPass {
     const MqParams *prm;
-    pa_dtype dtype;
+    pa_dtype dtype;        // the pools' (PA_FP8_E4M3 for e4m3 pools)
+    pa_dtype query_dtype;  // the query's and the output's
     const void *key_cache, *value_cache;
     long long max_units;
 };
@@ -940,7 +941,8 @@ static pa_status launch_decode(const DecodeParams &prm, const CUtensorMap &mk,
     DecodeParams pass = prm;
     pass.concurrent = 0;
     if (prefix != nullptr) {
-        const pa_status ps = launch_prefix_pass(*prefix->prm, prefix->dtype, prefix->key_cache,
+        const pa_status ps = launch_prefix_pass(*prefix->prm, prefix->dtype,
+                                                prefix->query_dtype, prefix->key_cache,
                                                 prefix->value_cache, D, stream,
                                                 prefix->max_units);
         if (ps != PA_OK)
@@ -1186,14 +1188,28 @@ static pa_status run_cascade(void *out, const void *query, void *key_cache, void
                              int num_blocks, float scale, const int32_t *prefix_plan,
                              int num_groups, int num_members, int partition_size,
                              void *workspace, size_t workspace_bytes, pa_dtype dtype,
+                             bool fp8, float k_scale, float v_scale,
                              int32_t *error_word, void *stream)
 {
     if (dtype != PA_F16 && dtype != PA_BF16)
-        return dtype == PA_FP8_E4M3 ? PA_ERR_UNSUPPORTED : PA_ERR_INVALID_ARG;
+        return dtype == PA_FP8_E4M3 && !fp8 ? PA_ERR_UNSUPPORTED : PA_ERR_INVALID_ARG;
     if (num_groups < 0 || num_members < 0 || (num_groups > 0 && num_members < 2 * num_groups) ||
-        !(scale > 0.f))
+        !(scale > 0.f) || (fp8 && !valid_fp8_scales(k_scale, v_scale)))
         return PA_ERR_INVALID_ARG;
     if (num_groups == 0) {
+        if (fp8) {
+            if (new_key == nullptr)
+                return pa_decode_attention_fp8(
+                    out, query, key_cache, value_cache, block_tables, max_blocks_per_seq,
+                    context_lens, max_context_len, num_seqs, num_heads, num_kv_heads, head_dim,
+                    block_size, num_blocks, scale, k_scale, v_scale, partition_size, workspace,
+                    workspace_bytes, dtype, error_word, stream);
+            return pa_decode_attention_append_fp8(
+                out, query, key_cache, value_cache, new_key, new_value, slot_mapping,
+                block_tables, max_blocks_per_seq, context_lens, max_context_len, num_seqs,
+                num_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, k_scale,
+                v_scale, partition_size, workspace, workspace_bytes, dtype, error_word, stream);
+        }
         if (new_key == nullptr)
             return pa_decode_attention(out, query, key_cache, value_cache, block_tables,
                                        max_blocks_per_seq, context_lens, max_context_len,
@@ -1216,10 +1232,21 @@ static pa_status run_cascade(void *out, const void *query, void *key_cache, void
         return ok;
     if (prefix_plan == nullptr)
         return PA_ERR_INVALID_ARG;
+    if (fp8 && head_dim != 128)
+        return PA_ERR_UNSUPPORTED;  // the FP8 prefix pass: head_dim 128
     if (new_key != nullptr) {
         ok = set_append(&prm, key_cache, value_cache, new_key, new_value, slot_mapping);
         if (ok != PA_OK)
             return ok;
+    }
+    if (fp8) {
+        // scores of the K codes (the K scale in the exponent's scale), the V
+        // scale on the outputs and partials; the append's codes as
+        // reshape_and_cache_fp8 computes them
+        prm.scale_log2 = scale * k_scale * kLog2e;
+        prm.out_scale = v_scale;
+        prm.k_inv_scale = 1.0f / k_scale;
+        prm.v_inv_scale = 1.0f / v_scale;
     }
     // the shared prefix [0, L) and the own tokens [L, ctx) are each cut into
     // partitions of part_tokens: ceil(L / P) + ceil((ctx - L) / P) <=
@@ -1270,15 +1297,17 @@ static pa_status run_cascade(void *out, const void *query, void *key_cache, void
     mq.max_parts = parts;
     mq.part_tokens = prm.part_tokens;
     mq.scale_log2 = prm.scale_log2;
+    mq.out_scale = prm.out_scale;
     const long long prefix_parts = (max_context_len + prm.part_tokens - 1) / prm.part_tokens;
-    PrefixPass pp{&mq, dtype, key_cache, value_cache,
+    const pa_dtype pool_dtype = fp8 ? PA_FP8_E4M3 : dtype;
+    PrefixPass pp{&mq, pool_dtype, dtype, key_cache, value_cache,
                   ((long long)num_members * prm.group / 128 + num_groups) * prefix_parts *
                       num_kv_heads};
 
     CUtensorMap mk, mv;
-    if (!encode_pool_map(&mk, key_cache, dtype, num_blocks, block_size, num_kv_heads,
+    if (!encode_pool_map(&mk, key_cache, pool_dtype, num_blocks, block_size, num_kv_heads,
                          head_dim) ||
-        !encode_pool_map(&mv, value_cache, dtype, num_blocks, block_size, num_kv_heads,
+        !encode_pool_map(&mv, value_cache, pool_dtype, num_blocks, block_size, num_kv_heads,
                          head_dim))
         return PA_ERR_CUDA;
     const long long max_units = (long long)num_seqs * num_kv_heads * parts;
@@ -1287,6 +1316,14 @@ static pa_status run_cascade(void *out, const void *query, void *key_cache, void
     const bool wide = prm.group > 8;
     using B16 = __nv_bfloat16;
     using F16 = __half;
+    using U8 = uint8_t;
+    if (fp8) {
+        if (bf)
+            return wide ? launch_decode<B16, U8, 128, 2>(prm, mk, mv, st, max_units, &pp)
+                        : launch_decode<B16, U8, 128, 1>(prm, mk, mv, st, max_units, &pp);
+        return wide ? launch_decode<F16, U8, 128, 2>(prm, mk, mv, st, max_units, &pp)
+                    : launch_decode<F16, U8, 128, 1>(prm, mk, mv, st, max_units, &pp);
+    }
     if (head_dim == 128) {
         if (bf)
             return wide ? launch_decode<B16, B16, 128, 2>(prm, mk, mv, st, max_units, &pp)
@@ -1314,7 +1351,23 @@ extern "C" pa_status pa_decode_attention_cascade(
                        block_tables, max_blocks_per_seq, context_lens, max_context_len,
                        num_seqs, num_heads, num_kv_heads, head_dim, block_size, num_blocks,
                        scale, prefix_plan, num_groups, num_members, partition_size, workspace,
-                       workspace_bytes, dtype, error_word, stream);
+                       workspace_bytes, dtype, false, 1.f, 1.f, error_word, stream);
+}
+
+extern "C" pa_status pa_decode_attention_cascade_fp8(
+    void *out, const void *query, const void *key_cache, const void *value_cache,
+    const int32_t *block_tables, int max_blocks_per_seq, const int32_t *context_lens,
+    int max_context_len, int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+    int block_size, int num_blocks, float scale, float k_scale, float v_scale,
+    const int32_t *prefix_plan, int num_groups, int num_members, int partition_size,
+    void *workspace, size_t workspace_bytes, pa_dtype dtype, int32_t *error_word, void *stream)
+{
+    return run_cascade(out, query, const_cast<void *>(key_cache),
+                       const_cast<void *>(value_cache), nullptr, nullptr, nullptr,
+                       block_tables, max_blocks_per_seq, context_lens, max_context_len,
+                       num_seqs, num_heads, num_kv_heads, head_dim, block_size, num_blocks,
+                       scale, prefix_plan, num_groups, num_members, partition_size, workspace,
+                       workspace_bytes, dtype, true, k_scale, v_scale, error_word, stream);
 }
 
 extern "C" pa_status pa_decode_attention_cascade_append(
@@ -1331,5 +1384,23 @@ extern "C" pa_status pa_decode_attention_cascade_append(
                        block_tables, max_blocks_per_seq, context_lens, max_context_len,
                        num_seqs, num_heads, num_kv_heads, head_dim, block_size, num_blocks,
                        scale, prefix_plan, num_groups, num_members, partition_size, workspace,
-                       workspace_bytes, dtype, error_word, stream);
+                       workspace_bytes, dtype, false, 1.f, 1.f, error_word, stream);
+}
+
+extern "C" pa_status pa_decode_attention_cascade_append_fp8(
+    void *out, const void *query, void *key_cache, void *value_cache, const void *new_key,
+    const void *new_value, int32_t *slot_mapping, const int32_t *block_tables,
+    int max_blocks_per_seq, const int32_t *context_lens, int max_context_len, int num_seqs,
+    int num_heads, int num_kv_heads, int head_dim, int block_size, int num_blocks, float scale,
+    float k_scale, float v_scale, const int32_t *prefix_plan, int num_groups, int num_members,
+    int partition_size, void *workspace, size_t workspace_bytes, pa_dtype dtype,
+    int32_t *error_word, void *stream)
+{
+    if (num_seqs > 0 && (new_key == nullptr || new_value == nullptr))
+        return PA_ERR_INVALID_ARG;
+    return run_cascade(out, query, key_cache, value_cache, new_key, new_value, slot_mapping,
+                       block_tables, max_blocks_per_seq, context_lens, max_context_len,
+                       num_seqs, num_heads, num_kv_heads, head_dim, block_size, num_blocks,
+                       scale, prefix_plan, num_groups, num_members, partition_size, workspace,
+                       workspace_bytes, dtype, true, k_scale, v_scale, error_word, stream);
 }

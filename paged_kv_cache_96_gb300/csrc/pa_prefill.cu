@@ -110,8 +110,8 @@ template <int D> struct TcLayout {
     static constexpr int kKVBytes = kHalves * kKVHalf;        // K (or V) of one stage
     static constexpr int kStageBytes = 2 * kKVBytes;          // K then V
     static constexpr int kQ = kTcStages * kStageBytes;
-    static constexpr int kBars = kQ + kHalves * kQHalf;       // 12 mbarriers
-    static constexpr int kTmemSlot = kBars + 12 * 8;
+    static constexpr int kBars = kQ + kHalves * kQHalf;       // 16 mbarriers
+    static constexpr int kTmemSlot = kBars + 16 * 8;
     static constexpr int kAbort = kTmemSlot + 8;
     static constexpr int kSeg = kTmemSlot + 16;               // int unit prefix[n + 1]
     static size_t bytes(int segments) { return 1024 + kSeg + 4 * ((size_t)segments + 1); }
@@ -153,14 +153,22 @@ __device__ __forceinline__ int mq_segment_units(const MqParams &p, int seg)
     return tiles * ((mq_group_prefix(p, seg) + p.part_tokens - 1) / p.part_tokens);
 }
 
-template <typename T, int D>
+// kFp8: the pools hold e4m3 codes.  The fetch warps land each 64-token FP8
+// tile in the upper half of its 16-bit stage and widen it there to fp16 (the
+// stage's K-major / MN-major operand layout, as a 16-bit fill leaves it),
+// then release the stage; the products run in fp16 with the query rounded to
+// fp16, the K scale folded into the exponent's scale and the V scale into
+// the output.
+template <typename T, int D, bool kFp8>
 __global__ void __launch_bounds__(kTcThreads, 2)
     paged_mq_kernel(const __grid_constant__ MqParams p,
                     const __grid_constant__ CUtensorMap tmap_k,
                     const __grid_constant__ CUtensorMap tmap_v)
 {
     using L = TcLayout<D>;
-    constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
+    static_assert(!kFp8 || D == 128, "FP8 pools: head_dim 128");
+    using OT = typename std::conditional<kFp8, __half, T>::type;  // operand type
+    constexpr bool kBf16 = std::is_same<OT, __nv_bfloat16>::value;
     constexpr uint32_t kIdescS = idesc_f16(kBf16, kTcRows, kTcTokens, false, false);
     constexpr uint32_t kIdescO = idesc_f16(kBf16, kTcRows, D, false, true);
     constexpr int KT = D / 16;  // MMAs of S = Q K^T (16 elements of d each)
@@ -184,6 +192,9 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     auto vfree = [&](int st) { return bar(6 + st); };
     auto pfull = [&](int b) { return bar(8 + b); };
     const uint32_t qfull = bar(10), mma_drain = bar(11);
+    // FP8 pools: the codes of K / V stage st landed (before widening)
+    auto kland = [&](int st) { return bar(12 + st); };
+    auto vland = [&](int st) { return bar(14 + st); };
     auto kbase = [&](int st) { return sbase + st * L::kStageBytes; };
     // operand descriptors of stage 0 and of the query tile; other stages and
     // k-steps add their byte offset / 16 to the start-address field
@@ -202,6 +213,8 @@ __global__ void __launch_bounds__(kTcThreads, 2)
             mbar_init(sfull(st), 1);
             mbar_init(vfree(st), 1);
             mbar_init(pfull(st), kRowWarps);
+            mbar_init(kland(st), 1);
+            mbar_init(vland(st), 1);
         }
         mbar_init(qfull, kRowWarps);
         mbar_init(mma_drain, 1);
@@ -379,6 +392,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         // a unit's query rows -> shared memory (K-major, 128-byte swizzle;
         // zeros past the tile), announced to the MMA warp.  Called once every
         // S of the unit before has finished (they read the query tile).
+        bool q_over = false;  // FP8 pools: a bf16 query element past the fp16 range
         auto write_q = [&](const Unit &w, const Row &r) {
             if (w.n <= 0)
                 return;
@@ -386,7 +400,18 @@ __global__ void __launch_bounds__(kTcThreads, 2)
                                                                (r.qoff < 0 ? 0 : r.qoff));
 #pragma unroll
             for (int c = 0; c < D / 8; ++c) {
-                const uint4 v = r.qoff >= 0 ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
+                uint4 v = r.qoff >= 0 ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
+                if constexpr (kFp8 && std::is_same<T, __nv_bfloat16>::value) {
+                    // the fp16 operand: a bf16 element past the fp16 range is flagged
+                    uint32_t *wv = reinterpret_cast<uint32_t *>(&v);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const float lo = __uint_as_float(wv[k] << 16);
+                        const float hi = __uint_as_float(wv[k] & 0xffff0000u);
+                        q_over |= fmaxf(fabsf(lo), fabsf(hi)) > 65504.f;
+                        wv[k] = pack_f16x2(lo, hi);
+                    }
+                }
                 const uint32_t a = qbase + (c >> 3) * L::kQHalf + tid * 128 +
                                    (((c & 7) ^ (tid & 7)) << 4);
                 asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(v.x),
@@ -480,7 +505,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
                                      e0, e1);
                         const float p0 = exp2f(e0), p1 = exp2f(e1);
                         acc[i & 1] = fadd_f32x2(acc[i & 1], pack_f32x2(p0, p1));
-                        pw[i] = MmaOp<T>::pack(p0, p1);
+                        pw[i] = MmaOp<OT>::pack(p0, p1);
                     }
                     {
                         float a0, a1, b0, b1;
@@ -543,7 +568,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
             }
 
             // epilogue: this thread's row of O / l (TMEM loads are warp-wide)
-            const float inv = (w.n > 0 && l_run > 0.f) ? 1.f / l_run : 0.f;
+            const float inv = (w.n > 0 && l_run > 0.f) ? p.out_scale / l_run : 0.f;
             if (p.prefix_mode && ooff >= 0) {
                 p.part_m[ooff] = m_ref * kLn2;
                 p.part_l[ooff] = l_run;
@@ -616,6 +641,8 @@ __global__ void __launch_bounds__(kTcThreads, 2)
             w = wn;
             rw = rn;
         }
+        if (kFp8 && __any_sync(kFull, q_over) && lane == 0)
+            flag_error(p.error_word, PA_DEVERR_QUERY_RANGE);
     } else if (warp == kKeyWarp || warp == kValueWarp) {
         // ===== fetch warps: keys (warp 4) and values (warp 5) into the 2-stage ring ====
         // Lane j < 2 * kTcSubs (j < kTcSubs for d = 64) owns the 16-token
@@ -624,7 +651,9 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         // its own 2 KB box.  K of tile g goes out once S of tile g - 2 is done,
         // V of tile g once the value product of tile g - 2 is.
         const bool values = warp == kValueWarp;
-        const int my_sb = lane / L::kHalves, my_hf = lane % L::kHalves;
+        // FP8: one box of 16 whole 128-byte rows per sub-tile
+        const int my_sb = kFp8 ? lane : lane / L::kHalves;
+        const int my_hf = kFp8 ? 0 : lane % L::kHalves;
         uint32_t g = 0;
         int last0 = -1, last1 = -1;  // last fill per stage
         bool ok = true;
@@ -648,17 +677,80 @@ __global__ void __launch_bounds__(kTcThreads, 2)
             auto issue = [&](int si, uint32_t st, int ent) {
                 const int t0 = w.kbeg + si * kTcTokens;
                 const int nsub = min(kTcSubs, (w.kend - t0 + kTileTokens - 1) / kTileTokens);
-                const uint32_t fb = values ? vfull(st) : kfull(st);
-                if (lane == 0)
-                    mbar_arrive_expect_tx(fb, (uint32_t)(nsub * L::kHalves * 2048));
-                __syncwarp();
-                if (my_sb < nsub) {
-                    const int row = (t0 + my_sb * kTileTokens) & (p.block_size - 1);
-                    tma_load_4d(kbase(st) + (values ? L::kKVBytes : 0) + my_hf * L::kKVHalf +
-                                    my_sb * 2048,
-                                values ? &tmap_v : &tmap_k, fb, my_hf * 64, w.kh, row, ent);
+                if constexpr (kFp8) {
+                    // the codes land in the stage's upper half (d-half 1's rows)
+                    const uint32_t fb = values ? vland(st) : kland(st);
+                    if (lane == 0)
+                        mbar_arrive_expect_tx(fb, (uint32_t)(nsub * 2048));
+                    __syncwarp();
+                    if (my_sb < nsub) {
+                        const int row = (t0 + my_sb * kTileTokens) & (p.block_size - 1);
+                        tma_load_4d(kbase(st) + (values ? L::kKVBytes : 0) + L::kKVHalf +
+                                        my_sb * 2048,
+                                    values ? &tmap_v : &tmap_k, fb, 0, w.kh, row, ent);
+                    }
+                } else {
+                    const uint32_t fb = values ? vfull(st) : kfull(st);
+                    if (lane == 0)
+                        mbar_arrive_expect_tx(fb, (uint32_t)(nsub * L::kHalves * 2048));
+                    __syncwarp();
+                    if (my_sb < nsub) {
+                        const int row = (t0 + my_sb * kTileTokens) & (p.block_size - 1);
+                        tma_load_4d(kbase(st) + (values ? L::kKVBytes : 0) + my_hf * L::kKVHalf +
+                                        my_sb * 2048,
+                                    values ? &tmap_v : &tmap_k, fb, my_hf * 64, w.kh, row, ent);
+                    }
                 }
+                return nsub;
             };
+            // FP8: widen the tile's landed codes in place -- row r's 128 codes
+            // (128-byte swizzled row r of the upper half) become fp16 row r of
+            // d-half 0 (d 0..63) and of d-half 1 (d 64..127, over the codes'
+            // own row: each lane reads its whole row before writing it) --
+            // then hand the stage to the tensor-core warp.
+            auto widen = [&](uint32_t gg, int nsub) -> bool {
+                const uint32_t st = gg & 1;
+                if (!wait(values ? vland(st) : kland(st), (gg >> 1) & 1))
+                    return false;
+                const uint32_t base = kbase(st) + (values ? L::kKVBytes : 0);
+                for (int r = lane; r < nsub * kTileTokens; r += 32) {
+                    uint4 src[8];
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        const uint32_t a = base + L::kKVHalf + r * 128 + ((c ^ (r & 7)) << 4);
+                        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                                     : "=r"(src[c].x), "=r"(src[c].y), "=r"(src[c].z),
+                                       "=r"(src[c].w)
+                                     : "r"(a)
+                                     : "memory");
+                    }
+#pragma unroll
+                    for (int hf = 0; hf < 2; ++hf)
+#pragma unroll
+                        for (int c = 0; c < 8; ++c) {
+                            // fp16 chunk c of d-half hf = codes 64hf + 8c .. + 7
+                            const uint4 sc = src[4 * hf + (c >> 1)];
+                            const uint32_t lo = (c & 1) ? sc.z : sc.x;
+                            const uint32_t hi = (c & 1) ? sc.w : sc.y;
+                            const uint32_t a = base + hf * L::kKVHalf + r * 128 +
+                                               ((c ^ (r & 7)) << 4);
+                            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a),
+                                         "r"(e4m3x2_to_f16x2((uint16_t)(lo & 0xffffu))),
+                                         "r"(e4m3x2_to_f16x2((uint16_t)(lo >> 16))),
+                                         "r"(e4m3x2_to_f16x2((uint16_t)(hi & 0xffffu))),
+                                         "r"(e4m3x2_to_f16x2((uint16_t)(hi >> 16)))
+                                         : "memory");
+                        }
+                }
+                fence_proxy_async_smem();  // the widened tile, for the tensor cores
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(values ? vfull(st) : kfull(st));
+                return true;
+            };
+            // FP8: a tile is widened after the next one has been issued, so
+            // that one's fill is in flight meanwhile
+            int pend = -1, pend_nsub = 0;
             int ent_next = w.n > 0 ? lookup(0) : 0;
             for (int si = 0; si < w.n; ++si) {
                 const uint32_t gg = g + si, st = gg & 1;
@@ -676,16 +768,32 @@ __global__ void __launch_bounds__(kTcThreads, 2)
                 // never issued, so the wait for it runs out
                 if (p.withhold_fill != 0 && !values && gg == 0)
                     continue;
-                issue(si, st, ent);
+                const int nsub = issue(si, st, ent);
                 (st ? last1 : last0) = (int)gg;
+                if constexpr (kFp8) {
+                    if (pend >= 0) {
+                        ok = widen(g + pend, pend_nsub);
+                        if (!ok)
+                            break;
+                    }
+                    pend = si;
+                    pend_nsub = nsub;
+                }
+            }
+            if constexpr (kFp8) {
+                if (ok && pend >= 0)
+                    ok = widen(g + pend, pend_nsub);
             }
             g += w.n;
         }
-        // fills still landing (only after an abort: the MMA warp waited the rest)
+        // fills still landing (only after an abort: the MMA warp -- or, for
+        // FP8 pools, the widening -- waited the rest)
+        const uint32_t landed0 = kFp8 ? (values ? vland(0) : kland(0)) : (values ? vfull(0) : kfull(0));
+        const uint32_t landed1 = kFp8 ? (values ? vland(1) : kland(1)) : (values ? vfull(1) : kfull(1));
         if (last0 >= 0)
-            mbar_wait_bounded(values ? vfull(0) : kfull(0), (last0 >> 1) & 1, kDrainWaitNs);
+            mbar_wait_bounded(landed0, (last0 >> 1) & 1, kDrainWaitNs);
         if (last1 >= 0)
-            mbar_wait_bounded(values ? vfull(1) : kfull(1), (last1 >> 1) & 1, kDrainWaitNs);
+            mbar_wait_bounded(landed1, (last1 >> 1) & 1, kDrainWaitNs);
     } else if (warp == kMmaWarp) {
         // ===== tensor-core warp: S = Q K^T and O += P V, one elected lane issues ========
         uint32_t g = 0, nq = 0;
@@ -780,12 +888,12 @@ __global__ void __launch_bounds__(kTcThreads, 2)
 
 // ---- host side -------------------------------------------------------------------
 
-template <typename T, int D>
+template <typename T, int D, bool kFp8>
 static pa_status launch_mq(const MqParams &prm, const CUtensorMap &mk, const CUtensorMap &mv,
                            cudaStream_t stream, long long max_units)
 {
     using L = TcLayout<D>;
-    auto kernel = paged_mq_kernel<T, D>;
+    auto kernel = paged_mq_kernel<T, D, kFp8>;
     static KernelSetting setting[kMaxDevices];
     static std::mutex mu;
     const size_t smem = L::bytes(prm.num_segments);
@@ -848,43 +956,49 @@ static pa_status launch_mq(const MqParams &prm, const CUtensorMap &mk, const CUt
                       mv);
 }
 
-static pa_status dispatch_mq(const MqParams &prm, pa_dtype dtype, const void *key_cache,
-                             const void *value_cache, int head_dim, cudaStream_t stream,
-                             long long max_units)
+// pool_dtype PA_FP8_E4M3: e4m3 pools (head_dim 128), query and output of
+// query_dtype; otherwise 16-bit pools and query of pool_dtype.
+static pa_status dispatch_mq(const MqParams &prm, pa_dtype pool_dtype, pa_dtype query_dtype,
+                             const void *key_cache, const void *value_cache, int head_dim,
+                             cudaStream_t stream, long long max_units)
 {
     CUtensorMap mk, mv;
-    if (!encode_pool_map(&mk, key_cache, dtype, prm.num_blocks, prm.block_size,
+    if (!encode_pool_map(&mk, key_cache, pool_dtype, prm.num_blocks, prm.block_size,
                          prm.num_kv_heads, head_dim) ||
-        !encode_pool_map(&mv, value_cache, dtype, prm.num_blocks, prm.block_size,
+        !encode_pool_map(&mv, value_cache, pool_dtype, prm.num_blocks, prm.block_size,
                          prm.num_kv_heads, head_dim))
         return PA_ERR_CUDA;
     using B16 = __nv_bfloat16;
+    if (pool_dtype == PA_FP8_E4M3)
+        return query_dtype == PA_BF16 ? launch_mq<B16, 128, true>(prm, mk, mv, stream, max_units)
+                                      : launch_mq<__half, 128, true>(prm, mk, mv, stream, max_units);
     if (head_dim == 128)
-        return dtype == PA_BF16 ? launch_mq<B16, 128>(prm, mk, mv, stream, max_units)
-                                : launch_mq<__half, 128>(prm, mk, mv, stream, max_units);
-    return dtype == PA_BF16 ? launch_mq<B16, 64>(prm, mk, mv, stream, max_units)
-                            : launch_mq<__half, 64>(prm, mk, mv, stream, max_units);
+        return pool_dtype == PA_BF16 ? launch_mq<B16, 128, false>(prm, mk, mv, stream, max_units)
+                                     : launch_mq<__half, 128, false>(prm, mk, mv, stream, max_units);
+    return pool_dtype == PA_BF16 ? launch_mq<B16, 64, false>(prm, mk, mv, stream, max_units)
+                                 : launch_mq<__half, 64, false>(prm, mk, mv, stream, max_units);
 }
 
-pa_status launch_prefix_pass(const MqParams &prm, pa_dtype dtype, const void *key_cache,
-                             const void *value_cache, int head_dim, cudaStream_t stream,
-                             long long max_units)
+pa_status launch_prefix_pass(const MqParams &prm, pa_dtype dtype, pa_dtype query_dtype,
+                             const void *key_cache, const void *value_cache, int head_dim,
+                             cudaStream_t stream, long long max_units)
 {
-    return dispatch_mq(prm, dtype, key_cache, value_cache, head_dim, stream, max_units);
+    return dispatch_mq(prm, dtype, query_dtype, key_cache, value_cache, head_dim, stream,
+                       max_units);
 }
 
 }  // namespace pa
 
 using namespace pa;
 
-extern "C" pa_status pa_prefill_attention(void *out, const void *query, const void *key_cache,
-                                          const void *value_cache, const int32_t *block_tables,
-                                          int max_blocks_per_seq, const int32_t *query_start,
-                                          const int32_t *context_lens, int max_context_len,
-                                          int num_seqs, int num_tokens, int num_heads,
-                                          int num_kv_heads, int head_dim, int block_size,
-                                          int num_blocks, float scale, pa_dtype dtype,
-                                          int32_t *error_word, void *stream)
+static pa_status run_prefill(void *out, const void *query, const void *key_cache,
+                             const void *value_cache, const int32_t *block_tables,
+                             int max_blocks_per_seq, const int32_t *query_start,
+                             const int32_t *context_lens, int max_context_len, int num_seqs,
+                             int num_tokens, int num_heads, int num_kv_heads, int head_dim,
+                             int block_size, int num_blocks, float scale, bool fp8,
+                             float k_scale, float v_scale, pa_dtype dtype,
+                             int32_t *error_word, void *stream)
 {
     if (num_seqs < 0 || num_tokens < 0 || num_heads <= 0 || num_kv_heads <= 0 ||
         head_dim <= 0 || block_size <= 0 || num_blocks <= 0 || max_blocks_per_seq <= 0 ||
@@ -892,7 +1006,10 @@ extern "C" pa_status pa_prefill_attention(void *out, const void *query, const vo
         num_heads % num_kv_heads != 0)
         return PA_ERR_INVALID_ARG;
     if (dtype != PA_F16 && dtype != PA_BF16)
-        return dtype == PA_FP8_E4M3 ? PA_ERR_UNSUPPORTED : PA_ERR_INVALID_ARG;
+        return dtype == PA_FP8_E4M3 && !fp8 ? PA_ERR_UNSUPPORTED : PA_ERR_INVALID_ARG;
+    if (fp8 && !(std::isfinite(k_scale) && std::isfinite(v_scale) && k_scale > 0.f &&
+                 v_scale > 0.f))
+        return PA_ERR_INVALID_ARG;
     if (num_seqs == 0 || num_tokens == 0)
         return PA_OK;
     if (!out || !query || !key_cache || !value_cache || !block_tables || !query_start ||
@@ -902,9 +1019,9 @@ extern "C" pa_status pa_prefill_attention(void *out, const void *query, const vo
         !aligned16(value_cache))
         return PA_ERR_INVALID_ARG;
     const int group = num_heads / num_kv_heads;
-    if ((head_dim != 64 && head_dim != 128) || block_size < kTileTokens || block_size > 256 ||
-        (block_size & (block_size - 1)) != 0 || group > 16 ||
-        (long long)num_blocks * block_size >= (1ll << 31) ||
+    if ((head_dim != 64 && head_dim != 128) || (fp8 && head_dim != 128) ||
+        block_size < kTileTokens || block_size > 256 || (block_size & (block_size - 1)) != 0 ||
+        group > 16 || (long long)num_blocks * block_size >= (1ll << 31) ||
         (long long)max_blocks_per_seq * block_size >= (1ll << 31))
         return PA_ERR_UNSUPPORTED;
 
@@ -930,10 +1047,39 @@ extern "C" pa_status pa_prefill_attention(void *out, const void *query, const vo
     prm.max_context_len = max_context_len;
     prm.max_parts = 0;
     prm.part_tokens = 0;
-    prm.scale_log2 = scale * kLog2e;
+    prm.scale_log2 = scale * (fp8 ? k_scale : 1.f) * kLog2e;
+    prm.out_scale = fp8 ? v_scale : 1.f;
     // row tiles: at most one partial tile per sequence beyond the full ones
     const long long max_units =
         ((long long)num_tokens * group / kTcRows + num_seqs) * num_kv_heads;
-    return dispatch_mq(prm, dtype, key_cache, value_cache, head_dim, as_stream(stream),
-                       max_units);
+    return dispatch_mq(prm, fp8 ? PA_FP8_E4M3 : dtype, dtype, key_cache, value_cache, head_dim,
+                       as_stream(stream), max_units);
+}
+
+extern "C" pa_status pa_prefill_attention(void *out, const void *query, const void *key_cache,
+                                          const void *value_cache, const int32_t *block_tables,
+                                          int max_blocks_per_seq, const int32_t *query_start,
+                                          const int32_t *context_lens, int max_context_len,
+                                          int num_seqs, int num_tokens, int num_heads,
+                                          int num_kv_heads, int head_dim, int block_size,
+                                          int num_blocks, float scale, pa_dtype dtype,
+                                          int32_t *error_word, void *stream)
+{
+    return run_prefill(out, query, key_cache, value_cache, block_tables, max_blocks_per_seq,
+                       query_start, context_lens, max_context_len, num_seqs, num_tokens,
+                       num_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, false,
+                       1.f, 1.f, dtype, error_word, stream);
+}
+
+extern "C" pa_status pa_prefill_attention_fp8(
+    void *out, const void *query, const void *key_cache, const void *value_cache,
+    const int32_t *block_tables, int max_blocks_per_seq, const int32_t *query_start,
+    const int32_t *context_lens, int max_context_len, int num_seqs, int num_tokens,
+    int num_heads, int num_kv_heads, int head_dim, int block_size, int num_blocks, float scale,
+    float k_scale, float v_scale, pa_dtype dtype, int32_t *error_word, void *stream)
+{
+    return run_prefill(out, query, key_cache, value_cache, block_tables, max_blocks_per_seq,
+                       query_start, context_lens, max_context_len, num_seqs, num_tokens,
+                       num_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, true,
+                       k_scale, v_scale, dtype, error_word, stream);
 }

@@ -32,13 +32,15 @@ struct MqParams {
     int max_blocks_per_seq, num_blocks, block_size, block_shift, max_context_len;
     int max_parts;     // partials per (sequence, head) in the workspace
     int part_tokens;   // prefix pass: tokens per prefix partition (partial j)
-    float scale_log2;
+    float scale_log2;  // scale * log2(e) (times the K scale for FP8 pools)
+    float out_scale;   // applied to the output / partials (the V scale for FP8 pools)
 };
 
-// Queue the shared-prefix pass (16-bit pools) on `stream` as a programmatic
-// dependent of the kernel before it.
-pa_status launch_prefix_pass(const MqParams &prm, pa_dtype dtype, const void *key_cache,
-                             const void *value_cache, int head_dim, cudaStream_t stream,
-                             long long max_units);
+// Queue the shared-prefix pass on `stream` as a programmatic dependent of the
+// kernel before it (dtype PA_FP8_E4M3: FP8 pools, query and output of
+// query_dtype; else 16-bit pools of dtype).
+pa_status launch_prefix_pass(const MqParams &prm, pa_dtype dtype, pa_dtype query_dtype,
+                             const void *key_cache, const void *value_cache, int head_dim,
+                             cudaStream_t stream, long long max_units);
 
 }  // namespace pa

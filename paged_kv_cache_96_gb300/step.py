@@ -155,7 +155,8 @@ class DecodeStep:
             B.pa_prefill_attention(self.out, self.query, self.key_cache, self.value_cache,
                                    self.step_block_tables, self.query_start,
                                    self.context_lens, self.max_context_len, w.scale,
-                                   error_word=self.error_word, stream=stream)
+                                   error_word=self.error_word, stream=stream,
+                                   k_scale=self.kv_scale, v_scale=self.kv_scale)
             return
         P = self.partition_size if partition_size is None else partition_size
         if self.cascade:
@@ -167,7 +168,8 @@ class DecodeStep:
                                           self.value_cache, self.step_block_tables,
                                           self.context_lens, self.max_context_len, w.scale,
                                           self.plan, self.num_groups, self.num_members, P, ws,
-                                          error_word=self.error_word, stream=stream)
+                                          error_word=self.error_word, stream=stream,
+                                          k_scale=self.kv_scale, v_scale=self.kv_scale)
             return
         ws = self.workspace
         if P != self.partition_size:
@@ -208,7 +210,8 @@ class DecodeStep:
                 self.out, self.query, self.key_cache, self.value_cache, self.new_key,
                 self.new_value, self.step_block_tables, self.context_lens, self.max_context_len,
                 w.scale, self.plan, self.num_groups, self.num_members, P, ws,
-                slot_mapping=self.slots, error_word=self.error_word, stream=stream)
+                slot_mapping=self.slots, error_word=self.error_word, stream=stream,
+                k_scale=self.kv_scale, v_scale=self.kv_scale)
             return
         if P != self.partition_size:
             ws = B.alloc_workspace(w.S, w.H, w.Hkv, w.D, self.max_context_len, P,

@@ -456,3 +456,5 @@ def small_variant(name: str, seed: int = 0) -> WorkloadSpec:
 
 CONFIGS["gqa70b-fp8"] = fp8_variant(CONFIGS["gqa70b"])
 CONFIGS["longctx-fp8"] = fp8_variant(CONFIGS["longctx"])
+CONFIGS["chunked-fp8"] = fp8_variant(CONFIGS["chunked"])
+CONFIGS["prefix-cascade-fp8"] = fp8_variant(CONFIGS["prefix-cascade"])

@@ -57,19 +57,25 @@ class OracleStep:
         sequence's table and the context ending at the row's position."""
         w = self.w
         if w.prefill:
+            if w.fp8:
+                def prefill(q, bt, qs, cl):
+                    return oracle.prefill_attention_fp8(q, self.key_cache, self.value_cache,
+                                                        bt, qs, cl, w.scale, odt(w),
+                                                        w.spec.kv_scale, w.spec.kv_scale)
+            else:
+                def prefill(q, bt, qs, cl):
+                    return oracle.prefill_attention(q, self.key_cache, self.value_cache,
+                                                    bt, qs, cl, w.scale, odt(w))
             if rows is None:
-                return oracle.prefill_attention(w.query, self.key_cache, self.value_cache,
-                                                w.step_block_tables, w.query_start,
-                                                w.context_lens, w.scale, odt(w))
+                return prefill(w.query, w.step_block_tables, w.query_start, w.context_lens)
             rows = np.asarray(rows, dtype=np.int64)
             seq_of = np.searchsorted(w.query_start, rows, side="right") - 1
             q_len = w.query_start[seq_of + 1] - w.query_start[seq_of]
             pos = w.context_lens[seq_of] - q_len + (rows - w.query_start[seq_of])
             qs = np.arange(rows.shape[0] + 1, dtype=np.int32)
-            return oracle.prefill_attention(
-                np.ascontiguousarray(w.query[rows]), self.key_cache, self.value_cache,
-                np.ascontiguousarray(w.step_block_tables[seq_of]), qs,
-                (pos + 1).astype(np.int32), w.scale, odt(w))
+            return prefill(np.ascontiguousarray(w.query[rows]),
+                           np.ascontiguousarray(w.step_block_tables[seq_of]), qs,
+                           (pos + 1).astype(np.int32))
         if w.fp8:
             return oracle.paged_attention_fp8(w.query, self.key_cache, self.value_cache,
                                               w.step_block_tables, w.context_lens, w.scale,

@@ -165,6 +165,52 @@ def test_cascade_append_argument_checks(B):
     assert f(*ok[:19], 1, 1, *ok[21:]) == B.PA_ERR_INVALID_ARG        # group of one
     assert f(*ok[:18], None, *ok[19:]) == B.PA_ERR_WORKSPACE          # no workspace first
     assert f(*ok[:11], 0, *ok[12:]) == B.PA_OK                        # no sequences
+    # FP8 pools: k_scale, v_scale after scale
+    f8 = L.pa_decode_attention_cascade_append_fp8
+    ok8 = ok[:18] + (0.5, 0.5) + ok[18:]
+    assert f8(*ok8[:11], 0, *ok8[12:]) == B.PA_OK                      # no sequences
+    assert f8(*ok8[:18], 0.0, 0.5, *ok8[20:]) == B.PA_ERR_INVALID_ARG  # zero K scale
+    assert f8(*ok8[:18], 0.5, float("inf"), *ok8[20:]) == B.PA_ERR_INVALID_ARG
+    assert f8(*ok8[:26], 2, *ok8[27:]) == B.PA_ERR_INVALID_ARG         # query not 16-bit
+    assert f8(*ok8[:5], None, *ok8[6:]) == B.PA_ERR_INVALID_ARG        # no new values
+    assert f8(*ok8[:21], 1, 1, *ok8[23:]) == B.PA_ERR_INVALID_ARG      # group of one
+    assert f8(*ok8[:20], None, *ok8[21:]) == B.PA_ERR_WORKSPACE        # no workspace
+    ws = (ctypes.c_uint8 * (1 << 22))()
+    wsp = (ctypes.addressof(ws) + 255) // 256 * 256
+    okw = ok8[:24] + (wsp, (1 << 22) - 256) + ok8[26:]
+    assert f8(*okw[:14], 64, *okw[15:]) == B.PA_ERR_UNSUPPORTED        # FP8 prefix pass: d 128
+    g8 = L.pa_decode_attention_cascade_fp8
+    # (out, query, kc, vc, tables, mb, ctx, maxctx, S, H, Hkv, d, bs, N, scale, k_scale,
+    #  v_scale, plan, groups, members, P, ws, ws_bytes, dtype, err, stream)
+    okc = (FAKE, FAKE, FAKE, FAKE, FAKE, 4, FAKE, 64, 2, 8, 2, 128, 16, 8, 0.1, 0.5, 0.5,
+           FAKE, 1, 2, 16, None, 0, 1, None, None)
+    assert g8(*okc[:8], 0, *okc[9:]) == B.PA_OK
+    assert g8(*okc[:15], -1.0, *okc[16:]) == B.PA_ERR_INVALID_ARG
+    assert g8(*okc[:21], None, *okc[22:]) == B.PA_ERR_WORKSPACE
+    assert g8(*okc[:11], 96, *okc[12:]) == B.PA_ERR_UNSUPPORTED
+
+
+def test_prefill_argument_checks(B):
+    """pa_prefill_attention(_fp8): sizes, scales and types, before any launch."""
+    L = B.lib()
+    f = L.pa_prefill_attention
+    f8 = L.pa_prefill_attention_fp8
+    # (out, query, kc, vc, tables, mb, query_start, ctx, maxctx, S, T, H, Hkv, d, bs, N,
+    #  scale, dtype, err, stream)
+    ok = (FAKE, FAKE, FAKE, FAKE, FAKE, 4, FAKE, FAKE, 64, 2, 10, 8, 2, 128, 16, 8, 0.1, 1,
+          None, None)
+    assert f(*ok[:10], 0, *ok[11:]) == B.PA_OK                        # no tokens
+    assert f(*ok[:16], 0.0, *ok[17:]) == B.PA_ERR_INVALID_ARG         # scale 0
+    assert f(*ok[:17], 2, *ok[18:]) == B.PA_ERR_UNSUPPORTED           # FP8 pools: _fp8
+    assert f(*ok[:13], 96, *ok[14:]) == B.PA_ERR_UNSUPPORTED          # head_dim 96
+    assert f(*ok[:12], 3, *ok[13:]) == B.PA_ERR_INVALID_ARG           # 8 heads over 3
+    ok8 = ok[:17] + (0.5, 0.5) + ok[17:]
+    assert f8(*ok8[:10], 0, *ok8[11:]) == B.PA_OK
+    assert f8(*ok8[:17], 0.0, 0.5, *ok8[19:]) == B.PA_ERR_INVALID_ARG  # zero K scale
+    assert f8(*ok8[:17], 0.5, float("nan"), *ok8[19:]) == B.PA_ERR_INVALID_ARG
+    assert f8(*ok8[:19], 2, *ok8[20:]) == B.PA_ERR_INVALID_ARG         # query not 16-bit
+    assert f8(*ok8[:13], 64, *ok8[14:]) == B.PA_ERR_UNSUPPORTED        # FP8: d 128 only
+    assert f8(*ok8[:2], FAKE_ODD, *ok8[3:]) == B.PA_ERR_INVALID_ARG    # unaligned pool
 
 
 def test_workspace_layout_sizes(B):
@@ -190,7 +236,9 @@ def test_workspace_layout_sizes(B):
 @pytest.mark.parametrize("name,fused", [("tiny", True), ("mha7b", True), ("gqa70b", True),
                                         ("longctx", True), ("prefix", True),
                                         ("prefix-cascade", True), ("gqa70b-fp8", True),
-                                        ("chunked", False), ("mixed", False)])
+                                        ("prefix-cascade-fp8", True),
+                                        ("chunked", False), ("chunked-fp8", False),
+                                        ("mixed", False)])
 def test_step_takes_the_fused_append(lib, name, fused):
     """Host logic of the step: a decode step whose new tokens are one per
     sequence at its last position (in the same block before and after

@@ -22,8 +22,9 @@ both sides of partition edges, the middle, the last cached row and the
 appended position context - 1; for prefix-aware decode also both sides of
 the shared-prefix end and inside the shared blocks; for chunked prefill at
 64-token tile edges, before and inside the chunk.  Each case runs the
-decode step (fused append and separate write; single pass and split), the
-FP8 pools, prefix-aware decode and chunked prefill, and compares every
+decode step (fused append and separate write; single pass and split),
+prefix-aware decode and chunked prefill, each over 16-bit and FP8 pools,
+and compares every
 output element with the oracle at the contract tolerance; dominant needles
 are also checked against their value row directly.
 """
@@ -76,6 +77,8 @@ SPECS = {
 }
 SPECS["gqa-fp8"] = W.fp8_variant(SPECS["gqa"])
 SPECS["d64-fp8"] = W.fp8_variant(SPECS["d64"])
+SPECS["cascade-fp8"] = W.fp8_variant(SPECS["cascade"])
+SPECS["prefill-fp8"] = W.fp8_variant(SPECS["prefill"])
 
 DOMINANT_SCORE = 20.0
 VROW = np.array([3.0, 3.25, 3.5, 3.75])   # exact in fp16 and bf16
@@ -249,14 +252,15 @@ def test_decode_needles(S, name, P, how):
             _check_dominant(w, got, want, s, 0)
 
 
+@pytest.mark.parametrize("name", ["cascade", "cascade-fp8"])
 @pytest.mark.parametrize("how", ["append", "separate"])
-def test_cascade_needles(S, how):
+def test_cascade_needles(S, how, name):
     """Prefix-aware decode.  KV head 0: a dominant needle in each sequence's
     own tokens; head 1: one dominant needle inside the shared prefix, every
     sequence's group query set to the same row; head 2: balanced needles
     (keys of head 2 zero everywhere, the shared prefix included); head 3:
     untouched."""
-    spec = SPECS["cascade"]
+    spec = SPECS[name]
     pre, P = spec.shared_prefix_tokens, spec.partition_size
     ctx = np.asarray(spec.context_lens(None))
     own = [positions(int(c), spec.block_size, P, pre, own_only=True) for c in ctx]
@@ -276,18 +280,19 @@ def test_cascade_needles(S, how):
         plant_dominant(w, 0, 1, ps, share=list(range(w.S)))
         got = _run(S, w, P, how)
         want = OracleStep(w).attention()
-        assert_attention_close(got, want, f"cascade {how} round {r} {plan} shared {ps}")
+        assert_attention_close(got, want, f"{name} {how} round {r} {plan} shared {ps}")
         for s, _, _ in plan:
             _check_dominant(w, got, want, s, 0)
             _check_dominant(w, got, want, s, 1)
 
 
-def test_prefill_needles(S):
+@pytest.mark.parametrize("name", ["prefill", "prefill-fp8"])
+def test_prefill_needles(S, name):
     """Chunked prefill: a dominant needle per (sequence, KV head) -- before
     the chunk, at its first row, at 64-token tile edges, inside it -- with
     every chunk row's group query set to one row; rows at or past the needle
     give its value row, rows before it must not see it."""
-    spec = SPECS["prefill"]
+    spec = SPECS[name]
     ctx = np.asarray(spec.context_lens(None))
     ql = np.asarray(spec.query_lens(None, ctx))
     lists = []
@@ -307,7 +312,7 @@ def test_prefill_needles(S):
             plan.append((s, p0, p1))
         got = _run(S, w, 0, "separate")
         want = OracleStep(w).attention()
-        assert_attention_close(got, want, f"prefill round {r} {plan}")
+        assert_attention_close(got, want, f"{name} round {r} {plan}")
         for s, p0, p1 in plan:
             c, q = int(w.context_lens[s]), int(ql[s])
             for kh, p in ((0, p0), (1, p1)):

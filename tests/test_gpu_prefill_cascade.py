@@ -41,7 +41,7 @@ def small():
 
 # ---- chunked prefill / mixed batch ------------------------------------------------
 
-@pytest.mark.parametrize("name", ["mixed", "chunked"])
+@pytest.mark.parametrize("name", ["mixed", "chunked", "chunked-fp8"])
 def test_prefill_step_matches_oracle(B, S, small, name):
     w, ref = small(name)
     st = S.DecodeStep(w)
@@ -78,8 +78,9 @@ def test_prompt_first_row_is_value_row(B, S, small):
             assert np.array_equal(out[r, h], w.new_value[r, h // G])
 
 
-def test_prefill_block_placement_invariance(B, S, small):
-    w, _ = small("chunked")
+@pytest.mark.parametrize("name", ["chunked", "chunked-fp8"])
+def test_prefill_block_placement_invariance(B, S, small, name):
+    w, _ = small(name)
     st = S.DecodeStep(w)
     a = st.run().clone()
     g = torch.Generator().manual_seed(5)
@@ -91,8 +92,48 @@ def test_prefill_block_placement_invariance(B, S, small):
     t2 = perm[st.step_block_tables.long()].to(torch.int32)
     b = torch.full_like(a, float("nan"))
     B.pa_prefill_attention(b, st.query, kc2, vc2, t2, st.query_start, st.context_lens,
-                           st.max_context_len, w.scale)
+                           st.max_context_len, w.scale, k_scale=st.kv_scale,
+                           v_scale=st.kv_scale)
     assert torch.equal(a, b)
+
+
+def test_prefill_fp8_query_beyond_fp16_is_flagged(B, S, small):
+    """The FP8 prefill rounds the query to fp16 for the tensor-core tiles: a
+    bf16 query element beyond the fp16 range is flagged, not silently
+    saturated."""
+    w, _ = small("chunked-fp8")
+    st = S.DecodeStep(w)
+    st.run()
+    torch.cuda.synchronize()
+    assert int(st.error_word.item()) == 0
+    assert st.query.dtype == torch.bfloat16
+    st.query[5, 3, 17] = 1.0e5
+    st.attention()
+    torch.cuda.synchronize()
+    assert int(st.error_word.item()) & B.DEVERR_QUERY_RANGE
+
+
+def test_prefill_fp8_scales_enter_as_stated(B, S, small):
+    """Doubling v_scale doubles every output (bit for bit: a power of two);
+    doubling k_scale equals doubling the softmax scale."""
+    w, _ = small("chunked-fp8")
+    st = S.DecodeStep(w)
+    st.run()
+    torch.cuda.synchronize()
+    args = (st.query, st.key_cache, st.value_cache, st.step_block_tables, st.query_start,
+            st.context_lens, st.max_context_len)
+    a = torch.empty_like(st.out)
+    b = torch.empty_like(st.out)
+    c = torch.empty_like(st.out)
+    k, v = st.kv_scale, st.kv_scale
+    B.pa_prefill_attention(a, *args, w.scale, k_scale=k, v_scale=v)
+    B.pa_prefill_attention(b, *args, w.scale, k_scale=k, v_scale=2 * v)
+    B.pa_prefill_attention(c, *args, 2 * w.scale, k_scale=k, v_scale=v)
+    d = torch.empty_like(st.out)
+    B.pa_prefill_attention(d, *args, w.scale, k_scale=2 * k, v_scale=v)
+    torch.cuda.synchronize()
+    assert torch.equal(b, 2 * a)
+    assert torch.equal(c, d)
 
 
 def test_prefill_index_errors_are_flagged(B, S, small):
@@ -137,17 +178,50 @@ def test_prefill_host_errors(B, S, small):
 
 # ---- prefix-aware (cascade) decode -------------------------------------------------
 
+@pytest.mark.parametrize("name", ["prefix-cascade", "prefix-cascade-fp8"])
 @pytest.mark.parametrize("P", [0, 48, 128])
-def test_cascade_step_matches_oracle(B, S, small, P):
-    w, ref = small("prefix-cascade")
+def test_cascade_step_matches_oracle(B, S, small, P, name):
+    w, ref = small(name)
     st = S.DecodeStep(w, partition_size=P)
     assert st.num_groups >= 1
+    assert st.fused_append
     out = st.run()
+    torch.cuda.synchronize()
+    assert int(st.error_word.item()) == 0
+    assert np.array_equal(st.slots.cpu().numpy().astype(np.int64), ref.new_slots)
+    assert np.array_equal(S.to_bits(st.key_cache), ref.key_cache)
+    assert np.array_equal(S.to_bits(st.value_cache), ref.value_cache)
+    assert_attention_close(S.to_float(out), ref.attention(), f"{name} P={P}")
+
+
+@pytest.mark.parametrize("name", ["prefix-cascade", "prefix-cascade-fp8"])
+def test_cascade_separate_write_matches_oracle(B, S, small, name):
+    """The step with its writes as their own launch and the prefix-aware
+    decode without append: same pools, same attention."""
+    w, ref = small(name)
+    st = S.DecodeStep(w)
+    st.slot_mapping_and_cache()
+    st.copy_blocks()
+    st.attention()
     torch.cuda.synchronize()
     assert int(st.error_word.item()) == 0
     assert np.array_equal(S.to_bits(st.key_cache), ref.key_cache)
     assert np.array_equal(S.to_bits(st.value_cache), ref.value_cache)
-    assert_attention_close(S.to_float(out), ref.attention(), f"cascade P={P}")
+    assert_attention_close(S.to_float(st.out), ref.attention(), f"{name} separate")
+
+
+def test_cascade_fp8_query_beyond_fp16_is_flagged(B, S, small):
+    w, _ = small("prefix-cascade-fp8")
+    st = S.DecodeStep(w)
+    st.run()
+    torch.cuda.synchronize()
+    assert int(st.error_word.item()) == 0
+    members = st.plan.cpu().numpy()[w.S + 2 * st.num_groups + 1:]
+    st.query[int(members[0]), 1, 5] = 1.0e5
+    st.slot_mapping_and_cache()
+    st.attention()
+    torch.cuda.synchronize()
+    assert int(st.error_word.item()) & B.DEVERR_QUERY_RANGE
 
 
 def test_cascade_prefix_partial_matches_oracle(B, S, small):

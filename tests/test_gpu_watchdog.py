@@ -30,7 +30,10 @@ CASES = [
     ("gqa70b-fp8", 128, "append"),
     ("prefix-cascade", 64, "attention"),
     ("prefix-cascade", 64, "append"),
+    ("prefix-cascade-fp8", 64, "attention"),
+    ("prefix-cascade-fp8", 64, "append"),
     ("chunked", 0, "prefill"),
+    ("chunked-fp8", 0, "prefill"),
     ("mixed", 0, "prefill"),
 ]
 
