@@ -227,6 +227,16 @@ def test_workspace_layout_sizes(B):
     assert counters2 > 4 << 18
     assert L.pa_decode_workspace_bytes(S2, H, Hkv, D, 3 * 512, 512) == \
         counters2 + 2 * a256(S2 * H * P2 * 4) + a256(S2 * H * P2 * D * 4)
+    # prefix-aware decode: the shared prefix and the own tokens each in
+    # partitions of P (P = 0: one of each), ceil(max_ctx / P) + 1 partials
+    def cascade(S_, mc, P_):
+        parts = (-(-mc // P_) if P_ > 0 and mc > 0 else 1) + 1
+        return a256(4 * max(1 << 18, S_ * Hkv)) + 2 * a256(S_ * H * parts * 4) + \
+            a256(S_ * H * parts * D * 4)
+    for S_, mc, P_ in ((256, 2048, 1024), (256, 2048, 0), (6, 328, 0), (6, 328, 64),
+                       (16, 32768, 512), (3, 100, 48), (1, 1, 0)):
+        assert L.pa_cascade_workspace_bytes(S_, H, Hkv, D, mc, P_) == cascade(S_, mc, P_), \
+            (S_, mc, P_)
     # everything fits one partition, or single pass: no workspace
     assert L.pa_decode_workspace_bytes(S, H, Hkv, D, 512, 512) == 0
     assert L.pa_decode_workspace_bytes(S, H, Hkv, D, 32768, 0) == 0

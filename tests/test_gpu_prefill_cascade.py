@@ -224,21 +224,28 @@ def test_cascade_fp8_query_beyond_fp16_is_flagged(B, S, small):
     assert int(st.error_word.item()) & B.DEVERR_QUERY_RANGE
 
 
-def test_cascade_prefix_partial_matches_oracle(B, S, small):
-    """Partial 0 of every grouped (sequence, head) is the attention over the
-    group's shared prefix: the oracle's first partition of that length."""
+@pytest.mark.parametrize("P", [0, 64])
+def test_cascade_prefix_partial_matches_oracle(B, S, small, P):
+    """The first partials of every grouped (sequence, head) are the attention
+    over the group's shared prefix [0, L), in partitions of P tokens (P = 0:
+    one): the oracle's partitions of that size over a context of L tokens."""
     w, ref = small("prefix-cascade")
-    st = S.DecodeStep(w, partition_size=0)
+    st = S.DecodeStep(w, partition_size=P)
     st.run()
     torch.cuda.synchronize()
+    assert int(st.error_word.item()) == 0
     plan = st.plan.cpu().numpy()
     Sn, H, D = w.S, w.H, w.D
     ng = st.num_groups
     gstart = plan[Sn:Sn + ng + 1]
     gprefix = plan[Sn + ng + 1:Sn + 2 * ng + 1]
     members = plan[Sn + 2 * ng + 1:]
-    parts = 2  # partition_size 0: the prefix's partial + one own partition
+    mc = st.max_context_len
+    split = P > 0 and mc > P
+    Q = P if split else (mc + 15) // 16 * 16  # tokens per prefix partition
+    parts = (-(-mc // P) if split else 1) + 1  # the workspace's partials per (sequence, head)
     ws = st.workspace
+    assert ws.numel() == B.pa_cascade_workspace_bytes(Sn, H, w.Hkv, D, mc, P)
 
     def a256(x):
         return (x + 255) // 256 * 256
@@ -256,12 +263,18 @@ def test_cascade_prefix_partial_matches_oracle(B, S, small):
     for g in range(ng):
         L = int(gprefix[g])
         mem = members[gstart[g]:gstart[g + 1]].tolist()
-        m_o, l_o, o_o = ref.partitions(L, 1, seqs=mem)
+        n = -(-L // Q)
+        ctx_l = np.full(Sn, L, dtype=np.int32)
+        m_o, l_o, o_o = oracle.partition_pass(w.query, ref.key_cache, ref.value_cache,
+                                              w.step_block_tables, ctx_l, w.scale,
+                                              oracle.BF16 if w.dtype == "bf16" else oracle.F16,
+                                              Q, n, seqs=mem)
         for s in mem:
-            lse_g = m_g[s, :, 0] + np.log(l_g[s, :, 0])
-            lse_o = m_o[s, :, 0] + np.log(l_o[s, :, 0])
-            assert np.allclose(lse_g, lse_o, atol=1e-3, rtol=1e-4), s
-            assert_attention_close(o_g[s, :, 0], o_o[s, :, 0], f"prefix partial s={s}")
+            for j in range(n):
+                lse_g = m_g[s, :, j] + np.log(l_g[s, :, j])
+                lse_o = m_o[s, :, j] + np.log(l_o[s, :, j])
+                assert np.allclose(lse_g, lse_o, atol=1e-3, rtol=1e-4), (s, j)
+                assert_attention_close(o_g[s, :, j], o_o[s, :, j], f"prefix partial s={s} j={j}")
 
 
 def test_cascade_without_groups_is_plain_decode(B, S, small):
