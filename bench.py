@@ -237,6 +237,7 @@ TRAFFIC_SUMMARIES = {
     "gqa70b": ("decode_gqa70b_ncu.md", DECODE_SOURCES),
     "gqa70b-fp8": ("decode_gqa70b_fp8_ncu.md", DECODE_SOURCES),
     "chunked": ("prefill_chunked_ncu.md", PREFILL_SOURCES),
+    "chunked-fp8": ("prefill_chunked_fp8_ncu.md", PREFILL_SOURCES),
 }
 
 
