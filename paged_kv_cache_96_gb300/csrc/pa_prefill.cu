@@ -208,7 +208,8 @@ __global__ void __launch_bounds__(kTcThreads, 2)
 
     if (tid == 0) {
         for (int st = 0; st < kTcStages; ++st) {
-            mbar_init(kfull(st), 1);
+            // FP8 pools: the 4 row warps widen the keys, the value warp the values
+            mbar_init(kfull(st), kFp8 ? kRowWarps : 1);
             mbar_init(vfull(st), 1);
             mbar_init(sfull(st), 1);
             mbar_init(vfree(st), 1);
@@ -423,12 +424,66 @@ __global__ void __launch_bounds__(kTcThreads, 2)
             if (lane == 0)
                 mbar_arrive(qfull);
         };
+        // FP8 pools: the row warps widen each key tile in place once its codes
+        // have landed (see the fetch warps), two threads per 128-code row, and
+        // announce it on the stage's "keys full" barrier.  Tile gg + 1 is widened
+        // before the row warps wait for S of tile gg, so it is ready when the
+        // tensor-core warp moves on.
+        int ntiles_cta = 0;  // tiles of this CTA, over all its units
+        if constexpr (kFp8) {
+            for (int u = blockIdx.x; u < total_units; u += gridDim.x) {
+                Unit x;
+                decode(u, x);
+                ntiles_cta += x.n;
+            }
+        }
+        auto widen_k = [&](uint32_t gg) -> bool {
+            const uint32_t st = gg & 1;
+            if (!wait(kland(st), (gg >> 1) & 1))
+                return false;
+            const uint32_t base = kbase(st);
+            const int r = tid >> 1, hf = tid & 1;  // row, and the d-half this thread writes
+            uint4 src[4];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const int cc = 4 * hf + c;  // code chunk: codes 16cc .. 16cc + 15
+                const uint32_t a = base + L::kKVHalf + r * 128 + ((cc ^ (r & 7)) << 4);
+                asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                             : "=r"(src[c].x), "=r"(src[c].y), "=r"(src[c].z), "=r"(src[c].w)
+                             : "r"(a)
+                             : "memory");
+            }
+            __syncwarp();  // both halves of the row are read before d-half 1 overwrites it
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                // fp16 chunk c of d-half hf = codes 64hf + 8c .. + 7
+                const uint4 sc = src[c >> 1];
+                const uint32_t lo = (c & 1) ? sc.z : sc.x;
+                const uint32_t hi = (c & 1) ? sc.w : sc.y;
+                const uint32_t a = base + hf * L::kKVHalf + r * 128 + ((c ^ (r & 7)) << 4);
+                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a),
+                             "r"(e4m3x2_to_f16x2((uint16_t)(lo & 0xffffu))),
+                             "r"(e4m3x2_to_f16x2((uint16_t)(lo >> 16))),
+                             "r"(e4m3x2_to_f16x2((uint16_t)(hi & 0xffffu))),
+                             "r"(e4m3x2_to_f16x2((uint16_t)(hi >> 16)))
+                             : "memory");
+            }
+            fence_proxy_async_smem();  // the widened tile, for the tensor cores
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(kfull(st));
+            return true;
+        };
         Unit w;
         Row rw;
         if ((int)blockIdx.x < total_units) {
             decode(blockIdx.x, w);
             row_of(w, rw, true);
             write_q(w, rw);
+        }
+        if constexpr (kFp8) {
+            if (ntiles_cta > 0)
+                ok = widen_k(0);
         }
         for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x) {
             const long long ooff = rw.ooff;
@@ -447,6 +502,13 @@ __global__ void __launch_bounds__(kTcThreads, 2)
                 for (int si = 0; si < w.n; ++si) {
                     const uint32_t gg = g + si, b = gg & 1;
                     const int t0 = w.kbeg + si * kTcTokens;
+                    if constexpr (kFp8) {
+                        if ((int)gg + 1 < ntiles_cta) {
+                            ok = widen_k(gg + 1);
+                            if (!ok)
+                                break;
+                        }
+                    }
                     // 1. S of this tile
                     ok = wait(sfull(b), (gg >> 1) & 1);
                     if (!ok)
@@ -771,17 +833,19 @@ __global__ void __launch_bounds__(kTcThreads, 2)
                 const int nsub = issue(si, st, ent);
                 (st ? last1 : last0) = (int)gg;
                 if constexpr (kFp8) {
-                    if (pend >= 0) {
-                        ok = widen(g + pend, pend_nsub);
-                        if (!ok)
-                            break;
+                    if (values) {  // (the row warps widen the keys)
+                        if (pend >= 0) {
+                            ok = widen(g + pend, pend_nsub);
+                            if (!ok)
+                                break;
+                        }
+                        pend = si;
+                        pend_nsub = nsub;
                     }
-                    pend = si;
-                    pend_nsub = nsub;
                 }
             }
             if constexpr (kFp8) {
-                if (ok && pend >= 0)
+                if (values && ok && pend >= 0)
                     ok = widen(g + pend, pend_nsub);
             }
             g += w.n;
