@@ -46,6 +46,7 @@ struct DecodeParams {
     int max_blocks_per_seq, num_blocks, block_size, max_context_len;
     int block_shift;  // log2(block_size)
     int part_tokens;  // tokens per work unit (a multiple of 16)
+    int reduce_heads; // reduce kernel: query heads per CTA (1 or the group)
     int max_parts;    // partitions per sequence the workspace holds
     float scale_log2; // scale * log2(e) (times the K scale for FP8 pools)
     float out_scale;  // applied to the attention output (the V scale for FP8 pools)
@@ -115,14 +116,20 @@ __device__ __forceinline__ int prefix_partitions(int start, int part_tokens)
 // by the partition pass itself.  With a shared prefix (start > 0) the first
 // partials are the prefix pass's and the sequence's own partitions follow.
 //
-// Thread (item, qg) -- item = (head, 8 consecutive d) -- takes partitions
-// q = qg, qg + QG, ... in chunks of kReduceUnroll whose loads are all issued
-// before any is used, and keeps its own (M_t, L_t, A_t) with the same
-// log-sum-exp rescaling; the QG threads of an item then combine theirs in
-// shared memory.  After the context length, every global load of a chunk is
+// One CTA per (sequence, run of R = reduce_heads query heads): R = 1 when
+// the batch is small enough that a CTA per head keeps the grid below
+// kReduceCtas (more threads per head, fewer trips to memory), else the G
+// heads of a KV head (a grid of one CTA per head would cost more to
+// schedule than it saves).  Thread (item, qg) -- item = (head, 8 consecutive
+// d), QG = 256 / (R * D / 8) threads per item -- takes partitions q = qg,
+// qg + QG, ... in chunks of kReduceUnroll whose loads are all issued before
+// any is used, and keeps its own (M_t, L_t, A_t) with the same log-sum-exp
+// rescaling; the QG threads of an item then combine theirs in shared
+// memory.  After the context length, every global load of a chunk is
 // independent, so a sequence with up to QG * kReduceUnroll partitions costs
-// two dependent trips to memory.
+// two dependent trips to memory (64 partitions at R = 1, d 128).
 constexpr int kReduceThreads = 256;
+constexpr int kReduceCtas = 1024;
 #ifndef PA_REDUCE_UNROLL
 #define PA_REDUCE_UNROLL 4
 #endif
@@ -143,10 +150,11 @@ __global__ void __launch_bounds__(kReduceThreads, PA_REDUCE_MINB)
     __shared__ float red_m[kReduceThreads], red_l[kReduceThreads];
     pdl_wait_primary();  // the partition pass's partials are visible past here
 
-    const int Hkv = p.num_kv_heads;
-    const int G = p.group;
-    const int s = blockIdx.x / Hkv;
-    const int kh = blockIdx.x - s * Hkv;
+    const int H = p.num_heads;
+    const int R = p.reduce_heads;
+    const int runs = H / R;
+    const int s = blockIdx.x / runs;
+    const int h0 = (blockIdx.x - s * runs) * R;  // first head of this CTA
     const int tid = threadIdx.x;
     const int ctx = clamp_context(p, s, false);
     const int start = seq_start_of(p, s, ctx);
@@ -157,16 +165,16 @@ __global__ void __launch_bounds__(kReduceThreads, PA_REDUCE_MINB)
     if (p.counters != nullptr && nparts <= kMergeMax)
         return;  // merged by the partition pass
 
-    // G * D / 8 <= 16 * 128 / 8 = kReduceThreads: one (item, qg) per thread.
+    // R * D / 8 <= 16 * 128 / 8 = kReduceThreads: one (item, qg) per thread.
     static_assert(16 * D / 8 <= kReduceThreads, "one work item per thread");
-    const int items = G * (D / 8);
-    const int qgroups = max(1, kReduceThreads / items);
+    const int items = R * (D / 8);
+    const int qgroups = kReduceThreads / items;
     const bool active = tid < items * qgroups;
     const int item = tid % items;
     const int qg = tid / items;
     const int jh = item / (D / 8);
     const int d0 = (item - jh * (D / 8)) * 8;
-    const size_t hrow = ((size_t)s * p.num_heads + (size_t)kh * G + jh) * p.max_parts;
+    const size_t hrow = ((size_t)s * H + h0 + jh) * p.max_parts;
 
     float mt = -INFINITY, lt = 0.f;  // natural-log units, like the stored m_q
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
@@ -213,7 +221,7 @@ __global__ void __launch_bounds__(kReduceThreads, PA_REDUCE_MINB)
         }
     }
 
-    const size_t out_off = ((size_t)s * p.num_heads + (size_t)kh * G + jh) * D + d0;
+    const size_t out_off = ((size_t)s * H + h0 + jh) * D + d0;
     if (qgroups == 1) {
         if (active) {
             const float inv = 1.f / lt;
@@ -515,8 +523,12 @@ struct KernelSetting {
 template <typename T, int D>
 static pa_status launch_reduce(const DecodeParams &prm, cudaStream_t stream)
 {
-    return launch_pdl(paged_reduce_kernel<T, D>, dim3((unsigned)(prm.num_seqs * prm.num_kv_heads)),
-                      dim3(kReduceThreads), 0, stream, prm);
+    DecodeParams r = prm;
+    const long long per_head = (long long)prm.num_seqs * prm.num_heads;
+    r.reduce_heads = per_head <= kReduceCtas ? 1 : prm.group;
+    return launch_pdl(paged_reduce_kernel<T, D>,
+                      dim3((unsigned)(per_head / r.reduce_heads)), dim3(kReduceThreads), 0,
+                      stream, r);
 }
 
 static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
