@@ -241,11 +241,21 @@ TRAFFIC_SUMMARIES = {
 }
 
 
+def _code_only(text: str) -> str:
+    """C/C++/CUDA source with its comments and blank lines removed (the
+    sources hold no comment markers inside string literals), so that a
+    change of comments alone keeps a recorded capture valid."""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
+
+
 def sources_sha256(names):
+    """sha256 over the code (comments stripped) of the named kernel sources."""
     h = hashlib.sha256()
     for n in names:
-        with open(os.path.join(CSRC, n), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(CSRC, n), encoding="utf-8") as f:
+            h.update(_code_only(f.read()).encode())
     return h.hexdigest()
 
 

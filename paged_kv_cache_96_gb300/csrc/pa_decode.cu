@@ -26,11 +26,15 @@
 //    accumulate); P goes from the S accumulator layout to the B-operand
 //    layout with movmatrix.  Every K/V byte is read from HBM once per step.
 //  * Softmax is online in fp32 (a reference max, running sum, exp2 with the
-//    scale folded into log2 units).  Warps merge their (m, l, O) through
-//    shared memory at the end of a unit.
+//    scale folded into log2 units).  At the end of a unit the tile warps
+//    hand their (m, l, O) to the CTA's merge warp through shared memory (two
+//    named barriers, no CTA-wide sync), which combines them and writes the
+//    output row or the unit's partial.
 //  * Split context: a unit that is one of several partitions of its
-//    sequence writes a partial (m, l, o) to the workspace; the reduce kernel
-//    queued behind this one merges them by log-sum-exp weights.
+//    sequence writes a partial (m, l, o) to the workspace and arrives on the
+//    sequence's counter; the arrival that completes a sequence of up to 8
+//    partials merges them by log-sum-exp weights in the same pass, and the
+//    reduce kernel queued behind this one merges longer sequences.
 //  * Bounds: table entries outside [0, num_blocks) are never fetched (the
 //    tile is skipped, an error bit is set); tokens past the context are
 //    masked in the scores and their value rows are zeroed before the

@@ -13,8 +13,10 @@
 //    blocks): the decode queries of every member of a group attend each
 //    partition of the group's shared prefix [0, L) once, read through the
 //    first member's table, and leave a partial (m, l, o) per (sequence,
-//    head, partition) for the split-context reduce to merge with the
-//    members' own partitions.
+//    head, partition) to be merged with the members' own partitions -- by
+//    whichever pass stores a sequence's last partial (the row warps here
+//    arrive on the sequence's counter after their stores), or by the reduce
+//    kernel for sequences of more than 8 partials.
 //
 // Design (GB300): a CTA takes 128 query rows of one KV head -- a chunk's
 // tokens times the G query heads of the group, or the members' decode
@@ -39,7 +41,10 @@
 // the first to run out stops all roles, and tensor memory is released on
 // every exit path.  Value rows past the key range are zeroed in shared
 // memory before the value product, so a poisoned (NaN) slot never reaches
-// the output.
+// the output.  FP8 (e4m3) pools: each tile lands as codes in the upper half
+// of its 16-bit stage and is widened there to fp16 before the tensor-core
+// warp may read it (keys by the row warps, values by the value warp); the
+// products run in fp16 with the query rounded to fp16.
 #include <cuda.h>
 
 #include <algorithm>
