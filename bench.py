@@ -61,7 +61,7 @@ def parse_args(argv=None):
     ap.add_argument("--config", default="gqa70b",
                     choices=["tiny", "mha7b", "gqa70b", "longctx", "prefix", "gqa70b-fp8",
                              "longctx-fp8", "prefix-cascade", "prefix-cascade-fp8", "mixed",
-                             "chunked", "chunked-fp8"])
+                             "mixed-fp8", "chunked", "chunked-fp8"])
     ap.add_argument("--partition", type=int, default=None,
                     help="split-context partition tokens (0 = single pass)")
     ap.add_argument("--separate-append", action="store_true",

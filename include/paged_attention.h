@@ -352,9 +352,8 @@ PA_API pa_status pa_prefill_attention(void *out, const void *query, const void *
  * 65504 is flagged PA_DEVERR_QUERY_RANGE and its rows are not finite); k_scale
  * joins the softmax scale, v_scale multiplies the output.  query and out are
  * dtype (PA_F16 or PA_BF16); k_scale and v_scale must be positive and finite
- * (PA_ERR_INVALID_ARG).  Supported: head_dim 128 (PA_ERR_UNSUPPORTED
- * otherwise); other limits, arguments, rows and errors as
- * pa_prefill_attention.
+ * (PA_ERR_INVALID_ARG).  Limits (head_dim 64 or 128 among them), other
+ * arguments, rows and errors as pa_prefill_attention.
  */
 PA_API pa_status pa_prefill_attention_fp8(void *out, const void *query, const void *key_cache,
                                           const void *value_cache, const int32_t *block_tables,
@@ -486,9 +485,8 @@ PA_API pa_status pa_decode_attention_cascade_append(
  * PA_DEVERR_QUERY_RANGE beyond it, k_scale in the softmax scale, v_scale on
  * the output) and the append's codes as pa_decode_attention_append_fp8
  * writes them.  k_scale, v_scale positive and finite (PA_ERR_INVALID_ARG).
- * Supported with groups: head_dim 128 (PA_ERR_UNSUPPORTED otherwise); with
- * num_groups == 0 these are pa_decode_attention_fp8 /
- * pa_decode_attention_append_fp8.  Other arguments, workspace and errors as
+ * With num_groups == 0 these are pa_decode_attention_fp8 /
+ * pa_decode_attention_append_fp8.  Other arguments, limits, workspace and errors as
  * pa_decode_attention_cascade(_append).
  */
 PA_API pa_status pa_decode_attention_cascade_fp8(

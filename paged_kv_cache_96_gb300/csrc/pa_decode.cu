@@ -1236,8 +1236,6 @@ static pa_status run_cascade(void *out, const void *query, void *key_cache, void
         return ok;
     if (prefix_plan == nullptr)
         return PA_ERR_INVALID_ARG;
-    if (fp8 && head_dim != 128)
-        return PA_ERR_UNSUPPORTED;  // the FP8 prefix pass: head_dim 128
     if (new_key != nullptr) {
         ok = set_append(&prm, key_cache, value_cache, new_key, new_value, slot_mapping);
         if (ok != PA_OK)
@@ -1321,12 +1319,19 @@ static pa_status run_cascade(void *out, const void *query, void *key_cache, void
     using B16 = __nv_bfloat16;
     using F16 = __half;
     using U8 = uint8_t;
-    if (fp8) {
+    if (fp8 && head_dim == 128) {
         if (bf)
             return wide ? launch_decode<B16, U8, 128, 2>(prm, mk, mv, st, max_units, &pp)
                         : launch_decode<B16, U8, 128, 1>(prm, mk, mv, st, max_units, &pp);
         return wide ? launch_decode<F16, U8, 128, 2>(prm, mk, mv, st, max_units, &pp)
                     : launch_decode<F16, U8, 128, 1>(prm, mk, mv, st, max_units, &pp);
+    }
+    if (fp8) {
+        if (bf)
+            return wide ? launch_decode<B16, U8, 64, 2>(prm, mk, mv, st, max_units, &pp)
+                        : launch_decode<B16, U8, 64, 1>(prm, mk, mv, st, max_units, &pp);
+        return wide ? launch_decode<F16, U8, 64, 2>(prm, mk, mv, st, max_units, &pp)
+                    : launch_decode<F16, U8, 64, 1>(prm, mk, mv, st, max_units, &pp);
     }
     if (head_dim == 128) {
         if (bf)

@@ -108,14 +108,20 @@ constexpr int kTcStages = 2;
 constexpr uint32_t kTmemCols = 256;  // S/P buffers at columns 0 and 64, O at column 128
 constexpr uint32_t kTmemO = 128;
 
-template <int D> struct TcLayout {
+template <int D, bool kFp8> struct TcLayout {
     static constexpr int kHalves = D / 64;                    // 128-byte rows of 64 elements
     static constexpr int kQHalf = kTcRows * 128;              // 16 KB: 128 rows of one d-half
     static constexpr int kKVHalf = kTcTokens * 128;           // 8 KB: 64 tokens of one d-half
     static constexpr int kKVBytes = kHalves * kKVHalf;        // K (or V) of one stage
     static constexpr int kStageBytes = 2 * kKVBytes;          // K then V
     static constexpr int kQ = kTcStages * kStageBytes;
-    static constexpr int kBars = kQ + kHalves * kQHalf;       // 16 mbarriers
+    // FP8 pools: a tile's e4m3 codes (kTcTokens rows of D bytes) land in the
+    // upper d-half of its 16-bit stage at d 128, in a region of their own
+    // (stage-major, K then V) at d 64
+    static constexpr int kCodeTile = kTcTokens * D;
+    static constexpr int kCodes = kQ + kHalves * kQHalf;
+    static constexpr int kCodesBytes = (kFp8 && D == 64) ? kTcStages * 2 * kCodeTile : 0;
+    static constexpr int kBars = kCodes + kCodesBytes;        // 16 mbarriers
     static constexpr int kTmemSlot = kBars + 16 * 8;
     static constexpr int kAbort = kTmemSlot + 8;
     static constexpr int kSeg = kTmemSlot + 16;               // int unit prefix[n + 1]
@@ -158,7 +164,7 @@ __device__ __forceinline__ int mq_segment_units(const MqParams &p, int seg)
     return tiles * ((mq_group_prefix(p, seg) + p.part_tokens - 1) / p.part_tokens);
 }
 
-// kFp8: the pools hold e4m3 codes.  The fetch warps land each 64-token FP8
+// kFp8: the pools hold e4m3 codes (head_dim 64 or 128).  The fetch warps land each 64-token FP8
 // tile in the upper half of its 16-bit stage and widen it there to fp16 (the
 // stage's K-major / MN-major operand layout, as a 16-bit fill leaves it),
 // then release the stage; the products run in fp16 with the query rounded to
@@ -170,8 +176,8 @@ __global__ void __launch_bounds__(kTcThreads, 2)
                     const __grid_constant__ CUtensorMap tmap_k,
                     const __grid_constant__ CUtensorMap tmap_v)
 {
-    using L = TcLayout<D>;
-    static_assert(!kFp8 || D == 128, "FP8 pools: head_dim 128");
+    using L = TcLayout<D, kFp8>;
+    static_assert(D == 64 || D == 128, "head_dim 64 or 128");
     using OT = typename std::conditional<kFp8, __half, T>::type;  // operand type
     constexpr bool kBf16 = std::is_same<OT, __nv_bfloat16>::value;
     constexpr uint32_t kIdescS = idesc_f16(kBf16, kTcRows, kTcTokens, false, false);
@@ -201,6 +207,25 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     auto kland = [&](int st) { return bar(12 + st); };
     auto vland = [&](int st) { return bar(14 + st); };
     auto kbase = [&](int st) { return sbase + st * L::kStageBytes; };
+    // FP8 pools: where the codes of stage st's keys (values) land, and the
+    // shared address of 16-byte chunk cc of code row r there (the TMA's
+    // 128-byte swizzle for 128-byte rows, 64-byte swizzle for 64-byte rows)
+    auto code_base = [&](int st, bool vals) -> uint32_t {
+        if constexpr (D == 128)
+            return kbase(st) + (vals ? L::kKVBytes : 0) + L::kKVHalf;
+        else
+            return sbase + L::kCodes + (st * 2 + (vals ? 1 : 0)) * L::kCodeTile;
+    };
+    auto code_chunk = [&](uint32_t cb, int r, int cc) -> uint32_t {
+        if constexpr (D == 128)
+            return cb + r * 128 + ((cc ^ (r & 7)) << 4);
+        else
+            return cb + r * 64 + ((cc ^ ((r >> 1) & 3)) << 4);
+    };
+    // fp16 chunk f (elements 8f .. 8f + 7) of row r of a 16-bit operand tile
+    auto f16_chunk = [&](uint32_t tb, int r, int f) -> uint32_t {
+        return tb + (f >> 3) * L::kKVHalf + r * 128 + (((f & 7) ^ (r & 7)) << 4);
+    };
     // operand descriptors of stage 0 and of the query tile; other stages and
     // k-steps add their byte offset / 16 to the start-address field
     const uint64_t desc_q0 = smem_desc_sw128(qbase, 16, 1024);
@@ -446,26 +471,28 @@ __global__ void __launch_bounds__(kTcThreads, 2)
             const uint32_t st = gg & 1;
             if (!wait(kland(st), (gg >> 1) & 1))
                 return false;
-            const uint32_t base = kbase(st);
-            const int r = tid >> 1, hf = tid & 1;  // row, and the d-half this thread writes
-            uint4 src[4];
+            const uint32_t base = kbase(st), cb = code_base(st, false);
+            // row r; this thread's half of its code chunks (16 codes each)
+            constexpr int kCh = D / 32;
+            const int r = tid >> 1, h = tid & 1;
+            uint4 src[kCh];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                const int cc = 4 * hf + c;  // code chunk: codes 16cc .. 16cc + 15
-                const uint32_t a = base + L::kKVHalf + r * 128 + ((cc ^ (r & 7)) << 4);
+            for (int j = 0; j < kCh; ++j) {
+                const uint32_t a = code_chunk(cb, r, h * kCh + j);
                 asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                             : "=r"(src[c].x), "=r"(src[c].y), "=r"(src[c].z), "=r"(src[c].w)
+                             : "=r"(src[j].x), "=r"(src[j].y), "=r"(src[j].z), "=r"(src[j].w)
                              : "r"(a)
                              : "memory");
             }
-            __syncwarp();  // both halves of the row are read before d-half 1 overwrites it
+            __syncwarp();  // (d 128) the row is read before d-half 1 overwrites its codes
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                // fp16 chunk c of d-half hf = codes 64hf + 8c .. + 7
+            for (int c = 0; c < 2 * kCh; ++c) {
+                // fp16 chunk f = codes 8f .. 8f + 7
+                const int f = 2 * h * kCh + c;
                 const uint4 sc = src[c >> 1];
                 const uint32_t lo = (c & 1) ? sc.z : sc.x;
                 const uint32_t hi = (c & 1) ? sc.w : sc.y;
-                const uint32_t a = base + hf * L::kKVHalf + r * 128 + ((c ^ (r & 7)) << 4);
+                const uint32_t a = f16_chunk(base, r, f);
                 asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a),
                              "r"(e4m3x2_to_f16x2((uint16_t)(lo & 0xffffu))),
                              "r"(e4m3x2_to_f16x2((uint16_t)(lo >> 16))),
@@ -745,15 +772,15 @@ __global__ void __launch_bounds__(kTcThreads, 2)
                 const int t0 = w.kbeg + si * kTcTokens;
                 const int nsub = min(kTcSubs, (w.kend - t0 + kTileTokens - 1) / kTileTokens);
                 if constexpr (kFp8) {
-                    // the codes land in the stage's upper half (d-half 1's rows)
+                    // the codes land where code_base says: one box of 16 rows
+                    // of D codes per sub-tile
                     const uint32_t fb = values ? vland(st) : kland(st);
                     if (lane == 0)
-                        mbar_arrive_expect_tx(fb, (uint32_t)(nsub * 2048));
+                        mbar_arrive_expect_tx(fb, (uint32_t)(nsub * kTileTokens * D));
                     __syncwarp();
                     if (my_sb < nsub) {
                         const int row = (t0 + my_sb * kTileTokens) & (p.block_size - 1);
-                        tma_load_4d(kbase(st) + (values ? L::kKVBytes : 0) + L::kKVHalf +
-                                        my_sb * 2048,
+                        tma_load_4d(code_base(st, values) + my_sb * kTileTokens * D,
                                     values ? &tmap_v : &tmap_k, fb, 0, w.kh, row, ent);
                     }
                 } else {
@@ -780,11 +807,12 @@ __global__ void __launch_bounds__(kTcThreads, 2)
                 if (!wait(values ? vland(st) : kland(st), (gg >> 1) & 1))
                     return false;
                 const uint32_t base = kbase(st) + (values ? L::kKVBytes : 0);
+                const uint32_t cb = code_base(st, values);
                 for (int r = lane; r < nsub * kTileTokens; r += 32) {
-                    uint4 src[8];
+                    uint4 src[D / 16];
 #pragma unroll
-                    for (int c = 0; c < 8; ++c) {
-                        const uint32_t a = base + L::kKVHalf + r * 128 + ((c ^ (r & 7)) << 4);
+                    for (int c = 0; c < D / 16; ++c) {
+                        const uint32_t a = code_chunk(cb, r, c);
                         asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
                                      : "=r"(src[c].x), "=r"(src[c].y), "=r"(src[c].z),
                                        "=r"(src[c].w)
@@ -792,22 +820,19 @@ __global__ void __launch_bounds__(kTcThreads, 2)
                                      : "memory");
                     }
 #pragma unroll
-                    for (int hf = 0; hf < 2; ++hf)
-#pragma unroll
-                        for (int c = 0; c < 8; ++c) {
-                            // fp16 chunk c of d-half hf = codes 64hf + 8c .. + 7
-                            const uint4 sc = src[4 * hf + (c >> 1)];
-                            const uint32_t lo = (c & 1) ? sc.z : sc.x;
-                            const uint32_t hi = (c & 1) ? sc.w : sc.y;
-                            const uint32_t a = base + hf * L::kKVHalf + r * 128 +
-                                               ((c ^ (r & 7)) << 4);
-                            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a),
-                                         "r"(e4m3x2_to_f16x2((uint16_t)(lo & 0xffffu))),
-                                         "r"(e4m3x2_to_f16x2((uint16_t)(lo >> 16))),
-                                         "r"(e4m3x2_to_f16x2((uint16_t)(hi & 0xffffu))),
-                                         "r"(e4m3x2_to_f16x2((uint16_t)(hi >> 16)))
-                                         : "memory");
-                        }
+                    for (int f = 0; f < D / 8; ++f) {
+                        // fp16 chunk f = codes 8f .. 8f + 7
+                        const uint4 sc = src[f >> 1];
+                        const uint32_t lo = (f & 1) ? sc.z : sc.x;
+                        const uint32_t hi = (f & 1) ? sc.w : sc.y;
+                        const uint32_t a = f16_chunk(base, r, f);
+                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a),
+                                     "r"(e4m3x2_to_f16x2((uint16_t)(lo & 0xffffu))),
+                                     "r"(e4m3x2_to_f16x2((uint16_t)(lo >> 16))),
+                                     "r"(e4m3x2_to_f16x2((uint16_t)(hi & 0xffffu))),
+                                     "r"(e4m3x2_to_f16x2((uint16_t)(hi >> 16)))
+                                     : "memory");
+                    }
                 }
                 fence_proxy_async_smem();  // the widened tile, for the tensor cores
                 __syncwarp();
@@ -961,7 +986,7 @@ template <typename T, int D, bool kFp8>
 static pa_status launch_mq(const MqParams &prm, const CUtensorMap &mk, const CUtensorMap &mv,
                            cudaStream_t stream, long long max_units)
 {
-    using L = TcLayout<D>;
+    using L = TcLayout<D, kFp8>;
     auto kernel = paged_mq_kernel<T, D, kFp8>;
     static KernelSetting setting[kMaxDevices];
     static std::mutex mu;
@@ -1025,7 +1050,7 @@ static pa_status launch_mq(const MqParams &prm, const CUtensorMap &mk, const CUt
                       mv);
 }
 
-// pool_dtype PA_FP8_E4M3: e4m3 pools (head_dim 128), query and output of
+// pool_dtype PA_FP8_E4M3: e4m3 pools, query and output of
 // query_dtype; otherwise 16-bit pools and query of pool_dtype.
 static pa_status dispatch_mq(const MqParams &prm, pa_dtype pool_dtype, pa_dtype query_dtype,
                              const void *key_cache, const void *value_cache, int head_dim,
@@ -1038,9 +1063,14 @@ static pa_status dispatch_mq(const MqParams &prm, pa_dtype pool_dtype, pa_dtype 
                          prm.num_kv_heads, head_dim))
         return PA_ERR_CUDA;
     using B16 = __nv_bfloat16;
-    if (pool_dtype == PA_FP8_E4M3)
-        return query_dtype == PA_BF16 ? launch_mq<B16, 128, true>(prm, mk, mv, stream, max_units)
-                                      : launch_mq<__half, 128, true>(prm, mk, mv, stream, max_units);
+    if (pool_dtype == PA_FP8_E4M3) {
+        const bool qbf = query_dtype == PA_BF16;
+        if (head_dim == 128)
+            return qbf ? launch_mq<B16, 128, true>(prm, mk, mv, stream, max_units)
+                       : launch_mq<__half, 128, true>(prm, mk, mv, stream, max_units);
+        return qbf ? launch_mq<B16, 64, true>(prm, mk, mv, stream, max_units)
+                   : launch_mq<__half, 64, true>(prm, mk, mv, stream, max_units);
+    }
     if (head_dim == 128)
         return pool_dtype == PA_BF16 ? launch_mq<B16, 128, false>(prm, mk, mv, stream, max_units)
                                      : launch_mq<__half, 128, false>(prm, mk, mv, stream, max_units);
@@ -1088,7 +1118,7 @@ static pa_status run_prefill(void *out, const void *query, const void *key_cache
         !aligned16(value_cache))
         return PA_ERR_INVALID_ARG;
     const int group = num_heads / num_kv_heads;
-    if ((head_dim != 64 && head_dim != 128) || (fp8 && head_dim != 128) ||
+    if ((head_dim != 64 && head_dim != 128) ||
         block_size < kTileTokens || block_size > 256 || (block_size & (block_size - 1)) != 0 ||
         group > 16 || (long long)num_blocks * block_size >= (1ll << 31) ||
         (long long)max_blocks_per_seq * block_size >= (1ll << 31))

@@ -458,3 +458,4 @@ CONFIGS["gqa70b-fp8"] = fp8_variant(CONFIGS["gqa70b"])
 CONFIGS["longctx-fp8"] = fp8_variant(CONFIGS["longctx"])
 CONFIGS["chunked-fp8"] = fp8_variant(CONFIGS["chunked"])
 CONFIGS["prefix-cascade-fp8"] = fp8_variant(CONFIGS["prefix-cascade"])
+CONFIGS["mixed-fp8"] = fp8_variant(CONFIGS["mixed"])

@@ -178,7 +178,7 @@ def test_cascade_append_argument_checks(B):
     ws = (ctypes.c_uint8 * (1 << 22))()
     wsp = (ctypes.addressof(ws) + 255) // 256 * 256
     okw = ok8[:24] + (wsp, (1 << 22) - 256) + ok8[26:]
-    assert f8(*okw[:14], 64, *okw[15:]) == B.PA_ERR_UNSUPPORTED        # FP8 prefix pass: d 128
+    assert f8(*okw[:14], 96, *okw[15:]) == B.PA_ERR_UNSUPPORTED        # head_dim 96
     g8 = L.pa_decode_attention_cascade_fp8
     # (out, query, kc, vc, tables, mb, ctx, maxctx, S, H, Hkv, d, bs, N, scale, k_scale,
     #  v_scale, plan, groups, members, P, ws, ws_bytes, dtype, err, stream)
@@ -209,7 +209,7 @@ def test_prefill_argument_checks(B):
     assert f8(*ok8[:17], 0.0, 0.5, *ok8[19:]) == B.PA_ERR_INVALID_ARG  # zero K scale
     assert f8(*ok8[:17], 0.5, float("nan"), *ok8[19:]) == B.PA_ERR_INVALID_ARG
     assert f8(*ok8[:19], 2, *ok8[20:]) == B.PA_ERR_INVALID_ARG         # query not 16-bit
-    assert f8(*ok8[:13], 64, *ok8[14:]) == B.PA_ERR_UNSUPPORTED        # FP8: d 128 only
+    assert f8(*ok8[:13], 96, *ok8[14:]) == B.PA_ERR_UNSUPPORTED        # head_dim 96
     assert f8(*ok8[:2], FAKE_ODD, *ok8[3:]) == B.PA_ERR_INVALID_ARG    # unaligned pool
 
 
@@ -248,7 +248,7 @@ def test_workspace_layout_sizes(B):
                                         ("prefix-cascade", True), ("gqa70b-fp8", True),
                                         ("prefix-cascade-fp8", True),
                                         ("chunked", False), ("chunked-fp8", False),
-                                        ("mixed", False)])
+                                        ("mixed", False), ("mixed-fp8", False)])
 def test_step_takes_the_fused_append(lib, name, fused):
     """Host logic of the step: a decode step whose new tokens are one per
     sequence at its last position (in the same block before and after

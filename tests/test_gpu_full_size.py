@@ -15,7 +15,7 @@ from paged_kv_cache_96_gb300 import workloads as W  # noqa: E402
 from stepping import OracleStep, assert_attention_close, attention_all  # noqa: E402
 
 NAMES = ["tiny", "mha7b", "gqa70b", "longctx", "prefix", "gqa70b-fp8", "longctx-fp8",
-         "prefix-cascade", "mixed", "chunked", "chunked-fp8", "prefix-cascade-fp8"]
+         "prefix-cascade", "mixed", "chunked", "chunked-fp8", "prefix-cascade-fp8", "mixed-fp8"]
 
 
 @pytest.mark.parametrize("name", NAMES)

@@ -79,6 +79,8 @@ SPECS["gqa-fp8"] = W.fp8_variant(SPECS["gqa"])
 SPECS["d64-fp8"] = W.fp8_variant(SPECS["d64"])
 SPECS["cascade-fp8"] = W.fp8_variant(SPECS["cascade"])
 SPECS["prefill-fp8"] = W.fp8_variant(SPECS["prefill"])
+SPECS["prefill-d64-fp8"] = W.fp8_variant(dataclasses.replace(
+    SPECS["prefill"], name="needle-prefill-d64", head_dim=64, block_size=32))
 
 DOMINANT_SCORE = 20.0
 VROW = np.array([3.0, 3.25, 3.5, 3.75])   # exact in fp16 and bf16
@@ -286,7 +288,7 @@ def test_cascade_needles(S, how, name):
             _check_dominant(w, got, want, s, 1)
 
 
-@pytest.mark.parametrize("name", ["prefill", "prefill-fp8"])
+@pytest.mark.parametrize("name", ["prefill", "prefill-fp8", "prefill-d64-fp8"])
 def test_prefill_needles(S, name):
     """Chunked prefill: a dominant needle per (sequence, KV head) -- before
     the chunk, at its first row, at 64-token tile edges, inside it -- with

@@ -41,7 +41,7 @@ def small():
 
 # ---- chunked prefill / mixed batch ------------------------------------------------
 
-@pytest.mark.parametrize("name", ["mixed", "chunked", "chunked-fp8"])
+@pytest.mark.parametrize("name", ["mixed", "chunked", "chunked-fp8", "mixed-fp8"])
 def test_prefill_step_matches_oracle(B, S, small, name):
     w, ref = small(name)
     st = S.DecodeStep(w)
@@ -208,6 +208,31 @@ def test_cascade_separate_write_matches_oracle(B, S, small, name):
     assert np.array_equal(S.to_bits(st.key_cache), ref.key_cache)
     assert np.array_equal(S.to_bits(st.value_cache), ref.value_cache)
     assert_attention_close(S.to_float(st.out), ref.attention(), f"{name} separate")
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+def test_cascade_head_dim_64(B, S, fp8):
+    """Prefix-aware decode at head_dim 64 (16-bit and FP8 pools), fused append
+    and separate write, against the oracle."""
+    import dataclasses
+    spec = W.small_variant("prefix-cascade-fp8" if fp8 else "prefix-cascade")
+    spec = dataclasses.replace(spec, name=spec.name + "-d64", head_dim=64)
+    w = W.build(spec)
+    ref = OracleStep(w)
+    for how in ("append", "separate"):
+        st = S.DecodeStep(w)
+        assert st.num_groups >= 1
+        if how == "append":
+            st.copy_blocks()
+            st.append_attention()
+        else:
+            st.slot_mapping_and_cache()
+            st.copy_blocks()
+            st.attention()
+        torch.cuda.synchronize()
+        assert int(st.error_word.item()) == 0
+        assert np.array_equal(S.to_bits(st.key_cache), ref.key_cache)
+        assert_attention_close(S.to_float(st.out), ref.attention(), f"d64 fp8={fp8} {how}")
 
 
 def test_cascade_fp8_query_beyond_fp16_is_flagged(B, S, small):

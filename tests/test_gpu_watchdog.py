@@ -35,6 +35,7 @@ CASES = [
     ("chunked", 0, "prefill"),
     ("chunked-fp8", 0, "prefill"),
     ("mixed", 0, "prefill"),
+    ("mixed-fp8", 0, "prefill"),
 ]
 
 
