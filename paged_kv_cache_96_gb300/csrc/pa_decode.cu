@@ -54,6 +54,17 @@
 
 namespace pa {
 
+// FP8 pools: units are numbered sequence by sequence, the sequences with
+// the most partitions first (by index within a count; counts from
+// kOrderBuckets - 1 up share the first place), so that the static deal's
+// last round -- run while most CTAs have finished -- holds the short
+// sequences' units (the FP8 pass is bound by its instructions per tile, so
+// the CTAs left at the end cannot take up the bandwidth the others free).
+// 16-bit pools, and batches of more than kOrderSeqs sequences, keep the
+// sequences' own order.
+constexpr int kOrderBuckets = 64;
+constexpr int kOrderSeqs = 512;
+
 // Shared-memory layout (offsets from a 1024-byte aligned base): NW warps,
 // each with a private ring of NST stages.  EB = bytes per cached element
 // (2 for fp16/bf16 pools, 1 for FP8 pools).
@@ -73,8 +84,15 @@ template <int D, int NT, int NW, int NST, int EB> struct Layout {
     static constexpr int kAppM = kAppV + 2 * D * 4;
     static constexpr int kBars = kAppM + 2 * kHeads * 4;  // NW * NST stage barriers
     static constexpr int kFlags = kBars + NW * NST * 8;
-    static constexpr int kSeq = kFlags + NW * NST * 4;  // int ctx[S], prefix[S + 1], start[S]
-    static size_t bytes(int num_seqs) { return 1024 + kSeq + 4 * (3 * (size_t)num_seqs + 1); }
+    static constexpr bool kOrdered = EB == 1;  // FP8 pools: the unit order below
+    static constexpr int kHist = kFlags + NW * NST * 4;  // the unit order's buckets
+    // int ctx[S], prefix[S + 1], start[S], then (ordered) order[S]
+    static constexpr int kSeq = kHist + (kOrdered ? kOrderBuckets * 4 : 0);
+    static size_t bytes(int num_seqs)
+    {
+        const size_t per_seq = kOrdered && num_seqs <= kOrderSeqs ? 4 : 3;
+        return 1024 + kSeq + 4 * (per_seq * (size_t)num_seqs + 1);
+    }
     static_assert(kBars % 8 == 0, "mbarriers need 8-byte alignment");
     static_assert(kStageBytes % 1024 == 0, "stages must keep 1024-byte alignment");
 };
@@ -241,8 +259,10 @@ __global__ void __launch_bounds__(bound_threads(NW + 1, MINB), MINB)
     const int napp = p.new_key != nullptr ? 1 : 0;
 
     int *ctx_s = reinterpret_cast<int *>(smem + L::kSeq);
-    int *pref = ctx_s + S;
+    int *pref = ctx_s + S;  // over the unit order: pref[k] = partitions of order[0 .. k)
     int *start_s = pref + S + 1;
+    const bool ordered = L::kOrdered && S <= kOrderSeqs;
+    int *order = start_s + S;  // k-th sequence of the unit order (when ordered)
     volatile int *flags = reinterpret_cast<volatile int *>(smem + L::kFlags);
     float *merge_o = reinterpret_cast<float *>(smem + L::kMergeO);
     float *merge_m = reinterpret_cast<float *>(smem + L::kMergeM);
@@ -283,10 +303,52 @@ __global__ void __launch_bounds__(bound_threads(NW + 1, MINB), MINB)
     }
     __syncthreads();
     if (warp == 0) {
+        if (ordered) {
+            // counting sort by partitions, most first, by index within a count;
+            // every CTA computes the same order
+            int *hist = reinterpret_cast<int *>(smem + L::kHist);
+            auto key_of = [&](int sq) {
+                return kOrderBuckets - 1 -
+                       min(own_partitions(ctx_s[sq], start_s[sq], P), kOrderBuckets - 1);
+            };
+            hist[lane] = 0;
+            hist[lane + 32] = 0;
+            __syncwarp();
+            for (int sq = lane; sq < S; sq += 32)
+                atomicAdd(&hist[key_of(sq)], 1);
+            __syncwarp();
+            const int c0 = hist[2 * lane], c1 = hist[2 * lane + 1];
+            int x = c0 + c1;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(kFull, x, o);
+                if (lane >= o)
+                    x += y;
+            }
+            __syncwarp();
+            hist[2 * lane] = x - c0 - c1;  // first place of each count
+            hist[2 * lane + 1] = x - c1;
+            __syncwarp();
+            for (int base = 0; base < S; base += 32) {
+                const int sq = base + lane;
+                const int key = sq < S ? key_of(sq) : -1;
+                const unsigned same = __match_any_sync(kFull, key);
+                const int rank = __popc(same & ((1u << lane) - 1u));
+                const int off = key >= 0 ? hist[key] : 0;
+                __syncwarp();
+                if (key >= 0) {
+                    order[off + rank] = sq;
+                    if (rank == 0)
+                        hist[key] = off + __popc(same);
+                }
+                __syncwarp();
+            }
+        }
         int carry = 0;
         for (int base = 0; base < S; base += 32) {
-            const int s = base + lane;
-            const int n = s < S ? own_partitions(ctx_s[s], start_s[s], P) : 0;
+            const int k = base + lane;
+            const int sq = k < S ? (ordered ? order[k] : k) : 0;
+            const int n = k < S ? own_partitions(ctx_s[sq], start_s[sq], P) : 0;
             int x = n;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
@@ -294,8 +356,8 @@ __global__ void __launch_bounds__(bound_threads(NW + 1, MINB), MINB)
                 if (lane >= o)
                     x += y;
             }
-            if (s < S)
-                pref[s] = carry + x - n;
+            if (k < S)
+                pref[k] = carry + x - n;
             carry += __shfl_sync(kFull, x, 31);
         }
         if (lane == 0)
@@ -316,8 +378,8 @@ __global__ void __launch_bounds__(bound_threads(NW + 1, MINB), MINB)
             row[i] = make_uint4(0, 0, 0, 0);
     }
 
-    // unit u -> partition q = u / Hkv, kv head u % Hkv; sequence s is the one
-    // with pref[s] <= q < pref[s + 1].
+    // unit u -> partition q = u / Hkv, kv head u % Hkv; sequence s is the
+    // k-th of the unit order, k the one with pref[k] <= q < pref[k + 1].
     auto decode_unit = [&](int u, int &s, int &kh, int &j, int &tok0, int &ntiles) {
         const int q = u / Hkv;
         kh = u - q * Hkv;
@@ -329,8 +391,8 @@ __global__ void __launch_bounds__(bound_threads(NW + 1, MINB), MINB)
             else
                 hi = mid - 1;
         }
-        s = lo;
-        j = q - pref[s];
+        j = q - pref[lo];
+        s = ordered ? order[lo] : lo;
         tok0 = start_s[s] + j * P;
         const int tok_end = min(ctx_s[s] - napp, tok0 + P);
         ntiles = (tok_end - tok0 + kTileTokens - 1) / kTileTokens;
@@ -742,7 +804,7 @@ __global__ void __launch_bounds__(bound_threads(NW + 1, MINB), MINB)
             int s, kh, j, tok0, ntiles;
             decode_unit(u, s, kh, j, tok0, ntiles);
             const bool app = napp != 0 && tok0 + P >= ctx_s[s];
-            const int nparts = pref[s + 1] - pref[s];
+            const int nparts = own_partitions(ctx_s[s], start_s[s], P);
             // the first partials belong to the prefix pass
             const int pbase = prefix_partitions(start_s[s], P);
             const bool split = nparts > 1 || pbase > 0;
