@@ -398,14 +398,21 @@ __global__ void __launch_bounds__(bound_threads(NW + 1, MINB), MINB)
         ntiles = (tok_end - tok0 + kTileTokens - 1) / kTileTokens;
     };
 
+    // this CTA's units: the first, and the one after unit u
+    const int early_units = p.early_rounds * p.early_ctas;
+    const int u_first = (int)blockIdx.x < p.early_ctas ? (int)blockIdx.x
+                                                        : early_units + (int)blockIdx.x;
+    auto next_u = [&](int u) -> int {
+        return u < early_units ? u + p.early_ctas : u + (int)gridDim.x;
+    };
     // ---- this warp's fetch cursor: its next tile, possibly in a later unit ----
-    int pu = blockIdx.x, ps = 0, pkh = 0, pj = 0, ptok0 = 0, pnt = 0, ptile = warp;
+    int pu = u_first, ps = 0, pkh = 0, pj = 0, ptok0 = 0, pnt = 0, ptile = warp;
     bool pdone = pu >= total_units || warp >= NW;  // the merge warp fetches nothing
     if (!pdone)
         decode_unit(pu, ps, pkh, pj, ptok0, pnt);
     auto skip_empty = [&]() {
         while (!pdone && ptile >= pnt) {
-            pu += gridDim.x;
+            pu = next_u(pu);
             if (pu >= total_units) {
                 pdone = true;
                 break;
@@ -532,9 +539,9 @@ __global__ void __launch_bounds__(bound_threads(NW + 1, MINB), MINB)
             }
         }
     };
-    if (blockIdx.x < total_units && warp < NW) {
+    if (u_first < total_units && warp < NW) {
         int s, kh, j, tok0, ntiles;
-        decode_unit(blockIdx.x, s, kh, j, tok0, ntiles);
+        decode_unit(u_first, s, kh, j, tok0, ntiles);
         load_query(s, kh);
     }
 
@@ -552,7 +559,7 @@ __global__ void __launch_bounds__(bound_threads(NW + 1, MINB), MINB)
     if (warp < NW) {
         int k_unit = 0;          // units of this CTA so far
         bool rec_aborted = false;
-        for (int u = blockIdx.x; u < total_units; u += gridDim.x, ++k_unit) {
+        for (int u = u_first; u < total_units; u = next_u(u), ++k_unit) {
             int s, kh, j, tok0, ntiles;
             decode_unit(u, s, kh, j, tok0, ntiles);
             const int tok_end = min(ctx_s[s] - napp, tok0 + P);
@@ -754,9 +761,9 @@ __global__ void __launch_bounds__(bound_threads(NW + 1, MINB), MINB)
             }
 
             // Next unit's query: its loads land while this unit's records go out.
-            if (u + (int)gridDim.x < total_units) {
+            if (next_u(u) < total_units) {
                 int sn, khn, jn, tn, ntn;
-                decode_unit(u + gridDim.x, sn, khn, jn, tn, ntn);
+                decode_unit(next_u(u), sn, khn, jn, tn, ntn);
                 load_query(sn, khn);
             }
 
@@ -800,7 +807,7 @@ __global__ void __launch_bounds__(bound_threads(NW + 1, MINB), MINB)
     } else {
         // ===== the merge warp ======================================================
         int k_unit = 0;
-        for (int u = blockIdx.x; u < total_units; u += gridDim.x, ++k_unit) {
+        for (int u = u_first; u < total_units; u = next_u(u), ++k_unit) {
             int s, kh, j, tok0, ntiles;
             decode_unit(u, s, kh, j, tok0, ntiles);
             const bool app = napp != 0 && tok0 + P >= ctx_s[s];
@@ -866,7 +873,7 @@ __global__ void __launch_bounds__(bound_threads(NW + 1, MINB), MINB)
             }
             // the records (and the append buffer) may be rewritten; the tile
             // warps wait for this only from their next unit on
-            if (u + (int)gridDim.x < total_units)
+            if (next_u(u) < total_units)
                 named_barrier_arrive(kRecFree, kThreads);
             if (split && p.counters != nullptr && pbase + nparts <= kMergeMax)
                 // records loaded per lane at once: fewer under the FP8 register cap
@@ -982,7 +989,18 @@ static pa_status launch_pass(const DecodeParams &prm, const CUtensorMap &mk,
         grid = max_units;
     if (grid < 1)
         grid = 1;
-    return launch_pdl(kernel, dim3((unsigned)grid), dim3(kThreads), smem, stream, prm, mk, mv);
+    // Beside the shared-prefix pass, the partition CTAs that do not fit on
+    // the SMs its CTAs hold (per_sm per such SM, the last ones dispatched)
+    // start only when those CTAs end: they skip the first round of units.
+    DecodeParams dp = prm;
+    dp.early_ctas = (int)grid;
+    dp.early_rounds = 0;
+    if (prm.concurrent && prm.prefix_sms > 0 && prm.prefix_sms < sms) {
+        const long long late = std::min<long long>(grid, (long long)per_sm * prm.prefix_sms);
+        dp.early_ctas = (int)(grid - late);
+        dp.early_rounds = dp.early_ctas > 0 ? 1 : 0;
+    }
+    return launch_pdl(kernel, dim3((unsigned)grid), dim3(kThreads), smem, stream, dp, mk, mv);
 }
 
 // The partition pass, then (prefix-aware decode) the shared-prefix pass, then
@@ -1326,6 +1344,12 @@ static pa_status run_cascade(void *out, const void *query, void *key_cache, void
     prm.part_l = reinterpret_cast<float *>(ws + wl.l_off);
     prm.part_o = reinterpret_cast<float *>(ws + wl.o_off);
     prm.max_parts = parts;
+    // SMs the shared-prefix pass holds, taken as one CTA per SM for each of
+    // its units with one partition of the prefix per group (its CTAs without
+    // a unit end at once)
+    prm.prefix_sms = (int)std::min<long long>(
+        ((long long)num_members * prm.group + 127LL * num_groups) / 128 * num_kv_heads,
+        1 << 30);
     prm.counters = reinterpret_cast<int32_t *>(ws + wl.cnt_off);
     prm.seq_start = prefix_plan;
 

@@ -50,6 +50,11 @@ struct DecodeParams {
     int max_parts;    // partitions per sequence the workspace holds
     float scale_log2; // scale * log2(e) (times the K scale for FP8 pools)
     float out_scale;  // applied to the attention output (the V scale for FP8 pools)
+    // Deal: the first early_rounds rounds go to CTAs [0, early_ctas) alone (the
+    // others start late, behind the shared-prefix pass's CTAs), then every
+    // CTA takes one unit per round.
+    int early_ctas, early_rounds;
+    int prefix_sms;   // SMs the shared-prefix pass is expected to hold (0: none)
     int concurrent;   // 1: the kernel before it on the stream (the shared-prefix
                       // pass) writes nothing this pass reads -- run alongside it
                       // and wait for it only before finishing

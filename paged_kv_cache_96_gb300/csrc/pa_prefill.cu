@@ -107,6 +107,16 @@ constexpr int kTcSubs = kTcTokens / kTileTokens;
 constexpr int kTcStages = 2;
 constexpr uint32_t kTmemCols = 256;  // S/P buffers at columns 0 and 64, O at column 128
 constexpr uint32_t kTmemO = 128;
+// Prefill batches whose units may take more than one round of the grid:
+// segments (up to kMqOrderSegs of them) are numbered by their longest unit's
+// key tiles, most first (a counting sort over kMqOrderBuckets buckets, stable
+// by index), each segment's row tiles last-first, and the ranks are dealt
+// boustrophedon (round r: CTA b takes rank r * grid + b, or r * grid + grid -
+// 1 - b for odd r), so that a CTA that drew a long unit in one round draws a
+// short one in the next.  The shared-prefix pass keeps the natural order and
+// the round-robin deal.
+constexpr int kMqOrderBuckets = 64;
+constexpr int kMqOrderSegs = 512;
 
 template <int D, bool kFp8> struct TcLayout {
     static constexpr int kHalves = D / 64;                    // 128-byte rows of 64 elements
@@ -124,8 +134,14 @@ template <int D, bool kFp8> struct TcLayout {
     static constexpr int kBars = kCodes + kCodesBytes;        // 16 mbarriers
     static constexpr int kTmemSlot = kBars + 16 * 8;
     static constexpr int kAbort = kTmemSlot + 8;
-    static constexpr int kSeg = kTmemSlot + 16;               // int unit prefix[n + 1]
-    static size_t bytes(int segments) { return 1024 + kSeg + 4 * ((size_t)segments + 1); }
+    // int unit prefix[n + 1], then (ordered) order[n], units[n], key[n] and
+    // the sort's buckets
+    static constexpr int kSeg = kTmemSlot + 16;
+    static size_t bytes(int segments, bool ordered)
+    {
+        return 1024 + kSeg + 4 * ((size_t)segments + 1) +
+               (ordered ? 4 * (3 * (size_t)segments + kMqOrderBuckets) : 0);
+    }
     static_assert(kStageBytes % 1024 == 0 && kQ % 1024 == 0, "1024-byte aligned operands");
 };
 
@@ -170,7 +186,7 @@ __device__ __forceinline__ int mq_segment_units(const MqParams &p, int seg)
 // then release the stage; the products run in fp16 with the query rounded to
 // fp16, the K scale folded into the exponent's scale and the V scale into
 // the output.
-template <typename T, int D, bool kFp8>
+template <typename T, int D, bool kFp8, bool kOrdered>
 __global__ void __launch_bounds__(kTcThreads, 2)
     paged_mq_kernel(const __grid_constant__ MqParams p,
                     const __grid_constant__ CUtensorMap tmap_k,
@@ -274,11 +290,63 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + L::kTmemSlot);
 
     // ---- work units per segment and their prefix sums -------------------------------
+    int *order = pref + nseg + 1;  // k-th segment of the unit order (kOrdered)
+    int *seg_units = order + nseg;
     if (warp == 0) {
+        if constexpr (kOrdered) {
+            // counting sort by the key tiles of the segment's last row tile
+            // (its context), most first, by index within a count; every CTA
+            // computes the same order.  Each segment's loads are issued once.
+            int *seg_key = seg_units + nseg;
+            int *hist = seg_key + nseg;
+            hist[lane] = 0;
+            hist[lane + 32] = 0;
+            __syncwarp();
+            for (int sg = lane; sg < nseg; sg += 32) {
+                const int tiles = (clamp_context_mq(p, sg) + kTcTokens - 1) / kTcTokens;
+                const int key = kMqOrderBuckets - 1 - min(tiles, kMqOrderBuckets - 1);
+                seg_units[sg] = mq_segment_units(p, sg);
+                seg_key[sg] = key;
+                atomicAdd(&hist[key], 1);
+            }
+            __syncwarp();
+            const int c0 = hist[2 * lane], c1 = hist[2 * lane + 1];
+            int x = c0 + c1;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(kFull, x, o);
+                if (lane >= o)
+                    x += y;
+            }
+            __syncwarp();
+            hist[2 * lane] = x - c0 - c1;  // first place of each count
+            hist[2 * lane + 1] = x - c1;
+            __syncwarp();
+            for (int base = 0; base < nseg; base += 32) {
+                const int sg = base + lane;
+                const int key = sg < nseg ? seg_key[sg] : -1;
+                const unsigned same = __match_any_sync(kFull, key);
+                const int rank = __popc(same & ((1u << lane) - 1u));
+                const int off = key >= 0 ? hist[key] : 0;
+                __syncwarp();
+                if (key >= 0) {
+                    order[off + rank] = sg;
+                    if (rank == 0)
+                        hist[key] = off + __popc(same);
+                }
+                __syncwarp();
+            }
+        }
         int carry = 0;
         for (int base = 0; base < nseg; base += 32) {
-            const int sg = base + lane;
-            const int n = sg < nseg ? mq_segment_units(p, sg) : 0;
+            const int k = base + lane;
+            int n = 0;
+            if (k < nseg) {
+                if constexpr (kOrdered)
+                    n = seg_units[order[k]];
+                else
+                    n = mq_segment_units(p, k);
+            }
             int x = n;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
@@ -286,8 +354,8 @@ __global__ void __launch_bounds__(kTcThreads, 2)
                 if (lane >= o)
                     x += y;
             }
-            if (sg < nseg)
-                pref[sg] = carry + x - n;
+            if (k < nseg)
+                pref[k] = carry + x - n;
             carry += __shfl_sync(kFull, x, 31);
         }
         if (lane == 0)
@@ -295,6 +363,16 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     }
     __syncthreads();
     const int total_units = pref[nseg] * Hkv;
+    // this CTA's unit after unit u in the deal (its first unit is blockIdx.x)
+    auto next_unit = [&](int u) -> int {
+        const int grid = gridDim.x;
+        if constexpr (kOrdered) {
+            const int r = u / grid + 1;  // the next round
+            return r * grid + ((r & 1) ? grid - 1 - (int)blockIdx.x : (int)blockIdx.x);
+        } else {
+            return u + grid;
+        }
+    };
 
     // ---- unit -> (segment, KV head, row tile, prefix partition, key range) -------------
     // Every role walks the same units in the same order and counts the same
@@ -316,10 +394,11 @@ __global__ void __launch_bounds__(kTcThreads, 2)
             else
                 hi = mid - 1;
         }
-        w.seg = lo;
+        w.seg = kOrdered ? order[lo] : lo;
         w.count = mq_segment_count(p, w.seg);
         const int tiles = (w.count * G + kTcRows - 1) / kTcRows;
-        const int idx = q - pref[w.seg];
+        // ordered: the segment's row tiles last-first
+        const int idx = kOrdered ? pref[lo + 1] - 1 - q : q - pref[lo];
         w.rt = idx % tiles;    // row tile
         w.part = idx / tiles;  // prefix partition (0 for prefill)
         w.nrows = min(kTcRows, w.count * G - w.rt * kTcRows);
@@ -461,7 +540,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         // tensor-core warp moves on.
         int ntiles_cta = 0;  // tiles of this CTA, over all its units
         if constexpr (kFp8) {
-            for (int u = blockIdx.x; u < total_units; u += gridDim.x) {
+            for (int u = blockIdx.x; u < total_units; u = next_unit(u)) {
                 Unit x;
                 decode(u, x);
                 ntiles_cta += x.n;
@@ -517,15 +596,16 @@ __global__ void __launch_bounds__(kTcThreads, 2)
             if (ntiles_cta > 0)
                 ok = widen_k(0);
         }
-        for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x) {
+        for (int u = blockIdx.x; u < total_units && ok; u = next_unit(u)) {
             const long long ooff = rw.ooff;
             const int lim = rw.lim;
-            const bool has_next = u + (int)gridDim.x < total_units;
+            const int u_next = next_unit(u);
+            const bool has_next = u_next < total_units;
             if (has_next) {
                 // the next unit's query rows, pulled into L2 while this unit runs
                 Unit wn;
                 Row rn;
-                decode(u + gridDim.x, wn);
+                decode(u_next, wn);
                 row_of(wn, rn, false);
                 prefetch_q(wn, rn);
             }
@@ -643,7 +723,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
             Unit wn;
             Row rn;
             if (has_next) {
-                decode(u + gridDim.x, wn);
+                decode(u_next, wn);
                 row_of(wn, rn, true);
                 write_q(wn, rn);
             } else {
@@ -751,7 +831,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         uint32_t g = 0;
         int last0 = -1, last1 = -1;  // last fill per stage
         bool ok = true;
-        for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x) {
+        for (int u = blockIdx.x; u < total_units && ok; u = next_unit(u)) {
             Unit w;
             decode(u, w);
             auto lookup = [&](int si) {
@@ -923,7 +1003,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
             }
             return true;
         };
-        for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x) {
+        for (int u = blockIdx.x; u < total_units && ok; u = next_unit(u)) {
             Unit w;
             decode(u, w);
             if (w.n == 0)
@@ -982,15 +1062,15 @@ __global__ void __launch_bounds__(kTcThreads, 2)
 
 // ---- host side -------------------------------------------------------------------
 
-template <typename T, int D, bool kFp8>
-static pa_status launch_mq(const MqParams &prm, const CUtensorMap &mk, const CUtensorMap &mv,
-                           cudaStream_t stream, long long max_units)
+template <typename T, int D, bool kFp8, bool kOrdered>
+static pa_status launch_mq_as(const MqParams &prm, const CUtensorMap &mk, const CUtensorMap &mv,
+                              cudaStream_t stream, long long max_units)
 {
     using L = TcLayout<D, kFp8>;
-    auto kernel = paged_mq_kernel<T, D, kFp8>;
+    auto kernel = paged_mq_kernel<T, D, kFp8, kOrdered>;
     static KernelSetting setting[kMaxDevices];
     static std::mutex mu;
-    const size_t smem = L::bytes(prm.num_segments);
+    const size_t smem = L::bytes(prm.num_segments, kOrdered);
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess)
@@ -1048,6 +1128,28 @@ static pa_status launch_mq(const MqParams &prm, const CUtensorMap &mk, const CUt
         grid = 1;
     return launch_pdl(kernel, dim3((unsigned)grid), dim3(kTcThreads), smem, stream, prm, mk,
                       mv);
+}
+
+// Prefill batches of up to kMqOrderSegs sequences whose units may take more
+// than one round of the grid (two CTAs per SM) take the ordered deal; in a
+// single round the order cannot matter and the sort would only add latency.
+template <typename T, int D, bool kFp8>
+static pa_status launch_mq(const MqParams &prm, const CUtensorMap &mk, const CUtensorMap &mv,
+                           cudaStream_t stream, long long max_units)
+{
+    if (!prm.prefix_mode && prm.num_segments <= kMqOrderSegs) {
+        int dev = 0;
+        const cudaError_t e = cudaGetDevice(&dev);
+        if (e != cudaSuccess)
+            return record_cuda(e);
+        DeviceInfo info;
+        const pa_status st = device_info(dev, &info);
+        if (st != PA_OK)
+            return st;
+        if (max_units > 2LL * info.sms)
+            return launch_mq_as<T, D, kFp8, true>(prm, mk, mv, stream, max_units);
+    }
+    return launch_mq_as<T, D, kFp8, false>(prm, mk, mv, stream, max_units);
 }
 
 // pool_dtype PA_FP8_E4M3: e4m3 pools, query and output of

@@ -332,3 +332,34 @@ def test_fp8_query_beyond_fp16_range_is_flagged(B, S, small):
     st.attention()
     torch.cuda.synchronize()
     assert int(st.error_word.item()) & B.DEVERR_QUERY_RANGE
+
+
+
+@pytest.mark.parametrize("P", [128, 0])
+def test_fp8_query_heads_far_apart_in_magnitude(B, S, small, P):
+    """FP8 pools with bf16 queries, every head's row scaled by its own power
+    of two from 2^-30 to 2^12 (rows below the fp16 range vanish in fp16, as
+    their scores do in the oracle's softmax), and one row whose elements
+    span 2^-14 .. 2^0 of its largest: the decode matches the oracle."""
+    w, ref = small("gqa70b-fp8")
+    st = S.DecodeStep(w, partition_size=w.spec.partition_size)
+    st.run()
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(96)
+    ex = torch.tensor(rng.integers(-30, 13, size=(w.S, w.H)), dtype=torch.float32)
+    q = (st.query.float() * torch.exp2(ex).to("cuda")[..., None]).to(torch.bfloat16)
+    row = q[0, 5].float()
+    spread = torch.exp2(-(torch.arange(w.D, device="cuda", dtype=torch.float32) % 15))
+    q[0, 5] = (row * spread).to(torch.bfloat16)
+    out = torch.full_like(st.out, float("nan"))
+    ws = B.alloc_workspace(w.S, w.H, w.Hkv, w.D, st.max_context_len, P, device=st.device)
+    B.pa_decode_attention_fp8(out, q, st.key_cache, st.value_cache, st.step_block_tables,
+                              st.context_lens, st.max_context_len, w.scale, st.kv_scale,
+                              st.kv_scale, P, ws, error_word=st.error_word)
+    torch.cuda.synchronize()
+    assert int(st.error_word.item()) == 0
+    qbits = q.view(torch.int16).cpu().numpy().view(np.uint16)
+    want = oracle.paged_attention_fp8(qbits, ref.key_cache, ref.value_cache,
+                                      w.step_block_tables, w.context_lens, w.scale, odt(w),
+                                      w.spec.kv_scale, w.spec.kv_scale)
+    assert_attention_close(S.to_float(out), want, f"fp8 heads 2^-30..2^12 P={P}")

@@ -2,6 +2,8 @@
 GPU against the CPU oracle: slots and pools bit-exact; attention within the
 contract tolerance on every row; invariants; plan and index errors flagged
 on the device without a fault."""
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -95,6 +97,40 @@ def test_prefill_block_placement_invariance(B, S, small, name):
                            st.max_context_len, w.scale, k_scale=st.kv_scale,
                            v_scale=st.kv_scale)
     assert torch.equal(a, b)
+
+
+def _many_segments(n, qmax, cmax, fp8):
+    """A prefill batch of n sequences (16 query heads over 2 KV heads, d 128)
+    with unsorted and tied contexts, a fifth of them single-token rows, and
+    two single-token rows past 64 key tiles (the deal's last sort bucket);
+    more row-tile units than one round of CTAs takes."""
+    rng = np.random.default_rng(9700 + n)
+    q = rng.integers(1, qmax, size=n)
+    q[::5] = 1
+    ctx = q + rng.integers(0, cmax, size=n)
+    q[3], ctx[3] = 1, 4500
+    q[8], ctx[8] = 1, 4100
+    spec = dataclasses.replace(W.CONFIGS["chunked"], name=f"chunked-{n}seg", seed=9700 + n,
+                               num_seqs=n, num_heads=16, num_kv_heads=2,
+                               context_lens=lambda r, c=ctx: c.copy(),
+                               query_lens=lambda r, c, qq=q: qq.copy())
+    return W.fp8_variant(spec) if fp8 else spec
+
+
+@pytest.mark.parametrize("n,qmax,cmax,fp8", [(56, 160, 500, False), (56, 160, 500, True),
+                                             (520, 3, 100, False)],
+                         ids=["56seg", "56seg-fp8", "520seg"])
+def test_prefill_many_segments(B, S, n, qmax, cmax, fp8):
+    """Segments numbered longest context first and dealt boustrophedon over
+    more than one round (56 sequences, 500 units); past 512 sequences the
+    natural order and round-robin deal (520 sequences, 1,040 units)."""
+    w = W.build(_many_segments(n, qmax, cmax, fp8))
+    ref = OracleStep(w)
+    st = S.DecodeStep(w)
+    out = st.run()
+    torch.cuda.synchronize()
+    assert int(st.error_word.item()) == 0
+    assert_attention_close(S.to_float(out), ref.attention(), w.spec.name)
 
 
 def test_prefill_fp8_query_beyond_fp16_is_flagged(B, S, small):
