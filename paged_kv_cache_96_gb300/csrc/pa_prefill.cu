@@ -49,6 +49,8 @@
 
 #include <algorithm>
 #include <cmath>
+#include <cstdint>
+#include <cstring>
 #include <mutex>
 
 #include "pa_decode_common.cuh"
@@ -145,6 +147,17 @@ template <int D, bool kFp8> struct TcLayout {
     static_assert(kStageBytes % 1024 == 0 && kQ % 1024 == 0, "1024-byte aligned operands");
 };
 
+// 3-D tiled bulk tensor load global -> shared, completion on an mbarrier.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *tmap, uint32_t bar,
+                                            int c0, int c1, int c2)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+}
+
 // Context length of a chunked-prefill sequence, clamped like the decode pass.
 __device__ __forceinline__ int clamp_context_mq(const MqParams &p, int s)
 {
@@ -190,7 +203,8 @@ template <typename T, int D, bool kFp8, bool kOrdered>
 __global__ void __launch_bounds__(kTcThreads, 2)
     paged_mq_kernel(const __grid_constant__ MqParams p,
                     const __grid_constant__ CUtensorMap tmap_k,
-                    const __grid_constant__ CUtensorMap tmap_v)
+                    const __grid_constant__ CUtensorMap tmap_v,
+                    const __grid_constant__ CUtensorMap tmap_q)
 {
     using L = TcLayout<D, kFp8>;
     static_assert(D == 64 || D == 128, "head_dim 64 or 128");
@@ -263,12 +277,15 @@ __global__ void __launch_bounds__(kTcThreads, 2)
             mbar_init(kland(st), 1);
             mbar_init(vland(st), 1);
         }
-        mbar_init(qfull, kRowWarps);
+        // the query tile: written by the 4 row warps, or one TMA transaction
+        mbar_init(qfull, p.q_tma ? 1 : kRowWarps);
         mbar_init(mma_drain, 1);
         *abort_flag = 0;
         fence_barrier_init();
         prefetch_tensormap(&tmap_k);
         prefetch_tensormap(&tmap_v);
+        if (p.q_tma)
+            prefetch_tensormap(&tmap_q);
     }
     // Everything from here on comes after the kernel before this one on the
     // stream has finished -- including an earlier launch of this kernel, so
@@ -590,7 +607,8 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         if ((int)blockIdx.x < total_units) {
             decode(blockIdx.x, w);
             row_of(w, rw, true);
-            write_q(w, rw);
+            if (!p.q_tma)  // (else the tensor-core warp brings it by TMA)
+                write_q(w, rw);
         }
         if constexpr (kFp8) {
             if (ntiles_cta > 0)
@@ -718,14 +736,16 @@ __global__ void __launch_bounds__(kTcThreads, 2)
                     break;
             }
             // every S of this unit has finished: the next unit's query rows go
-            // into shared memory now, so its first S can run during this unit's
-            // last value product and epilogue
+            // into shared memory now (unless the tensor-core warp brings them
+            // by TMA), so its first S can run during this unit's last value
+            // product and epilogue
             Unit wn;
             Row rn;
             if (has_next) {
                 decode(u_next, wn);
                 row_of(wn, rn, true);
-                write_q(wn, rn);
+                if (!p.q_tma)
+                    write_q(wn, rn);
             } else {
                 wn.n = 0;
                 rn.qoff = rn.ooff = -1;
@@ -743,6 +763,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
 
             // epilogue: this thread's row of O / l (TMEM loads are warp-wide)
             const float inv = (w.n > 0 && l_run > 0.f) ? p.out_scale / l_run : 0.f;
+            const bool out32 = (reinterpret_cast<uintptr_t>(p.out) & 31) == 0;
             if (p.prefix_mode && ooff >= 0) {
                 p.part_m[ooff] = m_ref * kLn2;
                 p.part_l[ooff] = l_run;
@@ -767,6 +788,23 @@ __global__ void __launch_bounds__(kTcThreads, 2)
                                              __uint_as_float(r[4 * i + 1]) * inv,
                                              __uint_as_float(r[4 * i + 2]) * inv,
                                              __uint_as_float(r[4 * i + 3]) * inv);
+                } else if (out32) {
+                    // 32-byte stores: half the store instructions of 16-byte ones
+                    // for the row's 256-byte run (rows sit 256 bytes apart)
+                    T *dst = static_cast<T *>(p.out) + ooff + c * 64;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        uint32_t v[8];
+#pragma unroll
+                        for (int k = 0; k < 8; ++k)
+                            v[k] = MmaOp<T>::pack(__uint_as_float(r[16 * i + 2 * k]) * inv,
+                                                  __uint_as_float(r[16 * i + 2 * k + 1]) * inv);
+                        asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(
+                                         dst + 16 * i),
+                                     "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]),
+                                     "r"(v[5]), "r"(v[6]), "r"(v[7])
+                                     : "memory");
+                    }
                 } else {
                     uint4 *dst =
                         reinterpret_cast<uint4 *>(static_cast<T *>(p.out) + ooff) + c * 8;
@@ -1008,6 +1046,20 @@ __global__ void __launch_bounds__(kTcThreads, 2)
             decode(u, w);
             if (w.n == 0)
                 continue;
+            // q_tma: this unit's query tile by TMA -- per d-half one box of 64
+            // elements x G heads x 128 / G tokens, rows in (token, head) order
+            // as the row tile numbers them, landing in the 128-byte swizzled
+            // K-major layout; rows past the segment read the next rows (or
+            // zero past T), whose keys are all masked.  Every S of the unit
+            // before has finished: its last value product, issued above,
+            // waited for the P of its last S.
+            if (p.q_tma && lane == 0) {
+                const int tok0 = p.query_start[w.seg] + w.rt * (kTcRows / G);
+                mbar_arrive_expect_tx(qfull, L::kHalves * L::kQHalf);
+#pragma unroll
+                for (int h = 0; h < L::kHalves; ++h)
+                    tma_load_3d(qbase + h * L::kQHalf, &tmap_q, qfull, 64 * h, w.kh * G, tok0);
+            }
             ok = wait(qfull, nq & 1);  // this unit's queries; O read out by the last unit
             ++nq;
             if (!ok)
@@ -1064,7 +1116,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
 
 template <typename T, int D, bool kFp8, bool kOrdered>
 static pa_status launch_mq_as(const MqParams &prm, const CUtensorMap &mk, const CUtensorMap &mv,
-                              cudaStream_t stream, long long max_units)
+                              const CUtensorMap &mq, cudaStream_t stream, long long max_units)
 {
     using L = TcLayout<D, kFp8>;
     auto kernel = paged_mq_kernel<T, D, kFp8, kOrdered>;
@@ -1127,17 +1179,22 @@ static pa_status launch_mq_as(const MqParams &prm, const CUtensorMap &mk, const 
     if (grid < 1)
         grid = 1;
     return launch_pdl(kernel, dim3((unsigned)grid), dim3(kTcThreads), smem, stream, prm, mk,
-                      mv);
+                      mv, mq);
 }
 
-// Prefill batches of up to kMqOrderSegs sequences whose units may take more
-// than one round of the grid (two CTAs per SM) take the ordered deal; in a
-// single round the order cannot matter and the sort would only add latency.
+// Prefill batches whose units may take more than one round of the grid (two
+// CTAs per SM) take the query tiles by TMA (when the query map applies), and
+// those of up to kMqOrderSegs sequences the ordered deal.  In a single round
+// the order cannot matter and the sort would only add latency, and each
+// CTA's one query tile comes sooner from the row warps' own loads than
+// through the table lookup and round trip of a TMA issued by the
+// tensor-core warp.
 template <typename T, int D, bool kFp8>
-static pa_status launch_mq(const MqParams &prm, const CUtensorMap &mk, const CUtensorMap &mv,
-                           cudaStream_t stream, long long max_units)
+static pa_status launch_mq(const MqParams &prm_in, const CUtensorMap &mk, const CUtensorMap &mv,
+                           const CUtensorMap &mq, cudaStream_t stream, long long max_units)
 {
-    if (!prm.prefix_mode && prm.num_segments <= kMqOrderSegs) {
+    MqParams prm = prm_in;
+    if (!prm.prefix_mode) {
         int dev = 0;
         const cudaError_t e = cudaGetDevice(&dev);
         if (e != cudaSuccess)
@@ -1146,38 +1203,76 @@ static pa_status launch_mq(const MqParams &prm, const CUtensorMap &mk, const CUt
         const pa_status st = device_info(dev, &info);
         if (st != PA_OK)
             return st;
-        if (max_units > 2LL * info.sms)
-            return launch_mq_as<T, D, kFp8, true>(prm, mk, mv, stream, max_units);
+        const bool rounds = max_units > 2LL * info.sms;
+        if (!rounds)
+            prm.q_tma = 0;
+        if (rounds && prm.num_segments <= kMqOrderSegs)
+            return launch_mq_as<T, D, kFp8, true>(prm, mk, mv, mq, stream, max_units);
     }
-    return launch_mq_as<T, D, kFp8, false>(prm, mk, mv, stream, max_units);
+    return launch_mq_as<T, D, kFp8, false>(prm, mk, mv, mq, stream, max_units);
+}
+
+// Tensor map of a prefill query [T][H][D] (16-bit): boxes of 64 elements x
+// group heads x 128 / group tokens, 128-byte swizzle, zero fill past T.
+static bool encode_query_map(CUtensorMap *map, const void *query, pa_dtype dtype, int tokens,
+                             int heads, int head_dim, int group)
+{
+    EncodeTiledFn fn = get_encode_fn();
+    if (!fn)
+        return false;
+    const CUtensorMapDataType ty = dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                    : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    const cuuint64_t dims[3] = {(cuuint64_t)head_dim, (cuuint64_t)heads, (cuuint64_t)tokens};
+    const cuuint64_t strides[2] = {(cuuint64_t)head_dim * 2, (cuuint64_t)heads * head_dim * 2};
+    const cuuint32_t box[3] = {64u, (cuuint32_t)group, (cuuint32_t)(kTcRows / group)};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return fn(map, ty, 3, const_cast<void *>(query), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // pool_dtype PA_FP8_E4M3: e4m3 pools, query and output of
 // query_dtype; otherwise 16-bit pools and query of pool_dtype.
-static pa_status dispatch_mq(const MqParams &prm, pa_dtype pool_dtype, pa_dtype query_dtype,
+static pa_status dispatch_mq(const MqParams &prm_in, pa_dtype pool_dtype, pa_dtype query_dtype,
                              const void *key_cache, const void *value_cache, int head_dim,
                              cudaStream_t stream, long long max_units)
 {
-    CUtensorMap mk, mv;
-    if (!encode_pool_map(&mk, key_cache, pool_dtype, prm.num_blocks, prm.block_size,
-                         prm.num_kv_heads, head_dim) ||
-        !encode_pool_map(&mv, value_cache, pool_dtype, prm.num_blocks, prm.block_size,
-                         prm.num_kv_heads, head_dim))
+    CUtensorMap mk, mv, mq;
+    if (!encode_pool_map(&mk, key_cache, pool_dtype, prm_in.num_blocks, prm_in.block_size,
+                         prm_in.num_kv_heads, head_dim) ||
+        !encode_pool_map(&mv, value_cache, pool_dtype, prm_in.num_blocks, prm_in.block_size,
+                         prm_in.num_kv_heads, head_dim))
         return PA_ERR_CUDA;
+    // Prefill over 16-bit pools with row tiles of whole tokens (the group
+    // divides 128) and a 16-byte aligned query: the query tiles may arrive by
+    // TMA (launch_mq keeps that for batches of more than one round).
+    MqParams prm = prm_in;
+    std::memset(&mq, 0, sizeof(mq));
+    prm.q_tma = 0;
+    if (!prm.prefix_mode && pool_dtype != PA_FP8_E4M3 && prm.group > 0 &&
+        kTcRows % prm.group == 0 && prm.num_tokens > 0 &&
+        (reinterpret_cast<uintptr_t>(prm.query) & 15) == 0) {
+        if (!encode_query_map(&mq, prm.query, pool_dtype, prm.num_tokens, prm.num_heads,
+                              head_dim, prm.group))
+            return PA_ERR_CUDA;
+        prm.q_tma = 1;
+    }
     using B16 = __nv_bfloat16;
     if (pool_dtype == PA_FP8_E4M3) {
         const bool qbf = query_dtype == PA_BF16;
         if (head_dim == 128)
-            return qbf ? launch_mq<B16, 128, true>(prm, mk, mv, stream, max_units)
-                       : launch_mq<__half, 128, true>(prm, mk, mv, stream, max_units);
-        return qbf ? launch_mq<B16, 64, true>(prm, mk, mv, stream, max_units)
-                   : launch_mq<__half, 64, true>(prm, mk, mv, stream, max_units);
+            return qbf ? launch_mq<B16, 128, true>(prm, mk, mv, mq, stream, max_units)
+                       : launch_mq<__half, 128, true>(prm, mk, mv, mq, stream, max_units);
+        return qbf ? launch_mq<B16, 64, true>(prm, mk, mv, mq, stream, max_units)
+                   : launch_mq<__half, 64, true>(prm, mk, mv, mq, stream, max_units);
     }
     if (head_dim == 128)
-        return pool_dtype == PA_BF16 ? launch_mq<B16, 128, false>(prm, mk, mv, stream, max_units)
-                                     : launch_mq<__half, 128, false>(prm, mk, mv, stream, max_units);
-    return pool_dtype == PA_BF16 ? launch_mq<B16, 64, false>(prm, mk, mv, stream, max_units)
-                                 : launch_mq<__half, 64, false>(prm, mk, mv, stream, max_units);
+        return pool_dtype == PA_BF16
+                   ? launch_mq<B16, 128, false>(prm, mk, mv, mq, stream, max_units)
+                   : launch_mq<__half, 128, false>(prm, mk, mv, mq, stream, max_units);
+    return pool_dtype == PA_BF16 ? launch_mq<B16, 64, false>(prm, mk, mv, mq, stream, max_units)
+                                 : launch_mq<__half, 64, false>(prm, mk, mv, mq, stream, max_units);
 }
 
 pa_status launch_prefix_pass(const MqParams &prm, pa_dtype dtype, pa_dtype query_dtype,
@@ -1250,6 +1345,7 @@ static pa_status run_prefill(void *out, const void *query, const void *key_cache
     prm.part_tokens = 0;
     prm.scale_log2 = scale * (fp8 ? k_scale : 1.f) * kLog2e;
     prm.out_scale = fp8 ? v_scale : 1.f;
+    prm.num_tokens = num_tokens;
     // row tiles: at most one partial tile per sequence beyond the full ones
     const long long max_units =
         ((long long)num_tokens * group / kTcRows + num_seqs) * num_kv_heads;

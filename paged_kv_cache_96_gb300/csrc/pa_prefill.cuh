@@ -34,6 +34,8 @@ struct MqParams {
     int part_tokens;   // prefix pass: tokens per prefix partition (partial j)
     float scale_log2;  // scale * log2(e) (times the K scale for FP8 pools)
     float out_scale;   // applied to the output / partials (the V scale for FP8 pools)
+    int num_tokens;    // prefill: rows of query and out (T)
+    int q_tma;         // 1: each unit's query tile arrives by TMA (the query map)
 };
 
 // Queue the shared-prefix pass on `stream` as a programmatic dependent of the

@@ -133,6 +133,51 @@ def test_prefill_many_segments(B, S, n, qmax, cmax, fp8):
     assert_attention_close(S.to_float(out), ref.attention(), w.spec.name)
 
 
+@pytest.mark.parametrize("name", ["chunked", "mixed"])
+def test_prefill_output_alignment_paths(B, S, small, name):
+    """The output goes out in 32-byte stores when it is 32-byte aligned and
+    in 16-byte stores otherwise; the query tiles come by TMA from any
+    16-byte aligned query (chunked: more units than one round of CTAs) or
+    from the row warps' loads (mixed, one round): every combination gives
+    the same bits, and a query off the 16-byte grid is refused on the host
+    (nothing is launched)."""
+    w, _ = small(name)
+    st = S.DecodeStep(w)
+    ref = st.run().clone()
+    for q_shift, o_shift in [(8, 0), (0, 8), (8, 8)]:  # elements of 2 bytes
+        qbuf = torch.empty(st.query.numel() + 16, dtype=st.query.dtype, device="cuda")
+        obuf = torch.full((st.out.numel() + 16,), float("nan"), dtype=st.out.dtype, device="cuda")
+        q = qbuf[q_shift:q_shift + st.query.numel()].view(st.query.shape)
+        o = obuf[o_shift:o_shift + st.out.numel()].view(st.out.shape)
+        q.copy_(st.query)
+        B.pa_prefill_attention(o, q, st.key_cache, st.value_cache, st.step_block_tables,
+                               st.query_start, st.context_lens, st.max_context_len, w.scale,
+                               error_word=st.error_word)
+        torch.cuda.synchronize()
+        assert int(st.error_word.item()) == 0
+        assert torch.equal(o, ref), (q_shift, o_shift)
+    q = qbuf[4:4 + st.query.numel()].view(st.query.shape)
+    with pytest.raises(B.PAError) as e:
+        B.pa_prefill_attention(st.out, q, st.key_cache, st.value_cache, st.step_block_tables,
+                               st.query_start, st.context_lens, st.max_context_len, w.scale)
+    assert e.value.status == B.PA_ERR_INVALID_ARG
+
+
+def test_prefill_group_not_dividing_row_tile(B, S):
+    """12 query heads over 2 KV heads: a group of 6 does not divide the
+    128-row tile, so the row warps write the query tiles (rows of a tile
+    straddle tokens) -- against the oracle."""
+    spec = dataclasses.replace(W.small_variant("chunked"), name="chunked-g6", num_heads=12,
+                               num_kv_heads=2)
+    w = W.build(spec)
+    ref = OracleStep(w)
+    st = S.DecodeStep(w)
+    out = st.run()
+    torch.cuda.synchronize()
+    assert int(st.error_word.item()) == 0
+    assert_attention_close(S.to_float(out), ref.attention(), "chunked, group 6")
+
+
 def test_prefill_fp8_query_beyond_fp16_is_flagged(B, S, small):
     """The FP8 prefill rounds the query to fp16 for the tensor-core tiles: a
     bf16 query element beyond the fp16 range is flagged, not silently
