@@ -178,6 +178,31 @@ def test_prefill_group_not_dividing_row_tile(B, S):
     assert_attention_close(S.to_float(out), ref.attention(), "chunked, group 6")
 
 
+@pytest.mark.parametrize("H,Hkv,counts,extra", [
+    (4, 4, [1300] * 8, 300),
+    (4, 2, [1250] * 8, 300),
+    (32, 2, [160, 200, 240, 180, 220, 260, 150, 190], 400)], ids=["group1", "group2", "group16"])
+def test_prefill_query_tiles_by_tma_groups(B, S, H, Hkv, counts, extra):
+    """More units than one round of CTAs, so the query tiles arrive by TMA as
+    boxes of 64 elements x G heads x 128 / G tokens: groups 1, 2 and 16
+    (boxes of 128 tokens x 1 head down to 8 tokens x 16 heads), most chunks
+    ending in a partial row tile, against the oracle on every row."""
+    from stepping import attention_all
+    rng = np.random.default_rng(9800 + H)
+    q = np.array(counts)
+    ctx = q + rng.integers(0, extra, size=len(q))
+    spec = dataclasses.replace(W.small_variant("chunked"), name=f"chunked-g{H // Hkv}",
+                               seed=9800 + H, num_seqs=len(q), num_heads=H, num_kv_heads=Hkv,
+                               context_lens=lambda r, c=ctx: c.copy(),
+                               query_lens=lambda r, c, qq=q: qq.copy())
+    w = W.build(spec)
+    st = S.DecodeStep(w)
+    out = st.run()
+    torch.cuda.synchronize()
+    assert int(st.error_word.item()) == 0
+    assert_attention_close(S.to_float(out), attention_all(OracleStep(w)), spec.name)
+
+
 def test_prefill_fp8_query_beyond_fp16_is_flagged(B, S, small):
     """The FP8 prefill rounds the query to fp16 for the tensor-core tiles: a
     bf16 query element beyond the fp16 range is flagged, not silently
