@@ -133,8 +133,8 @@ template <int D, bool kFp8> struct TcLayout {
     static constexpr int kCodeTile = kTcTokens * D;
     static constexpr int kCodes = kQ + kHalves * kQHalf;
     static constexpr int kCodesBytes = (kFp8 && D == 64) ? kTcStages * 2 * kCodeTile : 0;
-    static constexpr int kBars = kCodes + kCodesBytes;        // 16 mbarriers
-    static constexpr int kTmemSlot = kBars + 16 * 8;
+    static constexpr int kBars = kCodes + kCodesBytes;        // 17 mbarriers
+    static constexpr int kTmemSlot = kBars + 17 * 8;
     static constexpr int kAbort = kTmemSlot + 8;
     // int unit prefix[n + 1], then (ordered) order[n], units[n], key[n] and
     // the sort's buckets
@@ -236,6 +236,11 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     // FP8 pools: the codes of K / V stage st landed (before widening)
     auto kland = [&](int st) { return bar(12 + st); };
     auto vland = [&](int st) { return bar(14 + st); };
+    // FP8 pools, bf16 queries, query tiles by TMA: the bf16 tile landed (the
+    // row warps then round it to fp16 in place and arrive on qfull)
+    constexpr bool kConvQ = kFp8 && std::is_same<T, __nv_bfloat16>::value;
+    const uint32_t qland = bar(16);
+    const uint32_t qtma_bar = kConvQ ? qland : qfull;
     auto kbase = [&](int st) { return sbase + st * L::kStageBytes; };
     // FP8 pools: where the codes of stage st's keys (values) land, and the
     // shared address of 16-byte chunk cc of code row r there (the TMA's
@@ -278,7 +283,9 @@ __global__ void __launch_bounds__(kTcThreads, 2)
             mbar_init(vland(st), 1);
         }
         // the query tile: written by the 4 row warps, or one TMA transaction
-        mbar_init(qfull, p.q_tma ? 1 : kRowWarps);
+        // (rounded to fp16 by the row warps after it lands, for kConvQ)
+        mbar_init(qfull, (p.q_tma && !kConvQ) ? 1 : kRowWarps);
+        mbar_init(qland, 1);
         mbar_init(mma_drain, 1);
         *abort_flag = 0;
         fence_barrier_init();
@@ -550,6 +557,43 @@ __global__ void __launch_bounds__(kTcThreads, 2)
             if (lane == 0)
                 mbar_arrive(qfull);
         };
+        // kConvQ with q_tma: a unit's bf16 query tile has landed by TMA; each
+        // thread rounds its own row to fp16 in place (same swizzled chunks),
+        // flags a bf16 element past the fp16 range, and the row warps
+        // announce the tile on qfull.
+        uint32_t nql = 0;  // bf16 query tiles waited for
+        auto convert_q = [&](const Unit &w) -> bool {
+            if (w.n <= 0)
+                return true;
+            if (!wait(qland, nql & 1))
+                return false;
+            ++nql;
+#pragma unroll
+            for (int c = 0; c < D / 8; ++c) {
+                const uint32_t a = qbase + (c >> 3) * L::kQHalf + tid * 128 +
+                                   (((c & 7) ^ (tid & 7)) << 4);
+                uint32_t wv[4];
+                asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                             : "=r"(wv[0]), "=r"(wv[1]), "=r"(wv[2]), "=r"(wv[3])
+                             : "r"(a)
+                             : "memory");
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const float lo = __uint_as_float(wv[k] << 16);
+                    const float hi = __uint_as_float(wv[k] & 0xffff0000u);
+                    q_over |= fmaxf(fabsf(lo), fabsf(hi)) > 65504.f;
+                    wv[k] = pack_f16x2(lo, hi);
+                }
+                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(wv[0]),
+                             "r"(wv[1]), "r"(wv[2]), "r"(wv[3])
+                             : "memory");
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(qfull);
+            return true;
+        };
         // FP8 pools: the row warps widen each key tile in place once its codes
         // have landed (see the fetch warps), two threads per 128-code row, and
         // announce it on the stage's "keys full" barrier.  Tile gg + 1 is widened
@@ -609,9 +653,11 @@ __global__ void __launch_bounds__(kTcThreads, 2)
             row_of(w, rw, true);
             if (!p.q_tma)  // (else the tensor-core warp brings it by TMA)
                 write_q(w, rw);
+            else if constexpr (kConvQ)
+                ok = convert_q(w);
         }
         if constexpr (kFp8) {
-            if (ntiles_cta > 0)
+            if (ok && ntiles_cta > 0)
                 ok = widen_k(0);
         }
         for (int u = blockIdx.x; u < total_units && ok; u = next_unit(u)) {
@@ -746,6 +792,11 @@ __global__ void __launch_bounds__(kTcThreads, 2)
                 row_of(wn, rn, true);
                 if (!p.q_tma)
                     write_q(wn, rn);
+                else if constexpr (kConvQ) {
+                    ok = convert_q(wn);
+                    if (!ok)
+                        break;
+                }
             } else {
                 wn.n = 0;
                 rn.qoff = rn.ooff = -1;
@@ -1055,10 +1106,11 @@ __global__ void __launch_bounds__(kTcThreads, 2)
             // waited for the P of its last S.
             if (p.q_tma && lane == 0) {
                 const int tok0 = p.query_start[w.seg] + w.rt * (kTcRows / G);
-                mbar_arrive_expect_tx(qfull, L::kHalves * L::kQHalf);
+                mbar_arrive_expect_tx(qtma_bar, L::kHalves * L::kQHalf);
 #pragma unroll
                 for (int h = 0; h < L::kHalves; ++h)
-                    tma_load_3d(qbase + h * L::kQHalf, &tmap_q, qfull, 64 * h, w.kh * G, tok0);
+                    tma_load_3d(qbase + h * L::kQHalf, &tmap_q, qtma_bar, 64 * h, w.kh * G,
+                                tok0);
             }
             ok = wait(qfull, nq & 1);  // this unit's queries; O read out by the last unit
             ++nq;
@@ -1244,17 +1296,18 @@ static pa_status dispatch_mq(const MqParams &prm_in, pa_dtype pool_dtype, pa_dty
         !encode_pool_map(&mv, value_cache, pool_dtype, prm_in.num_blocks, prm_in.block_size,
                          prm_in.num_kv_heads, head_dim))
         return PA_ERR_CUDA;
-    // Prefill over 16-bit pools with row tiles of whole tokens (the group
-    // divides 128) and a 16-byte aligned query: the query tiles may arrive by
-    // TMA (launch_mq keeps that for batches of more than one round).
+    // Prefill with row tiles of whole tokens (the group divides 128) and a
+    // 16-byte aligned query: the query tiles may arrive by TMA (launch_mq
+    // keeps that for batches of more than one round; over FP8 pools a bf16
+    // tile is rounded to fp16 by the row warps once it lands).
     MqParams prm = prm_in;
     std::memset(&mq, 0, sizeof(mq));
     prm.q_tma = 0;
-    if (!prm.prefix_mode && pool_dtype != PA_FP8_E4M3 && prm.group > 0 &&
-        kTcRows % prm.group == 0 && prm.num_tokens > 0 &&
+    if (!prm.prefix_mode && prm.group > 0 && kTcRows % prm.group == 0 && prm.num_tokens > 0 &&
         (reinterpret_cast<uintptr_t>(prm.query) & 15) == 0) {
-        if (!encode_query_map(&mq, prm.query, pool_dtype, prm.num_tokens, prm.num_heads,
-                              head_dim, prm.group))
+        const pa_dtype qdt = pool_dtype == PA_FP8_E4M3 ? query_dtype : pool_dtype;
+        if (!encode_query_map(&mq, prm.query, qdt, prm.num_tokens, prm.num_heads, head_dim,
+                              prm.group))
             return PA_ERR_CUDA;
         prm.q_tma = 1;
     }

@@ -203,6 +203,22 @@ def test_prefill_query_tiles_by_tma_groups(B, S, H, Hkv, counts, extra):
     assert_attention_close(S.to_float(out), attention_all(OracleStep(w)), spec.name)
 
 
+def test_prefill_fp8_query_by_tma_beyond_fp16_is_flagged(B, S):
+    """FP8 pools, a multi-round batch: the bf16 query tiles arrive by TMA and
+    the row warps round them to fp16 in place; a bf16 element past the fp16
+    range is flagged there too (and a query inside it is not)."""
+    w = W.build(_many_segments(56, 160, 500, True))
+    st = S.DecodeStep(w)
+    st.run()
+    torch.cuda.synchronize()
+    assert int(st.error_word.item()) == 0
+    assert st.query.dtype == torch.bfloat16
+    st.query[w.T - 3, 5, 17] = 1.0e5   # bf16 holds it, fp16 does not
+    st.attention()
+    torch.cuda.synchronize()
+    assert int(st.error_word.item()) & B.DEVERR_QUERY_RANGE
+
+
 def test_prefill_fp8_query_beyond_fp16_is_flagged(B, S, small):
     """The FP8 prefill rounds the query to fp16 for the tensor-core tiles: a
     bf16 query element beyond the fp16 range is flagged, not silently
