@@ -22,8 +22,10 @@
 // tokens times the G query heads of the group, or the members' decode
 // queries times G -- as the M = 128 dimension of tcgen05.mma tiles, and its
 // seven warps split the work.  Warps 0-3 (one thread per row) write the rows
-// into shared memory as the K-major A operand (128-byte swizzle), read each
-// S row from tensor memory, apply the causal / range mask and the online
+// into shared memory as the K-major A operand (128-byte swizzle) -- unless
+// the tensor-core warp brings them by TMA in batches of more than one round
+// (whole-token row tiles; over FP8 pools the row warps then round a bf16
+// tile to fp16 in place) -- read each S row from tensor memory, apply the causal / range mask and the online
 // softmax (fp32, log2 units, a reference maximum that moves only when a
 // score exceeds it by 2^8, rescaling O in tensor memory then), and write P as
 // bf16/fp16 pairs back over S, where it is the A operand of the value
@@ -225,7 +227,8 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     // S of buffer b computed (its commit also frees K stage b); value product
     // of stage st done (frees V stage st and S buffer st, makes O current);
     // P of buffer b stored by the 4 row warps; query tile in shared memory
-    // (4 row warps); every tensor-core operation of the CTA done (drain)
+    // (4 row warps, or one TMA transaction); every tensor-core operation of
+    // the CTA done (drain)
     auto bar = [&](int i) { return sbase + L::kBars + 8 * i; };
     auto kfull = [&](int st) { return bar(st); };
     auto vfull = [&](int st) { return bar(2 + st); };
