@@ -99,7 +99,7 @@ def test_prefill_block_placement_invariance(B, S, small, name):
     assert torch.equal(a, b)
 
 
-def _many_segments(n, qmax, cmax, fp8):
+def _many_segments(n, qmax, cmax, fp8, dtype="bf16"):
     """A prefill batch of n sequences (16 query heads over 2 KV heads, d 128)
     with unsorted and tied contexts, a fifth of them single-token rows, and
     two single-token rows past 64 key tiles (the deal's last sort bucket);
@@ -111,20 +111,24 @@ def _many_segments(n, qmax, cmax, fp8):
     q[3], ctx[3] = 1, 4500
     q[8], ctx[8] = 1, 4100
     spec = dataclasses.replace(W.CONFIGS["chunked"], name=f"chunked-{n}seg", seed=9700 + n,
-                               num_seqs=n, num_heads=16, num_kv_heads=2,
+                               num_seqs=n, num_heads=16, num_kv_heads=2, dtype=dtype,
                                context_lens=lambda r, c=ctx: c.copy(),
                                query_lens=lambda r, c, qq=q: qq.copy())
     return W.fp8_variant(spec) if fp8 else spec
 
 
-@pytest.mark.parametrize("n,qmax,cmax,fp8", [(56, 160, 500, False), (56, 160, 500, True),
-                                             (520, 3, 100, False)],
-                         ids=["56seg", "56seg-fp8", "520seg"])
-def test_prefill_many_segments(B, S, n, qmax, cmax, fp8):
+@pytest.mark.parametrize("n,qmax,cmax,fp8,dtype", [(56, 160, 500, False, "bf16"),
+                                                   (56, 160, 500, True, "bf16"),
+                                                   (56, 160, 500, True, "f16"),
+                                                   (520, 3, 100, False, "bf16")],
+                         ids=["56seg", "56seg-fp8", "56seg-fp8-f16", "520seg"])
+def test_prefill_many_segments(B, S, n, qmax, cmax, fp8, dtype):
     """Segments numbered longest context first and dealt boustrophedon over
-    more than one round (56 sequences, 500 units); past 512 sequences the
-    natural order and round-robin deal (520 sequences, 1,040 units)."""
-    w = W.build(_many_segments(n, qmax, cmax, fp8))
+    more than one round (56 sequences, 500 units), the query tiles by TMA
+    (FP8 pools: bf16 tiles rounded to fp16 in place, fp16 tiles as they
+    land); past 512 sequences the natural order and round-robin deal (520
+    sequences, 1,040 units)."""
+    w = W.build(_many_segments(n, qmax, cmax, fp8, dtype))
     ref = OracleStep(w)
     st = S.DecodeStep(w)
     out = st.run()
